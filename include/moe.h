@@ -1,0 +1,233 @@
+/*
+ * moe.h -- C ABI of the GB300 sparse Mixture-of-Experts layer (libmoe.so).
+ *
+ * The layer is the one of "Adapting Trillion-Parameter MoE Models for LoRA Fine-Tuning:
+ * A Full-Stack Engineering Guide", section 2.1, equation 1:
+ *
+ *     y = sum_{i in TopK(x)} g_i(x) * E_i(x)
+ *
+ * run as the Dispatch-Compute-Combine pipeline of "Trillion-Parameter MoE Model Training
+ * Adaptation: Full-Stack Optimization Practices", section 4.3 (route, permute tokens by
+ * expert, grouped expert GEMMs, unpermute), with the LoRA update of the same guide,
+ * section 3, equation 1 (W' = W0 + (alpha/r) B A) on each expert projection.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every function returns an int status (MOE_OK on success).  Nothing throws.
+ *  - Tensor arguments are DEVICE pointers owned by the caller.  The library never
+ *    allocates or frees device memory; scratch space is a caller-supplied workspace
+ *    whose size the matching *_workspace_size() function returns ("Adapting Ultra-Large
+ *    MoE Models: Engineering Practices and Optimization Pathways", section 3.4:
+ *    pre-allocated reusable buffers).
+ *  - All work is enqueued asynchronously on `stream` (a cudaStream_t); no call
+ *    synchronises the device or the stream.
+ *  - Host-side argument errors return MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *    MOE_ERR_WORKSPACE before anything is enqueued.  A failed launch returns MOE_ERR_CUDA.
+ *  - Errors found on the device (an expert id out of range, a bounded wait that ran
+ *    out) are written to the caller's `dev_status` word (int32, device memory, may be
+ *    NULL) with first-error-wins semantics; the kernel skips the offending work instead of
+ *    faulting.  The caller zeroes the word and reads it back when it chooses.
+ *  - bf16 values are passed as raw 16-bit patterns (moe_bf16).  All matrices are
+ *    row-major and densely packed.
+ *  - Requirements (else MOE_ERR_UNSUPPORTED): d and F multiples of 64; 1 <= k <= 32;
+ *    k <= E <= 1024; r == 0 or (r a multiple of 8 and r <= 64); every pointer 16-byte
+ *    aligned.
+ *  - Shapes: T tokens, d model width, E experts, k experts per token, F expert FFN
+ *    width, r LoRA rank, N = T*k slots.  Slot (t, j) is numbered t*k + j; rank j = 0 is
+ *    the largest router logit.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, inconsistent sizes      */
+  MOE_ERR_UNSUPPORTED = 2,  /* shape or alignment outside the supported set             */
+  MOE_ERR_WORKSPACE = 3,    /* workspace pointer null or smaller than *_workspace_size */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed                        */
+  MOE_ERR_TIMEOUT = 5,      /* (device) a bounded wait inside a kernel ran out          */
+  MOE_ERR_BAD_INDEX = 6     /* (device) an expert id or row index was out of range      */
+};
+
+typedef uint16_t moe_bf16;                /* raw bfloat16 bits                          */
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t                  */
+
+/* Problem sizes.  Capacity factor cf = cap_num / cap_den; cap_den == 0 means an infinite
+ * factor (no token is ever dropped).  lora_scale is s = alpha / r. */
+typedef struct moe_problem {
+  int32_t T, d, E, k, F, r;
+  float lora_scale;
+  int32_t cap_num, cap_den;
+} moe_problem;
+
+/* LoRA factors of every expert (device pointers, bf16), or all NULL for none:
+ *   A_g, A_u [E, r, d]   B_g, B_u [E, F, r]   A_d [E, r, F]   B_d [E, d, r]
+ * so that the gate projection is  W_g x + s * B_g (A_g x)  and so on. */
+typedef struct moe_lora {
+  const moe_bf16 *A_g, *B_g, *A_u, *B_u, *A_d, *B_d;
+} moe_lora;
+
+/* Gradients of the LoRA factors (fp32, same shapes as moe_lora; overwritten). */
+typedef struct moe_lora_grad {
+  float *dA_g, *dB_g, *dA_u, *dB_u, *dA_d, *dB_d;
+} moe_lora_grad;
+
+/* Activations the expert forward saves for the backward (bf16, rows of x_perm order):
+ *   a_gate, a_up [rows, F]  pre-activations of the gate and up projections
+ *   u_gate, u_up [rows, r]  s * (x A_g^T), s * (x A_u^T)      (LoRA only)
+ *   u_down       [rows, r]  s * (h A_d^T)                     (LoRA only)
+ * Any pointer may be NULL when the backward will not run. */
+typedef struct moe_ffn_saved {
+  moe_bf16 *a_gate, *a_up, *u_gate, *u_up, *u_down;
+} moe_ffn_saved;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* moe_status_string(int status);
+
+/* ABI version of this library (major * 10000 + minor * 100 + patch). */
+int moe_version(void);
+
+/* ==================================================================== routing
+ * "Day-Level Adaptation and LoRA Fine-Tuning of Ultra-Large-Scale Sparse MoE Models",
+ * section 2.1 and section 3.3 (routing scoring fused with Top-k selection);
+ * "Adapting Trillion-Parameter MoE Models ...", section 2.1, equation 1 (gate g_i).
+ *
+ *   logits[t, e] = sum_c x[t, c] * w_router[e, c] + bias[e]        (fp32 accuracy)
+ *   topk_idx[t, j]  = the k largest logits, descending; equal logits -> lower index first
+ *   p[t, :]         = softmax(logits[t, :]) over all E experts (fp32)
+ *   topk_gate[t, j] = p[t, topk_idx[t, j]] / sum_j' p[t, topk_idx[t, j']]
+ *   prob_partials[b, e] = sum of p[t, e] over the tokens of row-block b
+ *                         (moe_route_num_partials() rows; feeds moe_aux_loss)
+ *
+ * x [T, d] bf16; w_router [E, d] fp32; bias [E] fp32 or NULL; topk_idx [T, k] int32;
+ * topk_gate [T, k] fp32; prob_partials [num_partials, E] fp32; logits [T, E] fp32 or NULL
+ * (when given, the fp32 logits are written there; else they live in the workspace).
+ */
+int moe_route_num_partials(const moe_problem* p);
+size_t moe_route_workspace_size(const moe_problem* p);
+int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router,
+              const float* bias, int32_t* topk_idx, float* topk_gate, float* prob_partials,
+              float* logits, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+              moe_stream_t stream);
+
+/* The selection, softmax and gate steps of moe_route alone, on caller-given fp32 logits
+ * [T, E] (same outputs, same rules). */
+int moe_route_from_logits(const moe_problem* p, const float* logits, int32_t* topk_idx,
+                          float* topk_gate, float* prob_partials, int32_t* dev_status,
+                          moe_stream_t stream);
+
+/* ==================================================================== dispatch
+ * "Adapting Ultra-Large MoE Models ...", section 3.3 (capacity factor, token dropping,
+ * batch reshaping into per-expert GEMM batches); "Trillion-Parameter MoE Model Training
+ * Adaptation ...", section 3 "Communication" (tokens permuted by routing result).
+ *
+ *   C = ceil(cf * T * k / E)   (no limit when cap_den == 0)
+ *   counts[e]      slots routed to expert e before any drop
+ *   pos(t, j)      number of tokens t' < t routed to the same expert (arrival order)
+ *   a slot is kept iff pos < C; kept_e = min(counts[e], C)
+ *   offsets[e]     exclusive prefix sum of kept_e; offsets[E] = n_kept
+ *   slot_row[t*k+j] = offsets[e] + pos if kept, else -1
+ *   row_slot[row]   inverse map for rows < n_kept; rows >= n_kept are set to -1
+ *   n_kept_dropped  {n_kept, n_dropped}
+ *   x_perm[row]     = x[row_slot[row] / k]  (rows >= n_kept are left untouched)
+ * Everything is deterministic and bit-exact.  topk_idx entries outside [0, E) set
+ * MOE_ERR_BAD_INDEX in dev_status and are treated as dropped.
+ * Sizes: counts [E], offsets [E+1], slot_row [T*k], row_slot [T*k] int32;
+ * x [T, d] and x_perm [T*k, d] bf16.
+ */
+size_t moe_dispatch_workspace_size(const moe_problem* p);
+int moe_dispatch(const moe_problem* p, const int32_t* topk_idx, const moe_bf16* x,
+                 int32_t* counts, int32_t* offsets, int32_t* slot_row, int32_t* row_slot,
+                 int32_t* n_kept_dropped, moe_bf16* x_perm, void* workspace,
+                 size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream);
+
+/* ==================================================================== experts
+ * Grouped SwiGLU expert GEMMs with LoRA ("Trillion-Parameter MoE Model Training
+ * Adaptation ...", section 4.3: grouped GEMM over experts; "Adapting Trillion-Parameter
+ * MoE Models ...", section 3, equation 1: LoRA).  For every permuted row of expert e
+ * (rows offsets[e] .. offsets[e+1]-1 of x_perm):
+ *
+ *   a_g = x W_g[e]^T + s (x A_g[e]^T) B_g[e]^T        (fp32 accumulate)
+ *   a_u = x W_u[e]^T + s (x A_u[e]^T) B_u[e]^T
+ *   h   = silu(a_g) * a_u                             -> h [rows, F] bf16
+ *   o   = h W_d[e]^T + s (h A_d[e]^T) B_d[e]^T
+ *   y_perm[row] = topk_gate[row_slot[row]] * o        -> y_perm [rows, d] bf16
+ *
+ * w_gate, w_up [E, F, d]; w_down [E, d, F] bf16.  lora may be NULL.  saved may be NULL.
+ * offsets [E+1] int32 (device); rows_max bounds offsets[E] and sizes x_perm/h/y_perm.
+ * topk_gate is indexed by slot (row_slot), as written by moe_route/moe_dispatch.
+ */
+size_t moe_expert_ffn_workspace_size(const moe_problem* p, int32_t rows_max);
+int moe_expert_ffn(const moe_problem* p, int32_t rows_max, const moe_bf16* x_perm,
+                   const int32_t* offsets, const int32_t* row_slot, const float* topk_gate,
+                   const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
+                   const moe_lora* lora, moe_bf16* h, moe_bf16* y_perm,
+                   const moe_ffn_saved* saved, void* workspace, size_t workspace_bytes,
+                   int32_t* dev_status, moe_stream_t stream);
+
+/* ==================================================================== combine / aux
+ * Unpermute and sum ("Trillion-Parameter MoE Model Training Adaptation ...", section 3
+ * "Communication": results are unpermuted and returned):
+ *   y[t] = sum_{j = 0..k-1, slot_row[t*k+j] >= 0} y_perm[slot_row[t*k+j]]
+ * summed in rank order in fp32, rounded once to bf16.  A token whose slots were all
+ * dropped gets y[t] = 0.  y_perm [rows, d], y [T, d] bf16.
+ */
+int moe_combine(const moe_problem* p, const moe_bf16* y_perm, const int32_t* slot_row,
+                moe_bf16* y, moe_stream_t stream);
+
+/* Auxiliary load-balancing loss ("Day-Level Adaptation ...", section 2.1):
+ *   aux = E * sum_e f_e P_e,  f_e = counts[e] / (T k) (before drops),
+ *   P_e = (1/T) sum_b prob_partials[b, e].   aux_out: one fp32 in device memory. */
+int moe_aux_loss(const moe_problem* p, const int32_t* counts, const float* prob_partials,
+                 int32_t n_partials, float* aux_out, moe_stream_t stream);
+
+/* ==================================================================== backward
+ * Gradient of <dy, y> with the routing decisions of the forward held fixed ("Day-Level
+ * Adaptation ...", section 5: checkpoint boundaries avoid dynamic routing) and the base
+ * weights and the router frozen ("Adapting Trillion-Parameter MoE Models ...", section 3:
+ * only adapter parameters are trained; routing gates are not tuned).
+ */
+
+/* dz_perm[row] = g(slot) * dy[t]  (bf16, rows < n_kept);
+ * dgate[t*k+j] = <dy[t], o(row)> = <dy[t], y_perm[row]> / g(slot) for kept slots, else 0.
+ * dy [T, d] bf16; y_perm [rows, d] bf16 (forward output); dgate [T*k] fp32. */
+int moe_combine_bwd(const moe_problem* p, const moe_bf16* dy, const moe_bf16* y_perm,
+                    const int32_t* slot_row, const float* topk_gate, moe_bf16* dz_perm,
+                    float* dgate, moe_stream_t stream);
+
+/* Expert backward for the rows of every expert:
+ *   dh   = dz W_d + s (dz B_d) A_d;   da_g = dh * a_u * silu'(a_g);   da_u = dh * silu(a_g)
+ *   dx_perm = da_g W_g + da_u W_u + s (da_g B_g) A_g + s (da_u B_u) A_u     (bf16 out)
+ *   dB_d = s dz^T (h A_d^T),  dA_d = s (dz B_d)^T h,  and likewise for gate and up.
+ * saved must hold a_gate and a_up (and u_* when lora is given); h is the forward's h.
+ * grads may be NULL when lora is NULL. */
+size_t moe_expert_ffn_bwd_workspace_size(const moe_problem* p, int32_t rows_max);
+int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x_perm,
+                       const int32_t* offsets, const moe_bf16* w_gate, const moe_bf16* w_up,
+                       const moe_bf16* w_down, const moe_lora* lora,
+                       const moe_ffn_saved* saved, const moe_bf16* h, const moe_bf16* dz_perm,
+                       moe_bf16* dx_perm, const moe_lora_grad* grads, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream);
+
+/* dx[t] = sum over kept slots of dx_perm[slot_row[t*k+j]]   (fp32 [T, d], overwritten) */
+int moe_dispatch_bwd(const moe_problem* p, const moe_bf16* dx_perm, const int32_t* slot_row,
+                     float* dx, moe_stream_t stream);
+
+/* Gate path through the renormalised softmax and the frozen router, accumulated:
+ *   dlogit[t, e_j] = g_j (dgate_j - sum_i g_i dgate_i)   (zero off the selection)
+ *   dx[t] += sum_j dlogit[t, e_j] * w_router[e_j]          (fp32 [T, d]) */
+int moe_route_bwd(const moe_problem* p, const int32_t* topk_idx, const float* topk_gate,
+                  const float* dgate, const float* w_router, float* dx, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,400 @@
+// The C ABI of libmoe.so (declared in include/moe.h): argument checks, workspace carving,
+// tensor-map encoding and the launch sequence of each step.  No entry point allocates,
+// frees or synchronises.
+#include <cuda_bf16.h>
+#include <string.h>
+
+#include "moe_internal.h"
+#include "route.h"
+
+using namespace moe;
+
+namespace {
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t up256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+int check_problem(const moe_problem* p) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (p->T <= 0 || p->d <= 0 || p->E <= 0 || p->k <= 0 || p->F <= 0 || p->r < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (p->cap_num < 0 || p->cap_den < 0) return MOE_ERR_INVALID_ARG;
+  if (p->d % 64 || p->F % 64) return MOE_ERR_UNSUPPORTED;
+  if (p->k > 32 || p->k > p->E || p->E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (p->r && (p->r % 8 || p->r > 64)) return MOE_ERR_UNSUPPORTED;
+  const long long slots = static_cast<long long>(p->T) * p->k;
+  if (slots > (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  if (slots * p->d > (1ll << 40)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// ceil(cap_num * T * k / (cap_den * E)), or -1 for an infinite capacity factor.
+int capacity_of(const moe_problem* p) {
+  if (p->cap_den == 0) return -1;
+  const long long num = static_cast<long long>(p->cap_num) * p->T * p->k;
+  const long long den = static_cast<long long>(p->cap_den) * p->E;
+  const long long c = (num + den - 1) / den;
+  return c > (1ll << 30) ? (1 << 30) : static_cast<int>(c);
+}
+
+int cuda_status(int e) { return e == 0 ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)              \
+  do {                             \
+    const int _st = (expr);        \
+    if (_st != MOE_OK) return _st; \
+  } while (0)
+#define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+
+int lora_tile(int r) { return r <= 16 ? 16 : (r <= 32 ? 32 : 64); }
+
+struct Carver {
+  uint8_t* base;
+  size_t used;
+  template <class T>
+  T* take(size_t count) {
+    T* p = reinterpret_cast<T*>(base + used);
+    used += up256(count * sizeof(T));
+    return p;
+  }
+};
+
+size_t route_ws(const moe_problem* p) {
+  return up256(2ull * p->E * p->d * 2) + up256(static_cast<size_t>(p->T) * p->E * 4);
+}
+
+size_t dispatch_ws(const moe_problem* p) {
+  return up256(static_cast<size_t>(p->T) * p->k * 4) +
+         up256(static_cast<size_t>(dispatch_num_chunks(p->T)) * p->E * 4);
+}
+
+size_t ffn_ws(const moe_problem* p, int rows_max) {
+  size_t b = up256((p->E + 1) * 4ull);
+  if (p->r) b += 3 * up256(static_cast<size_t>(rows_max) * p->r * 2);
+  return b;
+}
+
+GemmParams gemm_params() {
+  GemmParams P;
+  memset(&P, 0, sizeof(P));
+  return P;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: null pointer or inconsistent sizes";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: shape or alignment not supported";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing or too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded device wait ran out";
+    case MOE_ERR_BAD_INDEX: return "MOE_ERR_BAD_INDEX: an index was out of range";
+    default: return "unknown moe status";
+  }
+}
+
+int moe_version(void) { return 10000; }
+
+// ------------------------------------------------------------------------ routing
+
+int moe_route_num_partials(const moe_problem* p) {
+  return (p && p->T > 0) ? route_num_partials(p->T) : 0;
+}
+
+size_t moe_route_workspace_size(const moe_problem* p) {
+  return check_problem(p) == MOE_OK ? route_ws(p) : 0;
+}
+
+int moe_route_from_logits(const moe_problem* p, const float* logits, int32_t* topk_idx,
+                          float* topk_gate, float* prob_partials, int32_t* dev_status,
+                          moe_stream_t stream) {
+  (void)dev_status;
+  MOE_TRY(check_problem(p));
+  if (!logits || !topk_idx || !topk_gate || !prob_partials) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_topk_softmax(logits, p->T, p->E, p->k, topk_idx, topk_gate,
+                                         prob_partials, stream));
+}
+
+int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, const float* bias,
+              int32_t* topk_idx, float* topk_gate, float* prob_partials, float* logits,
+              void* workspace, size_t workspace_bytes, int32_t* dev_status,
+              moe_stream_t stream) {
+  MOE_TRY(check_problem(p));
+  if (!x || !w_router || !topk_idx || !topk_gate || !prob_partials) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(w_router) || (logits && !al16(logits))) return MOE_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < route_ws(p)) return MOE_ERR_WORKSPACE;
+  const int T = p->T, d = p->d, E = p->E;
+  Carver cv{static_cast<uint8_t*>(workspace), 0};
+  __nv_bfloat16* w_split = cv.take<__nv_bfloat16>(2ull * E * d);
+  float* logits_ws = cv.take<float>(static_cast<size_t>(T) * E);
+  float* L = logits ? logits : logits_ws;
+
+  MOE_CUDA(launch_split_router(w_router, w_split, w_split + static_cast<size_t>(E) * d,
+                               static_cast<size_t>(E) * d, stream));
+  GemmParams P = gemm_params();
+  MOE_TRY(encode_map_kmajor(&P.maps[0], x, d, T, 1, kBM));
+  MOE_TRY(encode_map_kmajor(&P.maps[1], w_split, d, E, 2, 128));
+  P.nmaps = 2;
+  P.seg[0] = GemmSeg{d / kBK, 0, 0, {1, -1}, {0, 0}, {0, 0}};
+  P.seg[1] = GemmSeg{d / kBK, 0, 0, {1, -1}, {0, 0}, {1, 0}};
+  P.nseg = 2;
+  P.M = T;
+  P.m_tiles = (T + kBM - 1) / kBM;
+  P.n_tiles = (E + 127) / 128;
+  P.N = E;
+  P.out0 = L;
+  P.ldo = E;
+  P.bias = bias;
+  P.dev_status = dev_status;
+  MOE_CUDA(launch_gemm_router(P, stream));
+  return cuda_status(launch_topk_softmax(L, T, E, p->k, topk_idx, topk_gate, prob_partials,
+                                         stream));
+}
+
+// ------------------------------------------------------------------------ dispatch
+
+size_t moe_dispatch_workspace_size(const moe_problem* p) {
+  return check_problem(p) == MOE_OK ? dispatch_ws(p) : 0;
+}
+
+int moe_dispatch(const moe_problem* p, const int32_t* topk_idx, const moe_bf16* x,
+                 int32_t* counts, int32_t* offsets, int32_t* slot_row, int32_t* row_slot,
+                 int32_t* n_kept_dropped, moe_bf16* x_perm, void* workspace,
+                 size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
+  MOE_TRY(check_problem(p));
+  if (!topk_idx || !x || !counts || !offsets || !slot_row || !row_slot || !n_kept_dropped ||
+      !x_perm)
+    return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(x_perm)) return MOE_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < dispatch_ws(p)) return MOE_ERR_WORKSPACE;
+  Carver cv{static_cast<uint8_t*>(workspace), 0};
+  int32_t* local_rank = cv.take<int32_t>(static_cast<size_t>(p->T) * p->k);
+  int32_t* chunk_cnt = cv.take<int32_t>(static_cast<size_t>(dispatch_num_chunks(p->T)) * p->E);
+  return cuda_status(launch_dispatch(
+      topk_idx, reinterpret_cast<const __nv_bfloat16*>(x), p->T, p->d, p->E, p->k,
+      capacity_of(p), counts, offsets, slot_row, row_slot, n_kept_dropped,
+      reinterpret_cast<__nv_bfloat16*>(x_perm), local_rank, chunk_cnt, dev_status, stream));
+}
+
+// ------------------------------------------------------------------------ experts
+
+size_t moe_expert_ffn_workspace_size(const moe_problem* p, int32_t rows_max) {
+  return (check_problem(p) == MOE_OK && rows_max > 0) ? ffn_ws(p, rows_max) : 0;
+}
+
+int moe_expert_ffn(const moe_problem* p, int32_t rows_max, const moe_bf16* x_perm,
+                   const int32_t* offsets, const int32_t* row_slot, const float* topk_gate,
+                   const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
+                   const moe_lora* lora, moe_bf16* h, moe_bf16* y_perm,
+                   const moe_ffn_saved* saved, void* workspace, size_t workspace_bytes,
+                   int32_t* dev_status, moe_stream_t stream) {
+  MOE_TRY(check_problem(p));
+  if (rows_max <= 0) return MOE_ERR_INVALID_ARG;
+  if (!x_perm || !offsets || !row_slot || !topk_gate || !w_gate || !w_up || !w_down || !h ||
+      !y_perm)
+    return MOE_ERR_INVALID_ARG;
+  const bool use_lora = lora != nullptr && p->r > 0;
+  if (lora && p->r == 0) return MOE_ERR_INVALID_ARG;
+  if (use_lora && (!lora->A_g || !lora->B_g || !lora->A_u || !lora->B_u || !lora->A_d ||
+                   !lora->B_d))
+    return MOE_ERR_INVALID_ARG;
+  const void* al[] = {x_perm, w_gate, w_up, w_down, h, y_perm};
+  for (const void* q : al)
+    if (!al16(q)) return MOE_ERR_UNSUPPORTED;
+  if (use_lora) {
+    const void* al2[] = {lora->A_g, lora->B_g, lora->A_u, lora->B_u, lora->A_d, lora->B_d};
+    for (const void* q : al2)
+      if (!al16(q)) return MOE_ERR_UNSUPPORTED;
+  }
+  if (saved) {
+    const void* al3[] = {saved->a_gate, saved->a_up, saved->u_gate, saved->u_up, saved->u_down};
+    for (const void* q : al3)
+      if (q && !al16(q)) return MOE_ERR_UNSUPPORTED;
+  }
+  if (!workspace || workspace_bytes < ffn_ws(p, rows_max)) return MOE_ERR_WORKSPACE;
+
+  const int d = p->d, E = p->E, F = p->F, r = p->r;
+  Carver cv{static_cast<uint8_t*>(workspace), 0};
+  int32_t* tile_off = cv.take<int32_t>(E + 1);
+  moe_bf16 *u_g = nullptr, *u_u = nullptr, *u_d = nullptr;
+  if (r) {
+    u_g = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * r);
+    u_u = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * r);
+    u_d = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * r);
+    if (saved && saved->u_gate) u_g = saved->u_gate;
+    if (saved && saved->u_up) u_u = saved->u_up;
+    if (saved && saved->u_down) u_d = saved->u_down;
+  }
+  MOE_CUDA(launch_tile_schedule(offsets, E, rows_max, tile_off, dev_status, stream));
+
+  auto grouped = [&](GemmParams& P) {
+    P.group_off = offsets;
+    P.tile_off = tile_off;
+    P.G = E;
+    P.dev_status = dev_status;
+  };
+
+  // LoRA down-projections of the input: u_g = s x A_g^T, u_u = s x A_u^T
+  if (use_lora) {
+    GemmParams P = gemm_params();
+    MOE_TRY(encode_map_kmajor(&P.maps[0], x_perm, d, rows_max, 1, kBM));
+    MOE_TRY(encode_map_kmajor(&P.maps[1], lora->A_g, d, r, E, lora_tile(r)));
+    MOE_TRY(encode_map_kmajor(&P.maps[2], lora->A_u, d, r, E, lora_tile(r)));
+    P.nmaps = 3;
+    P.seg[0] = GemmSeg{d / kBK, 0, 0, {1, 2}, {0, 0}, {0, 0}};
+    P.nseg = 1;
+    grouped(P);
+    P.n_tiles = 1;
+    P.N = r;
+    P.out0 = u_g;
+    P.out1 = u_u;
+    P.ldo = r;
+    P.scale = p->lora_scale;
+    MOE_CUDA(launch_gemm_lora_u2(P, r, stream));
+  }
+  // gate/up projections (+ LoRA K-blocks) with the SwiGLU epilogue -> h
+  {
+    GemmParams P = gemm_params();
+    MOE_TRY(encode_map_kmajor(&P.maps[0], x_perm, d, rows_max, 1, kBM));
+    MOE_TRY(encode_map_kmajor(&P.maps[1], w_gate, d, F, E, 128));
+    MOE_TRY(encode_map_kmajor(&P.maps[2], w_up, d, F, E, 128));
+    P.nmaps = 3;
+    P.seg[0] = GemmSeg{d / kBK, 0, 0, {1, 2}, {0, 0}, {0, 0}};
+    P.nseg = 1;
+    if (use_lora) {
+      MOE_TRY(encode_map_kmajor(&P.maps[3], u_g, r, rows_max, 1, kBM));
+      MOE_TRY(encode_map_kmajor(&P.maps[4], u_u, r, rows_max, 1, kBM));
+      MOE_TRY(encode_map_kmajor(&P.maps[5], lora->B_g, r, F, E, 128));
+      MOE_TRY(encode_map_kmajor(&P.maps[6], lora->B_u, r, F, E, 128));
+      P.nmaps = 7;
+      P.seg[1] = GemmSeg{(r + kBK - 1) / kBK, 3, 0, {5, -1}, {0, 0}, {0, 0}};
+      P.seg[2] = GemmSeg{(r + kBK - 1) / kBK, 4, 0, {-1, 6}, {0, 0}, {0, 0}};
+      P.nseg = 3;
+    }
+    grouped(P);
+    P.n_tiles = (F + 127) / 128;
+    P.N = F;
+    P.out0 = h;
+    P.out1 = saved ? saved->a_gate : nullptr;
+    P.out2 = saved ? saved->a_up : nullptr;
+    P.ldo = F;
+    MOE_CUDA(launch_gemm_gateup(P, stream));
+  }
+  // LoRA down-projection of h: u_d = s h A_d^T
+  if (use_lora) {
+    GemmParams P = gemm_params();
+    MOE_TRY(encode_map_kmajor(&P.maps[0], h, F, rows_max, 1, kBM));
+    MOE_TRY(encode_map_kmajor(&P.maps[1], lora->A_d, F, r, E, lora_tile(r)));
+    P.nmaps = 2;
+    P.seg[0] = GemmSeg{F / kBK, 0, 0, {1, -1}, {0, 0}, {0, 0}};
+    P.nseg = 1;
+    grouped(P);
+    P.n_tiles = 1;
+    P.N = r;
+    P.out0 = u_d;
+    P.ldo = r;
+    P.scale = p->lora_scale;
+    MOE_CUDA(launch_gemm_lora_u1(P, r, stream));
+  }
+  // down projection (+ LoRA K-block), scaled by the routing gate -> y_perm
+  {
+    GemmParams P = gemm_params();
+    MOE_TRY(encode_map_kmajor(&P.maps[0], h, F, rows_max, 1, kBM));
+    MOE_TRY(encode_map_kmajor(&P.maps[1], w_down, F, d, E, 256));
+    P.nmaps = 2;
+    P.seg[0] = GemmSeg{F / kBK, 0, 0, {1, -1}, {0, 0}, {0, 0}};
+    P.nseg = 1;
+    if (use_lora) {
+      MOE_TRY(encode_map_kmajor(&P.maps[2], u_d, r, rows_max, 1, kBM));
+      MOE_TRY(encode_map_kmajor(&P.maps[3], lora->B_d, r, d, E, 256));
+      P.nmaps = 4;
+      P.seg[1] = GemmSeg{(r + kBK - 1) / kBK, 2, 0, {3, -1}, {0, 0}, {0, 0}};
+      P.nseg = 2;
+    }
+    grouped(P);
+    P.n_tiles = (d + 255) / 256;
+    P.N = d;
+    P.out0 = y_perm;
+    P.ldo = d;
+    P.gate = topk_gate;
+    P.row_slot = row_slot;
+    MOE_CUDA(launch_gemm_down(P, stream));
+  }
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------------------ combine / aux
+
+int moe_combine(const moe_problem* p, const moe_bf16* y_perm, const int32_t* slot_row,
+                moe_bf16* y, moe_stream_t stream) {
+  MOE_TRY(check_problem(p));
+  if (!y_perm || !slot_row || !y) return MOE_ERR_INVALID_ARG;
+  if (!al16(y_perm) || !al16(y)) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_combine(reinterpret_cast<const __nv_bfloat16*>(y_perm), slot_row,
+                                    p->T, p->d, p->k, reinterpret_cast<__nv_bfloat16*>(y),
+                                    stream));
+}
+
+int moe_aux_loss(const moe_problem* p, const int32_t* counts, const float* prob_partials,
+                 int32_t n_partials, float* aux_out, moe_stream_t stream) {
+  MOE_TRY(check_problem(p));
+  if (!counts || !prob_partials || !aux_out || n_partials <= 0) return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_aux_loss(counts, prob_partials, n_partials, p->T, p->k, p->E, aux_out, stream));
+}
+
+// ------------------------------------------------------------------------ backward
+
+int moe_combine_bwd(const moe_problem* p, const moe_bf16* dy, const moe_bf16* y_perm,
+                    const int32_t* slot_row, const float* topk_gate, moe_bf16* dz_perm,
+                    float* dgate, moe_stream_t stream) {
+  MOE_TRY(check_problem(p));
+  if (!dy || !y_perm || !slot_row || !topk_gate || !dz_perm || !dgate) return MOE_ERR_INVALID_ARG;
+  if (!al16(dy) || !al16(y_perm) || !al16(dz_perm)) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_combine_bwd(
+      reinterpret_cast<const __nv_bfloat16*>(dy), reinterpret_cast<const __nv_bfloat16*>(y_perm),
+      slot_row, topk_gate, p->T, p->d, p->k, reinterpret_cast<__nv_bfloat16*>(dz_perm), dgate,
+      stream));
+}
+
+size_t moe_expert_ffn_bwd_workspace_size(const moe_problem* p, int32_t rows_max) {
+  (void)p;
+  (void)rows_max;
+  return 0;
+}
+
+int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x_perm,
+                       const int32_t* offsets, const moe_bf16* w_gate, const moe_bf16* w_up,
+                       const moe_bf16* w_down, const moe_lora* lora,
+                       const moe_ffn_saved* saved, const moe_bf16* h, const moe_bf16* dz_perm,
+                       moe_bf16* dx_perm, const moe_lora_grad* grads, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
+  (void)p; (void)rows_max; (void)x_perm; (void)offsets; (void)w_gate; (void)w_up;
+  (void)w_down; (void)lora; (void)saved; (void)h; (void)dz_perm; (void)dx_perm; (void)grads;
+  (void)workspace; (void)workspace_bytes; (void)dev_status; (void)stream;
+  return MOE_ERR_UNSUPPORTED;
+}
+
+int moe_dispatch_bwd(const moe_problem* p, const moe_bf16* dx_perm, const int32_t* slot_row,
+                     float* dx, moe_stream_t stream) {
+  MOE_TRY(check_problem(p));
+  if (!dx_perm || !slot_row || !dx) return MOE_ERR_INVALID_ARG;
+  if (!al16(dx_perm) || !al16(dx)) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_dispatch_bwd(reinterpret_cast<const __nv_bfloat16*>(dx_perm),
+                                         slot_row, p->T, p->d, p->k, dx, stream));
+}
+
+int moe_route_bwd(const moe_problem* p, const int32_t* topk_idx, const float* topk_gate,
+                  const float* dgate, const float* w_router, float* dx, moe_stream_t stream) {
+  MOE_TRY(check_problem(p));
+  if (!topk_idx || !topk_gate || !dgate || !w_router || !dx) return MOE_ERR_INVALID_ARG;
+  if (!al16(w_router) || !al16(dx)) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_route_bwd(topk_idx, topk_gate, dgate, w_router, p->T, p->d, p->E,
+                                      p->k, dx, stream));
+}
+
+}  // extern "C"

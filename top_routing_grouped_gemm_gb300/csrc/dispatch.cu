@@ -1,0 +1,407 @@
+// Dispatch (count, scan, capacity clip, arrival-ordered permutation, gather), combine,
+// their backward counterparts, and the router backward.
+//
+// "Adapting Ultra-Large MoE Models: Engineering Practices and Optimization Pathways",
+// section 3.3: a capacity limit per expert, excess tokens dropped, and the tokens each
+// expert receives organised into regular GEMM batches.  "Trillion-Parameter MoE Model
+// Training Adaptation: Full-Stack Optimization Practices", section 3 "Communication" and
+// section 4.3: tokens are permuted by routing result, the experts run as grouped GEMMs, and
+// the results are unpermuted.
+//
+// Determinism: positions come from sequential per-chunk counting in (token, rank) order and
+// an exclusive scan over chunks, so no result depends on the order of atomic operations.
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+#include "route.h"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ int block_exclusive_scan_1024(int v, int* sm, int* total) {
+  // blockDim.x == 1024
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = sm[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    sm[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int warp_excl = warp ? sm[warp - 1] : 0;
+  *total = sm[31];
+  return warp_excl + x - v;
+}
+
+// Pass 1: each warp counts one chunk of kDispatchChunk tokens, in (token, rank) order, and
+// records every slot's rank among the chunk's slots routed to the same expert.
+__global__ void __launch_bounds__(128) dispatch_count_kernel(
+    const int32_t* __restrict__ idx, int T, int E, int k, int32_t* __restrict__ local_rank,
+    int32_t* __restrict__ chunk_cnt, int32_t* dev_status) {
+  extern __shared__ int cnt_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * 4 + warp;
+  const int nch = dispatch_num_chunks(T);
+  if (c >= nch) return;
+  int* cnt = cnt_smem + warp * E;
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  __syncwarp();
+  const int t_end = min((c + 1) * kDispatchChunk, T);
+  for (int t = c * kDispatchChunk; t < t_end; ++t) {
+    const bool act = lane < k;
+    int e = -1;
+    if (act) {
+      e = idx[static_cast<size_t>(t) * k + lane];
+      if (e < 0 || e >= E) {
+        report_status(dev_status, MOE_ERR_BAD_INDEX);
+        e = -1;
+      }
+    }
+    const unsigned live = __ballot_sync(0xffffffffu, e >= 0);
+    if (e >= 0) {
+      // a token may repeat an expert only in caller-made input; ranks then follow j order
+      const unsigned grp = __match_any_sync(live, e);
+      const int before = __popc(grp & ((1u << lane) - 1u));
+      const int base = cnt[e];
+      __syncwarp(live);
+      local_rank[static_cast<size_t>(t) * k + lane] = base + before;
+      if (lane == 31 - __clz(grp)) cnt[e] = base + __popc(grp);
+    } else if (act) {
+      local_rank[static_cast<size_t>(t) * k + lane] = -1;
+    }
+    __syncwarp();
+  }
+  for (int e = lane; e < E; e += 32) chunk_cnt[static_cast<size_t>(c) * E + e] = cnt[e];
+}
+
+// Pass 2: per expert, exclusive scan of the chunk counts (in place -> chunk bases) and the
+// pre-drop totals.  Block (32 experts) x (32 parts of the chunk range).
+__global__ void __launch_bounds__(1024) dispatch_scan_chunks_kernel(
+    int32_t* __restrict__ chunk_cnt, int nch, int E, int32_t* __restrict__ counts) {
+  __shared__ int sm[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + tx;
+  const int per = (nch + 31) / 32;
+  const int c0 = ty * per, c1 = min(nch, c0 + per);
+  int sum = 0;
+  if (e < E)
+    for (int c = c0; c < c1; ++c) sum += chunk_cnt[static_cast<size_t>(c) * E + e];
+  sm[ty][tx] = sum;
+  __syncthreads();
+  if (ty == 0 && e < E) {
+    int run = 0;
+    for (int p = 0; p < 32; ++p) {
+      const int v = sm[p][tx];
+      sm[p][tx] = run;
+      run += v;
+    }
+    counts[e] = run;
+  }
+  __syncthreads();
+  if (e < E) {
+    int run = sm[ty][tx];
+    for (int c = c0; c < c1; ++c) {
+      const size_t i = static_cast<size_t>(c) * E + e;
+      const int v = chunk_cnt[i];
+      chunk_cnt[i] = run;
+      run += v;
+    }
+  }
+}
+
+// Pass 3: kept counts, expert offsets, n_kept / n_dropped.  One block, thread = expert.
+__global__ void __launch_bounds__(1024) dispatch_offsets_kernel(
+    const int32_t* __restrict__ counts, int E, int capacity, int slots,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ n_kept_dropped) {
+  __shared__ int sm[32];
+  const int e = threadIdx.x;
+  int kept = 0;
+  if (e < E) kept = capacity < 0 ? counts[e] : min(counts[e], capacity);
+  int total;
+  const int excl = block_exclusive_scan_1024(kept, sm, &total);
+  if (e < E) offsets[e] = excl;
+  if (e == 0) {
+    offsets[E] = total;
+    n_kept_dropped[0] = total;
+    n_kept_dropped[1] = slots - total;
+  }
+}
+
+// Pass 4: final rows, both index maps, and the gather x -> x_perm.  One warp per token:
+// x[t] is read once and written to each of its kept rows with 16-byte vector accesses.
+__global__ void __launch_bounds__(256) dispatch_scatter_kernel(
+    const int32_t* __restrict__ idx, const int32_t* __restrict__ local_rank,
+    const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
+    const int32_t* __restrict__ n_kept_dropped, const uint4* __restrict__ x, int T, int d,
+    int E, int k, int capacity, int32_t* __restrict__ slot_row, int32_t* __restrict__ row_slot,
+    uint4* __restrict__ x_perm) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  const int slots = T * k;
+  // rows past n_kept are marked unused (disjoint from the rows written below)
+  {
+    const int n_kept = n_kept_dropped[0];
+    for (int r = n_kept + blockIdx.x * blockDim.x + threadIdx.x; r < slots;
+         r += gridDim.x * blockDim.x)
+      row_slot[r] = -1;
+  }
+  if (t >= T) return;
+  int row = -1;
+  if (lane < k) {
+    const int slot = t * k + lane;
+    const int e = idx[slot];
+    const int lr = local_rank[slot];
+    if (e >= 0 && e < E && lr >= 0) {
+      const int pos = chunk_base[static_cast<size_t>(t / kDispatchChunk) * E + e] + lr;
+      if (capacity < 0 || pos < capacity) row = offsets[e] + pos;
+    }
+    slot_row[slot] = row;
+    if (row >= 0) row_slot[row] = slot;
+  }
+  const int nvec = d / 8;
+  const uint4* src = x + static_cast<size_t>(t) * nvec;
+#pragma unroll 2
+  for (int v = lane; v < nvec; v += 32) {
+    const uint4 val = src[v];
+    for (int j = 0; j < k; ++j) {
+      const int r = __shfl_sync(0xffffffffu, row, j);
+      if (r >= 0) x_perm[static_cast<size_t>(r) * nvec + v] = val;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __restrict__ offsets,
+                                                             int E, int rows_max,
+                                                             int32_t* __restrict__ tile_off,
+                                                             int32_t* dev_status) {
+  __shared__ int sm[32];
+  const int e = threadIdx.x;
+  int mt = 0;
+  if (e < E) {
+    const int lo = offsets[e], hi = offsets[e + 1];
+    if (lo < 0 || hi < lo || hi > rows_max) {
+      report_status(dev_status, MOE_ERR_BAD_INDEX);
+    } else {
+      mt = (hi - lo + kBM - 1) / kBM;
+    }
+  }
+  int total;
+  const int excl = block_exclusive_scan_1024(mt, sm, &total);
+  if (e < E) tile_off[e] = excl;
+  if (e == 0) tile_off[E] = total;
+}
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& v, float scale) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    acc[2 * i] += scale * f.x;
+    acc[2 * i + 1] += scale * f.y;
+  }
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&a)[8]) {
+  uint4 o;
+  o.x = pack_bf16x2(a[0], a[1]);
+  o.y = pack_bf16x2(a[2], a[3]);
+  o.z = pack_bf16x2(a[4], a[5]);
+  o.w = pack_bf16x2(a[6], a[7]);
+  return o;
+}
+
+// y[t] = sum_j y_perm[slot_row[t*k+j]] (kept slots, rank order, fp32) -> bf16.
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y_perm,
+                                                      const int32_t* __restrict__ slot_row,
+                                                      int T, int d, int k,
+                                                      uint4* __restrict__ y) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const int row = lane < k ? slot_row[static_cast<size_t>(t) * k + lane] : -1;
+  const int nvec = d / 8;
+  for (int v = lane; v < nvec; v += 32) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int j = 0; j < k; ++j) {
+      const int r = __shfl_sync(0xffffffffu, row, j);
+      if (r >= 0) add_bf16x8(acc, y_perm[static_cast<size_t>(r) * nvec + v], 1.f);
+    }
+    y[static_cast<size_t>(t) * nvec + v] = pack_bf16x8(acc);
+  }
+}
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// dz_perm[row] = g * dy[t];  dgate[slot] = <dy[t], y_perm[row]> / g  (kept slots), else 0.
+__global__ void __launch_bounds__(256) combine_bwd_kernel(
+    const uint4* __restrict__ dy, const uint4* __restrict__ y_perm,
+    const int32_t* __restrict__ slot_row, const float* __restrict__ gate, int T, int d, int k,
+    uint4* __restrict__ dz_perm, float* __restrict__ dgate) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const int nvec = d / 8;
+  const uint4* dyr = dy + static_cast<size_t>(t) * nvec;
+  for (int j = 0; j < k; ++j) {
+    const size_t slot = static_cast<size_t>(t) * k + j;
+    const int r = slot_row[slot];
+    if (r < 0) {
+      if (lane == 0) dgate[slot] = 0.f;
+      continue;
+    }
+    const float g = gate[slot];
+    float dot = 0.f;
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 a = dyr[v];
+      float fa[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float fb[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      add_bf16x8(fa, a, 1.f);
+      add_bf16x8(fb, y_perm[static_cast<size_t>(r) * nvec + v], 1.f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        dot += fa[i] * fb[i];
+        fa[i] *= g;
+      }
+      dz_perm[static_cast<size_t>(r) * nvec + v] = pack_bf16x8(fa);
+    }
+    dot = warp_sum_f(dot);
+    if (lane == 0) dgate[slot] = g > 0.f ? dot / g : 0.f;
+  }
+}
+
+// dx[t] = sum over kept slots of dx_perm rows (fp32, overwritten).
+__global__ void __launch_bounds__(256) dispatch_bwd_kernel(const uint4* __restrict__ dx_perm,
+                                                           const int32_t* __restrict__ slot_row,
+                                                           int T, int d, int k,
+                                                           float4* __restrict__ dx) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const int row = lane < k ? slot_row[static_cast<size_t>(t) * k + lane] : -1;
+  const int nvec = d / 8;
+  for (int v = lane; v < nvec; v += 32) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int j = 0; j < k; ++j) {
+      const int r = __shfl_sync(0xffffffffu, row, j);
+      if (r >= 0) add_bf16x8(acc, dx_perm[static_cast<size_t>(r) * nvec + v], 1.f);
+    }
+    float4* o = dx + (static_cast<size_t>(t) * nvec + v) * 2;
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
+// dx[t] += sum_j c_j W_r[e_j],  c_j = g_j (dg_j - sum_i g_i dg_i).
+__global__ void __launch_bounds__(256) route_bwd_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ gate,
+    const float* __restrict__ dgate, const float4* __restrict__ w_router, int T, int d, int E,
+    int k, float4* __restrict__ dx) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  float g = 0.f, dg = 0.f;
+  int e = 0;
+  if (lane < k) {
+    const size_t slot = static_cast<size_t>(t) * k + lane;
+    g = gate[slot];
+    dg = dgate[slot];
+    e = idx[slot];
+    if (e < 0 || e >= E) { e = 0; g = 0.f; }
+  }
+  const float sgd = warp_sum_f(g * dg);
+  const float c = g * (dg - sgd);
+  const int n4 = d / 4;
+  for (int v = lane; v < n4; v += 32) {
+    float4 acc = dx[static_cast<size_t>(t) * n4 + v];
+    for (int j = 0; j < k; ++j) {
+      const float cj = __shfl_sync(0xffffffffu, c, j);
+      const int ej = __shfl_sync(0xffffffffu, e, j);
+      const float4 w = __ldg(&w_router[static_cast<size_t>(ej) * n4 + v]);
+      acc.x += cj * w.x;
+      acc.y += cj * w.y;
+      acc.z += cj * w.z;
+      acc.w += cj * w.w;
+    }
+    dx[static_cast<size_t>(t) * n4 + v] = acc;
+  }
+}
+
+int grid_for_tokens(int T) { return (T + 7) / 8; }
+
+}  // namespace
+
+int launch_dispatch(const int32_t* idx, const __nv_bfloat16* x, int T, int d, int E, int k,
+                    int capacity, int32_t* counts, int32_t* offsets, int32_t* slot_row,
+                    int32_t* row_slot, int32_t* n_kept_dropped, __nv_bfloat16* x_perm,
+                    int32_t* local_rank, int32_t* chunk_cnt, int32_t* dev_status,
+                    cudaStream_t s) {
+  const int nch = dispatch_num_chunks(T);
+  dispatch_count_kernel<<<(nch + 3) / 4, 128, 4 * E * sizeof(int), s>>>(idx, T, E, k, local_rank,
+                                                                        chunk_cnt, dev_status);
+  dispatch_scan_chunks_kernel<<<(E + 31) / 32, 1024, 0, s>>>(chunk_cnt, nch, E, counts);
+  dispatch_offsets_kernel<<<1, 1024, 0, s>>>(counts, E, capacity, T * k, offsets,
+                                             n_kept_dropped);
+  dispatch_scatter_kernel<<<grid_for_tokens(T), 256, 0, s>>>(
+      idx, local_rank, chunk_cnt, offsets, n_kept_dropped, reinterpret_cast<const uint4*>(x),
+      T, d, E, k, capacity, slot_row, row_slot, reinterpret_cast<uint4*>(x_perm));
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_tile_schedule(const int32_t* offsets, int E, int rows_max, int32_t* tile_off,
+                         int32_t* dev_status, cudaStream_t s) {
+  tile_schedule_kernel<<<1, 1024, 0, s>>>(offsets, E, rows_max, tile_off, dev_status);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_combine(const __nv_bfloat16* y_perm, const int32_t* slot_row, int T, int d, int k,
+                   __nv_bfloat16* y, cudaStream_t s) {
+  combine_kernel<<<grid_for_tokens(T), 256, 0, s>>>(reinterpret_cast<const uint4*>(y_perm),
+                                                    slot_row, T, d, k,
+                                                    reinterpret_cast<uint4*>(y));
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_combine_bwd(const __nv_bfloat16* dy, const __nv_bfloat16* y_perm,
+                       const int32_t* slot_row, const float* gate, int T, int d, int k,
+                       __nv_bfloat16* dz_perm, float* dgate, cudaStream_t s) {
+  combine_bwd_kernel<<<grid_for_tokens(T), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(dy), reinterpret_cast<const uint4*>(y_perm), slot_row,
+      gate, T, d, k, reinterpret_cast<uint4*>(dz_perm), dgate);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_dispatch_bwd(const __nv_bfloat16* dx_perm, const int32_t* slot_row, int T, int d,
+                        int k, float* dx, cudaStream_t s) {
+  dispatch_bwd_kernel<<<grid_for_tokens(T), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(dx_perm), slot_row, T, d, k, reinterpret_cast<float4*>(dx));
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_route_bwd(const int32_t* idx, const float* gate, const float* dgate,
+                     const float* w_router, int T, int d, int E, int k, float* dx,
+                     cudaStream_t s) {
+  route_bwd_kernel<<<grid_for_tokens(T), 256, 0, s>>>(
+      idx, gate, dgate, reinterpret_cast<const float4*>(w_router), T, d, E, k,
+      reinterpret_cast<float4*>(dx));
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace moe

@@ -1,0 +1,445 @@
+// Persistent, warp-specialised tcgen05 GEMM used for every contraction of the MoE layer:
+// the router product, the grouped expert gate/up and down projections (with their
+// fused SwiGLU / gate-scaling epilogues and the LoRA K-blocks), the LoRA down-projections
+// and the backward data-gradient products.
+//
+// Roles (256 threads, one CTA per SM):
+//   warp 0       TMA producer: 64-wide K blocks of A and of each B into a STAGES-deep ring
+//   warp 1       TMEM allocator and MMA issuer (one thread issues tcgen05.mma)
+//   warps 4..7   epilogue: tcgen05.ld of the accumulator rows (warp w reads TMEM lanes
+//                32*(w%4) .. +31), fused math, global stores
+// Two TMEM accumulator buffers let the epilogue of tile i overlap the main loop of tile i+1.
+//
+// Operand tiles in shared memory use the 128-byte swizzle that TMA writes:
+//   K-major  (rows x 64 K): 128-byte rows, 8-row atoms of 1024 B -> SBO = 1024; the k-th
+//            16-wide MMA step starts 32 B further into the atom.
+//   MN-major (64 K x 64 MN per box): 128-byte K-rows; boxes for consecutive 64-wide MN
+//            chunks 8 KB apart -> LBO = 8192, SBO = 1024; the k-th MMA step starts 2 KB on.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace moe {
+
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES>
+struct GemmCfg {
+  static constexpr int A_BYTES = kBM * kBK * 2;
+  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
+  static constexpr int ACC_COLS = NB * BN;
+  static constexpr int TMEM_COLS = (2 * ACC_COLS <= 32)    ? 32
+                                   : (2 * ACC_COLS <= 64)  ? 64
+                                   : (2 * ACC_COLS <= 128) ? 128
+                                   : (2 * ACC_COLS <= 256) ? 256
+                                                           : 512;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
+  static_assert(2 * ACC_COLS <= 512, "two accumulators must fit in TMEM");
+  static_assert(!B_MN || BN % 64 == 0 || BN <= 64, "MN-major B uses 64-wide boxes");
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+};
+
+struct TileCoord {
+  int g, m, n, row0, rows_valid;
+};
+
+__device__ __forceinline__ bool decode_tile(const GemmParams& P, int tile, TileCoord& tc) {
+  if (P.group_off == nullptr) {
+    const int total = P.m_tiles * P.n_tiles;
+    if (tile >= total) return false;
+    tc.g = 0;
+    tc.n = tile / P.m_tiles;
+    tc.m = tile - tc.n * P.m_tiles;
+    tc.row0 = tc.m * kBM;
+    tc.rows_valid = min(kBM, P.M - tc.row0);
+    return true;
+  }
+  const int total = __ldg(&P.tile_off[P.G]) * P.n_tiles;
+  if (tile >= total) return false;
+  int lo = 0, hi = P.G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(&P.tile_off[mid]) * P.n_tiles <= tile) lo = mid; else hi = mid - 1;
+  }
+  const int t0 = __ldg(&P.tile_off[lo]);
+  const int mt = __ldg(&P.tile_off[lo + 1]) - t0;
+  const int local = tile - t0 * P.n_tiles;
+  tc.g = lo;
+  tc.n = local / mt;
+  tc.m = local - tc.n * mt;
+  const int r0 = __ldg(&P.group_off[lo]);
+  tc.row0 = r0 + tc.m * kBM;
+  tc.rows_valid = min(kBM, __ldg(&P.group_off[lo + 1]) - tc.row0);
+  return true;
+}
+
+// Store 16 consecutive bf16 values of one row, clipped to `ncols_left` columns.
+__device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float (&v)[16],
+                                              int ncols_left) {
+  if (ncols_left >= 16) {
+    uint4 a, b;
+    a.x = pack_bf16x2(v[0], v[1]);   a.y = pack_bf16x2(v[2], v[3]);
+    a.z = pack_bf16x2(v[4], v[5]);   a.w = pack_bf16x2(v[6], v[7]);
+    b.x = pack_bf16x2(v[8], v[9]);   b.y = pack_bf16x2(v[10], v[11]);
+    b.z = pack_bf16x2(v[12], v[13]); b.w = pack_bf16x2(v[14], v[15]);
+    reinterpret_cast<uint4*>(dst)[0] = a;
+    reinterpret_cast<uint4*>(dst)[1] = b;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (i < ncols_left) dst[i] = __float2bfloat16_rn(v[i]);
+  }
+}
+
+__device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* src, float (&v)[16]) {
+  const uint4 a = reinterpret_cast<const uint4*>(src)[0];
+  const uint4 b = reinterpret_cast<const uint4*>(src)[1];
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+    float2 f = __bfloat1622float2(p);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES>
+__global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ GemmParams P) {
+  using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* drain = reinterpret_cast<uint64_t*>(tmem_slot + 2);  // 8-byte aligned slot
+  __shared__ int zero_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    zero_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < P.nmaps; ++i) tma_prefetch_desc(&P.maps[i]);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    const uint64_t pol_a = l2_policy_evict_last();
+    const uint64_t pol_b = l2_policy_evict_first();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    TileCoord tc;
+    for (int tile = blockIdx.x; ok && decode_tile(P, tile, tc); tile += gridDim.x) {
+      for (int s = 0; ok && s < P.nseg; ++s) {
+        const GemmSeg& sg = P.seg[s];
+        for (int kb = 0; kb < sg.nkb; ++kb) {
+          int w = 1;
+          if (lane == 0) w = mbar_wait(&empty[stage], phase ^ 1, abort_flag) ? 1 : 0;
+          w = __shfl_sync(0xffffffffu, w, 0);
+          if (!w) { ok = false; break; }
+          if (lane == 0) {
+            uint8_t* sA = smem + stage * C::STAGE_BYTES;
+            uint32_t bytes = C::A_BYTES;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) bytes += (sg.b_map[b] >= 0) ? C::B_BYTES : 0;
+            mbar_arrive_expect_tx(&full[stage], bytes);
+            const int ka = sg.a_k0 + kb * kBK;
+            if (!A_MN) {
+              tma_load_3d(sA, &P.maps[sg.a_map], &full[stage], ka, tc.row0, 0, pol_a);
+            } else {
+              tma_load_3d(sA, &P.maps[sg.a_map], &full[stage], tc.row0, ka, 0, pol_a);
+              tma_load_3d(sA + 8192, &P.maps[sg.a_map], &full[stage], tc.row0 + 64, ka, 0,
+                          pol_a);
+            }
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              if (sg.b_map[b] < 0) continue;
+              uint8_t* sB = sA + C::A_BYTES + b * C::B_BYTES;
+              const int kbk = sg.b_k0[b] + kb * kBK;
+              const int z = (P.group_off != nullptr) ? tc.g : sg.b_z[b];
+              if (!B_MN) {
+                tma_load_3d(sB, &P.maps[sg.b_map[b]], &full[stage], kbk, tc.n * BN, z, pol_b);
+              } else {
+#pragma unroll
+                for (int c = 0; c < (BN + 63) / 64; ++c)
+                  tma_load_3d(sB + c * 8192, &P.maps[sg.b_map[b]], &full[stage],
+                              tc.n * BN + c * 64, kbk, z, pol_b);
+              }
+            }
+          }
+          __syncwarp();
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      report_status(P.dev_status, MOE_ERR_TIMEOUT);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, A_MN, B_MN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    TileCoord tc;
+    for (int tile = blockIdx.x; ok && decode_tile(P, tile, tc); tile += gridDim.x) {
+      int w = 1;
+      if (lane == 0) w = mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag) ? 1 : 0;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (!w) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_base = tmem_base + acc * C::ACC_COLS;
+      for (int s = 0; ok && s < P.nseg; ++s) {
+        const GemmSeg& sg = P.seg[s];
+        for (int kb = 0; kb < sg.nkb; ++kb) {
+          if (lane == 0) w = mbar_wait(&full[stage], phase, abort_flag) ? 1 : 0;
+          w = __shfl_sync(0xffffffffu, w, 0);
+          if (!w) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint64_t adesc = A_MN ? smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
+                                          : smem_desc_sw128(a_addr + k * 32, 16, 1024);
+              const uint32_t accumulate = (s > 0 || kb > 0 || k > 0) ? 1u : 0u;
+#pragma unroll
+              for (int b = 0; b < NB; ++b) {
+                if (sg.b_map[b] < 0) continue;
+                const uint32_t b_addr = a_addr + C::A_BYTES + b * C::B_BYTES;
+                const uint64_t bdesc = B_MN ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                            : smem_desc_sw128(b_addr + k * 32, 16, 1024);
+                umma_bf16(d_base + b * BN, adesc, bdesc, idesc, accumulate);
+              }
+            }
+            umma_commit(&empty[stage]);
+          }
+          __syncwarp();
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) umma_commit(&acc_full[acc]);
+      __syncwarp();
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      report_status(P.dev_status, MOE_ERR_TIMEOUT);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int r_local = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    TileCoord tc;
+    for (int tile = blockIdx.x; decode_tile(P, tile, tc); tile += gridDim.x) {
+      int w = 1;
+      if (lane == 0) w = mbar_wait(&acc_full[acc], acc_phase, abort_flag) ? 1 : 0;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (!w) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
+      const bool valid = r_local < tc.rows_valid;
+      const long row = static_cast<long>(tc.row0) + r_local;
+      const int col0 = tc.n * BN;
+
+      if constexpr (EPI == EPI_F32_BIAS) {
+        float* out = reinterpret_cast<float*>(P.out0);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(t_row + c, v);
+          tmem_ld_wait();
+          const int col = col0 + c;
+          if (valid && col < P.N) {
+            float* dst = out + row * P.ldo + col;
+            if (col + 16 <= P.N && (P.ldo & 3) == 0) {
+#pragma unroll
+              for (int i = 0; i < 16; i += 4) {
+                float4 o;
+                o.x = v[i] + (P.bias ? __ldg(&P.bias[col + i]) : 0.f);
+                o.y = v[i + 1] + (P.bias ? __ldg(&P.bias[col + i + 1]) : 0.f);
+                o.z = v[i + 2] + (P.bias ? __ldg(&P.bias[col + i + 2]) : 0.f);
+                o.w = v[i + 3] + (P.bias ? __ldg(&P.bias[col + i + 3]) : 0.f);
+                *reinterpret_cast<float4*>(dst + i) = o;
+              }
+            } else {
+              for (int i = 0; i < 16 && col + i < P.N; ++i)
+                dst[i] = v[i] + (P.bias ? __ldg(&P.bias[col + i]) : 0.f);
+            }
+          }
+        }
+      } else if constexpr (EPI == EPI_SWIGLU) {
+        __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(P.out0);
+        __nv_bfloat16* sg = reinterpret_cast<__nv_bfloat16*>(P.out1);
+        __nv_bfloat16* su = reinterpret_cast<__nv_bfloat16*>(P.out2);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          float g[16], u[16];
+          tmem_ld16(t_row + c, g);
+          tmem_ld16(t_row + BN + c, u);
+          tmem_ld_wait();
+          const int col = col0 + c;
+          if (valid && col < P.N) {
+            const long off = row * P.ldo + col;
+            if (sg) store_bf16x16(sg + off, g, P.N - col);
+            if (su) store_bf16x16(su + off, u, P.N - col);
+            float hv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) hv[i] = silu_f(g[i]) * u[i];
+            store_bf16x16(h + off, hv, P.N - col);
+          }
+        }
+      } else if constexpr (EPI == EPI_GATE_SCALE) {
+        __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(P.out0);
+        float gs = 0.f;
+        if (valid) gs = __ldg(&P.gate[__ldg(&P.row_slot[row])]);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(t_row + c, v);
+          tmem_ld_wait();
+          const int col = col0 + c;
+          if (valid && col < P.N) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] *= gs;
+            store_bf16x16(y + row * P.ldo + col, v, P.N - col);
+          }
+        }
+      } else if constexpr (EPI == EPI_SCALE) {
+#pragma unroll 1
+        for (int b = 0; b < NB; ++b) {
+          __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(b == 0 ? P.out0 : P.out1);
+#pragma unroll 1
+          for (int c = 0; c < BN; c += 16) {
+            float v[16];
+            tmem_ld16(t_row + b * BN + c, v);
+            tmem_ld_wait();
+            const int col = col0 + c;
+            if (valid && o != nullptr && col < P.N) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] *= P.scale;
+              store_bf16x16(o + row * P.ldo + col, v, P.N - col);
+            }
+          }
+        }
+      } else if constexpr (EPI == EPI_SWIGLU_BWD) {
+        // acc0 = dh; saved a_g (in0), a_u (in1) -> da_g (out0), da_u (out1)
+        const __nv_bfloat16* ag = reinterpret_cast<const __nv_bfloat16*>(P.in0);
+        const __nv_bfloat16* au = reinterpret_cast<const __nv_bfloat16*>(P.in1);
+        __nv_bfloat16* dag = reinterpret_cast<__nv_bfloat16*>(P.out0);
+        __nv_bfloat16* dau = reinterpret_cast<__nv_bfloat16*>(P.out1);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          float dh[16];
+          tmem_ld16(t_row + c, dh);
+          tmem_ld_wait();
+          const int col = col0 + c;
+          if (valid && col < P.N) {
+            const long off = row * P.ldo + col;
+            float g[16], u[16], o1[16], o2[16];
+            load_bf16x16(ag + off, g);
+            load_bf16x16(au + off, u);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float sgm = 1.0f / (1.0f + __expf(-g[i]));
+              o1[i] = dh[i] * u[i] * sgm * (1.0f + g[i] * (1.0f - sgm));
+              o2[i] = dh[i] * g[i] * sgm;
+            }
+            store_bf16x16(dag + off, o1, P.N - col);
+            store_bf16x16(dau + off, o2, P.N - col);
+          }
+        }
+      } else if constexpr (EPI == EPI_STORE) {
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(P.out0);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(t_row + c, v);
+          tmem_ld_wait();
+          const int col = col0 + c;
+          if (valid && col < P.N) store_bf16x16(o + row * P.ldo + col, v, P.N - col);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      report_status(P.dev_status, MOE_ERR_TIMEOUT);
+    }
+  }
+
+  // All roles are done.  On the normal path every TMA load was consumed and every MMA was
+  // waited for through acc_full.  After an abort, the MMA thread waits (bounded) for its
+  // own tcgen05 ops and thread 0 gives in-flight TMA copies a bounded grace period, so
+  // nothing lands in shared memory or TMEM after the CTA has released them.
+  __syncthreads();
+  if (*abort_flag) {
+    if (threadIdx.x == 32) {
+      umma_commit(drain);
+      mbar_wait(drain, 0, reinterpret_cast<volatile int*>(&zero_flag));
+    }
+    if (threadIdx.x == 0) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 2000000ull) {
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES>
+int launch_gemm(const GemmParams& P, cudaStream_t stream) {
+  using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES>;
+  auto kern = gemm_kernel<BN, NB, A_MN, B_MN, EPI, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  kern<<<num_sms(), 256, C::SMEM_BYTES, stream>>>(P);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace moe

@@ -1,0 +1,30 @@
+// Forward instantiations of the tcgen05 GEMM (router, expert gate/up, expert down, LoRA).
+#include "gemm.cuh"
+
+namespace moe {
+
+int launch_gemm_router(const GemmParams& P, cudaStream_t s) {
+  return launch_gemm<128, 1, false, false, EPI_F32_BIAS, 6>(P, s);
+}
+
+int launch_gemm_gateup(const GemmParams& P, cudaStream_t s) {
+  return launch_gemm<128, 2, false, false, EPI_SWIGLU, 4>(P, s);
+}
+
+int launch_gemm_down(const GemmParams& P, cudaStream_t s) {
+  return launch_gemm<256, 1, false, false, EPI_GATE_SCALE, 4>(P, s);
+}
+
+int launch_gemm_lora_u2(const GemmParams& P, int r, cudaStream_t s) {
+  if (r <= 16) return launch_gemm<16, 2, false, false, EPI_SCALE, 8>(P, s);
+  if (r <= 32) return launch_gemm<32, 2, false, false, EPI_SCALE, 8>(P, s);
+  return launch_gemm<64, 2, false, false, EPI_SCALE, 6>(P, s);
+}
+
+int launch_gemm_lora_u1(const GemmParams& P, int r, cudaStream_t s) {
+  if (r <= 16) return launch_gemm<16, 1, false, false, EPI_SCALE, 8>(P, s);
+  if (r <= 32) return launch_gemm<32, 1, false, false, EPI_SCALE, 8>(P, s);
+  return launch_gemm<64, 1, false, false, EPI_SCALE, 8>(P, s);
+}
+
+}  // namespace moe

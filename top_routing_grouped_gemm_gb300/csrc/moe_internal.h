@@ -1,0 +1,90 @@
+// Internal declarations shared by the translation units of libmoe.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Bounded device-side waits give up after this much wall time (ns).
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+// ------------------------------------------------------------------ GEMM description
+//
+// One persistent tcgen05 kernel serves every contraction of the layer.  A CTA owns a
+// 128-row output tile and up to two accumulators of BN columns each (NB operands "B"
+// sharing one operand "A"), walks a list of K segments (each segment names the tensor
+// maps and K offsets its 64-wide K blocks come from), then runs a fused epilogue.
+
+constexpr int kMaxMaps = 8;
+constexpr int kMaxSegs = 4;
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+
+enum Epilogue : int {
+  EPI_F32_BIAS = 0,    // out_f32[row, col] = acc0 + bias[col]           (router logits)
+  EPI_SWIGLU = 1,      // out_bf16 = silu(acc0) * acc1; optional save of acc0/acc1 as bf16
+  EPI_GATE_SCALE = 2,  // out_bf16 = gate[row_slot[row]] * acc0            (expert down)
+  EPI_SCALE = 3,       // out_bf16_i = scale * acc_i for each B operand     (LoRA u, v)
+  EPI_SWIGLU_BWD = 4,  // da_g, da_u from acc0 = dh and saved a_g, a_u
+  EPI_STORE = 5,       // out_bf16 = acc0                                   (dx_perm)
+};
+
+struct GemmSeg {
+  int nkb;        // number of 64-wide K blocks in this segment
+  int a_map;      // tensor map of operand A
+  int a_k0;       // K element offset of the first block in operand A
+  int b_map[2];   // tensor map of each B operand, -1 = this accumulator skips the segment
+  int b_k0[2];    // K element offset in each B operand
+  int b_z[2];     // third coordinate of B for dense problems (ignored when grouped)
+};
+
+struct GemmParams {
+  CUtensorMap maps[kMaxMaps];
+  int nmaps;
+  GemmSeg seg[kMaxSegs];
+  int nseg;
+  // M grouping.  Grouped: rows of group g are [group_off[g], group_off[g+1]) and its
+  // m-tiles are numbered tile_off[g] .. tile_off[g+1]-1; B's third coordinate is g.
+  // Dense (group_off == nullptr): one group of M rows, m_tiles tiles.
+  const int* group_off;
+  const int* tile_off;
+  int G;
+  int M;
+  int m_tiles;
+  int n_tiles;     // number of BN-wide column tiles of each accumulator
+  int N;           // valid columns of each accumulator (stores are clipped to N)
+  // epilogue operands
+  void* out0;
+  void* out1;
+  void* out2;
+  void* out3;
+  int ldo;                  // leading dimension (elements) of the outputs
+  const float* bias;        // EPI_F32_BIAS
+  const float* gate;        // EPI_GATE_SCALE: gate per slot
+  const int* row_slot;      // EPI_GATE_SCALE: slot per row
+  const void* in0;          // EPI_SWIGLU_BWD: saved a_g
+  const void* in1;          // EPI_SWIGLU_BWD: saved a_u
+  float scale;              // EPI_SCALE
+  int* dev_status;
+};
+
+// Host helpers (gemm_host.cu).
+int encode_map_kmajor(CUtensorMap* map, const void* base, uint64_t k_extent, uint64_t rows,
+                      uint64_t groups, uint32_t box_rows);
+int encode_map_mnmajor(CUtensorMap* map, const void* base, uint64_t mn_extent,
+                       uint64_t k_rows, uint64_t groups);
+int num_sms();
+
+// Kernel launchers (gemm_kernels.cu).  Return cudaError_t as int.
+int launch_gemm_router(const GemmParams& P, cudaStream_t s);        // BN=128, NB=1
+int launch_gemm_gateup(const GemmParams& P, cudaStream_t s);        // BN=128, NB=2, SwiGLU
+int launch_gemm_down(const GemmParams& P, cudaStream_t s);          // BN=256, NB=1
+int launch_gemm_lora_u2(const GemmParams& P, int r, cudaStream_t s); // BN=r pad, NB=2
+int launch_gemm_lora_u1(const GemmParams& P, int r, cudaStream_t s); // BN=r pad, NB=1
+
+}  // namespace moe

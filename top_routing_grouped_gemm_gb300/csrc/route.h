@@ -1,0 +1,46 @@
+// Launchers of the SIMT kernels (router tail, dispatch, combine, backward helpers).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+constexpr int kRouteTokensPerBlock = 64;  // tokens per row of prob_partials
+constexpr int kDispatchChunk = 64;        // tokens counted sequentially by one warp
+
+__host__ __device__ inline int route_num_partials(int T) {
+  return (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
+}
+__host__ __device__ inline int dispatch_num_chunks(int T) { return (T + kDispatchChunk - 1) / kDispatchChunk; }
+
+int launch_split_router(const float* w, __nv_bfloat16* hi, __nv_bfloat16* lo, size_t n,
+                        cudaStream_t s);
+int launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* idx, float* gate,
+                        float* partials, cudaStream_t s);
+int launch_aux_loss(const int32_t* counts, const float* partials, int n_partials, int T, int k,
+                    int E, float* aux_out, cudaStream_t s);
+
+// capacity < 0 means unlimited.
+int launch_dispatch(const int32_t* idx, const __nv_bfloat16* x, int T, int d, int E, int k,
+                    int capacity, int32_t* counts, int32_t* offsets, int32_t* slot_row,
+                    int32_t* row_slot, int32_t* n_kept_dropped, __nv_bfloat16* x_perm,
+                    int32_t* local_rank, int32_t* chunk_cnt, int32_t* dev_status,
+                    cudaStream_t s);
+int launch_tile_schedule(const int32_t* offsets, int E, int rows_max, int32_t* tile_off,
+                         int32_t* dev_status, cudaStream_t s);
+int launch_combine(const __nv_bfloat16* y_perm, const int32_t* slot_row, int T, int d, int k,
+                   __nv_bfloat16* y, cudaStream_t s);
+int launch_combine_bwd(const __nv_bfloat16* dy, const __nv_bfloat16* y_perm,
+                       const int32_t* slot_row, const float* gate, int T, int d, int k,
+                       __nv_bfloat16* dz_perm, float* dgate, cudaStream_t s);
+int launch_dispatch_bwd(const __nv_bfloat16* dx_perm, const int32_t* slot_row, int T, int d,
+                        int k, float* dx, cudaStream_t s);
+int launch_route_bwd(const int32_t* idx, const float* gate, const float* dgate,
+                     const float* w_router, int T, int d, int E, int k, float* dx,
+                     cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,334 @@
+"""ctypes binding of libmoe.so (the C ABI in include/moe.h).
+
+Each ``moe_*`` function here has the name and the argument order of the C entry point and
+only marshals arguments: torch tensors become device pointers, the problem becomes a
+``moe_problem`` struct, the current torch stream is passed as the CUDA stream, and a
+non-zero status raises :class:`MoEError`.  Every computation happens in the CUDA kernels
+of the library.  :func:`layer_forward` / :func:`layer_backward` chain the entry points for
+one layer and allocate the outputs with torch (the library itself never allocates).
+
+There is no fallback: if libmoe.so is missing or cannot be loaded, calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+c_i32 = ctypes.c_int32
+c_vp = ctypes.c_void_p
+c_sz = ctypes.c_size_t
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+                3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
+                6: "MOE_ERR_BAD_INDEX"}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+
+
+class moe_problem(ctypes.Structure):
+    _fields_ = [("T", c_i32), ("d", c_i32), ("E", c_i32), ("k", c_i32), ("F", c_i32),
+                ("r", c_i32), ("lora_scale", ctypes.c_float), ("cap_num", c_i32),
+                ("cap_den", c_i32)]
+
+
+class moe_lora(ctypes.Structure):
+    _fields_ = [(n, c_vp) for n in ("A_g", "B_g", "A_u", "B_u", "A_d", "B_d")]
+
+
+class moe_lora_grad(ctypes.Structure):
+    _fields_ = [(n, c_vp) for n in ("dA_g", "dB_g", "dA_u", "dB_u", "dA_d", "dB_d")]
+
+
+class moe_ffn_saved(ctypes.Structure):
+    _fields_ = [(n, c_vp) for n in ("a_gate", "a_up", "u_gate", "u_up", "u_down")]
+
+
+_P = ctypes.POINTER(moe_problem)
+_SIGS = {
+    "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_version": (ctypes.c_int, []),
+    "moe_route_num_partials": (ctypes.c_int, [_P]),
+    "moe_route_workspace_size": (c_sz, [_P]),
+    "moe_route": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+    "moe_route_from_logits": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "moe_dispatch_workspace_size": (c_sz, [_P]),
+    "moe_dispatch": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+    "moe_expert_ffn_workspace_size": (c_sz, [_P, c_i32]),
+    "moe_expert_ffn": (ctypes.c_int, [_P, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                      ctypes.POINTER(moe_lora), c_vp, c_vp,
+                                      ctypes.POINTER(moe_ffn_saved), c_vp, c_sz, c_vp, c_vp]),
+    "moe_combine": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp]),
+    "moe_aux_loss": (ctypes.c_int, [_P, c_vp, c_vp, c_i32, c_vp, c_vp]),
+    "moe_combine_bwd": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "moe_expert_ffn_bwd_workspace_size": (c_sz, [_P, c_i32]),
+    "moe_expert_ffn_bwd": (ctypes.c_int, [_P, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                          ctypes.POINTER(moe_lora), ctypes.POINTER(moe_ffn_saved),
+                                          c_vp, c_vp, c_vp, ctypes.POINTER(moe_lora_grad),
+                                          c_vp, c_sz, c_vp, c_vp]),
+    "moe_dispatch_bwd": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp]),
+    "moe_route_bwd": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+}
+
+_lib = None
+
+
+def lib():
+    """Load libmoe.so once; raise if it is missing (there is no fallback path)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run top_routing_grouped_gemm_gb300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+# ----------------------------------------------------------------------------- marshalling
+
+@dataclass
+class Problem:
+    T: int
+    d: int
+    E: int
+    k: int
+    F: int
+    r: int = 0
+    lora_scale: float = 0.0
+    cap_num: int = 0
+    cap_den: int = 0
+
+    def c(self):
+        return ctypes.byref(moe_problem(self.T, self.d, self.E, self.k, self.F, self.r,
+                                        self.lora_scale, self.cap_num, self.cap_den))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(name, status):
+    if status != MOE_OK:
+        raise MoEError(name, status)
+
+
+def _lora(lora):
+    if lora is None:
+        return None
+    return ctypes.byref(moe_lora(*[_ptr(lora[n]) for n in ("A_g", "B_g", "A_u", "B_u", "A_d", "B_d")]))
+
+
+def _saved(saved):
+    if saved is None:
+        return None
+    return ctypes.byref(moe_ffn_saved(*[_ptr(saved.get(n)) for n in
+                                        ("a_gate", "a_up", "u_gate", "u_up", "u_down")]))
+
+
+def _grads(grads):
+    if grads is None:
+        return None
+    return ctypes.byref(moe_lora_grad(*[_ptr(grads.get(n)) for n in
+                                        ("dA_g", "dB_g", "dA_u", "dB_u", "dA_d", "dB_d")]))
+
+
+def _ws(t):
+    return (_ptr(t), 0 if t is None else t.numel() * t.element_size())
+
+
+# ----------------------------------------------------------------------------- entry points
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(status).decode()
+
+
+def moe_version() -> int:
+    return lib().moe_version()
+
+
+def moe_route_num_partials(p: Problem) -> int:
+    return lib().moe_route_num_partials(p.c())
+
+
+def moe_route_workspace_size(p: Problem) -> int:
+    return lib().moe_route_workspace_size(p.c())
+
+
+def moe_route(p, x, w_router, bias, topk_idx, topk_gate, prob_partials, logits, workspace,
+              dev_status=None, stream=None):
+    wp, wn = _ws(workspace)
+    _check("moe_route", lib().moe_route(p.c(), _ptr(x), _ptr(w_router), _ptr(bias),
+                                        _ptr(topk_idx), _ptr(topk_gate), _ptr(prob_partials),
+                                        _ptr(logits), wp, wn, _ptr(dev_status), _stream(stream)))
+
+
+def moe_route_from_logits(p, logits, topk_idx, topk_gate, prob_partials, dev_status=None,
+                          stream=None):
+    _check("moe_route_from_logits",
+           lib().moe_route_from_logits(p.c(), _ptr(logits), _ptr(topk_idx), _ptr(topk_gate),
+                                       _ptr(prob_partials), _ptr(dev_status), _stream(stream)))
+
+
+def moe_dispatch_workspace_size(p: Problem) -> int:
+    return lib().moe_dispatch_workspace_size(p.c())
+
+
+def moe_dispatch(p, topk_idx, x, counts, offsets, slot_row, row_slot, n_kept_dropped, x_perm,
+                 workspace, dev_status=None, stream=None):
+    wp, wn = _ws(workspace)
+    _check("moe_dispatch", lib().moe_dispatch(p.c(), _ptr(topk_idx), _ptr(x), _ptr(counts),
+                                              _ptr(offsets), _ptr(slot_row), _ptr(row_slot),
+                                              _ptr(n_kept_dropped), _ptr(x_perm), wp, wn,
+                                              _ptr(dev_status), _stream(stream)))
+
+
+def moe_expert_ffn_workspace_size(p: Problem, rows_max: int) -> int:
+    return lib().moe_expert_ffn_workspace_size(p.c(), rows_max)
+
+
+def moe_expert_ffn(p, rows_max, x_perm, offsets, row_slot, topk_gate, w_gate, w_up, w_down,
+                   lora, h, y_perm, saved, workspace, dev_status=None, stream=None):
+    wp, wn = _ws(workspace)
+    _check("moe_expert_ffn",
+           lib().moe_expert_ffn(p.c(), rows_max, _ptr(x_perm), _ptr(offsets), _ptr(row_slot),
+                                _ptr(topk_gate), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                                _lora(lora), _ptr(h), _ptr(y_perm), _saved(saved), wp, wn,
+                                _ptr(dev_status), _stream(stream)))
+
+
+def moe_combine(p, y_perm, slot_row, y, stream=None):
+    _check("moe_combine", lib().moe_combine(p.c(), _ptr(y_perm), _ptr(slot_row), _ptr(y),
+                                            _stream(stream)))
+
+
+def moe_aux_loss(p, counts, prob_partials, n_partials, aux_out, stream=None):
+    _check("moe_aux_loss", lib().moe_aux_loss(p.c(), _ptr(counts), _ptr(prob_partials),
+                                              n_partials, _ptr(aux_out), _stream(stream)))
+
+
+def moe_combine_bwd(p, dy, y_perm, slot_row, topk_gate, dz_perm, dgate, stream=None):
+    _check("moe_combine_bwd", lib().moe_combine_bwd(p.c(), _ptr(dy), _ptr(y_perm), _ptr(slot_row),
+                                                    _ptr(topk_gate), _ptr(dz_perm), _ptr(dgate),
+                                                    _stream(stream)))
+
+
+def moe_expert_ffn_bwd_workspace_size(p: Problem, rows_max: int) -> int:
+    return lib().moe_expert_ffn_bwd_workspace_size(p.c(), rows_max)
+
+
+def moe_expert_ffn_bwd(p, rows_max, x_perm, offsets, w_gate, w_up, w_down, lora, saved, h,
+                       dz_perm, dx_perm, grads, workspace, dev_status=None, stream=None):
+    wp, wn = _ws(workspace)
+    _check("moe_expert_ffn_bwd",
+           lib().moe_expert_ffn_bwd(p.c(), rows_max, _ptr(x_perm), _ptr(offsets), _ptr(w_gate),
+                                    _ptr(w_up), _ptr(w_down), _lora(lora), _saved(saved), _ptr(h),
+                                    _ptr(dz_perm), _ptr(dx_perm), _grads(grads), wp, wn,
+                                    _ptr(dev_status), _stream(stream)))
+
+
+def moe_dispatch_bwd(p, dx_perm, slot_row, dx, stream=None):
+    _check("moe_dispatch_bwd", lib().moe_dispatch_bwd(p.c(), _ptr(dx_perm), _ptr(slot_row),
+                                                      _ptr(dx), _stream(stream)))
+
+
+def moe_route_bwd(p, topk_idx, topk_gate, dgate, w_router, dx, stream=None):
+    _check("moe_route_bwd", lib().moe_route_bwd(p.c(), _ptr(topk_idx), _ptr(topk_gate),
+                                                _ptr(dgate), _ptr(w_router), _ptr(dx),
+                                                _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- layer helpers
+
+def problem_of(cfg) -> Problem:
+    return Problem(cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.r, cfg.lora_scale, cfg.cap_num,
+                   cfg.cap_den)
+
+
+def _empty(shape, dtype, device):
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+def _bytes(n, device):
+    return torch.empty(max(int(n), 1), dtype=torch.uint8, device=device)
+
+
+class LayerBuffers:
+    """Every device buffer one forward (and, with ``train=True``, one backward) of the layer
+    uses, allocated once with torch and reused across calls."""
+
+    def __init__(self, p: Problem, device="cuda", train=False, keep_logits=True):
+        dev = torch.device(device)
+        T, d, E, k, F, r = p.T, p.d, p.E, p.k, p.F, p.r
+        N = T * k
+        self.p = p
+        self.rows_max = N
+        self.logits = _empty((T, E), torch.float32, dev) if keep_logits else None
+        self.topk_idx = _empty((T, k), torch.int32, dev)
+        self.topk_gate = _empty((T, k), torch.float32, dev)
+        self.n_partials = moe_route_num_partials(p)
+        self.partials = _empty((self.n_partials, E), torch.float32, dev)
+        self.counts = _empty((E,), torch.int32, dev)
+        self.offsets = _empty((E + 1,), torch.int32, dev)
+        self.slot_row = _empty((N,), torch.int32, dev)
+        self.row_slot = _empty((N,), torch.int32, dev)
+        self.n_kept_dropped = _empty((2,), torch.int32, dev)
+        self.x_perm = _empty((N, d), torch.bfloat16, dev)
+        self.h = _empty((N, F), torch.bfloat16, dev)
+        self.y_perm = _empty((N, d), torch.bfloat16, dev)
+        self.y = _empty((T, d), torch.bfloat16, dev)
+        self.aux = _empty((1,), torch.float32, dev)
+        self.dev_status = torch.zeros((1,), dtype=torch.int32, device=dev)
+        self.ws_route = _bytes(moe_route_workspace_size(p), dev)
+        self.ws_dispatch = _bytes(moe_dispatch_workspace_size(p), dev)
+        self.ws_ffn = _bytes(moe_expert_ffn_workspace_size(p, N), dev)
+        self.saved = None
+        if train:
+            self.saved = {"a_gate": _empty((N, F), torch.bfloat16, dev),
+                          "a_up": _empty((N, F), torch.bfloat16, dev)}
+            if r:
+                for n in ("u_gate", "u_up", "u_down"):
+                    self.saved[n] = _empty((N, r), torch.bfloat16, dev)
+
+
+def layer_forward(buf: LayerBuffers, x, w_router, bias, w_gate, w_up, w_down, lora=None,
+                  stream=None):
+    """route -> dispatch -> experts -> combine -> aux, all enqueued on one stream."""
+    p = buf.p
+    moe_route(p, x, w_router, bias, buf.topk_idx, buf.topk_gate, buf.partials, buf.logits,
+              buf.ws_route, buf.dev_status, stream)
+    moe_dispatch(p, buf.topk_idx, x, buf.counts, buf.offsets, buf.slot_row, buf.row_slot,
+                 buf.n_kept_dropped, buf.x_perm, buf.ws_dispatch, buf.dev_status, stream)
+    moe_expert_ffn(p, buf.rows_max, buf.x_perm, buf.offsets, buf.row_slot, buf.topk_gate,
+                   w_gate, w_up, w_down, lora, buf.h, buf.y_perm, buf.saved, buf.ws_ffn,
+                   buf.dev_status, stream)
+    moe_combine(p, buf.y_perm, buf.slot_row, buf.y, stream)
+    moe_aux_loss(p, buf.counts, buf.partials, buf.n_partials, buf.aux, stream)
+    return buf.y
