@@ -1,0 +1,433 @@
+#!/usr/bin/env python
+"""Throughput of the sparse-MoE layer (route -> dispatch -> grouped SwiGLU experts ->
+combine -> aux loss) on one GB300, through the C ABI of libmoe.so.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2] [--impl ours|reference]
+
+One step is one forward pass of the whole layer over one batch of the workload's seeded
+synthetic tokens, with every input already resident in HBM.  Rank 0 prints one JSON line.
+
+  value        tokens/s over all ranks (each rank runs its own batch: weak scaling, no
+               collective on the data path), CUDA events around K steps, max over ranks
+  e2e          the same through the public API with host buffers: pinned x copied in and
+               y (+aux) copied out inside the timed region, every step
+  roofline     the dominant kernel (grouped gate/up GEMM) timed live by CUDA events recorded
+               by the library around its launches, against MEASURED_PEAKS.json
+  cpu_baseline the fp64 oracle, single BLAS thread, on a bounded sample of the same batch
+  --impl reference  times the oracle alone (the slow reference program of this build)
+"""
+
+from __future__ import annotations
+
+import os
+
+# The oracle baseline runs numpy with one BLAS thread (set before numpy is imported).
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import argparse
+import hashlib
+import json
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s and grouped-GEMM TFLOP/s (% BF16 peak), 1×GB300"
+KERNELS = ["router_gemm", "topk", "dispatch", "gateup_gemm", "down_gemm", "combine"]
+KERNEL_SOURCES = ["gemm.cuh", "ptx.cuh", "gemm_fwd.cu", "capi.cu", "moe_internal.h"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="c2")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample", type=int, default=32, help="tokens in the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "top_routing_grouped_gemm_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the kernel
+    sources as they are now (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if "=" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_hash")):
+            k, v = line.strip().split("=", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in self.samples if num(s[1])]
+        mx = [num(s[2]) for s in self.samples if num(s[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for s in self.samples:
+            for n, v in zip(names, s[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------------ oracle baseline
+
+class HostExperts:
+    """[E, rows, cols] weight table of which only some experts are held on the host (as
+    float32, exact for bf16 values); the oracle converts each expert to fp64 on use."""
+
+    def __init__(self, E, rows, cols):
+        self.shape = (E, rows, cols)
+        self.store = {}
+
+    def __getitem__(self, e):
+        return self.store[int(e)]
+
+
+def oracle_sample_run(x_rows, w_router, tables, k, bias=None):
+    """Time the oracle's whole forward on a sample of tokens; returns seconds."""
+    import oracle
+    t0 = time.perf_counter()
+    out = oracle.moe_forward(x_rows, w_router, tables[0], tables[1], tables[2], k, bias=bias)
+    dt = time.perf_counter() - t0
+    return dt, out
+
+
+def cpu_baseline_from_device(inp, cfg, n_tok):
+    """Oracle on the first n_tok tokens of the device batch (weights of the experts those
+    tokens select copied to the host before timing)."""
+    import numpy as np
+    import oracle
+    x = inp["x"][:n_tok].float().cpu().double().numpy()
+    wr = inp["w_router"].cpu().double().numpy()
+    bias = None if inp.get("bias") is None else inp["bias"].cpu().double().numpy()
+    idx = oracle.topk_select(oracle.router_logits(x, wr, bias), cfg.k)
+    tabs = [HostExperts(cfg.E, cfg.F, cfg.d), HostExperts(cfg.E, cfg.F, cfg.d),
+            HostExperts(cfg.E, cfg.d, cfg.F)]
+    for e in np.unique(idx):
+        for tab, name in zip(tabs, ("w_gate", "w_up", "w_down")):
+            tab.store[int(e)] = inp[name][int(e)].float().cpu().numpy()
+    dt, _ = oracle_sample_run(x, wr, tabs, cfg.k, bias)
+    return {"value": n_tok / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n_tok} tokens of the {cfg.name} batch: fp64 router over all "
+                      f"{cfg.E} experts, top-{cfg.k}, {len(np.unique(idx))} experts' SwiGLU, "
+                      f"combine; numpy, 1 BLAS thread", "seconds": dt}
+
+
+def run_reference(args):
+    """The oracle as the reference program: each step a bounded sample of the workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    import oracle
+    from top_routing_grouped_gemm_gb300 import synth
+    torch.set_num_threads(1)
+    cfg = synth.config(args.workload)
+    per_step = max(1, args.cpu_sample // 16)
+    n_steps = args.steps + args.warmup
+    g = torch.Generator().manual_seed(0)
+    x_all = torch.randn((per_step * n_steps, cfg.d), generator=g).to(torch.bfloat16).double().numpy()
+    wr = (torch.randn((cfg.E, cfg.d), generator=g) * 0.02).double().numpy()
+    bias = synth.zipf_bias(cfg.E).double().numpy() if cfg.zipf_bias else None
+    idx = oracle.topk_select(oracle.router_logits(x_all, wr, bias), cfg.k)
+    tabs = [HostExperts(cfg.E, cfg.F, cfg.d), HostExperts(cfg.E, cfg.F, cfg.d),
+            HostExperts(cfg.E, cfg.d, cfg.F)]
+    for e in np.unique(idx):
+        ge = torch.Generator().manual_seed(1000 + int(e))
+        for tab, shape in zip(tabs, ((cfg.F, cfg.d), (cfg.F, cfg.d), (cfg.d, cfg.F))):
+            tab.store[int(e)] = (torch.randn(shape, generator=ge) * 0.02).to(torch.bfloat16).float().numpy()
+    times = []
+    for s in range(n_steps):
+        rows = x_all[s * per_step:(s + 1) * per_step]
+        dt, _ = oracle_sample_run(rows, wr, tabs, cfg.k, bias)
+        if s >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = per_step * len(times) / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * total / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(cfg),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} tokens per step of a {cfg.name}-shaped batch "
+                                   f"(fp64 oracle forward, numpy, 1 BLAS thread)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(cfg):
+    c = {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} top-{cfg.k} F={cfg.F}"
+                     + (f" LoRA r={cfg.r} alpha={cfg.alpha:g}" if cfg.r else "")
+                     + (f" capacity {cfg.cap_num}/{cfg.cap_den}" if cfg.cap_den else " capacity inf")
+                     + (" Zipf(1.1) router bias" if cfg.zipf_bias else ""),
+         "tokens_per_gpu": cfg.T, "experts": cfg.E, "top_k": cfg.k, "d_model": cfg.d,
+         "d_ffn": cfg.F, "lora_rank": cfg.r, "seed": 0,
+         "l2": "inputs larger than L2: the expert weights streamed every step exceed 129 MB"}
+    return c
+
+
+# ------------------------------------------------------------------------ GPU arm
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from top_routing_grouped_gemm_gb300 import moe, synth
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    cfg = synth.config(args.workload)
+    assert not cfg.prepermuted and not cfg.backward, "bench steps the routed forward workloads"
+    inp = synth.make_inputs(cfg, "cuda", seed=rank)
+    p = moe.problem_of(cfg)
+    buf = moe.LayerBuffers(p, "cuda", keep_logits=False)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.layer_forward(buf, inp["x"], inp["w_router"], inp["bias"], inp["w_gate"],
+                          inp["w_up"], inp["w_down"], inp.get("lora"))
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    status = int(buf.dev_status.item())
+    if status != 0:
+        raise RuntimeError(f"device status {moe.STATUS_NAMES.get(status, status)} after warm-up")
+
+    K = args.steps
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)] for n in KERNELS}
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    launches0 = moe.moe_launch_count()
+    start.record(stream)
+    for i in range(K):
+        for n in KERNELS:
+            moe.moe_set_kernel_events(n, ev[n][i][0], ev[n][i][1])
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    launches = moe.moe_launch_count() - launches0
+    for n in KERNELS:
+        moe.moe_set_kernel_events(n, None, None)
+    clocks.stop()
+    ms_step = max_over_ranks(start.elapsed_time(end) / K)
+    kern_us = {n: 1000.0 * sum(a.elapsed_time(b) for a, b in ev[n]) / K for n in KERNELS}
+
+    # routing statistics (identical every step: same inputs)
+    counts = buf.counts.cpu()
+    kept = int(buf.n_kept_dropped[0].item())
+    nonempty = int((buf.offsets[1:] - buf.offsets[:-1] > 0).sum().item())
+    d, F, E, T = cfg.d, cfg.F, cfg.E, cfg.T
+
+    # algorithmic bytes / flops per launch (units: non-empty experts, kept rows, tokens)
+    gateup_bytes = nonempty * 2 * F * d * 2 + kept * d * 2 + kept * F * 2
+    down_bytes = nonempty * d * F * 2 + kept * F * 2 + kept * d * 2
+    gateup_flops = kept * 4.0 * d * F
+    down_flops = kept * 2.0 * d * F
+    router_flops = 2.0 * T * d * E
+    dispatch_bytes = T * cfg.k * 4 * 3 + T * d * 2 + kept * d * 2
+    combine_bytes = kept * d * 2 + T * d * 2 + T * cfg.k * 4
+    pk = peaks()
+    hbm = pk["hbm_gbs"]
+
+    def gbs(b, us):
+        return b / (us * 1e-6) / 1e9
+
+    def tfs(f, us):
+        return f / (us * 1e-6) / 1e12
+
+    kernels = {
+        "router_gemm": {"us": kern_us["router_gemm"], "TFLOP/s": tfs(router_flops, kern_us["router_gemm"])},
+        "topk": {"us": kern_us["topk"], "GB/s": gbs(T * E * 4, kern_us["topk"])},
+        "dispatch": {"us": kern_us["dispatch"], "GB/s": gbs(dispatch_bytes, kern_us["dispatch"]),
+                     "frac_hbm": gbs(dispatch_bytes, kern_us["dispatch"]) / hbm},
+        "gateup_gemm": {"us": kern_us["gateup_gemm"], "GB/s": gbs(gateup_bytes, kern_us["gateup_gemm"]),
+                        "TFLOP/s": tfs(gateup_flops, kern_us["gateup_gemm"])},
+        "down_gemm": {"us": kern_us["down_gemm"], "GB/s": gbs(down_bytes, kern_us["down_gemm"]),
+                      "TFLOP/s": tfs(down_flops, kern_us["down_gemm"])},
+        "combine": {"us": kern_us["combine"], "GB/s": gbs(combine_bytes, kern_us["combine"]),
+                    "frac_hbm": gbs(combine_bytes, kern_us["combine"]) / hbm},
+    }
+    expert_us = kern_us["gateup_gemm"] + kern_us["down_gemm"]
+    gg_tflops = tfs(gateup_flops + down_flops, expert_us)
+    gg_bound_us = max((gateup_bytes + down_bytes) / (hbm * 1e9),
+                      (gateup_flops + down_flops) / (pk["bf16_tflops"] * 1e12)) * 1e6
+
+    # ---------------------------------------------------------------- end to end (host buffers)
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = torch.empty((T, d), dtype=torch.bfloat16).pin_memory()
+    aux_host = torch.empty((1,), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(inp["x"])
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.layer_forward(buf, x_dev, inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"],
+                          inp["w_down"], inp.get("lora"))
+        y_host.copy_(buf.y, non_blocking=True)
+        aux_host.copy_(buf.aux, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = max_over_ranks(s2.elapsed_time(e2) / K)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_from_device(inp, cfg, args.cpu_sample)
+
+    if rank == 0:
+        achieved = gbs(gateup_bytes, kern_us["gateup_gemm"])
+        line = {
+            "metric": METRIC,
+            "value": world * T / (ms_step * 1e-3),
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": ms_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": workload_config(cfg),
+            "grouped_gemm": {"TFLOP/s": gg_tflops, "pct_bf16_peak": 100.0 * gg_tflops / pk["bf16_tflops"],
+                             "us": expert_us, "roofline_us": gg_bound_us,
+                             "frac_of_roofline": gg_bound_us / expert_us,
+                             "flops": gateup_flops + down_flops, "kept_rows": kept,
+                             "nonempty_experts": nonempty},
+            "roofline": {"kernel": "gateup_gemm", "bound": "hbm", "achieved": achieved,
+                         "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": profiled_traffic("gateup_gemm", args.workload),
+                         "algorithmic_bytes": gateup_bytes, "peak_source": pk["source"]},
+            "kernels": kernels,
+            "e2e": {"value": world * T / (ms_e2e * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2 + 4},
+            "gpu_launches": launches,
+            "clocks": clocks.summary(),
+            "cpu_baseline": cpu,
+            "dropped_slots": int(buf.n_kept_dropped[1].item()),
+            "max_expert_count": int(counts.max().item()),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -226,6 +226,25 @@ int moe_dispatch_bwd(const moe_problem* p, const moe_bf16* dx_perm, const int32_
 int moe_route_bwd(const moe_problem* p, const int32_t* topk_idx, const float* topk_gate,
                   const float* dgate, const float* w_router, float* dx, moe_stream_t stream);
 
+/* ==================================================================== instrumentation
+ * Profiling aids, not part of the layer.  moe_set_kernel_events() makes the library record
+ * the caller's CUDA events (cudaEvent_t, passed as void*) on the launch stream immediately
+ * before and after its next launches of the given kernel, so that a caller can time one
+ * kernel inside a longer sequence; pass NULL events to stop.  moe_launch_count() returns
+ * the number of kernels this process has launched through the library.  Both use
+ * process-wide state and are not thread-safe. */
+enum moe_kernel_id {
+  MOE_KERNEL_ROUTER_GEMM = 0,   /* split-bf16 router product -> fp32 logits      */
+  MOE_KERNEL_TOPK = 1,          /* softmax, top-k, gates, probability partials  */
+  MOE_KERNEL_DISPATCH = 2,      /* the four dispatch kernels, count to gather    */
+  MOE_KERNEL_GATEUP_GEMM = 3,   /* grouped gate/up GEMM with SwiGLU (+LoRA)      */
+  MOE_KERNEL_DOWN_GEMM = 4,     /* grouped down GEMM with gate scaling (+LoRA)   */
+  MOE_KERNEL_COMBINE = 5,       /* weighted unpermute and sum                    */
+  MOE_KERNEL_COUNT = 6
+};
+int moe_set_kernel_events(int kernel_id, void* event_before, void* event_after);
+long long moe_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

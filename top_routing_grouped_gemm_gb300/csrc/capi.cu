@@ -4,6 +4,8 @@
 #include <cuda_bf16.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "moe_internal.h"
 #include "route.h"
 
@@ -74,6 +76,19 @@ size_t ffn_ws(const moe_problem* p, int rows_max) {
   return b;
 }
 
+// ---- instrumentation state (process-wide, see moe_set_kernel_events)
+cudaEvent_t g_ev_before[MOE_KERNEL_COUNT] = {nullptr};
+cudaEvent_t g_ev_after[MOE_KERNEL_COUNT] = {nullptr};
+std::atomic<long long> g_launches{0};
+
+inline void mark_before(int id, cudaStream_t s) {
+  if (g_ev_before[id]) cudaEventRecord(g_ev_before[id], s);
+}
+inline void mark_after(int id, cudaStream_t s) {
+  if (g_ev_after[id]) cudaEventRecord(g_ev_after[id], s);
+}
+inline void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
 GemmParams gemm_params() {
   GemmParams P;
   memset(&P, 0, sizeof(P));
@@ -115,8 +130,12 @@ int moe_route_from_logits(const moe_problem* p, const float* logits, int32_t* to
   (void)dev_status;
   MOE_TRY(check_problem(p));
   if (!logits || !topk_idx || !topk_gate || !prob_partials) return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_topk_softmax(logits, p->T, p->E, p->k, topk_idx, topk_gate,
-                                         prob_partials, stream));
+  mark_before(MOE_KERNEL_TOPK, stream);
+  MOE_CUDA(launch_topk_softmax(logits, p->T, p->E, p->k, topk_idx, topk_gate, prob_partials,
+                               stream));
+  mark_after(MOE_KERNEL_TOPK, stream);
+  count_launches(1);
+  return MOE_OK;
 }
 
 int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, const float* bias,
@@ -150,9 +169,14 @@ int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, co
   P.ldo = E;
   P.bias = bias;
   P.dev_status = dev_status;
+  mark_before(MOE_KERNEL_ROUTER_GEMM, stream);
   MOE_CUDA(launch_gemm_router(P, stream));
-  return cuda_status(launch_topk_softmax(L, T, E, p->k, topk_idx, topk_gate, prob_partials,
-                                         stream));
+  mark_after(MOE_KERNEL_ROUTER_GEMM, stream);
+  mark_before(MOE_KERNEL_TOPK, stream);
+  MOE_CUDA(launch_topk_softmax(L, T, E, p->k, topk_idx, topk_gate, prob_partials, stream));
+  mark_after(MOE_KERNEL_TOPK, stream);
+  count_launches(3);
+  return MOE_OK;
 }
 
 // ------------------------------------------------------------------------ dispatch
@@ -174,10 +198,14 @@ int moe_dispatch(const moe_problem* p, const int32_t* topk_idx, const moe_bf16* 
   Carver cv{static_cast<uint8_t*>(workspace), 0};
   int32_t* local_rank = cv.take<int32_t>(static_cast<size_t>(p->T) * p->k);
   int32_t* chunk_cnt = cv.take<int32_t>(static_cast<size_t>(dispatch_num_chunks(p->T)) * p->E);
-  return cuda_status(launch_dispatch(
-      topk_idx, reinterpret_cast<const __nv_bfloat16*>(x), p->T, p->d, p->E, p->k,
-      capacity_of(p), counts, offsets, slot_row, row_slot, n_kept_dropped,
-      reinterpret_cast<__nv_bfloat16*>(x_perm), local_rank, chunk_cnt, dev_status, stream));
+  mark_before(MOE_KERNEL_DISPATCH, stream);
+  MOE_CUDA(launch_dispatch(topk_idx, reinterpret_cast<const __nv_bfloat16*>(x), p->T, p->d,
+                           p->E, p->k, capacity_of(p), counts, offsets, slot_row, row_slot,
+                           n_kept_dropped, reinterpret_cast<__nv_bfloat16*>(x_perm), local_rank,
+                           chunk_cnt, dev_status, stream));
+  mark_after(MOE_KERNEL_DISPATCH, stream);
+  count_launches(4);
+  return MOE_OK;
 }
 
 // ------------------------------------------------------------------------ experts
@@ -282,7 +310,9 @@ int moe_expert_ffn(const moe_problem* p, int32_t rows_max, const moe_bf16* x_per
     P.out1 = saved ? saved->a_gate : nullptr;
     P.out2 = saved ? saved->a_up : nullptr;
     P.ldo = F;
+    mark_before(MOE_KERNEL_GATEUP_GEMM, stream);
     MOE_CUDA(launch_gemm_gateup(P, stream));
+    mark_after(MOE_KERNEL_GATEUP_GEMM, stream);
   }
   // LoRA down-projection of h: u_d = s h A_d^T
   if (use_lora) {
@@ -322,8 +352,11 @@ int moe_expert_ffn(const moe_problem* p, int32_t rows_max, const moe_bf16* x_per
     P.ldo = d;
     P.gate = topk_gate;
     P.row_slot = row_slot;
+    mark_before(MOE_KERNEL_DOWN_GEMM, stream);
     MOE_CUDA(launch_gemm_down(P, stream));
+    mark_after(MOE_KERNEL_DOWN_GEMM, stream);
   }
+  count_launches(use_lora ? 5 : 3);
   return MOE_OK;
 }
 
@@ -334,17 +367,21 @@ int moe_combine(const moe_problem* p, const moe_bf16* y_perm, const int32_t* slo
   MOE_TRY(check_problem(p));
   if (!y_perm || !slot_row || !y) return MOE_ERR_INVALID_ARG;
   if (!al16(y_perm) || !al16(y)) return MOE_ERR_UNSUPPORTED;
-  return cuda_status(launch_combine(reinterpret_cast<const __nv_bfloat16*>(y_perm), slot_row,
-                                    p->T, p->d, p->k, reinterpret_cast<__nv_bfloat16*>(y),
-                                    stream));
+  mark_before(MOE_KERNEL_COMBINE, stream);
+  MOE_CUDA(launch_combine(reinterpret_cast<const __nv_bfloat16*>(y_perm), slot_row, p->T, p->d,
+                          p->k, reinterpret_cast<__nv_bfloat16*>(y), stream));
+  mark_after(MOE_KERNEL_COMBINE, stream);
+  count_launches(1);
+  return MOE_OK;
 }
 
 int moe_aux_loss(const moe_problem* p, const int32_t* counts, const float* prob_partials,
                  int32_t n_partials, float* aux_out, moe_stream_t stream) {
   MOE_TRY(check_problem(p));
   if (!counts || !prob_partials || !aux_out || n_partials <= 0) return MOE_ERR_INVALID_ARG;
-  return cuda_status(
-      launch_aux_loss(counts, prob_partials, n_partials, p->T, p->k, p->E, aux_out, stream));
+  MOE_CUDA(launch_aux_loss(counts, prob_partials, n_partials, p->T, p->k, p->E, aux_out, stream));
+  count_launches(1);
+  return MOE_OK;
 }
 
 // ------------------------------------------------------------------------ backward
@@ -355,6 +392,7 @@ int moe_combine_bwd(const moe_problem* p, const moe_bf16* dy, const moe_bf16* y_
   MOE_TRY(check_problem(p));
   if (!dy || !y_perm || !slot_row || !topk_gate || !dz_perm || !dgate) return MOE_ERR_INVALID_ARG;
   if (!al16(dy) || !al16(y_perm) || !al16(dz_perm)) return MOE_ERR_UNSUPPORTED;
+  count_launches(1);
   return cuda_status(launch_combine_bwd(
       reinterpret_cast<const __nv_bfloat16*>(dy), reinterpret_cast<const __nv_bfloat16*>(y_perm),
       slot_row, topk_gate, p->T, p->d, p->k, reinterpret_cast<__nv_bfloat16*>(dz_perm), dgate,
@@ -384,6 +422,7 @@ int moe_dispatch_bwd(const moe_problem* p, const moe_bf16* dx_perm, const int32_
   MOE_TRY(check_problem(p));
   if (!dx_perm || !slot_row || !dx) return MOE_ERR_INVALID_ARG;
   if (!al16(dx_perm) || !al16(dx)) return MOE_ERR_UNSUPPORTED;
+  count_launches(1);
   return cuda_status(launch_dispatch_bwd(reinterpret_cast<const __nv_bfloat16*>(dx_perm),
                                          slot_row, p->T, p->d, p->k, dx, stream));
 }
@@ -393,8 +432,20 @@ int moe_route_bwd(const moe_problem* p, const int32_t* topk_idx, const float* to
   MOE_TRY(check_problem(p));
   if (!topk_idx || !topk_gate || !dgate || !w_router || !dx) return MOE_ERR_INVALID_ARG;
   if (!al16(w_router) || !al16(dx)) return MOE_ERR_UNSUPPORTED;
+  count_launches(1);
   return cuda_status(launch_route_bwd(topk_idx, topk_gate, dgate, w_router, p->T, p->d, p->E,
                                       p->k, dx, stream));
 }
+
+// ------------------------------------------------------------------------ instrumentation
+
+int moe_set_kernel_events(int kernel_id, void* event_before, void* event_after) {
+  if (kernel_id < 0 || kernel_id >= MOE_KERNEL_COUNT) return MOE_ERR_INVALID_ARG;
+  g_ev_before[kernel_id] = static_cast<cudaEvent_t>(event_before);
+  g_ev_after[kernel_id] = static_cast<cudaEvent_t>(event_after);
+  return MOE_OK;
+}
+
+long long moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

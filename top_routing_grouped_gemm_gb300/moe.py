@@ -79,7 +79,12 @@ _SIGS = {
                                           c_vp, c_sz, c_vp, c_vp]),
     "moe_dispatch_bwd": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp]),
     "moe_route_bwd": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "moe_set_kernel_events": (ctypes.c_int, [ctypes.c_int, c_vp, c_vp]),
+    "moe_launch_count": (ctypes.c_longlong, []),
 }
+
+KERNEL_IDS = {"router_gemm": 0, "topk": 1, "dispatch": 2, "gateup_gemm": 3, "down_gemm": 4,
+              "combine": 5}
 
 _lib = None
 
@@ -263,6 +268,19 @@ def moe_route_bwd(p, topk_idx, topk_gate, dgate, w_router, dx, stream=None):
     _check("moe_route_bwd", lib().moe_route_bwd(p.c(), _ptr(topk_idx), _ptr(topk_gate),
                                                 _ptr(dgate), _ptr(w_router), _ptr(dx),
                                                 _stream(stream)))
+
+
+def moe_set_kernel_events(kernel, before, after):
+    """Record torch.cuda.Event ``before``/``after`` around the next launches of ``kernel``
+    (a name of KERNEL_IDS); ``None`` stops recording."""
+    kid = KERNEL_IDS[kernel] if isinstance(kernel, str) else int(kernel)
+    hb = before.cuda_event if before is not None else None
+    ha = after.cuda_event if after is not None else None
+    _check("moe_set_kernel_events", lib().moe_set_kernel_events(kid, hb, ha))
+
+
+def moe_launch_count() -> int:
+    return lib().moe_launch_count()
 
 
 # ----------------------------------------------------------------------------- layer helpers
