@@ -39,7 +39,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer tokens/s and grouped-GEMM TFLOP/s (% BF16 peak), 1×GB300"
 KERNELS = ["router_gemm", "topk", "dispatch", "gateup_gemm", "down_gemm", "combine"]
-KERNEL_SOURCES = ["gemm.cuh", "ptx.cuh", "gemm_fwd.cu", "capi.cu", "moe_internal.h"]
+KERNEL_SOURCES = ["gemm.cuh", "ptx.cuh", "gemm_fwd.cu", "moe_internal.h"]
 
 
 def parse():
@@ -299,6 +299,12 @@ def main():
     K = args.steps
     ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(K)] for n in KERNELS}
+    # torch creates the CUDA event behind an Event on its first record: record each once so
+    # that the raw handles handed to the library are live
+    for n in KERNELS:
+        for a, b in ev[n]:
+            a.record(stream)
+            b.record(stream)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     time.sleep(0.3)

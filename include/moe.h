@@ -184,9 +184,12 @@ int moe_combine(const moe_problem* p, const moe_bf16* y_perm, const int32_t* slo
 
 /* Auxiliary load-balancing loss ("Day-Level Adaptation ...", section 2.1):
  *   aux = E * sum_e f_e P_e,  f_e = counts[e] / (T k) (before drops),
- *   P_e = (1/T) sum_b prob_partials[b, e].   aux_out: one fp32 in device memory. */
+ *   P_e = (1/T) sum_b prob_partials[b, e].   aux_out: one fp32 in device memory.
+ * The reduction runs in a fixed order (deterministic). */
+size_t moe_aux_loss_workspace_size(const moe_problem* p);
 int moe_aux_loss(const moe_problem* p, const int32_t* counts, const float* prob_partials,
-                 int32_t n_partials, float* aux_out, moe_stream_t stream);
+                 int32_t n_partials, float* aux_out, void* workspace, size_t workspace_bytes,
+                 moe_stream_t stream);
 
 /* ==================================================================== backward
  * Gradient of <dy, y> with the routing decisions of the forward held fixed ("Day-Level

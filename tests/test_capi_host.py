@@ -94,4 +94,4 @@ def test_workspace_sizes_grow_with_problem():
     a = moe.moe_expert_ffn_workspace_size(moe.Problem(64, 128, 16, 4, 128), 256)
     b = moe.moe_expert_ffn_workspace_size(moe.Problem(64, 128, 16, 4, 128, r=16), 256)
     assert b > a > 0
-    assert moe.moe_route_num_partials(moe.Problem(4096, 2048, 896, 16, 512)) == 64
+    assert moe.moe_route_num_partials(moe.Problem(4096, 2048, 896, 16, 512)) == 4096 // 8

@@ -95,11 +95,30 @@ def test_forward_is_deterministic():
         assert torch.equal(getattr(a, name), getattr(b, name)), name
 
 
-def test_route_from_logits_ties_and_zero():
-    T, E, k = 200, 40, 6
+def _route_logits_case(case, T, E):
     g = torch.Generator().manual_seed(3)
-    L = torch.randint(0, 4, (T, E), generator=g).float()
-    L[:10] = 0.0
+    if case == "ties":
+        L = torch.randint(0, 4, (T, E), generator=g).float()
+        L[:10] = 0.0
+    elif case == "one_lane":
+        # every large logit sits on experts = 5 (mod 32): one lane owns the whole top-k
+        L = torch.randn((T, E), generator=g)
+        L[:, 5::32] += 100.0
+    elif case == "neg_zero":
+        L = torch.zeros((T, E))
+        L[:, ::2] = -0.0
+        L[:, 7] = 1e-30
+    else:
+        L = torch.randn((T, E), generator=g) * 3
+    return L
+
+
+@pytest.mark.parametrize("case, E, k", [("ties", 40, 6), ("ties", 896, 16), ("one_lane", 896, 16),
+                                        ("neg_zero", 896, 32), ("normal", 1024, 32),
+                                        ("normal", 33, 32)])
+def test_route_from_logits_exact_selection(case, E, k):
+    T = 200
+    L = _route_logits_case(case, T, E)
     p = moe.Problem(T, 64, E, k, 64)
     idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
     gate = torch.empty((T, k), dtype=torch.float32, device="cuda")
@@ -109,9 +128,12 @@ def test_route_from_logits_ties_and_zero():
     L64 = L.double().numpy()
     ref = oracle.topk_select(L64, k)
     assert np.array_equal(idx.cpu().numpy(), ref)
-    assert (idx[:10].cpu().numpy() == np.arange(k)).all()
-    gref = oracle.renormalised_gates(oracle.softmax(L64), ref)
-    assert relerr(f64(gate), gref) <= 1e-6
+    if case == "ties":
+        assert (idx[:10].cpu().numpy() == np.arange(k)).all()
+    prob = oracle.softmax(L64)
+    gref = oracle.renormalised_gates(prob, ref)
+    assert relerr(f64(gate), gref) <= 1e-5
+    assert relerr(f64(part).sum(axis=0), prob.sum(axis=0)) <= 1e-5
 
 
 def test_bad_expert_id_is_reported_not_faulted():

@@ -375,12 +375,19 @@ int moe_combine(const moe_problem* p, const moe_bf16* y_perm, const int32_t* slo
   return MOE_OK;
 }
 
+size_t moe_aux_loss_workspace_size(const moe_problem* p) {
+  return check_problem(p) == MOE_OK ? up256(((p->E + 31) / 32) * sizeof(float)) : 0;
+}
+
 int moe_aux_loss(const moe_problem* p, const int32_t* counts, const float* prob_partials,
-                 int32_t n_partials, float* aux_out, moe_stream_t stream) {
+                 int32_t n_partials, float* aux_out, void* workspace, size_t workspace_bytes,
+                 moe_stream_t stream) {
   MOE_TRY(check_problem(p));
   if (!counts || !prob_partials || !aux_out || n_partials <= 0) return MOE_ERR_INVALID_ARG;
-  MOE_CUDA(launch_aux_loss(counts, prob_partials, n_partials, p->T, p->k, p->E, aux_out, stream));
-  count_launches(1);
+  if (!workspace || workspace_bytes < moe_aux_loss_workspace_size(p)) return MOE_ERR_WORKSPACE;
+  MOE_CUDA(launch_aux_loss(counts, prob_partials, n_partials, p->T, p->k, p->E, aux_out,
+                           static_cast<float*>(workspace), stream));
+  count_launches(2);
   return MOE_OK;
 }
 

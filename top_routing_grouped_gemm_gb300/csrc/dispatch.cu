@@ -46,31 +46,39 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* sm, int* to
 }
 
 // Pass 1: each warp counts one chunk of kDispatchChunk tokens, in (token, rank) order, and
-// records every slot's rank among the chunk's slots routed to the same expert.
-__global__ void __launch_bounds__(128) dispatch_count_kernel(
+// records every slot's rank among the chunk's slots routed to the same expert.  The chunk's
+// expert ids are loaded up front (lane j holds rank j of every token of the chunk).
+constexpr int kCountWarps = 8;
+__global__ void __launch_bounds__(256) dispatch_count_kernel(
     const int32_t* __restrict__ idx, int T, int E, int k, int32_t* __restrict__ local_rank,
     int32_t* __restrict__ chunk_cnt, int32_t* dev_status) {
   extern __shared__ int cnt_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.x * 4 + warp;
+  const int c = blockIdx.x * kCountWarps + warp;
   const int nch = dispatch_num_chunks(T);
   if (c >= nch) return;
   int* cnt = cnt_smem + warp * E;
   for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  const int t0 = c * kDispatchChunk;
+  int ev[kDispatchChunk];
+#pragma unroll
+  for (int i = 0; i < kDispatchChunk; ++i) {
+    const int t = t0 + i;
+    ev[i] = (lane < k && t < T) ? idx[static_cast<size_t>(t) * k + lane] : -1;
+  }
   __syncwarp();
-  const int t_end = min((c + 1) * kDispatchChunk, T);
-  for (int t = c * kDispatchChunk; t < t_end; ++t) {
+#pragma unroll
+  for (int i = 0; i < kDispatchChunk; ++i) {
+    const int t = t0 + i;
+    if (t >= T) break;
     const bool act = lane < k;
-    int e = -1;
-    if (act) {
-      e = idx[static_cast<size_t>(t) * k + lane];
-      if (e < 0 || e >= E) {
-        report_status(dev_status, MOE_ERR_BAD_INDEX);
-        e = -1;
-      }
+    int e = ev[i];
+    if (act && (e < 0 || e >= E)) {
+      report_status(dev_status, MOE_ERR_BAD_INDEX);
+      e = -1;
     }
-    const unsigned live = __ballot_sync(0xffffffffu, e >= 0);
-    if (e >= 0) {
+    const unsigned live = __ballot_sync(0xffffffffu, act && e >= 0);
+    if (act && e >= 0) {
       // a token may repeat an expert only in caller-made input; ranks then follow j order
       const unsigned grp = __match_any_sync(live, e);
       const int before = __popc(grp & ((1u << lane) - 1u));
@@ -139,44 +147,49 @@ __global__ void __launch_bounds__(1024) dispatch_offsets_kernel(
   }
 }
 
-// Pass 4: final rows, both index maps, and the gather x -> x_perm.  One warp per token:
-// x[t] is read once and written to each of its kept rows with 16-byte vector accesses.
-__global__ void __launch_bounds__(256) dispatch_scatter_kernel(
+// Pass 4: final rows, both index maps, and the gather x -> x_perm.  One block per token:
+// warp 0 resolves the k rows, then every thread moves 16-byte vectors of x[t], read once
+// and written to each kept row.
+constexpr int kRowThreads = 128;
+__global__ void __launch_bounds__(kRowThreads) dispatch_scatter_kernel(
     const int32_t* __restrict__ idx, const int32_t* __restrict__ local_rank,
     const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
     const int32_t* __restrict__ n_kept_dropped, const uint4* __restrict__ x, int T, int d,
     int E, int k, int capacity, int32_t* __restrict__ slot_row, int32_t* __restrict__ row_slot,
     uint4* __restrict__ x_perm) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
+  __shared__ int rows[32];
+  const int t = blockIdx.x;
   const int slots = T * k;
-  // rows past n_kept are marked unused (disjoint from the rows written below)
   {
+    // rows past n_kept are marked unused (disjoint from the rows written below)
     const int n_kept = n_kept_dropped[0];
     for (int r = n_kept + blockIdx.x * blockDim.x + threadIdx.x; r < slots;
          r += gridDim.x * blockDim.x)
       row_slot[r] = -1;
   }
-  if (t >= T) return;
-  int row = -1;
-  if (lane < k) {
-    const int slot = t * k + lane;
-    const int e = idx[slot];
-    const int lr = local_rank[slot];
-    if (e >= 0 && e < E && lr >= 0) {
-      const int pos = chunk_base[static_cast<size_t>(t / kDispatchChunk) * E + e] + lr;
-      if (capacity < 0 || pos < capacity) row = offsets[e] + pos;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int row = -1;
+    if (lane < k) {
+      const int slot = t * k + lane;
+      const int e = idx[slot];
+      const int lr = local_rank[slot];
+      if (e >= 0 && e < E && lr >= 0) {
+        const int pos = chunk_base[static_cast<size_t>(t / kDispatchChunk) * E + e] + lr;
+        if (capacity < 0 || pos < capacity) row = offsets[e] + pos;
+      }
+      slot_row[slot] = row;
+      if (row >= 0) row_slot[row] = slot;
     }
-    slot_row[slot] = row;
-    if (row >= 0) row_slot[row] = slot;
+    rows[lane] = row;
   }
+  __syncthreads();
   const int nvec = d / 8;
   const uint4* src = x + static_cast<size_t>(t) * nvec;
-#pragma unroll 2
-  for (int v = lane; v < nvec; v += 32) {
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
     const uint4 val = src[v];
     for (int j = 0; j < k; ++j) {
-      const int r = __shfl_sync(0xffffffffu, row, j);
+      const int r = rows[j];
       if (r >= 0) x_perm[static_cast<size_t>(r) * nvec + v] = val;
     }
   }
@@ -222,21 +235,22 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&a)[8]) {
   return o;
 }
 
-// y[t] = sum_j y_perm[slot_row[t*k+j]] (kept slots, rank order, fp32) -> bf16.
-__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y_perm,
-                                                      const int32_t* __restrict__ slot_row,
-                                                      int T, int d, int k,
-                                                      uint4* __restrict__ y) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  const int row = lane < k ? slot_row[static_cast<size_t>(t) * k + lane] : -1;
+// y[t] = sum_j y_perm[slot_row[t*k+j]] (kept slots, rank order, fp32) -> bf16.  One block
+// per token, one 16-byte vector per thread: the k row loads are independent.
+__global__ void __launch_bounds__(kRowThreads) combine_kernel(const uint4* __restrict__ y_perm,
+                                                              const int32_t* __restrict__ slot_row,
+                                                              int T, int d, int k,
+                                                              uint4* __restrict__ y) {
+  __shared__ int rows[32];
+  const int t = blockIdx.x;
+  if (threadIdx.x < 32) rows[threadIdx.x] = threadIdx.x < k ? slot_row[static_cast<size_t>(t) * k + threadIdx.x] : -1;
+  __syncthreads();
   const int nvec = d / 8;
-  for (int v = lane; v < nvec; v += 32) {
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
+#pragma unroll 8
     for (int j = 0; j < k; ++j) {
-      const int r = __shfl_sync(0xffffffffu, row, j);
+      const int r = rows[j];
       if (r >= 0) add_bf16x8(acc, y_perm[static_cast<size_t>(r) * nvec + v], 1.f);
     }
     y[static_cast<size_t>(t) * nvec + v] = pack_bf16x8(acc);
@@ -249,58 +263,55 @@ __device__ __forceinline__ float warp_sum_f(float v) {
   return v;
 }
 
-// dz_perm[row] = g * dy[t];  dgate[slot] = <dy[t], y_perm[row]> / g  (kept slots), else 0.
+// One warp per slot:  dz_perm[row] = g * dy[t];  dgate[slot] = <dy[t], y_perm[row]> / g
+// (kept slots; y_perm = g * o, so this is <dy, o> up to the bf16 rounding of y_perm), else 0.
 __global__ void __launch_bounds__(256) combine_bwd_kernel(
     const uint4* __restrict__ dy, const uint4* __restrict__ y_perm,
     const int32_t* __restrict__ slot_row, const float* __restrict__ gate, int T, int d, int k,
     uint4* __restrict__ dz_perm, float* __restrict__ dgate) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
+  const int lane = threadIdx.x & 31;
+  const size_t slot = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (slot >= static_cast<size_t>(T) * k) return;
+  const int r = slot_row[slot];
+  if (r < 0) {
+    if (lane == 0) dgate[slot] = 0.f;
+    return;
+  }
+  const int t = static_cast<int>(slot / k);
   const int nvec = d / 8;
   const uint4* dyr = dy + static_cast<size_t>(t) * nvec;
-  for (int j = 0; j < k; ++j) {
-    const size_t slot = static_cast<size_t>(t) * k + j;
-    const int r = slot_row[slot];
-    if (r < 0) {
-      if (lane == 0) dgate[slot] = 0.f;
-      continue;
-    }
-    const float g = gate[slot];
-    float dot = 0.f;
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 a = dyr[v];
-      float fa[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      float fb[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      add_bf16x8(fa, a, 1.f);
-      add_bf16x8(fb, y_perm[static_cast<size_t>(r) * nvec + v], 1.f);
+  const float g = gate[slot];
+  float dot = 0.f;
+  for (int v = lane; v < nvec; v += 32) {
+    float fa[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float fb[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    add_bf16x8(fa, dyr[v], 1.f);
+    add_bf16x8(fb, y_perm[static_cast<size_t>(r) * nvec + v], 1.f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        dot += fa[i] * fb[i];
-        fa[i] *= g;
-      }
-      dz_perm[static_cast<size_t>(r) * nvec + v] = pack_bf16x8(fa);
+    for (int i = 0; i < 8; ++i) {
+      dot += fa[i] * fb[i];
+      fa[i] *= g;
     }
-    dot = warp_sum_f(dot);
-    if (lane == 0) dgate[slot] = g > 0.f ? dot / g : 0.f;
+    dz_perm[static_cast<size_t>(r) * nvec + v] = pack_bf16x8(fa);
   }
+  dot = warp_sum_f(dot);
+  if (lane == 0) dgate[slot] = g > 0.f ? dot / g : 0.f;
 }
 
-// dx[t] = sum over kept slots of dx_perm rows (fp32, overwritten).
-__global__ void __launch_bounds__(256) dispatch_bwd_kernel(const uint4* __restrict__ dx_perm,
-                                                           const int32_t* __restrict__ slot_row,
-                                                           int T, int d, int k,
-                                                           float4* __restrict__ dx) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  const int row = lane < k ? slot_row[static_cast<size_t>(t) * k + lane] : -1;
+// dx[t] = sum over kept slots of dx_perm rows (fp32, overwritten).  One block per token.
+__global__ void __launch_bounds__(kRowThreads) dispatch_bwd_kernel(
+    const uint4* __restrict__ dx_perm, const int32_t* __restrict__ slot_row, int T, int d, int k,
+    float4* __restrict__ dx) {
+  __shared__ int rows[32];
+  const int t = blockIdx.x;
+  if (threadIdx.x < 32) rows[threadIdx.x] = threadIdx.x < k ? slot_row[static_cast<size_t>(t) * k + threadIdx.x] : -1;
+  __syncthreads();
   const int nvec = d / 8;
-  for (int v = lane; v < nvec; v += 32) {
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
+#pragma unroll 8
     for (int j = 0; j < k; ++j) {
-      const int r = __shfl_sync(0xffffffffu, row, j);
+      const int r = rows[j];
       if (r >= 0) add_bf16x8(acc, dx_perm[static_cast<size_t>(r) * nvec + v], 1.f);
     }
     float4* o = dx + (static_cast<size_t>(t) * nvec + v) * 2;
@@ -309,32 +320,37 @@ __global__ void __launch_bounds__(256) dispatch_bwd_kernel(const uint4* __restri
   }
 }
 
-// dx[t] += sum_j c_j W_r[e_j],  c_j = g_j (dg_j - sum_i g_i dg_i).
-__global__ void __launch_bounds__(256) route_bwd_kernel(
+// dx[t] += sum_j c_j W_r[e_j],  c_j = g_j (dg_j - sum_i g_i dg_i).  One block per token.
+__global__ void __launch_bounds__(kRowThreads) route_bwd_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ gate,
     const float* __restrict__ dgate, const float4* __restrict__ w_router, int T, int d, int E,
     int k, float4* __restrict__ dx) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  float g = 0.f, dg = 0.f;
-  int e = 0;
-  if (lane < k) {
-    const size_t slot = static_cast<size_t>(t) * k + lane;
-    g = gate[slot];
-    dg = dgate[slot];
-    e = idx[slot];
-    if (e < 0 || e >= E) { e = 0; g = 0.f; }
+  __shared__ float cs[32];
+  __shared__ int es[32];
+  const int t = blockIdx.x;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float g = 0.f, dg = 0.f;
+    int e = 0;
+    if (lane < k) {
+      const size_t slot = static_cast<size_t>(t) * k + lane;
+      g = gate[slot];
+      dg = dgate[slot];
+      e = idx[slot];
+      if (e < 0 || e >= E) { e = 0; g = 0.f; }
+    }
+    const float sgd = warp_sum_f(g * dg);
+    cs[lane] = g * (dg - sgd);
+    es[lane] = e;
   }
-  const float sgd = warp_sum_f(g * dg);
-  const float c = g * (dg - sgd);
+  __syncthreads();
   const int n4 = d / 4;
-  for (int v = lane; v < n4; v += 32) {
+  for (int v = threadIdx.x; v < n4; v += blockDim.x) {
     float4 acc = dx[static_cast<size_t>(t) * n4 + v];
+#pragma unroll 8
     for (int j = 0; j < k; ++j) {
-      const float cj = __shfl_sync(0xffffffffu, c, j);
-      const int ej = __shfl_sync(0xffffffffu, e, j);
-      const float4 w = __ldg(&w_router[static_cast<size_t>(ej) * n4 + v]);
+      const float cj = cs[j];
+      const float4 w = __ldg(&w_router[static_cast<size_t>(es[j]) * n4 + v]);
       acc.x += cj * w.x;
       acc.y += cj * w.y;
       acc.z += cj * w.z;
@@ -344,7 +360,7 @@ __global__ void __launch_bounds__(256) route_bwd_kernel(
   }
 }
 
-int grid_for_tokens(int T) { return (T + 7) / 8; }
+int grid_for_slots(long long slots) { return static_cast<int>((slots + 7) / 8); }
 
 }  // namespace
 
@@ -354,12 +370,13 @@ int launch_dispatch(const int32_t* idx, const __nv_bfloat16* x, int T, int d, in
                     int32_t* local_rank, int32_t* chunk_cnt, int32_t* dev_status,
                     cudaStream_t s) {
   const int nch = dispatch_num_chunks(T);
-  dispatch_count_kernel<<<(nch + 3) / 4, 128, 4 * E * sizeof(int), s>>>(idx, T, E, k, local_rank,
-                                                                        chunk_cnt, dev_status);
+  dispatch_count_kernel<<<(nch + kCountWarps - 1) / kCountWarps, 32 * kCountWarps,
+                          kCountWarps * E * sizeof(int), s>>>(idx, T, E, k, local_rank, chunk_cnt,
+                                                              dev_status);
   dispatch_scan_chunks_kernel<<<(E + 31) / 32, 1024, 0, s>>>(chunk_cnt, nch, E, counts);
   dispatch_offsets_kernel<<<1, 1024, 0, s>>>(counts, E, capacity, T * k, offsets,
                                              n_kept_dropped);
-  dispatch_scatter_kernel<<<grid_for_tokens(T), 256, 0, s>>>(
+  dispatch_scatter_kernel<<<T, kRowThreads, 0, s>>>(
       idx, local_rank, chunk_cnt, offsets, n_kept_dropped, reinterpret_cast<const uint4*>(x),
       T, d, E, k, capacity, slot_row, row_slot, reinterpret_cast<uint4*>(x_perm));
   return static_cast<int>(cudaGetLastError());
@@ -373,7 +390,7 @@ int launch_tile_schedule(const int32_t* offsets, int E, int rows_max, int32_t* t
 
 int launch_combine(const __nv_bfloat16* y_perm, const int32_t* slot_row, int T, int d, int k,
                    __nv_bfloat16* y, cudaStream_t s) {
-  combine_kernel<<<grid_for_tokens(T), 256, 0, s>>>(reinterpret_cast<const uint4*>(y_perm),
+  combine_kernel<<<T, kRowThreads, 0, s>>>(reinterpret_cast<const uint4*>(y_perm),
                                                     slot_row, T, d, k,
                                                     reinterpret_cast<uint4*>(y));
   return static_cast<int>(cudaGetLastError());
@@ -382,7 +399,7 @@ int launch_combine(const __nv_bfloat16* y_perm, const int32_t* slot_row, int T, 
 int launch_combine_bwd(const __nv_bfloat16* dy, const __nv_bfloat16* y_perm,
                        const int32_t* slot_row, const float* gate, int T, int d, int k,
                        __nv_bfloat16* dz_perm, float* dgate, cudaStream_t s) {
-  combine_bwd_kernel<<<grid_for_tokens(T), 256, 0, s>>>(
+  combine_bwd_kernel<<<grid_for_slots(static_cast<long long>(T) * k), 256, 0, s>>>(
       reinterpret_cast<const uint4*>(dy), reinterpret_cast<const uint4*>(y_perm), slot_row,
       gate, T, d, k, reinterpret_cast<uint4*>(dz_perm), dgate);
   return static_cast<int>(cudaGetLastError());
@@ -390,7 +407,7 @@ int launch_combine_bwd(const __nv_bfloat16* dy, const __nv_bfloat16* y_perm,
 
 int launch_dispatch_bwd(const __nv_bfloat16* dx_perm, const int32_t* slot_row, int T, int d,
                         int k, float* dx, cudaStream_t s) {
-  dispatch_bwd_kernel<<<grid_for_tokens(T), 256, 0, s>>>(
+  dispatch_bwd_kernel<<<T, kRowThreads, 0, s>>>(
       reinterpret_cast<const uint4*>(dx_perm), slot_row, T, d, k, reinterpret_cast<float4*>(dx));
   return static_cast<int>(cudaGetLastError());
 }
@@ -398,7 +415,7 @@ int launch_dispatch_bwd(const __nv_bfloat16* dx_perm, const int32_t* slot_row, i
 int launch_route_bwd(const int32_t* idx, const float* gate, const float* dgate,
                      const float* w_router, int T, int d, int E, int k, float* dx,
                      cudaStream_t s) {
-  route_bwd_kernel<<<grid_for_tokens(T), 256, 0, s>>>(
+  route_bwd_kernel<<<T, kRowThreads, 0, s>>>(
       idx, gate, dgate, reinterpret_cast<const float4*>(w_router), T, d, E, k,
       reinterpret_cast<float4*>(dx));
   return static_cast<int>(cudaGetLastError());

@@ -49,7 +49,9 @@ __global__ void split_router_kernel(const float4* __restrict__ w, uint2* __restr
   }
 }
 
-// One warp per token; lane i holds experts lane, lane+32, ... (VPL of them).
+// One warp per token; lane i holds the logits of experts lane, lane+32, ... (VPL of them).
+// Each warp accumulates the softmax probabilities of its tokens into its own shared-memory
+// row; the block then writes one row of per-block sums (fixed order: deterministic).
 template <int VPL>
 __global__ void __launch_bounds__(256) topk_softmax_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
@@ -58,11 +60,10 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(
   __shared__ float red[WARPS][VPL * 32];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) red[warp][lane + 32 * i] = 0.f;
   const int t_begin = blockIdx.x * kRouteTokensPerBlock;
   const int t_end = min(t_begin + kRouteTokensPerBlock, T);
-  float acc[VPL];
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
 
   for (int t = t_begin + warp; t < t_end; t += WARPS) {
     const float* row = logits + static_cast<size_t>(t) * E;
@@ -76,34 +77,52 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(
 #pragma unroll
     for (int i = 0; i < VPL; ++i) m = fmaxf(m, v[i]);
     m = warp_max(m);
-    float ex[VPL];
     float s = 0.f;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      ex[i] = (lane + 32 * i < E) ? expf(v[i] - m) : 0.f;
-      s += ex[i];
-    }
+    for (int i = 0; i < VPL; ++i) s += (lane + 32 * i < E) ? __expf(v[i] - m) : 0.f;
     s = warp_sum(s);
     const float inv = 1.0f / s;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) acc[i] += ex[i] * inv;
+    for (int i = 0; i < VPL; ++i)
+      if (lane + 32 * i < E) red[warp][lane + 32 * i] += __expf(v[i] - m) * inv;
 
-    // k rounds of a warp arg-max over the experts not taken yet; order (value desc,
-    // index asc) is total, so every lane ends each round with the same winner.
-    uint32_t taken = 0;
-    int my_idx = -1;
-    float my_val = 0.f;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int be = INT_MAX;
+    // Selection in (value desc, index asc) order.  Each lane keeps the best 4 of its own
+    // values, sorted; a round is one warp arg-max over the lanes' heads, and the winning
+    // lane pops its head.  A lane whose list runs dry rescans for the best values that
+    // follow its last taken one (rare: its 5th, 9th, ... win).
+    float hv[4];
+    int he[4];
+    float lv = INFINITY;  // last value taken from this lane (nothing taken yet)
+    int le = -1;
+    auto better = [](float x, int e, float y, int f) {
+      return f == INT_MAX || x > y || (x == y && e < f);
+    };
+    auto refill = [&]() {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) { hv[q] = -INFINITY; he[q] = INT_MAX; }
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (be == INT_MAX || v[i] > bv)) {
-          bv = v[i];
-          be = e;
+        const float x = v[i];
+        const bool after = x < lv || (x == lv && e > le);
+        if (e < E && after && better(x, e, hv[3], he[3])) {
+          hv[3] = x; he[3] = e;
+#pragma unroll
+          for (int q = 3; q > 0; --q) {
+            if (better(hv[q], he[q], hv[q - 1], he[q - 1])) {
+              const float tv = hv[q]; hv[q] = hv[q - 1]; hv[q - 1] = tv;
+              const int te = he[q]; he[q] = he[q - 1]; he[q - 1] = te;
+            }
+          }
         }
       }
+    };
+    refill();
+    int my_idx = -1;
+    float my_val = 0.f;
+    for (int j = 0; j < k; ++j) {
+      float bv = hv[0];
+      int be = he[0];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -113,22 +132,28 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(
           be = oe;
         }
       }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
       if (lane == j) {
         my_idx = be;
         my_val = bv;
       }
+      bool dry = false;
+      if ((be & 31) == lane) {
+        lv = hv[0]; le = he[0];
+        hv[0] = hv[1]; he[0] = he[1];
+        hv[1] = hv[2]; he[1] = he[2];
+        hv[2] = hv[3]; he[2] = he[3];
+        hv[3] = -INFINITY; he[3] = INT_MAX;
+        dry = he[0] == INT_MAX;
+      }
+      if (__any_sync(0xffffffffu, dry) && dry) refill();
     }
-    const float pj = (lane < k) ? expf(my_val - m) * inv : 0.f;
+    const float pj = (lane < k) ? __expf(my_val - m) * inv : 0.f;
     const float psum = warp_sum(pj);
     if (lane < k) {
       topk_idx[static_cast<size_t>(t) * k + lane] = my_idx;
       topk_gate[static_cast<size_t>(t) * k + lane] = pj / psum;
     }
   }
-
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) red[warp][lane + 32 * i] = acc[i];
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float sum = 0.f;
@@ -138,24 +163,37 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(
   }
 }
 
-__global__ void aux_loss_kernel(const int32_t* __restrict__ counts,
-                                const float* __restrict__ partials, int n_partials, int T,
-                                int k, int E, float* __restrict__ aux_out) {
-  __shared__ double red[1024];
-  double term = 0.0;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    double P = 0.0;
-    for (int b = 0; b < n_partials; ++b) P += partials[static_cast<size_t>(b) * E + e];
-    const double f = static_cast<double>(counts[e]) / (static_cast<double>(T) * k);
-    term += f * (P / T);
-  }
-  red[threadIdx.x] = term;
+// aux stage 1: block of 32 experts x 32 row stripes; P_e summed over the partial rows in a
+// fixed order, then f_e P_e summed over the block's experts -> one value per block.
+__global__ void __launch_bounds__(1024) aux_stage1_kernel(const int32_t* __restrict__ counts,
+                                                          const float* __restrict__ partials,
+                                                          int n_partials, int T, int k, int E,
+                                                          float* __restrict__ block_terms) {
+  __shared__ float sm[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + tx;
+  float s = 0.f;
+  if (e < E)
+    for (int b = ty; b < n_partials; b += 32) s += partials[static_cast<size_t>(b) * E + e];
+  sm[ty][tx] = s;
   __syncthreads();
-  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
-    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
-    __syncthreads();
+  if (ty == 0) {
+    float P = 0.f;
+    for (int y = 0; y < 32; ++y) P += sm[y][tx];
+    float term = 0.f;
+    if (e < E) term = (static_cast<float>(counts[e]) / (static_cast<float>(T) * k)) * (P / T);
+    for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
+    if (tx == 0) block_terms[blockIdx.x] = term;
   }
-  if (threadIdx.x == 0) aux_out[0] = static_cast<float>(E * red[0]);
+}
+
+__global__ void aux_stage2_kernel(const float* __restrict__ block_terms, int n_blocks, int E,
+                                  float* __restrict__ aux_out) {
+  if (threadIdx.x == 0) {
+    double s = 0.0;
+    for (int b = 0; b < n_blocks; ++b) s += block_terms[b];
+    aux_out[0] = static_cast<float>(E * s);
+  }
 }
 
 }  // namespace
@@ -189,8 +227,10 @@ int launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* idx, 
 }
 
 int launch_aux_loss(const int32_t* counts, const float* partials, int n_partials, int T, int k,
-                    int E, float* aux_out, cudaStream_t s) {
-  aux_loss_kernel<<<1, 1024, 0, s>>>(counts, partials, n_partials, T, k, E, aux_out);
+                    int E, float* aux_out, float* block_terms, cudaStream_t s) {
+  const int nb = (E + 31) / 32;
+  aux_stage1_kernel<<<nb, 1024, 0, s>>>(counts, partials, n_partials, T, k, E, block_terms);
+  aux_stage2_kernel<<<1, 32, 0, s>>>(block_terms, nb, E, aux_out);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -9,8 +9,8 @@
 
 namespace moe {
 
-constexpr int kRouteTokensPerBlock = 64;  // tokens per row of prob_partials
-constexpr int kDispatchChunk = 64;        // tokens counted sequentially by one warp
+constexpr int kRouteTokensPerBlock = 8;  // tokens per row of prob_partials
+constexpr int kDispatchChunk = 16;        // tokens counted sequentially by one warp
 
 __host__ __device__ inline int route_num_partials(int T) {
   return (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
@@ -21,8 +21,9 @@ int launch_split_router(const float* w, __nv_bfloat16* hi, __nv_bfloat16* lo, si
                         cudaStream_t s);
 int launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* idx, float* gate,
                         float* partials, cudaStream_t s);
+// block_terms: scratch of ceil(E/32) floats
 int launch_aux_loss(const int32_t* counts, const float* partials, int n_partials, int T, int k,
-                    int E, float* aux_out, cudaStream_t s);
+                    int E, float* aux_out, float* block_terms, cudaStream_t s);
 
 // capacity < 0 means unlimited.
 int launch_dispatch(const int32_t* idx, const __nv_bfloat16* x, int T, int d, int E, int k,

@@ -70,7 +70,8 @@ _SIGS = {
                                       ctypes.POINTER(moe_lora), c_vp, c_vp,
                                       ctypes.POINTER(moe_ffn_saved), c_vp, c_sz, c_vp, c_vp]),
     "moe_combine": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp]),
-    "moe_aux_loss": (ctypes.c_int, [_P, c_vp, c_vp, c_i32, c_vp, c_vp]),
+    "moe_aux_loss_workspace_size": (c_sz, [_P]),
+    "moe_aux_loss": (ctypes.c_int, [_P, c_vp, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp]),
     "moe_combine_bwd": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "moe_expert_ffn_bwd_workspace_size": (c_sz, [_P, c_i32]),
     "moe_expert_ffn_bwd": (ctypes.c_int, [_P, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
@@ -234,9 +235,14 @@ def moe_combine(p, y_perm, slot_row, y, stream=None):
                                             _stream(stream)))
 
 
-def moe_aux_loss(p, counts, prob_partials, n_partials, aux_out, stream=None):
+def moe_aux_loss_workspace_size(p: Problem) -> int:
+    return lib().moe_aux_loss_workspace_size(p.c())
+
+
+def moe_aux_loss(p, counts, prob_partials, n_partials, aux_out, workspace, stream=None):
+    wp, wn = _ws(workspace)
     _check("moe_aux_loss", lib().moe_aux_loss(p.c(), _ptr(counts), _ptr(prob_partials),
-                                              n_partials, _ptr(aux_out), _stream(stream)))
+                                              n_partials, _ptr(aux_out), wp, wn, _stream(stream)))
 
 
 def moe_combine_bwd(p, dy, y_perm, slot_row, topk_gate, dz_perm, dgate, stream=None):
@@ -276,6 +282,8 @@ def moe_set_kernel_events(kernel, before, after):
     kid = KERNEL_IDS[kernel] if isinstance(kernel, str) else int(kernel)
     hb = before.cuda_event if before is not None else None
     ha = after.cuda_event if after is not None else None
+    if (before is not None and not hb) or (after is not None and not ha):
+        raise ValueError("record each torch.cuda.Event once before handing it to the library")
     _check("moe_set_kernel_events", lib().moe_set_kernel_events(kid, hb, ha))
 
 
@@ -327,6 +335,7 @@ class LayerBuffers:
         self.ws_route = _bytes(moe_route_workspace_size(p), dev)
         self.ws_dispatch = _bytes(moe_dispatch_workspace_size(p), dev)
         self.ws_ffn = _bytes(moe_expert_ffn_workspace_size(p, N), dev)
+        self.ws_aux = _bytes(moe_aux_loss_workspace_size(p), dev)
         self.saved = None
         if train:
             self.saved = {"a_gate": _empty((N, F), torch.bfloat16, dev),
@@ -348,5 +357,5 @@ def layer_forward(buf: LayerBuffers, x, w_router, bias, w_gate, w_up, w_down, lo
                    w_gate, w_up, w_down, lora, buf.h, buf.y_perm, buf.saved, buf.ws_ffn,
                    buf.dev_status, stream)
     moe_combine(p, buf.y_perm, buf.slot_row, buf.y, stream)
-    moe_aux_loss(p, buf.counts, buf.partials, buf.n_partials, buf.aux, stream)
+    moe_aux_loss(p, buf.counts, buf.partials, buf.n_partials, buf.aux, buf.ws_aux, stream)
     return buf.y
