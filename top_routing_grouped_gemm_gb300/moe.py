@@ -65,6 +65,7 @@ _SIGS = {
     "moe_route_from_logits": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "moe_dispatch_workspace_size": (c_sz, [_P]),
     "moe_dispatch": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+    "moe_dispatch_noalloc": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "moe_expert_ffn_workspace_size": (c_sz, [_P, c_i32]),
     "moe_expert_ffn": (ctypes.c_int, [_P, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                       ctypes.POINTER(moe_lora), c_vp, c_vp,
@@ -214,6 +215,15 @@ def moe_dispatch(p, topk_idx, x, counts, offsets, slot_row, row_slot, n_kept_dro
                                               _ptr(offsets), _ptr(slot_row), _ptr(row_slot),
                                               _ptr(n_kept_dropped), _ptr(x_perm), wp, wn,
                                               _ptr(dev_status), _stream(stream)))
+
+
+def moe_dispatch_noalloc(p, topk_idx, x, counts, offsets, slot_row, row_slot, n_kept_dropped,
+                         x_perm, dev_status=None, stream=None):
+    """moe_dispatch with the library's built-in scratch instead of a caller workspace."""
+    _check("moe_dispatch_noalloc",
+           lib().moe_dispatch_noalloc(p.c(), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets),
+                                      _ptr(slot_row), _ptr(row_slot), _ptr(n_kept_dropped),
+                                      _ptr(x_perm), _ptr(dev_status), _stream(stream)))
 
 
 def moe_expert_ffn_workspace_size(p: Problem, rows_max: int) -> int:
