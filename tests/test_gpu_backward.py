@@ -1,0 +1,136 @@
+"""GPU parity of the LoRA backward (gradient of <dy, y> with routing fixed, base weights and
+router frozen) against the fp64 oracle, through the C ABI."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from top_routing_grouped_gemm_gb300 import moe, synth
+from parity_util import RTOL_FP, f64, lora64, relerr, to_dev
+
+pytestmark = pytest.mark.gpu
+
+GRADS = ("A_g", "B_g", "A_u", "B_u", "A_d", "B_d")
+
+
+def run_fwd_bwd(cfg, inp):
+    p = moe.problem_of(cfg)
+    buf = moe.LayerBuffers(p, "cuda", train=True)
+    moe.layer_forward(buf, inp["x"], inp["w_router"], inp.get("bias"), inp["w_gate"],
+                      inp["w_up"], inp["w_down"], inp.get("lora"))
+    moe.layer_backward(buf, inp["dy"], inp["x"], inp["w_router"], inp["w_gate"], inp["w_up"],
+                       inp["w_down"], inp.get("lora"))
+    torch.cuda.synchronize()
+    assert int(buf.dev_status.item()) == 0
+    return p, buf
+
+
+def small_cfg(**kw):
+    base = dict(name="small_bwd", T=300, d=192, E=6, k=2, F=192, r=16, alpha=32.0,
+                backward=True)
+    base.update(kw)
+    return synth.MoEConfig(**base)
+
+
+@pytest.mark.parametrize("cfg", [
+    small_cfg(),
+    small_cfg(T=777, d=320, E=9, k=3, F=448, r=24, alpha=48.0, cap_num=1, cap_den=1),
+    small_cfg(T=260, d=256, E=40, k=4, F=128, r=8, alpha=16.0, cap_num=3, cap_den=4,
+              zipf_bias=True),
+    small_cfg(r=0, alpha=0.0),
+], ids=["small", "ragged_capacity", "many_experts_some_empty", "no_lora"])
+def test_backward_whole(cfg):
+    inp = synth.make_inputs(cfg, "cpu")
+    dev = to_dev(inp)
+    p, buf = run_fwd_bwd(cfg, dev)
+    L_gpu = f64(buf.logits)
+    X, Wr = f64(inp["x"]), f64(inp["w_router"])
+    Wg, Wu, Wd = f64(inp["w_gate"]), f64(inp["w_up"]), f64(inp["w_down"])
+    lora = lora64(inp.get("lora"))
+    fwd = oracle.moe_forward(X, None, Wg, Wu, Wd, p.k, p.cap_num, p.cap_den, lora=lora,
+                             s=p.lora_scale, logits=L_gpu)
+    # the router's gradient path uses W_r: give the oracle the fp32 router weights
+    bwd = oracle.moe_backward(fwd, X, f64(inp["dy"]), Wr, Wg, Wu, Wd, lora, p.lora_scale)
+    n = fwd["disp"]["n_kept"]
+    assert relerr(f64(buf.dz_perm[:n]), bwd["dO"]) <= RTOL_FP
+    assert relerr(f64(buf.dgate), bwd["dgate"]) <= RTOL_FP
+    assert relerr(f64(buf.dx_perm[:n]), bwd["dx_perm"]) <= RTOL_FP
+    assert relerr(f64(buf.dx), bwd["dx"]) <= RTOL_FP
+    if p.r:
+        for nm in GRADS:
+            assert relerr(f64(buf.grads["d" + nm]), bwd["d" + nm]) <= RTOL_FP, nm
+        # experts that received no rows get exactly zero gradients
+        empty = np.where(np.diff(fwd["disp"]["offsets"]) == 0)[0]
+        for e in empty:
+            for nm in GRADS:
+                assert float(buf.grads["d" + nm][e].abs().max()) == 0.0
+
+
+def test_backward_gate_and_expert_paths_separately():
+    cfg = small_cfg(T=200, cap_num=5, cap_den=4)
+    inp = synth.make_inputs(cfg, "cpu")
+    dev = to_dev(inp)
+    p, buf = run_fwd_bwd(cfg, dev)
+    X = f64(inp["x"])
+    lora = lora64(inp.get("lora"))
+    fwd = oracle.moe_forward(X, None, f64(inp["w_gate"]), f64(inp["w_up"]), f64(inp["w_down"]),
+                             p.k, p.cap_num, p.cap_den, lora=lora, s=p.lora_scale,
+                             logits=f64(buf.logits))
+    bwd = oracle.moe_backward(fwd, X, f64(inp["dy"]), f64(inp["w_router"]), f64(inp["w_gate"]),
+                              f64(inp["w_up"]), f64(inp["w_down"]), lora, p.lora_scale)
+    # expert path alone: dispatch backward into a fresh buffer
+    dx_e = torch.empty_like(buf.dx)
+    moe.moe_dispatch_bwd(p, buf.dx_perm, buf.slot_row, dx_e)
+    torch.cuda.synchronize()
+    assert relerr(f64(dx_e), bwd["dx_expert"]) <= RTOL_FP
+    assert relerr(f64(buf.dx) - f64(dx_e), bwd["dx_gate"]) <= RTOL_FP
+
+
+def test_full_c5_sampled():
+    """c5 at full size: dgate and dx on sampled tokens (each kept slot's expert backward by
+    the oracle on that row alone), LoRA gradients of sampled experts (all their rows)."""
+    cfg = synth.config("c5")
+    inp = synth.make_inputs(cfg, "cuda")
+    p, buf = run_fwd_bwd(cfg, inp)
+    k, s = p.k, p.lora_scale
+    L_gpu = f64(buf.logits)
+    idx = oracle.topk_select(L_gpu, k)
+    assert np.array_equal(idx, buf.topk_idx.cpu().numpy())
+    prob = oracle.softmax(L_gpu)
+    gates = oracle.renormalised_gates(prob, idx)
+    D = oracle.dispatch(idx, p.E, None)
+    offs = D["offsets"]
+    rng = np.random.default_rng(5)
+    # LoRA gradients of a few experts (all their rows)
+    for e in sorted(set([0, p.E - 1] + list(rng.choice(p.E, 3, replace=False)))):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        rows = D["row_slot"][lo:hi]
+        Xe = f64(inp["x"][torch.from_numpy(rows // k).cuda()])
+        dOe = gates.reshape(-1)[rows][:, None] * f64(inp["dy"][torch.from_numpy(rows // k).cuda()])
+        Le = lora64(inp["lora"], e)
+        dX, ge = oracle.expert_backward(Xe, dOe, f64(inp["w_gate"][e]), f64(inp["w_up"][e]),
+                                        f64(inp["w_down"][e]), Le, s)
+        assert relerr(f64(buf.dx_perm[lo:hi]), dX) <= RTOL_FP
+        for nm in GRADS:
+            assert relerr(f64(buf.grads["d" + nm][e]), ge[nm]) <= RTOL_FP, (e, nm)
+    # dgate and dx of a few tokens
+    tokens = sorted(set([0, p.T - 1] + list(rng.choice(p.T, 3, replace=False))))
+    Wr = f64(inp["w_router"])
+    for t in tokens:
+        x_t = f64(inp["x"][t:t + 1])
+        dy_t = f64(inp["dy"][t:t + 1])
+        dx_t = np.zeros((1, p.d))
+        dg = np.zeros((1, k))
+        for j in range(k):
+            e = int(idx[t, j])
+            Le = lora64(inp["lora"], e)
+            Wg, Wu, Wd = f64(inp["w_gate"][e]), f64(inp["w_up"][e]), f64(inp["w_down"][e])
+            o = oracle.expert_forward(x_t, Wg, Wu, Wd, Le, s)[3]
+            dg[0, j] = float(dy_t[0] @ o[0])
+            dX, _ = oracle.expert_backward(x_t, gates[t, j] * dy_t, Wg, Wu, Wd, Le, s)
+            dx_t += dX
+        dl = oracle.route_backward(prob[t:t + 1], idx[t:t + 1], gates[t:t + 1], dg, np.ones((1, k)))
+        dx_t += dl @ Wr
+        assert relerr(f64(buf.dgate[t:t + 1]), dg) <= RTOL_FP
+        assert relerr(f64(buf.dx[t:t + 1]), dx_t) <= RTOL_FP

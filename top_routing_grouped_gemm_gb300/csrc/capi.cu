@@ -407,9 +407,10 @@ int moe_combine_bwd(const moe_problem* p, const moe_bf16* dy, const moe_bf16* y_
 }
 
 size_t moe_expert_ffn_bwd_workspace_size(const moe_problem* p, int32_t rows_max) {
-  (void)p;
-  (void)rows_max;
-  return 0;
+  if (check_problem(p) != MOE_OK || rows_max <= 0) return 0;
+  size_t b = up256((p->E + 1) * 4ull) + 2 * up256(static_cast<size_t>(rows_max) * p->F * 2);
+  if (p->r) b += 3 * up256(static_cast<size_t>(rows_max) * p->r * 2);
+  return b;
 }
 
 int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x_perm,
@@ -418,10 +419,171 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
                        const moe_ffn_saved* saved, const moe_bf16* h, const moe_bf16* dz_perm,
                        moe_bf16* dx_perm, const moe_lora_grad* grads, void* workspace,
                        size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
-  (void)p; (void)rows_max; (void)x_perm; (void)offsets; (void)w_gate; (void)w_up;
-  (void)w_down; (void)lora; (void)saved; (void)h; (void)dz_perm; (void)dx_perm; (void)grads;
-  (void)workspace; (void)workspace_bytes; (void)dev_status; (void)stream;
-  return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(check_problem(p));
+  if (rows_max <= 0) return MOE_ERR_INVALID_ARG;
+  if (!x_perm || !offsets || !w_gate || !w_up || !w_down || !saved || !saved->a_gate ||
+      !saved->a_up || !h || !dz_perm || !dx_perm)
+    return MOE_ERR_INVALID_ARG;
+  const bool use_lora = lora != nullptr && p->r > 0;
+  if (lora && p->r == 0) return MOE_ERR_INVALID_ARG;
+  if (use_lora) {
+    if (!lora->A_g || !lora->B_g || !lora->A_u || !lora->B_u || !lora->A_d || !lora->B_d ||
+        !saved->u_gate || !saved->u_up || !saved->u_down || !grads || !grads->dA_g ||
+        !grads->dB_g || !grads->dA_u || !grads->dB_u || !grads->dA_d || !grads->dB_d)
+      return MOE_ERR_INVALID_ARG;
+    const void* al2[] = {lora->A_g, lora->B_g, lora->A_u, lora->B_u, lora->A_d, lora->B_d,
+                         saved->u_gate, saved->u_up, saved->u_down};
+    for (const void* q : al2)
+      if (!al16(q)) return MOE_ERR_UNSUPPORTED;
+  }
+  const void* al[] = {x_perm, w_gate, w_up, w_down, saved->a_gate, saved->a_up, h, dz_perm,
+                      dx_perm};
+  for (const void* q : al)
+    if (!al16(q)) return MOE_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < moe_expert_ffn_bwd_workspace_size(p, rows_max))
+    return MOE_ERR_WORKSPACE;
+
+  const int d = p->d, E = p->E, F = p->F, r = p->r;
+  const float s = p->lora_scale;
+  Carver cv{static_cast<uint8_t*>(workspace), 0};
+  int32_t* tile_off = cv.take<int32_t>(E + 1);
+  moe_bf16* da_g = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * F);
+  moe_bf16* da_u = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * F);
+  moe_bf16 *v_d = nullptr, *v_g = nullptr, *v_u = nullptr;
+  if (r) {
+    v_d = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * r);
+    v_g = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * r);
+    v_u = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * r);
+  }
+  MOE_CUDA(launch_tile_schedule(offsets, E, rows_max, tile_off, dev_status, stream));
+  int launches = 1;
+  auto grouped = [&](GemmParams& P) {
+    P.group_off = offsets;
+    P.tile_off = tile_off;
+    P.G = E;
+    P.dev_status = dev_status;
+  };
+  auto lora_v = [&](const moe_bf16* a, int K, const moe_bf16* bmat, int bk_rows,
+                    moe_bf16* out) -> int {
+    // out = s * (a bmat), a [rows, K] K-major, bmat[e] [K, r] (MN-major B)
+    GemmParams P = gemm_params();
+    MOE_TRY(encode_map_kmajor(&P.maps[0], a, K, rows_max, 1, kBM));
+    MOE_TRY(encode_map_mnmajor(&P.maps[1], bmat, r, bk_rows, E));
+    P.nmaps = 2;
+    P.seg[0] = GemmSeg{K / kBK, 0, 0, {1, -1}, {0, 0}, {0, 0}};
+    P.nseg = 1;
+    grouped(P);
+    P.n_tiles = 1;
+    P.N = r;
+    P.out0 = out;
+    P.ldo = r;
+    P.scale = s;
+    ++launches;
+    return cuda_status(launch_gemm_bwd_lora_v(P, r, stream));
+  };
+
+  // v'_d = s dz B_d
+  if (use_lora) MOE_TRY(lora_v(dz_perm, d, lora->B_d, d, v_d));
+  // dh = dz W_d + v'_d A_d  ->  da_g, da_u (SwiGLU backward on the saved pre-activations)
+  {
+    GemmParams P = gemm_params();
+    MOE_TRY(encode_map_kmajor(&P.maps[0], dz_perm, d, rows_max, 1, kBM));
+    MOE_TRY(encode_map_mnmajor(&P.maps[1], w_down, F, d, E));
+    P.nmaps = 2;
+    P.seg[0] = GemmSeg{d / kBK, 0, 0, {1, -1}, {0, 0}, {0, 0}};
+    P.nseg = 1;
+    if (use_lora) {
+      MOE_TRY(encode_map_kmajor(&P.maps[2], v_d, r, rows_max, 1, kBM));
+      MOE_TRY(encode_map_mnmajor(&P.maps[3], lora->A_d, F, r, E));
+      P.nmaps = 4;
+      P.seg[1] = GemmSeg{(r + kBK - 1) / kBK, 2, 0, {3, -1}, {0, 0}, {0, 0}};
+      P.nseg = 2;
+    }
+    grouped(P);
+    P.n_tiles = (F + 127) / 128;
+    P.N = F;
+    P.ldo = F;
+    P.in0 = saved->a_gate;
+    P.in1 = saved->a_up;
+    P.out0 = da_g;
+    P.out1 = da_u;
+    ++launches;
+    MOE_CUDA(launch_gemm_bwd_dh(P, stream));
+  }
+  // v'_g = s da_g B_g, v'_u = s da_u B_u
+  if (use_lora) {
+    MOE_TRY(lora_v(da_g, F, lora->B_g, F, v_g));
+    MOE_TRY(lora_v(da_u, F, lora->B_u, F, v_u));
+  }
+  // dx_perm = da_g W_g + da_u W_u + v'_g A_g + v'_u A_u
+  {
+    GemmParams P = gemm_params();
+    MOE_TRY(encode_map_kmajor(&P.maps[0], da_g, F, rows_max, 1, kBM));
+    MOE_TRY(encode_map_kmajor(&P.maps[1], da_u, F, rows_max, 1, kBM));
+    MOE_TRY(encode_map_mnmajor(&P.maps[2], w_gate, d, F, E));
+    MOE_TRY(encode_map_mnmajor(&P.maps[3], w_up, d, F, E));
+    P.nmaps = 4;
+    P.seg[0] = GemmSeg{F / kBK, 0, 0, {2, -1}, {0, 0}, {0, 0}};
+    P.seg[1] = GemmSeg{F / kBK, 1, 0, {3, -1}, {0, 0}, {0, 0}};
+    P.nseg = 2;
+    if (use_lora) {
+      MOE_TRY(encode_map_kmajor(&P.maps[4], v_g, r, rows_max, 1, kBM));
+      MOE_TRY(encode_map_kmajor(&P.maps[5], v_u, r, rows_max, 1, kBM));
+      MOE_TRY(encode_map_mnmajor(&P.maps[6], lora->A_g, d, r, E));
+      MOE_TRY(encode_map_mnmajor(&P.maps[7], lora->A_u, d, r, E));
+      P.nmaps = 8;
+      P.seg[2] = GemmSeg{(r + kBK - 1) / kBK, 4, 0, {6, -1}, {0, 0}, {0, 0}};
+      P.seg[3] = GemmSeg{(r + kBK - 1) / kBK, 5, 0, {7, -1}, {0, 0}, {0, 0}};
+      P.nseg = 4;
+    }
+    grouped(P);
+    P.n_tiles = (d + 255) / 256;
+    P.N = d;
+    P.ldo = d;
+    P.out0 = dx_perm;
+    ++launches;
+    MOE_CUDA(launch_gemm_bwd_dx(P, stream));
+  }
+  // LoRA weight gradients: per expert, reductions over its rows (grouped over K)
+  if (use_lora) {
+    auto wgrad = [&](const moe_bf16* a, int M, const moe_bf16* b0, const moe_bf16* b1,
+                     float* out0, float* out1, bool transposed) -> int {
+      GemmParams P = gemm_params();
+      MOE_TRY(encode_map_mnmajor(&P.maps[0], a, M, rows_max, 1));
+      MOE_TRY(encode_map_mnmajor(&P.maps[1], b0, r, rows_max, 1));
+      P.nmaps = 2;
+      P.seg[0] = GemmSeg{0, 0, 0, {1, -1}, {0, 0}, {0, 0}};
+      if (b1) {
+        MOE_TRY(encode_map_mnmajor(&P.maps[2], b1, r, rows_max, 1));
+        P.nmaps = 3;
+        P.seg[0].b_map[1] = 2;
+      }
+      P.nseg = 1;
+      P.group_off = offsets;
+      P.G = E;
+      P.M = M;
+      P.m_tiles = (M + kBM - 1) / kBM;
+      P.n_tiles = 1;
+      P.N = r;
+      P.out0 = out0;
+      P.out1 = out1;
+      P.out_transposed = transposed ? 1 : 0;
+      P.dev_status = dev_status;
+      ++launches;
+      return cuda_status(launch_gemm_wgrad(P, r, b1 ? 2 : 1, stream));
+    };
+    // dA_g^T = x^T v'_g, dA_u^T = x^T v'_u   ([E, r, d] written transposed)
+    MOE_TRY(wgrad(x_perm, d, v_g, v_u, grads->dA_g, grads->dA_u, true));
+    // dB_d = dz^T u'_d   ([E, d, r])
+    MOE_TRY(wgrad(dz_perm, d, saved->u_down, nullptr, grads->dB_d, nullptr, false));
+    // dA_d^T = h^T v'_d  ([E, r, F] written transposed)
+    MOE_TRY(wgrad(h, F, v_d, nullptr, grads->dA_d, nullptr, true));
+    // dB_g = da_g^T u'_g, dB_u = da_u^T u'_u   ([E, F, r])
+    MOE_TRY(wgrad(da_g, F, saved->u_gate, nullptr, grads->dB_g, nullptr, false));
+    MOE_TRY(wgrad(da_u, F, saved->u_up, nullptr, grads->dB_u, nullptr, false));
+  }
+  count_launches(launches);
+  return MOE_OK;
 }
 
 int moe_dispatch_bwd(const moe_problem* p, const moe_bf16* dx_perm, const int32_t* slot_row,

@@ -24,7 +24,8 @@ namespace moe {
 template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES>
 struct GemmCfg {
   static constexpr int A_BYTES = kBM * kBK * 2;
-  static constexpr int B_BYTES = BN * kBK * 2;
+  // an MN-major B tile is always whole 64-wide TMA boxes (N below 64 is zero-filled)
+  static constexpr int B_BYTES = (B_MN ? ((BN + 63) / 64) * 64 : BN) * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
   static constexpr int ACC_COLS = NB * BN;
   static constexpr int TMEM_COLS = (2 * ACC_COLS <= 32)    ? 32
@@ -35,7 +36,7 @@ struct GemmCfg {
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
   static_assert(2 * ACC_COLS <= 512, "two accumulators must fit in TMEM");
-  static_assert(!B_MN || BN % 64 == 0 || BN <= 64, "MN-major B uses 64-wide boxes");
+  static_assert(!B_MN || BN % 64 == 0, "MN-major B is read in whole 64-wide boxes");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
 };
 
@@ -73,6 +74,42 @@ __device__ __forceinline__ bool decode_tile(const GemmParams& P, int tile, TileC
   return true;
 }
 
+// Grouped-over-K problems (LoRA weight gradients): tile = (group g, m-tile); the K range is
+// the rows [group_off[g], group_off[g+1]) of both operands; every group has m_tiles tiles.
+struct KRange {
+  int k0, nrows, nkb;
+};
+
+__device__ __forceinline__ bool decode_tile_wgrad(const GemmParams& P, int tile, TileCoord& tc,
+                                                  KRange& kr) {
+  if (tile >= P.G * P.m_tiles * P.n_tiles) return false;
+  tc.g = tile / (P.m_tiles * P.n_tiles);
+  const int rem = tile - tc.g * P.m_tiles * P.n_tiles;
+  tc.n = rem / P.m_tiles;
+  tc.m = rem - tc.n * P.m_tiles;
+  tc.row0 = tc.m * kBM;
+  tc.rows_valid = min(kBM, P.M - tc.row0);
+  const int lo = __ldg(&P.group_off[tc.g]);
+  const int hi = __ldg(&P.group_off[tc.g + 1]);
+  kr.k0 = lo;
+  kr.nrows = hi > lo ? hi - lo : 0;
+  kr.nkb = (kr.nrows + kBK - 1) / kBK;
+  return true;
+}
+
+// Zero the K rows [valid, 64) of an MN-major operand tile of `chunks` 64-wide boxes (each K
+// row is one 128-byte line of a box), by the 32 lanes of one warp.
+__device__ __forceinline__ void zero_k_tail(uint8_t* tile, int chunks, int valid, int lane) {
+  const int lines = (kBK - valid) * chunks;
+  for (int i = lane; i < lines * 8; i += 32) {
+    const int line = i >> 3, part = i & 7;
+    const int c = line / (kBK - valid);
+    const int kr = valid + (line - c * (kBK - valid));
+    uint4* p = reinterpret_cast<uint4*>(tile + c * 8192 + (kr >> 3) * 1024 + (kr & 7) * 128) + part;
+    *p = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // Store 16 consecutive bf16 values of one row, clipped to `ncols_left` columns.
 __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float (&v)[16],
                                               int ncols_left) {
@@ -105,6 +142,19 @@ __device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* src, float (&v
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+template <int EPI>
+__device__ __forceinline__ bool next_tile(const GemmParams& P, int tile, TileCoord& tc,
+                                          KRange& kr) {
+  if constexpr (EPI == EPI_WGRAD) {
+    return decode_tile_wgrad(P, tile, tc, kr);
+  } else {
+    kr.k0 = 0;
+    kr.nrows = 0;
+    kr.nkb = 0;
+    return decode_tile(P, tile, tc);
+  }
+}
 
 template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES>
 __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ GemmParams P) {
@@ -159,10 +209,13 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
     uint32_t phase = 0;
     bool ok = true;
     TileCoord tc;
-    for (int tile = blockIdx.x; ok && decode_tile(P, tile, tc); tile += gridDim.x) {
-      for (int s = 0; ok && s < P.nseg; ++s) {
+    KRange kr;
+    for (int tile = blockIdx.x; ok && next_tile<EPI>(P, tile, tc, kr); tile += gridDim.x) {
+      const int nseg = (EPI == EPI_WGRAD) ? 1 : P.nseg;
+      for (int s = 0; ok && s < nseg; ++s) {
         const GemmSeg& sg = P.seg[s];
-        for (int kb = 0; kb < sg.nkb; ++kb) {
+        const int nkb = (EPI == EPI_WGRAD) ? kr.nkb : sg.nkb;
+        for (int kb = 0; kb < nkb; ++kb) {
           int w = 1;
           if (lane == 0) w = mbar_wait(&empty[stage], phase ^ 1, abort_flag) ? 1 : 0;
           w = __shfl_sync(0xffffffffu, w, 0);
@@ -173,7 +226,7 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
 #pragma unroll
             for (int b = 0; b < NB; ++b) bytes += (sg.b_map[b] >= 0) ? C::B_BYTES : 0;
             mbar_arrive_expect_tx(&full[stage], bytes);
-            const int ka = sg.a_k0 + kb * kBK;
+            const int ka = (EPI == EPI_WGRAD) ? kr.k0 + kb * kBK : sg.a_k0 + kb * kBK;
             if (!A_MN) {
               tma_load_3d(sA, &P.maps[sg.a_map], &full[stage], ka, tc.row0, 0, pol_a);
             } else {
@@ -185,8 +238,8 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
             for (int b = 0; b < NB; ++b) {
               if (sg.b_map[b] < 0) continue;
               uint8_t* sB = sA + C::A_BYTES + b * C::B_BYTES;
-              const int kbk = sg.b_k0[b] + kb * kBK;
-              const int z = (P.group_off != nullptr) ? tc.g : sg.b_z[b];
+              const int kbk = (EPI == EPI_WGRAD) ? kr.k0 + kb * kBK : sg.b_k0[b] + kb * kBK;
+              const int z = (EPI == EPI_WGRAD) ? 0 : ((P.group_off != nullptr) ? tc.g : sg.b_z[b]);
               if (!B_MN) {
                 tma_load_3d(sB, &P.maps[sg.b_map[b]], &full[stage], kbk, tc.n * BN, z, pol_b);
               } else {
@@ -215,20 +268,38 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
     uint32_t acc_phase = 0;
     bool ok = true;
     TileCoord tc;
-    for (int tile = blockIdx.x; ok && decode_tile(P, tile, tc); tile += gridDim.x) {
+    KRange kr;
+    for (int tile = blockIdx.x; ok && next_tile<EPI>(P, tile, tc, kr); tile += gridDim.x) {
       int w = 1;
       if (lane == 0) w = mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag) ? 1 : 0;
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_base = tmem_base + acc * C::ACC_COLS;
-      for (int s = 0; ok && s < P.nseg; ++s) {
+      const int nseg = (EPI == EPI_WGRAD) ? 1 : P.nseg;
+      for (int s = 0; ok && s < nseg; ++s) {
         const GemmSeg& sg = P.seg[s];
-        for (int kb = 0; kb < sg.nkb; ++kb) {
+        const int nkb = (EPI == EPI_WGRAD) ? kr.nkb : sg.nkb;
+        for (int kb = 0; kb < nkb; ++kb) {
           if (lane == 0) w = mbar_wait(&full[stage], phase, abort_flag) ? 1 : 0;
           w = __shfl_sync(0xffffffffu, w, 0);
           if (!w) { ok = false; break; }
           tc_fence_after();
+          if constexpr (EPI == EPI_WGRAD) {
+            // rows past the group's end (the next group's rows, or memory never written)
+            // must contribute nothing: zero them in both operands before the MMAs
+            const int valid = min(kBK, kr.nrows - kb * kBK);
+            if (valid < kBK) {
+              uint8_t* sA = smem + stage * C::STAGE_BYTES;
+              zero_k_tail(sA, 2, valid, lane);
+#pragma unroll
+              for (int b = 0; b < NB; ++b)
+                if (sg.b_map[b] >= 0)
+                  zero_k_tail(sA + C::A_BYTES + b * C::B_BYTES, (BN + 63) / 64, valid, lane);
+              fence_proxy_async_smem();
+              __syncwarp();
+            }
+          }
           if (lane == 0) {
             const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
 #pragma unroll
@@ -268,7 +339,8 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
     uint32_t acc_phase = 0;
     bool ok = true;
     TileCoord tc;
-    for (int tile = blockIdx.x; decode_tile(P, tile, tc); tile += gridDim.x) {
+    KRange kr;
+    for (int tile = blockIdx.x; next_tile<EPI>(P, tile, tc, kr); tile += gridDim.x) {
       int w = 1;
       if (lane == 0) w = mbar_wait(&acc_full[acc], acc_phase, abort_flag) ? 1 : 0;
       w = __shfl_sync(0xffffffffu, w, 0);
@@ -384,6 +456,38 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
             }
             store_bf16x16(dag + off, o1, P.N - col);
             store_bf16x16(dau + off, o2, P.N - col);
+          }
+        }
+      } else if constexpr (EPI == EPI_WGRAD) {
+        // fp32 gradient of group g: [M, N] (ld N) or transposed [N, M] (ld M)
+#pragma unroll 1
+        for (int b = 0; b < NB; ++b) {
+          float* o = reinterpret_cast<float*>(b == 0 ? P.out0 : P.out1);
+          if (o == nullptr) continue;
+          float* base = o + static_cast<size_t>(tc.g) * P.M * P.N;
+          const int m = tc.row0 + r_local;
+#pragma unroll 1
+          for (int c = 0; c < BN; c += 16) {
+            float v[16];
+            if (kr.nkb > 0) {
+              tmem_ld16(t_row + b * BN + c, v);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            }
+            const int col = col0 + c;
+            if (valid && col < P.N) {
+              if (P.out_transposed) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  if (col + i < P.N) base[static_cast<size_t>(col + i) * P.M + m] = v[i];
+              } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  if (col + i < P.N) base[static_cast<size_t>(m) * P.N + col + i] = v[i];
+              }
+            }
           }
         }
       } else if constexpr (EPI == EPI_STORE) {

@@ -32,6 +32,7 @@ enum Epilogue : int {
   EPI_SCALE = 3,       // out_bf16_i = scale * acc_i for each B operand     (LoRA u, v)
   EPI_SWIGLU_BWD = 4,  // da_g, da_u from acc0 = dh and saved a_g, a_u
   EPI_STORE = 5,       // out_bf16 = acc0                                   (dx_perm)
+  EPI_WGRAD = 6,       // grouped over K: out_f32_i[g] = acc_i, plain or transposed (LoRA grads)
 };
 
 struct GemmSeg {
@@ -70,6 +71,7 @@ struct GemmParams {
   const void* in0;          // EPI_SWIGLU_BWD: saved a_g
   const void* in1;          // EPI_SWIGLU_BWD: saved a_u
   float scale;              // EPI_SCALE
+  int out_transposed;       // EPI_WGRAD: 1 -> out[g][n][m] (ld M), 0 -> out[g][m][n] (ld N)
   int* dev_status;
 };
 
@@ -86,5 +88,12 @@ int launch_gemm_gateup(const GemmParams& P, cudaStream_t s);        // BN=128, N
 int launch_gemm_down(const GemmParams& P, cudaStream_t s);          // BN=256, NB=1
 int launch_gemm_lora_u2(const GemmParams& P, int r, cudaStream_t s); // BN=r pad, NB=2
 int launch_gemm_lora_u1(const GemmParams& P, int r, cudaStream_t s); // BN=r pad, NB=1
+
+// Backward instantiations (gemm_bwd.cu).  B operands MN-major (weights used transposed).
+int launch_gemm_bwd_dh(const GemmParams& P, cudaStream_t s);         // BN=128, SwiGLU bwd
+int launch_gemm_bwd_dx(const GemmParams& P, cudaStream_t s);         // BN=256, store bf16
+int launch_gemm_bwd_lora_v(const GemmParams& P, int r, cudaStream_t s);  // BN=r pad, scale
+// LoRA weight gradients, grouped over K (rows of each expert); A and B MN-major.
+int launch_gemm_wgrad(const GemmParams& P, int r, int nb, cudaStream_t s);
 
 }  // namespace moe

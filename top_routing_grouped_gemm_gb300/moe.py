@@ -347,12 +347,26 @@ class LayerBuffers:
         self.ws_ffn = _bytes(moe_expert_ffn_workspace_size(p, N), dev)
         self.ws_aux = _bytes(moe_aux_loss_workspace_size(p), dev)
         self.saved = None
+        self.train = train
         if train:
             self.saved = {"a_gate": _empty((N, F), torch.bfloat16, dev),
                           "a_up": _empty((N, F), torch.bfloat16, dev)}
             if r:
                 for n in ("u_gate", "u_up", "u_down"):
                     self.saved[n] = _empty((N, r), torch.bfloat16, dev)
+            self.dz_perm = _empty((N, d), torch.bfloat16, dev)
+            self.dgate = _empty((T, k), torch.float32, dev)
+            self.dx_perm = _empty((N, d), torch.bfloat16, dev)
+            self.dx = _empty((T, d), torch.float32, dev)
+            self.ws_bwd = _bytes(moe_expert_ffn_bwd_workspace_size(p, N), dev)
+            self.grads = None
+            if r:
+                self.grads = {"dA_g": _empty((E, r, d), torch.float32, dev),
+                              "dB_g": _empty((E, F, r), torch.float32, dev),
+                              "dA_u": _empty((E, r, d), torch.float32, dev),
+                              "dB_u": _empty((E, F, r), torch.float32, dev),
+                              "dA_d": _empty((E, r, F), torch.float32, dev),
+                              "dB_d": _empty((E, d, r), torch.float32, dev)}
 
 
 def layer_forward(buf: LayerBuffers, x, w_router, bias, w_gate, w_up, w_down, lora=None,
@@ -369,3 +383,20 @@ def layer_forward(buf: LayerBuffers, x, w_router, bias, w_gate, w_up, w_down, lo
     moe_combine(p, buf.y_perm, buf.slot_row, buf.y, stream)
     moe_aux_loss(p, buf.counts, buf.partials, buf.n_partials, buf.aux, buf.ws_aux, stream)
     return buf.y
+
+
+def layer_backward(buf: LayerBuffers, dy, x, w_router, w_gate, w_up, w_down, lora=None,
+                   stream=None):
+    """Gradient of <dy, y> for the forward last run on ``buf`` (which must have been built
+    with train=True): combine backward -> expert backward (dx_perm, LoRA grads) -> dispatch
+    backward (expert path of dx) -> router backward (gate path of dx, accumulated)."""
+    p = buf.p
+    assert buf.train, "LayerBuffers(train=True) keeps what the backward needs"
+    moe_combine_bwd(p, dy, buf.y_perm, buf.slot_row, buf.topk_gate, buf.dz_perm, buf.dgate,
+                    stream)
+    moe_expert_ffn_bwd(p, buf.rows_max, buf.x_perm, buf.offsets, w_gate, w_up, w_down, lora,
+                       buf.saved, buf.h, buf.dz_perm, buf.dx_perm, buf.grads, buf.ws_bwd,
+                       buf.dev_status, stream)
+    moe_dispatch_bwd(p, buf.dx_perm, buf.slot_row, buf.dx, stream)
+    moe_route_bwd(p, buf.topk_idx, buf.topk_gate, buf.dgate, w_router, buf.dx, stream)
+    return buf.dx
