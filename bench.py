@@ -38,7 +38,6 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer tokens/s and grouped-GEMM TFLOP/s (% BF16 peak), 1×GB300"
-KERNELS = ["router_gemm", "topk", "dispatch", "gateup_gemm", "down_gemm", "combine"]
 KERNEL_SOURCES = ["gemm.cuh", "ptx.cuh", "gemm_fwd.cu", "moe_internal.h"]
 
 
@@ -250,6 +249,46 @@ def workload_config(cfg):
 
 # ------------------------------------------------------------------------ GPU arm
 
+def kernel_model(cfg, kept, nonempty, train, gather):
+    """Algorithmic bytes and flops of one launch of each timed kernel (units: non-empty
+    experts, kept rows, tokens), and which roofline bounds it.  With the permute fused into
+    the expert GEMM (gather), its A operand is the token matrix, read once (T rows), and
+    dispatch writes only the index maps."""
+    d, F, E, T, k, r = cfg.d, cfg.F, cfg.E, cfg.T, cfg.k, cfg.r
+    m = {}
+    a_rows = T if gather else kept
+    gu_b = nonempty * 2 * F * d * 2 + a_rows * d * 2 + kept * F * 2
+    gu_f = kept * 4.0 * d * F
+    dn_b = nonempty * d * F * 2 + kept * F * 2 + kept * d * 2
+    dn_f = kept * 2.0 * d * F
+    if r:
+        gu_b += kept * 2 * r * 2 + nonempty * 2 * F * r * 2
+        gu_f += kept * 2.0 * 2 * F * r
+        dn_b += kept * r * 2 + nonempty * d * r * 2
+        dn_f += kept * 2.0 * d * r
+    if train:
+        gu_b += kept * 2 * F * 2
+    m["gateup_gemm"] = (gu_b, gu_f)
+    m["down_gemm"] = (dn_b, dn_f)
+    if not cfg.prepermuted:
+        m["router_gemm"] = (T * d * 2 + E * d * 4 + T * E * 4, 2.0 * 2 * T * d * E)
+        m["topk"] = (T * E * 4 + T * k * 8, 0.0)
+        m["dispatch"] = (T * k * 4 * 3 + (0 if gather else T * d * 2 + kept * d * 2), 0.0)
+        m["combine"] = (kept * d * 2 + T * d * 2 + T * k * 4, 0.0)
+    if train:
+        m["bwd_dh_gemm"] = (nonempty * d * F * 2 + kept * d * 2 + kept * F * 2 * 4
+                            + (kept * r * 2 + nonempty * r * F * 2 if r else 0),
+                            kept * 2.0 * d * F + (kept * 2.0 * F * r if r else 0))
+        m["bwd_dx_gemm"] = (nonempty * 2 * d * F * 2 + kept * F * 2 * 2 + kept * d * 2
+                            + (kept * 2 * r * 2 + nonempty * 2 * r * d * 2 if r else 0),
+                            kept * 4.0 * d * F + (kept * 4.0 * d * r if r else 0))
+        if r:
+            m["wgrad"] = (kept * (2 * d + 3 * F) * 2 + kept * 5 * r * 2
+                          + E * r * (3 * d + 3 * F) * 4,
+                          kept * 2.0 * r * (3 * d + 3 * F))
+    return m
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -279,32 +318,63 @@ def main():
         return float(t.item())
 
     cfg = synth.config(args.workload)
-    assert not cfg.prepermuted and not cfg.backward, "bench steps the routed forward workloads"
+    train = cfg.backward
     inp = synth.make_inputs(cfg, "cuda", seed=rank)
     p = moe.problem_of(cfg)
-    buf = moe.LayerBuffers(p, "cuda", keep_logits=False)
     stream = torch.cuda.current_stream()
+    lora = inp.get("lora")
 
-    def step():
-        moe.layer_forward(buf, inp["x"], inp["w_router"], inp["bias"], inp["w_gate"],
-                          inp["w_up"], inp["w_down"], inp.get("lora"))
+    if cfg.prepermuted:
+        # one EP shard's experts on pre-permuted rows: the expert GEMMs alone
+        rows = cfg.T * cfg.k
+        h = torch.empty((rows, cfg.F), dtype=torch.bfloat16, device="cuda")
+        y_perm = torch.empty((rows, cfg.d), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(moe.moe_expert_ffn_workspace_size(p, rows), dtype=torch.uint8,
+                         device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+        def step():
+            moe.moe_expert_ffn(p, rows, inp["x_perm"], inp["offsets"], inp["row_slot"],
+                               inp["gates"], inp["w_gate"], inp["w_up"], inp["w_down"], lora, h,
+                               y_perm, None, ws, status)
+        kernels = ["gateup_gemm", "down_gemm"]
+        offs = inp["offsets"].cpu()
+        kept = int(offs[-1])
+        nonempty = int((offs[1:] - offs[:-1] > 0).sum())
+        out_bytes = (rows * cfg.d * 2, rows * cfg.d * 2)
+    else:
+        buf = moe.LayerBuffers(p, "cuda", train=train, keep_logits=train)
+        status = buf.dev_status
+
+        def step():
+            moe.layer_forward(buf, inp["x"], inp["w_router"], inp["bias"], inp["w_gate"],
+                              inp["w_up"], inp["w_down"], lora)
+            if train:
+                moe.layer_backward(buf, inp["dy"], inp["x"], inp["w_router"], inp["w_gate"],
+                                   inp["w_up"], inp["w_down"], lora)
+        kernels = ["router_gemm", "topk", "dispatch", "gateup_gemm", "down_gemm", "combine"]
+        if train:
+            kernels += ["bwd_dh_gemm", "bwd_dx_gemm"] + (["wgrad"] if cfg.r else [])
 
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
-    status = int(buf.dev_status.item())
-    if status != 0:
-        raise RuntimeError(f"device status {moe.STATUS_NAMES.get(status, status)} after warm-up")
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {moe.STATUS_NAMES.get(st, st)} after warm-up")
+    if not cfg.prepermuted:
+        kept = int(buf.n_kept_dropped[0].item())
+        nonempty = int((buf.offsets[1:] - buf.offsets[:-1] > 0).sum().item())
 
     K = args.steps
     ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(K)] for n in KERNELS}
+              for _ in range(K)] for n in kernels}
     # torch creates the CUDA event behind an Event on its first record: record each once so
     # that the raw handles handed to the library are live
-    for n in KERNELS:
-        for a, b in ev[n]:
+    for n in kernels:
+        for a, b2 in ev[n]:
             a.record(stream)
-            b.record(stream)
+            b2.record(stream)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     time.sleep(0.3)
@@ -313,71 +383,92 @@ def main():
     launches0 = moe.moe_launch_count()
     start.record(stream)
     for i in range(K):
-        for n in KERNELS:
+        for n in kernels:
             moe.moe_set_kernel_events(n, ev[n][i][0], ev[n][i][1])
         step()
     end.record(stream)
     torch.cuda.synchronize()
     barrier()
     launches = moe.moe_launch_count() - launches0
-    for n in KERNELS:
+    for n in kernels:
         moe.moe_set_kernel_events(n, None, None)
     clocks.stop()
     ms_step = max_over_ranks(start.elapsed_time(end) / K)
-    kern_us = {n: 1000.0 * sum(a.elapsed_time(b) for a, b in ev[n]) / K for n in KERNELS}
+    kern_us = {n: 1000.0 * sum(a.elapsed_time(b2) for a, b2 in ev[n]) / K for n in kernels}
 
-    # routing statistics (identical every step: same inputs)
-    counts = buf.counts.cpu()
-    kept = int(buf.n_kept_dropped[0].item())
-    nonempty = int((buf.offsets[1:] - buf.offsets[:-1] > 0).sum().item())
-    d, F, E, T = cfg.d, cfg.F, cfg.E, cfg.T
-
-    # algorithmic bytes / flops per launch (units: non-empty experts, kept rows, tokens)
-    gateup_bytes = nonempty * 2 * F * d * 2 + kept * d * 2 + kept * F * 2
-    down_bytes = nonempty * d * F * 2 + kept * F * 2 + kept * d * 2
-    gateup_flops = kept * 4.0 * d * F
-    down_flops = kept * 2.0 * d * F
-    router_flops = 2.0 * T * d * E
-    dispatch_bytes = T * cfg.k * 4 * 3 + T * d * 2 + kept * d * 2
-    combine_bytes = kept * d * 2 + T * d * 2 + T * cfg.k * 4
     pk = peaks()
     hbm = pk["hbm_gbs"]
-
-    def gbs(b, us):
-        return b / (us * 1e-6) / 1e9
-
-    def tfs(f, us):
-        return f / (us * 1e-6) / 1e12
-
-    kernels = {
-        "router_gemm": {"us": kern_us["router_gemm"], "TFLOP/s": tfs(router_flops, kern_us["router_gemm"])},
-        "topk": {"us": kern_us["topk"], "GB/s": gbs(T * E * 4, kern_us["topk"])},
-        "dispatch": {"us": kern_us["dispatch"], "GB/s": gbs(dispatch_bytes, kern_us["dispatch"]),
-                     "frac_hbm": gbs(dispatch_bytes, kern_us["dispatch"]) / hbm},
-        "gateup_gemm": {"us": kern_us["gateup_gemm"], "GB/s": gbs(gateup_bytes, kern_us["gateup_gemm"]),
-                        "TFLOP/s": tfs(gateup_flops, kern_us["gateup_gemm"])},
-        "down_gemm": {"us": kern_us["down_gemm"], "GB/s": gbs(down_bytes, kern_us["down_gemm"]),
-                      "TFLOP/s": tfs(down_flops, kern_us["down_gemm"])},
-        "combine": {"us": kern_us["combine"], "GB/s": gbs(combine_bytes, kern_us["combine"]),
-                    "frac_hbm": gbs(combine_bytes, kern_us["combine"]) / hbm},
-    }
-    expert_us = kern_us["gateup_gemm"] + kern_us["down_gemm"]
-    gg_tflops = tfs(gateup_flops + down_flops, expert_us)
-    gg_bound_us = max((gateup_bytes + down_bytes) / (hbm * 1e9),
-                      (gateup_flops + down_flops) / (pk["bf16_tflops"] * 1e12)) * 1e6
+    tpeak = pk["bf16_tflops"]
+    model = kernel_model(cfg, kept, nonempty, train, gather=False)
+    kstats = {}
+    for n in kernels:
+        by, fl = model[n]
+        us = kern_us[n]
+        t_hbm = by / (hbm * 1e9)
+        t_tc = fl / (tpeak * 1e12)
+        bound = "tensor" if t_tc > t_hbm else "hbm"
+        ent = {"us": us, "GB/s": by / (us * 1e-6) / 1e9, "bound": bound,
+               "algorithmic_bytes": by}
+        if fl:
+            ent["TFLOP/s"] = fl / (us * 1e-6) / 1e12
+            ent["flops"] = fl
+        ent["frac"] = (ent["TFLOP/s"] / tpeak) if bound == "tensor" else (ent["GB/s"] / hbm)
+        kstats[n] = ent
+    dominant = max(kernels, key=lambda n: kern_us[n])
+    dm = kstats[dominant]
+    if dm["bound"] == "tensor":
+        roof = {"kernel": dominant, "bound": "tensor", "achieved": dm["TFLOP/s"], "peak": tpeak,
+                "unit": "TFLOP/s", "frac": dm["TFLOP/s"] / tpeak,
+                "traffic": profiled_traffic(dominant, args.workload),
+                "algorithmic_flops": dm["flops"], "peak_source": pk["source"] + " bf16 burst"}
+    else:
+        roof = {"kernel": dominant, "bound": "hbm", "achieved": dm["GB/s"], "peak": hbm,
+                "unit": "GB/s", "frac": dm["GB/s"] / hbm,
+                "traffic": profiled_traffic(dominant, args.workload),
+                "algorithmic_bytes": dm["algorithmic_bytes"], "peak_source": pk["source"]}
+    gemms = [n for n in kernels if n.endswith("gemm") and n != "router_gemm"] + \
+        (["wgrad"] if "wgrad" in kernels else [])
+    g_us = sum(kern_us[n] for n in gemms)
+    g_fl = sum(model[n][1] for n in gemms)
+    g_by = sum(model[n][0] for n in gemms)
+    g_roof_us = max(g_by / (hbm * 1e9), g_fl / (tpeak * 1e12)) * 1e6
 
     # ---------------------------------------------------------------- end to end (host buffers)
-    x_host = inp["x"].cpu().pin_memory()
-    y_host = torch.empty((T, d), dtype=torch.bfloat16).pin_memory()
-    aux_host = torch.empty((1,), dtype=torch.float32).pin_memory()
-    x_dev = torch.empty_like(inp["x"])
+    if cfg.prepermuted:
+        x_host = inp["x_perm"].cpu().pin_memory()
+        y_host = torch.empty_like(y_perm, device="cpu").pin_memory()
+        x_dev = torch.empty_like(inp["x_perm"])
 
-    def e2e_step():
-        x_dev.copy_(x_host, non_blocking=True)
-        moe.layer_forward(buf, x_dev, inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"],
-                          inp["w_down"], inp.get("lora"))
-        y_host.copy_(buf.y, non_blocking=True)
-        aux_host.copy_(buf.aux, non_blocking=True)
+        def e2e_step():
+            x_dev.copy_(x_host, non_blocking=True)
+            moe.moe_expert_ffn(p, rows, x_dev, inp["offsets"], inp["row_slot"], inp["gates"],
+                               inp["w_gate"], inp["w_up"], inp["w_down"], lora, h, y_perm,
+                               None, ws, status)
+            y_host.copy_(y_perm, non_blocking=True)
+        h2d, d2h = out_bytes
+    else:
+        x_host = inp["x"].cpu().pin_memory()
+        y_host = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16).pin_memory()
+        aux_host = torch.empty((1,), dtype=torch.float32).pin_memory()
+        x_dev = torch.empty_like(inp["x"])
+        if train:
+            dy_host = inp["dy"].cpu().pin_memory()
+            dy_dev = torch.empty_like(inp["dy"])
+            dx_host = torch.empty((cfg.T, cfg.d), dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            x_dev.copy_(x_host, non_blocking=True)
+            moe.layer_forward(buf, x_dev, inp["w_router"], inp["bias"], inp["w_gate"],
+                              inp["w_up"], inp["w_down"], lora)
+            y_host.copy_(buf.y, non_blocking=True)
+            aux_host.copy_(buf.aux, non_blocking=True)
+            if train:
+                dy_dev.copy_(dy_host, non_blocking=True)
+                moe.layer_backward(buf, dy_dev, x_dev, inp["w_router"], inp["w_gate"],
+                                   inp["w_up"], inp["w_down"], lora)
+                dx_host.copy_(buf.dx, non_blocking=True)
+        h2d = cfg.T * cfg.d * 2 * (2 if train else 1)
+        d2h = cfg.T * cfg.d * 2 + 4 + (cfg.T * cfg.d * 4 if train else 0)
 
     for _ in range(3):
         e2e_step()
@@ -393,15 +484,15 @@ def main():
     ms_e2e = max_over_ranks(s2.elapsed_time(e2) / K)
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not cfg.prepermuted and not train:
         cpu = cpu_baseline_from_device(inp, cfg, args.cpu_sample)
 
     if rank == 0:
-        achieved = gbs(gateup_bytes, kern_us["gateup_gemm"])
+        units = cfg.T * cfg.k if cfg.prepermuted else cfg.T
         line = {
             "metric": METRIC,
-            "value": world * T / (ms_step * 1e-3),
-            "unit": "tokens/s",
+            "value": world * units / (ms_step * 1e-3),
+            "unit": "token-slots/s" if cfg.prepermuted else "tokens/s",
             "n_gpus": world,
             "steps": K,
             "warmup": args.warmup,
@@ -412,24 +503,22 @@ def main():
             "dtype": "bf16",
             "data": "synthetic",
             "config": workload_config(cfg),
-            "grouped_gemm": {"TFLOP/s": gg_tflops, "pct_bf16_peak": 100.0 * gg_tflops / pk["bf16_tflops"],
-                             "us": expert_us, "roofline_us": gg_bound_us,
-                             "frac_of_roofline": gg_bound_us / expert_us,
-                             "flops": gateup_flops + down_flops, "kept_rows": kept,
-                             "nonempty_experts": nonempty},
-            "roofline": {"kernel": "gateup_gemm", "bound": "hbm", "achieved": achieved,
-                         "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": profiled_traffic("gateup_gemm", args.workload),
-                         "algorithmic_bytes": gateup_bytes, "peak_source": pk["source"]},
-            "kernels": kernels,
-            "e2e": {"value": world * T / (ms_e2e * 1e-3), "unit": "tokens/s",
-                    "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2 + 4},
+            "grouped_gemm": {"TFLOP/s": g_fl / (g_us * 1e-6) / 1e12,
+                             "pct_bf16_peak": 100.0 * g_fl / (g_us * 1e-6) / 1e12 / tpeak,
+                             "us": g_us, "roofline_us": g_roof_us,
+                             "frac_of_roofline": g_roof_us / g_us, "flops": g_fl,
+                             "kernels": gemms, "kept_rows": kept, "nonempty_experts": nonempty},
+            "roofline": roof,
+            "kernels": kstats,
+            "e2e": {"value": world * units / (ms_e2e * 1e-3),
+                    "unit": "token-slots/s" if cfg.prepermuted else "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
-            "dropped_slots": int(buf.n_kept_dropped[1].item()),
-            "max_expert_count": int(counts.max().item()),
         }
+        if not cfg.prepermuted:
+            line["dropped_slots"] = int(buf.n_kept_dropped[1].item())
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -137,6 +137,8 @@ int moe_route_from_logits(const moe_problem* p, const float* logits, int32_t* to
  *   row_slot[row]   inverse map for rows < n_kept; rows >= n_kept are set to -1
  *   n_kept_dropped  {n_kept, n_dropped}
  *   x_perm[row]     = x[row_slot[row] / k]  (rows >= n_kept are left untouched)
+ * x and x_perm may both be NULL: then only the index maps are produced (for
+ * moe_expert_ffn_gather, which reads the token rows itself).
  * Everything is deterministic and bit-exact.  topk_idx entries outside [0, E) set
  * MOE_ERR_BAD_INDEX in dev_status and are treated as dropped.
  * Sizes: counts [E], offsets [E+1], slot_row [T*k], row_slot [T*k] int32;
@@ -187,6 +189,18 @@ int moe_expert_ffn(const moe_problem* p, int32_t rows_max, const moe_bf16* x_per
                    const moe_lora* lora, moe_bf16* h, moe_bf16* y_perm,
                    const moe_ffn_saved* saved, void* workspace, size_t workspace_bytes,
                    int32_t* dev_status, moe_stream_t stream);
+
+/* moe_expert_ffn with the permute fused into the first GEMMs ("Trillion-Parameter MoE Model
+ * Training Adaptation ...", section 4.3: deep fusion of Permute and Grouped GEMM): operand
+ * rows are gathered from the token matrix x [T, d] by slot, row r reading
+ * x[row_slot[r] / k], so no permuted copy of x is written or read.  Same outputs as
+ * moe_expert_ffn given x_perm = the dispatch gather of x. */
+int moe_expert_ffn_gather(const moe_problem* p, int32_t rows_max, const moe_bf16* x,
+                          const int32_t* offsets, const int32_t* row_slot,
+                          const float* topk_gate, const moe_bf16* w_gate, const moe_bf16* w_up,
+                          const moe_bf16* w_down, const moe_lora* lora, moe_bf16* h,
+                          moe_bf16* y_perm, const moe_ffn_saved* saved, void* workspace,
+                          size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream);
 
 /* ==================================================================== combine / aux
  * Unpermute and sum ("Trillion-Parameter MoE Model Training Adaptation ...", section 3
@@ -259,7 +273,10 @@ enum moe_kernel_id {
   MOE_KERNEL_GATEUP_GEMM = 3,   /* grouped gate/up GEMM with SwiGLU (+LoRA)      */
   MOE_KERNEL_DOWN_GEMM = 4,     /* grouped down GEMM with gate scaling (+LoRA)   */
   MOE_KERNEL_COMBINE = 5,       /* weighted unpermute and sum                    */
-  MOE_KERNEL_COUNT = 6
+  MOE_KERNEL_BWD_DH_GEMM = 6,   /* backward dh GEMM with the SwiGLU backward      */
+  MOE_KERNEL_BWD_DX_GEMM = 7,   /* backward dx_perm GEMM                         */
+  MOE_KERNEL_WGRAD = 8,         /* the LoRA weight-gradient GEMMs (first to last) */
+  MOE_KERNEL_COUNT = 9
 };
 int moe_set_kernel_events(int kernel_id, void* event_before, void* event_after);
 long long moe_launch_count(void);

@@ -35,10 +35,10 @@ def to_dev(inp, device="cuda"):
     return out
 
 
-def run_forward(p, inp, train=False):
+def run_forward(p, inp, train=False, gather=False):
     buf = moe.LayerBuffers(p, "cuda", train=train)
     moe.layer_forward(buf, inp["x"], inp["w_router"], inp.get("bias"), inp["w_gate"],
-                      inp["w_up"], inp["w_down"], inp.get("lora"))
+                      inp["w_up"], inp["w_down"], inp.get("lora"), gather=gather)
     torch.cuda.synchronize()
     assert int(buf.dev_status.item()) == 0
     return buf

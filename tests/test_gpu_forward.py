@@ -84,6 +84,26 @@ def test_layer_forward_whole(cfg):
         assert (buf.y[dropped_all].float().abs().sum() == 0).item()
 
 
+@pytest.mark.parametrize("cfg", [
+    synth.config("c1"),
+    small_cfg(T=777, d=320, E=9, k=3, F=448, r=24, alpha=48.0, cap_num=1, cap_den=1),
+    small_cfg(cap_num=5, cap_den=4, zipf_bias=True),
+], ids=["c1", "ragged_lora_capacity", "small_capacity_bias"])
+def test_fused_gather_matches_permuted_path(cfg):
+    """The permute fused into the expert GEMMs (rows gathered from x by slot) gives the same
+    bits as the separate gather + x_perm path (same products, same order)."""
+    dev = to_dev(synth.make_inputs(cfg, "cpu"))
+    p = moe.problem_of(cfg)
+    a = run_forward(p, dev, gather=False)
+    b = run_forward(p, dev, gather=True)
+    n = int(a.n_kept_dropped[0].item())
+    for name in ("slot_row", "offsets", "counts"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    assert torch.equal(a.h[:n], b.h[:n])
+    assert torch.equal(a.y_perm[:n], b.y_perm[:n])
+    assert torch.equal(a.y, b.y)
+
+
 def test_forward_is_deterministic():
     cfg = small_cfg(cap_num=5, cap_den=4, r=16, alpha=32.0)
     dev = to_dev(synth.make_inputs(cfg, "cpu"))
@@ -157,13 +177,13 @@ def test_bad_expert_id_is_reported_not_faulted():
 
 # ----------------------------------------------------------------------------- full sizes
 
-def _full_workload(name, n_sample):
+def _full_workload(name, n_sample, gather=False):
     cfg = synth.config(name)
     inp = synth.make_inputs(cfg, "cuda")
     p = moe.problem_of(cfg)
-    buf = run_forward(p, inp)
+    buf = run_forward(p, inp, gather=gather)
     L_gpu, idx, g, prob = check_routing(buf, p, inp)
-    D = check_dispatch(buf, p, idx, inp["x"])
+    D = check_dispatch(buf, p, idx, None if gather else inp["x"])
     rng = np.random.default_rng(1)
     tokens = sorted(set([0, p.T - 1] + list(rng.choice(p.T, n_sample, replace=False))))
     ys = oracle_tokens(inp, p, tokens, idx, g, D["slot_row"])
@@ -178,8 +198,17 @@ def test_full_c2_full_fanout():
     assert D["n_dropped"] == 0
 
 
+def test_full_c2_fused_gather():
+    cfg = synth.config("c2")
+    inp = synth.make_inputs(cfg, "cuda")
+    p = moe.problem_of(cfg)
+    a = run_forward(p, inp, gather=False)
+    b = run_forward(p, inp, gather=True)
+    assert torch.equal(a.y, b.y)
+
+
 def test_full_c3_skewed_capacity():
-    buf, D = _full_workload("c3", 6)
+    buf, D = _full_workload("c3", 6, gather=True)
     assert oracle.capacity(16384, 16, 896, 5, 4) == 366
     assert D["n_dropped"] > 0 and (D["kept"] <= 366).all()
 

@@ -190,10 +190,10 @@ int moe_dispatch(const moe_problem* p, const int32_t* topk_idx, const moe_bf16* 
                  int32_t* n_kept_dropped, moe_bf16* x_perm, void* workspace,
                  size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
   MOE_TRY(check_problem(p));
-  if (!topk_idx || !x || !counts || !offsets || !slot_row || !row_slot || !n_kept_dropped ||
-      !x_perm)
+  if (!topk_idx || !counts || !offsets || !slot_row || !row_slot || !n_kept_dropped)
     return MOE_ERR_INVALID_ARG;
-  if (!al16(x) || !al16(x_perm)) return MOE_ERR_UNSUPPORTED;
+  if (x_perm && !x) return MOE_ERR_INVALID_ARG;
+  if ((x && !al16(x)) || (x_perm && !al16(x_perm))) return MOE_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < dispatch_ws(p)) return MOE_ERR_WORKSPACE;
   Carver cv{static_cast<uint8_t*>(workspace), 0};
   int32_t* local_rank = cv.take<int32_t>(static_cast<size_t>(p->T) * p->k);
@@ -214,12 +214,20 @@ size_t moe_expert_ffn_workspace_size(const moe_problem* p, int32_t rows_max) {
   return (check_problem(p) == MOE_OK && rows_max > 0) ? ffn_ws(p, rows_max) : 0;
 }
 
-int moe_expert_ffn(const moe_problem* p, int32_t rows_max, const moe_bf16* x_perm,
-                   const int32_t* offsets, const int32_t* row_slot, const float* topk_gate,
-                   const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
-                   const moe_lora* lora, moe_bf16* h, moe_bf16* y_perm,
-                   const moe_ffn_saved* saved, void* workspace, size_t workspace_bytes,
-                   int32_t* dev_status, moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The expert step.  A rows come from `a_src`: the permuted rows themselves (gather = false,
+// a_src = x_perm [rows, d]) or token rows gathered by slot (gather = true, a_src = x [T, d],
+// row r reads x[row_slot[r] / k]).
+int expert_ffn_impl(const moe_problem* p, int32_t rows_max, const moe_bf16* a_src, bool gather,
+                    const int32_t* offsets, const int32_t* row_slot, const float* topk_gate,
+                    const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
+                    const moe_lora* lora, moe_bf16* h, moe_bf16* y_perm,
+                    const moe_ffn_saved* saved, void* workspace, size_t workspace_bytes,
+                    int32_t* dev_status, moe_stream_t stream) {
+  const moe_bf16* x_perm = a_src;
   MOE_TRY(check_problem(p));
   if (rows_max <= 0) return MOE_ERR_INVALID_ARG;
   if (!x_perm || !offsets || !row_slot || !topk_gate || !w_gate || !w_up || !w_down || !h ||
@@ -265,17 +273,30 @@ int moe_expert_ffn(const moe_problem* p, int32_t rows_max, const moe_bf16* x_per
     P.G = E;
     P.dev_status = dev_status;
   };
+  // operand A of the first-layer GEMMs: permuted rows, or token rows gathered by slot
+  auto a_map = [&](CUtensorMap* m) -> int {
+    return gather ? encode_map_gather(m, a_src, d, p->T)
+                  : encode_map_kmajor(m, a_src, d, rows_max, 1, kBM);
+  };
+  auto set_gather = [&](GemmParams& P) {
+    if (gather) {
+      P.gather_slot = row_slot;
+      P.gather_k = p->k;
+      P.gather_rows = p->T;
+    }
+  };
 
   // LoRA down-projections of the input: u_g = s x A_g^T, u_u = s x A_u^T
   if (use_lora) {
     GemmParams P = gemm_params();
-    MOE_TRY(encode_map_kmajor(&P.maps[0], x_perm, d, rows_max, 1, kBM));
+    MOE_TRY(a_map(&P.maps[0]));
     MOE_TRY(encode_map_kmajor(&P.maps[1], lora->A_g, d, r, E, lora_tile(r)));
     MOE_TRY(encode_map_kmajor(&P.maps[2], lora->A_u, d, r, E, lora_tile(r)));
     P.nmaps = 3;
-    P.seg[0] = GemmSeg{d / kBK, 0, 0, {1, 2}, {0, 0}, {0, 0}};
+    P.seg[0] = GemmSeg{d / kBK, 0, 0, {1, 2}, {0, 0}, {0, 0}, gather ? 1 : 0};
     P.nseg = 1;
     grouped(P);
+    set_gather(P);
     P.n_tiles = 1;
     P.N = r;
     P.out0 = u_g;
@@ -287,11 +308,11 @@ int moe_expert_ffn(const moe_problem* p, int32_t rows_max, const moe_bf16* x_per
   // gate/up projections (+ LoRA K-blocks) with the SwiGLU epilogue -> h
   {
     GemmParams P = gemm_params();
-    MOE_TRY(encode_map_kmajor(&P.maps[0], x_perm, d, rows_max, 1, kBM));
+    MOE_TRY(a_map(&P.maps[0]));
     MOE_TRY(encode_map_kmajor(&P.maps[1], w_gate, d, F, E, 128));
     MOE_TRY(encode_map_kmajor(&P.maps[2], w_up, d, F, E, 128));
     P.nmaps = 3;
-    P.seg[0] = GemmSeg{d / kBK, 0, 0, {1, 2}, {0, 0}, {0, 0}};
+    P.seg[0] = GemmSeg{d / kBK, 0, 0, {1, 2}, {0, 0}, {0, 0}, gather ? 1 : 0};
     P.nseg = 1;
     if (use_lora) {
       MOE_TRY(encode_map_kmajor(&P.maps[3], u_g, r, rows_max, 1, kBM));
@@ -304,6 +325,7 @@ int moe_expert_ffn(const moe_problem* p, int32_t rows_max, const moe_bf16* x_per
       P.nseg = 3;
     }
     grouped(P);
+    set_gather(P);
     P.n_tiles = (F + 127) / 128;
     P.N = F;
     P.out0 = h;
@@ -358,6 +380,32 @@ int moe_expert_ffn(const moe_problem* p, int32_t rows_max, const moe_bf16* x_per
   }
   count_launches(use_lora ? 5 : 3);
   return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_expert_ffn(const moe_problem* p, int32_t rows_max, const moe_bf16* x_perm,
+                   const int32_t* offsets, const int32_t* row_slot, const float* topk_gate,
+                   const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
+                   const moe_lora* lora, moe_bf16* h, moe_bf16* y_perm,
+                   const moe_ffn_saved* saved, void* workspace, size_t workspace_bytes,
+                   int32_t* dev_status, moe_stream_t stream) {
+  return expert_ffn_impl(p, rows_max, x_perm, false, offsets, row_slot, topk_gate, w_gate, w_up,
+                         w_down, lora, h, y_perm, saved, workspace, workspace_bytes, dev_status,
+                         stream);
+}
+
+int moe_expert_ffn_gather(const moe_problem* p, int32_t rows_max, const moe_bf16* x,
+                          const int32_t* offsets, const int32_t* row_slot,
+                          const float* topk_gate, const moe_bf16* w_gate, const moe_bf16* w_up,
+                          const moe_bf16* w_down, const moe_lora* lora, moe_bf16* h,
+                          moe_bf16* y_perm, const moe_ffn_saved* saved, void* workspace,
+                          size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
+  return expert_ffn_impl(p, rows_max, x, true, offsets, row_slot, topk_gate, w_gate, w_up,
+                         w_down, lora, h, y_perm, saved, workspace, workspace_bytes, dev_status,
+                         stream);
 }
 
 // ------------------------------------------------------------------------ combine / aux
@@ -508,7 +556,9 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
     P.out0 = da_g;
     P.out1 = da_u;
     ++launches;
+    mark_before(MOE_KERNEL_BWD_DH_GEMM, stream);
     MOE_CUDA(launch_gemm_bwd_dh(P, stream));
+    mark_after(MOE_KERNEL_BWD_DH_GEMM, stream);
   }
   // v'_g = s da_g B_g, v'_u = s da_u B_u
   if (use_lora) {
@@ -542,7 +592,9 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
     P.ldo = d;
     P.out0 = dx_perm;
     ++launches;
+    mark_before(MOE_KERNEL_BWD_DX_GEMM, stream);
     MOE_CUDA(launch_gemm_bwd_dx(P, stream));
+    mark_after(MOE_KERNEL_BWD_DX_GEMM, stream);
   }
   // LoRA weight gradients: per expert, reductions over its rows (grouped over K)
   if (use_lora) {
@@ -573,6 +625,7 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
       return cuda_status(launch_gemm_wgrad(P, r, b1 ? 2 : 1, stream));
     };
     // dA_g^T = x^T v'_g, dA_u^T = x^T v'_u   ([E, r, d] written transposed)
+    mark_before(MOE_KERNEL_WGRAD, stream);
     MOE_TRY(wgrad(x_perm, d, v_g, v_u, grads->dA_g, grads->dA_u, true));
     // dB_d = dz^T u'_d   ([E, d, r])
     MOE_TRY(wgrad(dz_perm, d, saved->u_down, nullptr, grads->dB_d, nullptr, false));
@@ -581,6 +634,7 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
     // dB_g = da_g^T u'_g, dB_u = da_u^T u'_u   ([E, F, r])
     MOE_TRY(wgrad(da_g, F, saved->u_gate, nullptr, grads->dB_g, nullptr, false));
     MOE_TRY(wgrad(da_u, F, saved->u_up, nullptr, grads->dB_u, nullptr, false));
+    mark_after(MOE_KERNEL_WGRAD, stream);
   }
   count_launches(launches);
   return MOE_OK;

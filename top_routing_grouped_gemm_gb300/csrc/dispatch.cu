@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(kRowThreads) dispatch_scatter_kernel(
     }
     rows[lane] = row;
   }
+  if (x_perm == nullptr) return;  // index maps only (the GEMM gathers the rows itself)
   __syncthreads();
   const int nvec = d / 8;
   const uint4* src = x + static_cast<size_t>(t) * nvec;

@@ -100,13 +100,14 @@ __device__ __forceinline__ bool decode_tile_wgrad(const GemmParams& P, int tile,
 // Zero the K rows [valid, 64) of an MN-major operand tile of `chunks` 64-wide boxes (each K
 // row is one 128-byte line of a box), by the 32 lanes of one warp.
 __device__ __forceinline__ void zero_k_tail(uint8_t* tile, int chunks, int valid, int lane) {
-  const int lines = (kBK - valid) * chunks;
-  for (int i = lane; i < lines * 8; i += 32) {
-    const int line = i >> 3, part = i & 7;
-    const int c = line / (kBK - valid);
-    const int kr = valid + (line - c * (kBK - valid));
-    uint4* p = reinterpret_cast<uint4*>(tile + c * 8192 + (kr >> 3) * 1024 + (kr & 7) * 128) + part;
-    *p = make_uint4(0u, 0u, 0u, 0u);
+  const int items = (kBK - valid) * 8;  // 16-byte parts of the lines to clear, per box
+  for (int c = 0; c < chunks; ++c) {
+    uint8_t* box = tile + c * 8192;
+    for (int i = lane; i < items; i += 32) {
+      const int kr = valid + (i >> 3);
+      reinterpret_cast<uint4*>(box + (kr >> 3) * 1024 + (kr & 7) * 128)[i & 7] =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
   }
 }
 
@@ -157,7 +158,7 @@ __device__ __forceinline__ bool next_tile(const GemmParams& P, int tile, TileCoo
 }
 
 template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES>
-__global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ GemmParams P) {
+__global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmParams P) {
   using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -211,6 +212,19 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
     TileCoord tc;
     KRange kr;
     for (int tile = blockIdx.x; ok && next_tile<EPI>(P, tile, tc, kr); tile += gridDim.x) {
+      // token rows of this tile for gathered A operands: lane l owns rows 4l .. 4l+3
+      int trow[4] = {0, 0, 0, 0};
+      if (P.gather_slot != nullptr) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int rl = 4 * lane + q;
+          if (rl < tc.rows_valid) {
+            const int slot = __ldg(&P.gather_slot[tc.row0 + rl]);
+            const int t = slot >= 0 ? slot / P.gather_k : 0;
+            trow[q] = t < P.gather_rows ? t : 0;
+          }
+        }
+      }
       const int nseg = (EPI == EPI_WGRAD) ? 1 : P.nseg;
       for (int s = 0; ok && s < nseg; ++s) {
         const GemmSeg& sg = P.seg[s];
@@ -220,15 +234,23 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
           if (lane == 0) w = mbar_wait(&empty[stage], phase ^ 1, abort_flag) ? 1 : 0;
           w = __shfl_sync(0xffffffffu, w, 0);
           if (!w) { ok = false; break; }
+          uint8_t* sA = smem + stage * C::STAGE_BYTES;
+          const int ka = (EPI == EPI_WGRAD) ? kr.k0 + kb * kBK : sg.a_k0 + kb * kBK;
           if (lane == 0) {
-            uint8_t* sA = smem + stage * C::STAGE_BYTES;
             uint32_t bytes = C::A_BYTES;
 #pragma unroll
             for (int b = 0; b < NB; ++b) bytes += (sg.b_map[b] >= 0) ? C::B_BYTES : 0;
             mbar_arrive_expect_tx(&full[stage], bytes);
-            const int ka = (EPI == EPI_WGRAD) ? kr.k0 + kb * kBK : sg.a_k0 + kb * kBK;
+          }
+          if (!A_MN && sg.a_gather) {
+            __syncwarp();
+            tma_gather4(sA + lane * 512, &P.maps[sg.a_map], &full[stage], ka, trow[0], trow[1],
+                        trow[2], trow[3]);
+          }
+          if (lane == 0) {
             if (!A_MN) {
-              tma_load_3d(sA, &P.maps[sg.a_map], &full[stage], ka, tc.row0, 0, pol_a);
+              if (!sg.a_gather)
+                tma_load_3d(sA, &P.maps[sg.a_map], &full[stage], ka, tc.row0, 0, pol_a);
             } else {
               tma_load_3d(sA, &P.maps[sg.a_map], &full[stage], tc.row0, ka, 0, pol_a);
               tma_load_3d(sA + 8192, &P.maps[sg.a_map], &full[stage], tc.row0 + 64, ka, 0,
@@ -535,14 +557,21 @@ __global__ void __launch_bounds__(256, 1) gemm_kernel(const __grid_constant__ Ge
   }
 }
 
-template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES>
+// ctas_per_sm > 1 only for instantiations whose ring and TMEM both fit that many times on an
+// SM (shared memory <= 227 KB / ctas_per_sm, TMEM columns <= 512 / ctas_per_sm), so that no
+// CTA can wait on another's TMEM allocation.
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int CTAS_PER_SM = 1>
 int launch_gemm(const GemmParams& P, cudaStream_t stream) {
   using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES>;
+  static_assert(CTAS_PER_SM * C::TMEM_COLS <= 512, "TMEM of co-resident CTAs");
+  static_assert(CTAS_PER_SM * (C::SMEM_BYTES + 1024) <= 232448, "shared memory per SM");
+  static_assert(CTAS_PER_SM > 1 || C::SMEM_BYTES > 232448 / 2,
+                "a single-CTA ring must be large enough to keep a second CTA off the SM");
   auto kern = gemm_kernel<BN, NB, A_MN, B_MN, EPI, STAGES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return static_cast<int>(e);
-  kern<<<num_sms(), 256, C::SMEM_BYTES, stream>>>(P);
+  kern<<<CTAS_PER_SM * num_sms(), 256, C::SMEM_BYTES, stream>>>(P);
   return static_cast<int>(cudaGetLastError());
 }
 

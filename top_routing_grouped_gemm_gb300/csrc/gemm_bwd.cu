@@ -23,8 +23,9 @@ int launch_gemm_bwd_lora_v(const GemmParams& P, int r, cudaStream_t s) {
 // LoRA weight gradients, reduction over each expert's rows
 int launch_gemm_wgrad(const GemmParams& P, int r, int nb, cudaStream_t s) {
   (void)r;
-  if (nb == 2) return launch_gemm<64, 2, true, true, EPI_WGRAD, 6>(P, s);
-  return launch_gemm<64, 1, true, true, EPI_WGRAD, 8>(P, s);
+  // small tiles with short K: two CTAs per SM keep twice as many tiles in flight
+  if (nb == 2) return launch_gemm<64, 2, true, true, EPI_WGRAD, 3, 2>(P, s);
+  return launch_gemm<64, 1, true, true, EPI_WGRAD, 4, 2>(P, s);
 }
 
 }  // namespace moe

@@ -70,6 +70,9 @@ _SIGS = {
     "moe_expert_ffn": (ctypes.c_int, [_P, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                       ctypes.POINTER(moe_lora), c_vp, c_vp,
                                       ctypes.POINTER(moe_ffn_saved), c_vp, c_sz, c_vp, c_vp]),
+    "moe_expert_ffn_gather": (ctypes.c_int, [_P, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                             ctypes.POINTER(moe_lora), c_vp, c_vp,
+                                             ctypes.POINTER(moe_ffn_saved), c_vp, c_sz, c_vp, c_vp]),
     "moe_combine": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp]),
     "moe_aux_loss_workspace_size": (c_sz, [_P]),
     "moe_aux_loss": (ctypes.c_int, [_P, c_vp, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp]),
@@ -86,7 +89,7 @@ _SIGS = {
 }
 
 KERNEL_IDS = {"router_gemm": 0, "topk": 1, "dispatch": 2, "gateup_gemm": 3, "down_gemm": 4,
-              "combine": 5}
+              "combine": 5, "bwd_dh_gemm": 6, "bwd_dx_gemm": 7, "wgrad": 8}
 
 _lib = None
 
@@ -240,6 +243,16 @@ def moe_expert_ffn(p, rows_max, x_perm, offsets, row_slot, topk_gate, w_gate, w_
                                 _ptr(dev_status), _stream(stream)))
 
 
+def moe_expert_ffn_gather(p, rows_max, x, offsets, row_slot, topk_gate, w_gate, w_up, w_down,
+                          lora, h, y_perm, saved, workspace, dev_status=None, stream=None):
+    wp, wn = _ws(workspace)
+    _check("moe_expert_ffn_gather",
+           lib().moe_expert_ffn_gather(p.c(), rows_max, _ptr(x), _ptr(offsets), _ptr(row_slot),
+                                       _ptr(topk_gate), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                                       _lora(lora), _ptr(h), _ptr(y_perm), _saved(saved), wp, wn,
+                                       _ptr(dev_status), _stream(stream)))
+
+
 def moe_combine(p, y_perm, slot_row, y, stream=None):
     _check("moe_combine", lib().moe_combine(p.c(), _ptr(y_perm), _ptr(slot_row), _ptr(y),
                                             _stream(stream)))
@@ -370,16 +383,25 @@ class LayerBuffers:
 
 
 def layer_forward(buf: LayerBuffers, x, w_router, bias, w_gate, w_up, w_down, lora=None,
-                  stream=None):
-    """route -> dispatch -> experts -> combine -> aux, all enqueued on one stream."""
+                  stream=None, gather=None):
+    """route -> dispatch -> experts -> combine -> aux, all enqueued on one stream.
+
+    gather=True fuses the permute into the expert GEMMs (moe_expert_ffn_gather: no x_perm is
+    written, the GEMM gathers token rows with TMA gather4).  It is off by default: on GB300
+    the 32 four-row gathers per A tile make the gate/up GEMM slower than the separate
+    gather pass plus a single 2-D TMA box per tile."""
     p = buf.p
+    if gather is None:
+        gather = False
     moe_route(p, x, w_router, bias, buf.topk_idx, buf.topk_gate, buf.partials, buf.logits,
               buf.ws_route, buf.dev_status, stream)
-    moe_dispatch(p, buf.topk_idx, x, buf.counts, buf.offsets, buf.slot_row, buf.row_slot,
-                 buf.n_kept_dropped, buf.x_perm, buf.ws_dispatch, buf.dev_status, stream)
-    moe_expert_ffn(p, buf.rows_max, buf.x_perm, buf.offsets, buf.row_slot, buf.topk_gate,
-                   w_gate, w_up, w_down, lora, buf.h, buf.y_perm, buf.saved, buf.ws_ffn,
-                   buf.dev_status, stream)
+    moe_dispatch(p, buf.topk_idx, None if gather else x, buf.counts, buf.offsets, buf.slot_row,
+                 buf.row_slot, buf.n_kept_dropped, None if gather else buf.x_perm,
+                 buf.ws_dispatch, buf.dev_status, stream)
+    ffn = moe_expert_ffn_gather if gather else moe_expert_ffn
+    ffn(p, buf.rows_max, x if gather else buf.x_perm, buf.offsets, buf.row_slot, buf.topk_gate,
+        w_gate, w_up, w_down, lora, buf.h, buf.y_perm, buf.saved, buf.ws_ffn, buf.dev_status,
+        stream)
     moe_combine(p, buf.y_perm, buf.slot_row, buf.y, stream)
     moe_aux_loss(p, buf.counts, buf.partials, buf.n_partials, buf.aux, buf.ws_aux, stream)
     return buf.y
