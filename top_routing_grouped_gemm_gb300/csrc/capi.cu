@@ -154,23 +154,26 @@ int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, co
 
   MOE_CUDA(launch_split_router(w_router, w_split, w_split + static_cast<size_t>(E) * d,
                                static_cast<size_t>(E) * d, stream));
+  // expert tile: 224 when it divides E (896 = 4 x 224: fewer, larger tiles, less L2 traffic
+  // per flop), else 128
+  const int bn = (E % 224 == 0) ? 224 : 128;
   GemmParams P = gemm_params();
   MOE_TRY(encode_map_kmajor(&P.maps[0], x, d, T, 1, kBM));
-  MOE_TRY(encode_map_kmajor(&P.maps[1], w_split, d, E, 2, 128));
+  MOE_TRY(encode_map_kmajor(&P.maps[1], w_split, d, E, 2, bn));
   P.nmaps = 2;
   P.seg[0] = GemmSeg{d / kBK, 0, 0, {1, -1}, {0, 0}, {0, 0}};
   P.seg[1] = GemmSeg{d / kBK, 0, 0, {1, -1}, {0, 0}, {1, 0}};
   P.nseg = 2;
   P.M = T;
   P.m_tiles = (T + kBM - 1) / kBM;
-  P.n_tiles = (E + 127) / 128;
+  P.n_tiles = (E + bn - 1) / bn;
   P.N = E;
   P.out0 = L;
   P.ldo = E;
   P.bias = bias;
   P.dev_status = dev_status;
   mark_before(MOE_KERNEL_ROUTER_GEMM, stream);
-  MOE_CUDA(launch_gemm_router(P, stream));
+  MOE_CUDA(launch_gemm_router(P, bn, stream));
   mark_after(MOE_KERNEL_ROUTER_GEMM, stream);
   mark_before(MOE_KERNEL_TOPK, stream);
   MOE_CUDA(launch_topk_softmax(L, T, E, p->k, topk_idx, topk_gate, prob_partials, stream));

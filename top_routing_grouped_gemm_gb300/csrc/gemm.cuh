@@ -48,9 +48,11 @@ __device__ __forceinline__ bool decode_tile(const GemmParams& P, int tile, TileC
   if (P.group_off == nullptr) {
     const int total = P.m_tiles * P.n_tiles;
     if (tile >= total) return false;
+    // m-major: the n-tiles of one row block run side by side, so each A tile is read from
+    // DRAM once and re-read from L2 (B is small and stays L2-resident for dense problems)
     tc.g = 0;
-    tc.n = tile / P.m_tiles;
-    tc.m = tile - tc.n * P.m_tiles;
+    tc.m = tile / P.n_tiles;
+    tc.n = tile - tc.m * P.n_tiles;
     tc.row0 = tc.m * kBM;
     tc.rows_valid = min(kBM, P.M - tc.row0);
     return true;

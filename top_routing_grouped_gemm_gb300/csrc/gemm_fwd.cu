@@ -3,7 +3,8 @@
 
 namespace moe {
 
-int launch_gemm_router(const GemmParams& P, cudaStream_t s) {
+int launch_gemm_router(const GemmParams& P, int bn, cudaStream_t s) {
+  if (bn == 224) return launch_gemm<224, 1, false, false, EPI_F32_BIAS, 4>(P, s);
   return launch_gemm<128, 1, false, false, EPI_F32_BIAS, 6>(P, s);
 }
 

@@ -90,7 +90,7 @@ int encode_map_gather(CUtensorMap* map, const void* base, uint64_t k_extent, uin
 int num_sms();
 
 // Kernel launchers (gemm_kernels.cu).  Return cudaError_t as int.
-int launch_gemm_router(const GemmParams& P, cudaStream_t s);        // BN=128, NB=1
+int launch_gemm_router(const GemmParams& P, int bn, cudaStream_t s);  // BN=128|224, NB=1
 int launch_gemm_gateup(const GemmParams& P, cudaStream_t s);        // BN=128, NB=2, SwiGLU
 int launch_gemm_down(const GemmParams& P, cudaStream_t s);          // BN=256, NB=1
 int launch_gemm_lora_u2(const GemmParams& P, int r, cudaStream_t s); // BN=r pad, NB=2

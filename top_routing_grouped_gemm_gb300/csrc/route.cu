@@ -49,6 +49,34 @@ __global__ void split_router_kernel(const float4* __restrict__ w, uint2* __restr
   }
 }
 
+// Order-preserving 64-bit key of (logit, expert): larger logit -> larger key, and for equal
+// logits the lower expert index -> larger key.  -0.0 and +0.0 compare equal as floats, so
+// both map to the key of +0.0.
+__device__ __forceinline__ uint64_t sel_key(float v, int e) {
+  uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(0x7FFFFFFF - e);
+}
+
+__device__ __forceinline__ float key_value(uint64_t key) {
+  uint32_t u = static_cast<uint32_t>(key >> 32);
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  return __uint_as_float(u);
+}
+
+__device__ __forceinline__ int key_expert(uint64_t key) {
+  return 0x7FFFFFFF - static_cast<int>(static_cast<uint32_t>(key));
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
 // One warp per token; lane i holds the logits of experts lane, lane+32, ... (VPL of them).
 // Each warp accumulates the softmax probabilities of its tokens into its own shared-memory
 // row; the block then writes one row of per-block sums (fixed order: deterministic).
@@ -73,10 +101,46 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(
       const int e = lane + 32 * i;
       v[i] = (e < E) ? __ldg(&row[e]) : -INFINITY;
     }
-    float m = -INFINITY;
+
+    // Selection in (value desc, index asc) order on the 64-bit keys.  Each lane keeps the
+    // best 4 of its own keys, sorted; a round is one warp max over the lanes' heads and the
+    // winning lane pops its head.  A lane whose list runs dry rescans for the best keys
+    // below its last taken one (rare: its 5th, 9th, ... win).  Key 0 marks an empty slot
+    // (no real key is 0: the index field of a real key is at least 0x7FFFFFFF - 1023).
+    uint64_t hk[4];
+    uint64_t last = ~0ull;
+    auto refill = [&]() {
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) m = fmaxf(m, v[i]);
-    m = warp_max(m);
+      for (int q = 0; q < 4; ++q) hk[q] = 0ull;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        const uint64_t key = sel_key(v[i], e);
+        if (e < E && key < last && key > hk[3]) {
+          hk[3] = key;
+#pragma unroll
+          for (int q = 3; q > 0; --q) {
+            if (hk[q] > hk[q - 1]) {
+              const uint64_t tk = hk[q]; hk[q] = hk[q - 1]; hk[q - 1] = tk;
+            }
+          }
+        }
+      }
+    };
+    refill();
+    uint64_t my_key = 0ull;
+    for (int j = 0; j < k; ++j) {
+      const uint64_t best = warp_max_u64(hk[0]);
+      if (lane == j) my_key = best;
+      bool dry = false;
+      if (hk[0] == best) {  // keys are unique, so exactly one lane owns the winner
+        last = best;
+        hk[0] = hk[1]; hk[1] = hk[2]; hk[2] = hk[3]; hk[3] = 0ull;
+        dry = hk[0] == 0ull;
+      }
+      if (__any_sync(0xffffffffu, dry) && dry) refill();
+    }
+    const float m = key_value(__shfl_sync(0xffffffffu, my_key, 0));  // the largest logit
     float s = 0.f;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) s += (lane + 32 * i < E) ? __expf(v[i] - m) : 0.f;
@@ -85,72 +149,10 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(
 #pragma unroll
     for (int i = 0; i < VPL; ++i)
       if (lane + 32 * i < E) red[warp][lane + 32 * i] += __expf(v[i] - m) * inv;
-
-    // Selection in (value desc, index asc) order.  Each lane keeps the best 4 of its own
-    // values, sorted; a round is one warp arg-max over the lanes' heads, and the winning
-    // lane pops its head.  A lane whose list runs dry rescans for the best values that
-    // follow its last taken one (rare: its 5th, 9th, ... win).
-    float hv[4];
-    int he[4];
-    float lv = INFINITY;  // last value taken from this lane (nothing taken yet)
-    int le = -1;
-    auto better = [](float x, int e, float y, int f) {
-      return f == INT_MAX || x > y || (x == y && e < f);
-    };
-    auto refill = [&]() {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) { hv[q] = -INFINITY; he[q] = INT_MAX; }
-#pragma unroll
-      for (int i = 0; i < VPL; ++i) {
-        const int e = lane + 32 * i;
-        const float x = v[i];
-        const bool after = x < lv || (x == lv && e > le);
-        if (e < E && after && better(x, e, hv[3], he[3])) {
-          hv[3] = x; he[3] = e;
-#pragma unroll
-          for (int q = 3; q > 0; --q) {
-            if (better(hv[q], he[q], hv[q - 1], he[q - 1])) {
-              const float tv = hv[q]; hv[q] = hv[q - 1]; hv[q - 1] = tv;
-              const int te = he[q]; he[q] = he[q - 1]; he[q - 1] = te;
-            }
-          }
-        }
-      }
-    };
-    refill();
-    int my_idx = -1;
-    float my_val = 0.f;
-    for (int j = 0; j < k; ++j) {
-      float bv = hv[0];
-      int be = he[0];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if (lane == j) {
-        my_idx = be;
-        my_val = bv;
-      }
-      bool dry = false;
-      if ((be & 31) == lane) {
-        lv = hv[0]; le = he[0];
-        hv[0] = hv[1]; he[0] = he[1];
-        hv[1] = hv[2]; he[1] = he[2];
-        hv[2] = hv[3]; he[2] = he[3];
-        hv[3] = -INFINITY; he[3] = INT_MAX;
-        dry = he[0] == INT_MAX;
-      }
-      if (__any_sync(0xffffffffu, dry) && dry) refill();
-    }
-    const float pj = (lane < k) ? __expf(my_val - m) * inv : 0.f;
+    const float pj = (lane < k) ? __expf(key_value(my_key) - m) * inv : 0.f;
     const float psum = warp_sum(pj);
     if (lane < k) {
-      topk_idx[static_cast<size_t>(t) * k + lane] = my_idx;
+      topk_idx[static_cast<size_t>(t) * k + lane] = key_expert(my_key);
       topk_gate[static_cast<size_t>(t) * k + lane] = pj / psum;
     }
   }
