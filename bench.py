@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=32, help="tokens in the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="launch every step from the host instead of replaying a CUDA graph")
     return ap.parse_args()
 
 
@@ -376,22 +378,46 @@ def main():
             a.record(stream)
             b2.record(stream)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def kernel_timed_steps():
+        for i in range(K):
+            for n in kernels:
+                moe.moe_set_kernel_events(n, ev[n][i][0], ev[n][i][1])
+            step()
+        for n in kernels:
+            moe.moe_set_kernel_events(n, None, None)
+
+    # Headline: the K steps captured once into a CUDA graph and replayed as one unit (no host
+    # launch overhead in the timed region).  Per-kernel durations: the same K steps launched
+    # from the host with the library recording CUDA events around each kernel (event timing
+    # is not available for events recorded inside a graph).
+    graph = None
+    launches0 = moe.moe_launch_count()
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+            for _ in range(K):
+                step()
+        torch.cuda.synchronize()
+        launches = moe.moe_launch_count() - launches0
     clocks = ClockSampler(local)
     time.sleep(0.3)
     barrier()
     torch.cuda.synchronize()
     launches0 = moe.moe_launch_count()
     start.record(stream)
-    for i in range(K):
-        for n in kernels:
-            moe.moe_set_kernel_events(n, ev[n][i][0], ev[n][i][1])
-        step()
+    if graph is not None:
+        graph.replay()
+    else:
+        kernel_timed_steps()
     end.record(stream)
     torch.cuda.synchronize()
     barrier()
-    launches = moe.moe_launch_count() - launches0
-    for n in kernels:
-        moe.moe_set_kernel_events(n, None, None)
+    if graph is None:
+        launches = moe.moe_launch_count() - launches0
+    else:
+        kernel_timed_steps()
+        torch.cuda.synchronize()
     clocks.stop()
     ms_step = max_over_ranks(start.elapsed_time(end) / K)
     kern_us = {n: 1000.0 * sum(a.elapsed_time(b2) for a, b2 in ev[n]) / K for n in kernels}
@@ -473,11 +499,21 @@ def main():
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
+    g2 = None
+    if args.graph:
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, capture_error_mode="relaxed"):
+            for _ in range(K):
+                e2e_step()
+        torch.cuda.synchronize()
     barrier()
     s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s2.record(stream)
-    for _ in range(K):
-        e2e_step()
+    if g2 is not None:
+        g2.replay()
+    else:
+        for _ in range(K):
+            e2e_step()
     e2.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -514,6 +550,7 @@ def main():
                     "unit": "token-slots/s" if cfg.prepermuted else "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
+            "cuda_graph": bool(args.graph),
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
         }
