@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=32, help="tokens in the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--permute", default="auto", choices=["auto", "fused", "separate"],
+                    help="fused: gather token rows inside the expert GEMM; separate: write "
+                         "x_perm in dispatch; auto: the library binding's default")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch every step from the host instead of replaying a CUDA graph")
     return ap.parse_args()
@@ -321,6 +324,9 @@ def main():
 
     cfg = synth.config(args.workload)
     train = cfg.backward
+    fused = {"fused": True, "separate": False}.get(
+        args.permute, moe.fused_permute_default(moe.problem_of(cfg), train))
+    fused = fused and not train and not cfg.prepermuted
     inp = synth.make_inputs(cfg, "cuda", seed=rank)
     p = moe.problem_of(cfg)
     stream = torch.cuda.current_stream()
@@ -350,7 +356,8 @@ def main():
 
         def step():
             moe.layer_forward(buf, inp["x"], inp["w_router"], inp["bias"], inp["w_gate"],
-                              inp["w_up"], inp["w_down"], lora)
+                              inp["w_up"], inp["w_down"], lora,
+                              gather=fused)
             if train:
                 moe.layer_backward(buf, inp["dy"], inp["x"], inp["w_router"], inp["w_gate"],
                                    inp["w_up"], inp["w_down"], lora)
@@ -425,7 +432,7 @@ def main():
     pk = peaks()
     hbm = pk["hbm_gbs"]
     tpeak = pk["bf16_tflops"]
-    model = kernel_model(cfg, kept, nonempty, train, gather=False)
+    model = kernel_model(cfg, kept, nonempty, train, gather=fused)
     kstats = {}
     for n in kernels:
         by, fl = model[n]
@@ -485,7 +492,8 @@ def main():
         def e2e_step():
             x_dev.copy_(x_host, non_blocking=True)
             moe.layer_forward(buf, x_dev, inp["w_router"], inp["bias"], inp["w_gate"],
-                              inp["w_up"], inp["w_down"], lora)
+                              inp["w_up"], inp["w_down"], lora,
+                              gather=fused)
             y_host.copy_(buf.y, non_blocking=True)
             aux_host.copy_(buf.aux, non_blocking=True)
             if train:
@@ -551,6 +559,7 @@ def main():
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
             "cuda_graph": bool(args.graph),
+            "fused_permute": bool(fused),
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
         }

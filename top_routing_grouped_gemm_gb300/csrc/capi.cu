@@ -276,9 +276,10 @@ int expert_ffn_impl(const moe_problem* p, int32_t rows_max, const moe_bf16* a_sr
     P.G = E;
     P.dev_status = dev_status;
   };
-  // operand A of the first-layer GEMMs: permuted rows, or token rows gathered by slot
+  // operand A of the first-layer GEMMs: permuted rows by TMA, or token rows gathered by
+  // slot inside the GEMM (then the map is a placeholder of the same shape, never read)
   auto a_map = [&](CUtensorMap* m) -> int {
-    return gather ? encode_map_gather(m, a_src, d, p->T)
+    return gather ? encode_map_kmajor(m, a_src, d, p->T, 1, kBM)
                   : encode_map_kmajor(m, a_src, d, rows_max, 1, kBM);
   };
   auto set_gather = [&](GemmParams& P) {
@@ -286,6 +287,8 @@ int expert_ffn_impl(const moe_problem* p, int32_t rows_max, const moe_bf16* a_sr
       P.gather_slot = row_slot;
       P.gather_k = p->k;
       P.gather_rows = p->T;
+      P.gather_src = a_src;
+      P.gather_ld = d;
     }
   };
 

@@ -178,8 +178,11 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    // with a gathered A operand a stage is full after the producer's expect-tx arrival
+    // (B bytes) and one arrival of the gather warp that filled its A tile
+    const uint32_t full_count = (P.gather_slot != nullptr) ? 2u : 1u;
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], full_count);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -214,19 +217,6 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
     TileCoord tc;
     KRange kr;
     for (int tile = blockIdx.x; ok && next_tile<EPI>(P, tile, tc, kr); tile += gridDim.x) {
-      // token rows of this tile for gathered A operands: lane l owns rows 4l .. 4l+3
-      int trow[4] = {0, 0, 0, 0};
-      if (P.gather_slot != nullptr) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int rl = 4 * lane + q;
-          if (rl < tc.rows_valid) {
-            const int slot = __ldg(&P.gather_slot[tc.row0 + rl]);
-            const int t = slot >= 0 ? slot / P.gather_k : 0;
-            trow[q] = t < P.gather_rows ? t : 0;
-          }
-        }
-      }
       const int nseg = (EPI == EPI_WGRAD) ? 1 : P.nseg;
       for (int s = 0; ok && s < nseg; ++s) {
         const GemmSeg& sg = P.seg[s];
@@ -239,15 +229,10 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
           uint8_t* sA = smem + stage * C::STAGE_BYTES;
           const int ka = (EPI == EPI_WGRAD) ? kr.k0 + kb * kBK : sg.a_k0 + kb * kBK;
           if (lane == 0) {
-            uint32_t bytes = C::A_BYTES;
+            uint32_t bytes = sg.a_gather ? 0u : C::A_BYTES;
 #pragma unroll
             for (int b = 0; b < NB; ++b) bytes += (sg.b_map[b] >= 0) ? C::B_BYTES : 0;
             mbar_arrive_expect_tx(&full[stage], bytes);
-          }
-          if (!A_MN && sg.a_gather) {
-            __syncwarp();
-            tma_gather4(sA + lane * 512, &P.maps[sg.a_map], &full[stage], ka, trow[0], trow[1],
-                        trow[2], trow[3]);
           }
           if (lane == 0) {
             if (!A_MN) {
@@ -354,6 +339,71 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
     if (!ok && lane == 0) {
       *abort_flag = 1;
       report_status(P.dev_status, MOE_ERR_TIMEOUT);
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ A-row gather
+    // Only with a gathered A operand.  The two warps take alternate k blocks: each fills the
+    // 128 x 64 A tile of its stage with 16-byte cp.async copies of token rows (zero fill for
+    // rows past the group's end) in the 128-byte-swizzled layout TMA would produce, waits for
+    // them, makes them visible to the tensor core (proxy fence) and arrives on the stage.
+    if constexpr (!A_MN && EPI != EPI_WGRAD) {
+      if (P.gather_slot != nullptr) {
+        const int gw = warp - 2;
+        const int part = lane & 7;      // 16-byte chunk of a 128-byte row this lane copies
+        const int rsub = lane >> 3;     // rows rsub, rsub + 4, ..., rsub + 124
+        const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(P.gather_src);
+        int stage = 0;
+        uint32_t phase = 0;
+        int q = 0;  // k blocks walked so far (all segments, all tiles)
+        bool ok = true;
+        TileCoord tc;
+        KRange kr;
+        for (int tile = blockIdx.x; ok && next_tile<EPI>(P, tile, tc, kr); tile += gridDim.x) {
+          int trow[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int rl = rsub + 4 * j;
+            int t = -1;
+            if (rl < tc.rows_valid) {
+              const int slot = __ldg(&P.gather_slot[tc.row0 + rl]);
+              t = slot >= 0 ? slot / P.gather_k : -1;
+              if (t >= P.gather_rows) t = -1;
+            }
+            trow[j] = t;
+          }
+          for (int s = 0; ok && s < P.nseg; ++s) {
+            const GemmSeg& sg = P.seg[s];
+            for (int kb = 0; kb < sg.nkb; ++kb, ++q) {
+              if ((q & 1) == gw) {
+                int w = 1;
+                if (lane == 0) w = mbar_wait(&empty[stage], phase ^ 1, abort_flag) ? 1 : 0;
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (!w) { ok = false; break; }
+                if (sg.a_gather) {
+                  uint8_t* sA = smem + stage * C::STAGE_BYTES;
+                  const int ka = sg.a_k0 + kb * kBK + part * 8;
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) {
+                    const int rl = rsub + 4 * j;
+                    const int t = trow[j];
+                    const __nv_bfloat16* g = src + static_cast<size_t>(t < 0 ? 0 : t) * P.gather_ld + ka;
+                    cp_async_16(sA + rl * 128 + ((part ^ (rl & 7)) << 4), g, t < 0 ? 0u : 16u);
+                  }
+                  cp_async_wait_all();
+                  fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[stage]);
+              }
+              if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+          }
+        }
+        if (!ok && lane == 0) {
+          *abort_flag = 1;
+          report_status(P.dev_status, MOE_ERR_TIMEOUT);
+        }
+      }
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue

@@ -57,20 +57,6 @@ int encode_map_mnmajor(CUtensorMap* map, const void* base, uint64_t mn_extent, u
   return encode3d(map, base, dims, strides, box);
 }
 
-// bf16 tensor [rows][k_extent] read by tile::gather4: boxes of 64 (K) x 1 row.
-int encode_map_gather(CUtensorMap* map, const void* base, uint64_t k_extent, uint64_t rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return MOE_ERR_CUDA;
-  const cuuint64_t dims[2] = {k_extent, rows};
-  const cuuint64_t strides[1] = {k_extent * 2};
-  const cuuint32_t box[2] = {64, 1};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
-}
-
 int num_sms() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;

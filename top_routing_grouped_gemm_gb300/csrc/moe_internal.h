@@ -42,7 +42,7 @@ struct GemmSeg {
   int b_map[2];   // tensor map of each B operand, -1 = this accumulator skips the segment
   int b_k0[2];    // K element offset in each B operand
   int b_z[2];     // third coordinate of B for dense problems (ignored when grouped)
-  int a_gather;   // 1: A rows are gathered by token (map a_map is 2-D with one-row boxes)
+  int a_gather;   // 1: A rows are gathered by token from P.gather_src (a_map unused)
 };
 
 struct GemmParams {
@@ -74,10 +74,12 @@ struct GemmParams {
   float scale;              // EPI_SCALE
   int out_transposed;       // EPI_WGRAD: 1 -> out[g][n][m] (ld M), 0 -> out[g][m][n] (ld N)
   // A-row gather (segments with a_gather): row r of the problem reads token row
-  // gather_slot[r] / gather_k of the gathered tensor, which has gather_rows rows
+  // gather_slot[r] / gather_k of gather_src [gather_rows, gather_ld] bf16
   const int* gather_slot;
   int gather_k;
   int gather_rows;
+  const void* gather_src;
+  int gather_ld;
   int* dev_status;
 };
 
@@ -86,7 +88,6 @@ int encode_map_kmajor(CUtensorMap* map, const void* base, uint64_t k_extent, uin
                       uint64_t groups, uint32_t box_rows);
 int encode_map_mnmajor(CUtensorMap* map, const void* base, uint64_t mn_extent,
                        uint64_t k_rows, uint64_t groups);
-int encode_map_gather(CUtensorMap* map, const void* base, uint64_t k_extent, uint64_t rows);
 int num_sms();
 
 // Kernel launchers (gemm_kernels.cu).  Return cudaError_t as int.

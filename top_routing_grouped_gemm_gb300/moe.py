@@ -382,17 +382,26 @@ class LayerBuffers:
                               "dB_d": _empty((E, d, r), torch.float32, dev)}
 
 
+# The fused permute gathers token rows inside the expert GEMM; it pays off while the token
+# matrix stays resident in the 129 MB L2 (the gathers then hit L2), not beyond.
+FUSED_PERMUTE_MAX_X_BYTES = 48 << 20
+
+
+def fused_permute_default(p: Problem, train: bool) -> bool:
+    return (not train) and p.T * p.d * 2 <= FUSED_PERMUTE_MAX_X_BYTES
+
+
 def layer_forward(buf: LayerBuffers, x, w_router, bias, w_gate, w_up, w_down, lora=None,
                   stream=None, gather=None):
     """route -> dispatch -> experts -> combine -> aux, all enqueued on one stream.
 
-    gather=True fuses the permute into the expert GEMMs (moe_expert_ffn_gather: no x_perm is
-    written, the GEMM gathers token rows with TMA gather4).  It is off by default: on GB300
-    the 32 four-row gathers per A tile make the gate/up GEMM slower than the separate
-    gather pass plus a single 2-D TMA box per tile."""
+    gather=True fuses the permute into the expert GEMMs (moe_expert_ffn_gather: dispatch
+    writes only the index maps and the GEMM copies token rows of x into its operand tiles);
+    gather=False writes x_perm.  The default fuses when x fits well in L2 and no backward
+    (which reads x_perm) will follow."""
     p = buf.p
     if gather is None:
-        gather = False
+        gather = fused_permute_default(p, buf.train)
     moe_route(p, x, w_router, bias, buf.topk_idx, buf.topk_gate, buf.partials, buf.logits,
               buf.ws_route, buf.dev_status, stream)
     moe_dispatch(p, buf.topk_idx, None if gather else x, buf.counts, buf.offsets, buf.slot_row,
