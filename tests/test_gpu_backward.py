@@ -39,7 +39,11 @@ def small_cfg(**kw):
     small_cfg(T=260, d=256, E=40, k=4, F=128, r=8, alpha=16.0, cap_num=3, cap_den=4,
               zipf_bias=True),
     small_cfg(r=0, alpha=0.0),
-], ids=["small", "ragged_capacity", "many_experts_some_empty", "no_lora"])
+    small_cfg(T=50, d=128, E=16, k=4, F=64, r=16, alpha=32.0, cap_num=0, cap_den=1),
+    small_cfg(T=1, d=128, E=8, k=2, F=64, r=8, alpha=16.0),
+    small_cfg(T=300, d=256, E=12, k=3, F=192, r=64, alpha=128.0),
+], ids=["small", "ragged_capacity", "many_experts_some_empty", "no_lora", "capacity_zero",
+        "one_token", "lora_r64"])
 def test_backward_whole(cfg):
     inp = synth.make_inputs(cfg, "cpu")
     dev = to_dev(inp)

@@ -61,7 +61,16 @@ def small_cfg(**kw):
     small_cfg(r=16, alpha=32.0),
     small_cfg(T=777, d=320, E=9, k=3, F=448, r=24, alpha=48.0, cap_num=1, cap_den=1),
     small_cfg(T=129, d=64, E=1, k=1, F=64),
-], ids=["c1", "small", "small_capacity_bias", "small_lora", "ragged_lora_capacity", "single_expert"])
+    small_cfg(T=1, d=128, E=8, k=2, F=64),
+    small_cfg(T=50, d=64, E=16, k=4, F=64, cap_num=0, cap_den=1),
+    small_cfg(T=200, d=128, E=1024, k=32, F=64),
+    small_cfg(T=64, d=128, E=32, k=32, F=128),
+    small_cfg(T=300, d=256, E=12, k=3, F=192, r=64, alpha=128.0),
+    small_cfg(T=300, d=256, E=12, k=3, F=192, r=8, alpha=16.0, cap_num=1, cap_den=2),
+    small_cfg(T=40, d=192, E=500, k=8, F=128, zipf_bias=True),
+], ids=["c1", "small", "small_capacity_bias", "small_lora", "ragged_lora_capacity", "single_expert",
+        "one_token", "capacity_zero", "max_experts_k32", "k_equals_E", "lora_r64", "lora_r8_half_capacity",
+        "mostly_empty_experts"])
 def test_layer_forward_whole(cfg):
     inp = synth.make_inputs(cfg, "cpu")
     dev = to_dev(inp)
