@@ -50,6 +50,15 @@ int cuda_status(int e) { return e == 0 ? MOE_OK : MOE_ERR_CUDA; }
 
 int lora_tile(int r) { return r <= 16 ? 16 : (r <= 32 ? 32 : 64); }
 
+// Experts whose rows span several 128-row tiles re-read each weight tile once per tile:
+// keep weights in L2 at normal priority then; with about one tile per expert they are
+// streamed once and loaded evict-first.
+bool weights_reused(const moe_problem* p, int rows_max) {
+  const int C = capacity_of(p);
+  return static_cast<long long>(rows_max) >= static_cast<long long>(kBM) * p->E &&
+         (C < 0 || C > kBM);
+}
+
 struct Carver {
   uint8_t* base;
   size_t used;
@@ -71,7 +80,7 @@ size_t dispatch_ws(const moe_problem* p) {
 }
 
 size_t ffn_ws(const moe_problem* p, int rows_max) {
-  size_t b = up256((p->E + 1) * 4ull);
+  size_t b = 2 * up256((p->E + 1) * 4ull);
   if (p->r) b += 3 * up256(static_cast<size_t>(rows_max) * p->r * 2);
   return b;
 }
@@ -157,9 +166,11 @@ int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, co
   // expert tile: 224 when it divides E (896 = 4 x 224: fewer, larger tiles, less L2 traffic
   // per flop), else 128
   const int bn = (E % 224 == 0) ? 224 : 128;
+  // clusters of two CTAs on consecutive token tiles share each weight tile by multicast
+  const bool pairs = bn == 224 && T > kBM;
   GemmParams P = gemm_params();
   MOE_TRY(encode_map_kmajor(&P.maps[0], x, d, T, 1, kBM));
-  MOE_TRY(encode_map_kmajor(&P.maps[1], w_split, d, E, 2, bn));
+  MOE_TRY(encode_map_kmajor(&P.maps[1], w_split, d, E, 2, pairs ? bn / 2 : bn));
   P.nmaps = 2;
   P.seg[0] = GemmSeg{d / kBK, 0, 0, {1, -1}, {0, 0}, {0, 0}};
   P.seg[1] = GemmSeg{d / kBK, 0, 0, {1, -1}, {0, 0}, {1, 0}};
@@ -171,9 +182,10 @@ int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, co
   P.out0 = L;
   P.ldo = E;
   P.bias = bias;
+  P.b_policy = 1;  // the router weights are re-read by every token tile
   P.dev_status = dev_status;
   mark_before(MOE_KERNEL_ROUTER_GEMM, stream);
-  MOE_CUDA(launch_gemm_router(P, bn, stream));
+  MOE_CUDA(launch_gemm_router(P, bn, pairs, stream));
   mark_after(MOE_KERNEL_ROUTER_GEMM, stream);
   mark_before(MOE_KERNEL_TOPK, stream);
   MOE_CUDA(launch_topk_softmax(L, T, E, p->k, topk_idx, topk_gate, prob_partials, stream));
@@ -259,6 +271,8 @@ int expert_ffn_impl(const moe_problem* p, int32_t rows_max, const moe_bf16* a_sr
   const int d = p->d, E = p->E, F = p->F, r = p->r;
   Carver cv{static_cast<uint8_t*>(workspace), 0};
   int32_t* tile_off = cv.take<int32_t>(E + 1);
+  int32_t* pair_off = cv.take<int32_t>(E + 1);
+  const int b_policy = weights_reused(p, rows_max) ? 1 : 0;
   moe_bf16 *u_g = nullptr, *u_u = nullptr, *u_d = nullptr;
   if (r) {
     u_g = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * r);
@@ -268,13 +282,15 @@ int expert_ffn_impl(const moe_problem* p, int32_t rows_max, const moe_bf16* a_sr
     if (saved && saved->u_up) u_u = saved->u_up;
     if (saved && saved->u_down) u_d = saved->u_down;
   }
-  MOE_CUDA(launch_tile_schedule(offsets, E, rows_max, tile_off, dev_status, stream));
+  MOE_CUDA(launch_tile_schedule(offsets, E, rows_max, tile_off, pair_off, dev_status, stream));
 
   auto grouped = [&](GemmParams& P) {
     P.group_off = offsets;
     P.tile_off = tile_off;
+    P.pair_off = pair_off;
     P.G = E;
     P.dev_status = dev_status;
+    P.b_policy = b_policy;
   };
   // operand A of the first-layer GEMMs: permuted rows by TMA, or token rows gathered by
   // slot inside the GEMM (then the map is a placeholder of the same shape, never read)
@@ -462,7 +478,7 @@ int moe_combine_bwd(const moe_problem* p, const moe_bf16* dy, const moe_bf16* y_
 
 size_t moe_expert_ffn_bwd_workspace_size(const moe_problem* p, int32_t rows_max) {
   if (check_problem(p) != MOE_OK || rows_max <= 0) return 0;
-  size_t b = up256((p->E + 1) * 4ull) + 2 * up256(static_cast<size_t>(rows_max) * p->F * 2);
+  size_t b = 2 * up256((p->E + 1) * 4ull) + 2 * up256(static_cast<size_t>(rows_max) * p->F * 2);
   if (p->r) b += 3 * up256(static_cast<size_t>(rows_max) * p->r * 2);
   return b;
 }
@@ -501,6 +517,8 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
   const float s = p->lora_scale;
   Carver cv{static_cast<uint8_t*>(workspace), 0};
   int32_t* tile_off = cv.take<int32_t>(E + 1);
+  int32_t* pair_off = cv.take<int32_t>(E + 1);
+  const int b_policy = weights_reused(p, rows_max) ? 1 : 0;  // as in the forward
   moe_bf16* da_g = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * F);
   moe_bf16* da_u = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * F);
   moe_bf16 *v_d = nullptr, *v_g = nullptr, *v_u = nullptr;
@@ -509,13 +527,15 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
     v_g = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * r);
     v_u = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * r);
   }
-  MOE_CUDA(launch_tile_schedule(offsets, E, rows_max, tile_off, dev_status, stream));
+  MOE_CUDA(launch_tile_schedule(offsets, E, rows_max, tile_off, pair_off, dev_status, stream));
   int launches = 1;
   auto grouped = [&](GemmParams& P) {
     P.group_off = offsets;
     P.tile_off = tile_off;
+    P.pair_off = pair_off;
     P.G = E;
     P.dev_status = dev_status;
+    P.b_policy = b_policy;
   };
   auto lora_v = [&](const moe_bf16* a, int K, const moe_bf16* bmat, int bk_rows,
                     moe_bf16* out) -> int {
@@ -627,6 +647,7 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
       P.out1 = out1;
       P.out_transposed = transposed ? 1 : 0;
       P.dev_status = dev_status;
+      P.b_policy = 1;  // the small B rows of an expert are re-read by each of its m-tiles
       ++launches;
       return cuda_status(launch_gemm_wgrad(P, r, b1 ? 2 : 1, stream));
     };

@@ -196,9 +196,12 @@ __global__ void __launch_bounds__(kRowThreads) dispatch_scatter_kernel(
   }
 }
 
+// m-tiles of 128 rows per group and their prefix (tile_off), and the prefix of m-tile pairs
+// (pair_off, for CTA-pair launches).  Malformed offsets disable the group and are reported.
 __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __restrict__ offsets,
                                                              int E, int rows_max,
                                                              int32_t* __restrict__ tile_off,
+                                                             int32_t* __restrict__ pair_off,
                                                              int32_t* dev_status) {
   __shared__ int sm[32];
   const int e = threadIdx.x;
@@ -215,6 +218,11 @@ __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __re
   const int excl = block_exclusive_scan_1024(mt, sm, &total);
   if (e < E) tile_off[e] = excl;
   if (e == 0) tile_off[E] = total;
+  __syncthreads();
+  int total_pairs;
+  const int pexcl = block_exclusive_scan_1024((mt + 1) >> 1, sm, &total_pairs);
+  if (e < E) pair_off[e] = pexcl;
+  if (e == 0) pair_off[E] = total_pairs;
 }
 
 __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& v, float scale) {
@@ -384,8 +392,9 @@ int launch_dispatch(const int32_t* idx, const __nv_bfloat16* x, int T, int d, in
 }
 
 int launch_tile_schedule(const int32_t* offsets, int E, int rows_max, int32_t* tile_off,
-                         int32_t* dev_status, cudaStream_t s) {
-  tile_schedule_kernel<<<1, 1024, 0, s>>>(offsets, E, rows_max, tile_off, dev_status);
+                         int32_t* pair_off, int32_t* dev_status, cudaStream_t s) {
+  tile_schedule_kernel<<<1, 1024, 0, s>>>(offsets, E, rows_max, tile_off, pair_off,
+                                          dev_status);
   return static_cast<int>(cudaGetLastError());
 }
 

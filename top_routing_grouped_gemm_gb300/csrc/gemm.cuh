@@ -99,6 +99,43 @@ __device__ __forceinline__ bool decode_tile_wgrad(const GemmParams& P, int tile,
   return true;
 }
 
+// CTA-pair launches (clusters of two): unit `pt` is a pair of m-tiles of one (group, n-tile);
+// CTA `rank` of the cluster takes m-tile 2*pair + rank.  Both CTAs need the same B tile,
+// which each loads half of and multicasts to both.  A CTA whose m-tile does not exist (odd
+// m-tile counts) is a ghost for that unit: rows_valid = 0, it loads no A, issues no MMA
+// and stores nothing, but still takes part in the B loads and the stage hand-off.
+__device__ __forceinline__ bool decode_pair_tile(const GemmParams& P, int pt, int rank,
+                                                 TileCoord& tc) {
+  if (P.group_off == nullptr) {
+    const int pairs = (P.m_tiles + 1) >> 1;
+    if (pt >= pairs * P.n_tiles) return false;
+    const int mp = pt / P.n_tiles;
+    tc.g = 0;
+    tc.n = pt - mp * P.n_tiles;
+    tc.m = 2 * mp + rank;
+    tc.row0 = tc.m * kBM;
+    tc.rows_valid = tc.m < P.m_tiles ? min(kBM, P.M - tc.row0) : 0;
+    return true;
+  }
+  const int total = __ldg(&P.pair_off[P.G]) * P.n_tiles;
+  if (pt >= total) return false;
+  int lo = 0, hi = P.G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(&P.pair_off[mid]) * P.n_tiles <= pt) lo = mid; else hi = mid - 1;
+  }
+  const int p0 = __ldg(&P.pair_off[lo]);
+  const int np = __ldg(&P.pair_off[lo + 1]) - p0;
+  const int local = pt - p0 * P.n_tiles;
+  tc.g = lo;
+  tc.n = local / np;
+  tc.m = 2 * (local - tc.n * np) + rank;
+  const int mt = __ldg(&P.tile_off[lo + 1]) - __ldg(&P.tile_off[lo]);
+  tc.row0 = __ldg(&P.group_off[lo]) + tc.m * kBM;
+  tc.rows_valid = tc.m < mt ? min(kBM, __ldg(&P.group_off[lo + 1]) - tc.row0) : 0;
+  return true;
+}
+
 // Zero the K rows [valid, 64) of an MN-major operand tile of `chunks` 64-wide boxes (each K
 // row is one 128-byte line of a box), by the 32 lanes of one warp.
 __device__ __forceinline__ void zero_k_tail(uint8_t* tile, int chunks, int valid, int lane) {
@@ -146,22 +183,25 @@ __device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* src, float (&v
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
-template <int EPI>
-__device__ __forceinline__ bool next_tile(const GemmParams& P, int tile, TileCoord& tc,
-                                          KRange& kr) {
+template <int EPI, int CL>
+__device__ __forceinline__ bool next_tile(const GemmParams& P, int tile, int rank,
+                                          TileCoord& tc, KRange& kr) {
   if constexpr (EPI == EPI_WGRAD) {
     return decode_tile_wgrad(P, tile, tc, kr);
   } else {
     kr.k0 = 0;
     kr.nrows = 0;
     kr.nkb = 0;
+    if constexpr (CL == 2) return decode_pair_tile(P, tile, rank, tc);
     return decode_tile(P, tile, tc);
   }
 }
 
-template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES>
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int CL>
 __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmParams P) {
   using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES>;
+  static_assert(CL == 1 || (EPI != EPI_WGRAD && !A_MN), "CTA pairs: M-grouped, K-major A");
+  static_assert(CL == 1 || B_MN || (BN / 2) % 8 == 0, "half B tiles stay swizzle-aligned");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -176,6 +216,10 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = (CL == 2) ? static_cast<int>(cluster_ctarank()) : 0;
+  const int unit0 = blockIdx.x / CL;       // first work unit of this CTA (or CTA pair)
+  const int unit_step = gridDim.x / CL;    // number of CTAs (or CTA pairs)
+  constexpr uint16_t kPairMask = 0x3;
 
   if (threadIdx.x == 0) {
     // with a gathered A operand a stage is full after the producer's expect-tx arrival
@@ -183,7 +227,7 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
     const uint32_t full_count = (P.gather_slot != nullptr) ? 2u : 1u;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], full_count);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CL);  // a stage is free once every CTA that reads it released it
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
@@ -203,20 +247,24 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CL == 2) {
+    cluster_sync();  // both CTAs' barriers exist before either multicasts into the other
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     const uint64_t pol_a = l2_policy_evict_last();
-    const uint64_t pol_b = l2_policy_evict_first();
+    const uint64_t pol_b = P.b_policy ? l2_policy_evict_normal() : l2_policy_evict_first();
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     TileCoord tc;
     KRange kr;
-    for (int tile = blockIdx.x; ok && next_tile<EPI>(P, tile, tc, kr); tile += gridDim.x) {
+    for (int tile = unit0; ok && next_tile<EPI, CL>(P, tile, rank, tc, kr); tile += unit_step) {
       const int nseg = (EPI == EPI_WGRAD) ? 1 : P.nseg;
       for (int s = 0; ok && s < nseg; ++s) {
         const GemmSeg& sg = P.seg[s];
@@ -228,15 +276,17 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
           if (!w) { ok = false; break; }
           uint8_t* sA = smem + stage * C::STAGE_BYTES;
           const int ka = (EPI == EPI_WGRAD) ? kr.k0 + kb * kBK : sg.a_k0 + kb * kBK;
+          const bool ghost = (CL == 2) && tc.rows_valid == 0;
           if (lane == 0) {
-            uint32_t bytes = sg.a_gather ? 0u : C::A_BYTES;
+            // B: the whole tile lands here (half of it from the other CTA of a pair)
+            uint32_t bytes = (sg.a_gather || ghost) ? 0u : C::A_BYTES;
 #pragma unroll
             for (int b = 0; b < NB; ++b) bytes += (sg.b_map[b] >= 0) ? C::B_BYTES : 0;
             mbar_arrive_expect_tx(&full[stage], bytes);
           }
           if (lane == 0) {
             if (!A_MN) {
-              if (!sg.a_gather)
+              if (!sg.a_gather && !ghost)
                 tma_load_3d(sA, &P.maps[sg.a_map], &full[stage], ka, tc.row0, 0, pol_a);
             } else {
               tma_load_3d(sA, &P.maps[sg.a_map], &full[stage], tc.row0, ka, 0, pol_a);
@@ -249,7 +299,19 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
               uint8_t* sB = sA + C::A_BYTES + b * C::B_BYTES;
               const int kbk = (EPI == EPI_WGRAD) ? kr.k0 + kb * kBK : sg.b_k0[b] + kb * kBK;
               const int z = (EPI == EPI_WGRAD) ? 0 : ((P.group_off != nullptr) ? tc.g : sg.b_z[b]);
-              if (!B_MN) {
+              if constexpr (CL == 2) {
+                // this CTA loads its half of B and multicasts it to both CTAs of the pair
+                if (!B_MN) {
+                  constexpr int HB = BN / 2;
+                  tma_load_3d_mc(sB + rank * HB * 128, &P.maps[sg.b_map[b]], &full[stage], kbk,
+                                 tc.n * BN + rank * HB, z, kPairMask, pol_b);
+                } else {
+#pragma unroll
+                  for (int c = rank; c < (BN + 63) / 64; c += 2)
+                    tma_load_3d_mc(sB + c * 8192, &P.maps[sg.b_map[b]], &full[stage],
+                                   tc.n * BN + c * 64, kbk, z, kPairMask, pol_b);
+                }
+              } else if (!B_MN) {
                 tma_load_3d(sB, &P.maps[sg.b_map[b]], &full[stage], kbk, tc.n * BN, z, pol_b);
               } else {
 #pragma unroll
@@ -278,7 +340,7 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
     bool ok = true;
     TileCoord tc;
     KRange kr;
-    for (int tile = blockIdx.x; ok && next_tile<EPI>(P, tile, tc, kr); tile += gridDim.x) {
+    for (int tile = unit0; ok && next_tile<EPI, CL>(P, tile, rank, tc, kr); tile += unit_step) {
       int w = 1;
       if (lane == 0) w = mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag) ? 1 : 0;
       w = __shfl_sync(0xffffffffu, w, 0);
@@ -311,8 +373,10 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
           }
           if (lane == 0) {
             const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
+            const bool ghost = (CL == 2) && tc.rows_valid == 0;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
+              if (ghost) break;
               const uint64_t adesc = A_MN ? smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
                                           : smem_desc_sw128(a_addr + k * 32, 16, 1024);
               const uint32_t accumulate = (s > 0 || kb > 0 || k > 0) ? 1u : 0u;
@@ -325,7 +389,11 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
                 umma_bf16(d_base + b * BN, adesc, bdesc, idesc, accumulate);
               }
             }
-            umma_commit(&empty[stage]);
+            if constexpr (CL == 2) {
+              umma_commit_mc(&empty[stage], kPairMask);  // both CTAs load into this stage
+            } else {
+              umma_commit(&empty[stage]);
+            }
           }
           __syncwarp();
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -358,7 +426,7 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
         bool ok = true;
         TileCoord tc;
         KRange kr;
-        for (int tile = blockIdx.x; ok && next_tile<EPI>(P, tile, tc, kr); tile += gridDim.x) {
+        for (int tile = unit0; ok && next_tile<EPI, CL>(P, tile, rank, tc, kr); tile += unit_step) {
           int trow[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -414,7 +482,7 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
     bool ok = true;
     TileCoord tc;
     KRange kr;
-    for (int tile = blockIdx.x; next_tile<EPI>(P, tile, tc, kr); tile += gridDim.x) {
+    for (int tile = unit0; next_tile<EPI, CL>(P, tile, rank, tc, kr); tile += unit_step) {
       int w = 1;
       if (lane == 0) w = mbar_wait(&acc_full[acc], acc_phase, abort_flag) ? 1 : 0;
       w = __shfl_sync(0xffffffffu, w, 0);
@@ -425,7 +493,9 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
       const long row = static_cast<long>(tc.row0) + r_local;
       const int col0 = tc.n * BN;
 
-      if constexpr (EPI == EPI_F32_BIAS) {
+      if (tc.rows_valid == 0) {
+        // ghost unit of a CTA pair: nothing was computed, nothing to store
+      } else if constexpr (EPI == EPI_F32_BIAS) {
         float* out = reinterpret_cast<float*>(P.out0);
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
@@ -588,8 +658,13 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
   // All roles are done.  On the normal path every TMA load was consumed and every MMA was
   // waited for through acc_full.  After an abort, the MMA thread waits (bounded) for its
   // own tcgen05 ops and thread 0 gives in-flight TMA copies a bounded grace period, so
-  // nothing lands in shared memory or TMEM after the CTA has released them.
-  __syncthreads();
+  // nothing lands in shared memory or TMEM after the CTA has released them.  A CTA pair
+  // leaves together: neither exits while the other may still signal its barriers.
+  if constexpr (CL == 2) {
+    cluster_sync();
+  } else {
+    __syncthreads();
+  }
   if (*abort_flag) {
     if (threadIdx.x == 32) {
       umma_commit(drain);
@@ -611,20 +686,53 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
 
 // ctas_per_sm > 1 only for instantiations whose ring and TMEM both fit that many times on an
 // SM (shared memory <= 227 KB / ctas_per_sm, TMEM columns <= 512 / ctas_per_sm), so that no
-// CTA can wait on another's TMEM allocation.
-template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int CTAS_PER_SM = 1>
+// CTA can wait on another's TMEM allocation.  CL = 2 launches clusters of two CTAs that share
+// B tiles by multicast; the grid is as many clusters as can be resident at once.
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int CTAS_PER_SM = 1,
+          int CL = 1>
 int launch_gemm(const GemmParams& P, cudaStream_t stream) {
   using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES>;
   static_assert(CTAS_PER_SM * C::TMEM_COLS <= 512, "TMEM of co-resident CTAs");
   static_assert(CTAS_PER_SM * (C::SMEM_BYTES + 1024) <= 232448, "shared memory per SM");
   static_assert(CTAS_PER_SM > 1 || C::SMEM_BYTES > 232448 / 2,
                 "a single-CTA ring must be large enough to keep a second CTA off the SM");
-  auto kern = gemm_kernel<BN, NB, A_MN, B_MN, EPI, STAGES>;
+  static_assert(CL == 1 || CTAS_PER_SM == 1, "clusters of single-CTA-per-SM kernels");
+  auto kern = gemm_kernel<BN, NB, A_MN, B_MN, EPI, STAGES, CL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return static_cast<int>(e);
-  kern<<<CTAS_PER_SM * num_sms(), 256, C::SMEM_BYTES, stream>>>(P);
-  return static_cast<int>(cudaGetLastError());
+  if constexpr (CL == 1) {
+    kern<<<CTAS_PER_SM * num_sms(), 256, C::SMEM_BYTES, stream>>>(P);
+    return static_cast<int>(cudaGetLastError());
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static int clusters_cache[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int nclusters = (dev >= 0 && dev < 64) ? clusters_cache[dev] : 0;
+    if (nclusters <= 0) {
+      cfg.gridDim = dim3(CL * (num_sms() / CL), 1, 1);
+      e = cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg);
+      if (e != cudaSuccess) return static_cast<int>(e);
+      if (nclusters <= 0) return static_cast<int>(cudaErrorInvalidConfiguration);
+      nclusters = min(nclusters, num_sms() / CL);
+      if (dev >= 0 && dev < 64) clusters_cache[dev] = nclusters;
+    }
+    cfg.gridDim = dim3(CL * nclusters, 1, 1);
+    e = cudaLaunchKernelEx(&cfg, kern, P);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    return static_cast<int>(cudaGetLastError());
+  }
 }
 
 }  // namespace moe

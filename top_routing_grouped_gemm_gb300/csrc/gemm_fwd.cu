@@ -3,8 +3,12 @@
 
 namespace moe {
 
-int launch_gemm_router(const GemmParams& P, int bn, cudaStream_t s) {
-  if (bn == 224) return launch_gemm<224, 1, false, false, EPI_F32_BIAS, 4>(P, s);
+// pairs: clusters of two CTAs on consecutive token tiles sharing each B tile by multicast
+int launch_gemm_router(const GemmParams& P, int bn, bool pairs, cudaStream_t s) {
+  if (bn == 224) {
+    if (pairs) return launch_gemm<224, 1, false, false, EPI_F32_BIAS, 4, 1, 2>(P, s);
+    return launch_gemm<224, 1, false, false, EPI_F32_BIAS, 4>(P, s);
+  }
   return launch_gemm<128, 1, false, false, EPI_F32_BIAS, 6>(P, s);
 }
 

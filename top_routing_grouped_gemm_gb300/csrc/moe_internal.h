@@ -55,6 +55,7 @@ struct GemmParams {
   // Dense (group_off == nullptr): one group of M rows, m_tiles tiles.
   const int* group_off;
   const int* tile_off;
+  const int* pair_off;   // CTA-pair launches: prefix over groups of ceil(m-tiles / 2)
   int G;
   int M;
   int m_tiles;
@@ -80,6 +81,7 @@ struct GemmParams {
   int gather_rows;
   const void* gather_src;
   int gather_ld;
+  int b_policy;             // L2 policy of B loads: 0 evict-first (streamed), 1 normal (reused)
   int* dev_status;
 };
 
@@ -91,15 +93,17 @@ int encode_map_mnmajor(CUtensorMap* map, const void* base, uint64_t mn_extent,
 int num_sms();
 
 // Kernel launchers (gemm_kernels.cu).  Return cudaError_t as int.
-int launch_gemm_router(const GemmParams& P, int bn, cudaStream_t s);  // BN=128|224, NB=1
-int launch_gemm_gateup(const GemmParams& P, cudaStream_t s);        // BN=128, NB=2, SwiGLU
-int launch_gemm_down(const GemmParams& P, cudaStream_t s);          // BN=256, NB=1
+// pairs: clusters of two CTAs sharing B by multicast (the B map then uses half-height
+// boxes: BN/2 rows)
+int launch_gemm_router(const GemmParams& P, int bn, bool pairs, cudaStream_t s);  // BN 128|224
+int launch_gemm_gateup(const GemmParams& P, cudaStream_t s);  // BN=128, NB=2, SwiGLU
+int launch_gemm_down(const GemmParams& P, cudaStream_t s);    // BN=256, NB=1, gate scale
 int launch_gemm_lora_u2(const GemmParams& P, int r, cudaStream_t s); // BN=r pad, NB=2
 int launch_gemm_lora_u1(const GemmParams& P, int r, cudaStream_t s); // BN=r pad, NB=1
 
 // Backward instantiations (gemm_bwd.cu).  B operands MN-major (weights used transposed).
-int launch_gemm_bwd_dh(const GemmParams& P, cudaStream_t s);         // BN=128, SwiGLU bwd
-int launch_gemm_bwd_dx(const GemmParams& P, cudaStream_t s);         // BN=256, store bf16
+int launch_gemm_bwd_dh(const GemmParams& P, cudaStream_t s);  // BN=128, SwiGLU bwd
+int launch_gemm_bwd_dx(const GemmParams& P, cudaStream_t s);  // BN=256, store bf16
 int launch_gemm_bwd_lora_v(const GemmParams& P, int r, cudaStream_t s);  // BN=r pad, scale
 // LoRA weight gradients, grouped over K (rows of each expert); A and B MN-major.
 int launch_gemm_wgrad(const GemmParams& P, int r, int nb, cudaStream_t s);

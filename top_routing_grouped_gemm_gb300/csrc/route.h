@@ -32,7 +32,7 @@ int launch_dispatch(const int32_t* idx, const __nv_bfloat16* x, int T, int d, in
                     int32_t* local_rank, int32_t* chunk_cnt, int32_t* dev_status,
                     cudaStream_t s);
 int launch_tile_schedule(const int32_t* offsets, int E, int rows_max, int32_t* tile_off,
-                         int32_t* dev_status, cudaStream_t s);
+                         int32_t* pair_off, int32_t* dev_status, cudaStream_t s);
 int launch_combine(const __nv_bfloat16* y_perm, const int32_t* slot_row, int T, int d, int k,
                    __nv_bfloat16* y, cudaStream_t s);
 int launch_combine_bwd(const __nv_bfloat16* dy, const __nv_bfloat16* y_perm,
