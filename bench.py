@@ -94,6 +94,24 @@ def profiled_traffic(kernel, workload):
         return None
 
 
+# ------------------------------------------------------------------------ multi-rank
+
+def max_over_ranks(v, world, device):
+    """Largest per-rank value (the step time the whole job waits for)."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, units_per_rank, ms_step):
+    """Whole-job rate: every rank processes its own batch of units (weak scaling)."""
+    return world * units_per_rank / (ms_step * 1e-3)
+
+
 # ------------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -315,12 +333,6 @@ def main():
         if world > 1:
             dist.barrier()
 
-    def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
 
     cfg = synth.config(args.workload)
     train = cfg.backward
@@ -426,7 +438,7 @@ def main():
         kernel_timed_steps()
         torch.cuda.synchronize()
     clocks.stop()
-    ms_step = max_over_ranks(start.elapsed_time(end) / K)
+    ms_step = max_over_ranks(start.elapsed_time(end) / K, world, "cuda")
     kern_us = {n: 1000.0 * sum(a.elapsed_time(b2) for a, b2 in ev[n]) / K for n in kernels}
 
     pk = peaks()
@@ -525,7 +537,7 @@ def main():
     e2.record(stream)
     torch.cuda.synchronize()
     barrier()
-    ms_e2e = max_over_ranks(s2.elapsed_time(e2) / K)
+    ms_e2e = max_over_ranks(s2.elapsed_time(e2) / K, world, "cuda")
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not cfg.prepermuted and not train:
@@ -535,7 +547,7 @@ def main():
         units = cfg.T * cfg.k if cfg.prepermuted else cfg.T
         line = {
             "metric": METRIC,
-            "value": world * units / (ms_step * 1e-3),
+            "value": job_throughput(world, units, ms_step),
             "unit": "token-slots/s" if cfg.prepermuted else "tokens/s",
             "n_gpus": world,
             "steps": K,
@@ -554,7 +566,7 @@ def main():
                              "kernels": gemms, "kept_rows": kept, "nonempty_experts": nonempty},
             "roofline": roof,
             "kernels": kstats,
-            "e2e": {"value": world * units / (ms_e2e * 1e-3),
+            "e2e": {"value": job_throughput(world, units, ms_e2e),
                     "unit": "token-slots/s" if cfg.prepermuted else "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,

@@ -281,6 +281,12 @@ enum moe_kernel_id {
 int moe_set_kernel_events(int kernel_id, void* event_before, void* event_after);
 long long moe_launch_count(void);
 
+/* Self-test of the bounded waits: launches one tiny kernel that waits on an mbarrier nothing
+ * arrives on, gives up after timeout_ms (1..2000) and writes MOE_ERR_TIMEOUT to *dev_status,
+ * exactly as a stalled pipeline stage of a GEMM would.  The kernel ends on its own; the
+ * context stays usable. */
+int moe_selftest_wait_timeout(int32_t* dev_status, int32_t timeout_ms, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

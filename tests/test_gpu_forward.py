@@ -248,3 +248,17 @@ def test_full_c4_lora_shard_sampled_rows():
         sel += rr
         refs.append(f64(inp["gates"][rr])[:, None] * o)
     assert relerr(f64(y[sel]), np.concatenate(refs)) <= RTOL_FP
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait that nothing will ever satisfy gives up after its limit, reports
+    MOE_ERR_TIMEOUT through the status word, and the context keeps working."""
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_selftest_wait_timeout(st, 20)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 5  # MOE_ERR_TIMEOUT
+    # the same context still runs the layer correctly afterwards
+    cfg = small_cfg(T=64)
+    inp = synth.make_inputs(cfg, "cpu")
+    buf = run_forward(moe.problem_of(cfg), to_dev(inp))
+    assert int(buf.dev_status.item()) == 0

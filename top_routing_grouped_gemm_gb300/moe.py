@@ -86,6 +86,7 @@ _SIGS = {
     "moe_route_bwd": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "moe_set_kernel_events": (ctypes.c_int, [ctypes.c_int, c_vp, c_vp]),
     "moe_launch_count": (ctypes.c_longlong, []),
+    "moe_selftest_wait_timeout": (ctypes.c_int, [c_vp, c_i32, c_vp]),
 }
 
 KERNEL_IDS = {"router_gemm": 0, "topk": 1, "dispatch": 2, "gateup_gemm": 3, "down_gemm": 4,
@@ -312,6 +313,11 @@ def moe_set_kernel_events(kernel, before, after):
 
 def moe_launch_count() -> int:
     return lib().moe_launch_count()
+
+
+def moe_selftest_wait_timeout(dev_status, timeout_ms, stream=None):
+    _check("moe_selftest_wait_timeout",
+           lib().moe_selftest_wait_timeout(_ptr(dev_status), timeout_ms, _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- layer helpers
