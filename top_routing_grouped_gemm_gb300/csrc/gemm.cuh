@@ -627,9 +627,17 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
                 for (int i = 0; i < 16; ++i)
                   if (col + i < P.N) base[static_cast<size_t>(col + i) * P.M + m] = v[i];
               } else {
+                float* dst = base + static_cast<size_t>(m) * P.N + col;
+                if (col + 16 <= P.N && (P.N & 3) == 0) {
+                  // the thread's row is contiguous: 16-byte stores
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                  if (col + i < P.N) base[static_cast<size_t>(m) * P.N + col + i] = v[i];
+                  for (int i = 0; i < 16; i += 4)
+                    *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 16; ++i)
+                    if (col + i < P.N) dst[i] = v[i];
+                }
               }
             }
           }
