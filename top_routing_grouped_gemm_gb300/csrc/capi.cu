@@ -574,7 +574,7 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
       P.nseg = 2;
     }
     grouped(P);
-    P.n_tiles = (F + 127) / 128;
+    P.n_tiles = (F + 255) / 256;
     P.N = F;
     P.ldo = F;
     P.in0 = saved->a_gate;

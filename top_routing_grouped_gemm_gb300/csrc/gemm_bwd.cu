@@ -6,7 +6,7 @@ namespace moe {
 
 // dh = dz W_d (+ v'_d A_d), epilogue: SwiGLU backward -> da_g, da_u
 int launch_gemm_bwd_dh(const GemmParams& P, cudaStream_t s) {
-  return launch_gemm<128, 1, false, true, EPI_SWIGLU_BWD, 6>(P, s);
+  return launch_gemm<256, 1, false, true, EPI_SWIGLU_BWD, 4>(P, s);
 }
 
 // dx_perm = da_g W_g + da_u W_u (+ v'_g A_g + v'_u A_u)
@@ -17,7 +17,7 @@ int launch_gemm_bwd_dx(const GemmParams& P, cudaStream_t s) {
 // v' = s (dz B_d), s (da_g B_g), s (da_u B_u): N = r (<= 64, zero-filled to 64)
 int launch_gemm_bwd_lora_v(const GemmParams& P, int r, cudaStream_t s) {
   (void)r;
-  return launch_gemm<64, 1, false, true, EPI_SCALE, 8>(P, s);
+  return launch_gemm<64, 1, false, true, EPI_SCALE, 9>(P, s);
 }
 
 // LoRA weight gradients, reduction over each expert's rows

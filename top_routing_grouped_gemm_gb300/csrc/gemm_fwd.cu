@@ -21,15 +21,15 @@ int launch_gemm_down(const GemmParams& P, cudaStream_t s) {
 }
 
 int launch_gemm_lora_u2(const GemmParams& P, int r, cudaStream_t s) {
-  if (r <= 16) return launch_gemm<16, 2, false, false, EPI_SCALE, 8>(P, s);
-  if (r <= 32) return launch_gemm<32, 2, false, false, EPI_SCALE, 8>(P, s);
+  if (r <= 16) return launch_gemm<16, 2, false, false, EPI_SCALE, 10>(P, s);
+  if (r <= 32) return launch_gemm<32, 2, false, false, EPI_SCALE, 9>(P, s);
   return launch_gemm<64, 2, false, false, EPI_SCALE, 6>(P, s);
 }
 
 int launch_gemm_lora_u1(const GemmParams& P, int r, cudaStream_t s) {
-  if (r <= 16) return launch_gemm<16, 1, false, false, EPI_SCALE, 8>(P, s);
-  if (r <= 32) return launch_gemm<32, 1, false, false, EPI_SCALE, 8>(P, s);
-  return launch_gemm<64, 1, false, false, EPI_SCALE, 8>(P, s);
+  if (r <= 16) return launch_gemm<16, 1, false, false, EPI_SCALE, 11>(P, s);
+  if (r <= 32) return launch_gemm<32, 1, false, false, EPI_SCALE, 10>(P, s);
+  return launch_gemm<64, 1, false, false, EPI_SCALE, 9>(P, s);
 }
 
 }  // namespace moe
