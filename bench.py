@@ -492,39 +492,78 @@ def main():
             y_host.copy_(y_perm, non_blocking=True)
         h2d, d2h = out_bytes
     else:
+        # Serving loop: each step copies its tokens in from pinned host memory and its
+        # output (and aux loss; dx for training) back out.  Two buffer sets alternate and the
+        # copies run on a copy stream, so step i's copies overlap the neighbours' compute.
+        copy_stream = torch.cuda.Stream()
+        main_stream = torch.cuda.current_stream()
+        bufs = [buf, moe.LayerBuffers(p, "cuda", train=train, keep_logits=train)]
         x_host = inp["x"].cpu().pin_memory()
-        y_host = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16).pin_memory()
-        aux_host = torch.empty((1,), dtype=torch.float32).pin_memory()
-        x_dev = torch.empty_like(inp["x"])
+        x_dev = [torch.empty_like(inp["x"]) for _ in range(2)]
+        y_host = [torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        aux_host = [torch.empty((1,), dtype=torch.float32).pin_memory() for _ in range(2)]
         if train:
             dy_host = inp["dy"].cpu().pin_memory()
-            dy_dev = torch.empty_like(inp["dy"])
-            dx_host = torch.empty((cfg.T, cfg.d), dtype=torch.float32).pin_memory()
+            dy_dev = [torch.empty_like(inp["dy"]) for _ in range(2)]
+            dx_host = [torch.empty((cfg.T, cfg.d), dtype=torch.float32).pin_memory() for _ in range(2)]
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        ev_back = [torch.cuda.Event() for _ in range(2)]
+
+        def e2e_run(n):
+            copy_stream.wait_stream(main_stream)
+            with torch.cuda.stream(copy_stream):
+                x_dev[0].copy_(x_host, non_blocking=True)
+                if train:
+                    dy_dev[0].copy_(dy_host, non_blocking=True)
+                ev_in[0].record(copy_stream)
+            for i in range(n):
+                cur, nxt = i % 2, 1 - i % 2
+                main_stream.wait_event(ev_in[cur])
+                if i >= 2:
+                    main_stream.wait_event(ev_back[cur])  # step i-2's outputs copied out
+                moe.layer_forward(bufs[cur], x_dev[cur], inp["w_router"], inp["bias"],
+                                  inp["w_gate"], inp["w_up"], inp["w_down"], lora, gather=fused)
+                if train:
+                    moe.layer_backward(bufs[cur], dy_dev[cur], x_dev[cur], inp["w_router"],
+                                       inp["w_gate"], inp["w_up"], inp["w_down"], lora)
+                ev_out[cur].record(main_stream)
+                with torch.cuda.stream(copy_stream):
+                    if i + 1 < n:
+                        if i >= 1:
+                            copy_stream.wait_event(ev_out[nxt])  # step i-1 done with x_dev[nxt]
+                        x_dev[nxt].copy_(x_host, non_blocking=True)
+                        if train:
+                            dy_dev[nxt].copy_(dy_host, non_blocking=True)
+                        ev_in[nxt].record(copy_stream)
+                    copy_stream.wait_event(ev_out[cur])
+                    y_host[cur].copy_(bufs[cur].y, non_blocking=True)
+                    aux_host[cur].copy_(bufs[cur].aux, non_blocking=True)
+                    if train:
+                        dx_host[cur].copy_(bufs[cur].dx, non_blocking=True)
+                    ev_back[cur].record(copy_stream)
+            main_stream.wait_stream(copy_stream)
 
         def e2e_step():
-            x_dev.copy_(x_host, non_blocking=True)
-            moe.layer_forward(buf, x_dev, inp["w_router"], inp["bias"], inp["w_gate"],
-                              inp["w_up"], inp["w_down"], lora,
-                              gather=fused)
-            y_host.copy_(buf.y, non_blocking=True)
-            aux_host.copy_(buf.aux, non_blocking=True)
-            if train:
-                dy_dev.copy_(dy_host, non_blocking=True)
-                moe.layer_backward(buf, dy_dev, x_dev, inp["w_router"], inp["w_gate"],
-                                   inp["w_up"], inp["w_down"], lora)
-                dx_host.copy_(buf.dx, non_blocking=True)
+            e2e_run(1)
         h2d = cfg.T * cfg.d * 2 * (2 if train else 1)
         d2h = cfg.T * cfg.d * 2 + 4 + (cfg.T * cfg.d * 4 if train else 0)
 
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
+    def e2e_all():
+        if cfg.prepermuted:
+            for _ in range(K):
+                e2e_step()
+        else:
+            e2e_run(K)
+
     g2 = None
     if args.graph:
         g2 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g2, capture_error_mode="relaxed"):
-            for _ in range(K):
-                e2e_step()
+            e2e_all()
         torch.cuda.synchronize()
     barrier()
     s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -532,8 +571,7 @@ def main():
     if g2 is not None:
         g2.replay()
     else:
-        for _ in range(K):
-            e2e_step()
+        e2e_all()
     e2.record(stream)
     torch.cuda.synchronize()
     barrier()
