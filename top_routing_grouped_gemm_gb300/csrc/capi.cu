@@ -167,7 +167,7 @@ int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, co
   // per flop), else 128
   const int bn = (E % 224 == 0) ? 224 : 128;
   // clusters of two CTAs on consecutive token tiles share each weight tile by multicast
-  const bool pairs = bn == 224 && T > kBM;
+  const bool pairs = bn == 224 && T >= 8192;  // measured: no gain for few token tiles
   GemmParams P = gemm_params();
   MOE_TRY(encode_map_kmajor(&P.maps[0], x, d, T, 1, kBM));
   MOE_TRY(encode_map_kmajor(&P.maps[1], w_split, d, E, 2, pairs ? bn / 2 : bn));

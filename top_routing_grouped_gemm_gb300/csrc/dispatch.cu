@@ -244,30 +244,8 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&a)[8]) {
   return o;
 }
 
-// Sum of the bf16 rows rows[0..k-1] (negative = skipped) at vector v, in rank order, fp32.
-// The loads of a batch of 16 rows are issued back to back before any is used, so every
-// thread keeps up to 16 independent 16-byte loads in flight.
-__device__ __forceinline__ void sum_rows_bf16x8(const uint4* __restrict__ src, const int* rows,
-                                                int k, int nvec, int v, float (&acc)[8]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (int j0 = 0; j0 < k; j0 += 16) {
-    uint4 val[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int r = (j0 + j < k) ? rows[j0 + j] : -1;
-      val[j] = r >= 0 ? src[static_cast<size_t>(r) * nvec + v] : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int r = (j0 + j < k) ? rows[j0 + j] : -1;
-      if (r >= 0) add_bf16x8(acc, val[j], 1.f);
-    }
-  }
-}
-
 // y[t] = sum_j y_perm[slot_row[t*k+j]] (kept slots, rank order, fp32) -> bf16.  One block
-// per token, one 16-byte vector per thread.
+// per token, one 16-byte vector per thread: the k row loads are independent.
 __global__ void __launch_bounds__(kRowThreads) combine_kernel(const uint4* __restrict__ y_perm,
                                                               const int32_t* __restrict__ slot_row,
                                                               int T, int d, int k,
@@ -278,8 +256,12 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(const uint4* __res
   __syncthreads();
   const int nvec = d / 8;
   for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-    float acc[8];
-    sum_rows_bf16x8(y_perm, rows, k, nvec, v, acc);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int j = 0; j < k; ++j) {
+      const int r = rows[j];
+      if (r >= 0) add_bf16x8(acc, y_perm[static_cast<size_t>(r) * nvec + v], 1.f);
+    }
     y[static_cast<size_t>(t) * nvec + v] = pack_bf16x8(acc);
   }
 }
@@ -335,8 +317,12 @@ __global__ void __launch_bounds__(kRowThreads) dispatch_bwd_kernel(
   __syncthreads();
   const int nvec = d / 8;
   for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-    float acc[8];
-    sum_rows_bf16x8(dx_perm, rows, k, nvec, v, acc);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int j = 0; j < k; ++j) {
+      const int r = rows[j];
+      if (r >= 0) add_bf16x8(acc, dx_perm[static_cast<size_t>(r) * nvec + v], 1.f);
+    }
     float4* o = dx + (static_cast<size_t>(t) * nvec + v) * 2;
     o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);

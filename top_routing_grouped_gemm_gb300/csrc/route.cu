@@ -81,7 +81,7 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
 // Each warp accumulates the softmax probabilities of its tokens into its own shared-memory
 // row; the block then writes one row of per-block sums (fixed order: deterministic).
 template <int VPL>
-__global__ void __launch_bounds__(256) topk_softmax_kernel(
+__global__ void __launch_bounds__(256, 3) topk_softmax_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_gate, float* __restrict__ partials) {
   constexpr int WARPS = 8;
