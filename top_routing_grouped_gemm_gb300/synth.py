@@ -65,8 +65,8 @@ CONFIGS = {
     "c5": MoEConfig("c5", T=8192, d=4096, E=896, k=16, F=1024, r=32, alpha=64.0,
                     backward=True),
     # small case of the c2 kernels for hardware-counter captures (0.8 GB of weights, about
-    # 128 rows per expert): same shapes per expert, fewer experts and tokens
-    "c2_small": MoEConfig("c2_small", T=1024, d=2048, E=128, k=16, F=512),
+    # 80 rows per expert like c2's 73): same shapes per expert, fewer experts and tokens
+    "c2_small": MoEConfig("c2_small", T=640, d=2048, E=128, k=16, F=512),
     # small case of the c5 kernels (3.2 GB of expert weights, about 256 rows per expert)
     "c5_small": MoEConfig("c5_small", T=2048, d=4096, E=128, k=16, F=1024, r=32, alpha=64.0,
                           backward=True),
