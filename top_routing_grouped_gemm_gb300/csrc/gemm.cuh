@@ -333,6 +333,12 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, A_MN, B_MN);
+    // Two B operands sit back to back in the stage (K-major: the second's rows follow the
+    // first's BN rows; MN-major: its 64-wide boxes follow the first's, 8 KB apart), so when
+    // both are enabled one MMA of N = 2*BN covers both accumulators (columns [0, BN) and
+    // [BN, 2*BN)), halving the MMA count.
+    constexpr bool kJoinB = (NB == 2) && (2 * BN <= 256) && (!B_MN || BN % 64 == 0);
+    constexpr uint32_t idesc2 = idesc_bf16_f32(kBM, kJoinB ? 2 * BN : BN, A_MN, B_MN);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -380,6 +386,13 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
               const uint64_t adesc = A_MN ? smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
                                           : smem_desc_sw128(a_addr + k * 32, 16, 1024);
               const uint32_t accumulate = (s > 0 || kb > 0 || k > 0) ? 1u : 0u;
+              if (kJoinB && sg.b_map[0] >= 0 && sg.b_map[1] >= 0) {
+                const uint32_t b_addr = a_addr + C::A_BYTES;
+                const uint64_t bdesc = B_MN ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                            : smem_desc_sw128(b_addr + k * 32, 16, 1024);
+                umma_bf16(d_base, adesc, bdesc, idesc2, accumulate);
+                continue;
+              }
 #pragma unroll
               for (int b = 0; b < NB; ++b) {
                 if (sg.b_map[b] < 0) continue;
