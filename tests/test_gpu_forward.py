@@ -68,9 +68,13 @@ def small_cfg(**kw):
     small_cfg(T=300, d=256, E=12, k=3, F=192, r=64, alpha=128.0),
     small_cfg(T=300, d=256, E=12, k=3, F=192, r=8, alpha=16.0, cap_num=1, cap_den=2),
     small_cfg(T=40, d=192, E=500, k=8, F=128, zipf_bias=True),
+    # groups of over 1024 rows on average: the expert GEMMs run on 256-row tiles
+    small_cfg(T=2600, d=192, E=4, k=2, F=192),
+    small_cfg(T=2200, d=256, E=2, k=1, F=320, r=16, alpha=32.0),
+    small_cfg(T=3000, d=128, E=4, k=2, F=128, cap_num=3, cap_den=4, zipf_bias=True),
 ], ids=["c1", "small", "small_capacity_bias", "small_lora", "ragged_lora_capacity", "single_expert",
         "one_token", "capacity_zero", "max_experts_k32", "k_equals_E", "lora_r64", "lora_r8_half_capacity",
-        "mostly_empty_experts"])
+        "mostly_empty_experts", "big_groups", "big_groups_lora", "big_groups_capacity"])
 def test_layer_forward_whole(cfg):
     inp = synth.make_inputs(cfg, "cpu")
     dev = to_dev(inp)
@@ -241,7 +245,8 @@ def test_full_c4_lora_shard_sampled_rows():
     sel, refs = [], []
     for e in range(p.E):
         lo, hi = int(offs[e]), int(offs[e + 1])
-        rr = sorted(set([lo, hi - 1, lo + 127, lo + 128] + list(rng.integers(lo, hi, 2))))
+        rr = sorted(set([lo, hi - 1, lo + 127, lo + 128, lo + 255, lo + 256, hi - 129] +
+                        list(rng.integers(lo, hi, 2))))
         Wg, Wu, Wd, L = W(e)
         X = f64(inp["x_perm"][rr])
         o = oracle.expert_forward(X, Wg, Wu, Wd, L, p.lora_scale)[3]

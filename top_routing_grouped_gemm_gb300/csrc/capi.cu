@@ -59,6 +59,14 @@ bool weights_reused(const moe_problem* p, int rows_max) {
          (C < 0 || C > kBM);
 }
 
+// Groups average at least 1024 rows (8 m-tiles): the first-layer and down GEMMs then run on
+// 256-row tiles, whose exposed epilogue (one TMEM accumulator) is small next to the time
+// saved by staging each weight tile once per 256 rows.
+bool big_groups(const moe_problem* p, int rows_max) {
+  const int C = capacity_of(p);
+  return static_cast<long long>(rows_max) >= 1024ll * p->E && (C < 0 || C >= 1024);
+}
+
 struct Carver {
   uint8_t* base;
   size_t used;
@@ -273,6 +281,7 @@ int expert_ffn_impl(const moe_problem* p, int32_t rows_max, const moe_bf16* a_sr
   int32_t* tile_off = cv.take<int32_t>(E + 1);
   int32_t* pair_off = cv.take<int32_t>(E + 1);
   const int b_policy = weights_reused(p, rows_max) ? 1 : 0;
+  const bool m256 = !gather && big_groups(p, rows_max);
   moe_bf16 *u_g = nullptr, *u_u = nullptr, *u_d = nullptr;
   if (r) {
     u_g = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * r);
@@ -355,7 +364,7 @@ int expert_ffn_impl(const moe_problem* p, int32_t rows_max, const moe_bf16* a_sr
     P.out2 = saved ? saved->a_up : nullptr;
     P.ldo = F;
     mark_before(MOE_KERNEL_GATEUP_GEMM, stream);
-    MOE_CUDA(launch_gemm_gateup(P, stream));
+    MOE_CUDA(launch_gemm_gateup(P, m256, stream));
     mark_after(MOE_KERNEL_GATEUP_GEMM, stream);
   }
   // LoRA down-projection of h: u_d = s h A_d^T
@@ -397,7 +406,7 @@ int expert_ffn_impl(const moe_problem* p, int32_t rows_max, const moe_bf16* a_sr
     P.gate = topk_gate;
     P.row_slot = row_slot;
     mark_before(MOE_KERNEL_DOWN_GEMM, stream);
-    MOE_CUDA(launch_gemm_down(P, stream));
+    MOE_CUDA(launch_gemm_down(P, m256, stream));
     mark_after(MOE_KERNEL_DOWN_GEMM, stream);
   }
   count_launches(use_lora ? 5 : 3);

@@ -21,21 +21,26 @@
 
 namespace moe {
 
-template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES>
+// MSUB: 128-row A subtiles per CTA tile (2: two consecutive m-tiles of one group share every
+// B stage).  NACC: TMEM accumulator buffers (2 overlaps a tile's epilogue with the next
+// tile's main loop; 1 when two buffers do not fit the 512 TMEM columns).
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int MSUB = 1>
 struct GemmCfg {
-  static constexpr int A_BYTES = kBM * kBK * 2;
+  static constexpr int A_SUB_BYTES = kBM * kBK * 2;
+  static constexpr int A_BYTES = MSUB * A_SUB_BYTES;
   // an MN-major B tile is always whole 64-wide TMA boxes (N below 64 is zero-filled)
   static constexpr int B_BYTES = (B_MN ? ((BN + 63) / 64) * 64 : BN) * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
-  static constexpr int ACC_COLS = NB * BN;
-  static constexpr int TMEM_COLS = (2 * ACC_COLS <= 32)    ? 32
-                                   : (2 * ACC_COLS <= 64)  ? 64
-                                   : (2 * ACC_COLS <= 128) ? 128
-                                   : (2 * ACC_COLS <= 256) ? 256
-                                                           : 512;
+  static constexpr int ACC_COLS = MSUB * NB * BN;
+  static constexpr int NACC = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int TMEM_COLS = (NACC * ACC_COLS <= 32)    ? 32
+                                   : (NACC * ACC_COLS <= 64)  ? 64
+                                   : (NACC * ACC_COLS <= 128) ? 128
+                                   : (NACC * ACC_COLS <= 256) ? 256
+                                                              : 512;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
-  static_assert(2 * ACC_COLS <= 512, "two accumulators must fit in TMEM");
+  static_assert(NACC * ACC_COLS <= 512, "accumulators must fit in TMEM");
   static_assert(!B_MN || BN % 64 == 0, "MN-major B is read in whole 64-wide boxes");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
 };
@@ -136,6 +141,19 @@ __device__ __forceinline__ bool decode_pair_tile(const GemmParams& P, int pt, in
   return true;
 }
 
+// Two-subtile launches (MSUB = 2): unit `pt` covers m-tiles 2*pair and 2*pair+1 of one
+// (group, n-tile) in one CTA (rows_valid up to 256); the second subtile is skipped when the
+// group's rows end inside the first.
+__device__ __forceinline__ bool decode_sub_tile(const GemmParams& P, int pt, TileCoord& tc) {
+  if (!decode_pair_tile(P, pt, 0, tc)) return false;
+  if (P.group_off == nullptr) {
+    tc.rows_valid = min(2 * kBM, P.M - tc.row0);
+  } else {
+    tc.rows_valid = min(2 * kBM, __ldg(&P.group_off[tc.g + 1]) - tc.row0);
+  }
+  return true;
+}
+
 // Zero the K rows [valid, 64) of an MN-major operand tile of `chunks` 64-wide boxes (each K
 // row is one 128-byte line of a box), by the 32 lanes of one warp.
 __device__ __forceinline__ void zero_k_tail(uint8_t* tile, int chunks, int valid, int lane) {
@@ -183,7 +201,7 @@ __device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* src, float (&v
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
-template <int EPI, int CL>
+template <int EPI, int CL, int MSUB>
 __device__ __forceinline__ bool next_tile(const GemmParams& P, int tile, int rank,
                                           TileCoord& tc, KRange& kr) {
   if constexpr (EPI == EPI_WGRAD) {
@@ -193,13 +211,16 @@ __device__ __forceinline__ bool next_tile(const GemmParams& P, int tile, int ran
     kr.nrows = 0;
     kr.nkb = 0;
     if constexpr (CL == 2) return decode_pair_tile(P, tile, rank, tc);
+    if constexpr (MSUB == 2) return decode_sub_tile(P, tile, tc);
     return decode_tile(P, tile, tc);
   }
 }
 
-template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int CL>
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int CL, int MSUB>
 __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmParams P) {
-  using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES>;
+  using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB>;
+  static_assert(MSUB == 1 || (CL == 1 && EPI != EPI_WGRAD && !A_MN),
+                "two subtiles: single CTA, M-grouped or dense, K-major A");
   static_assert(CL == 1 || (EPI != EPI_WGRAD && !A_MN), "CTA pairs: M-grouped, K-major A");
   static_assert(CL == 1 || B_MN || (BN / 2) % 8 == 0, "half B tiles stay swizzle-aligned");
   extern __shared__ uint8_t smem_raw[];
@@ -224,7 +245,8 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
   if (threadIdx.x == 0) {
     // with a gathered A operand a stage is full after the producer's expect-tx arrival
     // (B bytes) and one arrival of the gather warp that filled its A tile
-    const uint32_t full_count = (P.gather_slot != nullptr) ? 2u : 1u;
+    const uint32_t full_count =
+        (!A_MN && EPI != EPI_WGRAD && MSUB == 1 && P.gather_slot != nullptr) ? 2u : 1u;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], full_count);
       mbar_init(&empty[s], CL);  // a stage is free once every CTA that reads it released it
@@ -264,7 +286,7 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
     bool ok = true;
     TileCoord tc;
     KRange kr;
-    for (int tile = unit0; ok && next_tile<EPI, CL>(P, tile, rank, tc, kr); tile += unit_step) {
+    for (int tile = unit0; ok && next_tile<EPI, CL, MSUB>(P, tile, rank, tc, kr); tile += unit_step) {
       const int nseg = (EPI == EPI_WGRAD) ? 1 : P.nseg;
       for (int s = 0; ok && s < nseg; ++s) {
         const GemmSeg& sg = P.seg[s];
@@ -279,15 +301,20 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
           const bool ghost = (CL == 2) && tc.rows_valid == 0;
           if (lane == 0) {
             // B: the whole tile lands here (half of it from the other CTA of a pair)
-            uint32_t bytes = (sg.a_gather || ghost) ? 0u : C::A_BYTES;
+            const int nsub = (MSUB == 2 && tc.rows_valid > kBM) ? 2 : 1;
+            uint32_t bytes = (sg.a_gather || ghost) ? 0u : nsub * C::A_SUB_BYTES;
 #pragma unroll
             for (int b = 0; b < NB; ++b) bytes += (sg.b_map[b] >= 0) ? C::B_BYTES : 0;
             mbar_arrive_expect_tx(&full[stage], bytes);
           }
           if (lane == 0) {
             if (!A_MN) {
-              if (!sg.a_gather && !ghost)
+              if (!sg.a_gather && !ghost) {
                 tma_load_3d(sA, &P.maps[sg.a_map], &full[stage], ka, tc.row0, 0, pol_a);
+                if (MSUB == 2 && tc.rows_valid > kBM)
+                  tma_load_3d(sA + C::A_SUB_BYTES, &P.maps[sg.a_map], &full[stage], ka,
+                              tc.row0 + kBM, 0, pol_a);
+              }
             } else {
               tma_load_3d(sA, &P.maps[sg.a_map], &full[stage], tc.row0, ka, 0, pol_a);
               tma_load_3d(sA + 8192, &P.maps[sg.a_map], &full[stage], tc.row0 + 64, ka, 0,
@@ -346,7 +373,7 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
     bool ok = true;
     TileCoord tc;
     KRange kr;
-    for (int tile = unit0; ok && next_tile<EPI, CL>(P, tile, rank, tc, kr); tile += unit_step) {
+    for (int tile = unit0; ok && next_tile<EPI, CL, MSUB>(P, tile, rank, tc, kr); tile += unit_step) {
       int w = 1;
       if (lane == 0) w = mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag) ? 1 : 0;
       w = __shfl_sync(0xffffffffu, w, 0);
@@ -380,26 +407,33 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
           if (lane == 0) {
             const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
             const bool ghost = (CL == 2) && tc.rows_valid == 0;
+            const int nsub = (MSUB == 2 && tc.rows_valid > kBM) ? 2 : 1;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
               if (ghost) break;
-              const uint64_t adesc = A_MN ? smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
-                                          : smem_desc_sw128(a_addr + k * 32, 16, 1024);
               const uint32_t accumulate = (s > 0 || kb > 0 || k > 0) ? 1u : 0u;
-              if (kJoinB && sg.b_map[0] >= 0 && sg.b_map[1] >= 0) {
-                const uint32_t b_addr = a_addr + C::A_BYTES;
-                const uint64_t bdesc = B_MN ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
-                                            : smem_desc_sw128(b_addr + k * 32, 16, 1024);
-                umma_bf16(d_base, adesc, bdesc, idesc2, accumulate);
-                continue;
-              }
 #pragma unroll
-              for (int b = 0; b < NB; ++b) {
-                if (sg.b_map[b] < 0) continue;
-                const uint32_t b_addr = a_addr + C::A_BYTES + b * C::B_BYTES;
-                const uint64_t bdesc = B_MN ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
-                                            : smem_desc_sw128(b_addr + k * 32, 16, 1024);
-                umma_bf16(d_base + b * BN, adesc, bdesc, idesc, accumulate);
+              for (int sub = 0; sub < MSUB; ++sub) {
+                if (sub >= nsub) break;
+                const uint32_t as = a_addr + sub * C::A_SUB_BYTES;
+                const uint64_t adesc = A_MN ? smem_desc_sw128(as + k * 2048, 8192, 1024)
+                                            : smem_desc_sw128(as + k * 32, 16, 1024);
+                const uint32_t d_sub = d_base + sub * NB * BN;
+                if (kJoinB && sg.b_map[0] >= 0 && sg.b_map[1] >= 0) {
+                  const uint32_t b_addr = a_addr + C::A_BYTES;
+                  const uint64_t bdesc = B_MN ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                              : smem_desc_sw128(b_addr + k * 32, 16, 1024);
+                  umma_bf16(d_sub, adesc, bdesc, idesc2, accumulate);
+                  continue;
+                }
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                  if (sg.b_map[b] < 0) continue;
+                  const uint32_t b_addr = a_addr + C::A_BYTES + b * C::B_BYTES;
+                  const uint64_t bdesc = B_MN ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                              : smem_desc_sw128(b_addr + k * 32, 16, 1024);
+                  umma_bf16(d_sub + b * BN, adesc, bdesc, idesc, accumulate);
+                }
               }
             }
             if constexpr (CL == 2) {
@@ -415,7 +449,7 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
       if (!ok) break;
       if (lane == 0) umma_commit(&acc_full[acc]);
       __syncwarp();
-      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      if (++acc == C::NACC) { acc = 0; acc_phase ^= 1; }
     }
     if (!ok && lane == 0) {
       *abort_flag = 1;
@@ -427,7 +461,7 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
     // 128 x 64 A tile of its stage with 16-byte cp.async copies of token rows (zero fill for
     // rows past the group's end) in the 128-byte-swizzled layout TMA would produce, waits for
     // them, makes them visible to the tensor core (proxy fence) and arrives on the stage.
-    if constexpr (!A_MN && EPI != EPI_WGRAD) {
+    if constexpr (!A_MN && EPI != EPI_WGRAD && MSUB == 1) {
       if (P.gather_slot != nullptr) {
         const int gw = warp - 2;
         const int part = lane & 7;      // 16-byte chunk of a 128-byte row this lane copies
@@ -439,7 +473,7 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
         bool ok = true;
         TileCoord tc;
         KRange kr;
-        for (int tile = unit0; ok && next_tile<EPI, CL>(P, tile, rank, tc, kr); tile += unit_step) {
+        for (int tile = unit0; ok && next_tile<EPI, CL, MSUB>(P, tile, rank, tc, kr); tile += unit_step) {
           int trow[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -495,20 +529,22 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
     bool ok = true;
     TileCoord tc;
     KRange kr;
-    for (int tile = unit0; next_tile<EPI, CL>(P, tile, rank, tc, kr); tile += unit_step) {
+    for (int tile = unit0; next_tile<EPI, CL, MSUB>(P, tile, rank, tc, kr); tile += unit_step) {
       int w = 1;
       if (lane == 0) w = mbar_wait(&acc_full[acc], acc_phase, abort_flag) ? 1 : 0;
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) { ok = false; break; }
       tc_fence_after();
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
-      const bool valid = r_local < tc.rows_valid;
-      const long row = static_cast<long>(tc.row0) + r_local;
+      for (int sub = 0; sub < MSUB; ++sub) {
+      // a ghost unit of a CTA pair (rows_valid 0) and a missing second subtile store nothing
+      if (tc.rows_valid <= sub * kBM) break;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             acc * C::ACC_COLS + sub * NB * BN;
+      const bool valid = r_local + sub * kBM < tc.rows_valid;
+      const long row = static_cast<long>(tc.row0) + sub * kBM + r_local;
       const int col0 = tc.n * BN;
 
-      if (tc.rows_valid == 0) {
-        // ghost unit of a CTA pair: nothing was computed, nothing to store
-      } else if constexpr (EPI == EPI_F32_BIAS) {
+      if constexpr (EPI == EPI_F32_BIAS) {
         float* out = reinterpret_cast<float*>(P.out0);
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
@@ -666,9 +702,10 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
           if (valid && col < P.N) store_bf16x16(o + row * P.ldo + col, v, P.N - col);
         }
       }
+      }  // subtiles
       tc_fence_before();
       mbar_arrive(&acc_empty[acc]);
-      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      if (++acc == C::NACC) { acc = 0; acc_phase ^= 1; }
     }
     if (!ok && lane == 0) {
       *abort_flag = 1;
@@ -710,15 +747,15 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
 // CTA can wait on another's TMEM allocation.  CL = 2 launches clusters of two CTAs that share
 // B tiles by multicast; the grid is as many clusters as can be resident at once.
 template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int CTAS_PER_SM = 1,
-          int CL = 1>
+          int CL = 1, int MSUB = 1>
 int launch_gemm(const GemmParams& P, cudaStream_t stream) {
-  using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES>;
+  using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB>;
   static_assert(CTAS_PER_SM * C::TMEM_COLS <= 512, "TMEM of co-resident CTAs");
   static_assert(CTAS_PER_SM * (C::SMEM_BYTES + 1024) <= 232448, "shared memory per SM");
   static_assert(CTAS_PER_SM > 1 || C::SMEM_BYTES > 232448 / 2,
                 "a single-CTA ring must be large enough to keep a second CTA off the SM");
   static_assert(CL == 1 || CTAS_PER_SM == 1, "clusters of single-CTA-per-SM kernels");
-  auto kern = gemm_kernel<BN, NB, A_MN, B_MN, EPI, STAGES, CL>;
+  auto kern = gemm_kernel<BN, NB, A_MN, B_MN, EPI, STAGES, CL, MSUB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return static_cast<int>(e);

@@ -12,11 +12,19 @@ int launch_gemm_router(const GemmParams& P, int bn, bool pairs, cudaStream_t s) 
   return launch_gemm<128, 1, false, false, EPI_F32_BIAS, 6>(P, s);
 }
 
-int launch_gemm_gateup(const GemmParams& P, cudaStream_t s) {
+// m256: 256-row tiles (two 128-row subtiles sharing each B stage, one TMEM accumulator) for
+// groups of many rows, where reading each B stage into shared memory once per 256 rows
+// instead of once per 128 keeps the tensor core fed; no gathered A operand.
+int launch_gemm_gateup(const GemmParams& P, bool m256, cudaStream_t s) {
+  if (m256) {
+    if (P.gather_slot != nullptr) return static_cast<int>(cudaErrorInvalidValue);
+    return launch_gemm<128, 2, false, false, EPI_SWIGLU, 3, 1, 1, 2>(P, s);
+  }
   return launch_gemm<128, 2, false, false, EPI_SWIGLU, 4>(P, s);
 }
 
-int launch_gemm_down(const GemmParams& P, cudaStream_t s) {
+int launch_gemm_down(const GemmParams& P, bool m256, cudaStream_t s) {
+  if (m256) return launch_gemm<256, 1, false, false, EPI_GATE_SCALE, 3, 1, 1, 2>(P, s);
   return launch_gemm<256, 1, false, false, EPI_GATE_SCALE, 4>(P, s);
 }
 

@@ -96,8 +96,9 @@ int num_sms();
 // pairs: clusters of two CTAs sharing B by multicast (the B map then uses half-height
 // boxes: BN/2 rows)
 int launch_gemm_router(const GemmParams& P, int bn, bool pairs, cudaStream_t s);  // BN 128|224
-int launch_gemm_gateup(const GemmParams& P, cudaStream_t s);  // BN=128, NB=2, SwiGLU
-int launch_gemm_down(const GemmParams& P, cudaStream_t s);    // BN=256, NB=1, gate scale
+// BN=128, NB=2, SwiGLU / BN=256, NB=1, gate scale; m256: 256-row tiles (P.pair_off units)
+int launch_gemm_gateup(const GemmParams& P, bool m256, cudaStream_t s);
+int launch_gemm_down(const GemmParams& P, bool m256, cudaStream_t s);
 int launch_gemm_lora_u2(const GemmParams& P, int r, cudaStream_t s); // BN=r pad, NB=2
 int launch_gemm_lora_u1(const GemmParams& P, int r, cudaStream_t s); // BN=r pad, NB=1
 
