@@ -68,20 +68,22 @@ __device__ __forceinline__ int key_expert(uint64_t key) {
   return 0x7FFFFFFF - static_cast<int>(static_cast<uint32_t>(key));
 }
 
+// Warp maximum of 64-bit keys as two 32-bit warp reductions: the largest high word, then
+// the largest low word among the lanes holding that high word (lexicographic = unsigned
+// 64-bit order).
 __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const uint64_t w = __shfl_xor_sync(0xffffffffu, v, o);
-    v = w > v ? w : v;
-  }
-  return v;
+  const uint32_t hi = static_cast<uint32_t>(v >> 32);
+  const uint32_t m_hi = __reduce_max_sync(0xffffffffu, hi);
+  const uint32_t m_lo =
+      __reduce_max_sync(0xffffffffu, hi == m_hi ? static_cast<uint32_t>(v) : 0u);
+  return (static_cast<uint64_t>(m_hi) << 32) | m_lo;
 }
 
 // One warp per token; lane i holds the logits of experts lane, lane+32, ... (VPL of them).
 // Each warp accumulates the softmax probabilities of its tokens into its own shared-memory
 // row; the block then writes one row of per-block sums (fixed order: deterministic).
 template <int VPL>
-__global__ void __launch_bounds__(256, 3) topk_softmax_kernel(
+__global__ void __launch_bounds__(256, VPL > 28 ? 2 : 3) topk_softmax_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_gate, float* __restrict__ partials) {
   constexpr int WARPS = 8;
@@ -143,12 +145,15 @@ __global__ void __launch_bounds__(256, 3) topk_softmax_kernel(
     const float m = key_value(__shfl_sync(0xffffffffu, my_key, 0));  // the largest logit
     float s = 0.f;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) s += (lane + 32 * i < E) ? __expf(v[i] - m) : 0.f;
+    for (int i = 0; i < VPL; ++i) {
+      v[i] = (lane + 32 * i < E) ? __expf(v[i] - m) : 0.f;  // v now holds exp(l - max)
+      s += v[i];
+    }
     s = warp_sum(s);
     const float inv = 1.0f / s;
 #pragma unroll
     for (int i = 0; i < VPL; ++i)
-      if (lane + 32 * i < E) red[warp][lane + 32 * i] += __expf(v[i] - m) * inv;
+      if (lane + 32 * i < E) red[warp][lane + 32 * i] += v[i] * inv;
     const float pj = (lane < k) ? __expf(key_value(my_key) - m) * inv : 0.f;
     const float psum = warp_sum(pj);
     if (lane < k) {

@@ -67,6 +67,10 @@ CONFIGS = {
     # small case of the c2 kernels for hardware-counter captures (0.8 GB of weights, about
     # 80 rows per expert like c2's 73): same shapes per expert, fewer experts and tokens
     "c2_small": MoEConfig("c2_small", T=640, d=2048, E=128, k=16, F=512),
+    # small case of the c4 kernels (0.35 GB of expert weights, 4096 rows per expert like
+    # c4's 4681): same shapes per expert, four experts
+    "c4_small": MoEConfig("c4_small", T=16384, d=7168, E=4, k=1, F=2048, r=16, alpha=32.0,
+                          prepermuted=True),
     # small case of the c5 kernels (3.2 GB of expert weights, about 256 rows per expert)
     "c5_small": MoEConfig("c5_small", T=2048, d=4096, E=128, k=16, F=1024, r=32, alpha=64.0,
                           backward=True),
