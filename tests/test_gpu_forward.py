@@ -137,6 +137,9 @@ def _route_logits_case(case, T, E):
         # every large logit sits on experts = 5 (mod 32): one lane owns the whole top-k
         L = torch.randn((T, E), generator=g)
         L[:, 5::32] += 100.0
+    elif case == "rounded":
+        # logits on a 0.1 grid: ties among the selected experts (broken by lower index)
+        L = torch.round(torch.randn((T, E), generator=g) * 30) / 10
     elif case == "neg_zero":
         L = torch.zeros((T, E))
         L[:, ::2] = -0.0
@@ -148,7 +151,8 @@ def _route_logits_case(case, T, E):
 
 @pytest.mark.parametrize("case, E, k", [("ties", 40, 6), ("ties", 896, 16), ("one_lane", 896, 16),
                                         ("neg_zero", 896, 32), ("normal", 1024, 32),
-                                        ("normal", 33, 32)])
+                                        ("normal", 33, 32), ("normal", 896, 16), ("normal", 64, 4),
+                                        ("rounded", 896, 16), ("rounded", 200, 8)])
 def test_route_from_logits_exact_selection(case, E, k):
     T = 200
     L = _route_logits_case(case, T, E)
