@@ -38,7 +38,12 @@ struct GemmCfg {
                                    : (NACC * ACC_COLS <= 128) ? 128
                                    : (NACC * ACC_COLS <= 256) ? 256
                                                               : 512;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  // the gate-scale and store epilogues stage each warp's 32 rows in shared memory for
+  // coalesced stores (the SwiGLU epilogue stores per thread: staging it was slower at c2)
+  static constexpr bool STAGED_EPI = EPI == EPI_GATE_SCALE || EPI == EPI_STORE;
+  static constexpr int EPI_STAGE_BYTES = STAGED_EPI ? 4 * 32 * 128 : 0;
+  static constexpr int SMEM_BYTES =
+      STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + EPI_STAGE_BYTES;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
   static_assert(NACC * ACC_COLS <= 512, "accumulators must fit in TMEM");
   static_assert(!B_MN || BN % 64 == 0, "MN-major B is read in whole 64-wide boxes");
@@ -186,6 +191,40 @@ __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float (&
   }
 }
 
+// One epilogue warp's block of 32 rows (row r held by lane r) x CH bf16 columns, packed in
+// pairs, stored to out[row_base + r][0 .. CH) (ld ldo) for rows r < rows_valid and columns
+// < cols_valid (a multiple of 8).  Written row-wise into the warp's staging buffer (2*CH*32
+// bytes, 128-byte swizzle: 16-byte chunk index XOR bits 7-9 of the offset, so neither the
+// row-wise writes nor the column-wise reads conflict on banks), then read back so that each
+// store instruction writes 32 / (CH / 8) whole row segments of 2*CH contiguous bytes.
+template <int CH>
+__device__ __forceinline__ void warp_store_rows(uint8_t* buf, const uint32_t (&w)[CH / 2],
+                                                int lane, __nv_bfloat16* out, long ldo,
+                                                long row_base, int rows_valid, int cols_valid) {
+  constexpr int RB = CH * 2;    // bytes per row
+  constexpr int CPR = RB / 16;  // 16-byte chunks per row
+  constexpr int RPI = 32 / CPR; // rows per store instruction
+  static_assert(CH == 32 || CH == 64, "staged chunk width");
+#pragma unroll
+  for (int j = 0; j < CPR; ++j) {
+    uint32_t off = lane * RB + j * 16;
+    off ^= ((off >> 7) & 7u) << 4;
+    *reinterpret_cast<uint4*>(buf + off) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  }
+  __syncwarp();
+  const int j = lane % CPR;
+#pragma unroll
+  for (int it = 0; it < 32 / RPI; ++it) {
+    const int r = it * RPI + lane / CPR;
+    uint32_t off = r * RB + j * 16;
+    off ^= ((off >> 7) & 7u) << 4;
+    const uint4 v = *reinterpret_cast<const uint4*>(buf + off);
+    if (r < rows_valid && j * 8 < cols_valid)
+      *reinterpret_cast<uint4*>(out + (row_base + r) * ldo + j * 8) = v;
+  }
+  __syncwarp();  // the buffer is reused by the warp's next chunk
+}
+
 __device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* src, float (&v)[16]) {
   const uint4 a = reinterpret_cast<const uint4*>(src)[0];
   const uint4 b = reinterpret_cast<const uint4*>(src)[1];
@@ -217,7 +256,10 @@ __device__ __forceinline__ bool next_tile(const GemmParams& P, int tile, int ran
 }
 
 template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int CL, int MSUB>
-__global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmParams P) {
+// One CTA per SM (registers up to 255 per thread), except the weight-gradient launches,
+// which run two CTAs per SM.
+__global__ void __launch_bounds__(256, EPI == EPI_WGRAD ? 2 : 1)
+    gemm_kernel(const __grid_constant__ GemmParams P) {
   using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB>;
   static_assert(MSUB == 1 || (CL == 1 && EPI != EPI_WGRAD && !A_MN),
                 "two subtiles: single CTA, M-grouped or dense, K-major A");
@@ -524,6 +566,9 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int r_local = q * 32 + lane;
+    // this warp's staging buffer (after the barrier block; gate-scale and store epilogues)
+    uint8_t* epi_buf = smem + STAGES * C::STAGE_BYTES + 256 + q * (32 * 128);
+    (void)epi_buf;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -543,6 +588,9 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
       const bool valid = r_local + sub * kBM < tc.rows_valid;
       const long row = static_cast<long>(tc.row0) + sub * kBM + r_local;
       const int col0 = tc.n * BN;
+      // staged stores: this warp's rows are row_w .. row_w + 31, the first wrows of them valid
+      const long row_w = static_cast<long>(tc.row0) + sub * kBM + q * 32;
+      const int wrows = max(0, min(32, tc.rows_valid - sub * kBM - q * 32));
 
       if constexpr (EPI == EPI_F32_BIAS) {
         float* out = reinterpret_cast<float*>(P.out0);
@@ -595,16 +643,20 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
         __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(P.out0);
         float gs = 0.f;
         if (valid) gs = __ldg(&P.gate[__ldg(&P.row_slot[row])]);
+        static_assert(BN % 64 == 0, "gate-scale epilogue works in 64-column chunks");
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
-          float v[16];
-          tmem_ld16(t_row + c, v);
+        for (int c = 0; c < BN; c += 64) {
+          float v[4][16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tmem_ld16(t_row + c + 16 * j, v[j]);
           tmem_ld_wait();
           const int col = col0 + c;
-          if (valid && col < P.N) {
+          if (col < P.N) {  // warp-uniform
+            uint32_t w[32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] *= gs;
-            store_bf16x16(y + row * P.ldo + col, v, P.N - col);
+            for (int i = 0; i < 32; ++i)
+              w[i] = pack_bf16x2(v[i >> 3][2 * (i & 7)] * gs, v[i >> 3][2 * (i & 7) + 1] * gs);
+            warp_store_rows<64>(epi_buf, w, lane, y + col, P.ldo, row_w, wrows, P.N - col);
           }
         }
       } else if constexpr (EPI == EPI_SCALE) {
@@ -693,13 +745,21 @@ __global__ void __launch_bounds__(256) gemm_kernel(const __grid_constant__ GemmP
         }
       } else if constexpr (EPI == EPI_STORE) {
         __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(P.out0);
+        static_assert(BN % 64 == 0, "store epilogue works in 64-column chunks");
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
-          float v[16];
-          tmem_ld16(t_row + c, v);
+        for (int c = 0; c < BN; c += 64) {
+          float v[4][16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tmem_ld16(t_row + c + 16 * j, v[j]);
           tmem_ld_wait();
           const int col = col0 + c;
-          if (valid && col < P.N) store_bf16x16(o + row * P.ldo + col, v, P.N - col);
+          if (col < P.N) {  // warp-uniform
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              w[i] = pack_bf16x2(v[i >> 3][2 * (i & 7)], v[i >> 3][2 * (i & 7) + 1]);
+            warp_store_rows<64>(epi_buf, w, lane, o + col, P.ldo, row_w, wrows, P.N - col);
+          }
         }
       }
       }  // subtiles
@@ -752,6 +812,7 @@ int launch_gemm(const GemmParams& P, cudaStream_t stream) {
   using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB>;
   static_assert(CTAS_PER_SM * C::TMEM_COLS <= 512, "TMEM of co-resident CTAs");
   static_assert(CTAS_PER_SM * (C::SMEM_BYTES + 1024) <= 232448, "shared memory per SM");
+  static_assert((CTAS_PER_SM == 2) == (EPI == EPI_WGRAD), "register budget of gemm_kernel");
   static_assert(CTAS_PER_SM > 1 || C::SMEM_BYTES > 232448 / 2,
                 "a single-CTA ring must be large enough to keep a second CTA off the SM");
   static_assert(CL == 1 || CTAS_PER_SM == 1, "clusters of single-CTA-per-SM kernels");
