@@ -48,7 +48,11 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="c2")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-sample", type=int, default=32, help="tokens in the oracle baseline")
+    ap.add_argument("--cpu-sample", type=int, default=4096,
+                    help="tokens of the batch the oracle baseline runs on (the whole c2 batch: "
+                         "about 10-15 s of one CPU core)")
+    ap.add_argument("--ref-tokens-per-step", type=int, default=2,
+                    help="tokens per step of the --impl reference arm (the oracle)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--permute", default="auto", choices=["auto", "fused", "separate"],
                     help="fused: gather token rows inside the expert GEMM; separate: write "
@@ -223,7 +227,7 @@ def run_reference(args):
     from top_routing_grouped_gemm_gb300 import synth
     torch.set_num_threads(1)
     cfg = synth.config(args.workload)
-    per_step = max(1, args.cpu_sample // 16)
+    per_step = max(1, args.ref_tokens_per_step)
     n_steps = args.steps + args.warmup
     g = torch.Generator().manual_seed(0)
     x_all = torch.randn((per_step * n_steps, cfg.d), generator=g).to(torch.bfloat16).double().numpy()
