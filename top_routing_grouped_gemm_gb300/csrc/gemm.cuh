@@ -3,12 +3,16 @@
 // fused SwiGLU / gate-scaling epilogues and the LoRA K-blocks), the LoRA down-projections
 // and the backward data-gradient products.
 //
-// Roles (256 threads, one CTA per SM):
+// Roles (256 threads, one CTA per SM; two for the LoRA weight gradients):
 //   warp 0       TMA producer: 64-wide K blocks of A and of each B into a STAGES-deep ring
 //   warp 1       TMEM allocator and MMA issuer (one thread issues tcgen05.mma)
+//   warps 2..3   A-row gather (only when the permute is fused: cp.async of token rows)
 //   warps 4..7   epilogue: tcgen05.ld of the accumulator rows (warp w reads TMEM lanes
-//                32*(w%4) .. +31), fused math, global stores
-// Two TMEM accumulator buffers let the epilogue of tile i overlap the main loop of tile i+1.
+//                32*(w%4) .. +31), fused math, global stores (bf16 outputs of the gate-scale
+//                and store epilogues staged per warp in shared memory for whole-row writes)
+// Two TMEM accumulator buffers let the epilogue of tile i overlap the main loop of tile i+1,
+// except on 256-row tiles (two 128-row A subtiles per B stage), whose one accumulator fills
+// all 512 TMEM columns.
 //
 // Operand tiles in shared memory use the 128-byte swizzle that TMA writes:
 //   K-major  (rows x 64 K): 128-byte rows, 8-row atoms of 1024 B -> SBO = 1024; the k-th

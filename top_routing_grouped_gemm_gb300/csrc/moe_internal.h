@@ -16,9 +16,10 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 // ------------------------------------------------------------------ GEMM description
 //
 // One persistent tcgen05 kernel serves every contraction of the layer.  A CTA owns a
-// 128-row output tile and up to two accumulators of BN columns each (NB operands "B"
-// sharing one operand "A"), walks a list of K segments (each segment names the tensor
-// maps and K offsets its 64-wide K blocks come from), then runs a fused epilogue.
+// 128-row output tile (or two, on 256-row tiles) and up to two accumulators of BN columns
+// each (NB operands "B" sharing one operand "A"), walks a list of K segments (each segment
+// names the tensor maps and K offsets its 64-wide K blocks come from), then runs a fused
+// epilogue.
 
 constexpr int kMaxMaps = 8;
 constexpr int kMaxSegs = 4;
