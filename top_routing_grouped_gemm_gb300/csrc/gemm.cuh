@@ -26,9 +26,10 @@
 namespace moe {
 
 // MSUB: 128-row A subtiles per CTA tile (2: two consecutive m-tiles of one group share every
-// B stage).  NACC: TMEM accumulator buffers (2 overlaps a tile's epilogue with the next
-// tile's main loop; 1 when two buffers do not fit the 512 TMEM columns).
-template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int MSUB = 1>
+// B stage).  CTAS: CTAs resident per SM.  NACC: TMEM accumulator buffers per CTA (2 overlaps
+// a tile's epilogue with the next tile's main loop; 1 when two buffers of every resident CTA
+// do not fit the 512 TMEM columns, in which case a second CTA on the SM does the covering).
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int MSUB = 1, int CTAS = 1>
 struct GemmCfg {
   static constexpr int A_SUB_BYTES = kBM * kBK * 2;
   static constexpr int A_BYTES = MSUB * A_SUB_BYTES;
@@ -36,7 +37,7 @@ struct GemmCfg {
   static constexpr int B_BYTES = (B_MN ? ((BN + 63) / 64) * 64 : BN) * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
   static constexpr int ACC_COLS = MSUB * NB * BN;
-  static constexpr int NACC = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int NACC = (2 * ACC_COLS * CTAS <= 512) ? 2 : 1;
   static constexpr int TMEM_COLS = (NACC * ACC_COLS <= 32)    ? 32
                                    : (NACC * ACC_COLS <= 64)  ? 64
                                    : (NACC * ACC_COLS <= 128) ? 128
@@ -259,12 +260,10 @@ __device__ __forceinline__ bool next_tile(const GemmParams& P, int tile, int ran
   }
 }
 
-template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int CL, int MSUB>
-// One CTA per SM (registers up to 255 per thread), except the weight-gradient launches,
-// which run two CTAs per SM.
-__global__ void __launch_bounds__(256, EPI == EPI_WGRAD ? 2 : 1)
-    gemm_kernel(const __grid_constant__ GemmParams P) {
-  using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB>;
+// CTAS CTAs per SM: with one, a thread may use up to 255 registers; with two, 128.
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int CL, int MSUB, int CTAS>
+__global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__ GemmParams P) {
+  using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB, CTAS>;
   static_assert(MSUB == 1 || (CL == 1 && EPI != EPI_WGRAD && !A_MN),
                 "two subtiles: single CTA, M-grouped or dense, K-major A");
   static_assert(CL == 1 || (EPI != EPI_WGRAD && !A_MN), "CTA pairs: M-grouped, K-major A");
@@ -813,14 +812,13 @@ __global__ void __launch_bounds__(256, EPI == EPI_WGRAD ? 2 : 1)
 template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int CTAS_PER_SM = 1,
           int CL = 1, int MSUB = 1>
 int launch_gemm(const GemmParams& P, cudaStream_t stream) {
-  using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB>;
+  using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB, CTAS_PER_SM>;
   static_assert(CTAS_PER_SM * C::TMEM_COLS <= 512, "TMEM of co-resident CTAs");
   static_assert(CTAS_PER_SM * (C::SMEM_BYTES + 1024) <= 232448, "shared memory per SM");
-  static_assert((CTAS_PER_SM == 2) == (EPI == EPI_WGRAD), "register budget of gemm_kernel");
   static_assert(CTAS_PER_SM > 1 || C::SMEM_BYTES > 232448 / 2,
                 "a single-CTA ring must be large enough to keep a second CTA off the SM");
   static_assert(CL == 1 || CTAS_PER_SM == 1, "clusters of single-CTA-per-SM kernels");
-  auto kern = gemm_kernel<BN, NB, A_MN, B_MN, EPI, STAGES, CL, MSUB>;
+  auto kern = gemm_kernel<BN, NB, A_MN, B_MN, EPI, STAGES, CL, MSUB, CTAS_PER_SM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return static_cast<int>(e);

@@ -17,7 +17,7 @@ int launch_gemm_bwd_dx(const GemmParams& P, cudaStream_t s) {
 // v' = s (dz B_d), s (da_g B_g), s (da_u B_u): N = r (<= 64, zero-filled to 64)
 int launch_gemm_bwd_lora_v(const GemmParams& P, int r, cudaStream_t s) {
   (void)r;
-  return launch_gemm<64, 1, false, true, EPI_SCALE, 9>(P, s);
+  return launch_gemm<64, 1, false, true, EPI_SCALE, 4, 2>(P, s);  // two CTAs per SM, as the forward LoRA products
 }
 
 // LoRA weight gradients, reduction over each expert's rows

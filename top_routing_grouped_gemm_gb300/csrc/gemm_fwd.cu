@@ -28,16 +28,18 @@ int launch_gemm_down(const GemmParams& P, bool m256, cudaStream_t s) {
   return launch_gemm<256, 1, false, false, EPI_GATE_SCALE, 4>(P, s);
 }
 
+// The LoRA down-projections (N = r) stream their A operand through two CTAs per SM: two
+// independent TMA/MMA pipelines fill shared memory faster than one deeper ring.
 int launch_gemm_lora_u2(const GemmParams& P, int r, cudaStream_t s) {
-  if (r <= 16) return launch_gemm<16, 2, false, false, EPI_SCALE, 10>(P, s);
-  if (r <= 32) return launch_gemm<32, 2, false, false, EPI_SCALE, 9>(P, s);
-  return launch_gemm<64, 2, false, false, EPI_SCALE, 6>(P, s);
+  if (r <= 16) return launch_gemm<16, 2, false, false, EPI_SCALE, 5, 2>(P, s);
+  if (r <= 32) return launch_gemm<32, 2, false, false, EPI_SCALE, 4, 2>(P, s);
+  return launch_gemm<64, 2, false, false, EPI_SCALE, 3, 2>(P, s);
 }
 
 int launch_gemm_lora_u1(const GemmParams& P, int r, cudaStream_t s) {
-  if (r <= 16) return launch_gemm<16, 1, false, false, EPI_SCALE, 11>(P, s);
-  if (r <= 32) return launch_gemm<32, 1, false, false, EPI_SCALE, 10>(P, s);
-  return launch_gemm<64, 1, false, false, EPI_SCALE, 9>(P, s);
+  if (r <= 16) return launch_gemm<16, 1, false, false, EPI_SCALE, 5, 2>(P, s);
+  if (r <= 32) return launch_gemm<32, 1, false, false, EPI_SCALE, 5, 2>(P, s);
+  return launch_gemm<64, 1, false, false, EPI_SCALE, 4, 2>(P, s);
 }
 
 }  // namespace moe
