@@ -180,9 +180,9 @@ int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, co
   MOE_TRY(encode_map_kmajor(&P.maps[0], x, d, T, 1, kBM));
   MOE_TRY(encode_map_kmajor(&P.maps[1], w_split, d, E, 2, pairs ? bn / 2 : bn));
   P.nmaps = 2;
-  P.seg[0] = GemmSeg{d / kBK, 0, 0, {1, -1}, {0, 0}, {0, 0}};
-  P.seg[1] = GemmSeg{d / kBK, 0, 0, {1, -1}, {0, 0}, {1, 0}};
-  P.nseg = 2;
+  // one K pass: each A stage is multiplied by the hi (z = 0) and lo (z = 1) weight tiles
+  P.seg[0] = GemmSeg{d / kBK, 0, 0, {1, 1}, {0, 0}, {0, 1}};
+  P.nseg = 1;
   P.M = T;
   P.m_tiles = (T + kBM - 1) / kBM;
   P.n_tiles = (E + bn - 1) / bn;

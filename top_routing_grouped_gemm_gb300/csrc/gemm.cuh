@@ -36,7 +36,11 @@ struct GemmCfg {
   // an MN-major B tile is always whole 64-wide TMA boxes (N below 64 is zero-filled)
   static constexpr int B_BYTES = (B_MN ? ((BN + 63) / 64) * 64 : BN) * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
-  static constexpr int ACC_COLS = MSUB * NB * BN;
+  // The router (EPI_F32_BIAS) with two B operands sums them into one accumulator: they are
+  // the bf16 hi and lo parts of the same fp32 weights, both multiplied by the same A stage.
+  static constexpr bool SUMB = (EPI == EPI_F32_BIAS && NB == 2);
+  static constexpr int ACC_NB = SUMB ? 1 : NB;  // accumulators of BN columns per subtile
+  static constexpr int ACC_COLS = MSUB * ACC_NB * BN;
   static constexpr int NACC = (2 * ACC_COLS * CTAS <= 512) ? 2 : 1;
   static constexpr int TMEM_COLS = (NACC * ACC_COLS <= 32)    ? 32
                                    : (NACC * ACC_COLS <= 64)  ? 64
@@ -409,7 +413,7 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
     // first's BN rows; MN-major: its 64-wide boxes follow the first's, 8 KB apart), so when
     // both are enabled one MMA of N = 2*BN covers both accumulators (columns [0, BN) and
     // [BN, 2*BN)), halving the MMA count.
-    constexpr bool kJoinB = (NB == 2) && (2 * BN <= 256) && (!B_MN || BN % 64 == 0);
+    constexpr bool kJoinB = (NB == 2) && !C::SUMB && (2 * BN <= 256) && (!B_MN || BN % 64 == 0);
     constexpr uint32_t idesc2 = idesc_bf16_f32(kBM, kJoinB ? 2 * BN : BN, A_MN, B_MN);
     int stage = 0;
     uint32_t phase = 0;
@@ -463,7 +467,7 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
                 const uint32_t as = a_addr + sub * C::A_SUB_BYTES;
                 const uint64_t adesc = A_MN ? smem_desc_sw128(as + k * 2048, 8192, 1024)
                                             : smem_desc_sw128(as + k * 32, 16, 1024);
-                const uint32_t d_sub = d_base + sub * NB * BN;
+                const uint32_t d_sub = d_base + sub * C::ACC_NB * BN;
                 if (kJoinB && sg.b_map[0] >= 0 && sg.b_map[1] >= 0) {
                   const uint32_t b_addr = a_addr + C::A_BYTES;
                   const uint64_t bdesc = B_MN ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
@@ -477,7 +481,12 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
                   const uint32_t b_addr = a_addr + C::A_BYTES + b * C::B_BYTES;
                   const uint64_t bdesc = B_MN ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
                                               : smem_desc_sw128(b_addr + k * 32, 16, 1024);
-                  umma_bf16(d_sub + b * BN, adesc, bdesc, idesc, accumulate);
+                  if constexpr (C::SUMB) {
+                    // the second B adds to what the first wrote in this k step
+                    umma_bf16(d_sub, adesc, bdesc, idesc, (accumulate || b > 0) ? 1u : 0u);
+                  } else {
+                    umma_bf16(d_sub + b * BN, adesc, bdesc, idesc, accumulate);
+                  }
                 }
               }
             }
@@ -587,7 +596,7 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
       // a ghost unit of a CTA pair (rows_valid 0) and a missing second subtile store nothing
       if (tc.rows_valid <= sub * kBM) break;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                             acc * C::ACC_COLS + sub * NB * BN;
+                             acc * C::ACC_COLS + sub * C::ACC_NB * BN;
       const bool valid = r_local + sub * kBM < tc.rows_valid;
       const long row = static_cast<long>(tc.row0) + sub * kBM + r_local;
       const int col0 = tc.n * BN;

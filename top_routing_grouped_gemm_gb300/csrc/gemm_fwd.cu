@@ -4,12 +4,14 @@
 namespace moe {
 
 // pairs: clusters of two CTAs on consecutive token tiles sharing each B tile by multicast
+// Two B operands (the hi and lo parts of the split router weights) share each A stage and
+// sum into one accumulator.
 int launch_gemm_router(const GemmParams& P, int bn, bool pairs, cudaStream_t s) {
   if (bn == 224) {
-    if (pairs) return launch_gemm<224, 1, false, false, EPI_F32_BIAS, 4, 1, 2>(P, s);
-    return launch_gemm<224, 1, false, false, EPI_F32_BIAS, 4>(P, s);
+    if (pairs) return launch_gemm<224, 2, false, false, EPI_F32_BIAS, 3, 1, 2>(P, s);
+    return launch_gemm<224, 2, false, false, EPI_F32_BIAS, 3>(P, s);
   }
-  return launch_gemm<128, 1, false, false, EPI_F32_BIAS, 6>(P, s);
+  return launch_gemm<128, 2, false, false, EPI_F32_BIAS, 4>(P, s);
 }
 
 // m256: 256-row tiles (two 128-row subtiles sharing each B stage, one TMEM accumulator) for
