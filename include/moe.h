@@ -153,14 +153,16 @@ int moe_dispatch(const moe_problem* p, const int32_t* topk_idx, const moe_bf16* 
 /* moe_dispatch without a workspace argument, for callers that cannot allocate device memory
  * (their device memory is owned by another allocator that must not be bypassed, or they are
  * handed tensor pointers with no way to call cudaMalloc).  The pages have no counterpart:
- * this is a deployment convenience of this library.  Same outputs, bit for bit, as
- * moe_dispatch.  The scratch is a fixed device array inside the library (8 MiB per GPU that
- * loads the library, held until the process exits); a problem needing more than that
- * (moe_dispatch_workspace_size(p) > 8 MiB) returns MOE_ERR_WORKSPACE without enqueuing
- * anything.  The first call on each device looks up the array's device address (with that
- * device current) and caches it, so make that first call before any stream capture.  Every
- * call shares the one array: calls that overlap on the GPU (e.g. on two streams) race and
- * must be serialised by the caller.  Allocates nothing (no cudaMalloc/cudaFree). */
+ * this is a deployment convenience of this library.  Same arguments, argument checks,
+ * status codes and outputs (bit for bit) as moe_dispatch, including the index-maps-only
+ * mode with x and x_perm both NULL.  The scratch is a fixed device array inside the library
+ * (8 MiB per GPU that loads the library, held until the process exits); a problem needing
+ * more than that (moe_dispatch_workspace_size(p) > 8 MiB) returns MOE_ERR_WORKSPACE without
+ * enqueuing anything.  The first call on each device looks up the array's device address
+ * (with that device current) and caches it, so make that first call before any stream
+ * capture.  Every call shares the one array: calls that overlap on the GPU (e.g. on two
+ * streams) race and must be serialised by the caller.  Allocates nothing (no
+ * cudaMalloc/cudaFree). */
 int moe_dispatch_noalloc(const moe_problem* p, const int32_t* topk_idx, const moe_bf16* x,
                          int32_t* counts, int32_t* offsets, int32_t* slot_row,
                          int32_t* row_slot, int32_t* n_kept_dropped, moe_bf16* x_perm,

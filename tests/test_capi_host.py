@@ -72,6 +72,20 @@ def test_null_pointers_rejected():
                  1 << 30, None, None) == 1
 
 
+def test_noalloc_dispatch_follows_moe_dispatch_argument_rules():
+    # non-positive sizes: the same MOE_ERR_INVALID_ARG as moe_dispatch, nothing enqueued
+    bad = moe.Problem(T=0, d=128, E=16, k=4, F=128)
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None)
+    assert _call("moe_dispatch_noalloc", bad.c(), *args) == 1
+    assert _call("moe_dispatch", bad.c(), *args[:8], FAKE, 1 << 30, None, None) == 1
+    # x_perm without x is rejected by both
+    assert _call("moe_dispatch_noalloc", P_OK.c(), FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE,
+                 FAKE, None, None) == 1
+    # a null index map is rejected
+    assert _call("moe_dispatch_noalloc", P_OK.c(), FAKE, None, FAKE, FAKE, None, FAKE, FAKE,
+                 None, None, None) == 1
+
+
 def test_misaligned_pointers_rejected():
     assert _call("moe_combine", P_OK.c(), FAKE + 2, FAKE, FAKE, None) == 2
     assert _call("moe_route", P_OK.c(), FAKE + 8, FAKE, None, FAKE, FAKE, FAKE, None, FAKE,

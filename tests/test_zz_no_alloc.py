@@ -31,15 +31,17 @@ def _outputs(p, device="cuda"):
                 status=torch.zeros(1, dtype=torch.int32, device=device))
 
 
-def _dispatch(p, idx, x, noalloc):
+def _dispatch(p, idx, x, noalloc, maps_only=False):
     o = _outputs(p)
+    x_perm = None if maps_only else o["x_perm"]
+    x = None if maps_only else x
     if noalloc:
         moe.moe_dispatch_noalloc(p, idx, x, o["counts"], o["offsets"], o["slot_row"],
-                                 o["row_slot"], o["n_kept_dropped"], o["x_perm"], o["status"])
+                                 o["row_slot"], o["n_kept_dropped"], x_perm, o["status"])
     else:
         ws = torch.empty(moe.moe_dispatch_workspace_size(p), dtype=torch.uint8, device="cuda")
         moe.moe_dispatch(p, idx, x, o["counts"], o["offsets"], o["slot_row"], o["row_slot"],
-                         o["n_kept_dropped"], o["x_perm"], ws, o["status"])
+                         o["n_kept_dropped"], x_perm, ws, o["status"])
     torch.cuda.synchronize()
     return o
 
@@ -59,6 +61,19 @@ def test_noalloc_dispatch_matches_workspace_dispatch_on_consecutive_calls():
         assert torch.equal(got["x_perm"][:n_kept], ref["x_perm"][:n_kept]), cfg.name
         if cfg.cap_den:
             assert int(ref["n_kept_dropped"][1].item()) > 0
+
+
+def test_noalloc_dispatch_index_maps_only_matches_workspace_dispatch():
+    """x and x_perm both NULL: only the index maps (the mode the fused-permute expert GEMM
+    uses), on two consecutive calls."""
+    for n, cfg in enumerate([synth.config("c3", T=2048), synth.config("c2", T=1024)]):
+        p = moe.problem_of(cfg)
+        idx = _routing(cfg, seed=10 + n).cuda()
+        ref = _dispatch(p, idx, None, noalloc=False, maps_only=True)
+        got = _dispatch(p, idx, None, noalloc=True, maps_only=True)
+        assert int(got["status"].item()) == 0
+        for key in ("counts", "offsets", "slot_row", "row_slot", "n_kept_dropped"):
+            assert torch.equal(got[key], ref[key]), (cfg.name, key)
 
 
 def test_noalloc_dispatch_rejects_problems_beyond_its_scratch():

@@ -11,11 +11,9 @@
 
 using namespace moe;
 
-namespace {
+namespace moe {
 
-inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-inline size_t up256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
-
+// Shared with the other entry-point files through moe_internal.h.
 int check_problem(const moe_problem* p) {
   if (!p) return MOE_ERR_INVALID_ARG;
   if (p->T <= 0 || p->d <= 0 || p->E <= 0 || p->k <= 0 || p->F <= 0 || p->r < 0)
@@ -38,6 +36,39 @@ int capacity_of(const moe_problem* p) {
   const long long c = (num + den - 1) / den;
   return c > (1ll << 30) ? (1 << 30) : static_cast<int>(c);
 }
+
+size_t dispatch_ws(const moe_problem* p) {
+  return up256(static_cast<size_t>(p->T) * p->k * 4) +
+         up256(static_cast<size_t>(dispatch_num_chunks(p->T)) * p->E * 4);
+}
+
+// ---- instrumentation state (process-wide, see moe_set_kernel_events)
+namespace {
+cudaEvent_t g_ev_before[MOE_KERNEL_COUNT] = {nullptr};
+cudaEvent_t g_ev_after[MOE_KERNEL_COUNT] = {nullptr};
+std::atomic<long long> g_launches{0};
+}  // namespace
+
+void mark_before(int id, cudaStream_t s) {
+  if (g_ev_before[id]) cudaEventRecord(g_ev_before[id], s);
+}
+void mark_after(int id, cudaStream_t s) {
+  if (g_ev_after[id]) cudaEventRecord(g_ev_after[id], s);
+}
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+long long launch_count() { return g_launches.load(std::memory_order_relaxed); }
+int set_kernel_events(int kernel_id, void* event_before, void* event_after) {
+  if (kernel_id < 0 || kernel_id >= MOE_KERNEL_COUNT) return MOE_ERR_INVALID_ARG;
+  g_ev_before[kernel_id] = static_cast<cudaEvent_t>(event_before);
+  g_ev_after[kernel_id] = static_cast<cudaEvent_t>(event_after);
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+namespace {
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int cuda_status(int e) { return e == 0 ? MOE_OK : MOE_ERR_CUDA; }
 
@@ -82,29 +113,11 @@ size_t route_ws(const moe_problem* p) {
   return up256(2ull * p->E * p->d * 2) + up256(static_cast<size_t>(p->T) * p->E * 4);
 }
 
-size_t dispatch_ws(const moe_problem* p) {
-  return up256(static_cast<size_t>(p->T) * p->k * 4) +
-         up256(static_cast<size_t>(dispatch_num_chunks(p->T)) * p->E * 4);
-}
-
 size_t ffn_ws(const moe_problem* p, int rows_max) {
   size_t b = 2 * up256((p->E + 1) * 4ull);
   if (p->r) b += 3 * up256(static_cast<size_t>(rows_max) * p->r * 2);
   return b;
 }
-
-// ---- instrumentation state (process-wide, see moe_set_kernel_events)
-cudaEvent_t g_ev_before[MOE_KERNEL_COUNT] = {nullptr};
-cudaEvent_t g_ev_after[MOE_KERNEL_COUNT] = {nullptr};
-std::atomic<long long> g_launches{0};
-
-inline void mark_before(int id, cudaStream_t s) {
-  if (g_ev_before[id]) cudaEventRecord(g_ev_before[id], s);
-}
-inline void mark_after(int id, cudaStream_t s) {
-  if (g_ev_after[id]) cudaEventRecord(g_ev_after[id], s);
-}
-inline void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 GemmParams gemm_params() {
   GemmParams P;
@@ -174,11 +187,9 @@ int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, co
   // expert tile: 224 when it divides E (896 = 4 x 224: fewer, larger tiles, less L2 traffic
   // per flop), else 128
   const int bn = (E % 224 == 0) ? 224 : 128;
-  // clusters of two CTAs on consecutive token tiles share each weight tile by multicast
-  const bool pairs = bn == 224 && T >= 8192;  // measured: no gain for few token tiles
   GemmParams P = gemm_params();
   MOE_TRY(encode_map_kmajor(&P.maps[0], x, d, T, 1, kBM));
-  MOE_TRY(encode_map_kmajor(&P.maps[1], w_split, d, E, 2, pairs ? bn / 2 : bn));
+  MOE_TRY(encode_map_kmajor(&P.maps[1], w_split, d, E, 2, bn));
   P.nmaps = 2;
   // one K pass: each A stage is multiplied by the hi (z = 0) and lo (z = 1) weight tiles
   P.seg[0] = GemmSeg{d / kBK, 0, 0, {1, 1}, {0, 0}, {0, 1}};
@@ -193,7 +204,7 @@ int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, co
   P.b_policy = 1;  // the router weights are re-read by every token tile
   P.dev_status = dev_status;
   mark_before(MOE_KERNEL_ROUTER_GEMM, stream);
-  MOE_CUDA(launch_gemm_router(P, bn, pairs, stream));
+  MOE_CUDA(launch_gemm_router(P, bn, stream));
   mark_after(MOE_KERNEL_ROUTER_GEMM, stream);
   mark_before(MOE_KERNEL_TOPK, stream);
   MOE_CUDA(launch_topk_softmax(L, T, E, p->k, topk_idx, topk_gate, prob_partials, stream));
@@ -699,12 +710,9 @@ int moe_route_bwd(const moe_problem* p, const int32_t* topk_idx, const float* to
 // ------------------------------------------------------------------------ instrumentation
 
 int moe_set_kernel_events(int kernel_id, void* event_before, void* event_after) {
-  if (kernel_id < 0 || kernel_id >= MOE_KERNEL_COUNT) return MOE_ERR_INVALID_ARG;
-  g_ev_before[kernel_id] = static_cast<cudaEvent_t>(event_before);
-  g_ev_after[kernel_id] = static_cast<cudaEvent_t>(event_after);
-  return MOE_OK;
+  return moe::set_kernel_events(kernel_id, event_before, event_after);
 }
 
-long long moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+long long moe_launch_count(void) { return moe::launch_count(); }
 
 }  // extern "C"

@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kRowThreads) dispatch_scatter_kernel(
 }
 
 // m-tiles of 128 rows per group and their prefix (tile_off), and the prefix of m-tile pairs
-// (pair_off, for CTA-pair launches).  Malformed offsets disable the group and are reported.
+// (pair_off, for 256-row tiles).  Malformed offsets disable the group and are reported.
 __global__ void __launch_bounds__(1024) tile_schedule_kernel(const int32_t* __restrict__ offsets,
                                                              int E, int rows_max,
                                                              int32_t* __restrict__ tile_off,

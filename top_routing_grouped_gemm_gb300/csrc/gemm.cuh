@@ -118,22 +118,19 @@ __device__ __forceinline__ bool decode_tile_wgrad(const GemmParams& P, int tile,
   return true;
 }
 
-// CTA-pair launches (clusters of two): unit `pt` is a pair of m-tiles of one (group, n-tile);
-// CTA `rank` of the cluster takes m-tile 2*pair + rank.  Both CTAs need the same B tile,
-// which each loads half of and multicasts to both.  A CTA whose m-tile does not exist (odd
-// m-tile counts) is a ghost for that unit: rows_valid = 0, it loads no A, issues no MMA
-// and stores nothing, but still takes part in the B loads and the stage hand-off.
-__device__ __forceinline__ bool decode_pair_tile(const GemmParams& P, int pt, int rank,
-                                                 TileCoord& tc) {
+// Two-subtile launches (MSUB = 2): unit `pt` covers m-tiles 2*pair and 2*pair+1 of one
+// (group, n-tile) in one CTA (rows_valid up to 256); the second subtile is skipped when the
+// group's rows end inside the first.  pair_off is the prefix over groups of ceil(m-tiles/2).
+__device__ __forceinline__ bool decode_sub_tile(const GemmParams& P, int pt, TileCoord& tc) {
   if (P.group_off == nullptr) {
     const int pairs = (P.m_tiles + 1) >> 1;
     if (pt >= pairs * P.n_tiles) return false;
     const int mp = pt / P.n_tiles;
     tc.g = 0;
     tc.n = pt - mp * P.n_tiles;
-    tc.m = 2 * mp + rank;
+    tc.m = 2 * mp;
     tc.row0 = tc.m * kBM;
-    tc.rows_valid = tc.m < P.m_tiles ? min(kBM, P.M - tc.row0) : 0;
+    tc.rows_valid = min(2 * kBM, P.M - tc.row0);
     return true;
   }
   const int total = __ldg(&P.pair_off[P.G]) * P.n_tiles;
@@ -148,23 +145,9 @@ __device__ __forceinline__ bool decode_pair_tile(const GemmParams& P, int pt, in
   const int local = pt - p0 * P.n_tiles;
   tc.g = lo;
   tc.n = local / np;
-  tc.m = 2 * (local - tc.n * np) + rank;
-  const int mt = __ldg(&P.tile_off[lo + 1]) - __ldg(&P.tile_off[lo]);
+  tc.m = 2 * (local - tc.n * np);
   tc.row0 = __ldg(&P.group_off[lo]) + tc.m * kBM;
-  tc.rows_valid = tc.m < mt ? min(kBM, __ldg(&P.group_off[lo + 1]) - tc.row0) : 0;
-  return true;
-}
-
-// Two-subtile launches (MSUB = 2): unit `pt` covers m-tiles 2*pair and 2*pair+1 of one
-// (group, n-tile) in one CTA (rows_valid up to 256); the second subtile is skipped when the
-// group's rows end inside the first.
-__device__ __forceinline__ bool decode_sub_tile(const GemmParams& P, int pt, TileCoord& tc) {
-  if (!decode_pair_tile(P, pt, 0, tc)) return false;
-  if (P.group_off == nullptr) {
-    tc.rows_valid = min(2 * kBM, P.M - tc.row0);
-  } else {
-    tc.rows_valid = min(2 * kBM, __ldg(&P.group_off[tc.g + 1]) - tc.row0);
-  }
+  tc.rows_valid = min(2 * kBM, __ldg(&P.group_off[lo + 1]) - tc.row0);
   return true;
 }
 
@@ -249,29 +232,26 @@ __device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* src, float (&v
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
-template <int EPI, int CL, int MSUB>
-__device__ __forceinline__ bool next_tile(const GemmParams& P, int tile, int rank,
-                                          TileCoord& tc, KRange& kr) {
+template <int EPI, int MSUB>
+__device__ __forceinline__ bool next_tile(const GemmParams& P, int tile, TileCoord& tc,
+                                          KRange& kr) {
   if constexpr (EPI == EPI_WGRAD) {
     return decode_tile_wgrad(P, tile, tc, kr);
   } else {
     kr.k0 = 0;
     kr.nrows = 0;
     kr.nkb = 0;
-    if constexpr (CL == 2) return decode_pair_tile(P, tile, rank, tc);
     if constexpr (MSUB == 2) return decode_sub_tile(P, tile, tc);
     return decode_tile(P, tile, tc);
   }
 }
 
 // CTAS CTAs per SM: with one, a thread may use up to 255 registers; with two, 128.
-template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int CL, int MSUB, int CTAS>
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int MSUB, int CTAS>
 __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__ GemmParams P) {
   using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB, CTAS>;
-  static_assert(MSUB == 1 || (CL == 1 && EPI != EPI_WGRAD && !A_MN),
-                "two subtiles: single CTA, M-grouped or dense, K-major A");
-  static_assert(CL == 1 || (EPI != EPI_WGRAD && !A_MN), "CTA pairs: M-grouped, K-major A");
-  static_assert(CL == 1 || B_MN || (BN / 2) % 8 == 0, "half B tiles stay swizzle-aligned");
+  static_assert(MSUB == 1 || (EPI != EPI_WGRAD && !A_MN),
+                "two subtiles: M-grouped or dense, K-major A");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -286,10 +266,8 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int rank = (CL == 2) ? static_cast<int>(cluster_ctarank()) : 0;
-  const int unit0 = blockIdx.x / CL;       // first work unit of this CTA (or CTA pair)
-  const int unit_step = gridDim.x / CL;    // number of CTAs (or CTA pairs)
-  constexpr uint16_t kPairMask = 0x3;
+  const int unit0 = blockIdx.x;      // first work unit of this CTA
+  const int unit_step = gridDim.x;   // number of CTAs
 
   if (threadIdx.x == 0) {
     // with a gathered A operand a stage is full after the producer's expect-tx arrival
@@ -298,7 +276,7 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
         (!A_MN && EPI != EPI_WGRAD && MSUB == 1 && P.gather_slot != nullptr) ? 2u : 1u;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], full_count);
-      mbar_init(&empty[s], CL);  // a stage is free once every CTA that reads it released it
+      mbar_init(&empty[s], 1);  // a stage is free once the MMA warp has released it
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
@@ -318,11 +296,7 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
     tmem_relinquish();
   }
   tc_fence_before();
-  if constexpr (CL == 2) {
-    cluster_sync();  // both CTAs' barriers exist before either multicasts into the other
-  } else {
-    __syncthreads();
-  }
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -335,7 +309,7 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
     bool ok = true;
     TileCoord tc;
     KRange kr;
-    for (int tile = unit0; ok && next_tile<EPI, CL, MSUB>(P, tile, rank, tc, kr); tile += unit_step) {
+    for (int tile = unit0; ok && next_tile<EPI, MSUB>(P, tile, tc, kr); tile += unit_step) {
       const int nseg = (EPI == EPI_WGRAD) ? 1 : P.nseg;
       for (int s = 0; ok && s < nseg; ++s) {
         const GemmSeg& sg = P.seg[s];
@@ -347,18 +321,16 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
           if (!w) { ok = false; break; }
           uint8_t* sA = smem + stage * C::STAGE_BYTES;
           const int ka = (EPI == EPI_WGRAD) ? kr.k0 + kb * kBK : sg.a_k0 + kb * kBK;
-          const bool ghost = (CL == 2) && tc.rows_valid == 0;
           if (lane == 0) {
-            // B: the whole tile lands here (half of it from the other CTA of a pair)
             const int nsub = (MSUB == 2 && tc.rows_valid > kBM) ? 2 : 1;
-            uint32_t bytes = (sg.a_gather || ghost) ? 0u : nsub * C::A_SUB_BYTES;
+            uint32_t bytes = sg.a_gather ? 0u : nsub * C::A_SUB_BYTES;
 #pragma unroll
             for (int b = 0; b < NB; ++b) bytes += (sg.b_map[b] >= 0) ? C::B_BYTES : 0;
             mbar_arrive_expect_tx(&full[stage], bytes);
           }
           if (lane == 0) {
             if (!A_MN) {
-              if (!sg.a_gather && !ghost) {
+              if (!sg.a_gather) {
                 tma_load_3d(sA, &P.maps[sg.a_map], &full[stage], ka, tc.row0, 0, pol_a);
                 if (MSUB == 2 && tc.rows_valid > kBM)
                   tma_load_3d(sA + C::A_SUB_BYTES, &P.maps[sg.a_map], &full[stage], ka,
@@ -375,19 +347,7 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
               uint8_t* sB = sA + C::A_BYTES + b * C::B_BYTES;
               const int kbk = (EPI == EPI_WGRAD) ? kr.k0 + kb * kBK : sg.b_k0[b] + kb * kBK;
               const int z = (EPI == EPI_WGRAD) ? 0 : ((P.group_off != nullptr) ? tc.g : sg.b_z[b]);
-              if constexpr (CL == 2) {
-                // this CTA loads its half of B and multicasts it to both CTAs of the pair
-                if (!B_MN) {
-                  constexpr int HB = BN / 2;
-                  tma_load_3d_mc(sB + rank * HB * 128, &P.maps[sg.b_map[b]], &full[stage], kbk,
-                                 tc.n * BN + rank * HB, z, kPairMask, pol_b);
-                } else {
-#pragma unroll
-                  for (int c = rank; c < (BN + 63) / 64; c += 2)
-                    tma_load_3d_mc(sB + c * 8192, &P.maps[sg.b_map[b]], &full[stage],
-                                   tc.n * BN + c * 64, kbk, z, kPairMask, pol_b);
-                }
-              } else if (!B_MN) {
+              if (!B_MN) {
                 tma_load_3d(sB, &P.maps[sg.b_map[b]], &full[stage], kbk, tc.n * BN, z, pol_b);
               } else {
 #pragma unroll
@@ -422,7 +382,7 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
     bool ok = true;
     TileCoord tc;
     KRange kr;
-    for (int tile = unit0; ok && next_tile<EPI, CL, MSUB>(P, tile, rank, tc, kr); tile += unit_step) {
+    for (int tile = unit0; ok && next_tile<EPI, MSUB>(P, tile, tc, kr); tile += unit_step) {
       int w = 1;
       if (lane == 0) w = mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag) ? 1 : 0;
       w = __shfl_sync(0xffffffffu, w, 0);
@@ -455,11 +415,9 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
           }
           if (lane == 0) {
             const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
-            const bool ghost = (CL == 2) && tc.rows_valid == 0;
             const int nsub = (MSUB == 2 && tc.rows_valid > kBM) ? 2 : 1;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
-              if (ghost) break;
               const uint32_t accumulate = (s > 0 || kb > 0 || k > 0) ? 1u : 0u;
 #pragma unroll
               for (int sub = 0; sub < MSUB; ++sub) {
@@ -490,11 +448,7 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
                 }
               }
             }
-            if constexpr (CL == 2) {
-              umma_commit_mc(&empty[stage], kPairMask);  // both CTAs load into this stage
-            } else {
-              umma_commit(&empty[stage]);
-            }
+            umma_commit(&empty[stage]);
           }
           __syncwarp();
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -527,7 +481,7 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
         bool ok = true;
         TileCoord tc;
         KRange kr;
-        for (int tile = unit0; ok && next_tile<EPI, CL, MSUB>(P, tile, rank, tc, kr); tile += unit_step) {
+        for (int tile = unit0; ok && next_tile<EPI, MSUB>(P, tile, tc, kr); tile += unit_step) {
           int trow[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -586,14 +540,14 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
     bool ok = true;
     TileCoord tc;
     KRange kr;
-    for (int tile = unit0; next_tile<EPI, CL, MSUB>(P, tile, rank, tc, kr); tile += unit_step) {
+    for (int tile = unit0; next_tile<EPI, MSUB>(P, tile, tc, kr); tile += unit_step) {
       int w = 1;
       if (lane == 0) w = mbar_wait(&acc_full[acc], acc_phase, abort_flag) ? 1 : 0;
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) { ok = false; break; }
       tc_fence_after();
       for (int sub = 0; sub < MSUB; ++sub) {
-      // a ghost unit of a CTA pair (rows_valid 0) and a missing second subtile store nothing
+      // a missing second subtile stores nothing
       if (tc.rows_valid <= sub * kBM) break;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              acc * C::ACC_COLS + sub * C::ACC_NB * BN;
@@ -788,13 +742,8 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
   // All roles are done.  On the normal path every TMA load was consumed and every MMA was
   // waited for through acc_full.  After an abort, the MMA thread waits (bounded) for its
   // own tcgen05 ops and thread 0 gives in-flight TMA copies a bounded grace period, so
-  // nothing lands in shared memory or TMEM after the CTA has released them.  A CTA pair
-  // leaves together: neither exits while the other may still signal its barriers.
-  if constexpr (CL == 2) {
-    cluster_sync();
-  } else {
-    __syncthreads();
-  }
+  // nothing lands in shared memory or TMEM after the CTA has released them.
+  __syncthreads();
   if (*abort_flag) {
     if (threadIdx.x == 32) {
       umma_commit(drain);
@@ -816,53 +765,21 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
 
 // ctas_per_sm > 1 only for instantiations whose ring and TMEM both fit that many times on an
 // SM (shared memory <= 227 KB / ctas_per_sm, TMEM columns <= 512 / ctas_per_sm), so that no
-// CTA can wait on another's TMEM allocation.  CL = 2 launches clusters of two CTAs that share
-// B tiles by multicast; the grid is as many clusters as can be resident at once.
+// CTA can wait on another's TMEM allocation.
 template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int CTAS_PER_SM = 1,
-          int CL = 1, int MSUB = 1>
+          int MSUB = 1>
 int launch_gemm(const GemmParams& P, cudaStream_t stream) {
   using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB, CTAS_PER_SM>;
   static_assert(CTAS_PER_SM * C::TMEM_COLS <= 512, "TMEM of co-resident CTAs");
   static_assert(CTAS_PER_SM * (C::SMEM_BYTES + 1024) <= 232448, "shared memory per SM");
   static_assert(CTAS_PER_SM > 1 || C::SMEM_BYTES > 232448 / 2,
                 "a single-CTA ring must be large enough to keep a second CTA off the SM");
-  static_assert(CL == 1 || CTAS_PER_SM == 1, "clusters of single-CTA-per-SM kernels");
-  auto kern = gemm_kernel<BN, NB, A_MN, B_MN, EPI, STAGES, CL, MSUB, CTAS_PER_SM>;
+  auto kern = gemm_kernel<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB, CTAS_PER_SM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return static_cast<int>(e);
-  if constexpr (CL == 1) {
-    kern<<<CTAS_PER_SM * num_sms(), 256, C::SMEM_BYTES, stream>>>(P);
-    return static_cast<int>(cudaGetLastError());
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(256, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    static int clusters_cache[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int nclusters = (dev >= 0 && dev < 64) ? clusters_cache[dev] : 0;
-    if (nclusters <= 0) {
-      cfg.gridDim = dim3(CL * (num_sms() / CL), 1, 1);
-      e = cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg);
-      if (e != cudaSuccess) return static_cast<int>(e);
-      if (nclusters <= 0) return static_cast<int>(cudaErrorInvalidConfiguration);
-      nclusters = min(nclusters, num_sms() / CL);
-      if (dev >= 0 && dev < 64) clusters_cache[dev] = nclusters;
-    }
-    cfg.gridDim = dim3(CL * nclusters, 1, 1);
-    e = cudaLaunchKernelEx(&cfg, kern, P);
-    if (e != cudaSuccess) return static_cast<int>(e);
-    return static_cast<int>(cudaGetLastError());
-  }
+  kern<<<CTAS_PER_SM * num_sms(), 256, C::SMEM_BYTES, stream>>>(P);
+  return static_cast<int>(cudaGetLastError());
 }
 
 }  // namespace moe

@@ -3,14 +3,10 @@
 
 namespace moe {
 
-// pairs: clusters of two CTAs on consecutive token tiles sharing each B tile by multicast
 // Two B operands (the hi and lo parts of the split router weights) share each A stage and
 // sum into one accumulator.
-int launch_gemm_router(const GemmParams& P, int bn, bool pairs, cudaStream_t s) {
-  if (bn == 224) {
-    if (pairs) return launch_gemm<224, 2, false, false, EPI_F32_BIAS, 3, 1, 2>(P, s);
-    return launch_gemm<224, 2, false, false, EPI_F32_BIAS, 3>(P, s);
-  }
+int launch_gemm_router(const GemmParams& P, int bn, cudaStream_t s) {
+  if (bn == 224) return launch_gemm<224, 2, false, false, EPI_F32_BIAS, 3>(P, s);
   return launch_gemm<128, 2, false, false, EPI_F32_BIAS, 4>(P, s);
 }
 
@@ -20,13 +16,13 @@ int launch_gemm_router(const GemmParams& P, int bn, bool pairs, cudaStream_t s) 
 int launch_gemm_gateup(const GemmParams& P, bool m256, cudaStream_t s) {
   if (m256) {
     if (P.gather_slot != nullptr) return static_cast<int>(cudaErrorInvalidValue);
-    return launch_gemm<128, 2, false, false, EPI_SWIGLU, 3, 1, 1, 2>(P, s);
+    return launch_gemm<128, 2, false, false, EPI_SWIGLU, 3, 1, 2>(P, s);
   }
   return launch_gemm<128, 2, false, false, EPI_SWIGLU, 4>(P, s);
 }
 
 int launch_gemm_down(const GemmParams& P, bool m256, cudaStream_t s) {
-  if (m256) return launch_gemm<256, 1, false, false, EPI_GATE_SCALE, 3, 1, 1, 2>(P, s);
+  if (m256) return launch_gemm<256, 1, false, false, EPI_GATE_SCALE, 3, 1, 2>(P, s);
   return launch_gemm<256, 1, false, false, EPI_GATE_SCALE, 4>(P, s);
 }
 

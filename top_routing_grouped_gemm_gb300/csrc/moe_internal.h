@@ -13,6 +13,20 @@ namespace moe {
 // Bounded device-side waits give up after this much wall time (ns).
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
+inline size_t up256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+// Entry-point helpers shared by the files of the C ABI (defined in capi.cu).
+int check_problem(const moe_problem* p);    // MOE_OK or the status an entry point returns
+int capacity_of(const moe_problem* p);      // ceil(cf * T * k / E), -1 for cf = infinity
+size_t dispatch_ws(const moe_problem* p);   // scratch bytes of the dispatch kernels
+// Instrumentation (moe_set_kernel_events / moe_launch_count): caller events recorded
+// around a kernel's launches, and the process-wide launch counter.
+void mark_before(int kernel_id, cudaStream_t s);
+void mark_after(int kernel_id, cudaStream_t s);
+void count_launches(int n);
+long long launch_count();
+int set_kernel_events(int kernel_id, void* event_before, void* event_after);
+
 // ------------------------------------------------------------------ GEMM description
 //
 // One persistent tcgen05 kernel serves every contraction of the layer.  A CTA owns a
@@ -56,7 +70,7 @@ struct GemmParams {
   // Dense (group_off == nullptr): one group of M rows, m_tiles tiles.
   const int* group_off;
   const int* tile_off;
-  const int* pair_off;   // CTA-pair launches: prefix over groups of ceil(m-tiles / 2)
+  const int* pair_off;   // 256-row tiles: prefix over groups of ceil(m-tiles / 2)
   int G;
   int M;
   int m_tiles;
@@ -93,10 +107,8 @@ int encode_map_mnmajor(CUtensorMap* map, const void* base, uint64_t mn_extent,
                        uint64_t k_rows, uint64_t groups);
 int num_sms();
 
-// Kernel launchers (gemm_kernels.cu).  Return cudaError_t as int.
-// pairs: clusters of two CTAs sharing B by multicast (the B map then uses half-height
-// boxes: BN/2 rows)
-int launch_gemm_router(const GemmParams& P, int bn, bool pairs, cudaStream_t s);  // BN 128|224
+// Kernel launchers (gemm_fwd.cu).  Return cudaError_t as int.
+int launch_gemm_router(const GemmParams& P, int bn, cudaStream_t s);  // BN 128|224
 // BN=128, NB=2, SwiGLU / BN=256, NB=1, gate scale; m256: 256-row tiles (P.pair_off units)
 int launch_gemm_gateup(const GemmParams& P, bool m256, cudaStream_t s);
 int launch_gemm_down(const GemmParams& P, bool m256, cudaStream_t s);

@@ -38,8 +38,6 @@ int scratch_address(void** out) {
   return MOE_OK;
 }
 
-inline size_t up256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
-
 }  // namespace
 
 extern "C" int moe_dispatch_noalloc(const moe_problem* p, const int32_t* topk_idx,
@@ -48,32 +46,30 @@ extern "C" int moe_dispatch_noalloc(const moe_problem* p, const int32_t* topk_id
                                     int32_t* n_kept_dropped, moe_bf16* x_perm,
                                     int32_t* dev_status, moe_stream_t stream) {
   using namespace moe;
-  const size_t need = moe_dispatch_workspace_size(p);
-  if (need == 0) return p == nullptr ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
-  if (need > kNoallocScratchBytes) return MOE_ERR_WORKSPACE;
-  if (!topk_idx || !x || !counts || !offsets || !slot_row || !row_slot || !n_kept_dropped ||
-      !x_perm)
+  // the same argument rules as moe_dispatch: x_perm is optional (maps only), x is needed
+  // only when x_perm is given
+  const int st = check_problem(p);
+  if (st != MOE_OK) return st;
+  if (!topk_idx || !counts || !offsets || !slot_row || !row_slot || !n_kept_dropped)
     return MOE_ERR_INVALID_ARG;
+  if (x_perm && !x) return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(x_perm) & 15u))
     return MOE_ERR_UNSUPPORTED;
+  if (dispatch_ws(p) > kNoallocScratchBytes) return MOE_ERR_WORKSPACE;
   void* scratch = nullptr;
-  const int st = scratch_address(&scratch);
-  if (st != MOE_OK) return st;
+  const int sa = scratch_address(&scratch);
+  if (sa != MOE_OK) return sa;
   // Same carving as the workspace of moe_dispatch.  Both regions are fully written by the
   // counting kernel before they are read, so nothing needs clearing between calls.
   int32_t* local_rank = static_cast<int32_t*>(scratch);
   int32_t* chunk_cnt = reinterpret_cast<int32_t*>(
       static_cast<unsigned char*>(scratch) + up256(static_cast<size_t>(p->T) * p->k * 4));
-  int capacity = -1;  // ceil(cf * T * k / E), as moe_dispatch computes it
-  if (p->cap_den != 0) {
-    const long long num = static_cast<long long>(p->cap_num) * p->T * p->k;
-    const long long den = static_cast<long long>(p->cap_den) * p->E;
-    const long long c = (num + den - 1) / den;
-    capacity = c > (1ll << 30) ? (1 << 30) : static_cast<int>(c);
-  }
+  mark_before(MOE_KERNEL_DISPATCH, stream);
   const int e = launch_dispatch(topk_idx, reinterpret_cast<const __nv_bfloat16*>(x), p->T, p->d,
-                                p->E, p->k, capacity, counts, offsets, slot_row, row_slot,
+                                p->E, p->k, capacity_of(p), counts, offsets, slot_row, row_slot,
                                 n_kept_dropped, reinterpret_cast<__nv_bfloat16*>(x_perm),
                                 local_rank, chunk_cnt, dev_status, stream);
+  mark_after(MOE_KERNEL_DISPATCH, stream);
+  count_launches(4);
   return e == 0 ? MOE_OK : MOE_ERR_CUDA;
 }
