@@ -130,6 +130,94 @@ def test_dispatch_all_zero_logits_with_capacity():
         assert list(toks) == list(range(C))
 
 
+# ---------------------------------------------------------------- router bias
+# The router adds a per-expert bias to the logits before both the softmax and the selection
+# (the skewed-routing workload's Zipf bias goes through this term).
+
+def check_bias_two_experts_closed_form():
+    # integer inputs: every logit is exact, so p0 has the textbook two-class closed form
+    # p0 = sigma((w0 - w1) . x + b0 - b1)
+    x = np.array([[1.0, 2.0, -1.0], [0.0, -2.0, 3.0]])
+    W = np.array([[1.0, 0.0, 1.0], [0.0, 1.0, 0.0]])
+    b = np.array([0.5, -0.25])
+    L = oracle.router_logits(x, W, b)
+    # token 0: L = [1 + 0 - 1 + 0.5, 2 - 0.25] = [0.5, 1.75]; token 1: [3 + 0.5, -2 - 0.25]
+    assert L.tolist() == [[0.5, 1.75], [3.5, -2.25]]
+    idx, g, p = oracle.route(L, 1)
+    assert idx[:, 0].tolist() == [1, 0]
+    assert p[0, 0] == pytest.approx(1.0 / (1.0 + math.exp(1.25)), rel=1e-14)
+    assert p[1, 0] == pytest.approx(1.0 / (1.0 + math.exp(-5.75)), rel=1e-14)
+    assert g[:, 0].tolist() == [1.0, 1.0]
+
+
+def check_bias_makes_expert0_win_with_drops():
+    # W_r = 0, b = [3, 0, 2, 1]: every token's logits are b, so each selects experts 0 and 2
+    # (k = 2).  T = 6, E = 4, cf = 1 -> C = ceil(6 * 2 / 4) = 3: tokens 0..2 are kept on both
+    # experts, tokens 3..5 dropped on both (arrival order).
+    T, E, k, d = 6, 4, 2, 3
+    x = _rng(9).standard_normal((T, d))
+    b = np.array([3.0, 0.0, 2.0, 1.0])
+    Wz = np.zeros((E, d))
+    Wg = _rng(10).standard_normal((E, 2, d))
+    Wu = _rng(11).standard_normal((E, 2, d))
+    Wd = _rng(12).standard_normal((E, d, 2))
+    out = oracle.moe_forward(x, Wz, Wg, Wu, Wd, k, 1, 1, bias=b)
+    assert out["C"] == 3
+    assert out["idx"].tolist() == [[0, 2]] * T
+    D = out["disp"]
+    assert D["counts"].tolist() == [6, 0, 6, 0]
+    assert D["kept"].tolist() == [3, 0, 3, 0]
+    assert D["offsets"].tolist() == [0, 3, 3, 6, 6]
+    assert D["slot_row"].tolist() == [0, 3, 1, 4, 2, 5] + [-1] * 6
+    assert (D["n_kept"], D["n_dropped"]) == (6, 6)
+    # gates: e^3 / (e^3 + e^2) = sigma(1), and its complement
+    s1 = 1.0 / (1.0 + math.exp(-1.0))
+    assert np.allclose(out["gates"], [[s1, 1.0 - s1]] * T, rtol=1e-14)
+    # aux = E * (f0 P0 + f2 P2) with f0 = f2 = 1/2, P = softmax(b) for every token
+    Z = math.exp(3) + 1.0 + math.exp(2) + math.exp(1)
+    assert out["aux"] == pytest.approx(4 * 0.5 * (math.exp(3) + math.exp(2)) / Z, rel=1e-14)
+    # dropped tokens contribute nothing
+    assert (out["y"][3:] == 0).all() and np.abs(out["y"][:3]).sum() > 0
+
+
+def check_bias_shift_invariance():
+    # adding one constant to every expert's bias (the Zipf normaliser) shifts all logits of a
+    # token equally: the selection, probabilities and gates do not change
+    rng = _rng(13)
+    x = rng.standard_normal((50, 16))
+    W = rng.standard_normal((24, 16))
+    b = rng.standard_normal(24)
+    i1, g1, p1 = oracle.route(oracle.router_logits(x, W, b), 5)
+    i2, g2, p2 = oracle.route(oracle.router_logits(x, W, b - 7.25), 5)
+    assert np.array_equal(i1, i2)
+    assert np.allclose(p1, p2, rtol=1e-12, atol=0) and np.allclose(g1, g2, rtol=1e-12, atol=0)
+    # ... while a bias that is not constant over experts does change them
+    i3, _, p3 = oracle.route(oracle.router_logits(x, W, b + np.arange(24)), 5)
+    assert not np.array_equal(i1, i3) and not np.allclose(p1, p3)
+
+
+def test_bias_two_experts_closed_form():
+    check_bias_two_experts_closed_form()
+
+
+def test_bias_makes_expert0_win_with_drops():
+    check_bias_makes_expert0_win_with_drops()
+
+
+def test_bias_shift_invariance():
+    check_bias_shift_invariance()
+
+
+def test_zipf_bias_values():
+    # b_e = 1.5 ln(w_{e+1}), w_q = q^-1.1 / sum_q' q'^-1.1: expert 0 hottest, strictly
+    # decreasing, and exp(b / 1.5) sums to one
+    from top_routing_grouped_gemm_gb300 import synth
+    b = synth.zipf_bias(896).double().numpy()
+    assert (np.diff(b) < 0).all()
+    assert np.exp(b / 1.5).sum() == pytest.approx(1.0, rel=1e-5)
+    assert b[1] - b[0] == pytest.approx(-1.5 * 1.1 * math.log(2.0), rel=1e-5)
+
+
 # ---------------------------------------------------------------- aux loss
 
 def test_aux_is_one_for_uniform_probabilities():
@@ -404,3 +492,34 @@ def test_mutation_backward_dropped_lora_term_caught(monkeypatch):
         return dX, {n: (v * 0.5 if n == "A_d" else v) for n, v in g.items()}
     monkeypatch.setattr(O, "expert_backward", wrong)
     _expect_failure(check_backward_finite_differences)
+
+
+def test_mutation_bias_sign_flipped_caught(monkeypatch):
+    def minus_bias(x, w_router, bias=None):
+        L = np.asarray(x, float) @ np.asarray(w_router, float).T
+        return L if bias is None else L - np.asarray(bias, float)[None, :]
+    monkeypatch.setattr(O, "router_logits", minus_bias)
+    monkeypatch.setattr(oracle, "router_logits", minus_bias)
+    _expect_failure(check_bias_two_experts_closed_form)
+    _expect_failure(check_bias_makes_expert0_win_with_drops)
+
+
+def test_mutation_bias_dropped_caught(monkeypatch):
+    def no_bias(x, w_router, bias=None):
+        return np.asarray(x, float) @ np.asarray(w_router, float).T
+    monkeypatch.setattr(O, "router_logits", no_bias)
+    monkeypatch.setattr(oracle, "router_logits", no_bias)
+    _expect_failure(check_bias_two_experts_closed_form)
+    _expect_failure(check_bias_makes_expert0_win_with_drops)
+
+
+def test_mutation_bias_on_selection_only_caught(monkeypatch):
+    # a bias that steers the selection but is left out of the gate probabilities (the
+    # selection-only variant some routers use) changes the gates of the worked example
+    orig_fixed = O.moe_forward_fixed_routing
+
+    def gates_without_bias(x, logits, idx, disp, Wg, Wu, Wd, lora=None, s=0.0):
+        return orig_fixed(x, logits - np.array([3.0, 0.0, 2.0, 1.0])[None, :], idx, disp,
+                          Wg, Wu, Wd, lora, s)
+    monkeypatch.setattr(O, "moe_forward_fixed_routing", gates_without_bias)
+    _expect_failure(check_bias_makes_expert0_win_with_drops)
