@@ -168,6 +168,52 @@ int moe_dispatch_noalloc(const moe_problem* p, const int32_t* topk_idx, const mo
                          int32_t* row_slot, int32_t* n_kept_dropped, moe_bf16* x_perm,
                          int32_t* dev_status, moe_stream_t stream);
 
+/* ==================================================================== expert parallelism
+ * The exchange of "Trillion-Parameter MoE Model Training Adaptation: Full-Stack Optimization
+ * Practices", section 3 "Communication" (tokens permuted by routing result are sent with an
+ * All-to-All to the GPUs hosting their experts, computed in grouped GEMMs, unpermuted and
+ * returned) and section 4.1 (EP: the experts split evenly over the ranks, E/P contiguous
+ * experts per rank).  The collectives themselves are the caller's (NCCL or any all-to-all);
+ * these calls are the per-rank steps around them.
+ *
+ * moe_expert_counts: counts[e] = number of slots of topk_idx routed to expert e (before any
+ * drop), overwritten.  Deterministic.  counts [E] int32.
+ *
+ * moe_dispatch_ep: moe_dispatch for one rank's tokens when the capacity is shared with the
+ * other ranks' tokens in global arrival order (ranks in order, then tokens).  pos_base [E]
+ * int32 (device, may be NULL = all zeros) holds, per expert, the number of its slots that
+ * arrived on earlier ranks; a slot at local position pos is kept iff
+ * pos_base[e] + pos < C, so kept_e = clamp(C - pos_base[e], 0, counts[e]) and offsets is
+ * their exclusive scan.  C is computed from p as in moe_dispatch (ceil(cf * T * k / E)); when
+ * the capacity covers the tokens of P ranks, pass cap_num multiplied by P (the same ceiling
+ * of cf * P * T * k / E).  With pos_base NULL and gate_perm NULL it equals moe_dispatch.
+ * gate_perm [T*k] fp32 (may be NULL): gate_perm[row] = topk_gate[row_slot[row]], the gate
+ * travelling with each permuted row to the rank that computes it.  Workspace: as
+ * moe_dispatch (moe_dispatch_workspace_size).
+ *
+ * moe_ep_regroup: moves rows (d bf16 values each) and optionally one fp32 gate per row
+ * between the two layouts of the exchange.  kept [n_sources * n_local_experts] int32
+ * (device): rows of (source s, local expert e) at index s * n_local_experts + e.
+ * Source-major layout: blocks ordered (s, e), as an all-to-all delivers them; expert-major:
+ * blocks ordered (e, s), one contiguous group per local expert for the grouped GEMM (sources
+ * in rank order, i.e. global arrival order).  to_expert_major = 1 moves source-major src
+ * into expert-major dst, 0 the reverse.  rows_total = the sum of kept (a launch-size hint,
+ * known to the caller from the counts exchange).  expert_offsets [n_local_experts + 1]
+ * (may be NULL) receives the expert-major group starts.  src and dst must not overlap.
+ */
+int moe_expert_counts(const moe_problem* p, const int32_t* topk_idx, int32_t* counts,
+                      int32_t* dev_status, moe_stream_t stream);
+int moe_dispatch_ep(const moe_problem* p, const int32_t* topk_idx, const float* topk_gate,
+                    const moe_bf16* x, const int32_t* pos_base, int32_t* counts,
+                    int32_t* offsets, int32_t* slot_row, int32_t* row_slot,
+                    int32_t* n_kept_dropped, moe_bf16* x_perm, float* gate_perm,
+                    void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                    moe_stream_t stream);
+int moe_ep_regroup(const moe_bf16* src, const float* gate_src, const int32_t* kept,
+                   int32_t n_sources, int32_t n_local_experts, int32_t d,
+                   int32_t to_expert_major, int64_t rows_total, moe_bf16* dst,
+                   float* gate_dst, int32_t* expert_offsets, moe_stream_t stream);
+
 /* ==================================================================== experts
  * Grouped SwiGLU expert GEMMs with LoRA ("Trillion-Parameter MoE Model Training
  * Adaptation ...", section 4.3: grouped GEMM over experts; "Adapting Trillion-Parameter

@@ -242,6 +242,59 @@ int moe_dispatch(const moe_problem* p, const int32_t* topk_idx, const moe_bf16* 
   return MOE_OK;
 }
 
+int moe_dispatch_ep(const moe_problem* p, const int32_t* topk_idx, const float* topk_gate,
+                    const moe_bf16* x, const int32_t* pos_base, int32_t* counts,
+                    int32_t* offsets, int32_t* slot_row, int32_t* row_slot,
+                    int32_t* n_kept_dropped, moe_bf16* x_perm, float* gate_perm,
+                    void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                    moe_stream_t stream) {
+  MOE_TRY(check_problem(p));
+  if (!topk_idx || !counts || !offsets || !slot_row || !row_slot || !n_kept_dropped)
+    return MOE_ERR_INVALID_ARG;
+  if ((x_perm && !x) || (gate_perm && !topk_gate)) return MOE_ERR_INVALID_ARG;
+  if ((x && !al16(x)) || (x_perm && !al16(x_perm))) return MOE_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < dispatch_ws(p)) return MOE_ERR_WORKSPACE;
+  Carver cv{static_cast<uint8_t*>(workspace), 0};
+  int32_t* local_rank = cv.take<int32_t>(static_cast<size_t>(p->T) * p->k);
+  int32_t* chunk_cnt = cv.take<int32_t>(static_cast<size_t>(dispatch_num_chunks(p->T)) * p->E);
+  mark_before(MOE_KERNEL_DISPATCH, stream);
+  MOE_CUDA(launch_dispatch(topk_idx, reinterpret_cast<const __nv_bfloat16*>(x), p->T, p->d,
+                           p->E, p->k, capacity_of(p), counts, offsets, slot_row, row_slot,
+                           n_kept_dropped, reinterpret_cast<__nv_bfloat16*>(x_perm), local_rank,
+                           chunk_cnt, dev_status, stream, pos_base, topk_gate, gate_perm));
+  mark_after(MOE_KERNEL_DISPATCH, stream);
+  count_launches(4);
+  return MOE_OK;
+}
+
+int moe_expert_counts(const moe_problem* p, const int32_t* topk_idx, int32_t* counts,
+                      int32_t* dev_status, moe_stream_t stream) {
+  MOE_TRY(check_problem(p));
+  if (!topk_idx || !counts) return MOE_ERR_INVALID_ARG;
+  MOE_CUDA(launch_expert_counts(topk_idx, static_cast<long long>(p->T) * p->k, p->E, counts,
+                                dev_status, stream));
+  count_launches(2);
+  return MOE_OK;
+}
+
+int moe_ep_regroup(const moe_bf16* src, const float* gate_src, const int32_t* kept,
+                   int32_t n_sources, int32_t n_local_experts, int32_t d,
+                   int32_t to_expert_major, int64_t rows_total, moe_bf16* dst,
+                   float* gate_dst, int32_t* expert_offsets, moe_stream_t stream) {
+  if (!kept || n_sources <= 0 || n_local_experts <= 0 || d <= 0 || rows_total < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(n_sources) * n_local_experts > 65536) return MOE_ERR_UNSUPPORTED;
+  if ((gate_src == nullptr) != (gate_dst == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (rows_total > 0 && (!src || !dst)) return MOE_ERR_INVALID_ARG;
+  if (d % 8 || (src && !al16(src)) || (dst && !al16(dst))) return MOE_ERR_UNSUPPORTED;
+  MOE_CUDA(launch_ep_regroup(reinterpret_cast<const __nv_bfloat16*>(src), gate_src, kept,
+                             n_sources, n_local_experts, d, to_expert_major ? 1 : 0, rows_total,
+                             reinterpret_cast<__nv_bfloat16*>(dst), gate_dst, expert_offsets,
+                             stream));
+  count_launches(1);
+  return MOE_OK;
+}
+
 // ------------------------------------------------------------------------ experts
 
 size_t moe_expert_ffn_workspace_size(const moe_problem* p, int32_t rows_max) {

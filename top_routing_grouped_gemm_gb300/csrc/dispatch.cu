@@ -130,13 +130,20 @@ __global__ void __launch_bounds__(1024) dispatch_scan_chunks_kernel(
 }
 
 // Pass 3: kept counts, expert offsets, n_kept / n_dropped.  One block, thread = expert.
+// pos_base[e] (may be null): slots of expert e that arrived before this batch's first token
+// (held elsewhere); they occupy the first places of the expert's capacity.
 __global__ void __launch_bounds__(1024) dispatch_offsets_kernel(
-    const int32_t* __restrict__ counts, int E, int capacity, int slots,
-    int32_t* __restrict__ offsets, int32_t* __restrict__ n_kept_dropped) {
+    const int32_t* __restrict__ counts, const int32_t* __restrict__ pos_base, int E,
+    int capacity, int slots, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ n_kept_dropped) {
   __shared__ int sm[32];
   const int e = threadIdx.x;
   int kept = 0;
-  if (e < E) kept = capacity < 0 ? counts[e] : min(counts[e], capacity);
+  if (e < E) {
+    const int room = capacity < 0 ? counts[e]
+                                  : max(0, capacity - (pos_base ? max(0, pos_base[e]) : 0));
+    kept = min(counts[e], room);
+  }
   int total;
   const int excl = block_exclusive_scan_1024(kept, sm, &total);
   if (e < E) offsets[e] = excl;
@@ -154,9 +161,10 @@ constexpr int kRowThreads = 128;
 __global__ void __launch_bounds__(kRowThreads) dispatch_scatter_kernel(
     const int32_t* __restrict__ idx, const int32_t* __restrict__ local_rank,
     const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
-    const int32_t* __restrict__ n_kept_dropped, const uint4* __restrict__ x, int T, int d,
-    int E, int k, int capacity, int32_t* __restrict__ slot_row, int32_t* __restrict__ row_slot,
-    uint4* __restrict__ x_perm) {
+    const int32_t* __restrict__ n_kept_dropped, const int32_t* __restrict__ pos_base,
+    const float* __restrict__ gate, const uint4* __restrict__ x, int T, int d, int E, int k,
+    int capacity, int32_t* __restrict__ slot_row, int32_t* __restrict__ row_slot,
+    float* __restrict__ gate_perm, uint4* __restrict__ x_perm) {
   __shared__ int rows[32];
   const int t = blockIdx.x;
   const int slots = T * k;
@@ -176,10 +184,14 @@ __global__ void __launch_bounds__(kRowThreads) dispatch_scatter_kernel(
       const int lr = local_rank[slot];
       if (e >= 0 && e < E && lr >= 0) {
         const int pos = chunk_base[static_cast<size_t>(t / kDispatchChunk) * E + e] + lr;
-        if (capacity < 0 || pos < capacity) row = offsets[e] + pos;
+        const int base = pos_base ? max(0, pos_base[e]) : 0;
+        if (capacity < 0 || base + pos < capacity) row = offsets[e] + pos;
       }
       slot_row[slot] = row;
-      if (row >= 0) row_slot[row] = slot;
+      if (row >= 0) {
+        row_slot[row] = slot;
+        if (gate_perm) gate_perm[row] = gate[slot];
+      }
     }
     rows[lane] = row;
   }
@@ -369,6 +381,98 @@ __global__ void __launch_bounds__(kRowThreads) route_bwd_kernel(
   }
 }
 
+// ---------------------------------------------------------------- expert parallelism
+//
+// "Trillion-Parameter MoE Model Training Adaptation: Full-Stack Optimization Practices",
+// section 3 "Communication" and section 4.1: experts split evenly over the ranks of the
+// expert-parallel group; tokens permuted by routing result are sent with an all-to-all to
+// the ranks holding their experts, computed there as grouped GEMMs, and returned.
+
+__global__ void zero_i32_kernel(int32_t* __restrict__ v, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    v[i] = 0;
+}
+
+// counts[e] += number of slots routed to e (integer atomics: the totals do not depend on
+// their order).  Per-block shared-memory histograms, one global add per (block, expert).
+__global__ void __launch_bounds__(1024) expert_histogram_kernel(
+    const int32_t* __restrict__ idx, long long slots, int E, int32_t* __restrict__ counts,
+    int32_t* dev_status) {
+  extern __shared__ int hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < slots;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int e = idx[i];
+    if (e < 0 || e >= E) {
+      report_status(dev_status, MOE_ERR_BAD_INDEX);
+      continue;
+    }
+    atomicAdd(&hist[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (hist[e]) atomicAdd(&counts[e], hist[e]);
+}
+
+// Rows move between the two layouts of an expert-parallel exchange.  kept[s * El + e] rows
+// belong to (source s, local expert e).  Source-major layout: blocks ordered (s, e) (what
+// the all-to-all delivers); expert-major layout: blocks ordered (e, s) (one contiguous
+// group per expert for the grouped GEMM, sources in rank order = global arrival order).
+// to_expert = 1 moves source-major -> expert-major, 0 the reverse.  One block per (s, e)
+// pair (several when its rows are many); each finds its two block offsets by summing the
+// kept counts before it in either order.
+__global__ void __launch_bounds__(256) ep_regroup_kernel(
+    const uint4* __restrict__ src, const float* __restrict__ gsrc,
+    const int32_t* __restrict__ kept, int P, int El, int nvec, int to_expert, int parts,
+    uint4* __restrict__ dst, float* __restrict__ gdst, int32_t* __restrict__ expert_offsets) {
+  __shared__ long long red[2][8];
+  const int pair = blockIdx.x / parts;
+  const int part = blockIdx.x - pair * parts;
+  const int s = pair / El, e = pair - s * El;
+  long long off_se = 0, off_es = 0;
+  for (int i = threadIdx.x; i < P * El; i += blockDim.x) {
+    const int si = i / El, ei = i - si * El;
+    const long long c = kept[i];
+    if (i < pair) off_se += c;                       // (si, ei) before (s, e), source-major
+    if (ei < e || (ei == e && si < s)) off_es += c;  // (ei, si) before (e, s), expert-major
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    off_se += __shfl_xor_sync(0xffffffffu, off_se, o);
+    off_es += __shfl_xor_sync(0xffffffffu, off_es, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[0][threadIdx.x >> 5] = off_se;
+    red[1][threadIdx.x >> 5] = off_es;
+  }
+  __syncthreads();
+  off_se = 0;
+  off_es = 0;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+    off_se += red[0][w];
+    off_es += red[1][w];
+  }
+  const int rows = kept[pair];
+  if (expert_offsets && s == 0 && part == 0) {
+    expert_offsets[e] = static_cast<int32_t>(off_es);
+    if (e == El - 1 && threadIdx.x == 0) {
+      long long total = 0;
+      for (int i = 0; i < P * El; ++i) total += kept[i];
+      expert_offsets[El] = static_cast<int32_t>(total);
+    }
+  }
+  const long long from = to_expert ? off_se : off_es;
+  const long long to = to_expert ? off_es : off_se;
+  const long long n = static_cast<long long>(rows) * nvec;
+  for (long long i = part * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(parts) * blockDim.x)
+    dst[to * nvec + i] = src[from * nvec + i];
+  if (gsrc && gdst)
+    for (int i = part * blockDim.x + threadIdx.x; i < rows; i += parts * blockDim.x)
+      gdst[to + i] = gsrc[from + i];
+}
+
 int grid_for_slots(long long slots) { return static_cast<int>((slots + 7) / 8); }
 
 }  // namespace
@@ -377,17 +481,41 @@ int launch_dispatch(const int32_t* idx, const __nv_bfloat16* x, int T, int d, in
                     int capacity, int32_t* counts, int32_t* offsets, int32_t* slot_row,
                     int32_t* row_slot, int32_t* n_kept_dropped, __nv_bfloat16* x_perm,
                     int32_t* local_rank, int32_t* chunk_cnt, int32_t* dev_status,
-                    cudaStream_t s) {
+                    cudaStream_t s, const int32_t* pos_base, const float* gate,
+                    float* gate_perm) {
   const int nch = dispatch_num_chunks(T);
   dispatch_count_kernel<<<(nch + kCountWarps - 1) / kCountWarps, 32 * kCountWarps,
                           kCountWarps * E * sizeof(int), s>>>(idx, T, E, k, local_rank, chunk_cnt,
                                                               dev_status);
   dispatch_scan_chunks_kernel<<<(E + 31) / 32, 1024, 0, s>>>(chunk_cnt, nch, E, counts);
-  dispatch_offsets_kernel<<<1, 1024, 0, s>>>(counts, E, capacity, T * k, offsets,
+  dispatch_offsets_kernel<<<1, 1024, 0, s>>>(counts, pos_base, E, capacity, T * k, offsets,
                                              n_kept_dropped);
   dispatch_scatter_kernel<<<T, kRowThreads, 0, s>>>(
-      idx, local_rank, chunk_cnt, offsets, n_kept_dropped, reinterpret_cast<const uint4*>(x),
-      T, d, E, k, capacity, slot_row, row_slot, reinterpret_cast<uint4*>(x_perm));
+      idx, local_rank, chunk_cnt, offsets, n_kept_dropped, pos_base, gate,
+      reinterpret_cast<const uint4*>(x), T, d, E, k, capacity, slot_row, row_slot, gate_perm,
+      reinterpret_cast<uint4*>(x_perm));
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_expert_counts(const int32_t* idx, long long slots, int E, int32_t* counts,
+                         int32_t* dev_status, cudaStream_t s) {
+  zero_i32_kernel<<<1, 1024, 0, s>>>(counts, E);
+  const int blocks = static_cast<int>(std::min<long long>((slots + 1023) / 1024, 2 * 152));
+  expert_histogram_kernel<<<std::max(blocks, 1), 1024, E * sizeof(int), s>>>(idx, slots, E,
+                                                                             counts, dev_status);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_ep_regroup(const __nv_bfloat16* src, const float* gsrc, const int32_t* kept, int P,
+                      int El, int d, int to_expert, long long rows_hint, __nv_bfloat16* dst,
+                      float* gdst, int32_t* expert_offsets, cudaStream_t s) {
+  // enough blocks per (source, expert) pair to cover about two waves for the expected rows
+  const long long pairs = static_cast<long long>(P) * El;
+  const long long per_pair = std::max<long long>(1, rows_hint / std::max<long long>(1, pairs));
+  const int parts = static_cast<int>(std::min<long long>(8, std::max<long long>(1, per_pair / 64)));
+  ep_regroup_kernel<<<static_cast<int>(pairs * parts), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(src), gsrc, kept, P, El, d / 8, to_expert, parts,
+      reinterpret_cast<uint4*>(dst), gdst, expert_offsets);
   return static_cast<int>(cudaGetLastError());
 }
 

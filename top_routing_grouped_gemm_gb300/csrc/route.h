@@ -25,12 +25,23 @@ int launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* idx, 
 int launch_aux_loss(const int32_t* counts, const float* partials, int n_partials, int T, int k,
                     int E, float* aux_out, float* block_terms, cudaStream_t s);
 
-// capacity < 0 means unlimited.
+// capacity < 0 means unlimited.  pos_base [E] (may be null): slots of each expert that
+// arrived before this batch (held elsewhere).  gate / gate_perm (may be null): per-slot
+// gates gathered into row order.
 int launch_dispatch(const int32_t* idx, const __nv_bfloat16* x, int T, int d, int E, int k,
                     int capacity, int32_t* counts, int32_t* offsets, int32_t* slot_row,
                     int32_t* row_slot, int32_t* n_kept_dropped, __nv_bfloat16* x_perm,
                     int32_t* local_rank, int32_t* chunk_cnt, int32_t* dev_status,
-                    cudaStream_t s);
+                    cudaStream_t s, const int32_t* pos_base = nullptr,
+                    const float* gate = nullptr, float* gate_perm = nullptr);
+// counts[e] = slots of idx routed to expert e (overwritten)
+int launch_expert_counts(const int32_t* idx, long long slots, int E, int32_t* counts,
+                         int32_t* dev_status, cudaStream_t s);
+// rows (and per-row gates) between the source-major and expert-major layouts of an
+// expert-parallel exchange; expert_offsets [El+1] (may be null) gets the expert-major starts
+int launch_ep_regroup(const __nv_bfloat16* src, const float* gsrc, const int32_t* kept, int P,
+                      int El, int d, int to_expert, long long rows_hint, __nv_bfloat16* dst,
+                      float* gdst, int32_t* expert_offsets, cudaStream_t s);
 int launch_tile_schedule(const int32_t* offsets, int E, int rows_max, int32_t* tile_off,
                          int32_t* pair_off, int32_t* dev_status, cudaStream_t s);
 int launch_combine(const __nv_bfloat16* y_perm, const int32_t* slot_row, int T, int d, int k,

@@ -66,6 +66,11 @@ _SIGS = {
     "moe_dispatch_workspace_size": (c_sz, [_P]),
     "moe_dispatch": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "moe_dispatch_noalloc": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "moe_dispatch_ep": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                       c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+    "moe_expert_counts": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp]),
+    "moe_ep_regroup": (ctypes.c_int, [c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32,
+                                      ctypes.c_int64, c_vp, c_vp, c_vp, c_vp]),
     "moe_expert_ffn_workspace_size": (c_sz, [_P, c_i32]),
     "moe_expert_ffn": (ctypes.c_int, [_P, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                       ctypes.POINTER(moe_lora), c_vp, c_vp,
@@ -228,6 +233,30 @@ def moe_dispatch_noalloc(p, topk_idx, x, counts, offsets, slot_row, row_slot, n_
            lib().moe_dispatch_noalloc(p.c(), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets),
                                       _ptr(slot_row), _ptr(row_slot), _ptr(n_kept_dropped),
                                       _ptr(x_perm), _ptr(dev_status), _stream(stream)))
+
+
+def moe_dispatch_ep(p, topk_idx, topk_gate, x, pos_base, counts, offsets, slot_row, row_slot,
+                    n_kept_dropped, x_perm, gate_perm, workspace, dev_status=None, stream=None):
+    wp, wn = _ws(workspace)
+    _check("moe_dispatch_ep",
+           lib().moe_dispatch_ep(p.c(), _ptr(topk_idx), _ptr(topk_gate), _ptr(x), _ptr(pos_base),
+                                 _ptr(counts), _ptr(offsets), _ptr(slot_row), _ptr(row_slot),
+                                 _ptr(n_kept_dropped), _ptr(x_perm), _ptr(gate_perm), wp, wn,
+                                 _ptr(dev_status), _stream(stream)))
+
+
+def moe_expert_counts(p, topk_idx, counts, dev_status=None, stream=None):
+    _check("moe_expert_counts", lib().moe_expert_counts(p.c(), _ptr(topk_idx), _ptr(counts),
+                                                        _ptr(dev_status), _stream(stream)))
+
+
+def moe_ep_regroup(src, gate_src, kept, n_sources, n_local_experts, d, to_expert_major,
+                   rows_total, dst, gate_dst, expert_offsets, stream=None):
+    _check("moe_ep_regroup",
+           lib().moe_ep_regroup(_ptr(src), _ptr(gate_src), _ptr(kept), n_sources,
+                                n_local_experts, d, 1 if to_expert_major else 0, rows_total,
+                                _ptr(dst), _ptr(gate_dst), _ptr(expert_offsets),
+                                _stream(stream)))
 
 
 def moe_expert_ffn_workspace_size(p: Problem, rows_max: int) -> int:
