@@ -1,32 +1,43 @@
 #!/usr/bin/env python
-"""Throughput of the sparse-MoE layer (route -> dispatch -> grouped SwiGLU experts ->
-combine -> aux loss) on one GB300, through the C ABI of libmoe.so.
+"""Throughput of the sparse-MoE layer (route -> dispatch -> grouped SwiGLU experts with LoRA
+-> combine -> aux loss, and for training workloads the LoRA backward) on one GB300, through
+the C ABI of libmoe.so.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5] [--impl ours|reference]
 
-One step is one forward pass of the whole layer over one batch of the workload's seeded
-synthetic tokens, with every input already resident in HBM.  Rank 0 prints one JSON line.
+The headline workload is c5 (T=8192 tokens, d=4096, 896 experts, top-16, F=1024, LoRA r=32:
+forward plus the whole LoRA backward), the configuration with the most work per step.  The
+line also carries sub-records for c2 (full-fanout routing), c3 (skewed routing with capacity
+drops) and c4 (LoRA forward on one 14-expert shard, the tensor-bound grouped GEMM), each
+with its own roofline.  One step is one pass of the whole layer over one batch of the
+workload's seeded synthetic tokens, every input already resident in HBM.  Rank 0 prints one
+JSON line.
 
   value        tokens/s over all ranks (each rank runs its own batch: weak scaling, no
-               collective on the data path), CUDA events around K steps, max over ranks
-  e2e          the same through the public API with host buffers: pinned x copied in and
-               y (+aux) copied out inside the timed region, every step
-  roofline     the dominant kernel (grouped gate/up GEMM) timed live by CUDA events recorded
-               by the library around its launches, against MEASURED_PEAKS.json
-  cpu_baseline the fp64 oracle, single BLAS thread, on a bounded sample of the same batch
-  --impl reference  times the oracle alone (the slow reference program of this build)
+               collective on the data path), CUDA events around K steps replayed as one CUDA
+               graph, max over ranks
+  e2e          the same through the public API with host buffers: pinned inputs copied in
+               and outputs copied out inside the timed region, every step
+  roofline     the dominant kernel, timed live by CUDA events the library records around its
+               launches, against MEASURED_PEAKS.json
+  cpu_baseline the fp64 oracle on a bounded sample of the same batch, on every host core
+               (one thread per token shard, one BLAS thread each), plus the same oracle on
+               one core
+  --impl reference  times the oracle alone (the slow reference program of this build) on
+               the host cores, same workload, metric and unit
 """
 
 from __future__ import annotations
 
 import os
 
-# The oracle baseline runs numpy with one BLAS thread (set before numpy is imported).
+# The oracle runs numpy with one BLAS thread per worker thread (set before numpy loads).
 os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
 os.environ.setdefault("OMP_NUM_THREADS", "1")
 os.environ.setdefault("MKL_NUM_THREADS", "1")
 
 import argparse
+import concurrent.futures as cf
 import hashlib
 import json
 import statistics
@@ -38,28 +49,40 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer tokens/s and grouped-GEMM TFLOP/s (% BF16 peak), 1×GB300"
-KERNEL_SOURCES = ["gemm.cuh", "ptx.cuh", "gemm_fwd.cu", "moe_internal.h"]
+KERNEL_SOURCES = ["gemm.cuh", "ptx.cuh", "gemm_fwd.cu", "gemm_bwd.cu", "moe_internal.h"]
+DEFAULT_WORKLOAD = "c5"
+# sub-records carried by the headline line
+DEFAULT_SUBS = {"c5": ["c2", "c3", "c4"]}
+# tokens per host thread of the oracle baseline (forward-only workloads run more tokens:
+# their oracle step is cheaper)
+CPU_TOKENS_PER_THREAD = {"train": 2, "fwd": 16, "prepermuted_rows": 64}
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="c2")
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--sub-workloads", default="auto",
+                    help="comma-separated workloads reported as sub-records of the line; "
+                         "'auto': c2,c3,c4 under the c5 headline; 'none': no sub-records")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-sample", type=int, default=4096,
-                    help="tokens of the batch the oracle baseline runs on (the whole c2 batch: "
-                         "about 10-15 s of one CPU core)")
-    ap.add_argument("--ref-tokens-per-step", type=int, default=2,
-                    help="tokens per step of the --impl reference arm (the oracle)")
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="host threads of the oracle baseline and the reference arm (0: all "
+                         "cores this process may run on)")
+    ap.add_argument("--cpu-tokens-per-thread", type=int, default=0,
+                    help="tokens (rows for c4) per host thread of the oracle baseline "
+                         "(0: the workload's default)")
+    ap.add_argument("--ref-tokens-per-step", type=int, default=0,
+                    help="tokens per step of the --impl reference arm (0: one per thread)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--permute", default="auto", choices=["auto", "fused", "separate"],
                     help="fused: gather token rows inside the expert GEMM; separate: write "
                          "x_perm in dispatch; auto: the library binding's default")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch every step from the host instead of replaying a CUDA graph")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def peaks():
@@ -106,6 +129,25 @@ def profiled_traffic(kernel, workload):
         return float(vals["traffic_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
+
+
+def host_threads():
+    """Host cores this process may run on."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def host_mem_available():
+    """Bytes of host memory available (MemAvailable), or a large number if unknown."""
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 1 << 50
 
 
 # ------------------------------------------------------------------------ multi-rank
@@ -183,101 +225,262 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------ oracle baseline
+#
+# The oracle is timed as it stands: its public moe_forward / moe_backward / expert_forward
+# on shards of a token sample, one shard per host thread.  numpy releases the interpreter
+# lock inside its array kernels (matrix products, dtype conversions, exp), so the shards
+# run side by side; every thread uses one BLAS thread.
 
 class HostExperts:
-    """[E, rows, cols] weight table of which only some experts are held on the host (as
-    float32, exact for bf16 values); the oracle converts each expert to fp64 on use."""
+    """[E, rows, cols] weight table of which only the experts a sample touches are held on
+    the host, as bf16 torch tensors; an access returns the expert as float32 numpy (exact for
+    bf16 values), which the oracle converts to float64."""
 
     def __init__(self, E, rows, cols):
         self.shape = (E, rows, cols)
         self.store = {}
 
     def __getitem__(self, e):
-        return self.store[int(e)]
+        return self.store[int(e)].float().numpy()
 
 
-def oracle_sample_run(x_rows, w_router, tables, k, bias=None):
-    """Time the oracle's whole forward on a sample of tokens; returns seconds."""
-    import oracle
+def run_sharded(fn, shards, threads):
+    """Run fn(shard) for every shard on `threads` host threads; wall seconds."""
     t0 = time.perf_counter()
-    out = oracle.moe_forward(x_rows, w_router, tables[0], tables[1], tables[2], k, bias=bias)
-    dt = time.perf_counter() - t0
-    return dt, out
+    if threads == 1:
+        for s in shards:
+            fn(s)
+    else:
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(fn, shards))
+    return time.perf_counter() - t0
 
 
-def cpu_baseline_from_device(inp, cfg, n_tok):
-    """Oracle on the first n_tok tokens of the device batch (weights of the experts those
-    tokens select copied to the host before timing)."""
+class OracleProblem:
+    """Host copies of one workload's inputs (only the experts a token sample touches) and the
+    oracle step on a shard of that sample: the whole forward (and the LoRA backward for
+    training workloads) of those tokens, or, for a pre-permuted shard, the expert forward of
+    those rows."""
+
+    def __init__(self, cfg, x, w_router, bias, dy, tables, lora, rows=None):
+        self.cfg = cfg
+        self.x, self.w_router, self.bias, self.dy = x, w_router, bias, dy
+        self.tables = tables
+        self.lora = lora
+        self.rows = rows   # pre-permuted: blocks (expert, first row, end row) of x
+
+    def step(self, shard):
+        import oracle
+        cfg = self.cfg
+        s = cfg.lora_scale
+        if cfg.prepermuted:
+            for e, lo, hi in shard:
+                L = None if self.lora is None else {n: v[e] for n, v in self.lora.items()}
+                oracle.expert_forward(self.x[lo:hi], self.tables[0][e], self.tables[1][e],
+                                      self.tables[2][e], L, s)
+            return
+        xs = self.x[shard]
+        fwd = oracle.moe_forward(xs, self.w_router, self.tables[0], self.tables[1],
+                                 self.tables[2], cfg.k, cfg.cap_num, cfg.cap_den,
+                                 bias=self.bias, lora=self.lora, s=s)
+        if cfg.backward:
+            oracle.moe_backward(fwd, xs, self.dy[shard], self.w_router, self.tables[0],
+                                self.tables[1], self.tables[2], self.lora, s)
+
+
+def _touched_experts(cfg, x64, wr64, bias64):
     import numpy as np
     import oracle
-    x = inp["x"][:n_tok].float().cpu().double().numpy()
-    wr = inp["w_router"].cpu().double().numpy()
-    bias = None if inp.get("bias") is None else inp["bias"].cpu().double().numpy()
-    idx = oracle.topk_select(oracle.router_logits(x, wr, bias), cfg.k)
-    tabs = [HostExperts(cfg.E, cfg.F, cfg.d), HostExperts(cfg.E, cfg.F, cfg.d),
-            HostExperts(cfg.E, cfg.d, cfg.F)]
-    for e in np.unique(idx):
-        for tab, name in zip(tabs, ("w_gate", "w_up", "w_down")):
-            tab.store[int(e)] = inp[name][int(e)].float().cpu().numpy()
-    dt, _ = oracle_sample_run(x, wr, tabs, cfg.k, bias)
-    return {"value": n_tok / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {n_tok} tokens of the {cfg.name} batch: fp64 router over all "
-                      f"{cfg.E} experts, top-{cfg.k}, {len(np.unique(idx))} experts' SwiGLU, "
-                      f"combine; numpy, 1 BLAS thread", "seconds": dt}
+    idx = oracle.topk_select(oracle.router_logits(x64, wr64, bias64), cfg.k)
+    return [int(e) for e in np.unique(idx)]
+
+
+def _lora_host(cfg, get, experts):
+    """float64 LoRA factors [E, ...] with the touched experts filled (others never read)."""
+    import numpy as np
+    if not cfg.r:
+        return None
+    shapes = {"A_g": (cfg.r, cfg.d), "B_g": (cfg.F, cfg.r), "A_u": (cfg.r, cfg.d),
+              "B_u": (cfg.F, cfg.r), "A_d": (cfg.r, cfg.F), "B_d": (cfg.d, cfg.r)}
+    out = {n: np.zeros((cfg.E,) + sh) for n, sh in shapes.items()}
+    for e in experts:
+        for n in shapes:
+            out[n][e] = get(n, e)
+    return out
+
+
+def oracle_problem_from_device(inp, cfg, n_tokens):
+    """The oracle's inputs for the first n_tokens tokens (rows, for c4) of the device batch:
+    the same values the CUDA path consumes."""
+    import numpy as np
+    f64 = lambda t: t.detach().float().cpu().double().numpy()
+    names = ("w_gate", "w_up", "w_down")
+    shapes = ((cfg.E, cfg.F, cfg.d), (cfg.E, cfg.F, cfg.d), (cfg.E, cfg.d, cfg.F))
+    tabs = [HostExperts(*sh) for sh in shapes]
+    if cfg.prepermuted:
+        # the first rows of every expert, copied compactly; blocks (expert, start, end) index
+        # the compact copy
+        offs = inp["offsets"].cpu().tolist()
+        per = max(1, n_tokens // cfg.E)
+        blocks, sel = [], []
+        for e in range(cfg.E):
+            lo = offs[e]
+            hi = min(offs[e + 1], lo + per)
+            if hi > lo:
+                blocks.append((e, len(sel), len(sel) + hi - lo))
+                sel.extend(range(lo, hi))
+        x = f64(inp["x_perm"][sel])
+        experts = sorted({e for e, _, _ in blocks})
+        for e in experts:
+            for tab, n in zip(tabs, names):
+                tab.store[e] = inp[n][e].cpu()
+        lora = _lora_host(cfg, lambda n, e: f64(inp["lora"][n][e]), experts)
+        return OracleProblem(cfg, x, None, None, None, tabs, lora, blocks), len(sel)
+    n = min(n_tokens, cfg.T)
+    wr = f64(inp["w_router"])
+    bias = None if inp.get("bias") is None else f64(inp["bias"])
+    while True:
+        x = f64(inp["x"][:n])
+        experts = _touched_experts(cfg, x, wr, bias)
+        # the touched experts' bf16 weights are held on the host: keep them well inside the
+        # host memory (halve the sample until they fit)
+        if n == 1 or len(experts) * 6 * cfg.d * cfg.F <= 0.3 * host_mem_available():
+            break
+        n //= 2
+    for e in experts:
+        for tab, nm in zip(tabs, names):
+            tab.store[e] = inp[nm][e].cpu()
+    lora = _lora_host(cfg, lambda nm, e: f64(inp["lora"][nm][e]), experts)
+    dy = f64(inp["dy"][:n]) if cfg.backward else None
+    return OracleProblem(cfg, x, wr, bias, dy, tabs, lora), n
+
+
+def shards_of(prob, n_units, threads):
+    """Split the sample into `threads` contiguous shards."""
+    import numpy as np
+    if prob.cfg.prepermuted:
+        blocks = prob.rows
+        return [blocks[i::threads] for i in range(threads) if blocks[i::threads]]
+    parts = np.array_split(np.arange(n_units), threads)
+    return [p for p in parts if len(p)]
+
+
+def cpu_baseline(inp, cfg, args):
+    """The oracle on every host core (the timed CPU baseline) and on one core."""
+    threads = args.cpu_threads or host_threads()
+    kind = "prepermuted_rows" if cfg.prepermuted else ("train" if cfg.backward else "fwd")
+    per = args.cpu_tokens_per_thread or CPU_TOKENS_PER_THREAD[kind]
+    prob, n = oracle_problem_from_device(inp, cfg, per * threads)
+    shards = shards_of(prob, n, threads)
+    unit = "token-slots/s" if cfg.prepermuted else "tokens/s"
+    size = (lambda sh: sum(hi - lo for _, lo, hi in sh)) if cfg.prepermuted else len
+    wall = run_sharded(prob.step, shards, len(shards))
+    one = shards[0]
+    wall1 = run_sharded(prob.step, [one], 1)
+    what = ("expert forward (SwiGLU with LoRA) of the first rows of every expert"
+            if cfg.prepermuted else
+            "fp64 router over all experts, top-k, dispatch, the selected experts' SwiGLU"
+            + (" with LoRA" if cfg.r else "") + ", combine, aux"
+            + (" + the LoRA backward (dx, dA, dB)" if cfg.backward else ""))
+    return {"value": n / wall, "unit": unit, "cores": len(shards), "kind": "oracle",
+            "sample": f"first {n} {'rows' if cfg.prepermuted else 'tokens'} of the {cfg.name} "
+                      f"batch in {len(shards)} shards, one host thread each (numpy, 1 BLAS "
+                      f"thread per shard): {what}",
+            "seconds": wall,
+            "single_core": {"value": size(one) / wall1, "unit": unit, "cores": 1,
+                            "seconds": wall1, "units": size(one)}}
 
 
 def run_reference(args):
-    """The oracle as the reference program: each step a bounded sample of the workload."""
+    """The oracle as the reference program: every step the same bounded sample of a
+    workload-shaped batch (host-generated, seeded), on every host core."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     import numpy as np
     import torch
-    import oracle
     from top_routing_grouped_gemm_gb300 import synth
-    torch.set_num_threads(1)
     cfg = synth.config(args.workload)
-    per_step = max(1, args.ref_tokens_per_step)
-    n_steps = args.steps + args.warmup
+    threads = getattr(args, "cpu_threads", 0) or host_threads()
+    torch.set_num_threads(threads)
+    n = getattr(args, "ref_tokens_per_step", 0) or threads
     g = torch.Generator().manual_seed(0)
-    x_all = torch.randn((per_step * n_steps, cfg.d), generator=g).to(torch.bfloat16).double().numpy()
-    wr = (torch.randn((cfg.E, cfg.d), generator=g) * 0.02).double().numpy()
-    bias = synth.zipf_bias(cfg.E).double().numpy() if cfg.zipf_bias else None
-    idx = oracle.topk_select(oracle.router_logits(x_all, wr, bias), cfg.k)
-    tabs = [HostExperts(cfg.E, cfg.F, cfg.d), HostExperts(cfg.E, cfg.F, cfg.d),
-            HostExperts(cfg.E, cfg.d, cfg.F)]
-    for e in np.unique(idx):
+    bf = lambda t: t.to(torch.bfloat16)
+    names = ("w_gate", "w_up", "w_down")
+    shapes = ((cfg.F, cfg.d), (cfg.F, cfg.d), (cfg.d, cfg.F))
+    tabs = [HostExperts(cfg.E, *sh) for sh in shapes]
+
+    def expert_weights(e):
         ge = torch.Generator().manual_seed(1000 + int(e))
-        for tab, shape in zip(tabs, ((cfg.F, cfg.d), (cfg.F, cfg.d), (cfg.d, cfg.F))):
-            tab.store[int(e)] = (torch.randn(shape, generator=ge) * 0.02).to(torch.bfloat16).float().numpy()
+        for tab, sh in zip(tabs, shapes):
+            tab.store[int(e)] = bf(torch.randn(sh, generator=ge) * 0.02)
+
+    def lora_of(nm, e):
+        ge = torch.Generator().manual_seed(5000 + 7 * int(e) + "A_g B_g A_u B_u A_d B_d".split().index(nm))
+        sh = {"A_g": (cfg.r, cfg.d), "B_g": (cfg.F, cfg.r), "A_u": (cfg.r, cfg.d),
+              "B_u": (cfg.F, cfg.r), "A_d": (cfg.r, cfg.F), "B_d": (cfg.d, cfg.r)}[nm]
+        std = 0.02 if nm.startswith("A") else 0.01
+        return bf(torch.randn(sh, generator=ge) * std).double().numpy()
+
+    if cfg.prepermuted:
+        per = max(1, n * CPU_TOKENS_PER_THREAD["prepermuted_rows"] // cfg.E)
+        rows = [(e, e * per, (e + 1) * per) for e in range(cfg.E)]
+        x = bf(torch.randn((cfg.E * per, cfg.d), generator=g)).double().numpy()
+        experts = list(range(cfg.E))
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(expert_weights, experts))
+        prob = OracleProblem(cfg, x, None, None, None, tabs, _lora_host(cfg, lora_of, experts),
+                             rows)
+        shards = [rows[i::threads] for i in range(threads) if rows[i::threads]]
+        units = cfg.E * per
+        unit = "token-slots/s"
+    else:
+        x = bf(torch.randn((n, cfg.d), generator=g)).double().numpy()
+        wr = (torch.randn((cfg.E, cfg.d), generator=g) * 0.02).double().numpy()
+        bias = synth.zipf_bias(cfg.E).double().numpy() if cfg.zipf_bias else None
+        dy = bf(torch.randn((n, cfg.d), generator=g)).double().numpy() if cfg.backward else None
+        experts = _touched_experts(cfg, x, wr, bias)
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(expert_weights, experts))
+        prob = OracleProblem(cfg, x, wr, bias, dy, tabs, _lora_host(cfg, lora_of, experts))
+        shards = shards_of(prob, n, threads)
+        units = n
+        unit = "tokens/s"
     times = []
-    for s in range(n_steps):
-        rows = x_all[s * per_step:(s + 1) * per_step]
-        dt, _ = oracle_sample_run(rows, wr, tabs, cfg.k, bias)
+    for s in range(args.steps + args.warmup):
+        dt = run_sharded(prob.step, shards, len(shards))
         if s >= args.warmup:
             times.append(dt)
     total = sum(times)
-    value = per_step * len(times) / total
+    value = units * len(times) / total
+    sample = (f"{units} {'rows' if cfg.prepermuted else 'tokens'} per step of a "
+              f"{cfg.name}-shaped batch (host-generated, seed 0; the same sample every step), "
+              f"in {len(shards)} shards on {len(shards)} host threads: fp64 oracle "
+              + ("expert forward" if cfg.prepermuted else "forward")
+              + (" + LoRA backward" if cfg.backward else "") + ", numpy, 1 BLAS thread each")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1000 * total / len(times), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "ms_per_step": 1000 * total / max(1, len(times)), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(cfg),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{per_step} tokens per step of a {cfg.name}-shaped batch "
-                                   f"(fp64 oracle forward, numpy, 1 BLAS thread)"},
-        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+        "cpu_baseline": {"value": value, "unit": unit, "cores": len(shards), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
 def workload_config(cfg):
-    c = {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} top-{cfg.k} F={cfg.F}"
+    c = {"workload": f"{cfg.name}: "
+                     + (f"{cfg.T * cfg.k} pre-permuted rows over {cfg.E} experts"
+                        if cfg.prepermuted else f"T={cfg.T} top-{cfg.k}")
+                     + f" d={cfg.d} E={cfg.E} F={cfg.F}"
                      + (f" LoRA r={cfg.r} alpha={cfg.alpha:g}" if cfg.r else "")
                      + (f" capacity {cfg.cap_num}/{cfg.cap_den}" if cfg.cap_den else " capacity inf")
-                     + (" Zipf(1.1) router bias" if cfg.zipf_bias else ""),
+                     + (" Zipf(1.1) router bias" if cfg.zipf_bias else "")
+                     + (" forward + LoRA backward" if cfg.backward else " forward"),
          "tokens_per_gpu": cfg.T, "experts": cfg.E, "top_k": cfg.k, "d_model": cfg.d,
          "d_ffn": cfg.F, "lora_rank": cfg.r, "seed": 0,
          "l2": "inputs larger than L2: the expert weights streamed every step exceed 129 MB"}
@@ -326,29 +529,19 @@ def kernel_model(cfg, kept, nonempty, train, gather):
     return m
 
 
-def main():
-    args = parse()
-    if args.impl == "reference":
-        run_reference(args)
-        return
+class Ctx:
+    def __init__(self, args, rank, world, local, barrier):
+        self.args, self.rank, self.world, self.local, self.barrier = (args, rank, world, local,
+                                                                      barrier)
 
+
+def run_workload(name, ctx, with_cpu):
+    """Time one workload on this rank's GPU; returns the fields of its JSON record."""
     import torch
-    import torch.distributed as dist
     from top_routing_grouped_gemm_gb300 import moe, synth
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl")
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-
-    cfg = synth.config(args.workload)
+    args, world, rank = ctx.args, ctx.world, ctx.rank
+    cfg = synth.config(name)
     train = cfg.backward
     fused = {"fused": True, "separate": False}.get(
         args.permute, moe.fused_permute_default(moe.problem_of(cfg), train))
@@ -396,7 +589,7 @@ def main():
     torch.cuda.synchronize()
     st = int(status.item())
     if st != 0:
-        raise RuntimeError(f"device status {moe.STATUS_NAMES.get(st, st)} after warm-up")
+        raise RuntimeError(f"{name}: device status {moe.STATUS_NAMES.get(st, st)} after warm-up")
     if not cfg.prepermuted:
         kept = int(buf.n_kept_dropped[0].item())
         nonempty = int((buf.offsets[1:] - buf.offsets[:-1] > 0).sum().item())
@@ -433,9 +626,9 @@ def main():
                 step()
         torch.cuda.synchronize()
         launches = moe.moe_launch_count() - launches0
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(ctx.local)
     time.sleep(0.3)
-    barrier()
+    ctx.barrier()
     torch.cuda.synchronize()
     launches0 = moe.moe_launch_count()
     start.record(stream)
@@ -445,7 +638,7 @@ def main():
         kernel_timed_steps()
     end.record(stream)
     torch.cuda.synchronize()
-    barrier()
+    ctx.barrier()
     if graph is None:
         launches = moe.moe_launch_count() - launches0
     else:
@@ -454,10 +647,12 @@ def main():
     clocks.stop()
     ms_step = max_over_ranks(start.elapsed_time(end) / K, world, "cuda")
     kern_us = {n: 1000.0 * sum(a.elapsed_time(b2) for a, b2 in ev[n]) / K for n in kernels}
+    del graph
 
     pk = peaks()
     hbm = pk["hbm_gbs"]
     tpeak = pk["bf16_tflops"]
+    tpeak_sus = pk["bf16_tflops_sustained"] or tpeak
     model = kernel_model(cfg, kept, nonempty, train, gather=fused)
     kstats = {}
     for n in kernels:
@@ -478,13 +673,16 @@ def main():
     if dm["bound"] == "tensor":
         roof = {"kernel": dominant, "bound": "tensor", "achieved": dm["TFLOP/s"], "peak": tpeak,
                 "unit": "TFLOP/s", "frac": dm["TFLOP/s"] / tpeak,
-                "traffic": profiled_traffic(dominant, args.workload),
-                "algorithmic_flops": dm["flops"], "peak_source": pk["source"] + " bf16 burst"}
+                "frac_of_sustained": dm["TFLOP/s"] / tpeak_sus,
+                "traffic": profiled_traffic(dominant, name),
+                "algorithmic_flops": dm["flops"], "launch_us": dm["us"],
+                "peak_source": pk["source"] + " bf16 burst"}
     else:
         roof = {"kernel": dominant, "bound": "hbm", "achieved": dm["GB/s"], "peak": hbm,
                 "unit": "GB/s", "frac": dm["GB/s"] / hbm,
-                "traffic": profiled_traffic(dominant, args.workload),
-                "algorithmic_bytes": dm["algorithmic_bytes"], "peak_source": pk["source"]}
+                "traffic": profiled_traffic(dominant, name),
+                "algorithmic_bytes": dm["algorithmic_bytes"], "launch_us": dm["us"],
+                "peak_source": pk["source"]}
     gemms = [n for n in kernels if n.endswith("gemm") and n != "router_gemm"] + \
         (["wgrad"] if "wgrad" in kernels else [])
     g_us = sum(kern_us[n] for n in gemms)
@@ -563,8 +761,6 @@ def main():
         main_stream.wait_stream(h2d_stream)
         main_stream.wait_stream(d2h_stream)
 
-    def e2e_step():
-        e2e_run(1)
     if cfg.prepermuted:
         h2d, d2h = out_bytes
     else:
@@ -572,67 +768,120 @@ def main():
         d2h = cfg.T * cfg.d * 2 + 4 + (cfg.T * cfg.d * 4 if train else 0)
 
     for _ in range(3):
-        e2e_step()
+        e2e_run(1)
     torch.cuda.synchronize()
-    def e2e_all():
-        e2e_run(K)
 
     g2 = None
     if args.graph:
         g2 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g2, capture_error_mode="relaxed"):
-            e2e_all()
+            e2e_run(K)
         torch.cuda.synchronize()
-    barrier()
+    ctx.barrier()
     s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s2.record(stream)
     if g2 is not None:
         g2.replay()
     else:
-        e2e_all()
+        e2e_run(K)
     e2.record(stream)
     torch.cuda.synchronize()
-    barrier()
+    ctx.barrier()
     ms_e2e = max_over_ranks(s2.elapsed_time(e2) / K, world, "cuda")
+    del g2
 
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline and not cfg.prepermuted and not train:
-        cpu = cpu_baseline_from_device(inp, cfg, args.cpu_sample)
+    units = cfg.T * cfg.k if cfg.prepermuted else cfg.T
+    unit = "token-slots/s" if cfg.prepermuted else "tokens/s"
+    rec = {
+        "value": job_throughput(world, units, ms_step),
+        "unit": unit,
+        "ms_per_step": ms_step,
+        "config": workload_config(cfg),
+        "grouped_gemm": {"TFLOP/s": g_fl / (g_us * 1e-6) / 1e12,
+                         "pct_bf16_peak": 100.0 * g_fl / (g_us * 1e-6) / 1e12 / tpeak,
+                         "pct_bf16_sustained": 100.0 * g_fl / (g_us * 1e-6) / 1e12 / tpeak_sus,
+                         "us": g_us, "roofline_us": g_roof_us,
+                         "frac_of_roofline": g_roof_us / g_us, "flops": g_fl,
+                         "kernels": gemms, "kept_rows": kept, "nonempty_experts": nonempty},
+        "roofline": roof,
+        "kernels": kstats,
+        "e2e": {"value": job_throughput(world, units, ms_e2e), "unit": unit,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "cuda_graph": bool(args.graph),
+        "fused_permute": bool(fused),
+        "clocks": clocks.summary(),
+    }
+    if not cfg.prepermuted:
+        rec["dropped_slots"] = int(buf.n_kept_dropped[1].item())
+    if with_cpu:
+        rec["cpu_baseline"] = cpu_baseline(inp, cfg, args)
+    return rec
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    ctx = Ctx(args, rank, world, local, barrier)
+    if args.sub_workloads == "auto":
+        subs = DEFAULT_SUBS.get(args.workload, [])
+    elif args.sub_workloads in ("", "none"):
+        subs = []
+    else:
+        subs = [w for w in args.sub_workloads.split(",") if w and w != args.workload]
+
+    with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    head = run_workload(args.workload, ctx, with_cpu=False)
+    torch.cuda.empty_cache()
+    sub_recs = {}
+    for w in subs:
+        sub_recs[w] = run_workload(w, ctx, with_cpu=False)
+        torch.cuda.empty_cache()
+    if with_cpu:
+        # the oracle baseline runs after every GPU timing, so it never overlaps one
+        from top_routing_grouped_gemm_gb300 import synth
+        cfg = synth.config(args.workload)
+        inp = synth.make_inputs(cfg, "cuda", seed=rank)
+        head["cpu_baseline"] = cpu_baseline(inp, cfg, args)
+        del inp
+        torch.cuda.empty_cache()
 
     if rank == 0:
-        units = cfg.T * cfg.k if cfg.prepermuted else cfg.T
         line = {
             "metric": METRIC,
-            "value": job_throughput(world, units, ms_step),
-            "unit": "token-slots/s" if cfg.prepermuted else "tokens/s",
+            "value": head["value"],
+            "unit": head["unit"],
             "n_gpus": world,
-            "steps": K,
+            "steps": args.steps,
             "warmup": args.warmup,
-            "ms_per_step": ms_step,
+            "ms_per_step": head["ms_per_step"],
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic",
-            "config": workload_config(cfg),
-            "grouped_gemm": {"TFLOP/s": g_fl / (g_us * 1e-6) / 1e12,
-                             "pct_bf16_peak": 100.0 * g_fl / (g_us * 1e-6) / 1e12 / tpeak,
-                             "us": g_us, "roofline_us": g_roof_us,
-                             "frac_of_roofline": g_roof_us / g_us, "flops": g_fl,
-                             "kernels": gemms, "kept_rows": kept, "nonempty_experts": nonempty},
-            "roofline": roof,
-            "kernels": kstats,
-            "e2e": {"value": job_throughput(world, units, ms_e2e),
-                    "unit": "token-slots/s" if cfg.prepermuted else "tokens/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches,
-            "cuda_graph": bool(args.graph),
-            "fused_permute": bool(fused),
-            "clocks": clocks.summary(),
-            "cpu_baseline": cpu,
         }
-        if not cfg.prepermuted:
-            line["dropped_slots"] = int(buf.n_kept_dropped[1].item())
+        line.update({k: v for k, v in head.items() if k not in line})
+        line.setdefault("cpu_baseline", None)
+        if sub_recs:
+            line["workloads"] = sub_recs
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -84,3 +84,36 @@ def oracle_tokens(inp, p, tokens, idx, gates64, slot_row):
             o = oracle.expert_forward(x[n:n + 1], Wg, Wu, Wd, L, p.lora_scale)[3]
             ys[n] += gates64[t, j] * o[0]
     return ys
+
+
+class DeviceExperts:
+    """[E, rows, cols] weight table read from a device tensor one expert at a time (as
+    float32, exact for bf16 values), so the oracle's per-expert loops can run at full size
+    without a host copy of every expert."""
+
+    def __init__(self, t):
+        self.t = t
+        self.shape = tuple(t.shape)
+
+    def __getitem__(self, e):
+        return self.t[int(e)].float().cpu().numpy()
+
+
+def oracle_experts_backward(inp, p, slots_by_expert, gates64, x64, dy64):
+    """For the slots (t, j) of each expert, the oracle's expert forward and backward:
+    o[(t, j)] (ungated expert output) and dX[(t, j)] (input gradient with dO = g dy).
+    Weights are fetched one expert at a time."""
+    o, dX = {}, {}
+    for e in sorted(slots_by_expert):
+        sl = slots_by_expert[e]
+        ts = [t for t, _ in sl]
+        Wg, Wu, Wd = f64(inp["w_gate"][e]), f64(inp["w_up"][e]), f64(inp["w_down"][e])
+        L = lora64(inp.get("lora"), e)
+        X = x64[ts]
+        oe = oracle.expert_forward(X, Wg, Wu, Wd, L, p.lora_scale)[3]
+        dO = np.array([gates64[t, j] for t, j in sl])[:, None] * dy64[ts]
+        dXe, _ = oracle.expert_backward(X, dO, Wg, Wu, Wd, L, p.lora_scale)
+        for n, (t, j) in enumerate(sl):
+            o[(t, j)] = oe[n]
+            dX[(t, j)] = dXe[n]
+    return o, dX

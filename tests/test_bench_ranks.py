@@ -53,3 +53,30 @@ def test_reference_arm_other_ranks_exit_quietly(monkeypatch, capsys):
     args = bench.argparse.Namespace(steps=1, warmup=0, workload="c2", cpu_sample=32, gpus=2)
     bench.run_reference(args)
     assert capsys.readouterr().out == ""
+
+
+def test_oracle_baseline_runs_every_shard_on_host_threads():
+    sys.path.insert(0, ROOT)
+    import bench
+    from top_routing_grouped_gemm_gb300 import synth
+    cfg = synth.config("c5", T=32, d=128, E=16, F=64)
+    inp = synth.make_inputs(cfg, "cpu")
+    args = bench.parse(["--cpu-threads", "3", "--cpu-tokens-per-thread", "2"])
+    r = bench.cpu_baseline(inp, cfg, args)
+    assert r["kind"] == "oracle" and r["cores"] == 3 and r["value"] > 0
+    assert r["single_core"]["cores"] == 1 and r["single_core"]["units"] == 2
+    assert "first 6 tokens" in r["sample"]
+
+
+def test_reference_arm_line(capsys):
+    sys.path.insert(0, ROOT)
+    import json
+    import bench
+    args = bench.parse(["--impl", "reference", "--workload", "c1", "--steps", "2", "--warmup",
+                        "1", "--cpu-threads", "2"])
+    bench.run_reference(args)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "tokens/s" and line["value"] > 0 and line["higher_is_better"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["cores"] == 2
+    assert line["config"]["workload"].startswith("c1:")

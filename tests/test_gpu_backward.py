@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from top_routing_grouped_gemm_gb300 import moe, synth
-from parity_util import RTOL_FP, f64, lora64, relerr, to_dev
+from parity_util import RTOL_FP, f64, lora64, oracle_experts_backward, relerr, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -92,8 +92,9 @@ def test_backward_gate_and_expert_paths_separately():
 
 
 def test_full_c5_sampled():
-    """c5 at full size: dgate and dx on sampled tokens (each kept slot's expert backward by
-    the oracle on that row alone), LoRA gradients of sampled experts (all their rows)."""
+    """c5 at full size: the LoRA gradients and dx_perm rows of 32 experts (all their rows),
+    and dgate and dx of 64 tokens (each token's 16 expert slots plus the gate path through
+    the renormalised softmax), against the oracle."""
     cfg = synth.config("c5")
     inp = synth.make_inputs(cfg, "cuda")
     p, buf = run_fwd_bwd(cfg, inp)
@@ -104,37 +105,44 @@ def test_full_c5_sampled():
     prob = oracle.softmax(L_gpu)
     gates = oracle.renormalised_gates(prob, idx)
     D = oracle.dispatch(idx, p.E, None)
+    assert np.array_equal(buf.slot_row.cpu().numpy(), D["slot_row"])
     offs = D["offsets"]
     rng = np.random.default_rng(5)
-    # LoRA gradients of a few experts (all their rows)
-    for e in sorted(set([0, p.E - 1] + list(rng.choice(p.E, 3, replace=False)))):
+    # LoRA gradients of 32 experts (all their rows)
+    experts = sorted(set([0, p.E - 1] + list(rng.choice(np.arange(1, p.E - 1), 30, replace=False))))
+    assert len(experts) >= 32
+    for e in experts:
         lo, hi = int(offs[e]), int(offs[e + 1])
         rows = D["row_slot"][lo:hi]
-        Xe = f64(inp["x"][torch.from_numpy(rows // k).cuda()])
-        dOe = gates.reshape(-1)[rows][:, None] * f64(inp["dy"][torch.from_numpy(rows // k).cuda()])
+        tok = torch.from_numpy(rows // k).cuda()
+        Xe = f64(inp["x"][tok])
+        dOe = gates.reshape(-1)[rows][:, None] * f64(inp["dy"][tok])
         Le = lora64(inp["lora"], e)
         dX, ge = oracle.expert_backward(Xe, dOe, f64(inp["w_gate"][e]), f64(inp["w_up"][e]),
                                         f64(inp["w_down"][e]), Le, s)
-        assert relerr(f64(buf.dx_perm[lo:hi]), dX) <= RTOL_FP
+        assert relerr(f64(buf.dx_perm[lo:hi]), dX) <= RTOL_FP, e
         for nm in GRADS:
             assert relerr(f64(buf.grads["d" + nm][e]), ge[nm]) <= RTOL_FP, (e, nm)
-    # dgate and dx of a few tokens
-    tokens = sorted(set([0, p.T - 1] + list(rng.choice(p.T, 3, replace=False))))
-    Wr = f64(inp["w_router"])
+    # dgate and dx of 64 tokens: each expert's slots evaluated together
+    tokens = sorted(set([0, p.T - 1] + list(rng.choice(np.arange(1, p.T - 1), 62, replace=False))))
+    assert len(tokens) >= 64
+    x64 = np.zeros((p.T, p.d))
+    dy64 = np.zeros((p.T, p.d))
+    tt = torch.tensor(tokens).cuda()
+    x64[tokens] = f64(inp["x"][tt])
+    dy64[tokens] = f64(inp["dy"][tt])
+    by_expert = {}
     for t in tokens:
-        x_t = f64(inp["x"][t:t + 1])
-        dy_t = f64(inp["dy"][t:t + 1])
-        dx_t = np.zeros((1, p.d))
-        dg = np.zeros((1, k))
         for j in range(k):
-            e = int(idx[t, j])
-            Le = lora64(inp["lora"], e)
-            Wg, Wu, Wd = f64(inp["w_gate"][e]), f64(inp["w_up"][e]), f64(inp["w_down"][e])
-            o = oracle.expert_forward(x_t, Wg, Wu, Wd, Le, s)[3]
-            dg[0, j] = float(dy_t[0] @ o[0])
-            dX, _ = oracle.expert_backward(x_t, gates[t, j] * dy_t, Wg, Wu, Wd, Le, s)
-            dx_t += dX
-        dl = oracle.route_backward(prob[t:t + 1], idx[t:t + 1], gates[t:t + 1], dg, np.ones((1, k)))
-        dx_t += dl @ Wr
-        assert relerr(f64(buf.dgate[t:t + 1]), dg) <= RTOL_FP
-        assert relerr(f64(buf.dx[t:t + 1]), dx_t) <= RTOL_FP
+            by_expert.setdefault(int(idx[t, j]), []).append((t, j))
+    o, dXs = oracle_experts_backward(inp, p, by_expert, gates, x64, dy64)
+    Wr = f64(inp["w_router"])
+    dg = np.array([[float(dy64[t] @ o[(t, j)]) for j in range(k)] for t in tokens])
+    dx_ref = np.array([sum(dXs[(t, j)] for j in range(k)) for t in tokens])
+    dl = oracle.route_backward(prob[tokens], idx[tokens], gates[tokens], dg,
+                               np.ones((len(tokens), k)))
+    dx_ref = dx_ref + dl @ Wr
+    assert relerr(f64(buf.dgate[tt]), dg) <= RTOL_FP
+    assert relerr(f64(buf.dx[tt]), dx_ref) <= RTOL_FP
+    for n, t in enumerate(tokens[:8]):
+        assert relerr(f64(buf.dx[t:t + 1]), dx_ref[n:n + 1]) <= RTOL_FP, t

@@ -7,8 +7,8 @@ import torch
 
 import oracle
 from top_routing_grouped_gemm_gb300 import moe, synth
-from parity_util import (RTOL_FP, RTOL_LOGITS, ExpertCache, f64, lora64, oracle_tokens, relerr,
-                         run_forward, to_dev)
+from parity_util import (RTOL_FP, RTOL_LOGITS, DeviceExperts, ExpertCache, f64, lora64,
+                         oracle_tokens, relerr, run_forward, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -213,6 +213,55 @@ def _full_workload(name, n_sample, gather=False):
 def test_full_c2_full_fanout():
     buf, D = _full_workload("c2", 12)
     assert D["n_dropped"] == 0
+
+
+def _whole_batch_oracle(name, gather):
+    """The oracle's whole forward of a full-size workload on the GPU's logits (selection on
+    identical fp32 inputs), its expert weights fetched one expert at a time."""
+    cfg = synth.config(name)
+    inp = synth.make_inputs(cfg, "cuda")
+    p = moe.problem_of(cfg)
+    buf = run_forward(p, inp, gather=gather)
+    L_gpu, idx, g, prob = check_routing(buf, p, inp, full_logits_check=False)
+    check_dispatch(buf, p, idx)
+    ref = oracle.moe_forward(f64(inp["x"]), None, DeviceExperts(inp["w_gate"]),
+                             DeviceExperts(inp["w_up"]), DeviceExperts(inp["w_down"]), p.k,
+                             p.cap_num, p.cap_den, logits=L_gpu)
+    return cfg, p, buf, ref
+
+
+def test_full_c2_whole_batch():
+    """c2 at full size against the oracle's whole forward: y on all 4096 tokens, and h and
+    y_perm on every row of 48 experts (first, last, and a seeded sample)."""
+    cfg, p, buf, ref = _whole_batch_oracle("c2", gather=True)
+    assert relerr(f64(buf.y), ref["y"]) <= RTOL_FP
+    D = ref["disp"]
+    offs = D["offsets"]
+    rng = np.random.default_rng(7)
+    experts = sorted(set([0, p.E - 1] + list(rng.choice(np.arange(1, p.E - 1), 46, replace=False))))
+    rows = np.concatenate([np.arange(offs[e], offs[e + 1]) for e in experts])
+    assert len(experts) >= 32 and len(rows) > 32 * 64
+    assert relerr(f64(buf.h[torch.from_numpy(rows).cuda()]), ref["h"][rows]) <= RTOL_FP
+    g_row = ref["gates"].reshape(-1)[D["row_slot"][rows]]
+    assert relerr(f64(buf.y_perm[torch.from_numpy(rows).cuda()]),
+                  g_row[:, None] * ref["o"][rows]) <= RTOL_FP
+    # per expert too, so that one bad expert cannot hide in the aggregate
+    for e in experts:
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        assert relerr(f64(buf.h[lo:hi]), ref["h"][lo:hi]) <= RTOL_FP, e
+
+
+def test_full_c3_whole_batch():
+    """c3 at full size (skewed routing, capacity 366, about 89 % of the slots dropped): y on
+    all 16384 tokens against the oracle's whole forward, and the all-dropped tokens exactly
+    zero."""
+    cfg, p, buf, ref = _whole_batch_oracle("c3", gather=False)
+    assert ref["C"] == 366 and ref["disp"]["n_dropped"] > 0
+    assert relerr(f64(buf.y), ref["y"]) <= RTOL_FP
+    sr = ref["disp"]["slot_row"].reshape(p.T, p.k)
+    dropped_all = np.where((sr < 0).all(axis=1))[0]
+    if len(dropped_all):
+        assert float(buf.y[torch.from_numpy(dropped_all).cuda()].float().abs().max()) == 0.0
 
 
 def test_full_c2_fused_gather():

@@ -71,6 +71,11 @@ CONFIGS = {
     # c4's 4681): same shapes per expert, four experts
     "c4_small": MoEConfig("c4_small", T=16384, d=7168, E=4, k=1, F=2048, r=16, alpha=32.0,
                           prepermuted=True),
+    # small case of the c5 kernels with c5's rows per expert (1024 x 16 / 112 = 146; 2.8 GB
+    # of expert weights, larger than L2): hardware-counter captures of the c5 GEMMs, whose
+    # DRAM traffic then scales to c5 by the number of experts (x 8)
+    "c5_shard": MoEConfig("c5_shard", T=1024, d=4096, E=112, k=16, F=1024, r=32, alpha=64.0,
+                          backward=True),
     # small case of the c5 kernels (3.2 GB of expert weights, about 256 rows per expert)
     "c5_small": MoEConfig("c5_small", T=2048, d=4096, E=128, k=16, F=1024, r=32, alpha=64.0,
                           backward=True),
