@@ -36,6 +36,7 @@ __all__ = [
     "renormalised_gates",
     "route",
     "dispatch",
+    "dispatch_remap",
     "permute",
     "silu",
     "lora_linear",
@@ -157,6 +158,64 @@ def dispatch(idx, E: int, C):
                 row_slot=row_slot, n_kept=n_kept, n_dropped=T * k - n_kept)
 
 
+def dispatch_remap(order, k: int, E: int, C, rounds: int):
+    """Dispatch that remaps overflowing slots instead of dropping them at once.
+
+    "Adapting Ultra-Large MoE Models ...", section 3.3: tokens beyond an expert's capacity
+    are handled by remapping or dropping.  The pages give no mechanism; the rule taken:
+
+    * ``order[t]`` lists token t's experts in preference order (the key (-logit, expert));
+      its first k entries are the selection, slot j's alternatives are the entries
+      j + k, j + 2k, ..., j + rounds * k (none of them selected, none shared by two slots).
+    * Pass 0 is the plain dispatch: each expert takes the slots routed to it in arrival
+      order (ascending token, then rank) while it holds fewer than C slots.
+    * In round r = 1 .. rounds every slot still unplaced proposes its r-th alternative; each
+      expert again takes the proposals in arrival order while it holds fewer than C slots.
+    * Slots still unplaced after the last round are dropped.  A remapped slot keeps its gate.
+
+    Within an expert the rows are in placement order (pass 0, then round 1, ...; arrival
+    order inside a pass).  ``counts`` stays the pre-drop count of the original selection.
+    Returns the dict of :func:`dispatch` plus ``slot_expert`` [T*k] (the expert a slot was
+    placed on, -1 when dropped) and ``slot_pass`` [T*k] (the pass that placed it, -1).
+    """
+    order = np.asarray(order)
+    T = order.shape[0]
+    if order.shape[1] < (rounds + 1) * k:
+        raise ValueError("order must list (rounds + 1) * k experts per token")
+    held = [[] for _ in range(E)]
+    slot_expert = np.full(T * k, -1, dtype=np.int64)
+    slot_pass = np.full(T * k, -1, dtype=np.int64)
+    pending = [(t, j) for t in range(T) for j in range(k)]   # arrival order
+    for r in range(rounds + 1):
+        rejected = []
+        for t, j in pending:
+            e = int(order[t, j + k * r])
+            if C is None or len(held[e]) < C:
+                held[e].append(t * k + j)
+                slot_expert[t * k + j] = e
+                slot_pass[t * k + j] = r
+            else:
+                rejected.append((t, j))
+        pending = rejected
+    counts = np.zeros(E, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            counts[int(order[t, j])] += 1
+    kept = np.array([len(q) for q in held], dtype=np.int64)
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(kept)
+    n_kept = int(offsets[E])
+    slot_row = np.full(T * k, -1, dtype=np.int64)
+    row_slot = np.zeros(n_kept, dtype=np.int64)
+    for e in range(E):
+        for q, slot in enumerate(held[e]):
+            slot_row[slot] = offsets[e] + q
+            row_slot[offsets[e] + q] = slot
+    return dict(counts=counts, kept=kept, offsets=offsets, slot_row=slot_row,
+                row_slot=row_slot, n_kept=n_kept, n_dropped=T * k - n_kept,
+                slot_expert=slot_expert, slot_pass=slot_pass)
+
+
 def permute(x, row_slot, k: int):
     """``x_perm[row] = x[row_slot[row] // k]`` (the gather that feeds the grouped GEMM)."""
     x = np.asarray(x)
@@ -248,12 +307,14 @@ def moe_forward_fixed_routing(x, logits, idx, disp, Wg, Wu, Wd, lora=None, s=0.0
 
 
 def moe_forward(x, w_router, Wg, Wu, Wd, k, cap_num=0, cap_den=0, bias=None, lora=None,
-                s=0.0, logits=None):
+                s=0.0, logits=None, remap_rounds=0):
     """The whole layer ``y = sum_{i in TopK(x)} g_i(x) E_i(x)``.
 
     When ``logits`` is given (e.g. the fp32 logits another implementation computed), the
     selection, gates and probabilities are taken from those logits instead of the fp64
     router product, so that integer decisions are made on identical inputs.
+    ``remap_rounds`` > 0 remaps overflowing slots (:func:`dispatch_remap`) instead of
+    dropping them; a slot's gate stays that of its original selection.
     """
     x = _f64(x)
     T = x.shape[0]
@@ -261,7 +322,10 @@ def moe_forward(x, w_router, Wg, Wu, Wd, k, cap_num=0, cap_den=0, bias=None, lor
     L = router_logits(x, w_router, bias) if logits is None else _f64(logits)
     idx = topk_select(L, k)
     C = capacity(T, k, E, cap_num, cap_den)
-    disp = dispatch(idx, E, C)
+    if remap_rounds:
+        disp = dispatch_remap(topk_select(L, (remap_rounds + 1) * k), k, E, C, remap_rounds)
+    else:
+        disp = dispatch(idx, E, C)
     out = moe_forward_fixed_routing(x, L, idx, disp, Wg, Wu, Wd, lora, s)
     out.update(logits=L, idx=idx, C=C, disp=disp,
                aux=aux_loss(disp["counts"], out["p"], T, k, E))

@@ -218,6 +218,127 @@ def test_zipf_bias_values():
     assert b[1] - b[0] == pytest.approx(-1.5 * 1.1 * math.log(2.0), rel=1e-5)
 
 
+# ---------------------------------------------------------------- overflow remapping
+# A slot beyond its expert's capacity moves to the token's next-preferred experts (slot j's
+# alternatives are the token's preference ranks j + k, j + 2k, ...) in rounds, each expert
+# taking proposals in arrival order into its remaining capacity; the gate stays g_j.
+
+def check_remap_hand_example_k2():
+    # orders (descending logit): t0 [0,1,2,3,4,5], t1 [0,1,4,5,2,3], t2 [1,0,2,5,4,3]
+    L = np.array([[6, 5, 4, 3, 2, 1], [6, 5, 1, 0, 4, 3], [5, 6, 4, 0, 1, 3]], float)
+    order = oracle.topk_select(L, 4)
+    assert order.tolist() == [[0, 1, 2, 3], [0, 1, 4, 5], [1, 0, 2, 5]]
+    D = oracle.dispatch_remap(order, 2, 6, 1, 1)
+    # pass 0 (C = 1): t0 takes e0 and e1; t1's and t2's slots all overflow.  Round 1: slot
+    # (t, j) proposes order[t][j + 2]: t1 -> e4, e5 (taken); t2 -> e2 (taken), e5 (full).
+    assert D["slot_expert"].tolist() == [0, 1, 4, 5, 2, -1]
+    assert D["slot_pass"].tolist() == [0, 0, 1, 1, 1, -1]
+    assert D["kept"].tolist() == [1, 1, 1, 0, 1, 1]
+    assert D["offsets"].tolist() == [0, 1, 2, 3, 3, 4, 5]
+    assert D["slot_row"].tolist() == [0, 1, 3, 4, 2, -1]
+    assert (D["n_kept"], D["n_dropped"]) == (5, 1)
+    assert D["counts"].tolist() == [3, 3, 0, 0, 0, 0]   # the original selection, pre-drop
+
+
+def check_remap_hand_example_k1():
+    L = np.array([[3, 2, 1, 0], [3, 2, 1, 0], [3, 2, 1, 0], [0, 1, 2, 3]], float)
+    order = oracle.topk_select(L, 2)
+    D0 = oracle.dispatch_remap(order, 1, 4, 1, 0)
+    assert D0["slot_expert"].tolist() == [0, -1, -1, 3]
+    D1 = oracle.dispatch_remap(order, 1, 4, 1, 1)
+    # round 1: t1 and t2 both propose e1; t1 arrives first and takes it, t2 is dropped
+    assert D1["slot_expert"].tolist() == [0, 1, -1, 3]
+    assert D1["row_slot"].tolist() == [0, 1, 3]
+
+
+def check_remap_invariants():
+    rng = _rng(21)
+    for trial in range(6):
+        T, E, k = 40, 10, 2 + trial % 2
+        R = 1 + trial % 3
+        if (R + 1) * k > E:
+            R = E // k - 1
+        L = rng.integers(0, 5, size=(T, E)).astype(float)   # ties exercise the order key
+        order = oracle.topk_select(L, (R + 1) * k)
+        C = oracle.capacity(T, k, E, 1, 2 + trial % 3)
+        D = oracle.dispatch_remap(order, k, E, C, R)
+        D_prev = oracle.dispatch_remap(order, k, E, C, R - 1)
+        se, sp = D["slot_expert"], D["slot_pass"]
+        assert (D["kept"] <= C).all()
+        assert D["n_dropped"] <= D_prev["n_dropped"]
+        # remapping only adds placements: every slot kept by the plain rule stays put
+        plain = oracle.dispatch(order[:, :k], E, C)
+        assert (se[plain["slot_row"] >= 0] == order[:, :k].reshape(-1)[plain["slot_row"] >= 0]).all()
+        for t in range(T):
+            placed = [int(se[t * k + j]) for j in range(k) if se[t * k + j] >= 0]
+            assert len(placed) == len(set(placed))   # never two slots of a token on one expert
+            for j in range(k):
+                if sp[t * k + j] >= 0:
+                    assert se[t * k + j] == order[t, j + k * sp[t * k + j]]
+        for e in range(E):
+            rows = D["row_slot"][D["offsets"][e]:D["offsets"][e + 1]]
+            assert (se[rows] == e).all()
+            keys = [(int(sp[s]), int(s)) for s in rows]
+            assert keys == sorted(keys)       # placement order: pass, then arrival
+        # a slot the last round rejected had every one of its proposals refused by a full
+        # expert
+        for slot in np.where(se < 0)[0]:
+            t, j = divmod(int(slot), k)
+            for r in range(R + 1):
+                assert D["kept"][order[t, j + k * r]] == C
+
+
+def test_remap_hand_examples():
+    check_remap_hand_example_k2()
+    check_remap_hand_example_k1()
+
+
+def test_remap_invariants():
+    check_remap_invariants()
+
+
+def test_remap_zero_rounds_is_the_dropping_rule():
+    rng = _rng(22)
+    for C in (1, 3, 7, None):
+        L = rng.standard_normal((50, 8))
+        idx = oracle.topk_select(L, 3)
+        D0 = oracle.dispatch(idx, 8, C)
+        D1 = oracle.dispatch_remap(idx, 3, 8, C, 0)
+        for key in ("counts", "kept", "offsets", "slot_row", "row_slot", "n_kept", "n_dropped"):
+            assert np.array_equal(np.asarray(D0[key]), np.asarray(D1[key])), key
+
+
+def test_remap_ample_capacity_places_everything_in_pass0():
+    rng = _rng(23)
+    L = rng.standard_normal((30, 8))
+    order = oracle.topk_select(L, 6)
+    D = oracle.dispatch_remap(order, 2, 8, 30, 2)
+    assert (D["slot_pass"] == 0).all() and D["n_dropped"] == 0
+
+
+def test_remap_hand_example_layer_output():
+    """The four-token worked example with one remap round: the slot (t2, rank 0) that the
+    dropping rule loses moves to t2's third-ranked expert e3 (which holds one of its two
+    places), keeping its gate 1/2; every other output is the dropping rule's."""
+    G = json.load(open(os.path.join(HERE, "golden", "hand_example.json")))
+    L = np.array(G["logits"], float)
+    x = np.array(G["x"], float)
+    E, d = 4, 2
+    Wg = np.array([[[1.0, 0.0]]] * E)
+    Wu = np.array([[[0.0, 1.0]]] * E)
+    Wd = np.array([[[e + 1.0], [-(e + 1.0)]] for e in range(E)])
+    out = oracle.moe_forward(x, None, Wg, Wu, Wd, 2, 1, 1, logits=L, remap_rounds=1)
+    D = out["disp"]
+    assert D["slot_expert"].tolist() == [0, 1, 0, 1, 3, 2, 2, 3]
+    assert D["n_dropped"] == 0 and D["row_slot"][D["offsets"][3]:].tolist() == [7, 4]
+    silu = lambda z: z / (1.0 + math.exp(-z))
+    y2 = 0.5 * (4 + 3) * silu(0.5) * (-1.0)     # (E_3 + E_2)(x_2) / 2, E_e = (e+1) silu(x0) x1
+    assert np.allclose(out["y"][2], [y2, -y2], rtol=1e-14)
+    ref = np.array(G["expected"]["y"])
+    assert np.allclose(out["y"][[0, 1, 3]], ref[[0, 1, 3]], rtol=1e-14)
+    assert out["aux"] == pytest.approx(G["expected"]["aux"], rel=1e-14)  # counts pre-drop
+
+
 # ---------------------------------------------------------------- aux loss
 
 def test_aux_is_one_for_uniform_probabilities():
@@ -523,3 +644,30 @@ def test_mutation_bias_on_selection_only_caught(monkeypatch):
                           Wg, Wu, Wd, lora, s)
     monkeypatch.setattr(O, "moe_forward_fixed_routing", gates_without_bias)
     _expect_failure(check_bias_makes_expert0_win_with_drops)
+
+
+def test_mutation_remap_alternative_rank_caught(monkeypatch):
+    # alternatives taken as the next ranks j + r (shared between a token's slots) instead
+    # of j + k r
+    orig = O.dispatch_remap
+
+    def wrong(order, k, E, C, rounds):
+        order = np.asarray(order).copy()
+        T = order.shape[0]
+        fixed = order.copy()
+        for r in range(1, rounds + 1):
+            for j in range(k):
+                fixed[:, j + k * r] = order[:, min(j + r, order.shape[1] - 1)]
+        return orig(fixed, k, E, C, rounds)
+    monkeypatch.setattr(O, "dispatch_remap", wrong)
+    monkeypatch.setattr(oracle, "dispatch_remap", wrong)
+    _expect_failure(check_remap_hand_example_k2)
+
+
+def test_mutation_remap_ignores_capacity_caught(monkeypatch):
+    orig = O.dispatch_remap
+    monkeypatch.setattr(O, "dispatch_remap",
+                        lambda order, k, E, C, rounds: orig(order, k, E, None if rounds else C,
+                                                            rounds))
+    monkeypatch.setattr(oracle, "dispatch_remap", O.dispatch_remap)
+    _expect_failure(check_remap_invariants)
