@@ -76,10 +76,14 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
 // One warp per token; lane i holds the logits of experts lane, lane+32, ... (VPL of them).
 // Each warp accumulates the softmax probabilities of its tokens into its own shared-memory
 // row; the block then writes one row of per-block sums (fixed order: deterministic).
+// k_sel >= k keys are selected; lanes k .. k_sel-1 (the token's next preferences after its
+// top-k) go to alt_idx [T, k_sel - k] when it is given.  Null topk_idx / topk_gate /
+// partials skip those outputs.
 template <int VPL>
 __global__ void __launch_bounds__(256, VPL > 28 ? 2 : 3) topk_softmax_kernel(
-    const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
-    float* __restrict__ topk_gate, float* __restrict__ partials) {
+    const float* __restrict__ logits, int T, int E, int k, int k_sel,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate,
+    float* __restrict__ partials, int32_t* __restrict__ alt_idx) {
   constexpr int WARPS = 8;
   __shared__ float red[WARPS][VPL * 32];
   const int warp = threadIdx.x >> 5;
@@ -125,7 +129,7 @@ __global__ void __launch_bounds__(256, VPL > 28 ? 2 : 3) topk_softmax_kernel(
     };
     refill();
     uint64_t my_key = 0ull;
-    for (int j = 0; j < k; ++j) {
+    for (int j = 0; j < k_sel; ++j) {
       const uint64_t best = warp_max_u64(hk[0]);
       if (lane == j) my_key = best;
       bool dry = false;
@@ -150,11 +154,14 @@ __global__ void __launch_bounds__(256, VPL > 28 ? 2 : 3) topk_softmax_kernel(
       if (lane + 32 * i < E) red[warp][lane + 32 * i] += v[i] * inv;
     const float pj = (lane < k) ? __expf(key_value(my_key) - m) * inv : 0.f;
     const float psum = warp_sum(pj);
-    if (lane < k) {
+    if (lane < k && topk_idx) {
       topk_idx[static_cast<size_t>(t) * k + lane] = key_expert(my_key);
       topk_gate[static_cast<size_t>(t) * k + lane] = pj / psum;
     }
+    if (alt_idx && lane >= k && lane < k_sel)
+      alt_idx[static_cast<size_t>(t) * (k_sel - k) + (lane - k)] = key_expert(my_key);
   }
+  if (partials == nullptr) return;
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float sum = 0.f;
@@ -210,20 +217,24 @@ int launch_split_router(const float* w, __nv_bfloat16* hi, __nv_bfloat16* lo, si
 }
 
 int launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* idx, float* gate,
-                        float* partials, cudaStream_t s) {
+                        float* partials, cudaStream_t s, int n_alt, int32_t* alt_idx) {
   const int grid = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
+  const int ks = k + (alt_idx ? n_alt : 0);
+#define MOE_TOPK(V) \
+  topk_softmax_kernel<V><<<grid, 256, 0, s>>>(logits, T, E, k, ks, idx, gate, partials, alt_idx)
   if (E <= 64)
-    topk_softmax_kernel<2><<<grid, 256, 0, s>>>(logits, T, E, k, idx, gate, partials);
+    MOE_TOPK(2);
   else if (E <= 128)
-    topk_softmax_kernel<4><<<grid, 256, 0, s>>>(logits, T, E, k, idx, gate, partials);
+    MOE_TOPK(4);
   else if (E <= 256)
-    topk_softmax_kernel<8><<<grid, 256, 0, s>>>(logits, T, E, k, idx, gate, partials);
+    MOE_TOPK(8);
   else if (E <= 512)
-    topk_softmax_kernel<16><<<grid, 256, 0, s>>>(logits, T, E, k, idx, gate, partials);
+    MOE_TOPK(16);
   else if (E <= 896)
-    topk_softmax_kernel<28><<<grid, 256, 0, s>>>(logits, T, E, k, idx, gate, partials);
+    MOE_TOPK(28);
   else
-    topk_softmax_kernel<32><<<grid, 256, 0, s>>>(logits, T, E, k, idx, gate, partials);
+    MOE_TOPK(32);
+#undef MOE_TOPK
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -19,8 +19,11 @@ __host__ __device__ inline int dispatch_num_chunks(int T) { return (T + kDispatc
 
 int launch_split_router(const float* w, __nv_bfloat16* hi, __nv_bfloat16* lo, size_t n,
                         cudaStream_t s);
+// n_alt > 0 with alt_idx: also the next n_alt preferences of every token (k + n_alt <= 32);
+// null idx / gate / partials skip those outputs
 int launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* idx, float* gate,
-                        float* partials, cudaStream_t s);
+                        float* partials, cudaStream_t s, int n_alt = 0,
+                        int32_t* alt_idx = nullptr);
 // block_terms: scratch of ceil(E/32) floats
 int launch_aux_loss(const int32_t* counts, const float* partials, int n_partials, int T, int k,
                     int E, float* aux_out, float* block_terms, cudaStream_t s);
@@ -42,6 +45,15 @@ int launch_expert_counts(const int32_t* idx, long long slots, int E, int32_t* co
 int launch_ep_regroup(const __nv_bfloat16* src, const float* gsrc, const int32_t* kept, int P,
                       int El, int d, int to_expert, long long rows_hint, __nv_bfloat16* dst,
                       float* gdst, int32_t* expert_offsets, cudaStream_t s);
+// Dispatch with overflow remapping: rounds passes after the plain one; ws holds
+// remap_ws_bytes(T, k, E, rounds).  slot_expert [T*k]: the expert each slot was placed on.
+size_t remap_ws_bytes(int T, int k, int E, int rounds);
+int launch_dispatch_remap(const int32_t* idx, const int32_t* alt, int rounds,
+                          const __nv_bfloat16* x, int T, int d, int E, int k, int capacity,
+                          int32_t* counts, int32_t* offsets, int32_t* slot_row,
+                          int32_t* row_slot, int32_t* slot_expert, int32_t* n_kept_dropped,
+                          __nv_bfloat16* x_perm, void* ws, int32_t* dev_status,
+                          cudaStream_t s);
 int launch_tile_schedule(const int32_t* offsets, int E, int rows_max, int32_t* tile_off,
                          int32_t* pair_off, int32_t* dev_status, cudaStream_t s);
 int launch_combine(const __nv_bfloat16* y_perm, const int32_t* slot_row, int T, int d, int k,

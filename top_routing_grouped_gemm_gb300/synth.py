@@ -45,6 +45,7 @@ class MoEConfig:
     zipf_bias: bool = False   # router bias b_e = 1.5 ln(Zipf(1.1) weight of rank e+1)
     prepermuted: bool = False  # rows given already grouped by expert (local shard)
     backward: bool = False
+    remap_rounds: int = 0      # overflowing slots remapped to later preferences (rounds)
 
     @property
     def lora_scale(self) -> float:
@@ -60,6 +61,9 @@ CONFIGS = {
     "c2": MoEConfig("c2", T=4096, d=2048, E=896, k=16, F=512),
     "c3": MoEConfig("c3", T=16384, d=4096, E=896, k=16, F=1024, cap_num=5, cap_den=4,
                     zipf_bias=True),
+    # c3 with one remap round: slots beyond capacity move to the token's next preferences
+    "c3_remap": MoEConfig("c3_remap", T=16384, d=4096, E=896, k=16, F=1024, cap_num=5,
+                          cap_den=4, zipf_bias=True, remap_rounds=1),
     "c4": MoEConfig("c4", T=65536, d=7168, E=14, k=1, F=2048, r=16, alpha=32.0,
                     prepermuted=True),
     "c5": MoEConfig("c5", T=8192, d=4096, E=896, k=16, F=1024, r=32, alpha=64.0,
