@@ -52,7 +52,7 @@ METRIC = "MoE layer tokens/s and grouped-GEMM TFLOP/s (% BF16 peak), 1×GB300"
 KERNEL_SOURCES = ["gemm.cuh", "ptx.cuh", "gemm_fwd.cu", "gemm_bwd.cu", "moe_internal.h"]
 DEFAULT_WORKLOAD = "c5"
 # sub-records carried by the headline line
-DEFAULT_SUBS = {"c5": ["c2", "c3", "c4"]}
+DEFAULT_SUBS = {"c5": ["c2", "c3", "c3_remap", "c3_chunked", "c4", "la"]}
 # tokens per host thread of the oracle baseline (forward-only workloads run more tokens:
 # their oracle step is cheaper)
 CPU_TOKENS_PER_THREAD = {"train": 2, "fwd": 16, "prepermuted_rows": 64}
@@ -66,7 +66,8 @@ def parse(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--sub-workloads", default="auto",
                     help="comma-separated workloads reported as sub-records of the line; "
-                         "'auto': c2,c3,c4 under the c5 headline; 'none': no sub-records")
+                         "'auto': c2,c3,c3_remap,c4 under the c5 headline; 'none': no "
+                         "sub-records")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-threads", type=int, default=0,
                     help="host threads of the oracle baseline and the reference arm (0: all "
@@ -80,6 +81,8 @@ def parse(argv=None):
     ap.add_argument("--permute", default="auto", choices=["auto", "fused", "separate"],
                     help="fused: gather token rows inside the expert GEMM; separate: write "
                          "x_perm in dispatch; auto: the library binding's default")
+    ap.add_argument("--combine", default="separate", choices=["separate", "fused"],
+                    help="fused: the unpermute inside the down GEMM's epilogue (same bits)")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch every step from the host instead of replaying a CUDA graph")
     return ap.parse_args(argv)
@@ -480,6 +483,8 @@ def workload_config(cfg):
                      + (f" LoRA r={cfg.r} alpha={cfg.alpha:g}" if cfg.r else "")
                      + (f" capacity {cfg.cap_num}/{cfg.cap_den}" if cfg.cap_den else " capacity inf")
                      + (" Zipf(1.1) router bias" if cfg.zipf_bias else "")
+                     + (f" {cfg.remap_rounds} remap round(s)" if cfg.remap_rounds else "")
+                     + (f" in {cfg.chunks} pipelined chunks" if cfg.chunks > 1 else "")
                      + (" forward + LoRA backward" if cfg.backward else " forward"),
          "tokens_per_gpu": cfg.T, "experts": cfg.E, "top_k": cfg.k, "d_model": cfg.d,
          "d_ffn": cfg.F, "lora_rank": cfg.r, "seed": 0,
@@ -489,7 +494,7 @@ def workload_config(cfg):
 
 # ------------------------------------------------------------------------ GPU arm
 
-def kernel_model(cfg, kept, nonempty, train, gather):
+def kernel_model(cfg, kept, nonempty, train, gather, fused_combine=False):
     """Algorithmic bytes and flops of one launch of each timed kernel (units: non-empty
     experts, kept rows, tokens), and which roofline bounds it.  With the permute fused into
     the expert GEMM (gather), its A operand is the token matrix, read once (T rows), and
@@ -508,6 +513,8 @@ def kernel_model(cfg, kept, nonempty, train, gather):
         dn_f += kept * 2.0 * d * r
     if train:
         gu_b += kept * 2 * F * 2
+    if fused_combine:  # the down GEMM also reads the kept rows back and writes y
+        dn_b += kept * d * 2 + T * d * 2 + T * k * 4
     m["gateup_gemm"] = (gu_b, gu_f)
     m["down_gemm"] = (dn_b, dn_f)
     if not cfg.prepermuted:
@@ -535,13 +542,147 @@ class Ctx:
                                                                       barrier)
 
 
+def fp32_alu_peak_tflops():
+    """fp32 FMA rate of the SIMT pipes: 152 SMs x 128 lanes x 2 flop x 2.07 GHz (the
+    maximum SM clock of these GPUs; the recipe's unit counts and clock)."""
+    return 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def la_flops_per_chunk(dk, dv, C=64):
+    """Multiply-adds of one 64-token chunk of one head in the chunked algorithm, x 2:
+    chunk factors (the K^K^T and Q^K^T triangles, the triangular inverse, Y and U) and the
+    scan (W = U - Y S^T, O = gamma Q^ S^T + P W, the state update)."""
+    tri = C * (C + 1) // 2
+    chunk = 2 * tri * dk + C ** 3 // 6 + tri * dk + tri * dv
+    scan = C * dv * dk + (C * dv * dk + tri * dv) + dv * dk * C
+    return 2.0 * (chunk + scan)
+
+
+def run_linear_attention(name, ctx):
+    """The chunked gated delta-rule linear attention forward on its workload; K steps
+    replayed as one CUDA graph, per-kernel CUDA events from a host-launched pass."""
+    import torch
+    from top_routing_grouped_gemm_gb300 import moe, synth
+    args = ctx.args
+    cfg = synth.la_config(name)
+    inp = synth.make_la_inputs(cfg, "cuda", seed=ctx.rank)
+    B, T, H, dk, dv = cfg.B, cfg.T, cfg.H, cfg.dk, cfg.dv
+    o = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device="cuda")
+    ST = torch.empty((B, H, dv, dk), dtype=torch.float32, device="cuda")
+    ws = torch.empty(moe.moe_gdr_workspace_size(B, T, H, dk, dv), dtype=torch.uint8,
+                     device="cuda")
+
+    def step():
+        moe.moe_gdr_forward(B, T, H, dk, dv, inp["q"], inp["k"], inp["v"], inp["beta"],
+                            inp["g"], inp["S0"], dk ** -0.5, o, ST, None, ws)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    kernels = ["gdr_chunk", "gdr_scan"]
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)] for n in kernels}
+    for n in kernels:
+        for a, b in ev[n]:
+            a.record()
+            b.record()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(K):
+            step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(ctx.local)
+    ctx.barrier()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    graph.replay()
+    s1.record()
+    torch.cuda.synchronize()
+    ctx.barrier()
+    clocks.stop()
+    for i in range(K):
+        for n in kernels:
+            moe.moe_set_kernel_events(n, ev[n][i][0], ev[n][i][1])
+        step()
+    for n in kernels:
+        moe.moe_set_kernel_events(n, None, None)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(s0.elapsed_time(s1) / K, ctx.world, "cuda")
+    us = {n: 1000.0 * sum(a.elapsed_time(b) for a, b in ev[n]) / K for n in kernels}
+    nch = (T + 63) // 64
+    flops = la_flops_per_chunk(dk, dv) * nch * B * H
+    peak = fp32_alu_peak_tflops()
+    tot_us = sum(us.values())
+    achieved = flops / (tot_us * 1e-6) / 1e12
+    return {"value": job_throughput(ctx.world, B * T, ms), "unit": "tokens/s",
+            "ms_per_step": ms, "cuda_graph": True, "gpu_launches": 2 * K,
+            "config": {"workload": f"{cfg.name}: gated delta-rule linear attention, B={B} "
+                                   f"T={T} H={H} dk={dk} dv={dv}, 64-token chunks, forward",
+                       "seed": 0},
+            "kernels": {n: {"us": us[n]} for n in kernels},
+            "roofline": {"kernel": "gdr_chunk + gdr_scan", "bound": "alu",
+                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "algorithmic_flops": flops,
+                         "peak_source": "fp32 FMA pipes: 152 SMs x 128 lanes x 2 x 2.07 GHz"},
+            "clocks": clocks.summary()}
+
+
+def run_chunked(cfg, ctx):
+    """The layer with its tokens in cfg.chunks chunks, each chunk's dispatch running on a
+    second stream during the previous chunk's expert GEMMs (the expert-parallel driver with
+    one rank).  Host-launched (its exchange plan reads the per-chunk counts on the host), so
+    no CUDA graph; K steps between CUDA events."""
+    import torch
+    from top_routing_grouped_gemm_gb300 import ep, moe, synth
+    args = ctx.args
+    inp = synth.make_inputs(cfg, "cuda", seed=ctx.rank)
+    p = moe.problem_of(cfg)
+    r = ep.EPRank(rank=0, x=inp["x"], w_gate=inp["w_gate"], w_up=inp["w_up"],
+                  w_down=inp["w_down"], lora=inp.get("lora"))
+    be = ep.CudaBackend()
+
+    def step():
+        return ep.ep_forward(p, [r], inp["w_router"], inp.get("bias"), ep.LocalExchange(1), be,
+                             n_chunks=cfg.chunks)[0]
+    for _ in range(max(args.warmup, 3)):
+        out = step()
+    torch.cuda.synchronize()
+    if int(out["state"].dev_status.item()) != 0:
+        raise RuntimeError(f"{cfg.name}: device status after warm-up")
+    clocks = ClockSampler(ctx.local)
+    ctx.barrier()
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = moe.moe_launch_count()
+    s0.record()
+    for _ in range(args.steps):
+        out = step()
+    s1.record()
+    torch.cuda.synchronize()
+    ctx.barrier()
+    clocks.stop()
+    ms = max_over_ranks(s0.elapsed_time(s1) / args.steps, ctx.world, "cuda")
+    kept = sum(int(pl.kept.sum()) for pl in out["plans"])
+    return {"value": job_throughput(ctx.world, cfg.T, ms), "unit": "tokens/s",
+            "ms_per_step": ms, "config": workload_config(cfg), "chunks": cfg.chunks,
+            "kept_rows": kept, "cuda_graph": False,
+            "gpu_launches": moe.moe_launch_count() - launches0, "clocks": clocks.summary(),
+            "note": "host-launched steps (the per-chunk plan reads counts on the host); "
+                    "bit-exact with the unchunked layer (tests/test_gpu_ep.py)"}
+
+
 def run_workload(name, ctx, with_cpu):
     """Time one workload on this rank's GPU; returns the fields of its JSON record."""
     import torch
     from top_routing_grouped_gemm_gb300 import moe, synth
 
     args, world, rank = ctx.args, ctx.world, ctx.rank
+    if name in synth.LA_CONFIGS:
+        return run_linear_attention(name, ctx)
     cfg = synth.config(name)
+    if cfg.chunks > 1:
+        return run_chunked(cfg, ctx)
     train = cfg.backward
     fused = {"fused": True, "separate": False}.get(
         args.permute, moe.fused_permute_default(moe.problem_of(cfg), train))
@@ -570,17 +711,21 @@ def run_workload(name, ctx, with_cpu):
         nonempty = int((offs[1:] - offs[:-1] > 0).sum())
         out_bytes = (rows * cfg.d * 2, rows * cfg.d * 2)
     else:
-        buf = moe.LayerBuffers(p, "cuda", train=train, keep_logits=train)
+        buf = moe.LayerBuffers(p, "cuda", train=train, keep_logits=train,
+                               remap_rounds=cfg.remap_rounds)
         status = buf.dev_status
+
+        fuse_combine = args.combine == "fused"
 
         def step():
             moe.layer_forward(buf, inp["x"], inp["w_router"], inp["bias"], inp["w_gate"],
                               inp["w_up"], inp["w_down"], lora,
-                              gather=fused)
+                              gather=fused, fuse_combine=fuse_combine)
             if train:
                 moe.layer_backward(buf, inp["dy"], inp["x"], inp["w_router"], inp["w_gate"],
                                    inp["w_up"], inp["w_down"], lora)
-        kernels = ["router_gemm", "topk", "dispatch", "gateup_gemm", "down_gemm", "combine"]
+        kernels = ["router_gemm", "topk", "dispatch", "gateup_gemm", "down_gemm"] + \
+            ([] if fuse_combine else ["combine"])
         if train:
             kernels += ["bwd_dh_gemm", "bwd_dx_gemm"] + (["wgrad"] if cfg.r else [])
 
@@ -653,7 +798,8 @@ def run_workload(name, ctx, with_cpu):
     hbm = pk["hbm_gbs"]
     tpeak = pk["bf16_tflops"]
     tpeak_sus = pk["bf16_tflops_sustained"] or tpeak
-    model = kernel_model(cfg, kept, nonempty, train, gather=fused)
+    model = kernel_model(cfg, kept, nonempty, train, gather=fused,
+                         fused_combine=(not cfg.prepermuted) and args.combine == "fused")
     kstats = {}
     for n in kernels:
         by, fl = model[n]
@@ -710,7 +856,8 @@ def run_workload(name, ctx, with_cpu):
                                None, ws, status)
     else:
         # the whole layer: tokens (and dy for training) in; y, aux (and dx) out
-        bufs = [buf, moe.LayerBuffers(p, "cuda", train=train, keep_logits=train)]
+        bufs = [buf, moe.LayerBuffers(p, "cuda", train=train, keep_logits=train,
+                                      remap_rounds=cfg.remap_rounds)]
         in_src = [inp["x"]] + ([inp["dy"]] if train else [])
 
         def outputs(cur):
@@ -720,7 +867,8 @@ def run_workload(name, ctx, with_cpu):
         def compute(cur, dev_in):
             b = bufs[cur]
             moe.layer_forward(b, dev_in[0], inp["w_router"], inp["bias"], inp["w_gate"],
-                              inp["w_up"], inp["w_down"], lora, gather=fused)
+                              inp["w_up"], inp["w_down"], lora, gather=fused,
+                              fuse_combine=fuse_combine)
             if train:
                 moe.layer_backward(b, dev_in[1], dev_in[0], inp["w_router"], inp["w_gate"],
                                    inp["w_up"], inp["w_down"], lora)
@@ -810,6 +958,7 @@ def run_workload(name, ctx, with_cpu):
         "gpu_launches": launches,
         "cuda_graph": bool(args.graph),
         "fused_permute": bool(fused),
+        "fused_combine": (not cfg.prepermuted) and args.combine == "fused",
         "clocks": clocks.summary(),
     }
     if not cfg.prepermuted:

@@ -1,0 +1,55 @@
+/*
+ * linear_attention.h -- C ABI of the chunked gated delta-rule linear attention in
+ * libmoe.so (the second workload of the hot path).
+ *
+ * "Fine-Tuning Trillion-Parameter Sparse MoE Models: Challenges and Engineering Practices",
+ * section 5 (large fused forward and backward kernels for linear attention: normalization
+ * coefficients, gating and decay, intra-chunk query-state interaction and the output; fixed
+ * chunks computed with dense intra-chunk products and one small state recurrence between
+ * chunks) and "Adapting Ultra-Large MoE Models: Engineering Practices and Optimization
+ * Pathways", section 3.2 (state recursion and chunked computation).  The pages give no
+ * equations; the operator implemented is the gated delta rule, per sequence b and head h:
+ *
+ *   q^_t = q_t / ||q_t||,  k^_t = k_t / ||k_t||            (L2 over the key width dk)
+ *   S_t  = exp(g_t) S_{t-1} (I - beta_t k^_t k^_t^T) + beta_t v_t k^_t^T     S_t [dv, dk]
+ *   o_t  = scale * S_t q^_t
+ *
+ * Conventions as in moe.h (status codes, caller-owned device pointers, asynchronous on
+ * `stream`, no allocation: scratch is the caller's workspace).  Layouts (row-major):
+ *   q, k [B, T, H, dk] bf16;  v [B, T, H, dv] bf16;  beta, g [B, T, H] fp32 (beta in [0, 1],
+ *   g <= 0 the log decay);  S0 [B, H, dv, dk] fp32 initial state or NULL (zero);
+ *   o [B, T, H, dv] bf16;  S_T [B, H, dv, dk] fp32 final state or NULL;
+ *   S_chunks [B, H, ceil(T/64), dv, dk] fp32 or NULL: the state at the start of every
+ *   64-token chunk (what a backward pass restarts from).
+ * Supported: dk and dv in {64, 128}; any T >= 1 (the last chunk may be partial).  A zero
+ * q or k row is treated as a zero vector (no division by zero).
+ */
+#ifndef MOE_LINEAR_ATTENTION_H
+#define MOE_LINEAR_ATTENTION_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Workspace bytes of moe_gdr_forward (the per-chunk factors: about
+ * 4 * (3 dk + dv + 65) bytes per token and head), 0 for non-positive sizes. */
+size_t moe_gdr_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv);
+
+/* Forward of the gated delta rule over all B x H sequences (two launches: the per-chunk
+ * factors of every chunk in parallel, then the scan over chunks in slices of 16 value rows
+ * of the state). */
+int moe_gdr_forward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, const moe_bf16* q,
+                    const moe_bf16* k, const moe_bf16* v, const float* beta, const float* g,
+                    const float* S0, float scale, moe_bf16* o, float* S_T, float* S_chunks,
+                    void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LINEAR_ATTENTION_H */

@@ -168,6 +168,36 @@ int moe_dispatch_noalloc(const moe_problem* p, const int32_t* topk_idx, const mo
                          int32_t* row_slot, int32_t* n_kept_dropped, moe_bf16* x_perm,
                          int32_t* dev_status, moe_stream_t stream);
 
+/* ==================================================================== overflow remapping
+ * "Adapting Ultra-Large MoE Models ...", section 3.3: tokens beyond an expert's capacity are
+ * handled by remapping or dropping.  The pages give no mechanism; the rule implemented:
+ * token t orders all experts by the selection key (descending logit, ties -> lower index);
+ * its first k are the selection, and slot j's alternatives are its preference ranks
+ * j + k, j + 2k, ..., j + rounds * k (none selected, none shared by two of its slots).  Pass
+ * 0 is moe_dispatch's rule; in round q = 1 .. rounds every slot still unplaced proposes its
+ * q-th alternative and each expert takes the proposals in arrival order (ascending token,
+ * then rank) while it holds fewer than C slots.  Slots unplaced after the last round are
+ * dropped.  A remapped slot keeps its gate topk_gate[t, j] (moe_expert_ffn reads gates by
+ * slot, so nothing else changes).  Within an expert the rows are in placement order: pass 0,
+ * then round 1, ..., arrival order inside each.  counts stays the pre-drop histogram of the
+ * original selection (what moe_aux_loss uses).
+ *
+ * moe_route_alternatives: alt_idx [T, n_alt] int32 = each token's preference ranks
+ * k .. k + n_alt - 1 from the fp32 logits moe_route wrote (pass moe_route a logits buffer);
+ * n_alt = rounds * k; k + n_alt <= min(32, E).
+ * moe_dispatch_remap: outputs as moe_dispatch (x, x_perm both NULL: index maps only), plus
+ * slot_expert [T*k] int32 (may be NULL): the expert each slot was placed on, -1 if dropped.
+ * rounds = 0 gives moe_dispatch's result.  (rounds + 1) * k <= min(32, E).  Deterministic.
+ */
+int moe_route_alternatives(const moe_problem* p, const float* logits, int32_t n_alt,
+                           int32_t* alt_idx, moe_stream_t stream);
+size_t moe_dispatch_remap_workspace_size(const moe_problem* p, int32_t rounds);
+int moe_dispatch_remap(const moe_problem* p, const int32_t* topk_idx, const int32_t* alt_idx,
+                       int32_t rounds, const moe_bf16* x, int32_t* counts, int32_t* offsets,
+                       int32_t* slot_row, int32_t* row_slot, int32_t* slot_expert,
+                       int32_t* n_kept_dropped, moe_bf16* x_perm, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream);
+
 /* ==================================================================== expert parallelism
  * The exchange of "Trillion-Parameter MoE Model Training Adaptation: Full-Stack Optimization
  * Practices", section 3 "Communication" (tokens permuted by routing result are sent with an
@@ -179,17 +209,17 @@ int moe_dispatch_noalloc(const moe_problem* p, const int32_t* topk_idx, const mo
  * moe_expert_counts: counts[e] = number of slots of topk_idx routed to expert e (before any
  * drop), overwritten.  Deterministic.  counts [E] int32.
  *
- * moe_dispatch_ep: moe_dispatch for one rank's tokens when the capacity is shared with the
- * other ranks' tokens in global arrival order (ranks in order, then tokens).  pos_base [E]
- * int32 (device, may be NULL = all zeros) holds, per expert, the number of its slots that
- * arrived on earlier ranks; a slot at local position pos is kept iff
+ * moe_dispatch_ep: moe_dispatch for one part of a larger batch (one rank's tokens, or one
+ * chunk of them) when the capacity is shared with the rest of the batch in global arrival
+ * order.  capacity: C of the whole batch, computed by the caller (ceil(cf * T_total * k / E));
+ * negative = no limit (p's cap_num / cap_den are not used).  pos_base [E] int32 (device, may
+ * be NULL = all zeros) holds, per expert, the number of its slots that arrived earlier in the
+ * batch (on earlier ranks or chunks); a slot at local position pos is kept iff
  * pos_base[e] + pos < C, so kept_e = clamp(C - pos_base[e], 0, counts[e]) and offsets is
- * their exclusive scan.  C is computed from p as in moe_dispatch (ceil(cf * T * k / E)); when
- * the capacity covers the tokens of P ranks, pass cap_num multiplied by P (the same ceiling
- * of cf * P * T * k / E).  With pos_base NULL and gate_perm NULL it equals moe_dispatch.
- * gate_perm [T*k] fp32 (may be NULL): gate_perm[row] = topk_gate[row_slot[row]], the gate
- * travelling with each permuted row to the rank that computes it.  Workspace: as
- * moe_dispatch (moe_dispatch_workspace_size).
+ * their exclusive scan.  With pos_base and gate_perm NULL and C = moe_dispatch's it equals
+ * moe_dispatch.  gate_perm [T*k] fp32 (may be NULL): gate_perm[row] =
+ * topk_gate[row_slot[row]], the gate travelling with each permuted row to the rank that
+ * computes it.  Workspace: as moe_dispatch (moe_dispatch_workspace_size).
  *
  * moe_ep_regroup: moves rows (d bf16 values each) and optionally one fp32 gate per row
  * between the two layouts of the exchange.  kept [n_sources * n_local_experts] int32
@@ -203,9 +233,9 @@ int moe_dispatch_noalloc(const moe_problem* p, const int32_t* topk_idx, const mo
  */
 int moe_expert_counts(const moe_problem* p, const int32_t* topk_idx, int32_t* counts,
                       int32_t* dev_status, moe_stream_t stream);
-int moe_dispatch_ep(const moe_problem* p, const int32_t* topk_idx, const float* topk_gate,
-                    const moe_bf16* x, const int32_t* pos_base, int32_t* counts,
-                    int32_t* offsets, int32_t* slot_row, int32_t* row_slot,
+int moe_dispatch_ep(const moe_problem* p, int32_t capacity, const int32_t* topk_idx,
+                    const float* topk_gate, const moe_bf16* x, const int32_t* pos_base,
+                    int32_t* counts, int32_t* offsets, int32_t* slot_row, int32_t* row_slot,
                     int32_t* n_kept_dropped, moe_bf16* x_perm, float* gate_perm,
                     void* workspace, size_t workspace_bytes, int32_t* dev_status,
                     moe_stream_t stream);
@@ -249,6 +279,27 @@ int moe_expert_ffn_gather(const moe_problem* p, int32_t rows_max, const moe_bf16
                           const moe_bf16* w_down, const moe_lora* lora, moe_bf16* h,
                           moe_bf16* y_perm, const moe_ffn_saved* saved, void* workspace,
                           size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream);
+
+/* moe_expert_ffn with the unpermute fused into the down GEMM ("Trillion-Parameter MoE Model
+ * Training Adaptation ...", section 4.3: deep fusion of Permute, Unpermute and Grouped GEMM):
+ * y [T, d] bf16 is written by the GEMM's epilogue, bit for bit what moe_combine computes
+ * from y_perm (which is still written: the epilogue reads the token's other rows from it).
+ * Deterministic: every stored row counts down a per-(token, 256-column strip) counter, and
+ * the warp that stores a token's last row of a strip sums that token's kept rows in rank
+ * order (j = 0 .. k-1, fp32, one rounding), exactly as moe_combine does; no atomic touches
+ * the sum.  a_is_tokens = 1: a_src is the token matrix x [T, d] gathered by slot (as
+ * moe_expert_ffn_gather), 0: the permuted rows x_perm.  slot_row [T*k] from the dispatch.
+ * Workspace: moe_expert_ffn_combine_workspace_size (the expert workspace plus one counter
+ * per token and strip). */
+size_t moe_expert_ffn_combine_workspace_size(const moe_problem* p, int32_t rows_max);
+int moe_expert_ffn_combine(const moe_problem* p, int32_t rows_max, const moe_bf16* a_src,
+                           int32_t a_is_tokens, const int32_t* offsets, const int32_t* row_slot,
+                           const int32_t* slot_row, const float* topk_gate,
+                           const moe_bf16* w_gate, const moe_bf16* w_up,
+                           const moe_bf16* w_down, const moe_lora* lora, moe_bf16* h,
+                           moe_bf16* y_perm, moe_bf16* y, const moe_ffn_saved* saved,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           moe_stream_t stream);
 
 /* ==================================================================== combine / aux
  * Unpermute and sum ("Trillion-Parameter MoE Model Training Adaptation ...", section 3
@@ -324,7 +375,9 @@ enum moe_kernel_id {
   MOE_KERNEL_BWD_DH_GEMM = 6,   /* backward dh GEMM with the SwiGLU backward      */
   MOE_KERNEL_BWD_DX_GEMM = 7,   /* backward dx_perm GEMM                         */
   MOE_KERNEL_WGRAD = 8,         /* the LoRA weight-gradient GEMMs (first to last) */
-  MOE_KERNEL_COUNT = 9
+  MOE_KERNEL_GDR_CHUNK = 9,     /* linear attention: per-chunk factors           */
+  MOE_KERNEL_GDR_SCAN = 10,     /* linear attention: state scan over chunks      */
+  MOE_KERNEL_COUNT = 11
 };
 int moe_set_kernel_events(int kernel_id, void* event_before, void* event_after);
 long long moe_launch_count(void);

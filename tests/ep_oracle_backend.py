@@ -22,13 +22,14 @@ class OracleBackend:
         st.topk_gate = torch.from_numpy(g)
         st.partials = torch.from_numpy(prob.sum(axis=0, keepdims=True))
 
-    def counts(self, p, st):
-        st.counts = torch.bincount(st.topk_idx.reshape(-1), minlength=p.E).to(torch.int64)
-        return st.counts
+    def counts(self, p, idx, st):
+        return torch.bincount(idx.reshape(-1), minlength=p.E).to(torch.int64)
 
-    def dispatch(self, p, x, pos_base, st):
-        C = oracle.capacity(p.T, p.k, p.E, p.cap_num, p.cap_den)
-        idx = st.topk_idx.numpy()
+    def dispatch(self, p, C, idx, gate, x, pos_base, st):
+        class Ch:
+            pass
+        ch = Ch()
+        idx = idx.numpy()
         base = np.asarray(pos_base, dtype=np.int64)
         T, k = idx.shape
         queues = [[] for _ in range(p.E)]
@@ -45,11 +46,12 @@ class OracleBackend:
         offsets[1:] = np.cumsum([len(q) for q in queues])
         slot_row = np.full(T * k, -1, dtype=np.int64)
         slot_row[row_slot] = np.arange(len(row_slot))
-        st.offsets = torch.from_numpy(offsets)
-        st.slot_row = torch.from_numpy(slot_row)
-        st.row_slot = torch.from_numpy(row_slot)
-        st.x_perm = x[torch.from_numpy(row_slot // k)].to(self.dtype)
-        st.gate_perm = st.topk_gate.reshape(-1)[torch.from_numpy(row_slot)]
+        ch.offsets = torch.from_numpy(offsets)
+        ch.slot_row = torch.from_numpy(slot_row)
+        ch.row_slot = torch.from_numpy(row_slot)
+        ch.x_perm = x[torch.from_numpy(row_slot // k)].to(self.dtype)
+        ch.gate_perm = gate.reshape(-1)[torch.from_numpy(row_slot)]
+        return ch
 
     def regroup(self, src, gsrc, kept, to_expert, d):
         P, El = kept.shape
@@ -85,15 +87,17 @@ class OracleBackend:
             y[lo:hi] = gates[lo:hi, None] * torch.from_numpy(o)
         return y
 
-    def combine(self, p, y_perm, st):
-        y = torch.zeros((p.T, p.d), dtype=self.dtype)
-        sr = st.slot_row.numpy()
+    def combine(self, p, y_perm, slot_row, y_out, st):
+        sr = slot_row.numpy()
+        y_out.zero_()
         for t in range(p.T):
             for j in range(p.k):
                 r = sr[t * p.k + j]
                 if r >= 0:
-                    y[t] += y_perm[r]
-        return y
+                    y_out[t] += y_perm[r]
+
+    def new_output(self, T, d):
+        return torch.zeros((T, d), dtype=self.dtype)
 
     def aux(self, p_total, counts_total, partials_all, st):
         f = counts_total.to(torch.float64) / (p_total.T * p_total.k)

@@ -49,6 +49,33 @@ def test_plan_matches_single_device_capacity():
     assert ep.capacity(P * T, k, E, 5, 4) == C
 
 
+def test_chunk_plans_follow_global_arrival_order():
+    """Chunks of ranks: the bases follow (rank, chunk, token) order, so the kept totals per
+    expert are the single-device ones on the concatenated batch."""
+    rng = np.random.default_rng(1)
+    P, n, T, E, k = 2, 3, 24, 6, 2
+    L = rng.standard_normal((P * T, E))
+    idx = oracle.topk_select(L, k)
+    C = oracle.capacity(P * T, k, E, 1, 2)
+    D = oracle.dispatch(idx, E, C)
+    bounds = ep.chunk_bounds(T, n)
+    cnt = np.zeros((P, len(bounds), E), dtype=np.int64)
+    for r in range(P):
+        for c, (t0, t1) in enumerate(bounds):
+            cnt[r, c] = np.bincount(idx[r * T + t0:r * T + t1].ravel(), minlength=E)
+    plans = ep.plan_chunks(cnt, C)
+    kept = sum(pl.kept for pl in plans)
+    assert (kept.sum(axis=0) == D["kept"]).all()
+    assert plans[1].base[0].tolist() == cnt[0, 0].tolist()
+    assert plans[0].base[1].tolist() == cnt[0].sum(axis=0).tolist()
+
+
+def test_chunk_bounds():
+    assert ep.chunk_bounds(100, 3) == [(0, 40), (40, 80), (80, 100)]
+    assert ep.chunk_bounds(5, 8) == [(0, 1), (1, 2), (2, 3), (3, 4), (4, 5)]
+    assert ep.chunk_bounds(64, 1) == [(0, 64)]
+
+
 def test_local_exchange_all_to_all():
     X = ep.LocalExchange(2)
     a = torch.arange(5).float()[:, None]
@@ -105,22 +132,23 @@ def _check_rank(cfg, P, rank, out, ref):
     y = out["y"].numpy()
     assert np.allclose(y, ref["y"][rank * T:(rank + 1) * T], rtol=1e-12, atol=1e-12)
     # the kept slots of this rank's tokens are the oracle's kept slots of those tokens
-    sr = out["state"].slot_row.numpy()
+    kept = sum(int(pl.kept[rank].sum()) for pl in out["plans"])
     ref_sr = ref["disp"]["slot_row"][rank * T * cfg.k:(rank + 1) * T * cfg.k]
-    assert ((sr >= 0) == (ref_sr >= 0)).all()
+    assert kept == int((ref_sr >= 0).sum())
     assert np.array_equal(out["state"].topk_idx.numpy(), ref["idx"][rank * T:(rank + 1) * T])
     assert abs(float(out["aux"][0]) - ref["aux"]) <= 1e-12 * abs(ref["aux"])
 
 
+@pytest.mark.parametrize("chunks", [1, 3])
 @pytest.mark.parametrize("cfg", CASES, ids=[c.name for c in CASES])
-def test_local_exchange_two_ranks_equal_whole_batch_oracle(cfg):
+def test_local_exchange_two_ranks_equal_whole_batch_oracle(cfg, chunks):
     P = 2
     inp = _inputs(cfg, P)
     ref = _oracle_whole(cfg, inp)
     xchg = ep.LocalExchange(P)
     ranks = [_ep_rank_run(r, P, cfg, inp, xchg) for r in range(P)]
     outs = ep.ep_forward(_problem(cfg, P), ranks, inp["w_router"], inp.get("bias"), xchg,
-                         OracleBackend())
+                         OracleBackend(), n_chunks=chunks)
     for r, out in enumerate(outs):
         _check_rank(cfg, P, r, out, ref)
     if cfg.cap_den:
@@ -149,7 +177,7 @@ def _gloo_rank(rank, world, port, case, res):
         xchg = ep_.DistExchange()
         r = _ep_rank_run(rank, world, cfg, inp, xchg)
         out = ep_.ep_forward(_problem(cfg, world), [r], inp["w_router"], inp.get("bias"), xchg,
-                             OB())[0]
+                             OB(), n_chunks=1 + case)[0]
         ref = _oracle_whole(cfg, inp)
         _check_rank(cfg, world, rank, out, ref)
         res[rank] = "ok"

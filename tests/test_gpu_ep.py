@@ -16,7 +16,7 @@ from parity_util import RTOL_FP, f64, lora64, relerr, run_forward, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def _ep_run(cfg, dev, P):
+def _ep_run(cfg, dev, P, chunks=1):
     T = cfg.T // P
     El = cfg.E // P
     ranks = []
@@ -28,7 +28,7 @@ def _ep_run(cfg, dev, P):
     p = moe.Problem(T=T, d=cfg.d, E=cfg.E, k=cfg.k, F=cfg.F, r=cfg.r,
                     lora_scale=cfg.lora_scale, cap_num=cfg.cap_num, cap_den=cfg.cap_den)
     outs = ep.ep_forward(p, ranks, dev["w_router"], dev.get("bias"), ep.LocalExchange(P),
-                         ep.CudaBackend())
+                         ep.CudaBackend(), n_chunks=chunks)
     torch.cuda.synchronize()
     for o in outs:
         assert int(o["state"].dev_status.item()) == 0
@@ -46,23 +46,38 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("chunks", [1, 3])
 @pytest.mark.parametrize("P, cfg", CASES, ids=[c.name for _, c in CASES])
-def test_ep_lockstep_equals_single_device(P, cfg):
+def test_ep_lockstep_equals_single_device(P, cfg, chunks):
     inp = synth.make_inputs(cfg, "cpu")
     dev = to_dev(inp)
     buf = run_forward(moe.problem_of(cfg), dev)
-    outs = _ep_run(cfg, dev, P)
+    outs = _ep_run(cfg, dev, P, chunks)
     T = cfg.T // P
     for r, o in enumerate(outs):
         st = o["state"]
         assert torch.equal(st.topk_idx, buf.topk_idx[r * T:(r + 1) * T]), r
-        kept_ep = st.slot_row >= 0
-        kept_1 = buf.slot_row[r * T * cfg.k:(r + 1) * T * cfg.k] >= 0
-        assert torch.equal(kept_ep, kept_1), r
+        kept_ep = sum(int(pl.kept[r].sum()) for pl in o["plans"])
+        kept_1 = int((buf.slot_row[r * T * cfg.k:(r + 1) * T * cfg.k] >= 0).sum().item())
+        assert kept_ep == kept_1, r
         assert torch.equal(o["y"], buf.y[r * T:(r + 1) * T]), r
         assert abs(float(o["aux"].item()) - float(buf.aux.item())) <= 1e-6 * float(buf.aux.item())
     if cfg.cap_den:
         assert int(buf.n_kept_dropped[1].item()) > 0
+
+
+@pytest.mark.parametrize("chunks", [2, 4])
+def test_single_device_chunk_pipeline_c3(chunks):
+    """P = 1 with chunks: the single-device layer with each chunk's dispatch overlapping the
+    previous chunk's expert GEMMs (c3: capacity decided across chunks in arrival order), bit
+    for bit the unchunked layer."""
+    cfg = synth.config("c3")
+    dev = synth.make_inputs(cfg, "cuda")
+    buf = run_forward(moe.problem_of(cfg), dev, gather=False)
+    outs = _ep_run(cfg, dev, 1, chunks)
+    assert torch.equal(outs[0]["y"], buf.y)
+    kept = sum(int(pl.kept.sum()) for pl in outs[0]["plans"])
+    assert kept == int(buf.n_kept_dropped[0].item())
 
 
 def test_ep_c2_four_ranks_against_oracle_sampled():

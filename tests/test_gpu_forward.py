@@ -72,9 +72,13 @@ def small_cfg(**kw):
     small_cfg(T=2600, d=192, E=4, k=2, F=192),
     small_cfg(T=2200, d=256, E=2, k=1, F=320, r=16, alpha=32.0),
     small_cfg(T=3000, d=128, E=4, k=2, F=128, cap_num=3, cap_den=4, zipf_bias=True),
+    # 129..256 rows per expert: the down GEMM on 256-row tiles
+    small_cfg(T=400, d=192, E=4, k=2, F=192),
+    small_cfg(T=500, d=320, E=5, k=2, F=256, r=16, alpha=32.0, cap_num=5, cap_den=4),
 ], ids=["c1", "small", "small_capacity_bias", "small_lora", "ragged_lora_capacity", "single_expert",
         "one_token", "capacity_zero", "max_experts_k32", "k_equals_E", "lora_r64", "lora_r8_half_capacity",
-        "mostly_empty_experts", "big_groups", "big_groups_lora", "big_groups_capacity"])
+        "mostly_empty_experts", "big_groups", "big_groups_lora", "big_groups_capacity",
+        "two_tile_groups", "two_tile_groups_lora_capacity"])
 def test_layer_forward_whole(cfg):
     inp = synth.make_inputs(cfg, "cpu")
     dev = to_dev(inp)

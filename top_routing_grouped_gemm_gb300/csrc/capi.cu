@@ -98,6 +98,15 @@ bool big_groups(const moe_problem* p, int rows_max) {
   return static_cast<long long>(rows_max) >= 1024ll * p->E && (C < 0 || C >= 1024);
 }
 
+// Groups average 129..256 rows (two m-tiles, the second partly empty): the backward dx GEMM
+// stages each weight tile once for both m-tiles on 256-row tiles instead of once per m-tile
+// (measured at c5: dx 3309 -> 2955 us; dh and down got slower, their epilogues exposed).
+bool two_tile_groups(const moe_problem* p, int rows_max) {
+  const int C = capacity_of(p);
+  const long long per = rows_max / p->E;
+  return per > kBM && per <= 2 * kBM && (C < 0 || C > kBM);
+}
+
 struct Carver {
   uint8_t* base;
   size_t used;
@@ -242,9 +251,9 @@ int moe_dispatch(const moe_problem* p, const int32_t* topk_idx, const moe_bf16* 
   return MOE_OK;
 }
 
-int moe_dispatch_ep(const moe_problem* p, const int32_t* topk_idx, const float* topk_gate,
-                    const moe_bf16* x, const int32_t* pos_base, int32_t* counts,
-                    int32_t* offsets, int32_t* slot_row, int32_t* row_slot,
+int moe_dispatch_ep(const moe_problem* p, int32_t capacity, const int32_t* topk_idx,
+                    const float* topk_gate, const moe_bf16* x, const int32_t* pos_base,
+                    int32_t* counts, int32_t* offsets, int32_t* slot_row, int32_t* row_slot,
                     int32_t* n_kept_dropped, moe_bf16* x_perm, float* gate_perm,
                     void* workspace, size_t workspace_bytes, int32_t* dev_status,
                     moe_stream_t stream) {
@@ -259,11 +268,55 @@ int moe_dispatch_ep(const moe_problem* p, const int32_t* topk_idx, const float* 
   int32_t* chunk_cnt = cv.take<int32_t>(static_cast<size_t>(dispatch_num_chunks(p->T)) * p->E);
   mark_before(MOE_KERNEL_DISPATCH, stream);
   MOE_CUDA(launch_dispatch(topk_idx, reinterpret_cast<const __nv_bfloat16*>(x), p->T, p->d,
-                           p->E, p->k, capacity_of(p), counts, offsets, slot_row, row_slot,
-                           n_kept_dropped, reinterpret_cast<__nv_bfloat16*>(x_perm), local_rank,
-                           chunk_cnt, dev_status, stream, pos_base, topk_gate, gate_perm));
+                           p->E, p->k, capacity < 0 ? -1 : capacity, counts, offsets, slot_row,
+                           row_slot, n_kept_dropped, reinterpret_cast<__nv_bfloat16*>(x_perm),
+                           local_rank, chunk_cnt, dev_status, stream, pos_base, topk_gate,
+                           gate_perm));
   mark_after(MOE_KERNEL_DISPATCH, stream);
   count_launches(4);
+  return MOE_OK;
+}
+
+int moe_route_alternatives(const moe_problem* p, const float* logits, int32_t n_alt,
+                           int32_t* alt_idx, moe_stream_t stream) {
+  MOE_TRY(check_problem(p));
+  if (!logits || !alt_idx || n_alt <= 0) return MOE_ERR_INVALID_ARG;
+  if (p->k + n_alt > 32 || p->k + n_alt > p->E) return MOE_ERR_UNSUPPORTED;
+  MOE_CUDA(launch_topk_softmax(logits, p->T, p->E, p->k, nullptr, nullptr, nullptr, stream,
+                               n_alt, alt_idx));
+  count_launches(1);
+  return MOE_OK;
+}
+
+size_t moe_dispatch_remap_workspace_size(const moe_problem* p, int32_t rounds) {
+  if (check_problem(p) != MOE_OK || rounds < 0) return 0;
+  return remap_ws_bytes(p->T, p->k, p->E, rounds);
+}
+
+int moe_dispatch_remap(const moe_problem* p, const int32_t* topk_idx, const int32_t* alt_idx,
+                       int32_t rounds, const moe_bf16* x, int32_t* counts, int32_t* offsets,
+                       int32_t* slot_row, int32_t* row_slot, int32_t* slot_expert,
+                       int32_t* n_kept_dropped, moe_bf16* x_perm, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
+  MOE_TRY(check_problem(p));
+  if (rounds < 0) return MOE_ERR_INVALID_ARG;
+  if ((rounds + 1) * p->k > 32 || (rounds + 1) * p->k > p->E) return MOE_ERR_UNSUPPORTED;
+  if (!topk_idx || (rounds > 0 && !alt_idx) || !counts || !offsets || !slot_row || !row_slot ||
+      !n_kept_dropped)
+    return MOE_ERR_INVALID_ARG;
+  if (x_perm && !x) return MOE_ERR_INVALID_ARG;
+  if ((x && !al16(x)) || (x_perm && !al16(x_perm))) return MOE_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < remap_ws_bytes(p->T, p->k, p->E, rounds))
+    return MOE_ERR_WORKSPACE;
+  mark_before(MOE_KERNEL_DISPATCH, stream);
+  MOE_CUDA(launch_dispatch_remap(topk_idx, alt_idx, rounds,
+                                 reinterpret_cast<const __nv_bfloat16*>(x), p->T, p->d, p->E,
+                                 p->k, capacity_of(p), counts, offsets, slot_row, row_slot,
+                                 slot_expert, n_kept_dropped,
+                                 reinterpret_cast<__nv_bfloat16*>(x_perm), workspace, dev_status,
+                                 stream));
+  mark_after(MOE_KERNEL_DISPATCH, stream);
+  count_launches(3 * (rounds + 1) + 2);
   return MOE_OK;
 }
 
@@ -308,15 +361,23 @@ namespace {
 // The expert step.  A rows come from `a_src`: the permuted rows themselves (gather = false,
 // a_src = x_perm [rows, d]) or token rows gathered by slot (gather = true, a_src = x [T, d],
 // row r reads x[row_slot[r] / k]).
+// y_comb / slot_row (both or neither): the combine fused into the down GEMM's epilogue,
+// y [T, d] written there (counters in the workspace after the plain carving).
 int expert_ffn_impl(const moe_problem* p, int32_t rows_max, const moe_bf16* a_src, bool gather,
                     const int32_t* offsets, const int32_t* row_slot, const float* topk_gate,
                     const moe_bf16* w_gate, const moe_bf16* w_up, const moe_bf16* w_down,
                     const moe_lora* lora, moe_bf16* h, moe_bf16* y_perm,
                     const moe_ffn_saved* saved, void* workspace, size_t workspace_bytes,
-                    int32_t* dev_status, moe_stream_t stream) {
+                    int32_t* dev_status, moe_stream_t stream, const int32_t* slot_row = nullptr,
+                    moe_bf16* y_comb = nullptr) {
   const moe_bf16* x_perm = a_src;
   MOE_TRY(check_problem(p));
   if (rows_max <= 0) return MOE_ERR_INVALID_ARG;
+  const bool fuse_combine = y_comb != nullptr;
+  if ((slot_row == nullptr) == fuse_combine) return MOE_ERR_INVALID_ARG;
+  if (fuse_combine && !al16(y_comb)) return MOE_ERR_UNSUPPORTED;
+  const size_t comb_bytes =
+      fuse_combine ? up256(static_cast<size_t>(p->T) * ((p->d + 255) / 256) * 4) : 0;
   if (!x_perm || !offsets || !row_slot || !topk_gate || !w_gate || !w_up || !w_down || !h ||
       !y_perm)
     return MOE_ERR_INVALID_ARG;
@@ -338,7 +399,7 @@ int expert_ffn_impl(const moe_problem* p, int32_t rows_max, const moe_bf16* a_sr
     for (const void* q : al3)
       if (q && !al16(q)) return MOE_ERR_UNSUPPORTED;
   }
-  if (!workspace || workspace_bytes < ffn_ws(p, rows_max)) return MOE_ERR_WORKSPACE;
+  if (!workspace || workspace_bytes < ffn_ws(p, rows_max) + comb_bytes) return MOE_ERR_WORKSPACE;
 
   const int d = p->d, E = p->E, F = p->F, r = p->r;
   Carver cv{static_cast<uint8_t*>(workspace), 0};
@@ -469,11 +530,21 @@ int expert_ffn_impl(const moe_problem* p, int32_t rows_max, const moe_bf16* a_sr
     P.ldo = d;
     P.gate = topk_gate;
     P.row_slot = row_slot;
+    if (fuse_combine) {
+      int32_t* comb_cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) +
+                                                     ffn_ws(p, rows_max));
+      MOE_CUDA(launch_combine_prepare(slot_row, p->T, p->k, P.n_tiles, d, comb_cnt,
+                                      reinterpret_cast<__nv_bfloat16*>(y_comb), stream));
+      P.comb_cnt = comb_cnt;
+      P.comb_slot_row = slot_row;
+      P.comb_y = y_comb;
+      P.comb_k = p->k;
+    }
     mark_before(MOE_KERNEL_DOWN_GEMM, stream);
     MOE_CUDA(launch_gemm_down(P, m256, stream));
     mark_after(MOE_KERNEL_DOWN_GEMM, stream);
   }
-  count_launches(use_lora ? 5 : 3);
+  count_launches((use_lora ? 5 : 3) + (fuse_combine ? 1 : 0));
   return MOE_OK;
 }
 
@@ -501,6 +572,25 @@ int moe_expert_ffn_gather(const moe_problem* p, int32_t rows_max, const moe_bf16
   return expert_ffn_impl(p, rows_max, x, true, offsets, row_slot, topk_gate, w_gate, w_up,
                          w_down, lora, h, y_perm, saved, workspace, workspace_bytes, dev_status,
                          stream);
+}
+
+size_t moe_expert_ffn_combine_workspace_size(const moe_problem* p, int32_t rows_max) {
+  if (check_problem(p) != MOE_OK || rows_max <= 0) return 0;
+  return ffn_ws(p, rows_max) + up256(static_cast<size_t>(p->T) * ((p->d + 255) / 256) * 4);
+}
+
+int moe_expert_ffn_combine(const moe_problem* p, int32_t rows_max, const moe_bf16* a_src,
+                           int32_t a_is_tokens, const int32_t* offsets, const int32_t* row_slot,
+                           const int32_t* slot_row, const float* topk_gate,
+                           const moe_bf16* w_gate, const moe_bf16* w_up,
+                           const moe_bf16* w_down, const moe_lora* lora, moe_bf16* h,
+                           moe_bf16* y_perm, moe_bf16* y, const moe_ffn_saved* saved,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           moe_stream_t stream) {
+  if (!slot_row || !y) return MOE_ERR_INVALID_ARG;
+  return expert_ffn_impl(p, rows_max, a_src, a_is_tokens != 0, offsets, row_slot, topk_gate,
+                         w_gate, w_up, w_down, lora, h, y_perm, saved, workspace,
+                         workspace_bytes, dev_status, stream, slot_row, y);
 }
 
 // ------------------------------------------------------------------------ combine / aux
@@ -602,6 +692,10 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
   }
   MOE_CUDA(launch_tile_schedule(offsets, E, rows_max, tile_off, pair_off, dev_status, stream));
   int launches = 1;
+  // 256-row tiles: dh only for big groups (its SwiGLU-backward epilogue is heavy and stays
+  // exposed with one accumulator); dx (plain store epilogue) also for two-tile groups
+  const bool m256_dh = big_groups(p, rows_max);
+  const bool m256_dx = m256_dh || two_tile_groups(p, rows_max);
   auto grouped = [&](GemmParams& P) {
     P.group_off = offsets;
     P.tile_off = tile_off;
@@ -656,7 +750,7 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
     P.out1 = da_u;
     ++launches;
     mark_before(MOE_KERNEL_BWD_DH_GEMM, stream);
-    MOE_CUDA(launch_gemm_bwd_dh(P, stream));
+    MOE_CUDA(launch_gemm_bwd_dh(P, m256_dh, stream));
     mark_after(MOE_KERNEL_BWD_DH_GEMM, stream);
   }
   // v'_g = s da_g B_g, v'_u = s da_u B_u
@@ -692,7 +786,7 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
     P.out0 = dx_perm;
     ++launches;
     mark_before(MOE_KERNEL_BWD_DX_GEMM, stream);
-    MOE_CUDA(launch_gemm_bwd_dx(P, stream));
+    MOE_CUDA(launch_gemm_bwd_dx(P, m256_dx, stream));
     mark_after(MOE_KERNEL_BWD_DX_GEMM, stream);
   }
   // LoRA weight gradients: per expert, reductions over its rows (grouped over K)

@@ -381,6 +381,181 @@ __global__ void __launch_bounds__(kRowThreads) route_bwd_kernel(
   }
 }
 
+// ---------------------------------------------------------------- overflow remapping
+//
+// "Adapting Ultra-Large MoE Models: Engineering Practices and Optimization Pathways",
+// section 3.3: tokens beyond an expert's capacity are remapped or dropped.  Pass 0 is the
+// plain dispatch; in round q = 1 .. rounds every slot (t, j) still unplaced proposes its
+// token's preference rank j + q k (alt[t][(q-1) k + j]), and each expert takes proposals in
+// arrival order into its remaining capacity.  One count / scan / decide launch triple per
+// pass keeps every decision deterministic (positions from sequential chunk counting and
+// scans, never from the order of atomics).
+
+// Pass q, step 1: per 16-token chunk, the arrival rank of every proposing slot among the
+// chunk's proposals to the same expert, and the chunk's per-expert proposal counts.
+__global__ void __launch_bounds__(256) remap_count_kernel(
+    const int32_t* __restrict__ idx, const int32_t* __restrict__ alt,
+    const int32_t* __restrict__ state, int q, int rounds, int T, int E, int k,
+    int32_t* __restrict__ local_rank, int32_t* __restrict__ chunk_cnt, int32_t* dev_status) {
+  extern __shared__ int cnt_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * kCountWarps + warp;
+  const int nch = dispatch_num_chunks(T);
+  if (c >= nch) return;
+  int* cnt = cnt_smem + warp * E;
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  __syncwarp();
+  const int t0 = c * kDispatchChunk;
+  for (int i = 0; i < kDispatchChunk; ++i) {
+    const int t = t0 + i;
+    if (t >= T) break;
+    const bool act = lane < k;
+    const size_t slot = static_cast<size_t>(t) * k + lane;
+    int e = -1;
+    if (act) {
+      if (q == 0) {
+        e = idx[slot];
+      } else if (state[slot] < 0) {
+        e = alt[static_cast<size_t>(t) * rounds * k + (q - 1) * k + lane];
+      }
+      if (e >= E || (q == 0 && e < 0)) {
+        report_status(dev_status, MOE_ERR_BAD_INDEX);
+        e = -1;
+      }
+    }
+    const unsigned live = __ballot_sync(0xffffffffu, act && e >= 0);
+    if (act && e >= 0) {
+      const unsigned grp = __match_any_sync(live, e);
+      const int before = __popc(grp & ((1u << lane) - 1u));
+      const int base = cnt[e];
+      __syncwarp(live);
+      local_rank[slot] = base + before;
+      if (lane == 31 - __clz(grp)) cnt[e] = base + __popc(grp);
+    } else if (act) {
+      local_rank[slot] = -1;
+    }
+    __syncwarp();
+  }
+  for (int e = lane; e < E; e += 32) chunk_cnt[static_cast<size_t>(c) * E + e] = cnt[e];
+}
+
+// Pass q, step 2: per expert, exclusive scan of the chunk counts (in place) and the pass
+// total; the expert's places held before this pass (held_before) and after it (held).
+// counts (pass 0 only) receives the pre-drop totals of the original selection.
+__global__ void __launch_bounds__(1024) remap_scan_kernel(
+    int32_t* __restrict__ chunk_cnt, int nch, int E, int q, int capacity,
+    int32_t* __restrict__ held, int32_t* __restrict__ held_before,
+    int32_t* __restrict__ counts) {
+  __shared__ int sm[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + tx;
+  const int per = (nch + 31) / 32;
+  const int c0 = ty * per, c1 = min(nch, c0 + per);
+  int sum = 0;
+  if (e < E)
+    for (int c = c0; c < c1; ++c) sum += chunk_cnt[static_cast<size_t>(c) * E + e];
+  sm[ty][tx] = sum;
+  __syncthreads();
+  if (ty == 0 && e < E) {
+    int run = 0;
+    for (int pp = 0; pp < 32; ++pp) {
+      const int v = sm[pp][tx];
+      sm[pp][tx] = run;
+      run += v;
+    }
+    const int h = q == 0 ? 0 : held[e];
+    held_before[e] = h;
+    held[e] = capacity < 0 ? h + run : min(capacity, h + run);
+    if (q == 0) counts[e] = run;
+  }
+  __syncthreads();
+  if (e < E) {
+    int run = sm[ty][tx];
+    for (int c = c0; c < c1; ++c) {
+      const size_t i = static_cast<size_t>(c) * E + e;
+      const int v = chunk_cnt[i];
+      chunk_cnt[i] = run;
+      run += v;
+    }
+  }
+}
+
+// Pass q, step 3: a proposing slot is placed iff its expert's places held before the pass
+// plus its arrival position stay below the capacity; it then records the expert and its
+// index among the expert's rows.  Pass 0 also initialises every slot's state.
+__global__ void remap_decide_kernel(const int32_t* __restrict__ idx,
+                                    const int32_t* __restrict__ alt,
+                                    const int32_t* __restrict__ local_rank,
+                                    const int32_t* __restrict__ chunk_base,
+                                    const int32_t* __restrict__ held_before, int q, int rounds,
+                                    int T, int E, int k, int capacity,
+                                    int32_t* __restrict__ state,
+                                    int32_t* __restrict__ slot_expert,
+                                    int32_t* __restrict__ slot_index) {
+  const long long slots = static_cast<long long>(T) * k;
+  for (long long s = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; s < slots;
+       s += static_cast<long long>(gridDim.x) * blockDim.x) {
+    if (q > 0 && state[s] >= 0) continue;
+    const int lr = local_rank[s];
+    const int t = static_cast<int>(s / k), j = static_cast<int>(s - static_cast<long long>(t) * k);
+    bool placed = false;
+    int e = -1, index = -1;
+    if (lr >= 0) {
+      e = q == 0 ? idx[s] : alt[static_cast<size_t>(t) * rounds * k + (q - 1) * k + j];
+      index = held_before[e] + chunk_base[static_cast<size_t>(t / kDispatchChunk) * E + e] + lr;
+      placed = capacity < 0 || index < capacity;
+    }
+    if (placed) {
+      state[s] = q;
+      slot_expert[s] = e;
+      slot_index[s] = index;
+    } else if (q == 0) {
+      state[s] = -1;
+      slot_expert[s] = -1;
+    }
+  }
+}
+
+// Final rows, both index maps and the gather x -> x_perm (one block per token).
+__global__ void __launch_bounds__(kRowThreads) remap_scatter_kernel(
+    const int32_t* __restrict__ slot_expert, const int32_t* __restrict__ slot_index,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ n_kept_dropped,
+    const uint4* __restrict__ x, int T, int d, int k, int32_t* __restrict__ slot_row,
+    int32_t* __restrict__ row_slot, uint4* __restrict__ x_perm) {
+  __shared__ int rows[32];
+  const int t = blockIdx.x;
+  const int slots = T * k;
+  {
+    const int n_kept = n_kept_dropped[0];
+    for (int r = n_kept + blockIdx.x * blockDim.x + threadIdx.x; r < slots;
+         r += gridDim.x * blockDim.x)
+      row_slot[r] = -1;
+  }
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int row = -1;
+    if (lane < k) {
+      const int slot = t * k + lane;
+      const int e = slot_expert[slot];
+      if (e >= 0) row = offsets[e] + slot_index[slot];
+      slot_row[slot] = row;
+      if (row >= 0) row_slot[row] = slot;
+    }
+    rows[lane] = row;
+  }
+  if (x_perm == nullptr) return;
+  __syncthreads();
+  const int nvec = d / 8;
+  const uint4* src = x + static_cast<size_t>(t) * nvec;
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    const uint4 val = src[v];
+    for (int j = 0; j < k; ++j) {
+      const int r = rows[j];
+      if (r >= 0) x_perm[static_cast<size_t>(r) * nvec + v] = val;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- expert parallelism
 //
 // "Trillion-Parameter MoE Model Training Adaptation: Full-Stack Optimization Practices",
@@ -473,6 +648,23 @@ __global__ void __launch_bounds__(256) ep_regroup_kernel(
       gdst[to + i] = gsrc[from + i];
 }
 
+// Fused combine set-up: one warp per token counts its kept slots, sets its per-n-tile
+// counters to that count, and zeroes y[t] when nothing was kept (no finisher will write it).
+__global__ void __launch_bounds__(256) combine_prepare_kernel(
+    const int32_t* __restrict__ slot_row, int T, int k, int n_tiles, int d,
+    int32_t* __restrict__ comb_cnt, uint4* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const bool kept = lane < k && slot_row[static_cast<size_t>(t) * k + lane] >= 0;
+  const int n = __popc(__ballot_sync(0xffffffffu, kept));
+  for (int i = lane; i < n_tiles; i += 32) comb_cnt[static_cast<size_t>(t) * n_tiles + i] = n;
+  if (n == 0) {
+    const int nvec = d / 8;
+    for (int v = lane; v < nvec; v += 32) y[static_cast<size_t>(t) * nvec + v] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 int grid_for_slots(long long slots) { return static_cast<int>((slots + 7) / 8); }
 
 }  // namespace
@@ -516,6 +708,57 @@ int launch_ep_regroup(const __nv_bfloat16* src, const float* gsrc, const int32_t
   ep_regroup_kernel<<<static_cast<int>(pairs * parts), 256, 0, s>>>(
       reinterpret_cast<const uint4*>(src), gsrc, kept, P, El, d / 8, to_expert, parts,
       reinterpret_cast<uint4*>(dst), gdst, expert_offsets);
+  return static_cast<int>(cudaGetLastError());
+}
+
+size_t remap_ws_bytes(int T, int k, int E, int rounds) {
+  const size_t slots = static_cast<size_t>(T) * k;
+  return up256(slots * 4) * 3 +                                        // local_rank, state, index
+         up256(static_cast<size_t>(dispatch_num_chunks(T)) * E * 4) +  // chunk counts
+         up256(static_cast<size_t>(E) * 4) * 2 +                       // held, held_before
+         up256(slots * 4);                                             // slot_expert (if not given)
+}
+
+int launch_dispatch_remap(const int32_t* idx, const int32_t* alt, int rounds,
+                          const __nv_bfloat16* x, int T, int d, int E, int k, int capacity,
+                          int32_t* counts, int32_t* offsets, int32_t* slot_row,
+                          int32_t* row_slot, int32_t* slot_expert, int32_t* n_kept_dropped,
+                          __nv_bfloat16* x_perm, void* ws, int32_t* dev_status,
+                          cudaStream_t s) {
+  const size_t slots = static_cast<size_t>(T) * k;
+  const int nch = dispatch_num_chunks(T);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* local_rank = reinterpret_cast<int32_t*>(w);  w += up256(slots * 4);
+  int32_t* state = reinterpret_cast<int32_t*>(w);       w += up256(slots * 4);
+  int32_t* slot_idx = reinterpret_cast<int32_t*>(w);    w += up256(slots * 4);
+  int32_t* chunk_cnt = reinterpret_cast<int32_t*>(w);   w += up256(static_cast<size_t>(nch) * E * 4);
+  int32_t* held = reinterpret_cast<int32_t*>(w);        w += up256(static_cast<size_t>(E) * 4);
+  int32_t* held_before = reinterpret_cast<int32_t*>(w); w += up256(static_cast<size_t>(E) * 4);
+  if (slot_expert == nullptr) slot_expert = reinterpret_cast<int32_t*>(w);
+  const int decide_blocks = static_cast<int>(std::min<size_t>((slots + 255) / 256, 8 * 152));
+  for (int q = 0; q <= rounds; ++q) {
+    remap_count_kernel<<<(nch + kCountWarps - 1) / kCountWarps, 32 * kCountWarps,
+                         kCountWarps * E * sizeof(int), s>>>(idx, alt, state, q, rounds, T, E, k,
+                                                             local_rank, chunk_cnt, dev_status);
+    remap_scan_kernel<<<(E + 31) / 32, 1024, 0, s>>>(chunk_cnt, nch, E, q, capacity, held,
+                                                    held_before, counts);
+    remap_decide_kernel<<<decide_blocks, 256, 0, s>>>(idx, alt, local_rank, chunk_cnt,
+                                                      held_before, q, rounds, T, E, k, capacity,
+                                                      state, slot_expert, slot_idx);
+  }
+  dispatch_offsets_kernel<<<1, 1024, 0, s>>>(held, nullptr, E, -1, T * k, offsets,
+                                             n_kept_dropped);
+  remap_scatter_kernel<<<T, kRowThreads, 0, s>>>(slot_expert, slot_idx, offsets, n_kept_dropped,
+                                                 reinterpret_cast<const uint4*>(x), T, d, k,
+                                                 slot_row, row_slot,
+                                                 reinterpret_cast<uint4*>(x_perm));
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_combine_prepare(const int32_t* slot_row, int T, int k, int n_tiles, int d,
+                           int32_t* comb_cnt, __nv_bfloat16* y, cudaStream_t s) {
+  combine_prepare_kernel<<<(T + 7) / 8, 256, 0, s>>>(slot_row, T, k, n_tiles, d, comb_cnt,
+                                                     reinterpret_cast<uint4*>(y));
   return static_cast<int>(cudaGetLastError());
 }
 

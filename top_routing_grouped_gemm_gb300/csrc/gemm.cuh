@@ -232,6 +232,71 @@ __device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* src, float (&v
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
+// Fused combine, after an epilogue warp stored its rows row_w .. row_w + wrows - 1 of the
+// 256-wide n-tile strip n: each stored row counts down its token's strip counter; a warp that
+// brings a counter to zero holds the token's last row of that strip and sums the token's kept
+// rows (rank order j = 0 .. k-1, fp32, one bf16 rounding: the separate combine's arithmetic)
+// into y.  Writers fence before counting and finishers after, so every row a finisher reads
+// is visible; rows are read from L2 (written by other SMs during this kernel).
+__device__ __forceinline__ void combine_finish(const GemmParams& P, int n, long row_w,
+                                               int wrows, int lane) {
+  __threadfence();
+  __syncwarp();
+  int tok = -1;
+  bool fin = false;
+  if (lane < wrows) {
+    const int slot = __ldg(&P.row_slot[row_w + lane]);
+    tok = slot / P.comb_k;
+    fin = atomicSub(&P.comb_cnt[static_cast<size_t>(tok) * P.n_tiles + n], 1) == 1;
+  }
+  unsigned fm = __ballot_sync(0xffffffffu, fin);
+  if (!fm) return;
+  __threadfence();
+  const __nv_bfloat16* yp = reinterpret_cast<const __nv_bfloat16*>(P.out0);
+  __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(P.comb_y);
+  const int col = n * 256 + lane * 8;  // one 16-byte vector of the strip per lane
+  while (fm) {
+    const int src = __ffs(fm) - 1;
+    fm &= fm - 1;
+    const int t = __shfl_sync(0xffffffffu, tok, src);
+    const int r = lane < P.comb_k ? __ldcg(&P.comb_slot_row[static_cast<size_t>(t) * P.comb_k + lane]) : -1;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // the token's rows in batches of 8: all loads of a batch in flight, then summed in rank
+    // order
+    for (int j0 = 0; j0 < P.comb_k; j0 += 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int rj = __shfl_sync(0xffffffffu, r, (j0 + u) & 31);
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (j0 + u < P.comb_k && rj >= 0 && col < P.N)
+          v[u] = __ldcg(reinterpret_cast<const uint4*>(yp + static_cast<size_t>(rj) * P.ldo + col));
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int rj = __shfl_sync(0xffffffffu, r, (j0 + u) & 31);
+        if (j0 + u < P.comb_k && rj >= 0) {
+          const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+            acc[2 * i] += f.x;
+            acc[2 * i + 1] += f.y;
+          }
+        }
+      }
+    }
+    if (col < P.N) {
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * P.N + col) = o;
+    }
+  }
+}
+
 template <int EPI, int MSUB>
 __device__ __forceinline__ bool next_tile(const GemmParams& P, int tile, TileCoord& tc,
                                           KRange& kr) {
@@ -625,6 +690,7 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
             warp_store_rows<64>(epi_buf, w, lane, y + col, P.ldo, row_w, wrows, P.N - col);
           }
         }
+        if (P.comb_cnt != nullptr) combine_finish(P, tc.n, row_w, wrows, lane);
       } else if constexpr (EPI == EPI_SCALE) {
 #pragma unroll 1
         for (int b = 0; b < NB; ++b) {

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -97,6 +98,13 @@ struct GemmParams {
   const void* gather_src;
   int gather_ld;
   int b_policy;             // L2 policy of B loads: 0 evict-first (streamed), 1 normal (reused)
+  // Fused combine (EPI_GATE_SCALE with comb_cnt set): comb_cnt[t * n_tiles + n] counts the
+  // rows of token t whose n-tile strip is not stored yet; the epilogue warp that stores the
+  // last one sums the token's kept rows (comb_slot_row, rank order, fp32) into comb_y [T, N].
+  int* comb_cnt;
+  const int* comb_slot_row;
+  void* comb_y;
+  int comb_k;
   int* dev_status;
 };
 
@@ -115,9 +123,15 @@ int launch_gemm_down(const GemmParams& P, bool m256, cudaStream_t s);
 int launch_gemm_lora_u2(const GemmParams& P, int r, cudaStream_t s); // BN=r pad, NB=2
 int launch_gemm_lora_u1(const GemmParams& P, int r, cudaStream_t s); // BN=r pad, NB=1
 
+// Fused combine: counters = kept slots per (token, n-tile), y rows of tokens with no kept slot
+// zeroed (dispatch.cu)
+int launch_combine_prepare(const int32_t* slot_row, int T, int k, int n_tiles, int d,
+                           int32_t* comb_cnt, __nv_bfloat16* y, cudaStream_t s);
+
 // Backward instantiations (gemm_bwd.cu).  B operands MN-major (weights used transposed).
-int launch_gemm_bwd_dh(const GemmParams& P, cudaStream_t s);  // BN=128, SwiGLU bwd
-int launch_gemm_bwd_dx(const GemmParams& P, cudaStream_t s);  // BN=256, store bf16
+// m256: 256-row tiles (P.pair_off units)
+int launch_gemm_bwd_dh(const GemmParams& P, bool m256, cudaStream_t s);  // BN=256, SwiGLU bwd
+int launch_gemm_bwd_dx(const GemmParams& P, bool m256, cudaStream_t s);  // BN=256, store bf16
 int launch_gemm_bwd_lora_v(const GemmParams& P, int r, cudaStream_t s);  // BN=r pad, scale
 // LoRA weight gradients, grouped over K (rows of each expert); A and B MN-major.
 int launch_gemm_wgrad(const GemmParams& P, int r, int nb, cudaStream_t s);

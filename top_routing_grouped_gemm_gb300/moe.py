@@ -66,8 +66,12 @@ _SIGS = {
     "moe_dispatch_workspace_size": (c_sz, [_P]),
     "moe_dispatch": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "moe_dispatch_noalloc": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
-    "moe_dispatch_ep": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
-                                       c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+    "moe_route_alternatives": (ctypes.c_int, [_P, c_vp, c_i32, c_vp, c_vp]),
+    "moe_dispatch_remap_workspace_size": (c_sz, [_P, c_i32]),
+    "moe_dispatch_remap": (ctypes.c_int, [_P, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                          c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+    "moe_dispatch_ep": (ctypes.c_int, [_P, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                       c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "moe_expert_counts": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp]),
     "moe_ep_regroup": (ctypes.c_int, [c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32,
                                       ctypes.c_int64, c_vp, c_vp, c_vp, c_vp]),
@@ -78,6 +82,11 @@ _SIGS = {
     "moe_expert_ffn_gather": (ctypes.c_int, [_P, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                              ctypes.POINTER(moe_lora), c_vp, c_vp,
                                              ctypes.POINTER(moe_ffn_saved), c_vp, c_sz, c_vp, c_vp]),
+    "moe_expert_ffn_combine_workspace_size": (c_sz, [_P, c_i32]),
+    "moe_expert_ffn_combine": (ctypes.c_int, [_P, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp,
+                                              c_vp, c_vp, c_vp, ctypes.POINTER(moe_lora), c_vp,
+                                              c_vp, c_vp, ctypes.POINTER(moe_ffn_saved), c_vp,
+                                              c_sz, c_vp, c_vp]),
     "moe_combine": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp]),
     "moe_aux_loss_workspace_size": (c_sz, [_P]),
     "moe_aux_loss": (ctypes.c_int, [_P, c_vp, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp]),
@@ -89,13 +98,18 @@ _SIGS = {
                                           c_vp, c_sz, c_vp, c_vp]),
     "moe_dispatch_bwd": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp]),
     "moe_route_bwd": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "moe_gdr_workspace_size": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
+    "moe_gdr_forward": (ctypes.c_int, [c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp,
+                                       c_vp, c_vp, ctypes.c_float, c_vp, c_vp, c_vp, c_vp, c_sz,
+                                       c_vp]),
     "moe_set_kernel_events": (ctypes.c_int, [ctypes.c_int, c_vp, c_vp]),
     "moe_launch_count": (ctypes.c_longlong, []),
     "moe_selftest_wait_timeout": (ctypes.c_int, [c_vp, c_i32, c_vp]),
 }
 
 KERNEL_IDS = {"router_gemm": 0, "topk": 1, "dispatch": 2, "gateup_gemm": 3, "down_gemm": 4,
-              "combine": 5, "bwd_dh_gemm": 6, "bwd_dx_gemm": 7, "wgrad": 8}
+              "combine": 5, "bwd_dh_gemm": 6, "bwd_dx_gemm": 7, "wgrad": 8, "gdr_chunk": 9,
+              "gdr_scan": 10}
 
 _lib = None
 
@@ -235,11 +249,35 @@ def moe_dispatch_noalloc(p, topk_idx, x, counts, offsets, slot_row, row_slot, n_
                                       _ptr(x_perm), _ptr(dev_status), _stream(stream)))
 
 
-def moe_dispatch_ep(p, topk_idx, topk_gate, x, pos_base, counts, offsets, slot_row, row_slot,
-                    n_kept_dropped, x_perm, gate_perm, workspace, dev_status=None, stream=None):
+def moe_route_alternatives(p, logits, n_alt, alt_idx, stream=None):
+    _check("moe_route_alternatives",
+           lib().moe_route_alternatives(p.c(), _ptr(logits), n_alt, _ptr(alt_idx),
+                                        _stream(stream)))
+
+
+def moe_dispatch_remap_workspace_size(p: Problem, rounds: int) -> int:
+    return lib().moe_dispatch_remap_workspace_size(p.c(), rounds)
+
+
+def moe_dispatch_remap(p, topk_idx, alt_idx, rounds, x, counts, offsets, slot_row, row_slot,
+                       slot_expert, n_kept_dropped, x_perm, workspace, dev_status=None,
+                       stream=None):
     wp, wn = _ws(workspace)
+    _check("moe_dispatch_remap",
+           lib().moe_dispatch_remap(p.c(), _ptr(topk_idx), _ptr(alt_idx), rounds, _ptr(x),
+                                    _ptr(counts), _ptr(offsets), _ptr(slot_row), _ptr(row_slot),
+                                    _ptr(slot_expert), _ptr(n_kept_dropped), _ptr(x_perm), wp, wn,
+                                    _ptr(dev_status), _stream(stream)))
+
+
+def moe_dispatch_ep(p, capacity, topk_idx, topk_gate, x, pos_base, counts, offsets, slot_row,
+                    row_slot, n_kept_dropped, x_perm, gate_perm, workspace, dev_status=None,
+                    stream=None):
+    """capacity: C of the whole batch (None or negative: no limit)."""
+    wp, wn = _ws(workspace)
+    C = -1 if capacity is None or capacity < 0 else int(capacity)
     _check("moe_dispatch_ep",
-           lib().moe_dispatch_ep(p.c(), _ptr(topk_idx), _ptr(topk_gate), _ptr(x), _ptr(pos_base),
+           lib().moe_dispatch_ep(p.c(), C, _ptr(topk_idx), _ptr(topk_gate), _ptr(x), _ptr(pos_base),
                                  _ptr(counts), _ptr(offsets), _ptr(slot_row), _ptr(row_slot),
                                  _ptr(n_kept_dropped), _ptr(x_perm), _ptr(gate_perm), wp, wn,
                                  _ptr(dev_status), _stream(stream)))
@@ -281,6 +319,23 @@ def moe_expert_ffn_gather(p, rows_max, x, offsets, row_slot, topk_gate, w_gate, 
                                        _ptr(topk_gate), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
                                        _lora(lora), _ptr(h), _ptr(y_perm), _saved(saved), wp, wn,
                                        _ptr(dev_status), _stream(stream)))
+
+
+def moe_expert_ffn_combine_workspace_size(p: Problem, rows_max: int) -> int:
+    return lib().moe_expert_ffn_combine_workspace_size(p.c(), rows_max)
+
+
+def moe_expert_ffn_combine(p, rows_max, a_src, a_is_tokens, offsets, row_slot, slot_row,
+                           topk_gate, w_gate, w_up, w_down, lora, h, y_perm, y, saved,
+                           workspace, dev_status=None, stream=None):
+    wp, wn = _ws(workspace)
+    _check("moe_expert_ffn_combine",
+           lib().moe_expert_ffn_combine(p.c(), rows_max, _ptr(a_src), 1 if a_is_tokens else 0,
+                                        _ptr(offsets), _ptr(row_slot), _ptr(slot_row),
+                                        _ptr(topk_gate), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                                        _lora(lora), _ptr(h), _ptr(y_perm), _ptr(y),
+                                        _saved(saved), wp, wn, _ptr(dev_status),
+                                        _stream(stream)))
 
 
 def moe_combine(p, y_perm, slot_row, y, stream=None):
@@ -329,6 +384,21 @@ def moe_route_bwd(p, topk_idx, topk_gate, dgate, w_router, dx, stream=None):
                                                 _stream(stream)))
 
 
+# ---- gated delta-rule linear attention (include/linear_attention.h)
+
+def moe_gdr_workspace_size(B, T, H, dk, dv) -> int:
+    return lib().moe_gdr_workspace_size(B, T, H, dk, dv)
+
+
+def moe_gdr_forward(B, T, H, dk, dv, q, k, v, beta, g, S0, scale, o, S_T, S_chunks, workspace,
+                    stream=None):
+    wp, wn = _ws(workspace)
+    _check("moe_gdr_forward",
+           lib().moe_gdr_forward(B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                                 _ptr(S0), scale, _ptr(o), _ptr(S_T), _ptr(S_chunks), wp, wn,
+                                 _stream(stream)))
+
+
 def moe_set_kernel_events(kernel, before, after):
     """Record torch.cuda.Event ``before``/``after`` around the next launches of ``kernel``
     (a name of KERNEL_IDS); ``None`` stops recording."""
@@ -368,13 +438,20 @@ class LayerBuffers:
     """Every device buffer one forward (and, with ``train=True``, one backward) of the layer
     uses, allocated once with torch and reused across calls."""
 
-    def __init__(self, p: Problem, device="cuda", train=False, keep_logits=True):
+    def __init__(self, p: Problem, device="cuda", train=False, keep_logits=True,
+                 remap_rounds=0):
         dev = torch.device(device)
         T, d, E, k, F, r = p.T, p.d, p.E, p.k, p.F, p.r
         N = T * k
         self.p = p
         self.rows_max = N
+        self.remap_rounds = remap_rounds
+        keep_logits = keep_logits or remap_rounds > 0   # the alternatives are read from them
         self.logits = _empty((T, E), torch.float32, dev) if keep_logits else None
+        if remap_rounds:
+            self.alt_idx = _empty((T, remap_rounds * k), torch.int32, dev)
+            self.slot_expert = _empty((N,), torch.int32, dev)
+            self.ws_remap = _bytes(moe_dispatch_remap_workspace_size(p, remap_rounds), dev)
         self.topk_idx = _empty((T, k), torch.int32, dev)
         self.topk_gate = _empty((T, k), torch.float32, dev)
         self.n_partials = moe_route_num_partials(p)
@@ -392,7 +469,7 @@ class LayerBuffers:
         self.dev_status = torch.zeros((1,), dtype=torch.int32, device=dev)
         self.ws_route = _bytes(moe_route_workspace_size(p), dev)
         self.ws_dispatch = _bytes(moe_dispatch_workspace_size(p), dev)
-        self.ws_ffn = _bytes(moe_expert_ffn_workspace_size(p, N), dev)
+        self.ws_ffn = _bytes(moe_expert_ffn_combine_workspace_size(p, N), dev)
         self.ws_aux = _bytes(moe_aux_loss_workspace_size(p), dev)
         self.saved = None
         self.train = train
@@ -427,7 +504,7 @@ def fused_permute_default(p: Problem, train: bool) -> bool:
 
 
 def layer_forward(buf: LayerBuffers, x, w_router, bias, w_gate, w_up, w_down, lora=None,
-                  stream=None, gather=None):
+                  stream=None, gather=None, fuse_combine=False):
     """route -> dispatch -> experts -> combine -> aux, all enqueued on one stream.
 
     gather=True fuses the permute into the expert GEMMs (moe_expert_ffn_gather: dispatch
@@ -439,14 +516,30 @@ def layer_forward(buf: LayerBuffers, x, w_router, bias, w_gate, w_up, w_down, lo
         gather = fused_permute_default(p, buf.train)
     moe_route(p, x, w_router, bias, buf.topk_idx, buf.topk_gate, buf.partials, buf.logits,
               buf.ws_route, buf.dev_status, stream)
-    moe_dispatch(p, buf.topk_idx, None if gather else x, buf.counts, buf.offsets, buf.slot_row,
-                 buf.row_slot, buf.n_kept_dropped, None if gather else buf.x_perm,
-                 buf.ws_dispatch, buf.dev_status, stream)
-    ffn = moe_expert_ffn_gather if gather else moe_expert_ffn
-    ffn(p, buf.rows_max, x if gather else buf.x_perm, buf.offsets, buf.row_slot, buf.topk_gate,
-        w_gate, w_up, w_down, lora, buf.h, buf.y_perm, buf.saved, buf.ws_ffn, buf.dev_status,
-        stream)
-    moe_combine(p, buf.y_perm, buf.slot_row, buf.y, stream)
+    if buf.remap_rounds:
+        # overflowing slots move to the token's next preferences instead of being dropped
+        R = buf.remap_rounds
+        moe_route_alternatives(p, buf.logits, R * p.k, buf.alt_idx, stream)
+        moe_dispatch_remap(p, buf.topk_idx, buf.alt_idx, R, None if gather else x, buf.counts,
+                           buf.offsets, buf.slot_row, buf.row_slot, buf.slot_expert,
+                           buf.n_kept_dropped, None if gather else buf.x_perm, buf.ws_remap,
+                           buf.dev_status, stream)
+    else:
+        moe_dispatch(p, buf.topk_idx, None if gather else x, buf.counts, buf.offsets,
+                     buf.slot_row, buf.row_slot, buf.n_kept_dropped,
+                     None if gather else buf.x_perm, buf.ws_dispatch, buf.dev_status, stream)
+    if fuse_combine:
+        # unpermute inside the down GEMM's epilogue (same bits as the separate combine)
+        moe_expert_ffn_combine(p, buf.rows_max, x if gather else buf.x_perm, gather,
+                               buf.offsets, buf.row_slot, buf.slot_row, buf.topk_gate, w_gate,
+                               w_up, w_down, lora, buf.h, buf.y_perm, buf.y, buf.saved,
+                               buf.ws_ffn, buf.dev_status, stream)
+    else:
+        ffn = moe_expert_ffn_gather if gather else moe_expert_ffn
+        ffn(p, buf.rows_max, x if gather else buf.x_perm, buf.offsets, buf.row_slot,
+            buf.topk_gate, w_gate, w_up, w_down, lora, buf.h, buf.y_perm, buf.saved, buf.ws_ffn,
+            buf.dev_status, stream)
+        moe_combine(p, buf.y_perm, buf.slot_row, buf.y, stream)
     moe_aux_loss(p, buf.counts, buf.partials, buf.n_partials, buf.aux, buf.ws_aux, stream)
     return buf.y
 

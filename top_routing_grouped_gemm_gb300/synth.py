@@ -46,6 +46,7 @@ class MoEConfig:
     prepermuted: bool = False  # rows given already grouped by expert (local shard)
     backward: bool = False
     remap_rounds: int = 0      # overflowing slots remapped to later preferences (rounds)
+    chunks: int = 1            # token chunks pipelined (dispatch of chunk i+1 during chunk i)
 
     @property
     def lora_scale(self) -> float:
@@ -64,6 +65,9 @@ CONFIGS = {
     # c3 with one remap round: slots beyond capacity move to the token's next preferences
     "c3_remap": MoEConfig("c3_remap", T=16384, d=4096, E=896, k=16, F=1024, cap_num=5,
                           cap_den=4, zipf_bias=True, remap_rounds=1),
+    # c3 in 4 token chunks, each chunk's dispatch overlapping the previous chunk's experts
+    "c3_chunked": MoEConfig("c3_chunked", T=16384, d=4096, E=896, k=16, F=1024, cap_num=5,
+                            cap_den=4, zipf_bias=True, chunks=4),
     "c4": MoEConfig("c4", T=65536, d=7168, E=14, k=1, F=2048, r=16, alpha=32.0,
                     prepermuted=True),
     "c5": MoEConfig("c5", T=8192, d=4096, E=896, k=16, F=1024, r=32, alpha=64.0,
@@ -157,4 +161,49 @@ def make_inputs(cfg: MoEConfig, device="cpu", seed: int = 0, weights: bool = Tru
             }
     if cfg.backward:
         out["dy"] = _normal(gen, (cfg.T, cfg.d), 1.0, dev, torch.bfloat16)
+    return out
+
+
+# ----------------------------------------------------------------------------- linear attention
+
+@dataclass(frozen=True)
+class LAConfig:
+    """Gated delta-rule linear attention: B sequences of T tokens, H heads, key width dk,
+    value width dv."""
+    name: str
+    B: int
+    T: int
+    H: int
+    dk: int = 128
+    dv: int = 128
+    with_state: bool = False   # start from a random state S0 instead of zero
+
+
+LA_CONFIGS = {
+    # one long sequence (the pages fine-tune with micro-batch 1 and long context), 16 heads
+    "la": LAConfig("la", B=1, T=32768, H=16),
+    "la_small": LAConfig("la_small", B=2, T=1000, H=4, with_state=True),
+}
+
+
+def la_config(name: str, **overrides) -> LAConfig:
+    cfg = LA_CONFIGS[name]
+    return replace(cfg, **overrides) if overrides else cfg
+
+
+def make_la_inputs(cfg: LAConfig, device="cpu", seed: int = 0):
+    """q, k, v ~ N(0, 1) bf16; beta = sigmoid(N(0, 1)); decay alpha = sigmoid(a), a ~ N(4, 1)
+    (close to 1, as forget gates are), g = log(alpha) = -softplus(-a); S0 ~ N(0, 0.1)."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    sh = (cfg.B, cfg.T, cfg.H)
+    out = {"q": _normal(gen, sh + (cfg.dk,), 1.0, dev, torch.bfloat16),
+           "k": _normal(gen, sh + (cfg.dk,), 1.0, dev, torch.bfloat16),
+           "v": _normal(gen, sh + (cfg.dv,), 1.0, dev, torch.bfloat16)}
+    out["beta"] = torch.sigmoid(torch.randn(sh, generator=gen, device=dev))
+    a = torch.randn(sh, generator=gen, device=dev) + 4.0
+    out["g"] = -torch.nn.functional.softplus(-a)
+    out["S0"] = (torch.randn((cfg.B, cfg.H, cfg.dv, cfg.dk), generator=gen, device=dev) * 0.1
+                 if cfg.with_state else None)
     return out
