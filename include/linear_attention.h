@@ -48,6 +48,21 @@ int moe_gdr_forward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, con
                     const float* S0, float scale, moe_bf16* o, float* S_T, float* S_chunks,
                     void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* Backward: gradients of <d_o, o> + <dS_T, S_T> with respect to q, k, v, beta, g and S0
+ * (three launches: the per-chunk factors rebuilt, a backward scan over chunks for the state
+ * gradient in slices of 16 value rows, then every chunk's local backward in parallel).
+ * S_chunks: the forward's chunk-start states (required).  d_o [B, T, H, dv] bf16; dS_T
+ * [B, H, dv, dk] fp32 or NULL (zero).  Outputs fp32, overwritten: dq, d_k [B, T, H, dk],
+ * d_v [B, T, H, dv], dbeta, dg [B, T, H], dS0 [B, H, dv, dk] (may be NULL).  Deterministic:
+ * every reduction runs in a fixed order. */
+size_t moe_gdr_backward_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk,
+                                       int32_t dv);
+int moe_gdr_backward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, const moe_bf16* q,
+                     const moe_bf16* k, const moe_bf16* v, const float* beta, const float* g,
+                     float scale, const moe_bf16* d_o, const float* dS_T, const float* S_chunks,
+                     float* dq, float* d_k, float* d_v, float* dbeta, float* dg, float* dS0,
+                     void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

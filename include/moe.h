@@ -377,7 +377,8 @@ enum moe_kernel_id {
   MOE_KERNEL_WGRAD = 8,         /* the LoRA weight-gradient GEMMs (first to last) */
   MOE_KERNEL_GDR_CHUNK = 9,     /* linear attention: per-chunk factors           */
   MOE_KERNEL_GDR_SCAN = 10,     /* linear attention: state scan over chunks      */
-  MOE_KERNEL_COUNT = 11
+  MOE_KERNEL_GDR_BWD = 11,      /* linear attention: per-chunk backward          */
+  MOE_KERNEL_COUNT = 12
 };
 int moe_set_kernel_events(int kernel_id, void* event_before, void* event_after);
 long long moe_launch_count(void);

@@ -93,3 +93,60 @@ def test_gdr_long_sequence_sampled_heads():
         o_ref, S_ref = ref_of(sub)
         assert relerr(f64(o[:, :, h:h + 1]), o_ref) <= RTOL_O, h
         assert relerr(f64(ST[:, h:h + 1]), S_ref) <= 10 * RTOL_S, h
+
+
+# ---------------------------------------------------------------- backward
+
+RTOL_G = 5e-3
+
+
+def run_gdr_bwd(cfg, inp, d_o, dST):
+    B, T, H, dk, dv = cfg.B, cfg.T, cfg.H, cfg.dk, cfg.dv
+    _, _, Sc = run_gdr(cfg, inp, checkpoints=True)
+    dev = {n: (None if t is None else t.cuda()) for n, t in inp.items()}
+    out = {"dq": torch.empty((B, T, H, dk), device="cuda"),
+           "dk": torch.empty((B, T, H, dk), device="cuda"),
+           "dv": torch.empty((B, T, H, dv), device="cuda"),
+           "dbeta": torch.empty((B, T, H), device="cuda"),
+           "dg": torch.empty((B, T, H), device="cuda"),
+           "dS0": torch.empty((B, H, dv, dk), device="cuda")}
+    ws = torch.empty(moe.moe_gdr_backward_workspace_size(B, T, H, dk, dv), dtype=torch.uint8,
+                     device="cuda")
+    moe.moe_gdr_backward(B, T, H, dk, dv, dev["q"], dev["k"], dev["v"], dev["beta"], dev["g"],
+                         dk ** -0.5, d_o.cuda(), None if dST is None else dST.cuda(), Sc,
+                         out["dq"], out["dk"], out["dv"], out["dbeta"], out["dg"], out["dS0"], ws)
+    torch.cuda.synchronize()
+    return out
+
+
+BWD_CASES = [
+    synth.LAConfig("la_bwd_small", B=1, T=200, H=2, dk=128, dv=128, with_state=True),
+    synth.LAConfig("la_bwd_64x128", B=2, T=130, H=1, dk=64, dv=128),
+    synth.LAConfig("la_bwd_128x64_one_chunk", B=1, T=64, H=3, dk=128, dv=64, with_state=True),
+    synth.LAConfig("la_bwd_ragged", B=1, T=333, H=2, dk=64, dv=64),
+]
+
+
+@pytest.mark.parametrize("with_dST", [False, True])
+@pytest.mark.parametrize("cfg", BWD_CASES, ids=[c.name for c in BWD_CASES])
+def test_gdr_backward_whole(cfg, with_dST):
+    inp = synth.make_la_inputs(cfg)
+    gen = torch.Generator().manual_seed(11)
+    d_o = torch.randn((cfg.B, cfg.T, cfg.H, cfg.dv), generator=gen).to(torch.bfloat16)
+    dST = torch.randn((cfg.B, cfg.H, cfg.dv, cfg.dk), generator=gen) if with_dST else None
+    got = run_gdr_bwd(cfg, inp, d_o, dST)
+    ref = LA.gated_delta_rule_backward(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]),
+                                       f64(inp["beta"]), f64(inp["g"]), f64(d_o),
+                                       dS_T=f64(dST), S0=f64(inp["S0"]))
+    for name in ("dq", "dk", "dv", "dbeta", "dg", "dS0"):
+        assert relerr(f64(got[name]), ref[name]) <= RTOL_G, name
+
+
+def test_gdr_backward_is_deterministic():
+    cfg = BWD_CASES[0]
+    inp = synth.make_la_inputs(cfg)
+    d_o = torch.randn((cfg.B, cfg.T, cfg.H, cfg.dv)).to(torch.bfloat16)
+    a = run_gdr_bwd(cfg, inp, d_o, None)
+    b = run_gdr_bwd(cfg, inp, d_o, None)
+    for name in a:
+        assert torch.equal(a[name], b[name]), name

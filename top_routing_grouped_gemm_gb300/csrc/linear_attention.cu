@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ beta,
     const float* __restrict__ g, int T, int H, int nch, float* __restrict__ Qh,
     float* __restrict__ Kh, float* __restrict__ Y, float* __restrict__ U,
-    float* __restrict__ Pm, float* __restrict__ Gc) {
+    float* __restrict__ Pm, float* __restrict__ Gc, float* __restrict__ Ai) {
   constexpr int LK = Ld<DK>::v, LC = Ld<kC>::v;
   extern __shared__ float sm[];
   float* sK = sm;                    // [C][LK]
@@ -136,16 +136,20 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
     Pm[chunk_id * kC * kC + e] = p;
   }
   __syncthreads();
-  // A^-1 by forward substitution, one column per thread (unit lower triangular)
-  if (tid < kC) {
-    const int col = tid;
+  // A^-1 (unit lower triangular), one row per step: X_i = e_i - sum_{j<i} A_ij X_j, the 64
+  // columns in parallel with 4 threads per column (each a quarter of the j range, combined by
+  // shuffles within the 4 lanes)
+  {
+    const int col = tid >> 2, part = tid & 3;
     for (int i = 0; i < kC; ++i) {
-      float x = (i == col) ? 1.f : 0.f;
-      for (int j = col; j < i; ++j) x -= sA[i * LC + j] * sI[j * LC + col];
-      sI[i * LC + col] = i < col ? 0.f : x;
+      float x = 0.f;
+      for (int j = col + part; j < i; j += 4) x -= sA[i * LC + j] * sI[j * LC + col];
+      x += __shfl_xor_sync(0xffffffffu, x, 1);
+      x += __shfl_xor_sync(0xffffffffu, x, 2);
+      if (part == 0) sI[i * LC + col] = i < col ? 0.f : (i == col ? 1.f : x);
+      __syncthreads();
     }
   }
-  __syncthreads();
   // Y = A^-1 diag(beta gamma) K^, U = A^-1 diag(beta) V; q^, k^ out for the scan
   for (int e = tid; e < kC * DK; e += 256) {
     const int i = e / DK, x = e - i * DK;
@@ -173,6 +177,8 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
     U[chunk_id * kC * DV + e] = u;
   }
   if (tid < kC) Gc[chunk_id * kC + tid] = sG[tid];
+  if (Ai)
+    for (int e = tid; e < kC * kC; e += 256) Ai[chunk_id * kC * kC + e] = sI[(e / kC) * LC + (e % kC)];
 }
 
 // Scan over the chunks of one (b, h) for RS value rows of the state (grid: DV/RS x H x B,
@@ -194,7 +200,11 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
   float* sY = sK + kC * LK;         // [C][LK]
   float* sP = sY + kC * LK;         // [C][LC]
   float* sW = sP + kC * LC;         // [C][RS]
-  float* sG = sW + kC * kRS;        // [C]
+  float* sWd = sW + kC * kRS;       // [C][RS] W decayed to the chunk end
+  float* sG = sWd + kC * kRS;       // [C]
+  float* sGam = sG + kC;            // [C] gamma_i
+  float* sDec = sGam + kC;          // [C] gamma_C / gamma_i
+  static_assert(kC * kRS == 4 * 256, "W / O tiling: 4 outputs per thread");
   const int r0 = blockIdx.x * kRS, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
   const size_t bh = static_cast<size_t>(b) * H + h;
@@ -213,47 +223,82 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
       sY[i * LK + x] = Y[cid * kC * DK + e];
     }
     for (int e = tid; e < kC * kC; e += 256) sP[(e / kC) * LC + (e % kC)] = Pm[cid * kC * kC + e];
-    if (tid < kC) sG[tid] = Gc[cid * kC + tid];
+    if (tid < kC) {
+      const float gi = Gc[cid * kC + tid];
+      sG[tid] = gi;
+      sGam[tid] = __expf(gi);                                 // gamma_i
+      sDec[tid] = __expf(Gc[cid * kC + kC - 1] - gi);         // gamma_C / gamma_i
+    }
     if (Schk)
       for (int e = tid; e < kRS * DK; e += 256) {
         const int r = e / DK, x = e - r * DK;
         Schk[(cid * DV + r0 + r) * DK + x] = sS[r * LK + x];
       }
     __syncthreads();
-    // W = U - Y S^T   ([C][RS])
-    for (int e = tid; e < kC * kRS; e += 256) {
-      const int i = e / kRS, r = e - i * kRS;
-      float w = cU[i * DV + r0 + r];
+    // W = U - Y S^T ([C][RS]); thread: row i = tid / 4, columns r = 4 (tid % 4) .. + 3
+    {
+      const int i = tid >> 2, rb = (tid & 3) * 4;
+      float w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) w[u] = cU[i * DV + r0 + rb + u];
       const float* yi = sY + i * LK;
-      const float* sr = sS + r * LK;
-#pragma unroll 8
-      for (int x = 0; x < DK; ++x) w -= yi[x] * sr[x];
-      sW[e] = w;
+#pragma unroll 4
+      for (int x = 0; x < DK; ++x) {
+        const float y = yi[x];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) w[u] -= y * sS[(rb + u) * LK + x];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        sW[i * kRS + rb + u] = w[u];
+        sWd[i * kRS + rb + u] = w[u] * sDec[i];               // decayed to the chunk end
+      }
     }
     __syncthreads();
-    // O = scale (gamma_i Q^_i . S_r + sum_{j<=i} P_ij w_jr)
-    for (int e = tid; e < kC * kRS; e += 256) {
-      const int i = e / kRS, r = e - i * kRS;
+    // O = scale (gamma_i Q^_i . S_r + sum_{j<=i} P_ij w_jr); same thread tiling
+    {
+      const int i = tid >> 2, rb = (tid & 3) * 4;
       const int t = c * kC + i;
-      if (t >= T) continue;
-      float a = 0.f;
+      float a[4] = {0.f, 0.f, 0.f, 0.f};
       const float* qi = sQ + i * LK;
-      const float* sr = sS + r * LK;
-#pragma unroll 8
-      for (int x = 0; x < DK; ++x) a += qi[x] * sr[x];
-      a *= __expf(sG[i]);
+#pragma unroll 4
+      for (int x = 0; x < DK; ++x) {
+        const float qv = qi[x];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a[u] += qv * sS[(rb + u) * LK + x];
+      }
+      const float gi = sGam[i];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] *= gi;
       const float* pi = sP + i * LC;
-      for (int j = 0; j <= i; ++j) a += pi[j] * sW[j * kRS + r];
-      o[((static_cast<size_t>(b) * T + t) * H + h) * DV + r0 + r] = __float2bfloat16_rn(scale * a);
+      for (int j = 0; j <= i; ++j) {
+        const float pv = pi[j];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a[u] += pv * sW[j * kRS + rb + u];
+      }
+      if (t < T) {
+        __nv_bfloat16* orow = o + ((static_cast<size_t>(b) * T + t) * H + h) * DV + r0 + rb;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) orow[u] = __float2bfloat16_rn(scale * a[u]);
+      }
     }
     __syncthreads();
-    // S_r = gamma_C S_r + sum_j exp(G_C - G_j) w_jr k^_j
-    const float gl = sG[kC - 1];
-    for (int e = tid; e < kRS * DK; e += 256) {
-      const int r = e / DK, x = e - r * DK;
-      float s = __expf(gl) * sS[r * LK + x];
-      for (int j = 0; j < kC; ++j) s += __expf(gl - sG[j]) * sW[j * kRS + r] * sK[j * LK + x];
-      sS[r * LK + x] = s;
+    // S_r = gamma_C S_r + sum_j (gamma_C / gamma_j) w_jr k^_j; thread: column x, RS*DK/256
+    // rows
+    {
+      constexpr int RPT = kRS * DK / 256;        // rows per thread (8 for DK 128, 4 for 64)
+      const int x = tid % DK, rb = (tid / DK) * RPT;
+      const float eC = sGam[kC - 1];
+      float acc[RPT];
+#pragma unroll
+      for (int u = 0; u < RPT; ++u) acc[u] = eC * sS[(rb + u) * LK + x];
+      for (int j = 0; j < kC; ++j) {
+        const float kv = sK[j * LK + x];
+#pragma unroll
+        for (int u = 0; u < RPT; ++u) acc[u] += sWd[j * kRS + rb + u] * kv;
+      }
+#pragma unroll
+      for (int u = 0; u < RPT; ++u) sS[(rb + u) * LK + x] = acc[u];
     }
   }
   __syncthreads();
@@ -262,6 +307,406 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
       const int r = e / DK, x = e - r * DK;
       ST[(bh * DV + r0 + r) * DK + x] = sS[r * LK + x];
     }
+}
+
+// ---------------------------------------------------------------------------- backward
+//
+// Gradients of <do, o> + <dS_T, S_T> (chunked form, derived for these kernels).  Per chunk,
+// with dS1 the gradient of the state at the chunk's end:
+//     dW  = s P^T dO + E dS1^T                       E = diag(gamma_C / gamma) K^
+//     dS0 = gamma_C dS1 + s dO^T diag(gamma) Q^ - dW^T Y      (the state gradient one chunk
+//                                                              earlier: a scan backwards)
+// and then, locally in the chunk, with W = U - Y S0^T:
+//     dP = s dO W^T (lower triangle)   dQ^ = (Gam . dP) K^ + s diag(gamma) dO S0
+//     dK^ = (Gam . dP)^T Q^ + diag(gamma_C / gamma) W dS1 + diag(beta gamma) dBk + (Z + Z^T) K^
+//     dBv = A^-T dW,  dBk = -A^-T dW S0,  dM = -(dBv U^T + dBk Y^T) (strictly lower)
+//     dV = diag(beta) dBv,  Z = dM . beta Gam,  and the beta and log-decay gradients of every
+//     place they enter (A, U, Y, P, E, gamma); dg is the reverse cumulative sum of dG.
+
+// Backward scan over chunks for RS value rows of dS (grid: DV/RS x H x B).  Writes dW (the
+// slice's columns) and the state gradient at every chunk end; dS0 at the end.
+template <int DK, int DV>
+__global__ void __launch_bounds__(256) gdr_bwd_scan_kernel(
+    const float* __restrict__ Qh, const float* __restrict__ Kh, const float* __restrict__ Y,
+    const float* __restrict__ Pm, const float* __restrict__ Gc,
+    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ dST, int T, int H, int nch,
+    float scale, float* __restrict__ dW, float* __restrict__ dSchk, float* __restrict__ dS0) {
+  constexpr int LK = Ld<DK>::v, LC = Ld<kC>::v;
+  extern __shared__ float sm[];
+  float* sD = sm;                   // [RS][LK] state gradient rows
+  float* sQ = sD + kRS * LK;        // [C][LK]
+  float* sK = sQ + kC * LK;         // [C][LK]
+  float* sY = sK + kC * LK;         // [C][LK]
+  float* sP = sY + kC * LK;         // [C][LC]
+  float* sO = sP + kC * LC;         // [C][RS] dO slice
+  float* sW = sO + kC * kRS;        // [C][RS] dW slice
+  float* sOg = sW + kC * kRS;       // [C][RS] s gamma_i dO
+  float* sG = sOg + kC * kRS;       // [C]
+  float* sGam = sG + kC;            // [C] gamma_i
+  float* sDec = sGam + kC;          // [C] gamma_C / gamma_i
+  static_assert(kC * kRS == 4 * 256, "dW tiling: 4 outputs per thread");
+  const int r0 = blockIdx.x * kRS, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  const size_t bh = static_cast<size_t>(b) * H + h;
+  for (int e = tid; e < kRS * DK; e += 256) {
+    const int r = e / DK, x = e - r * DK;
+    sD[r * LK + x] = dST ? dST[(bh * DV + r0 + r) * DK + x] : 0.f;
+  }
+  for (int c = nch - 1; c >= 0; --c) {
+    const size_t cid = bh * nch + c;
+    __syncthreads();
+    for (int e = tid; e < kC * DK; e += 256) {
+      const int i = e / DK, x = e - i * DK;
+      sQ[i * LK + x] = Qh[cid * kC * DK + e];
+      sK[i * LK + x] = Kh[cid * kC * DK + e];
+      sY[i * LK + x] = Y[cid * kC * DK + e];
+    }
+    for (int e = tid; e < kC * kC; e += 256) sP[(e / kC) * LC + (e % kC)] = Pm[cid * kC * kC + e];
+    for (int e = tid; e < kC * kRS; e += 256) {
+      const int i = e / kRS, r = e - i * kRS;
+      const int t = c * kC + i;
+      sO[e] = t < T ? bf(dO[((static_cast<size_t>(b) * T + t) * H + h) * DV + r0 + r]) : 0.f;
+    }
+    if (tid < kC) {
+      const float gi = Gc[cid * kC + tid];
+      sG[tid] = gi;
+      sGam[tid] = __expf(gi);
+      sDec[tid] = __expf(Gc[cid * kC + kC - 1] - gi);
+    }
+    for (int e = tid; e < kRS * DK; e += 256) {
+      const int r = e / DK, x = e - r * DK;
+      dSchk[(cid * DV + r0 + r) * DK + x] = sD[r * LK + x];
+    }
+    __syncthreads();
+    // dW = s P^T dO + E dS1^T; thread: row i = tid / 4, columns r = 4 (tid % 4) .. + 3
+    {
+      const int i = tid >> 2, rb = (tid & 3) * 4;
+      float a[4] = {0.f, 0.f, 0.f, 0.f}, bs[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int t = i; t < kC; ++t) {
+        const float pv = sP[t * LC + i];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a[u] += pv * sO[t * kRS + rb + u];
+      }
+      const float* ki = sK + i * LK;
+#pragma unroll 4
+      for (int x = 0; x < DK; ++x) {
+        const float kv = ki[x];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) bs[u] += kv * sD[(rb + u) * LK + x];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float w = scale * a[u] + sDec[i] * bs[u];
+        sW[i * kRS + rb + u] = w;
+        dW[cid * kC * DV + i * DV + r0 + rb + u] = w;
+        sOg[i * kRS + rb + u] = scale * sGam[i] * sO[i * kRS + rb + u];
+      }
+    }
+    __syncthreads();
+    // dS0 = gamma_C dS1 + sum_i (s gamma_i dO_ir) q^_i - sum_i dW_ir Y_i; thread: column x
+    {
+      constexpr int RPT = kRS * DK / 256;
+      const int x = tid % DK, rb = (tid / DK) * RPT;
+      const float eC = sGam[kC - 1];
+      float acc[RPT];
+#pragma unroll
+      for (int u = 0; u < RPT; ++u) acc[u] = eC * sD[(rb + u) * LK + x];
+      for (int i = 0; i < kC; ++i) {
+        const float qv = sQ[i * LK + x], yv = sY[i * LK + x];
+#pragma unroll
+        for (int u = 0; u < RPT; ++u)
+          acc[u] += sOg[i * kRS + rb + u] * qv - sW[i * kRS + rb + u] * yv;
+      }
+#pragma unroll
+      for (int u = 0; u < RPT; ++u) sD[(rb + u) * LK + x] = acc[u];
+    }
+  }
+  __syncthreads();
+  if (dS0)
+    for (int e = tid; e < kRS * DK; e += 256) {
+      const int r = e / DK, x = e - r * DK;
+      dS0[(bh * DV + r0 + r) * DK + x] = sD[r * LK + x];
+    }
+}
+
+// Per-chunk backward (grid: chunks x H x B): everything local to the chunk once dW and the
+// state gradient at its end are known.  dq^, dk^ accumulate in the outputs dq, dk (fp32),
+// then the L2 normalisations are back-propagated in place.
+template <int DK, int DV>
+__global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
+    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+    const __nv_bfloat16* __restrict__ v, const float* __restrict__ beta,
+    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ Qh,
+    const float* __restrict__ Kh, const float* __restrict__ Y, const float* __restrict__ U,
+    const float* __restrict__ Pm, const float* __restrict__ Gc, const float* __restrict__ Ai,
+    const float* __restrict__ Schk, const float* __restrict__ dSchk,
+    const float* __restrict__ dWg, int T, int H, int nch, float scale,
+    float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
+    float* __restrict__ dbeta, float* __restrict__ dg) {
+  constexpr int LK = Ld<DK>::v, LV = Ld<DV>::v, LC = Ld<kC>::v;
+  constexpr int LX = LK > LV ? LK : LV;
+  extern __shared__ float sm[];
+  float* sQ = sm;                   // [C][LK] q^
+  float* sK = sQ + kC * LK;         // [C][LK] k^
+  float* sW = sK + kC * LK;         // [C][LX] W, later dBk
+  float* sdW = sW + kC * LX;        // [C][LV] dW
+  float* sX = sdW + kC * LV;        // [C][LX] dO, later dY, later dBv
+  float* sC1 = sX + kC * LX;        // [C][LC] dP masked by Gam (G . dP), later Z
+  float* sC2 = sC1 + kC * LC;       // [C][LC] R = dP . P + dM . M (log-decay gradient)
+  float* sC3 = sC2 + kC * LC;       // [C][LC] dM . Gam . K^K^T (beta gradient)
+  float* sG = sC3 + kC * LC;        // [C] cumulative log decay
+  float* sB = sG + kC;              // [C] beta
+  float* sdG = sB + kC;             // [C] log-decay gradient
+  float* sdB = sdG + kC;            // [C] beta gradient
+  float* sPart = sdB + kC;          // [C][8] per-warp partial sums
+  float* sRed = sPart + kC * 8;     // [8] block reduction
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const size_t bh = static_cast<size_t>(b) * H + h;
+  const size_t cid = bh * nch + c;
+  const int t0 = c * kC;
+  const float* S0 = Schk + cid * DV * DK;    // state at the chunk start
+  const float* dS1 = dSchk + cid * DV * DK;  // gradient of the state at the chunk end
+  const float* cU = U + cid * kC * DV;
+  const float* cY = Y + cid * kC * DK;
+  const float* cP = Pm + cid * kC * kC;
+  const float* cA = Ai + cid * kC * kC;      // A^-1 (lower triangular)
+  auto row = [&](int i) { return ((static_cast<size_t>(b) * T + t0 + i) * H + h); };
+  // partial sums of 32 lanes, then the 8 warps in order (deterministic block reductions
+  // keyed by a row index i: one warp covers 32 consecutive columns of one row)
+  auto warp_sum = [](float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+  };
+
+  for (int e = tid; e < kC * DK; e += 256) {
+    const int i = e / DK, x = e - i * DK;
+    sQ[i * LK + x] = Qh[cid * kC * DK + e];
+    sK[i * LK + x] = Kh[cid * kC * DK + e];
+  }
+  for (int e = tid; e < kC * DV; e += 256) {
+    const int i = e / DV, r = e - i * DV;
+    sdW[i * LV + r] = dWg[cid * kC * DV + e];
+    sX[i * LX + r] = t0 + i < T ? bf(dO[row(i) * DV + r]) : 0.f;
+  }
+  if (tid < kC) {
+    sG[tid] = Gc[cid * kC + tid];
+    sB[tid] = t0 + tid < T ? beta[row(tid)] : 0.f;
+    sdG[tid] = 0.f;
+    sdB[tid] = 0.f;
+  }
+  __syncthreads();
+  const float gl = sG[kC - 1];
+  // W = U - Y S0^T  (lanes over i: Y staged rows; S0 row r broadcast)
+  for (int e = tid; e < kC * DV; e += 256) {
+    const int r = e / kC, i = e - r * kC;
+    float w = cU[i * DV + r];
+    const float* yi = cY + i * DK;
+    const float* s0 = S0 + r * DK;
+    for (int x = 0; x < DK; ++x) w -= __ldg(&yi[x]) * __ldg(&s0[x]);
+    sW[i * LX + r] = w;
+  }
+  __syncthreads();
+  // dP_ij = s dO_i . W_j (j <= i), kept as (Gam . dP); and R_ij = dP_ij P_ij
+  for (int e = tid; e < kC * kC; e += 256) {
+    const int i = e / kC, j = e - i * kC;
+    float gd = 0.f, rr = 0.f;
+    if (j <= i) {
+      float a = 0.f;
+      for (int r = 0; r < DV; ++r) a += sX[i * LX + r] * sW[j * LX + r];
+      const float dp = scale * a;
+      gd = __expf(sG[i] - sG[j]) * dp;
+      rr = dp * __ldg(&cP[i * kC + j]);
+    }
+    sC1[i * LC + j] = gd;
+    sC2[i * LC + j] = rr;
+  }
+  __syncthreads();
+  // dq^ = (Gam . dP) K^ + s gamma_i dO_i S0, and dG_i += s gamma_i (dO S0)_i . q^_i
+  for (int e = tid; e < kC * DK; e += 256) {
+    const int i = e / DK, x = e - i * DK;
+    float a = 0.f;
+    for (int j = 0; j <= i; ++j) a += sC1[i * LC + j] * sK[j * LK + x];
+    float os = 0.f;
+    for (int r = 0; r < DV; ++r) os += sX[i * LX + r] * __ldg(&S0[r * DK + x]);
+    const float gi = __expf(sG[i]);
+    a += scale * gi * os;
+    if (t0 + i < T) dq[row(i) * DK + x] = a;
+    const float part = warp_sum(scale * gi * os * sQ[i * LK + x]);
+    if (lane == 0) sPart[i * 8 + (x >> 5)] = part;
+  }
+  __syncthreads();
+  if (tid < kC) {
+    float a = 0.f;
+    for (int w = 0; w < DK / 32; ++w) a += sPart[tid * 8 + w];
+    sdG[tid] += a;
+  }
+  __syncthreads();
+  // dk^ = (Gam . dP)^T Q^ + diag(gamma_C / gamma) (W dS1); dG from E
+  for (int e = tid; e < kC * DK; e += 256) {
+    const int j = e / DK, x = e - j * DK;
+    float a = 0.f;
+    for (int i = j; i < kC; ++i) a += sC1[i * LC + j] * sQ[i * LK + x];
+    float de = 0.f;
+    for (int r = 0; r < DV; ++r) de += sW[j * LX + r] * __ldg(&dS1[r * DK + x]);
+    const float ej = __expf(gl - sG[j]);
+    a += ej * de;
+    if (t0 + j < T) dk[row(j) * DK + x] = a;
+    const float part = warp_sum(ej * de * sK[j * LK + x]);
+    if (lane == 0) sPart[j * 8 + (x >> 5)] = part;
+  }
+  // gamma_C <dS1, S0> (block reduction in a fixed order)
+  {
+    float a = 0.f;
+    for (int e = tid; e < DV * DK; e += 256) a += __ldg(&dS1[e]) * __ldg(&S0[e]);
+    a = warp_sum(a);
+    if (lane == 0) sRed[warp] = a;
+  }
+  __syncthreads();
+  if (tid < kC) {
+    float a = 0.f;
+    for (int w = 0; w < DK / 32; ++w) a += sPart[tid * 8 + w];
+    sdG[tid] -= a;                       // exp(G_C - G_j): d/dG_j = -(...)
+    float tot = 0.f;
+    if (tid == kC - 1) {
+      for (int j = 0; j < kC; ++j) {
+        float aj = 0.f;
+        for (int w = 0; w < DK / 32; ++w) aj += sPart[j * 8 + w];
+        tot += aj;                       // d/dG_C of every exp(G_C - G_j)
+      }
+      float sr = 0.f;
+      for (int w = 0; w < 8; ++w) sr += sRed[w];
+      tot += __expf(gl) * sr;            // gamma_C S0
+      sdG[tid] += tot;
+    }
+  }
+  __syncthreads();
+  // dY = -dW S0 -> sX (dO is no longer needed)
+  for (int e = tid; e < kC * DK; e += 256) {
+    const int i = e / DK, x = e - i * DK;
+    float a = 0.f;
+    for (int r = 0; r < DV; ++r) a -= sdW[i * LV + r] * __ldg(&S0[r * DK + x]);
+    sX[i * LX + x] = a;
+  }
+  __syncthreads();
+  // dBk = A^-T dY -> sW (W is no longer needed); dk^ += beta gamma dBk; beta, G from Bk
+  for (int e = tid; e < kC * DK; e += 256) {
+    const int j = e / DK, x = e - j * DK;
+    float a = 0.f;
+    for (int i = j; i < kC; ++i) a += __ldg(&cA[i * kC + j]) * sX[i * LX + x];
+    sW[j * LX + x] = a;
+    const float bg = sB[j] * __expf(sG[j]);
+    if (t0 + j < T) dk[row(j) * DK + x] += bg * a;
+    const float part = warp_sum(a * sK[j * LK + x]);
+    if (lane == 0) sPart[j * 8 + (x >> 5)] = part;
+  }
+  __syncthreads();
+  if (tid < kC) {
+    float a = 0.f;
+    for (int w = 0; w < DK / 32; ++w) a += sPart[tid * 8 + w];
+    const float gj = __expf(sG[tid]);
+    sdB[tid] += gj * a;
+    sdG[tid] += sB[tid] * gj * a;
+  }
+  __syncthreads();
+  // dBv = A^-T dW -> sX (dY is no longer needed); dV = beta dBv; beta from Bv
+  for (int e = tid; e < kC * DV; e += 256) {
+    const int j = e / DV, r = e - j * DV;
+    float a = 0.f;
+    for (int i = j; i < kC; ++i) a += __ldg(&cA[i * kC + j]) * sdW[i * LV + r];
+    sX[j * LX + r] = a;
+    float vj = 0.f;
+    if (t0 + j < T) {
+      dv[row(j) * DV + r] = sB[j] * a;
+      vj = bf(v[row(j) * DV + r]);
+    }
+    const float part = warp_sum(a * vj);
+    if (lane == 0) sPart[j * 8 + (r >> 5)] = part;
+  }
+  __syncthreads();
+  if (tid < kC) {
+    float a = 0.f;
+    for (int w = 0; w < DV / 32; ++w) a += sPart[tid * 8 + w];
+    sdB[tid] += a;
+  }
+  __syncthreads();
+  // dM_ij = -(dBv_i . U_j + dBk_i . Y_j) for j < i; with M_ij = beta_i Gam_ij k^_i.k^_j:
+  // Z_ij = dM_ij beta_i Gam_ij (-> sC1, for dk^), dM_ij M_ij (-> R in sC2, for dG) and
+  // dM_ij Gam_ij k^_i.k^_j (-> sC3, for dbeta)
+  for (int e = tid; e < kC * kC; e += 256) {
+    const int j = e / kC, i = e - j * kC;
+    float z = 0.f, bt = 0.f;
+    if (j < i) {
+      float a = 0.f;
+      const float* uj = cU + j * DV;
+      for (int r = 0; r < DV; ++r) a += sX[i * LX + r] * __ldg(&uj[r]);
+      const float* yj = cY + j * DK;
+      for (int x = 0; x < DK; ++x) a += sW[i * LX + x] * __ldg(&yj[x]);
+      float kk = 0.f;
+      for (int x = 0; x < DK; ++x) kk += sK[i * LK + x] * sK[j * LK + x];
+      const float gk = __expf(sG[i] - sG[j]) * kk;   // Gam_ij k^_i.k^_j
+      bt = -a * gk;
+      z = -a * sB[i] * __expf(sG[i] - sG[j]);
+      sC2[i * LC + j] += bt * sB[i];                   // dM_ij M_ij
+    }
+    sC1[i * LC + j] = z;
+    sC3[i * LC + j] = bt;
+  }
+  __syncthreads();
+  if (tid < kC) {
+    const int i = tid;
+    float rs = 0.f, cs = 0.f, db = 0.f;
+    for (int j = 0; j < kC; ++j) {
+      rs += sC2[i * LC + j];
+      cs += sC2[j * LC + i];
+      db += sC3[i * LC + j];
+    }
+    sdB[i] += db;
+    sdG[i] += rs - cs;
+  }
+  __syncthreads();
+  // dk^ += Z K^ + Z^T K^
+  for (int e = tid; e < kC * DK; e += 256) {
+    const int i = e / DK, x = e - i * DK;
+    float a = 0.f;
+    for (int j = 0; j < kC; ++j) a += (sC1[i * LC + j] + sC1[j * LC + i]) * sK[j * LK + x];
+    if (t0 + i < T) dk[row(i) * DK + x] += a;
+  }
+  __syncthreads();
+  // dg = reverse cumulative sum of dG within the chunk; dbeta out
+  if (tid == 0) {
+    float run = 0.f;
+    for (int i = kC - 1; i >= 0; --i) {
+      run += sdG[i];
+      if (t0 + i < T) {
+        dg[row(i)] = run;
+        dbeta[row(i)] = sdB[i];
+      }
+    }
+  }
+  // L2 normalisations: dx = (dx^ - x^ (x^ . dx^)) / ||x||  (one warp per row)
+  for (int i = warp; i < kC; i += 8) {
+    if (t0 + i >= T) continue;
+    float nq = 0.f, nk = 0.f, pq = 0.f, pk = 0.f;
+    for (int x = lane; x < DK; x += 32) {
+      const float qv = bf(q[row(i) * DK + x]), kv = bf(k[row(i) * DK + x]);
+      nq += qv * qv;
+      nk += kv * kv;
+      pq += dq[row(i) * DK + x] * sQ[i * LK + x];
+      pk += dk[row(i) * DK + x] * sK[i * LK + x];
+    }
+    nq = warp_sum(nq);
+    nk = warp_sum(nk);
+    pq = warp_sum(pq);
+    pk = warp_sum(pk);
+    const float iq = nq > 0.f ? 1.0f / sqrtf(nq) : 0.f;
+    const float ik = nk > 0.f ? 1.0f / sqrtf(nk) : 0.f;
+    for (int x = lane; x < DK; x += 32) {
+      dq[row(i) * DK + x] = (dq[row(i) * DK + x] - sQ[i * LK + x] * pq) * iq;
+      dk[row(i) * DK + x] = (dk[row(i) * DK + x] - sK[i * LK + x] * pk) * ik;
+    }
+  }
 }
 
 size_t gdr_ws(int B, int T, int H, int dk, int dv) {
@@ -291,10 +736,11 @@ int gdr_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloat16*
                                        static_cast<int>(sm1));
   if (e != cudaSuccess) return static_cast<int>(e);
   mark_before(MOE_KERNEL_GDR_CHUNK, s);
-  k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, Qh, Kh, Yw, Uw, Pw, Gw);
+  k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, Qh, Kh, Yw, Uw, Pw, Gw,
+                                       nullptr);
   mark_after(MOE_KERNEL_GDR_CHUNK, s);
-  const size_t sm2 = (kRS * Ld<DK>::v + 3 * kC * Ld<DK>::v + kC * Ld<kC>::v + kC * kRS + kC) *
-                     sizeof(float);
+  const size_t sm2 = (kRS * Ld<DK>::v + 3 * kC * Ld<DK>::v + kC * Ld<kC>::v + 2 * kC * kRS +
+                      3 * kC) * sizeof(float);
   auto k2 = gdr_scan_kernel<DK, DV>;
   e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm2));
   if (e != cudaSuccess) return static_cast<int>(e);
@@ -302,6 +748,57 @@ int gdr_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloat16*
   k2<<<dim3(DV / kRS, H, B), 256, sm2, s>>>(
       Qh, Kh, Yw, Uw, Pw, Gw, S0, T, H, nch, scale, o, ST, Schk);
   mark_after(MOE_KERNEL_GDR_SCAN, s);
+  return static_cast<int>(cudaGetLastError());
+}
+
+size_t gdr_bwd_ws(int B, int T, int H, int dk, int dv) {
+  const size_t nch = (T + kC - 1) / kC;
+  const size_t chunks = static_cast<size_t>(B) * H * nch;
+  return gdr_ws(B, T, H, dk, dv) + up256(chunks * kC * kC * 4) + up256(chunks * kC * dv * 4) +
+         up256(chunks * static_cast<size_t>(dv) * dk * 4);
+}
+
+template <int DK, int DV>
+int gdr_bwd_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                   const __nv_bfloat16* v, const float* beta, const float* g, float scale,
+                   const __nv_bfloat16* dO, const float* dST, const float* Schk, float* dq,
+                   float* dk, float* dv, float* dbeta, float* dg, float* dS0, void* ws,
+                   cudaStream_t s) {
+  const int nch = (T + kC - 1) / kC;
+  const size_t chunks = static_cast<size_t>(B) * H * nch;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* Qh = reinterpret_cast<float*>(w); w += up256(chunks * kC * DK * 4);
+  float* Kh = reinterpret_cast<float*>(w); w += up256(chunks * kC * DK * 4);
+  float* Yw = reinterpret_cast<float*>(w); w += up256(chunks * kC * DK * 4);
+  float* Uw = reinterpret_cast<float*>(w); w += up256(chunks * kC * DV * 4);
+  float* Pw = reinterpret_cast<float*>(w); w += up256(chunks * kC * kC * 4);
+  float* Gw = reinterpret_cast<float*>(w); w += up256(chunks * kC * 4);
+  float* Aw = reinterpret_cast<float*>(w); w += up256(chunks * kC * kC * 4);
+  float* dWw = reinterpret_cast<float*>(w); w += up256(chunks * kC * DV * 4);
+  float* dSw = reinterpret_cast<float*>(w);
+  const size_t sm1 = (2 * kC * Ld<DK>::v + 2 * kC * Ld<kC>::v + 3 * kC) * sizeof(float);
+  auto k1 = gdr_chunk_kernel<DK, DV>;
+  cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(sm1));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, Qh, Kh, Yw, Uw, Pw, Gw, Aw);
+  const size_t sm2 = (kRS * Ld<DK>::v + 3 * kC * Ld<DK>::v + kC * Ld<kC>::v + 3 * kC * kRS +
+                      3 * kC) * sizeof(float);
+  auto k2 = gdr_bwd_scan_kernel<DK, DV>;
+  e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm2));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  k2<<<dim3(DV / kRS, H, B), 256, sm2, s>>>(Qh, Kh, Yw, Pw, Gw, dO, dST, T, H, nch, scale, dWw,
+                                            dSw, dS0);
+  constexpr int LX = Ld<DK>::v > Ld<DV>::v ? Ld<DK>::v : Ld<DV>::v;
+  const size_t sm3 = (2 * kC * Ld<DK>::v + 2 * kC * LX + kC * Ld<DV>::v + 3 * kC * Ld<kC>::v +
+                      4 * kC + 8 * kC + 8) * sizeof(float);
+  auto k3 = gdr_bwd_chunk_kernel<DK, DV>;
+  e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm3));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  mark_before(MOE_KERNEL_GDR_BWD, s);
+  k3<<<dim3(nch, H, B), 256, sm3, s>>>(q, k, v, beta, dO, Qh, Kh, Yw, Uw, Pw, Gw, Aw, Schk, dSw,
+                                       dWw, T, H, nch, scale, dq, dk, dv, dbeta, dg);
+  mark_after(MOE_KERNEL_GDR_BWD, s);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -341,6 +838,39 @@ int moe_gdr_forward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, con
   else
     e = gdr_launch<64, 64>(B, T, H, q_, k_, v_, beta, g, S0, scale, o_, S_T, S_chunks, workspace, stream);
   count_launches(2);
+  return e == 0 ? MOE_OK : MOE_ERR_CUDA;
+}
+
+size_t moe_gdr_backward_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv) {
+  if (B <= 0 || T <= 0 || H <= 0 || dk <= 0 || dv <= 0) return 0;
+  return gdr_bwd_ws(B, T, H, dk, dv);
+}
+
+int moe_gdr_backward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, const moe_bf16* q,
+                     const moe_bf16* k, const moe_bf16* v, const float* beta, const float* g,
+                     float scale, const moe_bf16* d_o, const float* dS_T, const float* S_chunks,
+                     float* dq, float* dk_out, float* dv_out, float* dbeta, float* dg,
+                     float* dS0, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  if (B <= 0 || T <= 0 || H <= 0 || !q || !k || !v || !beta || !g || !d_o || !S_chunks || !dq ||
+      !dk_out || !dv_out || !dbeta || !dg)
+    return MOE_ERR_INVALID_ARG;
+  if (!((dk == 64 || dk == 128) && (dv == 64 || dv == 128))) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H * ((T + kC - 1) / kC) > (1ll << 24)) return MOE_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < gdr_bwd_ws(B, T, H, dk, dv)) return MOE_ERR_WORKSPACE;
+  const auto* q_ = reinterpret_cast<const __nv_bfloat16*>(q);
+  const auto* k_ = reinterpret_cast<const __nv_bfloat16*>(k);
+  const auto* v_ = reinterpret_cast<const __nv_bfloat16*>(v);
+  const auto* o_ = reinterpret_cast<const __nv_bfloat16*>(d_o);
+  int e;
+  if (dk == 128 && dv == 128)
+    e = gdr_bwd_launch<128, 128>(B, T, H, q_, k_, v_, beta, g, scale, o_, dS_T, S_chunks, dq, dk_out, dv_out, dbeta, dg, dS0, workspace, stream);
+  else if (dk == 128)
+    e = gdr_bwd_launch<128, 64>(B, T, H, q_, k_, v_, beta, g, scale, o_, dS_T, S_chunks, dq, dk_out, dv_out, dbeta, dg, dS0, workspace, stream);
+  else if (dv == 128)
+    e = gdr_bwd_launch<64, 128>(B, T, H, q_, k_, v_, beta, g, scale, o_, dS_T, S_chunks, dq, dk_out, dv_out, dbeta, dg, dS0, workspace, stream);
+  else
+    e = gdr_bwd_launch<64, 64>(B, T, H, q_, k_, v_, beta, g, scale, o_, dS_T, S_chunks, dq, dk_out, dv_out, dbeta, dg, dS0, workspace, stream);
+  count_launches(3);
   return e == 0 ? MOE_OK : MOE_ERR_CUDA;
 }
 
