@@ -118,8 +118,15 @@ struct Carver {
   }
 };
 
+// expert tile of the router GEMM: 224 when it divides E (896 = 4 x 224: fewer, larger tiles,
+// less L2 traffic per flop), else 128
+int router_bn(const moe_problem* p) { return (p->E % 224 == 0) ? 224 : 128; }
+
 size_t route_ws(const moe_problem* p) {
-  return up256(2ull * p->E * p->d * 2) + up256(static_cast<size_t>(p->T) * p->E * 4);
+  const size_t nt = (p->E + router_bn(p) - 1) / router_bn(p);
+  return up256(2ull * p->E * p->d * 2) + up256(static_cast<size_t>(p->T) * p->E * 4) +
+         up256(static_cast<size_t>(p->T) * nt * kRouteTileK * 8) +
+         up256(static_cast<size_t>(p->T) * nt * 8);
 }
 
 size_t ffn_ws(const moe_problem* p, int rows_max) {
@@ -190,12 +197,15 @@ int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, co
   __nv_bfloat16* w_split = cv.take<__nv_bfloat16>(2ull * E * d);
   float* logits_ws = cv.take<float>(static_cast<size_t>(T) * E);
   float* L = logits ? logits : logits_ws;
+  const int bn = router_bn(p);
+  const int nt = (E + bn - 1) / bn;
+  uint64_t* cand = cv.take<uint64_t>(static_cast<size_t>(T) * nt * kRouteTileK);
+  float* stats = cv.take<float>(static_cast<size_t>(T) * nt * 2);
+  // top-k fused into the router GEMM's epilogue when the per-tile candidates suffice
+  const bool fused = p->k <= kRouteTileK;
 
   MOE_CUDA(launch_split_router(w_router, w_split, w_split + static_cast<size_t>(E) * d,
                                static_cast<size_t>(E) * d, stream));
-  // expert tile: 224 when it divides E (896 = 4 x 224: fewer, larger tiles, less L2 traffic
-  // per flop), else 128
-  const int bn = (E % 224 == 0) ? 224 : 128;
   GemmParams P = gemm_params();
   MOE_TRY(encode_map_kmajor(&P.maps[0], x, d, T, 1, kBM));
   MOE_TRY(encode_map_kmajor(&P.maps[1], w_split, d, E, 2, bn));
@@ -212,11 +222,20 @@ int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, co
   P.bias = bias;
   P.b_policy = 1;  // the router weights are re-read by every token tile
   P.dev_status = dev_status;
+  if (fused) {
+    P.out1 = cand;
+    P.out2 = stats;
+  }
   mark_before(MOE_KERNEL_ROUTER_GEMM, stream);
-  MOE_CUDA(launch_gemm_router(P, bn, stream));
+  MOE_CUDA(fused ? launch_gemm_router_topk(P, bn, stream) : launch_gemm_router(P, bn, stream));
   mark_after(MOE_KERNEL_ROUTER_GEMM, stream);
   mark_before(MOE_KERNEL_TOPK, stream);
-  MOE_CUDA(launch_topk_softmax(L, T, E, p->k, topk_idx, topk_gate, prob_partials, stream));
+  if (fused) {
+    MOE_CUDA(launch_route_merge(L, cand, stats, T, E, p->k, nt, topk_idx, topk_gate,
+                                prob_partials, stream));
+  } else {
+    MOE_CUDA(launch_topk_softmax(L, T, E, p->k, topk_idx, topk_gate, prob_partials, stream));
+  }
   mark_after(MOE_KERNEL_TOPK, stream);
   count_launches(3);
   return MOE_OK;

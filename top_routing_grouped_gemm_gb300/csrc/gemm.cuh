@@ -22,6 +22,7 @@
 #pragma once
 
 #include "ptx.cuh"
+#include "topk_keys.cuh"
 
 namespace moe {
 
@@ -38,7 +39,7 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
   // The router (EPI_F32_BIAS) with two B operands sums them into one accumulator: they are
   // the bf16 hi and lo parts of the same fp32 weights, both multiplied by the same A stage.
-  static constexpr bool SUMB = (EPI == EPI_F32_BIAS && NB == 2);
+  static constexpr bool SUMB = ((EPI == EPI_F32_BIAS || EPI == EPI_ROUTE) && NB == 2);
   static constexpr int ACC_NB = SUMB ? 1 : NB;  // accumulators of BN columns per subtile
   static constexpr int ACC_COLS = MSUB * ACC_NB * BN;
   static constexpr int NACC = (2 * ACC_COLS * CTAS <= 512) ? 2 : 1;
@@ -644,10 +645,77 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
                 *reinterpret_cast<float4*>(dst + i) = o;
               }
             } else {
-              for (int i = 0; i < 16 && col + i < P.N; ++i)
-                dst[i] = v[i] + (P.bias ? __ldg(&P.bias[col + i]) : 0.f);
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (col + i < P.N) dst[i] = v[i] + (P.bias ? __ldg(&P.bias[col + i]) : 0.f);
             }
           }
+        }
+      } else if constexpr (EPI == EPI_ROUTE) {
+        // The router logits (fp32, as EPI_F32_BIAS) and, for the merge kernel, each token
+        // row's tile statistics: max, sum of exp(L - max) and the 16 largest (logit, expert)
+        // keys in descending order ("Day-Level Adaptation ...", section 3.3: routing scoring
+        // and top-k selection in one kernel).
+        float* out = reinterpret_cast<float*>(P.out0);
+        uint64_t top[kRouteTileK];
+#pragma unroll
+        for (int q2 = 0; q2 < kRouteTileK; ++q2) top[q2] = 0ull;
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(t_row + c, v);
+          tmem_ld_wait();
+          const int col = col0 + c;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            v[i] += (P.bias && col + i < P.N) ? __ldg(&P.bias[col + i]) : 0.f;
+          if (valid && col < P.N) {
+            float* dst = out + row * P.ldo + col;
+            if (col + 16 <= P.N && (P.ldo & 3) == 0) {
+#pragma unroll
+              for (int i = 0; i < 16; i += 4)
+                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (col + i < P.N) dst[i] = v[i];
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              if (col + i < P.N) {
+                mx = fmaxf(mx, v[i]);
+                topk_insert(top, sel_key(v[i], col + i));
+              }
+            }
+          }
+        }
+        float sum = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(t_row + c, v);
+          tmem_ld_wait();
+          const int col = col0 + c;
+          if (valid && col < P.N) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (col + i < P.N)
+                sum += __expf(v[i] + (P.bias ? __ldg(&P.bias[col + i]) : 0.f) - mx);
+          }
+        }
+        if (valid) {
+          uint4* cand = reinterpret_cast<uint4*>(reinterpret_cast<uint64_t*>(P.out1) +
+                                                 (static_cast<size_t>(row) * P.n_tiles + tc.n) *
+                                                     kRouteTileK);
+#pragma unroll
+          for (int q2 = 0; q2 < kRouteTileK; q2 += 2)
+            cand[q2 / 2] = make_uint4(static_cast<uint32_t>(top[q2]),
+                                      static_cast<uint32_t>(top[q2] >> 32),
+                                      static_cast<uint32_t>(top[q2 + 1]),
+                                      static_cast<uint32_t>(top[q2 + 1] >> 32));
+          reinterpret_cast<float2*>(P.out2)[static_cast<size_t>(row) * P.n_tiles + tc.n] =
+              make_float2(mx, sum);
         }
       } else if constexpr (EPI == EPI_SWIGLU) {
         __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(P.out0);

@@ -10,6 +10,13 @@ int launch_gemm_router(const GemmParams& P, int bn, cudaStream_t s) {
   return launch_gemm<128, 2, false, false, EPI_F32_BIAS, 4>(P, s);
 }
 
+// The same product with the fused top-k epilogue (candidates to P.out1, statistics to
+// P.out2).
+int launch_gemm_router_topk(const GemmParams& P, int bn, cudaStream_t s) {
+  if (bn == 224) return launch_gemm<224, 2, false, false, EPI_ROUTE, 3>(P, s);
+  return launch_gemm<128, 2, false, false, EPI_ROUTE, 4>(P, s);
+}
+
 // m256: 256-row tiles (two 128-row subtiles sharing each B stage, one TMEM accumulator) for
 // groups of many rows, where reading each B stage into shared memory once per 256 rows
 // instead of once per 128 keeps the tensor core fed; no gathered A operand.

@@ -116,24 +116,48 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
   }
   __syncthreads();
   // A (strictly lower part beta_i Gam_ij k^_i.k^_j, unit diagonal) and P (Gam_ij q^_i.k^_j,
-  // j <= i)
-  for (int e = tid; e < kC * kC; e += 256) {
-    const int i = e / kC, j = e - i * kC;
-    float a = 0.f, p = 0.f;
-    if (j <= i) {
-      float dkk = 0.f, dqk = 0.f;
-#pragma unroll 8
+  // j <= i).  Thread (ti, tj) computes the 4 x 4 block of rows 4 ti .. and columns 4 tj ..
+  // (blocks above the diagonal are zero), 12 shared loads per 32 multiply-adds.
+  {
+    const int ti = tid >> 4, tj = tid & 15;
+    float ak[4][4], aq[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int c2 = 0; c2 < 4; ++c2) ak[a][c2] = aq[a][c2] = 0.f;
+    if (tj <= ti) {
+#pragma unroll 4
       for (int x = 0; x < DK; ++x) {
-        const float kj = sK[j * LK + x];
-        dkk += sK[i * LK + x] * kj;
-        dqk += sQ[i * LK + x] * kj;
+        float ki[4], qi[4], kj[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          ki[a] = sK[(4 * ti + a) * LK + x];
+          qi[a] = sQ[(4 * ti + a) * LK + x];
+          kj[a] = sK[(4 * tj + a) * LK + x];
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int c2 = 0; c2 < 4; ++c2) {
+            ak[a][c2] += ki[a] * kj[c2];
+            aq[a][c2] += qi[a] * kj[c2];
+          }
       }
-      const float gam = __expf(sG[i] - sG[j]);
-      a = j < i ? sB[i] * gam * dkk : 1.f;
-      p = gam * dqk;
     }
-    sA[i * LC + j] = a;
-    Pm[chunk_id * kC * kC + e] = p;
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int c2 = 0; c2 < 4; ++c2) {
+        const int i = 4 * ti + a, j = 4 * tj + c2;
+        float av = 0.f, pv = 0.f;
+        if (j <= i) {
+          const float gam = __expf(sG[i] - sG[j]);
+          av = j < i ? sB[i] * gam * ak[a][c2] : 1.f;
+          pv = gam * aq[a][c2];
+        }
+        sA[i * LC + j] = av;
+        Pm[chunk_id * kC * kC + i * kC + j] = pv;
+      }
   }
   __syncthreads();
   // A^-1 (unit lower triangular), one row per step: X_i = e_i - sum_{j<i} A_ij X_j, the 64
@@ -150,17 +174,47 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
       __syncthreads();
     }
   }
-  // Y = A^-1 diag(beta gamma) K^, U = A^-1 diag(beta) V; q^, k^ out for the scan
+  // q^, k^ out for the scan; then K^ rows scaled by beta gamma in place
   for (int e = tid; e < kC * DK; e += 256) {
     const int i = e / DK, x = e - i * DK;
-    float y = 0.f;
-    for (int j = 0; j <= i; ++j) y += sI[i * LC + j] * sBG[j] * sK[j * LK + x];
-    Y[chunk_id * kC * DK + e] = y;
     Qh[chunk_id * kC * DK + e] = sQ[i * LK + x];
     Kh[chunk_id * kC * DK + e] = sK[i * LK + x];
   }
   __syncthreads();
-  // V rows (beta-scaled) into the space of the K and Q tiles (no longer needed), then U
+  for (int e = tid; e < kC * DK; e += 256) {
+    const int i = e / DK, x = e - i * DK;
+    sK[i * LK + x] *= sBG[i];
+  }
+  __syncthreads();
+  // Y = A^-1 (diag(beta gamma) K^): thread (ti, tx) computes rows 4 ti .. 4 ti + 3 and
+  // columns tx, tx + 16, ... (A^-1 is zero above the diagonal)
+  {
+    constexpr int TX = DK / 16;
+    const int ti = tid >> 4, tx = tid & 15;
+    float acc[4][TX];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int u = 0; u < TX; ++u) acc[a][u] = 0.f;
+    for (int j = 0; j <= 4 * ti + 3; ++j) {
+      float ai[4], kv[TX];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) ai[a] = sI[(4 * ti + a) * LC + j];
+#pragma unroll
+      for (int u = 0; u < TX; ++u) kv[u] = sK[j * LK + tx + 16 * u];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int u = 0; u < TX; ++u) acc[a][u] += ai[a] * kv[u];
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int u = 0; u < TX; ++u) Y[chunk_id * kC * DK + (4 * ti + a) * DK + tx + 16 * u] = acc[a][u];
+  }
+  __syncthreads();
+  // V rows (beta-scaled) into the space of the K and Q tiles (no longer needed), then
+  // U = A^-1 (diag(beta) V) with the same tiling
   constexpr int LV = Ld<DV>::v;
   static_assert(kC * LV <= 2 * kC * LK, "the V tile fits where the K and Q tiles were");
   float* sV = sK;  // [C][LV]
@@ -170,11 +224,29 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
     sV[i * LV + x] = t < T ? sB[i] * bf(v[((static_cast<size_t>(b) * T + t) * H + h) * DV + x]) : 0.f;
   }
   __syncthreads();
-  for (int e = tid; e < kC * DV; e += 256) {
-    const int i = e / DV, x = e - i * DV;
-    float u = 0.f;
-    for (int j = 0; j <= i; ++j) u += sI[i * LC + j] * sV[j * LV + x];
-    U[chunk_id * kC * DV + e] = u;
+  {
+    constexpr int TX = DV / 16;
+    const int ti = tid >> 4, tx = tid & 15;
+    float acc[4][TX];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int u = 0; u < TX; ++u) acc[a][u] = 0.f;
+    for (int j = 0; j <= 4 * ti + 3; ++j) {
+      float ai[4], vv[TX];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) ai[a] = sI[(4 * ti + a) * LC + j];
+#pragma unroll
+      for (int u = 0; u < TX; ++u) vv[u] = sV[j * LV + tx + 16 * u];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int u = 0; u < TX; ++u) acc[a][u] += ai[a] * vv[u];
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int u = 0; u < TX; ++u) U[chunk_id * kC * DV + (4 * ti + a) * DV + tx + 16 * u] = acc[a][u];
   }
   if (tid < kC) Gc[chunk_id * kC + tid] = sG[tid];
   if (Ai)

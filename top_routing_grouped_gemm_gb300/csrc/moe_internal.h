@@ -49,7 +49,12 @@ enum Epilogue : int {
   EPI_SWIGLU_BWD = 4,  // da_g, da_u from acc0 = dh and saved a_g, a_u
   EPI_STORE = 5,       // out_bf16 = acc0                                   (dx_perm)
   EPI_WGRAD = 6,       // grouped over K: out_f32_i[g] = acc_i, plain or transposed (LoRA grads)
+  EPI_ROUTE = 7,       // EPI_F32_BIAS plus, per row and n-tile, max / sum exp / top-16 keys
 };
+
+// Candidates the fused router epilogue keeps per (token, expert tile): the tile's 16 largest
+// (logit, expert) keys; routing with k <= 16 merges them exactly.
+constexpr int kRouteTileK = 16;
 
 struct GemmSeg {
   int nkb;        // number of 64-wide K blocks in this segment
@@ -117,6 +122,7 @@ int num_sms();
 
 // Kernel launchers (gemm_fwd.cu).  Return cudaError_t as int.
 int launch_gemm_router(const GemmParams& P, int bn, cudaStream_t s);  // BN 128|224
+int launch_gemm_router_topk(const GemmParams& P, int bn, cudaStream_t s);  // + tile top-16
 // BN=128, NB=2, SwiGLU / BN=256, NB=1, gate scale; m256: 256-row tiles (P.pair_off units)
 int launch_gemm_gateup(const GemmParams& P, bool m256, cudaStream_t s);
 int launch_gemm_down(const GemmParams& P, bool m256, cudaStream_t s);

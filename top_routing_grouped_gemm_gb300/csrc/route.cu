@@ -15,6 +15,7 @@
 
 #include "moe_internal.h"
 #include "route.h"
+#include "topk_keys.cuh"
 
 namespace moe {
 
@@ -41,36 +42,6 @@ __global__ void split_router_kernel(const float4* __restrict__ w, uint2* __restr
     hi[i] = *reinterpret_cast<uint2*>(h);
     lo[i] = *reinterpret_cast<uint2*>(l);
   }
-}
-
-// Order-preserving 64-bit key of (logit, expert): larger logit -> larger key, and for equal
-// logits the lower expert index -> larger key.  -0.0 and +0.0 compare equal as floats, so
-// both map to the key of +0.0.
-__device__ __forceinline__ uint64_t sel_key(float v, int e) {
-  uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(0x7FFFFFFF - e);
-}
-
-__device__ __forceinline__ float key_value(uint64_t key) {
-  uint32_t u = static_cast<uint32_t>(key >> 32);
-  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
-  return __uint_as_float(u);
-}
-
-__device__ __forceinline__ int key_expert(uint64_t key) {
-  return 0x7FFFFFFF - static_cast<int>(static_cast<uint32_t>(key));
-}
-
-// Warp maximum of 64-bit keys as two 32-bit warp reductions: the largest high word, then
-// the largest low word among the lanes holding that high word (lexicographic = unsigned
-// 64-bit order).
-__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
-  const uint32_t hi = static_cast<uint32_t>(v >> 32);
-  const uint32_t m_hi = __reduce_max_sync(0xffffffffu, hi);
-  const uint32_t m_lo =
-      __reduce_max_sync(0xffffffffu, hi == m_hi ? static_cast<uint32_t>(v) : 0u);
-  return (static_cast<uint64_t>(m_hi) << 32) | m_lo;
 }
 
 // One warp per token; lane i holds the logits of experts lane, lane+32, ... (VPL of them).
@@ -171,6 +142,76 @@ __global__ void __launch_bounds__(256, VPL > 28 ? 2 : 3) topk_softmax_kernel(
   }
 }
 
+// After the router GEMM's fused top-k epilogue: per token, the global top-k merged from the
+// NT tiles' 16-key candidate lists (every global winner is a winner of its own tile, so the
+// merge is exact), the softmax normaliser from the tiles' (max, sum exp), the renormalised
+// gates, and the per-block probability sums for the auxiliary loss.  One warp per token,
+// 8 tokens per block (the row blocks of prob_partials, as topk_softmax_kernel).
+template <int VPL>
+__global__ void __launch_bounds__(256, VPL > 28 ? 2 : 3) route_merge_kernel(
+    const float* __restrict__ logits, const uint64_t* __restrict__ cand,
+    const float2* __restrict__ stats, int T, int E, int k, int NT,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate,
+    float* __restrict__ partials) {
+  constexpr int WARPS = 8;
+  __shared__ float red[WARPS][VPL * 32];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) red[warp][lane + 32 * i] = 0.f;
+  const int t_begin = blockIdx.x * kRouteTokensPerBlock;
+  const int t_end = min(t_begin + kRouteTokensPerBlock, T);
+  const int ncand = NT * kRouteTileK;
+
+  for (int t = t_begin + warp; t < t_end; t += WARPS) {
+    // this lane's candidates (at most 4 of at most 8 x 16), sorted descending
+    uint64_t hk[4] = {0ull, 0ull, 0ull, 0ull};
+    const uint64_t* ct = cand + static_cast<size_t>(t) * ncand;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int c = lane + 32 * q;
+      if (c < ncand) topk_insert(hk, __ldg(&ct[c]));
+    }
+    // softmax normaliser of the whole row from the tiles' statistics
+    float M = -INFINITY;
+    for (int n = 0; n < NT; ++n) M = fmaxf(M, __ldg(&stats[static_cast<size_t>(t) * NT + n]).x);
+    float S = 0.f;
+    for (int n = 0; n < NT; ++n) {
+      const float2 st = __ldg(&stats[static_cast<size_t>(t) * NT + n]);
+      S += st.y * __expf(st.x - M);
+    }
+    const float inv = 1.0f / S;
+    // k rounds: the warp's largest head wins; its lane pops it
+    uint64_t my_key = 0ull;
+    for (int j = 0; j < k; ++j) {
+      const uint64_t best = warp_max_u64(hk[0]);
+      if (lane == j) my_key = best;
+      if (hk[0] == best) {  // keys are unique: exactly one lane owns the winner
+        hk[0] = hk[1]; hk[1] = hk[2]; hk[2] = hk[3]; hk[3] = 0ull;
+      }
+    }
+    const float pj = (lane < k) ? __expf(key_value(my_key) - M) * inv : 0.f;
+    const float psum = warp_sum(pj);
+    if (lane < k) {
+      topk_idx[static_cast<size_t>(t) * k + lane] = key_expert(my_key);
+      topk_gate[static_cast<size_t>(t) * k + lane] = pj / psum;
+    }
+    const float* row = logits + static_cast<size_t>(t) * E;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) red[warp][e] += __expf(__ldg(&row[e]) - M) * inv;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) sum += red[w][e];
+    partials[static_cast<size_t>(blockIdx.x) * E + e] = sum;
+  }
+}
+
 // aux stage 1: block of 32 experts x 32 row stripes; P_e summed over the partial rows in a
 // fixed order, then f_e P_e summed over the block's experts -> one value per block.
 __global__ void __launch_bounds__(1024) aux_stage1_kernel(const int32_t* __restrict__ counts,
@@ -235,6 +276,29 @@ int launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* idx, 
   else
     MOE_TOPK(32);
 #undef MOE_TOPK
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_route_merge(const float* logits, const uint64_t* cand, const float* stats, int T,
+                       int E, int k, int NT, int32_t* idx, float* gate, float* partials,
+                       cudaStream_t s) {
+  const int grid = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
+  const float2* st = reinterpret_cast<const float2*>(stats);
+#define MOE_MERGE(V) \
+  route_merge_kernel<V><<<grid, 256, 0, s>>>(logits, cand, st, T, E, k, NT, idx, gate, partials)
+  if (E <= 64)
+    MOE_MERGE(2);
+  else if (E <= 128)
+    MOE_MERGE(4);
+  else if (E <= 256)
+    MOE_MERGE(8);
+  else if (E <= 512)
+    MOE_MERGE(16);
+  else if (E <= 896)
+    MOE_MERGE(28);
+  else
+    MOE_MERGE(32);
+#undef MOE_MERGE
   return static_cast<int>(cudaGetLastError());
 }
 

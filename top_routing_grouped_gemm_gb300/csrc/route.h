@@ -24,6 +24,11 @@ int launch_split_router(const float* w, __nv_bfloat16* hi, __nv_bfloat16* lo, si
 int launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* idx, float* gate,
                         float* partials, cudaStream_t s, int n_alt = 0,
                         int32_t* alt_idx = nullptr);
+// After the router GEMM's fused top-k epilogue: cand [T, NT, 16] keys, stats [T, NT] (max,
+// sum exp) -> top-k, gates, probability partials (k <= 16)
+int launch_route_merge(const float* logits, const uint64_t* cand, const float* stats, int T,
+                       int E, int k, int NT, int32_t* idx, float* gate, float* partials,
+                       cudaStream_t s);
 // block_terms: scratch of ceil(E/32) floats
 int launch_aux_loss(const int32_t* counts, const float* partials, int n_partials, int T, int k,
                     int E, float* aux_out, float* block_terms, cudaStream_t s);
