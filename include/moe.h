@@ -117,6 +117,19 @@ int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router,
               float* logits, void* workspace, size_t workspace_bytes, int32_t* dev_status,
               moe_stream_t stream);
 
+/* moe_route with the softmax and top-k folded into the router GEMM: its epilogue keeps, per
+ * token and 224-expert tile, the tile maximum and the 16 largest (logit, expert) keys, and a
+ * light kernel merges the tiles' lists (exact: every selected expert is among its tile's 16
+ * largest), normalises over all E logits and renormalises the gates.  Same arguments, same
+ * workspace and the same outputs as moe_route (identical topk_idx; gates and probability
+ * partials equal up to fp32 summation order); k <= 16, else MOE_ERR_UNSUPPORTED.  On GB300
+ * it measured slower than moe_route's separate top-k kernel (c2 64 vs 57 us, c5 139 vs
+ * 132 us for router GEMM + selection), so moe_route does not use it. */
+int moe_route_fused_topk(const moe_problem* p, const moe_bf16* x, const float* w_router,
+                         const float* bias, int32_t* topk_idx, float* topk_gate,
+                         float* prob_partials, float* logits, void* workspace,
+                         size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream);
+
 /* The selection, softmax and gate steps of moe_route alone, on caller-given fp32 logits
  * [T, E] (same outputs, same rules). */
 int moe_route_from_logits(const moe_problem* p, const float* logits, int32_t* topk_idx,

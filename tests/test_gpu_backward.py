@@ -42,11 +42,14 @@ def small_cfg(**kw):
     small_cfg(T=50, d=128, E=16, k=4, F=64, r=16, alpha=32.0, cap_num=0, cap_den=1),
     small_cfg(T=1, d=128, E=8, k=2, F=64, r=8, alpha=16.0),
     small_cfg(T=300, d=256, E=12, k=3, F=192, r=64, alpha=128.0),
-    # 129..256 rows per expert: backward GEMMs on 256-row tiles
+    # 129..256 rows per expert: the dx GEMM on 256-row tiles
     small_cfg(T=400, d=192, E=4, k=2, F=192),
     small_cfg(T=500, d=320, E=5, k=2, F=256, r=8, alpha=16.0, cap_num=5, cap_den=4),
+    # over 1024 rows per expert: the dh and dx GEMMs on CTA pairs
+    small_cfg(T=2600, d=192, E=4, k=2, F=192),
 ], ids=["small", "ragged_capacity", "many_experts_some_empty", "no_lora", "capacity_zero",
-        "one_token", "lora_r64", "two_tile_groups", "two_tile_groups_ragged_capacity"])
+        "one_token", "lora_r64", "two_tile_groups", "two_tile_groups_ragged_capacity",
+        "big_groups"])
 def test_backward_whole(cfg):
     inp = synth.make_inputs(cfg, "cpu")
     dev = to_dev(inp)

@@ -68,11 +68,11 @@ def small_cfg(**kw):
     small_cfg(T=300, d=256, E=12, k=3, F=192, r=64, alpha=128.0),
     small_cfg(T=300, d=256, E=12, k=3, F=192, r=8, alpha=16.0, cap_num=1, cap_den=2),
     small_cfg(T=40, d=192, E=500, k=8, F=128, zipf_bias=True),
-    # groups of over 1024 rows on average: the expert GEMMs run on 256-row tiles
+    # groups of over 1024 rows on average: the expert GEMMs run on CTA pairs
     small_cfg(T=2600, d=192, E=4, k=2, F=192),
     small_cfg(T=2200, d=256, E=2, k=1, F=320, r=16, alpha=32.0),
     small_cfg(T=3000, d=128, E=4, k=2, F=128, cap_num=3, cap_den=4, zipf_bias=True),
-    # 129..256 rows per expert: the down GEMM on 256-row tiles
+    # 129..256 rows per expert: the gate/up GEMM on CTA pairs
     small_cfg(T=400, d=192, E=4, k=2, F=192),
     small_cfg(T=500, d=320, E=5, k=2, F=256, r=16, alpha=32.0, cap_num=5, cap_den=4),
 ], ids=["c1", "small", "small_capacity_bias", "small_lora", "ragged_lora_capacity", "single_expert",

@@ -1,6 +1,6 @@
 """The unpermute fused into the down GEMM's epilogue (moe_expert_ffn_combine): y must be
 bit for bit the separate combine's, on whole problems with drops, all-dropped tokens, LoRA,
-ragged widths, 256-row tiles, the fused permute, and c2 at full size."""
+ragged widths, CTA-pair tiles, the fused permute, and c2 at full size."""
 
 import pytest
 import torch
@@ -34,7 +34,7 @@ CASES = [
     small(T=777, d=320, E=9, k=3, F=448, r=24, alpha=48.0, cap_num=1, cap_den=1),
     small(T=50, d=64, E=16, k=4, F=64, cap_num=0, cap_den=1),      # every slot dropped
     small(T=200, d=128, E=1024, k=32, F=64),
-    small(T=2600, d=192, E=4, k=2, F=192),                          # 256-row tiles
+    small(T=2600, d=192, E=4, k=2, F=192),                          # CTA-pair tiles
     small(T=400, d=192, E=4, k=2, F=192),                           # two-tile groups
 ]
 

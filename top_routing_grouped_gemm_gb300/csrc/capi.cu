@@ -98,13 +98,30 @@ bool big_groups(const moe_problem* p, int rows_max) {
   return static_cast<long long>(rows_max) >= 1024ll * p->E && (C < 0 || C >= 1024);
 }
 
-// Groups average 129..256 rows (two m-tiles, the second partly empty): the backward dx GEMM
-// stages each weight tile once for both m-tiles on 256-row tiles instead of once per m-tile
-// (measured at c5: dx 3309 -> 2955 us; dh and down got slower, their epilogues exposed).
+// Groups average 129..256 rows (two m-tiles, the second partly empty): staging each weight
+// tile once for both m-tiles pays.
 bool two_tile_groups(const moe_problem* p, int rows_max) {
   const int C = capacity_of(p);
   const long long per = rows_max / p->E;
   return per > kBM && per <= 2 * kBM && (C < 0 || C > kBM);
+}
+
+// Tile shapes of the grouped expert GEMMs.  CTA pairs stage half of every weight tile per SM
+// and keep two accumulators per CTA (the epilogue of one tile overlaps the next tile's main
+// loop).  Measured on GB300: groups of over 1024 rows (c4 shard: 4.3 -> 3.9 ms) take pairs
+// everywhere; at 129..256 rows (c5) pairs pay for the gate/up GEMM (3253 -> 2907 us) but not
+// for down (1767 vs 1775 us) or the backward dh (1710 vs 1804 us) and dx GEMMs (256-row
+// tiles in one CTA 2972 vs 3173 us).  A gathered A operand takes 128-row tiles.
+enum ExpertGemm { kGemmGateUp, kGemmDown, kGemmDh, kGemmDx };
+
+int expert_tile_shape(const moe_problem* p, int rows_max, bool gather, ExpertGemm g) {
+  if (gather) return kTile128;
+  if (big_groups(p, rows_max)) return kTilePair;
+  if (two_tile_groups(p, rows_max)) {
+    if (g == kGemmGateUp) return kTilePair;
+    if (g == kGemmDx) return kTile256;
+  }
+  return kTile128;
 }
 
 struct Carver {
@@ -126,7 +143,7 @@ size_t route_ws(const moe_problem* p) {
   const size_t nt = (p->E + router_bn(p) - 1) / router_bn(p);
   return up256(2ull * p->E * p->d * 2) + up256(static_cast<size_t>(p->T) * p->E * 4) +
          up256(static_cast<size_t>(p->T) * nt * kRouteTileK * 8) +
-         up256(static_cast<size_t>(p->T) * nt * 8);
+         up256(static_cast<size_t>(p->T) * nt * 4);
 }
 
 size_t ffn_ws(const moe_problem* p, int rows_max) {
@@ -184,11 +201,14 @@ int moe_route_from_logits(const moe_problem* p, const float* logits, int32_t* to
   return MOE_OK;
 }
 
-int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, const float* bias,
-              int32_t* topk_idx, float* topk_gate, float* prob_partials, float* logits,
-              void* workspace, size_t workspace_bytes, int32_t* dev_status,
-              moe_stream_t stream) {
+namespace {
+
+int route_impl(const moe_problem* p, const moe_bf16* x, const float* w_router, const float* bias,
+               int32_t* topk_idx, float* topk_gate, float* prob_partials, float* logits,
+               void* workspace, size_t workspace_bytes, int32_t* dev_status,
+               moe_stream_t stream, bool fused) {
   MOE_TRY(check_problem(p));
+  if (fused && p->k > kRouteTileK) return MOE_ERR_UNSUPPORTED;
   if (!x || !w_router || !topk_idx || !topk_gate || !prob_partials) return MOE_ERR_INVALID_ARG;
   if (!al16(x) || !al16(w_router) || (logits && !al16(logits))) return MOE_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < route_ws(p)) return MOE_ERR_WORKSPACE;
@@ -200,9 +220,7 @@ int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, co
   const int bn = router_bn(p);
   const int nt = (E + bn - 1) / bn;
   uint64_t* cand = cv.take<uint64_t>(static_cast<size_t>(T) * nt * kRouteTileK);
-  float* stats = cv.take<float>(static_cast<size_t>(T) * nt * 2);
-  // top-k fused into the router GEMM's epilogue when the per-tile candidates suffice
-  const bool fused = p->k <= kRouteTileK;
+  float* tile_max = cv.take<float>(static_cast<size_t>(T) * nt);
 
   MOE_CUDA(launch_split_router(w_router, w_split, w_split + static_cast<size_t>(E) * d,
                                static_cast<size_t>(E) * d, stream));
@@ -224,14 +242,14 @@ int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, co
   P.dev_status = dev_status;
   if (fused) {
     P.out1 = cand;
-    P.out2 = stats;
+    P.out2 = tile_max;
   }
   mark_before(MOE_KERNEL_ROUTER_GEMM, stream);
   MOE_CUDA(fused ? launch_gemm_router_topk(P, bn, stream) : launch_gemm_router(P, bn, stream));
   mark_after(MOE_KERNEL_ROUTER_GEMM, stream);
   mark_before(MOE_KERNEL_TOPK, stream);
   if (fused) {
-    MOE_CUDA(launch_route_merge(L, cand, stats, T, E, p->k, nt, topk_idx, topk_gate,
+    MOE_CUDA(launch_route_merge(L, cand, tile_max, T, E, p->k, nt, topk_idx, topk_gate,
                                 prob_partials, stream));
   } else {
     MOE_CUDA(launch_topk_softmax(L, T, E, p->k, topk_idx, topk_gate, prob_partials, stream));
@@ -239,6 +257,24 @@ int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, co
   mark_after(MOE_KERNEL_TOPK, stream);
   count_launches(3);
   return MOE_OK;
+}
+
+}  // namespace
+
+int moe_route(const moe_problem* p, const moe_bf16* x, const float* w_router, const float* bias,
+              int32_t* topk_idx, float* topk_gate, float* prob_partials, float* logits,
+              void* workspace, size_t workspace_bytes, int32_t* dev_status,
+              moe_stream_t stream) {
+  return route_impl(p, x, w_router, bias, topk_idx, topk_gate, prob_partials, logits, workspace,
+                    workspace_bytes, dev_status, stream, false);
+}
+
+int moe_route_fused_topk(const moe_problem* p, const moe_bf16* x, const float* w_router,
+                         const float* bias, int32_t* topk_idx, float* topk_gate,
+                         float* prob_partials, float* logits, void* workspace,
+                         size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
+  return route_impl(p, x, w_router, bias, topk_idx, topk_gate, prob_partials, logits, workspace,
+                    workspace_bytes, dev_status, stream, true);
 }
 
 // ------------------------------------------------------------------------ dispatch
@@ -425,7 +461,8 @@ int expert_ffn_impl(const moe_problem* p, int32_t rows_max, const moe_bf16* a_sr
   int32_t* tile_off = cv.take<int32_t>(E + 1);
   int32_t* pair_off = cv.take<int32_t>(E + 1);
   const int b_policy = weights_reused(p, rows_max) ? 1 : 0;
-  const bool m256 = !gather && big_groups(p, rows_max);
+  const int shape_gu = expert_tile_shape(p, rows_max, gather, kGemmGateUp);
+  const int shape_dn = expert_tile_shape(p, rows_max, gather, kGemmDown);
   moe_bf16 *u_g = nullptr, *u_u = nullptr, *u_d = nullptr;
   if (r) {
     u_g = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * r);
@@ -508,7 +545,7 @@ int expert_ffn_impl(const moe_problem* p, int32_t rows_max, const moe_bf16* a_sr
     P.out2 = saved ? saved->a_up : nullptr;
     P.ldo = F;
     mark_before(MOE_KERNEL_GATEUP_GEMM, stream);
-    MOE_CUDA(launch_gemm_gateup(P, m256, stream));
+    MOE_CUDA(launch_gemm_gateup(P, shape_gu, stream));
     mark_after(MOE_KERNEL_GATEUP_GEMM, stream);
   }
   // LoRA down-projection of h: u_d = s h A_d^T
@@ -531,13 +568,15 @@ int expert_ffn_impl(const moe_problem* p, int32_t rows_max, const moe_bf16* a_sr
   {
     GemmParams P = gemm_params();
     MOE_TRY(encode_map_kmajor(&P.maps[0], h, F, rows_max, 1, kBM));
-    MOE_TRY(encode_map_kmajor(&P.maps[1], w_down, F, d, E, 256));
+    // CTA pairs: each CTA stages 128 of the tile's 256 weight rows
+    const int box_n = shape_dn == kTilePair ? 128 : 256;
+    MOE_TRY(encode_map_kmajor(&P.maps[1], w_down, F, d, E, box_n));
     P.nmaps = 2;
     P.seg[0] = GemmSeg{F / kBK, 0, 0, {1, -1}, {0, 0}, {0, 0}};
     P.nseg = 1;
     if (use_lora) {
       MOE_TRY(encode_map_kmajor(&P.maps[2], u_d, r, rows_max, 1, kBM));
-      MOE_TRY(encode_map_kmajor(&P.maps[3], lora->B_d, r, d, E, 256));
+      MOE_TRY(encode_map_kmajor(&P.maps[3], lora->B_d, r, d, E, box_n));
       P.nmaps = 4;
       P.seg[1] = GemmSeg{(r + kBK - 1) / kBK, 2, 0, {3, -1}, {0, 0}, {0, 0}};
       P.nseg = 2;
@@ -560,7 +599,7 @@ int expert_ffn_impl(const moe_problem* p, int32_t rows_max, const moe_bf16* a_sr
       P.comb_k = p->k;
     }
     mark_before(MOE_KERNEL_DOWN_GEMM, stream);
-    MOE_CUDA(launch_gemm_down(P, m256, stream));
+    MOE_CUDA(launch_gemm_down(P, shape_dn, stream));
     mark_after(MOE_KERNEL_DOWN_GEMM, stream);
   }
   count_launches((use_lora ? 5 : 3) + (fuse_combine ? 1 : 0));
@@ -713,8 +752,8 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
   int launches = 1;
   // 256-row tiles: dh only for big groups (its SwiGLU-backward epilogue is heavy and stays
   // exposed with one accumulator); dx (plain store epilogue) also for two-tile groups
-  const bool m256_dh = big_groups(p, rows_max);
-  const bool m256_dx = m256_dh || two_tile_groups(p, rows_max);
+  const int shape_dh = expert_tile_shape(p, rows_max, false, kGemmDh);
+  const int shape_dx = expert_tile_shape(p, rows_max, false, kGemmDx);
   auto grouped = [&](GemmParams& P) {
     P.group_off = offsets;
     P.tile_off = tile_off;
@@ -769,7 +808,7 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
     P.out1 = da_u;
     ++launches;
     mark_before(MOE_KERNEL_BWD_DH_GEMM, stream);
-    MOE_CUDA(launch_gemm_bwd_dh(P, m256_dh, stream));
+    MOE_CUDA(launch_gemm_bwd_dh(P, shape_dh, stream));
     mark_after(MOE_KERNEL_BWD_DH_GEMM, stream);
   }
   // v'_g = s da_g B_g, v'_u = s da_u B_u
@@ -805,7 +844,7 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
     P.out0 = dx_perm;
     ++launches;
     mark_before(MOE_KERNEL_BWD_DX_GEMM, stream);
-    MOE_CUDA(launch_gemm_bwd_dx(P, m256_dx, stream));
+    MOE_CUDA(launch_gemm_bwd_dx(P, shape_dx, stream));
     mark_after(MOE_KERNEL_BWD_DX_GEMM, stream);
   }
   // LoRA weight gradients: per expert, reductions over its rows (grouped over K)

@@ -30,12 +30,21 @@ namespace moe {
 // B stage).  CTAS: CTAs resident per SM.  NACC: TMEM accumulator buffers per CTA (2 overlaps
 // a tile's epilogue with the next tile's main loop; 1 when two buffers of every resident CTA
 // do not fit the 512 TMEM columns, in which case a second CTA on the SM does the covering).
-template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int MSUB = 1, int CTAS = 1>
+// CG: CTAs per MMA (2: a CTA pair issues M = 256 tcgen05.mma.cta_group::2 tiles, each CTA
+// staging its own 128 A rows and half of every B tile).
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int MSUB = 1, int CTAS = 1,
+          int CG = 1>
 struct GemmCfg {
   static constexpr int A_SUB_BYTES = kBM * kBK * 2;
   static constexpr int A_BYTES = MSUB * A_SUB_BYTES;
+  // B rows (K-major) or MN columns (MN-major) of one B operand staged by this CTA
+  static constexpr int B_ROWS = CG == 2 ? BN / 2 : BN;
   // an MN-major B tile is always whole 64-wide TMA boxes (N below 64 is zero-filled)
-  static constexpr int B_BYTES = (B_MN ? ((BN + 63) / 64) * 64 : BN) * kBK * 2;
+  static constexpr int B_BYTES = (B_MN ? ((B_ROWS + 63) / 64) * 64 : B_ROWS) * kBK * 2;
+  // CTA pairs with two K-major B operands (gate and up) run one MMA of N = 2*BN per k step:
+  // its B rows 0..BN-1 (the first operand's tile) sit in the first CTA and BN..2BN-1 (the
+  // second's) in the second, so each CTA stages one whole operand tile
+  static constexpr bool PAIR_JOIN = CG == 2 && NB == 2 && !B_MN && 2 * BN <= 256;
   static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
   // The router (EPI_F32_BIAS) with two B operands sums them into one accumulator: they are
   // the bf16 hi and lo parts of the same fp32 weights, both multiplied by the same A stage.
@@ -58,6 +67,10 @@ struct GemmCfg {
   static_assert(NACC * ACC_COLS <= 512, "accumulators must fit in TMEM");
   static_assert(!B_MN || BN % 64 == 0, "MN-major B is read in whole 64-wide boxes");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+  static_assert(CG == 1 || (MSUB == 1 && CTAS == 1 && !A_MN && EPI != EPI_WGRAD && !SUMB),
+                "CTA pairs: M-grouped K-major A, one CTA per SM");
+  static_assert(CG == 1 || (B_MN ? BN % 128 == 0 : (BN / 2) % 8 == 0),
+                "half B tiles stay whole boxes / swizzle atoms");
 };
 
 struct TileCoord {
@@ -152,10 +165,11 @@ __device__ __forceinline__ bool decode_sub_tile(const GemmParams& P, int pt, Til
   return true;
 }
 
-// Zero the K rows [valid, 64) of an MN-major operand tile of `chunks` 64-wide boxes (each K
+// Zero the K rows [valid, end) of an MN-major operand tile of `chunks` 64-wide boxes (each K
 // row is one 128-byte line of a box), by the 32 lanes of one warp.
-__device__ __forceinline__ void zero_k_tail(uint8_t* tile, int chunks, int valid, int lane) {
-  const int items = (kBK - valid) * 8;  // 16-byte parts of the lines to clear, per box
+__device__ __forceinline__ void zero_k_tail(uint8_t* tile, int chunks, int valid, int end,
+                                            int lane) {
+  const int items = (end - valid) * 8;  // 16-byte parts of the lines to clear, per box
   for (int c = 0; c < chunks; ++c) {
     uint8_t* box = tile + c * 8192;
     for (int i = lane; i < items; i += 32) {
@@ -298,8 +312,11 @@ __device__ __forceinline__ void combine_finish(const GemmParams& P, int n, long 
   }
 }
 
-template <int EPI, int MSUB>
-__device__ __forceinline__ bool next_tile(const GemmParams& P, int tile, TileCoord& tc,
+// CTA pairs (CG = 2) walk the two-subtile units: CTA `rank` of the pair takes the unit's
+// rows rank*128 .. rank*128+127 (none of them valid when the group ends in the first half:
+// that CTA still stages A rows and takes part in every barrier, and stores nothing).
+template <int EPI, int MSUB, int CG>
+__device__ __forceinline__ bool next_tile(const GemmParams& P, int tile, int rank, TileCoord& tc,
                                           KRange& kr) {
   if constexpr (EPI == EPI_WGRAD) {
     return decode_tile_wgrad(P, tile, tc, kr);
@@ -307,15 +324,22 @@ __device__ __forceinline__ bool next_tile(const GemmParams& P, int tile, TileCoo
     kr.k0 = 0;
     kr.nrows = 0;
     kr.nkb = 0;
+    if constexpr (CG == 2) {
+      if (!decode_sub_tile(P, tile, tc)) return false;
+      tc.m += rank;
+      tc.row0 += rank * kBM;
+      tc.rows_valid = max(0, min(kBM, tc.rows_valid - rank * kBM));
+      return true;
+    }
     if constexpr (MSUB == 2) return decode_sub_tile(P, tile, tc);
     return decode_tile(P, tile, tc);
   }
 }
 
 // CTAS CTAs per SM: with one, a thread may use up to 255 registers; with two, 128.
-template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int MSUB, int CTAS>
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int MSUB, int CTAS, int CG>
 __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__ GemmParams P) {
-  using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB, CTAS>;
+  using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB, CTAS, CG>;
   static_assert(MSUB == 1 || (EPI != EPI_WGRAD && !A_MN),
                 "two subtiles: M-grouped or dense, K-major A");
   extern __shared__ uint8_t smem_raw[];
@@ -332,21 +356,25 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int unit0 = blockIdx.x;      // first work unit of this CTA
-  const int unit_step = gridDim.x;   // number of CTAs
+  // CTA pairs: clusters of two consecutive CTAs; rank 0 issues the pair's MMAs
+  const int rank = (CG == 2) ? static_cast<int>(cluster_ctarank()) : 0;
+  const int unit0 = blockIdx.x / CG;     // first work unit of this CTA (pair)
+  const int unit_step = gridDim.x / CG;  // number of CTAs (pairs)
 
   if (threadIdx.x == 0) {
     // with a gathered A operand a stage is full after the producer's expect-tx arrival
     // (B bytes) and one arrival of the gather warp that filled its A tile
     const uint32_t full_count =
-        (!A_MN && EPI != EPI_WGRAD && MSUB == 1 && P.gather_slot != nullptr) ? 2u : 1u;
+        (!A_MN && EPI != EPI_WGRAD && MSUB == 1 && CG == 1 && P.gather_slot != nullptr) ? 2u
+                                                                                      : 1u;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], full_count);
       mbar_init(&empty[s], 1);  // a stage is free once the MMA warp has released it
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 128);
+      // every epilogue thread (one CTA), or lane 0 of each epilogue warp of both CTAs
+      mbar_init(&acc_empty[a], CG == 2 ? 8 : 128);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -358,11 +386,15 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
     for (int i = 0; i < P.nmaps; ++i) tma_prefetch_desc(&P.maps[i]);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc<CG>(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2) {
+    cluster_sync();  // both CTAs' barriers exist before either signals the other's
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -375,18 +407,70 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
     bool ok = true;
     TileCoord tc;
     KRange kr;
-    for (int tile = unit0; ok && next_tile<EPI, MSUB>(P, tile, tc, kr); tile += unit_step) {
+    for (int tile = unit0; ok && next_tile<EPI, MSUB, CG>(P, tile, rank, tc, kr); tile += unit_step) {
       const int nseg = (EPI == EPI_WGRAD) ? 1 : P.nseg;
       for (int s = 0; ok && s < nseg; ++s) {
         const GemmSeg& sg = P.seg[s];
         const int nkb = (EPI == EPI_WGRAD) ? kr.nkb : sg.nkb;
         for (int kb = 0; kb < nkb; ++kb) {
           int w = 1;
-          if (lane == 0) w = mbar_wait(&empty[stage], phase ^ 1, abort_flag) ? 1 : 0;
+          if (lane == 0) {
+            // with CTA pairs the stage is released by the first CTA's tensor-core commit
+            w = ((CG == 2) ? mbar_wait_cluster(&empty[stage], phase ^ 1, abort_flag)
+                           : mbar_wait(&empty[stage], phase ^ 1, abort_flag))
+                    ? 1
+                    : 0;
+          }
           w = __shfl_sync(0xffffffffu, w, 0);
           if (!w) { ok = false; break; }
           uint8_t* sA = smem + stage * C::STAGE_BYTES;
           const int ka = (EPI == EPI_WGRAD) ? kr.k0 + kb * kBK : sg.a_k0 + kb * kBK;
+          if constexpr (CG == 2) {
+            // Both CTAs' copies complete on the first CTA's stage barrier, which expects the
+            // bytes of both (every box is delivered whole: rows past the tensor are zeros).
+            if (lane == 0) {
+              const uint32_t fb = cluster_addr(&full[stage], 0);
+              uint32_t bytes = C::A_SUB_BYTES;
+              if (C::PAIR_JOIN) {
+                bytes += NB * C::B_BYTES;
+              } else {
+#pragma unroll
+                for (int b = 0; b < NB; ++b) bytes += (sg.b_map[b] >= 0) ? C::B_BYTES : 0;
+              }
+              if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * bytes);
+              tma_load_3d_pair(sA, &P.maps[sg.a_map], fb, ka, tc.row0, 0, pol_a);
+              if constexpr (C::PAIR_JOIN) {
+                // this CTA stages operand `rank`; in a segment without it (the LoRA block of
+                // the other projection) it stages zeros instead: a box wholly before row 0,
+                // which TMA fills with zeros, so the MMA adds nothing to that half
+                const bool has = sg.b_map[rank] >= 0;
+                const int b = has ? rank : 1 - rank;
+                const int z = (P.group_off != nullptr) ? tc.g : sg.b_z[b];
+                tma_load_3d_pair(sA + C::A_BYTES, &P.maps[sg.b_map[b]], fb,
+                                 sg.b_k0[b] + kb * kBK, has ? tc.n * BN : -BN, z, pol_b);
+              } else {
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                  if (sg.b_map[b] < 0) continue;
+                  uint8_t* sB = sA + C::A_BYTES + b * C::B_BYTES;
+                  const int kbk = sg.b_k0[b] + kb * kBK;
+                  const int z = (P.group_off != nullptr) ? tc.g : sg.b_z[b];
+                  const int n0 = tc.n * BN + rank * (BN / 2);  // this CTA's half of B
+                  if (!B_MN) {
+                    tma_load_3d_pair(sB, &P.maps[sg.b_map[b]], fb, kbk, n0, z, pol_b);
+                  } else {
+#pragma unroll
+                    for (int c = 0; c < C::B_ROWS / 64; ++c)
+                      tma_load_3d_pair(sB + c * 8192, &P.maps[sg.b_map[b]], fb, n0 + c * 64,
+                                       kbk, z, pol_b);
+                  }
+                }
+              }
+            }
+            __syncwarp();
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            continue;
+          }
           if (lane == 0) {
             const int nsub = (MSUB == 2 && tc.rows_valid > kBM) ? 2 : 1;
             uint32_t bytes = sg.a_gather ? 0u : nsub * C::A_SUB_BYTES;
@@ -432,8 +516,9 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
       *abort_flag = 1;
       report_status(P.dev_status, MOE_ERR_TIMEOUT);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && (CG == 1 || rank == 0)) {
     // ------------------------------------------------------------ MMA issuer
+    // (with CTA pairs only the first CTA issues: each M = 256 MMA covers both CTAs' rows)
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, A_MN, B_MN);
     // Two B operands sit back to back in the stage (K-major: the second's rows follow the
     // first's BN rows; MN-major: its 64-wide boxes follow the first's, 8 KB apart), so when
@@ -448,9 +533,14 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
     bool ok = true;
     TileCoord tc;
     KRange kr;
-    for (int tile = unit0; ok && next_tile<EPI, MSUB>(P, tile, tc, kr); tile += unit_step) {
+    for (int tile = unit0; ok && next_tile<EPI, MSUB, CG>(P, tile, rank, tc, kr); tile += unit_step) {
       int w = 1;
-      if (lane == 0) w = mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag) ? 1 : 0;
+      if (lane == 0) {
+        w = ((CG == 2) ? mbar_wait_cluster(&acc_empty[acc], acc_phase ^ 1, abort_flag)
+                       : mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag))
+                ? 1
+                : 0;
+      }
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) { ok = false; break; }
       tc_fence_after();
@@ -460,30 +550,65 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
         const GemmSeg& sg = P.seg[s];
         const int nkb = (EPI == EPI_WGRAD) ? kr.nkb : sg.nkb;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (lane == 0) w = mbar_wait(&full[stage], phase, abort_flag) ? 1 : 0;
+          if (lane == 0) {
+            w = ((CG == 2) ? mbar_wait_cluster(&full[stage], phase, abort_flag)
+                           : mbar_wait(&full[stage], phase, abort_flag))
+                    ? 1
+                    : 0;
+          }
           w = __shfl_sync(0xffffffffu, w, 0);
           if (!w) { ok = false; break; }
           tc_fence_after();
+          int ksteps = kBK / 16;  // 16-deep MMA steps of this k block
           if constexpr (EPI == EPI_WGRAD) {
             // rows past the group's end (the next group's rows, or memory never written)
-            // must contribute nothing: zero them in both operands before the MMAs
+            // must contribute nothing: the k block's MMA steps stop at the first 16-row step
+            // boundary past them, and the rows in between are zeroed in both operands
             const int valid = min(kBK, kr.nrows - kb * kBK);
-            if (valid < kBK) {
+            ksteps = (valid + 15) / 16;
+            const int end = 16 * ksteps;
+            if (valid < end) {
               uint8_t* sA = smem + stage * C::STAGE_BYTES;
-              zero_k_tail(sA, 2, valid, lane);
+              zero_k_tail(sA, 2, valid, end, lane);
 #pragma unroll
               for (int b = 0; b < NB; ++b)
                 if (sg.b_map[b] >= 0)
-                  zero_k_tail(sA + C::A_BYTES + b * C::B_BYTES, (BN + 63) / 64, valid, lane);
+                  zero_k_tail(sA + C::A_BYTES + b * C::B_BYTES, (BN + 63) / 64, valid, end, lane);
               fence_proxy_async_smem();
               __syncwarp();
             }
           }
-          if (lane == 0) {
+          if constexpr (CG == 2) {
+            if (lane == 0) {
+              // M = 256 over the pair: A rows and B halves at the same offsets in both CTAs
+              constexpr uint32_t idp = idesc_bf16_f32(2 * kBM, C::PAIR_JOIN ? 2 * BN : BN, false, B_MN);
+              const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k) {
+                const uint32_t accumulate = (s > 0 || kb > 0 || k > 0) ? 1u : 0u;
+                const uint64_t adesc = smem_desc_sw128(a_addr + k * 32, 16, 1024);
+                if constexpr (C::PAIR_JOIN) {
+                  const uint64_t bdesc = smem_desc_sw128(a_addr + C::A_BYTES + k * 32, 16, 1024);
+                  umma_bf16<2>(d_base, adesc, bdesc, idp, accumulate);
+                } else {
+#pragma unroll
+                  for (int b = 0; b < NB; ++b) {
+                    if (sg.b_map[b] < 0) continue;
+                    const uint32_t b_addr = a_addr + C::A_BYTES + b * C::B_BYTES;
+                    const uint64_t bdesc = B_MN ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                                : smem_desc_sw128(b_addr + k * 32, 16, 1024);
+                    umma_bf16<2>(d_base + b * BN, adesc, bdesc, idp, accumulate);
+                  }
+                }
+              }
+              umma_commit<2>(&empty[stage]);
+            }
+          } else if (lane == 0) {
             const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
             const int nsub = (MSUB == 2 && tc.rows_valid > kBM) ? 2 : 1;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
+              if (k >= ksteps) break;
               const uint32_t accumulate = (s > 0 || kb > 0 || k > 0) ? 1u : 0u;
 #pragma unroll
               for (int sub = 0; sub < MSUB; ++sub) {
@@ -521,7 +646,7 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
         }
       }
       if (!ok) break;
-      if (lane == 0) umma_commit(&acc_full[acc]);
+      if (lane == 0) umma_commit<CG>(&acc_full[acc]);
       __syncwarp();
       if (++acc == C::NACC) { acc = 0; acc_phase ^= 1; }
     }
@@ -535,7 +660,7 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
     // 128 x 64 A tile of its stage with 16-byte cp.async copies of token rows (zero fill for
     // rows past the group's end) in the 128-byte-swizzled layout TMA would produce, waits for
     // them, makes them visible to the tensor core (proxy fence) and arrives on the stage.
-    if constexpr (!A_MN && EPI != EPI_WGRAD && MSUB == 1) {
+    if constexpr (!A_MN && EPI != EPI_WGRAD && MSUB == 1 && CG == 1) {
       if (P.gather_slot != nullptr) {
         const int gw = warp - 2;
         const int part = lane & 7;      // 16-byte chunk of a 128-byte row this lane copies
@@ -547,7 +672,7 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
         bool ok = true;
         TileCoord tc;
         KRange kr;
-        for (int tile = unit0; ok && next_tile<EPI, MSUB>(P, tile, tc, kr); tile += unit_step) {
+        for (int tile = unit0; ok && next_tile<EPI, MSUB, CG>(P, tile, rank, tc, kr); tile += unit_step) {
           int trow[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -606,9 +731,14 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
     bool ok = true;
     TileCoord tc;
     KRange kr;
-    for (int tile = unit0; next_tile<EPI, MSUB>(P, tile, tc, kr); tile += unit_step) {
+    for (int tile = unit0; next_tile<EPI, MSUB, CG>(P, tile, rank, tc, kr); tile += unit_step) {
       int w = 1;
-      if (lane == 0) w = mbar_wait(&acc_full[acc], acc_phase, abort_flag) ? 1 : 0;
+      if (lane == 0) {
+        w = ((CG == 2) ? mbar_wait_cluster(&acc_full[acc], acc_phase, abort_flag)
+                       : mbar_wait(&acc_full[acc], acc_phase, abort_flag))
+                ? 1
+                : 0;
+      }
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) { ok = false; break; }
       tc_fence_after();
@@ -653,23 +783,28 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
         }
       } else if constexpr (EPI == EPI_ROUTE) {
         // The router logits (fp32, as EPI_F32_BIAS) and, for the merge kernel, each token
-        // row's tile statistics: max, sum of exp(L - max) and the 16 largest (logit, expert)
-        // keys in descending order ("Day-Level Adaptation ...", section 3.3: routing scoring
-        // and top-k selection in one kernel).
+        // row's tile maximum and the keys of its 16 largest (logit, expert) pairs
+        // ("Day-Level Adaptation ...", section 3.3: routing scoring and top-k selection in
+        // one kernel).  Pass 1 keeps the 16 largest VALUES with sorting networks (each
+        // 16-column chunk sorted, then merged into the running list: independent min/max
+        // pairs, no data-dependent branches); pass 2 re-reads the accumulator and emits the
+        // keys of the values above the 16th largest plus, of the values equal to it, the
+        // lowest-indexed ones (the tie rule).
         float* out = reinterpret_cast<float*>(P.out0);
-        uint64_t top[kRouteTileK];
+        float best[kRouteTileK];
 #pragma unroll
-        for (int q2 = 0; q2 < kRouteTileK; ++q2) top[q2] = 0ull;
-        float mx = -INFINITY;
+        for (int q2 = 0; q2 < kRouteTileK; ++q2) best[q2] = -INFINITY;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
           float v[16];
           tmem_ld16(t_row + c, v);
           tmem_ld_wait();
           const int col = col0 + c;
+          if (P.bias) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            v[i] += (P.bias && col + i < P.N) ? __ldg(&P.bias[col + i]) : 0.f;
+            for (int i = 0; i < 16; ++i)
+              if (col + i < P.N) v[i] += __ldg(&P.bias[col + i]);
+          }
           if (valid && col < P.N) {
             float* dst = out + row * P.ldo + col;
             if (col + 16 <= P.N && (P.ldo & 3) == 0) {
@@ -682,15 +817,20 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
                 if (col + i < P.N) dst[i] = v[i];
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              if (col + i < P.N) {
-                mx = fmaxf(mx, v[i]);
-                topk_insert(top, sel_key(v[i], col + i));
-              }
-            }
+            for (int i = 0; i < 16; ++i)
+              if (col + i >= P.N) v[i] = -INFINITY;
+            sort16_desc(v);
+            merge16_desc(best, v);
           }
         }
-        float sum = 0.f;
+        const float mx = best[0];
+        const float tau = best[kRouteTileK - 1];
+        int need_eq = 0;  // values equal to tau that belong to the tile's 16
+#pragma unroll
+        for (int q2 = 0; q2 < kRouteTileK; ++q2) need_eq += (best[q2] == tau) ? 1 : 0;
+        uint64_t* cand = reinterpret_cast<uint64_t*>(P.out1) +
+                         (static_cast<size_t>(row) * P.n_tiles + tc.n) * kRouteTileK;
+        int pos = 0;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
           float v[16];
@@ -699,23 +839,21 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
           const int col = col0 + c;
           if (valid && col < P.N) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (col + i < P.N)
-                sum += __expf(v[i] + (P.bias ? __ldg(&P.bias[col + i]) : 0.f) - mx);
+            for (int i = 0; i < 16; ++i) {
+              if (col + i < P.N) {
+                const float x = v[i] + (P.bias ? __ldg(&P.bias[col + i]) : 0.f);
+                const bool eq = (x == tau) && need_eq > 0;
+                if ((x > tau || eq) && pos < kRouteTileK) {
+                  cand[pos++] = sel_key(x, col + i);
+                  need_eq -= eq ? 1 : 0;
+                }
+              }
+            }
           }
         }
         if (valid) {
-          uint4* cand = reinterpret_cast<uint4*>(reinterpret_cast<uint64_t*>(P.out1) +
-                                                 (static_cast<size_t>(row) * P.n_tiles + tc.n) *
-                                                     kRouteTileK);
-#pragma unroll
-          for (int q2 = 0; q2 < kRouteTileK; q2 += 2)
-            cand[q2 / 2] = make_uint4(static_cast<uint32_t>(top[q2]),
-                                      static_cast<uint32_t>(top[q2] >> 32),
-                                      static_cast<uint32_t>(top[q2 + 1]),
-                                      static_cast<uint32_t>(top[q2 + 1] >> 32));
-          reinterpret_cast<float2*>(P.out2)[static_cast<size_t>(row) * P.n_tiles + tc.n] =
-              make_float2(mx, sum);
+          for (; pos < kRouteTileK; ++pos) cand[pos] = 0ull;  // fewer than 16 columns
+          reinterpret_cast<float*>(P.out2)[static_cast<size_t>(row) * P.n_tiles + tc.n] = mx;
         }
       } else if constexpr (EPI == EPI_SWIGLU) {
         __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(P.out0);
@@ -864,7 +1002,14 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
       }
       }  // subtiles
       tc_fence_before();
-      mbar_arrive(&acc_empty[acc]);
+      if constexpr (CG == 2) {
+        // the accumulator buffer is free for the pair's next tile once both CTAs' four
+        // epilogue warps have read their rows
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(cluster_addr(&acc_empty[acc], 0));
+      } else {
+        mbar_arrive(&acc_empty[acc]);
+      }
       if (++acc == C::NACC) { acc = 0; acc_phase ^= 1; }
     }
     if (!ok && lane == 0) {
@@ -878,42 +1023,86 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
   // own tcgen05 ops and thread 0 gives in-flight TMA copies a bounded grace period, so
   // nothing lands in shared memory or TMEM after the CTA has released them.
   __syncthreads();
-  if (*abort_flag) {
-    if (threadIdx.x == 32) {
+  if constexpr (CG == 2) {
+    // The pair's MMAs write both CTAs' TMEM: the first CTA waits (bounded) for all of them
+    // before either CTA passes the pair barrier and frees its columns.  The barrier also
+    // keeps both CTAs alive until every signal one sends the other has landed.
+    if (rank == 0 && threadIdx.x == 32) {
+      umma_commit_pair_local(drain);
+      mbar_wait(drain, 0, reinterpret_cast<volatile int*>(&zero_flag));
+    }
+  } else {
+    if (*abort_flag && threadIdx.x == 32) {
       umma_commit(drain);
       mbar_wait(drain, 0, reinterpret_cast<volatile int*>(&zero_flag));
     }
-    if (threadIdx.x == 0) {
-      const uint64_t t0 = globaltimer_ns();
-      while (globaltimer_ns() - t0 < 2000000ull) {
-      }
+  }
+  if (*abort_flag && threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 2000000ull) {
     }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2) {
+    cluster_sync();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);
   }
 }
 
 // ctas_per_sm > 1 only for instantiations whose ring and TMEM both fit that many times on an
 // SM (shared memory <= 227 KB / ctas_per_sm, TMEM columns <= 512 / ctas_per_sm), so that no
-// CTA can wait on another's TMEM allocation.
+// CTA can wait on another's TMEM allocation.  CG = 2 launches clusters of two CTAs (one per
+// SM of a pair of SMs), as many as can be resident at once.
 template <int BN, int NB, bool A_MN, bool B_MN, int EPI, int STAGES, int CTAS_PER_SM = 1,
-          int MSUB = 1>
+          int MSUB = 1, int CG = 1>
 int launch_gemm(const GemmParams& P, cudaStream_t stream) {
-  using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB, CTAS_PER_SM>;
+  using C = GemmCfg<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB, CTAS_PER_SM, CG>;
   static_assert(CTAS_PER_SM * C::TMEM_COLS <= 512, "TMEM of co-resident CTAs");
   static_assert(CTAS_PER_SM * (C::SMEM_BYTES + 1024) <= 232448, "shared memory per SM");
   static_assert(CTAS_PER_SM > 1 || C::SMEM_BYTES > 232448 / 2,
                 "a single-CTA ring must be large enough to keep a second CTA off the SM");
-  auto kern = gemm_kernel<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB, CTAS_PER_SM>;
+  auto kern = gemm_kernel<BN, NB, A_MN, B_MN, EPI, STAGES, MSUB, CTAS_PER_SM, CG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return static_cast<int>(e);
-  kern<<<CTAS_PER_SM * num_sms(), 256, C::SMEM_BYTES, stream>>>(P);
-  return static_cast<int>(cudaGetLastError());
+  if constexpr (CG == 1) {
+    kern<<<CTAS_PER_SM * num_sms(), 256, C::SMEM_BYTES, stream>>>(P);
+    return static_cast<int>(cudaGetLastError());
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static int pairs_cache[64] = {0};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    int pairs = (dev >= 0 && dev < 64) ? pairs_cache[dev] : 0;
+    if (pairs <= 0) {
+      cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+      e = cudaOccupancyMaxActiveClusters(&pairs, kern, &cfg);
+      if (e != cudaSuccess) return static_cast<int>(e);
+      if (pairs <= 0) return static_cast<int>(cudaErrorInvalidConfiguration);
+      pairs = min(pairs, num_sms() / 2);
+      if (dev >= 0 && dev < 64) pairs_cache[dev] = pairs;
+    }
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    e = cudaLaunchKernelEx(&cfg, kern, P);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    return static_cast<int>(cudaGetLastError());
+  }
 }
 
 }  // namespace moe

@@ -4,16 +4,18 @@
 
 namespace moe {
 
-// dh = dz W_d (+ v'_d A_d), epilogue: SwiGLU backward -> da_g, da_u.  m256: 256-row tiles
-// (two 128-row subtiles share each weight stage; P.pair_off units).
-int launch_gemm_bwd_dh(const GemmParams& P, bool m256, cudaStream_t s) {
-  if (m256) return launch_gemm<256, 1, false, true, EPI_SWIGLU_BWD, 3, 1, 2>(P, s);
+// dh = dz W_d (+ v'_d A_d), epilogue: SwiGLU backward -> da_g, da_u.  Tile shapes as the
+// forward GEMMs (TileShape; each CTA of a pair reads two of the tile's four 64-wide boxes).
+int launch_gemm_bwd_dh(const GemmParams& P, int shape, cudaStream_t s) {
+  if (shape == kTilePair) return launch_gemm<256, 1, false, true, EPI_SWIGLU_BWD, 6, 1, 1, 2>(P, s);
+  if (shape == kTile256) return launch_gemm<256, 1, false, true, EPI_SWIGLU_BWD, 3, 1, 2>(P, s);
   return launch_gemm<256, 1, false, true, EPI_SWIGLU_BWD, 4>(P, s);
 }
 
 // dx_perm = da_g W_g + da_u W_u (+ v'_g A_g + v'_u A_u)
-int launch_gemm_bwd_dx(const GemmParams& P, bool m256, cudaStream_t s) {
-  if (m256) return launch_gemm<256, 1, false, true, EPI_STORE, 3, 1, 2>(P, s);
+int launch_gemm_bwd_dx(const GemmParams& P, int shape, cudaStream_t s) {
+  if (shape == kTilePair) return launch_gemm<256, 1, false, true, EPI_STORE, 6, 1, 1, 2>(P, s);
+  if (shape == kTile256) return launch_gemm<256, 1, false, true, EPI_STORE, 3, 1, 2>(P, s);
   return launch_gemm<256, 1, false, true, EPI_STORE, 4>(P, s);
 }
 

@@ -17,19 +17,23 @@ int launch_gemm_router_topk(const GemmParams& P, int bn, cudaStream_t s) {
   return launch_gemm<128, 2, false, false, EPI_ROUTE, 4>(P, s);
 }
 
-// m256: 256-row tiles (two 128-row subtiles sharing each B stage, one TMEM accumulator) for
-// groups of many rows, where reading each B stage into shared memory once per 256 rows
-// instead of once per 128 keeps the tensor core fed; no gathered A operand.
-int launch_gemm_gateup(const GemmParams& P, bool m256, cudaStream_t s) {
-  if (m256) {
-    if (P.gather_slot != nullptr) return static_cast<int>(cudaErrorInvalidValue);
-    return launch_gemm<128, 2, false, false, EPI_SWIGLU, 3, 1, 2>(P, s);
-  }
+// Tile shapes of the grouped expert GEMMs (TileShape): 128-row tiles; 256-row tiles in one
+// CTA (two 128-row subtiles sharing each B stage, one TMEM accumulator: P.pair_off units);
+// CTA pairs (tcgen05.mma.cta_group::2 over two SMs, M = 256: each SM stages its own 128 A rows
+// and half of the weight tile, and keeps two accumulators of its 128 rows).  Neither 256-row
+// shape takes a gathered A operand.
+int launch_gemm_gateup(const GemmParams& P, int shape, cudaStream_t s) {
+  if (shape != kTile128 && P.gather_slot != nullptr) return static_cast<int>(cudaErrorInvalidValue);
+  if (shape == kTilePair) return launch_gemm<128, 2, false, false, EPI_SWIGLU, 6, 1, 1, 2>(P, s);
+  if (shape == kTile256) return launch_gemm<128, 2, false, false, EPI_SWIGLU, 3, 1, 2>(P, s);
   return launch_gemm<128, 2, false, false, EPI_SWIGLU, 4>(P, s);
 }
 
-int launch_gemm_down(const GemmParams& P, bool m256, cudaStream_t s) {
-  if (m256) return launch_gemm<256, 1, false, false, EPI_GATE_SCALE, 3, 1, 2>(P, s);
+// With CTA pairs the weight maps are encoded with 128-row boxes (each CTA's half of the
+// 256-row weight tile).
+int launch_gemm_down(const GemmParams& P, int shape, cudaStream_t s) {
+  if (shape == kTilePair) return launch_gemm<256, 1, false, false, EPI_GATE_SCALE, 6, 1, 1, 2>(P, s);
+  if (shape == kTile256) return launch_gemm<256, 1, false, false, EPI_GATE_SCALE, 3, 1, 2>(P, s);
   return launch_gemm<256, 1, false, false, EPI_GATE_SCALE, 4>(P, s);
 }
 

@@ -41,6 +41,10 @@ constexpr int kMaxSegs = 4;
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 
+// Tile shapes of the grouped expert GEMMs: 128-row tiles, 256-row tiles in one CTA, or CTA
+// pairs (an M = 256 tile over two SMs).
+enum TileShape { kTile128 = 0, kTile256 = 1, kTilePair = 2 };
+
 enum Epilogue : int {
   EPI_F32_BIAS = 0,    // out_f32[row, col] = acc0 + bias[col]           (router logits)
   EPI_SWIGLU = 1,      // out_bf16 = silu(acc0) * acc1; optional save of acc0/acc1 as bf16
@@ -123,9 +127,9 @@ int num_sms();
 // Kernel launchers (gemm_fwd.cu).  Return cudaError_t as int.
 int launch_gemm_router(const GemmParams& P, int bn, cudaStream_t s);  // BN 128|224
 int launch_gemm_router_topk(const GemmParams& P, int bn, cudaStream_t s);  // + tile top-16
-// BN=128, NB=2, SwiGLU / BN=256, NB=1, gate scale; m256: 256-row tiles (P.pair_off units)
-int launch_gemm_gateup(const GemmParams& P, bool m256, cudaStream_t s);
-int launch_gemm_down(const GemmParams& P, bool m256, cudaStream_t s);
+// BN=128, NB=2, SwiGLU / BN=256, NB=1, gate scale; shape: a TileShape
+int launch_gemm_gateup(const GemmParams& P, int shape, cudaStream_t s);
+int launch_gemm_down(const GemmParams& P, int shape, cudaStream_t s);
 int launch_gemm_lora_u2(const GemmParams& P, int r, cudaStream_t s); // BN=r pad, NB=2
 int launch_gemm_lora_u1(const GemmParams& P, int r, cudaStream_t s); // BN=r pad, NB=1
 
@@ -135,9 +139,9 @@ int launch_combine_prepare(const int32_t* slot_row, int T, int k, int n_tiles, i
                            int32_t* comb_cnt, __nv_bfloat16* y, cudaStream_t s);
 
 // Backward instantiations (gemm_bwd.cu).  B operands MN-major (weights used transposed).
-// m256: 256-row tiles (P.pair_off units)
-int launch_gemm_bwd_dh(const GemmParams& P, bool m256, cudaStream_t s);  // BN=256, SwiGLU bwd
-int launch_gemm_bwd_dx(const GemmParams& P, bool m256, cudaStream_t s);  // BN=256, store bf16
+// shape: a TileShape (the 256-row shapes walk P.pair_off units)
+int launch_gemm_bwd_dh(const GemmParams& P, int shape, cudaStream_t s);  // BN=256, SwiGLU bwd
+int launch_gemm_bwd_dx(const GemmParams& P, int shape, cudaStream_t s);  // BN=256, store bf16
 int launch_gemm_bwd_lora_v(const GemmParams& P, int r, cudaStream_t s);  // BN=r pad, scale
 // LoRA weight gradients, grouped over K (rows of each expert); A and B MN-major.
 int launch_gemm_wgrad(const GemmParams& P, int r, int nb, cudaStream_t s);

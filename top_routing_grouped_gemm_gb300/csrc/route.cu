@@ -144,13 +144,14 @@ __global__ void __launch_bounds__(256, VPL > 28 ? 2 : 3) topk_softmax_kernel(
 
 // After the router GEMM's fused top-k epilogue: per token, the global top-k merged from the
 // NT tiles' 16-key candidate lists (every global winner is a winner of its own tile, so the
-// merge is exact), the softmax normaliser from the tiles' (max, sum exp), the renormalised
-// gates, and the per-block probability sums for the auxiliary loss.  One warp per token,
+// merge is exact), the softmax normaliser (the row maximum from the tiles' maxima, the sum
+// from the logits), the renormalised gates, and the per-block probability sums for the
+// auxiliary loss.  One warp per token,
 // 8 tokens per block (the row blocks of prob_partials, as topk_softmax_kernel).
 template <int VPL>
 __global__ void __launch_bounds__(256, VPL > 28 ? 2 : 3) route_merge_kernel(
     const float* __restrict__ logits, const uint64_t* __restrict__ cand,
-    const float2* __restrict__ stats, int T, int E, int k, int NT,
+    const float* __restrict__ tile_max, int T, int E, int k, int NT,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate,
     float* __restrict__ partials) {
   constexpr int WARPS = 8;
@@ -164,23 +165,37 @@ __global__ void __launch_bounds__(256, VPL > 28 ? 2 : 3) route_merge_kernel(
   const int ncand = NT * kRouteTileK;
 
   for (int t = t_begin + warp; t < t_end; t += WARPS) {
-    // this lane's candidates (at most 4 of at most 8 x 16), sorted descending
-    uint64_t hk[4] = {0ull, 0ull, 0ull, 0ull};
+    // every load of the token up front: this lane's candidates (at most 4 of at most
+    // 8 x 16), the tiles' statistics (lane n < NT holds tile n) and its logits
     const uint64_t* ct = cand + static_cast<size_t>(t) * ncand;
+    uint64_t c4[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int c = lane + 32 * q;
-      if (c < ncand) topk_insert(hk, __ldg(&ct[c]));
+      c4[q] = (c < ncand) ? __ldg(&ct[c]) : 0ull;
     }
-    // softmax normaliser of the whole row from the tiles' statistics
-    float M = -INFINITY;
-    for (int n = 0; n < NT; ++n) M = fmaxf(M, __ldg(&stats[static_cast<size_t>(t) * NT + n]).x);
-    float S = 0.f;
-    for (int n = 0; n < NT; ++n) {
-      const float2 st = __ldg(&stats[static_cast<size_t>(t) * NT + n]);
-      S += st.y * __expf(st.x - M);
+    float M = (lane < NT) ? __ldg(&tile_max[static_cast<size_t>(t) * NT + lane]) : -INFINITY;
+    const float* row = logits + static_cast<size_t>(t) * E;
+    float v[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < E) ? __ldg(&row[e]) : -INFINITY;
     }
-    const float inv = 1.0f / S;
+    uint64_t hk[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) topk_insert(hk, c4[q]);
+    // softmax of the whole row: the maximum from the tiles' maxima, then exp(L - max) of
+    // this lane's logits and the warp's sum
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float part = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      v[i] = (lane + 32 * i < E) ? __expf(v[i] - M) : 0.f;
+      part += v[i];
+    }
+    const float inv = 1.0f / warp_sum(part);
     // k rounds: the warp's largest head wins; its lane pops it
     uint64_t my_key = 0ull;
     for (int j = 0; j < k; ++j) {
@@ -196,11 +211,10 @@ __global__ void __launch_bounds__(256, VPL > 28 ? 2 : 3) route_merge_kernel(
       topk_idx[static_cast<size_t>(t) * k + lane] = key_expert(my_key);
       topk_gate[static_cast<size_t>(t) * k + lane] = pj / psum;
     }
-    const float* row = logits + static_cast<size_t>(t) * E;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       const int e = lane + 32 * i;
-      if (e < E) red[warp][e] += __expf(__ldg(&row[e]) - M) * inv;
+      if (e < E) red[warp][e] += v[i] * inv;
     }
   }
   __syncthreads();
@@ -279,13 +293,13 @@ int launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* idx, 
   return static_cast<int>(cudaGetLastError());
 }
 
-int launch_route_merge(const float* logits, const uint64_t* cand, const float* stats, int T,
+int launch_route_merge(const float* logits, const uint64_t* cand, const float* tile_max, int T,
                        int E, int k, int NT, int32_t* idx, float* gate, float* partials,
                        cudaStream_t s) {
   const int grid = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
-  const float2* st = reinterpret_cast<const float2*>(stats);
 #define MOE_MERGE(V) \
-  route_merge_kernel<V><<<grid, 256, 0, s>>>(logits, cand, st, T, E, k, NT, idx, gate, partials)
+  route_merge_kernel<V><<<grid, 256, 0, s>>>(logits, cand, tile_max, T, E, k, NT, idx, gate, \
+                                             partials)
   if (E <= 64)
     MOE_MERGE(2);
   else if (E <= 128)

@@ -24,9 +24,9 @@ int launch_split_router(const float* w, __nv_bfloat16* hi, __nv_bfloat16* lo, si
 int launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* idx, float* gate,
                         float* partials, cudaStream_t s, int n_alt = 0,
                         int32_t* alt_idx = nullptr);
-// After the router GEMM's fused top-k epilogue: cand [T, NT, 16] keys, stats [T, NT] (max,
-// sum exp) -> top-k, gates, probability partials (k <= 16)
-int launch_route_merge(const float* logits, const uint64_t* cand, const float* stats, int T,
+// After the router GEMM's fused top-k epilogue: cand [T, NT, 16] keys, tile_max [T, NT] ->
+// top-k, gates, probability partials (k <= 16)
+int launch_route_merge(const float* logits, const uint64_t* cand, const float* tile_max, int T,
                        int E, int k, int NT, int32_t* idx, float* gate, float* partials,
                        cudaStream_t s);
 // block_terms: scratch of ceil(E/32) floats

@@ -53,4 +53,46 @@ __device__ __forceinline__ void topk_insert(uint64_t (&top)[K], uint64_t key) {
   }
 }
 
+// Compare-exchange keeping the larger value first (min/max pairs: no branches).
+__host__ __device__ __forceinline__ void cx_desc(float& a, float& b) {
+  const float hi = fmaxf(a, b), lo = fminf(a, b);
+  a = hi;
+  b = lo;
+}
+
+// Bitonic sorting network on 16 values in registers, descending (80 compare-exchanges in 10
+// stages of 8 independent ones).
+__host__ __device__ __forceinline__ void sort16_desc(float (&v)[16]) {
+#pragma unroll
+  for (int k = 2; k <= 16; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          if ((i & k) == 0 || k == 16) cx_desc(v[i], v[l]);
+          else cx_desc(v[l], v[i]);
+        }
+      }
+    }
+  }
+}
+
+// best <- the 16 largest of best ∪ v (both sorted descending; result sorted descending):
+// the elementwise maximum of best and reversed v is a bitonic sequence holding the 16
+// largest values, which a 4-stage bitonic merger sorts.
+__host__ __device__ __forceinline__ void merge16_desc(float (&best)[16], const float (&v)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) best[i] = fmaxf(best[i], v[15 - i]);
+#pragma unroll
+  for (int j = 8; j > 0; j >>= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int l = i ^ j;
+      if (l > i) cx_desc(best[i], best[l]);
+    }
+  }
+}
+
 }  // namespace moe

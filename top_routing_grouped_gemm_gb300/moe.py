@@ -62,6 +62,7 @@ _SIGS = {
     "moe_route_num_partials": (ctypes.c_int, [_P]),
     "moe_route_workspace_size": (c_sz, [_P]),
     "moe_route": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+    "moe_route_fused_topk": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "moe_route_from_logits": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "moe_dispatch_workspace_size": (c_sz, [_P]),
     "moe_dispatch": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
@@ -222,6 +223,15 @@ def moe_route(p, x, w_router, bias, topk_idx, topk_gate, prob_partials, logits, 
     _check("moe_route", lib().moe_route(p.c(), _ptr(x), _ptr(w_router), _ptr(bias),
                                         _ptr(topk_idx), _ptr(topk_gate), _ptr(prob_partials),
                                         _ptr(logits), wp, wn, _ptr(dev_status), _stream(stream)))
+
+
+def moe_route_fused_topk(p, x, w_router, bias, topk_idx, topk_gate, prob_partials, logits,
+                         workspace, dev_status=None, stream=None):
+    wp, wn = _ws(workspace)
+    _check("moe_route_fused_topk",
+           lib().moe_route_fused_topk(p.c(), _ptr(x), _ptr(w_router), _ptr(bias),
+                                      _ptr(topk_idx), _ptr(topk_gate), _ptr(prob_partials),
+                                      _ptr(logits), wp, wn, _ptr(dev_status), _stream(stream)))
 
 
 def moe_route_from_logits(p, logits, topk_idx, topk_gate, prob_partials, dev_status=None,
