@@ -25,6 +25,7 @@
 
 #include "../../include/linear_attention.h"
 #include "moe_internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -254,95 +255,132 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
 }
 
 // Scan over the chunks of one (b, h) for RS value rows of the state (grid: DV/RS x H x B,
-// 256 threads).  Per chunk, with its q^, k^, Y and P staged in shared memory:
-// W = U - Y S^T, O = scale (gamma Q^ S^T + P W), then S = gamma_C S + sum_j exp(G_C - G_j)
-// w_j k^_j^T.  S_chunks (optional) receives the state at every chunk start (the backward's
-// checkpoints).
+// 256 threads).  Per chunk: W = U - Y S^T, O = scale (gamma Q^ S^T + P W), then
+// S = gamma_C S + sum_j exp(G_C - G_j) w_j k^_j^T.  S_chunks (optional) receives the state
+// at every chunk start (the backward's checkpoints).
+//
+// The chunk tiles do not depend on the state, so they stream in with cp.async while the
+// previous phase computes, one shared buffer per tile: Y, the U slice and the log decays are
+// needed by W and reloaded (for the next chunk) right after it, Q^ and P by O, K^ by the
+// state update.  Every phase thus waits only for copies issued one or two phases earlier
+// (wait_group 2: the two later groups may still be in flight).
+__device__ __forceinline__ void la_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void la_wait2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
+
+// rows x D fp32 tile (global row stride D) -> shared (row stride LDS, a multiple of 4)
+template <int ROWS, int D, int LDS>
+__device__ __forceinline__ void tile_async(float* dst, const float* src, int src_ld, int tid) {
+  constexpr int CPR = D / 4;  // 16-byte pieces per row
+  for (int e = tid; e < ROWS * CPR; e += 256) {
+    const int i = e / CPR, x4 = e - i * CPR;
+    cp_async_16(dst + i * LDS + 4 * x4, src + static_cast<size_t>(i) * src_ld + 4 * x4, 16u);
+  }
+}
+
+template <int DK>
+struct ScanLd {
+  static constexpr int T = DK + 4;  // streamed tiles: 16-byte rows (bank offset 4 per row)
+  static constexpr int P = kC + 4;
+};
+
 template <int DK, int DV>
 __global__ void __launch_bounds__(256) gdr_scan_kernel(
     const float* __restrict__ Qh, const float* __restrict__ Kh, const float* __restrict__ Y,
     const float* __restrict__ U, const float* __restrict__ Pm, const float* __restrict__ Gc,
     const float* __restrict__ S0, int T, int H, int nch, float scale,
     __nv_bfloat16* __restrict__ o, float* __restrict__ ST, float* __restrict__ Schk) {
-  constexpr int LK = Ld<DK>::v, LC = Ld<kC>::v;
-  extern __shared__ float sm[];
-  float* sS = sm;                   // [RS][LK] state rows
-  float* sQ = sS + kRS * LK;        // [C][LK]
-  float* sK = sQ + kC * LK;         // [C][LK]
-  float* sY = sK + kC * LK;         // [C][LK]
-  float* sP = sY + kC * LK;         // [C][LC]
-  float* sW = sP + kC * LC;         // [C][RS]
+  constexpr int LS = Ld<DK>::v, LT = ScanLd<DK>::T, LP = ScanLd<DK>::P;
+  extern __shared__ float4 sm4[];
+  float* sm = reinterpret_cast<float*>(sm4);
+  float* sQ = sm;                   // [C][LT]
+  float* sK = sQ + kC * LT;         // [C][LT]
+  float* sY = sK + kC * LT;         // [C][LT]
+  float* sP = sY + kC * LT;         // [C][LP]
+  float* sU = sP + kC * LP;         // [C][RS] U slice
+  float* sGr = sU + kC * kRS;       // [C] log decays
+  float* sS = sGr + kC;             // [RS][LS] state rows
+  float* sW = sS + kRS * LS;        // [C][RS]
   float* sWd = sW + kC * kRS;       // [C][RS] W decayed to the chunk end
-  float* sG = sWd + kC * kRS;       // [C]
-  float* sGam = sG + kC;            // [C] gamma_i
-  float* sDec = sGam + kC;          // [C] gamma_C / gamma_i
   static_assert(kC * kRS == 4 * 256, "W / O tiling: 4 outputs per thread");
   const int r0 = blockIdx.x * kRS, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
   const size_t bh = static_cast<size_t>(b) * H + h;
+  auto issue_a = [&](int c) {  // Y, U slice, log decays
+    if (c < nch) {
+      const size_t cid = bh * nch + c;
+      tile_async<kC, DK, LT>(sY, Y + cid * kC * DK, DK, tid);
+      tile_async<kC, kRS, kRS>(sU, U + cid * kC * DV + r0, DV, tid);
+      tile_async<1, kC, kC>(sGr, Gc + cid * kC, kC, tid);
+    }
+    la_commit();
+  };
+  auto issue_b = [&](int c) {  // Q^, P
+    if (c < nch) {
+      const size_t cid = bh * nch + c;
+      tile_async<kC, DK, LT>(sQ, Qh + cid * kC * DK, DK, tid);
+      tile_async<kC, kC, LP>(sP, Pm + cid * kC * kC, kC, tid);
+    }
+    la_commit();
+  };
+  auto issue_c = [&](int c) {  // K^
+    if (c < nch) tile_async<kC, DK, LT>(sK, Kh + (bh * nch + c) * kC * DK, DK, tid);
+    la_commit();
+  };
   for (int e = tid; e < kRS * DK; e += 256) {
     const int r = e / DK, x = e - r * DK;
-    sS[r * LK + x] = S0 ? S0[(bh * DV + r0 + r) * DK + x] : 0.f;
+    sS[r * LS + x] = S0 ? S0[(bh * DV + r0 + r) * DK + x] : 0.f;
   }
+  issue_a(0);
+  issue_b(0);
+  issue_c(0);
+  const int i = tid >> 2, rb = (tid & 3) * 4;  // W / O tiling: row i, value rows rb .. rb+3
   for (int c = 0; c < nch; ++c) {
     const size_t cid = bh * nch + c;
-    const float* cU = U + cid * kC * DV;
-    __syncthreads();  // the previous chunk is done with the tiles
-    for (int e = tid; e < kC * DK; e += 256) {
-      const int i = e / DK, x = e - i * DK;
-      sQ[i * LK + x] = Qh[cid * kC * DK + e];
-      sK[i * LK + x] = Kh[cid * kC * DK + e];
-      sY[i * LK + x] = Y[cid * kC * DK + e];
-    }
-    for (int e = tid; e < kC * kC; e += 256) sP[(e / kC) * LC + (e % kC)] = Pm[cid * kC * kC + e];
-    if (tid < kC) {
-      const float gi = Gc[cid * kC + tid];
-      sG[tid] = gi;
-      sGam[tid] = __expf(gi);                                 // gamma_i
-      sDec[tid] = __expf(Gc[cid * kC + kC - 1] - gi);         // gamma_C / gamma_i
-    }
+    la_wait2();        // Y, U, decays of chunk c
+    __syncthreads();   // (everyone's copies; the previous chunk's state update is done)
+    const float gi = sGr[i], gC = sGr[kC - 1];
+    const float gam_i = __expf(gi), dec_i = __expf(gC - gi), gam_C = __expf(gC);
     if (Schk)
       for (int e = tid; e < kRS * DK; e += 256) {
         const int r = e / DK, x = e - r * DK;
-        Schk[(cid * DV + r0 + r) * DK + x] = sS[r * LK + x];
+        Schk[(cid * DV + r0 + r) * DK + x] = sS[r * LS + x];
       }
-    __syncthreads();
-    // W = U - Y S^T ([C][RS]); thread: row i = tid / 4, columns r = 4 (tid % 4) .. + 3
+    // W = U - Y S^T ([C][RS])
     {
-      const int i = tid >> 2, rb = (tid & 3) * 4;
       float w[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) w[u] = cU[i * DV + r0 + rb + u];
-      const float* yi = sY + i * LK;
+      for (int u = 0; u < 4; ++u) w[u] = sU[i * kRS + rb + u];
+      const float* yi = sY + i * LT;
 #pragma unroll 4
       for (int x = 0; x < DK; ++x) {
         const float y = yi[x];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) w[u] -= y * sS[(rb + u) * LK + x];
+        for (int u = 0; u < 4; ++u) w[u] -= y * sS[(rb + u) * LS + x];
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         sW[i * kRS + rb + u] = w[u];
-        sWd[i * kRS + rb + u] = w[u] * sDec[i];               // decayed to the chunk end
+        sWd[i * kRS + rb + u] = w[u] * dec_i;               // decayed to the chunk end
       }
     }
+    __syncthreads();   // W is complete; Y, U and the decays are free
+    issue_a(c + 1);
+    la_wait2();        // Q^, P of chunk c
     __syncthreads();
-    // O = scale (gamma_i Q^_i . S_r + sum_{j<=i} P_ij w_jr); same thread tiling
+    // O = scale (gamma_i Q^_i . S_r + sum_{j<=i} P_ij w_jr)
     {
-      const int i = tid >> 2, rb = (tid & 3) * 4;
       const int t = c * kC + i;
       float a[4] = {0.f, 0.f, 0.f, 0.f};
-      const float* qi = sQ + i * LK;
+      const float* qi = sQ + i * LT;
 #pragma unroll 4
       for (int x = 0; x < DK; ++x) {
         const float qv = qi[x];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) a[u] += qv * sS[(rb + u) * LK + x];
+        for (int u = 0; u < 4; ++u) a[u] += qv * sS[(rb + u) * LS + x];
       }
-      const float gi = sGam[i];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) a[u] *= gi;
-      const float* pi = sP + i * LC;
+      for (int u = 0; u < 4; ++u) a[u] *= gam_i;
+      const float* pi = sP + i * LP;
       for (int j = 0; j <= i; ++j) {
         const float pv = pi[j];
 #pragma unroll
@@ -354,31 +392,41 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
         for (int u = 0; u < 4; ++u) orow[u] = __float2bfloat16_rn(scale * a[u]);
       }
     }
+    __syncthreads();   // Q^ and P are free
+    issue_b(c + 1);
+    la_wait2();        // K^ of chunk c
     __syncthreads();
     // S_r = gamma_C S_r + sum_j (gamma_C / gamma_j) w_jr k^_j; thread: column x, RS*DK/256
     // rows
     {
       constexpr int RPT = kRS * DK / 256;        // rows per thread (8 for DK 128, 4 for 64)
-      const int x = tid % DK, rb = (tid / DK) * RPT;
-      const float eC = sGam[kC - 1];
+      const int x = tid % DK, rs = (tid / DK) * RPT;
       float acc[RPT];
 #pragma unroll
-      for (int u = 0; u < RPT; ++u) acc[u] = eC * sS[(rb + u) * LK + x];
+      for (int u = 0; u < RPT; ++u) acc[u] = gam_C * sS[(rs + u) * LS + x];
       for (int j = 0; j < kC; ++j) {
-        const float kv = sK[j * LK + x];
+        const float kv = sK[j * LT + x];
 #pragma unroll
-        for (int u = 0; u < RPT; ++u) acc[u] += sWd[j * kRS + rb + u] * kv;
+        for (int u = 0; u < RPT; ++u) acc[u] += sWd[j * kRS + rs + u] * kv;
       }
 #pragma unroll
-      for (int u = 0; u < RPT; ++u) sS[(rb + u) * LK + x] = acc[u];
+      for (int u = 0; u < RPT; ++u) sS[(rs + u) * LS + x] = acc[u];
     }
+    __syncthreads();   // K^ is free (the next chunk's first barrier orders the new state)
+    issue_c(c + 1);
   }
   __syncthreads();
   if (ST)
     for (int e = tid; e < kRS * DK; e += 256) {
       const int r = e / DK, x = e - r * DK;
-      ST[(bh * DV + r0 + r) * DK + x] = sS[r * LK + x];
+      ST[(bh * DV + r0 + r) * DK + x] = sS[r * LS + x];
     }
+}
+
+template <int DK>
+constexpr size_t scan_smem_bytes() {
+  return (3 * kC * ScanLd<DK>::T + kC * ScanLd<DK>::P + kC * kRS + kC + kRS * Ld<DK>::v +
+          2 * kC * kRS) * sizeof(float);
 }
 
 // ---------------------------------------------------------------------------- backward
@@ -396,109 +444,137 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
 //     place they enter (A, U, Y, P, E, gamma); dg is the reverse cumulative sum of dG.
 
 // Backward scan over chunks for RS value rows of dS (grid: DV/RS x H x B).  Writes dW (the
-// slice's columns) and the state gradient at every chunk end; dS0 at the end.
+// slice's columns) and the state gradient at every chunk end; dS0 at the end.  The chunk
+// tiles stream in with cp.async as in the forward scan: P, K^, the dO slice and the log
+// decays (needed by dW) are reloaded for the next chunk right after dW, Q^ and Y (needed by
+// the state-gradient update) right after it (wait_group 1).
+__device__ __forceinline__ void la_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
 template <int DK, int DV>
 __global__ void __launch_bounds__(256) gdr_bwd_scan_kernel(
     const float* __restrict__ Qh, const float* __restrict__ Kh, const float* __restrict__ Y,
     const float* __restrict__ Pm, const float* __restrict__ Gc,
     const __nv_bfloat16* __restrict__ dO, const float* __restrict__ dST, int T, int H, int nch,
     float scale, float* __restrict__ dW, float* __restrict__ dSchk, float* __restrict__ dS0) {
-  constexpr int LK = Ld<DK>::v, LC = Ld<kC>::v;
-  extern __shared__ float sm[];
-  float* sD = sm;                   // [RS][LK] state gradient rows
-  float* sQ = sD + kRS * LK;        // [C][LK]
-  float* sK = sQ + kC * LK;         // [C][LK]
-  float* sY = sK + kC * LK;         // [C][LK]
-  float* sP = sY + kC * LK;         // [C][LC]
-  float* sO = sP + kC * LC;         // [C][RS] dO slice
-  float* sW = sO + kC * kRS;        // [C][RS] dW slice
+  constexpr int LS = Ld<DK>::v, LT = ScanLd<DK>::T, LP = ScanLd<DK>::P;
+  extern __shared__ float4 sm4[];
+  float* sm = reinterpret_cast<float*>(sm4);
+  float* sQ = sm;                   // [C][LT]
+  float* sK = sQ + kC * LT;         // [C][LT]
+  float* sY = sK + kC * LT;         // [C][LT]
+  float* sP = sY + kC * LT;         // [C][LP]
+  float* sGr = sP + kC * LP;        // [C] log decays
+  __nv_bfloat16* sOb = reinterpret_cast<__nv_bfloat16*>(sGr + kC);  // [C][RS] dO slice
+  float* sD = sGr + kC + kC * kRS / 2;  // [RS][LS] state gradient rows
+  float* sW = sD + kRS * LS;        // [C][RS] dW slice
   float* sOg = sW + kC * kRS;       // [C][RS] s gamma_i dO
-  float* sG = sOg + kC * kRS;       // [C]
-  float* sGam = sG + kC;            // [C] gamma_i
-  float* sDec = sGam + kC;          // [C] gamma_C / gamma_i
   static_assert(kC * kRS == 4 * 256, "dW tiling: 4 outputs per thread");
+  static_assert(kRS * 2 % 16 == 0, "dO slice rows are whole 16-byte pieces");
   const int r0 = blockIdx.x * kRS, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
   const size_t bh = static_cast<size_t>(b) * H + h;
+  auto issue_a = [&](int c) {  // P, K^, dO slice, log decays
+    if (c >= 0) {
+      const size_t cid = bh * nch + c;
+      tile_async<kC, kC, LP>(sP, Pm + cid * kC * kC, kC, tid);
+      tile_async<kC, DK, LT>(sK, Kh + cid * kC * DK, DK, tid);
+      tile_async<1, kC, kC>(sGr, Gc + cid * kC, kC, tid);
+      constexpr int PPR = kRS * 2 / 16;  // 16-byte pieces per dO row
+      for (int e = tid; e < kC * PPR; e += 256) {
+        const int i = e / PPR, pc = e - i * PPR;
+        const int t = c * kC + i;
+        // rows past the sequence read row 0 and are zeroed when used (t >= T below)
+        const size_t row = (static_cast<size_t>(b) * T + (t < T ? t : 0)) * H + h;
+        cp_async_16(sOb + i * kRS + pc * 8, dO + row * DV + r0 + pc * 8, 16u);
+      }
+    }
+    la_commit();
+  };
+  auto issue_b = [&](int c) {  // Q^, Y
+    if (c >= 0) {
+      const size_t cid = bh * nch + c;
+      tile_async<kC, DK, LT>(sQ, Qh + cid * kC * DK, DK, tid);
+      tile_async<kC, DK, LT>(sY, Y + cid * kC * DK, DK, tid);
+    }
+    la_commit();
+  };
   for (int e = tid; e < kRS * DK; e += 256) {
     const int r = e / DK, x = e - r * DK;
-    sD[r * LK + x] = dST ? dST[(bh * DV + r0 + r) * DK + x] : 0.f;
+    sD[r * LS + x] = dST ? dST[(bh * DV + r0 + r) * DK + x] : 0.f;
   }
+  issue_a(nch - 1);
+  issue_b(nch - 1);
+  const int i = tid >> 2, rb = (tid & 3) * 4;  // dW tiling: row i, value rows rb .. rb+3
   for (int c = nch - 1; c >= 0; --c) {
     const size_t cid = bh * nch + c;
+    la_wait1();        // P, K^, dO, decays of chunk c
     __syncthreads();
-    for (int e = tid; e < kC * DK; e += 256) {
-      const int i = e / DK, x = e - i * DK;
-      sQ[i * LK + x] = Qh[cid * kC * DK + e];
-      sK[i * LK + x] = Kh[cid * kC * DK + e];
-      sY[i * LK + x] = Y[cid * kC * DK + e];
-    }
-    for (int e = tid; e < kC * kC; e += 256) sP[(e / kC) * LC + (e % kC)] = Pm[cid * kC * kC + e];
-    for (int e = tid; e < kC * kRS; e += 256) {
-      const int i = e / kRS, r = e - i * kRS;
-      const int t = c * kC + i;
-      sO[e] = t < T ? bf(dO[((static_cast<size_t>(b) * T + t) * H + h) * DV + r0 + r]) : 0.f;
-    }
-    if (tid < kC) {
-      const float gi = Gc[cid * kC + tid];
-      sG[tid] = gi;
-      sGam[tid] = __expf(gi);
-      sDec[tid] = __expf(Gc[cid * kC + kC - 1] - gi);
-    }
+    const float gi = sGr[i], gC = sGr[kC - 1];
+    const float gam_i = __expf(gi), dec_i = __expf(gC - gi), gam_C = __expf(gC);
     for (int e = tid; e < kRS * DK; e += 256) {
       const int r = e / DK, x = e - r * DK;
-      dSchk[(cid * DV + r0 + r) * DK + x] = sD[r * LK + x];
+      dSchk[(cid * DV + r0 + r) * DK + x] = sD[r * LS + x];
     }
-    __syncthreads();
-    // dW = s P^T dO + E dS1^T; thread: row i = tid / 4, columns r = 4 (tid % 4) .. + 3
+    // dW = s P^T dO + E dS1^T
     {
-      const int i = tid >> 2, rb = (tid & 3) * 4;
       float a[4] = {0.f, 0.f, 0.f, 0.f}, bs[4] = {0.f, 0.f, 0.f, 0.f};
       for (int t = i; t < kC; ++t) {
-        const float pv = sP[t * LC + i];
+        const float pv = sP[t * LP + i];
+        const bool in = c * kC + t < T;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) a[u] += pv * sO[t * kRS + rb + u];
+        for (int u = 0; u < 4; ++u) a[u] += pv * (in ? bf(sOb[t * kRS + rb + u]) : 0.f);
       }
-      const float* ki = sK + i * LK;
+      const float* ki = sK + i * LT;
 #pragma unroll 4
       for (int x = 0; x < DK; ++x) {
         const float kv = ki[x];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) bs[u] += kv * sD[(rb + u) * LK + x];
+        for (int u = 0; u < 4; ++u) bs[u] += kv * sD[(rb + u) * LS + x];
       }
+      const bool in_i = c * kC + i < T;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const float w = scale * a[u] + sDec[i] * bs[u];
+        const float w = scale * a[u] + dec_i * bs[u];
         sW[i * kRS + rb + u] = w;
         dW[cid * kC * DV + i * DV + r0 + rb + u] = w;
-        sOg[i * kRS + rb + u] = scale * sGam[i] * sO[i * kRS + rb + u];
+        sOg[i * kRS + rb + u] = in_i ? scale * gam_i * bf(sOb[i * kRS + rb + u]) : 0.f;
       }
     }
+    __syncthreads();   // dW is complete; P, K^, dO and the decays are free
+    issue_a(c - 1);
+    la_wait1();        // Q^, Y of chunk c
     __syncthreads();
     // dS0 = gamma_C dS1 + sum_i (s gamma_i dO_ir) q^_i - sum_i dW_ir Y_i; thread: column x
     {
       constexpr int RPT = kRS * DK / 256;
-      const int x = tid % DK, rb = (tid / DK) * RPT;
-      const float eC = sGam[kC - 1];
+      const int x = tid % DK, rs = (tid / DK) * RPT;
       float acc[RPT];
 #pragma unroll
-      for (int u = 0; u < RPT; ++u) acc[u] = eC * sD[(rb + u) * LK + x];
-      for (int i = 0; i < kC; ++i) {
-        const float qv = sQ[i * LK + x], yv = sY[i * LK + x];
+      for (int u = 0; u < RPT; ++u) acc[u] = gam_C * sD[(rs + u) * LS + x];
+      for (int j = 0; j < kC; ++j) {
+        const float qv = sQ[j * LT + x], yv = sY[j * LT + x];
 #pragma unroll
         for (int u = 0; u < RPT; ++u)
-          acc[u] += sOg[i * kRS + rb + u] * qv - sW[i * kRS + rb + u] * yv;
+          acc[u] += sOg[j * kRS + rs + u] * qv - sW[j * kRS + rs + u] * yv;
       }
 #pragma unroll
-      for (int u = 0; u < RPT; ++u) sD[(rb + u) * LK + x] = acc[u];
+      for (int u = 0; u < RPT; ++u) sD[(rs + u) * LS + x] = acc[u];
     }
+    __syncthreads();   // Q^ and Y are free
+    issue_b(c - 1);
   }
   __syncthreads();
   if (dS0)
     for (int e = tid; e < kRS * DK; e += 256) {
       const int r = e / DK, x = e - r * DK;
-      dS0[(bh * DV + r0 + r) * DK + x] = sD[r * LK + x];
+      dS0[(bh * DV + r0 + r) * DK + x] = sD[r * LS + x];
     }
+}
+
+template <int DK>
+constexpr size_t bwd_scan_smem_bytes() {
+  return (3 * kC * ScanLd<DK>::T + kC * ScanLd<DK>::P + kC + kC * kRS / 2 + kRS * Ld<DK>::v +
+          2 * kC * kRS) * sizeof(float);
 }
 
 // Per-chunk backward (grid: chunks x H x B): everything local to the chunk once dW and the
@@ -811,8 +887,7 @@ int gdr_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloat16*
   k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, Qh, Kh, Yw, Uw, Pw, Gw,
                                        nullptr);
   mark_after(MOE_KERNEL_GDR_CHUNK, s);
-  const size_t sm2 = (kRS * Ld<DK>::v + 3 * kC * Ld<DK>::v + kC * Ld<kC>::v + 2 * kC * kRS +
-                      3 * kC) * sizeof(float);
+  const size_t sm2 = scan_smem_bytes<DK>();
   auto k2 = gdr_scan_kernel<DK, DV>;
   e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm2));
   if (e != cudaSuccess) return static_cast<int>(e);
@@ -854,8 +929,7 @@ int gdr_bwd_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloa
                                        static_cast<int>(sm1));
   if (e != cudaSuccess) return static_cast<int>(e);
   k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, Qh, Kh, Yw, Uw, Pw, Gw, Aw);
-  const size_t sm2 = (kRS * Ld<DK>::v + 3 * kC * Ld<DK>::v + kC * Ld<kC>::v + 3 * kC * kRS +
-                      3 * kC) * sizeof(float);
+  const size_t sm2 = bwd_scan_smem_bytes<DK>();
   auto k2 = gdr_bwd_scan_kernel<DK, DV>;
   e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm2));
   if (e != cudaSuccess) return static_cast<int>(e);
@@ -896,6 +970,7 @@ int moe_gdr_forward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, con
   if (!((dk == 64 || dk == 128) && (dv == 64 || dv == 128))) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * H * ((T + kC - 1) / kC) > (1ll << 24)) return MOE_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < gdr_ws(B, T, H, dk, dv)) return MOE_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return MOE_ERR_UNSUPPORTED;
   const auto* q_ = reinterpret_cast<const __nv_bfloat16*>(q);
   const auto* k_ = reinterpret_cast<const __nv_bfloat16*>(k);
   const auto* v_ = reinterpret_cast<const __nv_bfloat16*>(v);
@@ -929,6 +1004,8 @@ int moe_gdr_backward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, co
   if (!((dk == 64 || dk == 128) && (dv == 64 || dv == 128))) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * H * ((T + kC - 1) / kC) > (1ll << 24)) return MOE_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < gdr_bwd_ws(B, T, H, dk, dv)) return MOE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(d_o)) & 15u)
+    return MOE_ERR_UNSUPPORTED;
   const auto* q_ = reinterpret_cast<const __nv_bfloat16*>(q);
   const auto* k_ = reinterpret_cast<const __nv_bfloat16*>(k);
   const auto* v_ = reinterpret_cast<const __nv_bfloat16*>(v);
