@@ -289,7 +289,8 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
     const float* __restrict__ U, const float* __restrict__ Pm, const float* __restrict__ Gc,
     const float* __restrict__ S0, int T, int H, int nch, float scale,
     __nv_bfloat16* __restrict__ o, float* __restrict__ ST, float* __restrict__ Schk) {
-  constexpr int LS = Ld<DK>::v, LT = ScanLd<DK>::T, LP = ScanLd<DK>::P;
+  constexpr int LT = ScanLd<DK>::T, LP = ScanLd<DK>::P;
+  constexpr int LS = ScanLd<DK>::T;  // state rows: 16-byte aligned (read as float4)
   extern __shared__ float4 sm4[];
   float* sm = reinterpret_cast<float*>(sm4);
   float* sQ = sm;                   // [C][LT]
@@ -299,9 +300,10 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
   float* sU = sP + kC * LP;         // [C][RS] U slice
   float* sGr = sU + kC * kRS;       // [C] log decays
   float* sS = sGr + kC;             // [RS][LS] state rows
-  float* sW = sS + kRS * LS;        // [C][RS]
-  float* sWd = sW + kC * kRS;       // [C][RS] W decayed to the chunk end
+  float* sW = sS + kRS * LS;        // [C][4][4]: W[j][q + 4u] at j*16 + 4q + u
+  float* sWd = sW + kC * kRS;       // the same, decayed to the chunk end
   static_assert(kC * kRS == 4 * 256, "W / O tiling: 4 outputs per thread");
+  static_assert(kRS == 16 && DK % 4 == 0, "thread tiling");
   const int r0 = blockIdx.x * kRS, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
   const size_t bh = static_cast<size_t>(b) * H + h;
@@ -333,7 +335,16 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
   issue_a(0);
   issue_b(0);
   issue_c(0);
-  const int i = tid >> 2, rb = (tid & 3) * 4;  // W / O tiling: row i, value rows rb .. rb+3
+  // W / O tiling: token row i, value rows q, q + 4, q + 8, q + 12 (interleaved, so that the
+  // four 16-byte state reads of a quarter warp fall in different banks)
+  const int i = tid >> 2, q = tid & 3;
+  // state update tiling: columns 4 xg .. 4 xg + 3, value rows 2 rp and 2 rp + 1 (rp is the
+  // warp: its row weights are broadcast reads)
+  constexpr int XG = DK / 4;                 // float4 column groups
+  constexpr int RP = 256 / XG;               // row groups (8 for DK 128, 16 for 64)
+  constexpr int RPG = kRS / RP;              // rows per group (2 for DK 128, 1 for 64)
+  static_assert(RPG >= 1 && RP * RPG == kRS, "state update tiling");
+  const int xg = tid % XG, rp = tid / XG;
   for (int c = 0; c < nch; ++c) {
     const size_t cid = bh * nch + c;
     la_wait2();        // Y, U, decays of chunk c
@@ -349,68 +360,87 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
     {
       float w[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) w[u] = sU[i * kRS + rb + u];
-      const float* yi = sY + i * LT;
+      for (int u = 0; u < 4; ++u) w[u] = sU[i * kRS + q + 4 * u];
+      const float4* yi = reinterpret_cast<const float4*>(sY + i * LT);
 #pragma unroll 4
-      for (int x = 0; x < DK; ++x) {
-        const float y = yi[x];
+      for (int x4 = 0; x4 < DK / 4; ++x4) {
+        const float4 y = yi[x4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) w[u] -= y * sS[(rb + u) * LS + x];
+        for (int u = 0; u < 4; ++u) {
+          const float4 sv = reinterpret_cast<const float4*>(sS + (q + 4 * u) * LS)[x4];
+          w[u] -= y.x * sv.x + y.y * sv.y + y.z * sv.z + y.w * sv.w;
+        }
       }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        sW[i * kRS + rb + u] = w[u];
-        sWd[i * kRS + rb + u] = w[u] * dec_i;               // decayed to the chunk end
-      }
+      *reinterpret_cast<float4*>(sW + i * kRS + 4 * q) = make_float4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<float4*>(sWd + i * kRS + 4 * q) =
+          make_float4(w[0] * dec_i, w[1] * dec_i, w[2] * dec_i, w[3] * dec_i);
     }
     __syncthreads();   // W is complete; Y, U and the decays are free
     issue_a(c + 1);
     la_wait2();        // Q^, P of chunk c
     __syncthreads();
-    // O = scale (gamma_i Q^_i . S_r + sum_{j<=i} P_ij w_jr)
+    // O = scale (gamma_i Q^_i . S_r + sum_{j<=i} P_ij w_jr)  (P is zero above the diagonal)
     {
       const int t = c * kC + i;
       float a[4] = {0.f, 0.f, 0.f, 0.f};
-      const float* qi = sQ + i * LT;
+      const float4* qi = reinterpret_cast<const float4*>(sQ + i * LT);
 #pragma unroll 4
-      for (int x = 0; x < DK; ++x) {
-        const float qv = qi[x];
+      for (int x4 = 0; x4 < DK / 4; ++x4) {
+        const float4 qv = qi[x4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) a[u] += qv * sS[(rb + u) * LS + x];
+        for (int u = 0; u < 4; ++u) {
+          const float4 sv = reinterpret_cast<const float4*>(sS + (q + 4 * u) * LS)[x4];
+          a[u] += qv.x * sv.x + qv.y * sv.y + qv.z * sv.z + qv.w * sv.w;
+        }
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) a[u] *= gam_i;
       const float* pi = sP + i * LP;
-      for (int j = 0; j <= i; ++j) {
-        const float pv = pi[j];
+      for (int j0 = 0; j0 <= i; j0 += 4) {
+        const float4 pv = *reinterpret_cast<const float4*>(pi + j0);
+        const float pj[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) a[u] += pv * sW[j * kRS + rb + u];
+        for (int jj = 0; jj < 4; ++jj) {
+          const float4 wv = *reinterpret_cast<const float4*>(sW + (j0 + jj) * kRS + 4 * q);
+          a[0] += pj[jj] * wv.x;
+          a[1] += pj[jj] * wv.y;
+          a[2] += pj[jj] * wv.z;
+          a[3] += pj[jj] * wv.w;
+        }
       }
       if (t < T) {
-        __nv_bfloat16* orow = o + ((static_cast<size_t>(b) * T + t) * H + h) * DV + r0 + rb;
+        __nv_bfloat16* orow = o + ((static_cast<size_t>(b) * T + t) * H + h) * DV + r0 + q;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) orow[u] = __float2bfloat16_rn(scale * a[u]);
+        for (int u = 0; u < 4; ++u) orow[4 * u] = __float2bfloat16_rn(scale * a[u]);
       }
     }
     __syncthreads();   // Q^ and P are free
     issue_b(c + 1);
     la_wait2();        // K^ of chunk c
     __syncthreads();
-    // S_r = gamma_C S_r + sum_j (gamma_C / gamma_j) w_jr k^_j; thread: column x, RS*DK/256
-    // rows
+    // S_r = gamma_C S_r + sum_j (gamma_C / gamma_j) w_jr k^_j
     {
-      constexpr int RPT = kRS * DK / 256;        // rows per thread (8 for DK 128, 4 for 64)
-      const int x = tid % DK, rs = (tid / DK) * RPT;
-      float acc[RPT];
+      float4 acc[RPG];
 #pragma unroll
-      for (int u = 0; u < RPT; ++u) acc[u] = gam_C * sS[(rs + u) * LS + x];
+      for (int v = 0; v < RPG; ++v) {
+        const float4 sv = reinterpret_cast<const float4*>(sS + (rp * RPG + v) * LS)[xg];
+        acc[v] = make_float4(gam_C * sv.x, gam_C * sv.y, gam_C * sv.z, gam_C * sv.w);
+      }
       for (int j = 0; j < kC; ++j) {
-        const float kv = sK[j * LT + x];
+        const float4 kv = reinterpret_cast<const float4*>(sK + j * LT)[xg];
 #pragma unroll
-        for (int u = 0; u < RPT; ++u) acc[u] += sWd[j * kRS + rs + u] * kv;
+        for (int v = 0; v < RPG; ++v) {
+          const int r = rp * RPG + v;
+          const float wd = sWd[j * kRS + 4 * (r & 3) + (r >> 2)];
+          acc[v].x += wd * kv.x;
+          acc[v].y += wd * kv.y;
+          acc[v].z += wd * kv.z;
+          acc[v].w += wd * kv.w;
+        }
       }
 #pragma unroll
-      for (int u = 0; u < RPT; ++u) sS[(rs + u) * LS + x] = acc[u];
+      for (int v = 0; v < RPG; ++v)
+        reinterpret_cast<float4*>(sS + (rp * RPG + v) * LS)[xg] = acc[v];
     }
     __syncthreads();   // K^ is free (the next chunk's first barrier orders the new state)
     issue_c(c + 1);
@@ -425,7 +455,7 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
 
 template <int DK>
 constexpr size_t scan_smem_bytes() {
-  return (3 * kC * ScanLd<DK>::T + kC * ScanLd<DK>::P + kC * kRS + kC + kRS * Ld<DK>::v +
+  return (3 * kC * ScanLd<DK>::T + kC * ScanLd<DK>::P + kC * kRS + kC + kRS * ScanLd<DK>::T +
           2 * kC * kRS) * sizeof(float);
 }
 
