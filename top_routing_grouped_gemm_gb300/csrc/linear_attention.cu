@@ -259,13 +259,15 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
 // S = gamma_C S + sum_j exp(G_C - G_j) w_j k^_j^T.  S_chunks (optional) receives the state
 // at every chunk start (the backward's checkpoints).
 //
-// The chunk tiles do not depend on the state, so they stream in with cp.async while the
-// previous phase computes, one shared buffer per tile: Y, the U slice and the log decays are
-// needed by W and reloaded (for the next chunk) right after it, Q^ and P by O, K^ by the
-// state update.  Every phase thus waits only for copies issued one or two phases earlier
-// (wait_group 2: the two later groups may still be in flight).
+// Two phases per chunk: W, then the output and the state update together (the update
+// writes the other of two state buffers, so both read the chunk-start state without a
+// barrier between them).  The chunk tiles do not depend on the state, so they stream in with
+// cp.async while the other phase computes, one shared buffer per tile: Y, the U slice and
+// the log decays (phase 1) are reloaded for the next chunk right after phase 1, Q^, P and K^
+// (phase 2) right after phase 2; each phase waits only for the copies issued one phase
+// earlier (wait_group 1: the later group may still be in flight).
 __device__ __forceinline__ void la_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void la_wait2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
+__device__ __forceinline__ void la_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // rows x D fp32 tile (global row stride D) -> shared (row stride LDS, a multiple of 4)
 template <int ROWS, int D, int LDS>
@@ -299,15 +301,15 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
   float* sP = sY + kC * LT;         // [C][LP]
   float* sU = sP + kC * LP;         // [C][RS] U slice
   float* sGr = sU + kC * kRS;       // [C] log decays
-  float* sS = sGr + kC;             // [RS][LS] state rows
-  float* sW = sS + kRS * LS;        // [C][4][4]: W[j][q + 4u] at j*16 + 4q + u
+  float* sSb = sGr + kC;            // 2 x [RS][LS] state rows (ping-pong over chunks)
+  float* sW = sSb + 2 * kRS * LS;   // [C][4][4]: W[j][q + 4u] at j*16 + 4q + u
   float* sWd = sW + kC * kRS;       // the same, decayed to the chunk end
   static_assert(kC * kRS == 4 * 256, "W / O tiling: 4 outputs per thread");
   static_assert(kRS == 16 && DK % 4 == 0, "thread tiling");
   const int r0 = blockIdx.x * kRS, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
   const size_t bh = static_cast<size_t>(b) * H + h;
-  auto issue_a = [&](int c) {  // Y, U slice, log decays
+  auto issue_a = [&](int c) {  // Y, U slice, log decays (phase 1)
     if (c < nch) {
       const size_t cid = bh * nch + c;
       tile_async<kC, DK, LT>(sY, Y + cid * kC * DK, DK, tid);
@@ -316,30 +318,26 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
     }
     la_commit();
   };
-  auto issue_b = [&](int c) {  // Q^, P
+  auto issue_b = [&](int c) {  // Q^, P, K^ (phase 2)
     if (c < nch) {
       const size_t cid = bh * nch + c;
       tile_async<kC, DK, LT>(sQ, Qh + cid * kC * DK, DK, tid);
       tile_async<kC, kC, LP>(sP, Pm + cid * kC * kC, kC, tid);
+      tile_async<kC, DK, LT>(sK, Kh + cid * kC * DK, DK, tid);
     }
-    la_commit();
-  };
-  auto issue_c = [&](int c) {  // K^
-    if (c < nch) tile_async<kC, DK, LT>(sK, Kh + (bh * nch + c) * kC * DK, DK, tid);
     la_commit();
   };
   for (int e = tid; e < kRS * DK; e += 256) {
     const int r = e / DK, x = e - r * DK;
-    sS[r * LS + x] = S0 ? S0[(bh * DV + r0 + r) * DK + x] : 0.f;
+    sSb[r * LS + x] = S0 ? S0[(bh * DV + r0 + r) * DK + x] : 0.f;
   }
   issue_a(0);
   issue_b(0);
-  issue_c(0);
   // W / O tiling: token row i, value rows q, q + 4, q + 8, q + 12 (interleaved, so that the
   // four 16-byte state reads of a quarter warp fall in different banks)
   const int i = tid >> 2, q = tid & 3;
-  // state update tiling: columns 4 xg .. 4 xg + 3, value rows 2 rp and 2 rp + 1 (rp is the
-  // warp: its row weights are broadcast reads)
+  // state update tiling: columns 4 xg .. 4 xg + 3, value rows rp * RPG .. (rp: the warp's
+  // row group, so its row weights are broadcast reads)
   constexpr int XG = DK / 4;                 // float4 column groups
   constexpr int RP = 256 / XG;               // row groups (8 for DK 128, 16 for 64)
   constexpr int RPG = kRS / RP;              // rows per group (2 for DK 128, 1 for 64)
@@ -347,8 +345,10 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
   const int xg = tid % XG, rp = tid / XG;
   for (int c = 0; c < nch; ++c) {
     const size_t cid = bh * nch + c;
-    la_wait2();        // Y, U, decays of chunk c
-    __syncthreads();   // (everyone's copies; the previous chunk's state update is done)
+    const float* sS = sSb + (c & 1) * kRS * LS;      // state at the chunk start
+    float* sSn = sSb + ((c & 1) ^ 1) * kRS * LS;     // state at the chunk end
+    la_wait1();        // Y, U, decays of chunk c
+    __syncthreads();   // (everyone's copies; the previous chunk is done with every tile)
     const float gi = sGr[i], gC = sGr[kC - 1];
     const float gam_i = __expf(gi), dec_i = __expf(gC - gi), gam_C = __expf(gC);
     if (Schk)
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
         const int r = e / DK, x = e - r * DK;
         Schk[(cid * DV + r0 + r) * DK + x] = sS[r * LS + x];
       }
-    // W = U - Y S^T ([C][RS])
+    // phase 1: W = U - Y S^T ([C][RS])
     {
       float w[4];
 #pragma unroll
@@ -377,9 +377,10 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
     }
     __syncthreads();   // W is complete; Y, U and the decays are free
     issue_a(c + 1);
-    la_wait2();        // Q^, P of chunk c
+    la_wait1();        // Q^, P, K^ of chunk c
     __syncthreads();
-    // O = scale (gamma_i Q^_i . S_r + sum_{j<=i} P_ij w_jr)  (P is zero above the diagonal)
+    // phase 2a: O = scale (gamma_i Q^_i . S_r + sum_{j<=i} P_ij w_jr)  (P is zero above the
+    // diagonal)
     {
       const int t = c * kC + i;
       float a[4] = {0.f, 0.f, 0.f, 0.f};
@@ -414,10 +415,7 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
         for (int u = 0; u < 4; ++u) orow[4 * u] = __float2bfloat16_rn(scale * a[u]);
       }
     }
-    __syncthreads();   // Q^ and P are free
-    issue_b(c + 1);
-    la_wait2();        // K^ of chunk c
-    __syncthreads();
+    // phase 2b (same phase: it writes the other state buffer):
     // S_r = gamma_C S_r + sum_j (gamma_C / gamma_j) w_jr k^_j
     {
       float4 acc[RPG];
@@ -440,23 +438,25 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
       }
 #pragma unroll
       for (int v = 0; v < RPG; ++v)
-        reinterpret_cast<float4*>(sS + (rp * RPG + v) * LS)[xg] = acc[v];
+        reinterpret_cast<float4*>(sSn + (rp * RPG + v) * LS)[xg] = acc[v];
     }
-    __syncthreads();   // K^ is free (the next chunk's first barrier orders the new state)
-    issue_c(c + 1);
+    __syncthreads();   // Q^, P and K^ are free (the next chunk's first barrier orders the state)
+    issue_b(c + 1);
   }
   __syncthreads();
-  if (ST)
+  if (ST) {
+    const float* sS = sSb + (nch & 1) * kRS * LS;
     for (int e = tid; e < kRS * DK; e += 256) {
       const int r = e / DK, x = e - r * DK;
       ST[(bh * DV + r0 + r) * DK + x] = sS[r * LS + x];
     }
+  }
 }
 
 template <int DK>
 constexpr size_t scan_smem_bytes() {
-  return (3 * kC * ScanLd<DK>::T + kC * ScanLd<DK>::P + kC * kRS + kC + kRS * ScanLd<DK>::T +
-          2 * kC * kRS) * sizeof(float);
+  return (3 * kC * ScanLd<DK>::T + kC * ScanLd<DK>::P + kC * kRS + kC +
+          2 * kRS * ScanLd<DK>::T + 2 * kC * kRS) * sizeof(float);
 }
 
 // ---------------------------------------------------------------------------- backward
@@ -478,8 +478,6 @@ constexpr size_t scan_smem_bytes() {
 // tiles stream in with cp.async as in the forward scan: P, K^, the dO slice and the log
 // decays (needed by dW) are reloaded for the next chunk right after dW, Q^ and Y (needed by
 // the state-gradient update) right after it (wait_group 1).
-__device__ __forceinline__ void la_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-
 template <int DK, int DV>
 __global__ void __launch_bounds__(256) gdr_bwd_scan_kernel(
     const float* __restrict__ Qh, const float* __restrict__ Kh, const float* __restrict__ Y,

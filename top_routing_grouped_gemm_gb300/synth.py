@@ -183,6 +183,8 @@ LA_CONFIGS = {
     # one long sequence (the pages fine-tune with micro-batch 1 and long context), 16 heads
     "la": LAConfig("la", B=1, T=32768, H=16),
     "la_small": LAConfig("la_small", B=2, T=1000, H=4, with_state=True),
+    # the same 16 heads on a 4096-token sequence (a hardware-counter capture case)
+    "la_mid": LAConfig("la_mid", B=1, T=4096, H=16),
 }
 
 
