@@ -226,7 +226,9 @@ int route_impl(const moe_problem* p, const moe_bf16* x, const float* w_router, c
                                static_cast<size_t>(E) * d, stream));
   GemmParams P = gemm_params();
   MOE_TRY(encode_map_kmajor(&P.maps[0], x, d, T, 1, kBM));
-  MOE_TRY(encode_map_kmajor(&P.maps[1], w_split, d, E, 2, bn));
+  // the logits GEMM runs on CTA pairs (half of the bn expert rows per CTA); the fused top-k
+  // variant on single CTAs
+  MOE_TRY(encode_map_kmajor(&P.maps[1], w_split, d, E, 2, fused ? bn : bn / 2));
   P.nmaps = 2;
   // one K pass: each A stage is multiplied by the hi (z = 0) and lo (z = 1) weight tiles
   P.seg[0] = GemmSeg{d / kBK, 0, 0, {1, 1}, {0, 0}, {0, 1}};

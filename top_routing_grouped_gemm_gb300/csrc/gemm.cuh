@@ -44,7 +44,8 @@ struct GemmCfg {
   // CTA pairs with two K-major B operands (gate and up) run one MMA of N = 2*BN per k step:
   // its B rows 0..BN-1 (the first operand's tile) sit in the first CTA and BN..2BN-1 (the
   // second's) in the second, so each CTA stages one whole operand tile
-  static constexpr bool PAIR_JOIN = CG == 2 && NB == 2 && !B_MN && 2 * BN <= 256;
+  static constexpr bool PAIR_JOIN = CG == 2 && NB == 2 && !B_MN && 2 * BN <= 256 &&
+                                    EPI != EPI_F32_BIAS && EPI != EPI_ROUTE;
   static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
   // The router (EPI_F32_BIAS) with two B operands sums them into one accumulator: they are
   // the bf16 hi and lo parts of the same fp32 weights, both multiplied by the same A stage.
@@ -67,8 +68,8 @@ struct GemmCfg {
   static_assert(NACC * ACC_COLS <= 512, "accumulators must fit in TMEM");
   static_assert(!B_MN || BN % 64 == 0, "MN-major B is read in whole 64-wide boxes");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
-  static_assert(CG == 1 || (MSUB == 1 && CTAS == 1 && !A_MN && EPI != EPI_WGRAD && !SUMB),
-                "CTA pairs: M-grouped K-major A, one CTA per SM");
+  static_assert(CG == 1 || (MSUB == 1 && CTAS == 1 && !A_MN && EPI != EPI_WGRAD),
+                "CTA pairs: K-major A, one CTA per SM");
   static_assert(CG == 1 || (B_MN ? BN % 128 == 0 : (BN / 2) % 8 == 0),
                 "half B tiles stay whole boxes / swizzle atoms");
 };
@@ -597,7 +598,12 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
                     const uint32_t b_addr = a_addr + C::A_BYTES + b * C::B_BYTES;
                     const uint64_t bdesc = B_MN ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
                                                 : smem_desc_sw128(b_addr + k * 32, 16, 1024);
-                    umma_bf16<2>(d_base + b * BN, adesc, bdesc, idp, accumulate);
+                    if constexpr (C::SUMB) {
+                      // the router's lo weight part adds to what the hi part wrote
+                      umma_bf16<2>(d_base, adesc, bdesc, idp, (accumulate || b > 0) ? 1u : 0u);
+                    } else {
+                      umma_bf16<2>(d_base + b * BN, adesc, bdesc, idp, accumulate);
+                    }
                   }
                 }
               }

@@ -4,10 +4,11 @@
 namespace moe {
 
 // Two B operands (the hi and lo parts of the split router weights) share each A stage and
-// sum into one accumulator.
+// sum into one accumulator.  On CTA pairs (M = 256 token rows over two SMs, each staging half
+// of the bn expert rows of both parts; the weight map boxes are bn / 2 rows).
 int launch_gemm_router(const GemmParams& P, int bn, cudaStream_t s) {
-  if (bn == 224) return launch_gemm<224, 2, false, false, EPI_F32_BIAS, 3>(P, s);
-  return launch_gemm<128, 2, false, false, EPI_F32_BIAS, 4>(P, s);
+  if (bn == 224) return launch_gemm<224, 2, false, false, EPI_F32_BIAS, 5, 1, 1, 2>(P, s);
+  return launch_gemm<128, 2, false, false, EPI_F32_BIAS, 6, 1, 1, 2>(P, s);
 }
 
 // The same product with the fused top-k epilogue (candidates to P.out1, statistics to
