@@ -67,32 +67,60 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
   const int t0 = c * kC;
   const size_t chunk_id = (static_cast<size_t>(b) * H + h) * nch + c;
 
-  // q, k rows, L2 normalised (one warp per row)
-  for (int i = warp; i < kC; i += 8) {
+  // v rows: 16-byte loads issued first, held in registers until U needs them (rows past the
+  // sequence are zero)
+  constexpr int VPR = DV / 8, VPER = kC * VPR / 256;  // 16-byte pieces per row / per thread
+  uint4 va[VPER];
+#pragma unroll
+  for (int m = 0; m < VPER; ++m) {
+    const int e = tid + 256 * m, i = e / VPR, pc = e - i * VPR;
     const int t = t0 + i;
-    float sq = 0.f, sk = 0.f;
-    for (int x = lane; x < DK; x += 32) {
-      float qv = 0.f, kv = 0.f;
-      if (t < T) {
-        const size_t o = ((static_cast<size_t>(b) * T + t) * H + h) * DK + x;
-        qv = bf(q[o]);
-        kv = bf(k[o]);
-      }
-      sQ[i * LK + x] = qv;
-      sK[i * LK + x] = kv;
-      sq += qv * qv;
-      sk += kv * kv;
+    va[m] = t < T ? *reinterpret_cast<const uint4*>(
+                        v + ((static_cast<size_t>(b) * T + t) * H + h) * DV + pc * 8)
+                  : make_uint4(0u, 0u, 0u, 0u);
+  }
+  // q, k rows, L2 normalised: every 16-byte load of the two tiles in flight at once; a row's
+  // PPR pieces sit in PPR consecutive threads, which reduce its squared norm by shuffles
+  {
+    constexpr int PPR = DK / 8, PER = kC * PPR / 256;
+    static_assert(32 % PPR == 0 && PER * 256 == kC * PPR, "q/k tile loading");
+    uint4 qa[PER], ka[PER];
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+      const int e = tid + 256 * m, i = e / PPR, pc = e - i * PPR;
+      const int t = t0 + i;
+      const size_t o = ((static_cast<size_t>(b) * T + t) * H + h) * DK + pc * 8;
+      qa[m] = t < T ? *reinterpret_cast<const uint4*>(q + o) : make_uint4(0u, 0u, 0u, 0u);
+      ka[m] = t < T ? *reinterpret_cast<const uint4*>(k + o) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      sq += __shfl_xor_sync(0xffffffffu, sq, o);
-      sk += __shfl_xor_sync(0xffffffffu, sk, o);
-    }
-    const float iq = sq > 0.f ? 1.0f / sqrtf(sq) : 0.f;
-    const float ik = sk > 0.f ? 1.0f / sqrtf(sk) : 0.f;
-    for (int x = lane; x < DK; x += 32) {
-      sQ[i * LK + x] *= iq;
-      sK[i * LK + x] *= ik;
+    for (int m = 0; m < PER; ++m) {
+      const int e = tid + 256 * m, i = e / PPR, pc = e - i * PPR;
+      float qf[8], kf[8];
+      const uint32_t qw[4] = {qa[m].x, qa[m].y, qa[m].z, qa[m].w};
+      const uint32_t kw[4] = {ka[m].x, ka[m].y, ka[m].z, ka[m].w};
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 a2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qw[j]));
+        const float2 b2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw[j]));
+        qf[2 * j] = a2.x; qf[2 * j + 1] = a2.y;
+        kf[2 * j] = b2.x; kf[2 * j + 1] = b2.y;
+        sq += a2.x * a2.x + a2.y * a2.y;
+        sk += b2.x * b2.x + b2.y * b2.y;
+      }
+#pragma unroll
+      for (int o = PPR / 2; o > 0; o >>= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        sk += __shfl_xor_sync(0xffffffffu, sk, o);
+      }
+      const float iq = sq > 0.f ? 1.0f / sqrtf(sq) : 0.f;
+      const float ik = sk > 0.f ? 1.0f / sqrtf(sk) : 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        sQ[i * LK + pc * 8 + j] = qf[j] * iq;
+        sK[i * LK + pc * 8 + j] = kf[j] * ik;
+      }
     }
   }
   // beta and the cumulative log decay (warp 0, in token order)
@@ -219,10 +247,16 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
   constexpr int LV = Ld<DV>::v;
   static_assert(kC * LV <= 2 * kC * LK, "the V tile fits where the K and Q tiles were");
   float* sV = sK;  // [C][LV]
-  for (int e = tid; e < kC * DV; e += 256) {
-    const int i = e / DV, x = e - i * DV;
-    const int t = t0 + i;
-    sV[i * LV + x] = t < T ? sB[i] * bf(v[((static_cast<size_t>(b) * T + t) * H + h) * DV + x]) : 0.f;
+#pragma unroll
+  for (int m = 0; m < VPER; ++m) {
+    const int e = tid + 256 * m, i = e / VPR, pc = e - i * VPR;
+    const uint32_t vw[4] = {va[m].x, va[m].y, va[m].z, va[m].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 a2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vw[j]));
+      sV[i * LV + pc * 8 + 2 * j] = sB[i] * a2.x;
+      sV[i * LV + pc * 8 + 2 * j + 1] = sB[i] * a2.y;
+    }
   }
   __syncthreads();
   {
@@ -998,7 +1032,9 @@ int moe_gdr_forward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, con
   if (!((dk == 64 || dk == 128) && (dv == 64 || dv == 128))) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * H * ((T + kC - 1) / kC) > (1ll << 24)) return MOE_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < gdr_ws(B, T, H, dk, dv)) return MOE_ERR_WORKSPACE;
-  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return MOE_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(q) |
+       reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u)
+    return MOE_ERR_UNSUPPORTED;
   const auto* q_ = reinterpret_cast<const __nv_bfloat16*>(q);
   const auto* k_ = reinterpret_cast<const __nv_bfloat16*>(k);
   const auto* v_ = reinterpret_cast<const __nv_bfloat16*>(v);
@@ -1032,7 +1068,9 @@ int moe_gdr_backward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, co
   if (!((dk == 64 || dk == 128) && (dv == 64 || dv == 128))) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * H * ((T + kC - 1) / kC) > (1ll << 24)) return MOE_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < gdr_bwd_ws(B, T, H, dk, dv)) return MOE_ERR_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(d_o)) & 15u)
+  if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(d_o) |
+       reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+       reinterpret_cast<uintptr_t>(v)) & 15u)
     return MOE_ERR_UNSUPPORTED;
   const auto* q_ = reinterpret_cast<const __nv_bfloat16*>(q);
   const auto* k_ = reinterpret_cast<const __nv_bfloat16*>(k);
