@@ -342,7 +342,10 @@ int moe_aux_loss(const moe_problem* p, const int32_t* counts, const float* prob_
 
 /* dz_perm[row] = g(slot) * dy[t]  (bf16, rows < n_kept);
  * dgate[t*k+j] = <dy[t], o(row)> = <dy[t], y_perm[row]> / g(slot) for kept slots, else 0.
- * dy [T, d] bf16; y_perm [rows, d] bf16 (forward output); dgate [T*k] fp32. */
+ * dy [T, d] bf16; y_perm [rows, d] bf16 (forward output) or NULL; dgate [T*k] fp32.
+ * With y_perm NULL the kept slots' gate gradients are left to moe_expert_ffn_bwd (which
+ * forms them from its dh product without reading y_perm again): dgate, if given, is then
+ * set to 0 for every slot. */
 int moe_combine_bwd(const moe_problem* p, const moe_bf16* dy, const moe_bf16* y_perm,
                     const int32_t* slot_row, const float* topk_gate, moe_bf16* dz_perm,
                     float* dgate, moe_stream_t stream);
@@ -352,14 +355,20 @@ int moe_combine_bwd(const moe_problem* p, const moe_bf16* dy, const moe_bf16* y_
  *   dx_perm = da_g W_g + da_u W_u + s (da_g B_g) A_g + s (da_u B_u) A_u     (bf16 out)
  *   dB_d = s dz^T (h A_d^T),  dA_d = s (dz B_d)^T h,  and likewise for gate and up.
  * saved must hold a_gate and a_up (and u_* when lora is given); h is the forward's h.
- * grads may be NULL when lora is NULL. */
+ * grads may be NULL when lora is NULL.
+ * dgate (optional, with row_slot [rows] and topk_gate [T*k] per slot): the gate gradients
+ * of the kept slots, dgate[row_slot[r]] = <dh_r, h_r> / g = <dy[t], o_r> (dh = g dy W_d +
+ * ... is linear in dy; h_r = silu(a_g) a_u recomputed in fp32 in the dh epilogue); other
+ * slots are not written (see moe_combine_bwd with y_perm NULL). */
 size_t moe_expert_ffn_bwd_workspace_size(const moe_problem* p, int32_t rows_max);
 int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x_perm,
                        const int32_t* offsets, const moe_bf16* w_gate, const moe_bf16* w_up,
                        const moe_bf16* w_down, const moe_lora* lora,
                        const moe_ffn_saved* saved, const moe_bf16* h, const moe_bf16* dz_perm,
-                       moe_bf16* dx_perm, const moe_lora_grad* grads, void* workspace,
-                       size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream);
+                       moe_bf16* dx_perm, const moe_lora_grad* grads,
+                       const int32_t* row_slot, const float* topk_gate, float* dgate,
+                       void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                       moe_stream_t stream);
 
 /* dx[t] = sum over kept slots of dx_perm[slot_row[t*k+j]]   (fp32 [T, d], overwritten) */
 int moe_dispatch_bwd(const moe_problem* p, const moe_bf16* dx_perm, const int32_t* slot_row,

@@ -77,6 +77,23 @@ def test_backward_whole(cfg):
                 assert float(buf.grads["d" + nm][e].abs().max()) == 0.0
 
 
+def test_gate_gradient_from_dh_matches_combine_backward():
+    """The gate gradients the expert backward forms from its dh product (<dh, h> / g) against
+    the combine backward's <dy, y_perm> / g on the same step (two roundings apart)."""
+    cfg = small_cfg(T=300, cap_num=5, cap_den=4)
+    inp = synth.make_inputs(cfg, "cpu")
+    dev = to_dev(inp)
+    p, buf = run_fwd_bwd(cfg, dev)
+    dg_ref = torch.empty_like(buf.dgate)
+    dz = torch.empty_like(buf.dz_perm)
+    moe.moe_combine_bwd(p, dev["dy"], buf.y_perm, buf.slot_row, buf.topk_gate, dz, dg_ref)
+    torch.cuda.synchronize()
+    assert torch.equal(dz, buf.dz_perm)
+    assert relerr(f64(buf.dgate), f64(dg_ref)) <= RTOL_FP
+    dropped = buf.slot_row < 0
+    assert bool((buf.dgate[dropped.view(buf.dgate.shape)] == 0).all())
+
+
 def test_backward_gate_and_expert_paths_separately():
     cfg = small_cfg(T=200, cap_num=5, cap_den=4)
     inp = synth.make_inputs(cfg, "cpu")

@@ -690,8 +690,9 @@ int moe_combine_bwd(const moe_problem* p, const moe_bf16* dy, const moe_bf16* y_
                     const int32_t* slot_row, const float* topk_gate, moe_bf16* dz_perm,
                     float* dgate, moe_stream_t stream) {
   MOE_TRY(check_problem(p));
-  if (!dy || !y_perm || !slot_row || !topk_gate || !dz_perm || !dgate) return MOE_ERR_INVALID_ARG;
-  if (!al16(dy) || !al16(y_perm) || !al16(dz_perm)) return MOE_ERR_UNSUPPORTED;
+  if (!dy || !slot_row || !topk_gate || !dz_perm || (y_perm && !dgate))
+    return MOE_ERR_INVALID_ARG;
+  if (!al16(dy) || (y_perm && !al16(y_perm)) || !al16(dz_perm)) return MOE_ERR_UNSUPPORTED;
   count_launches(1);
   return cuda_status(launch_combine_bwd(
       reinterpret_cast<const __nv_bfloat16*>(dy), reinterpret_cast<const __nv_bfloat16*>(y_perm),
@@ -703,6 +704,7 @@ size_t moe_expert_ffn_bwd_workspace_size(const moe_problem* p, int32_t rows_max)
   if (check_problem(p) != MOE_OK || rows_max <= 0) return 0;
   size_t b = 2 * up256((p->E + 1) * 4ull) + 2 * up256(static_cast<size_t>(rows_max) * p->F * 2);
   if (p->r) b += 3 * up256(static_cast<size_t>(rows_max) * p->r * 2);
+  b += up256(static_cast<size_t>(rows_max) * ((p->F + 255) / 256) * 4);  // gate-gradient parts
   return b;
 }
 
@@ -710,10 +712,13 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
                        const int32_t* offsets, const moe_bf16* w_gate, const moe_bf16* w_up,
                        const moe_bf16* w_down, const moe_lora* lora,
                        const moe_ffn_saved* saved, const moe_bf16* h, const moe_bf16* dz_perm,
-                       moe_bf16* dx_perm, const moe_lora_grad* grads, void* workspace,
-                       size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
+                       moe_bf16* dx_perm, const moe_lora_grad* grads,
+                       const int32_t* row_slot, const float* topk_gate, float* dgate,
+                       void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                       moe_stream_t stream) {
   MOE_TRY(check_problem(p));
   if (rows_max <= 0) return MOE_ERR_INVALID_ARG;
+  if (dgate && (!row_slot || !topk_gate)) return MOE_ERR_INVALID_ARG;
   if (!x_perm || !offsets || !w_gate || !w_up || !w_down || !saved || !saved->a_gate ||
       !saved->a_up || !h || !dz_perm || !dx_perm)
     return MOE_ERR_INVALID_ARG;
@@ -750,6 +755,8 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
     v_g = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * r);
     v_u = cv.take<moe_bf16>(static_cast<size_t>(rows_max) * r);
   }
+  const int dh_tiles = (F + 255) / 256;
+  float* gate_parts = cv.take<float>(static_cast<size_t>(rows_max) * dh_tiles);
   MOE_CUDA(launch_tile_schedule(offsets, E, rows_max, tile_off, pair_off, dev_status, stream));
   int launches = 1;
   // 256-row tiles: dh only for big groups (its SwiGLU-backward epilogue is heavy and stays
@@ -808,10 +815,16 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
     P.in1 = saved->a_up;
     P.out0 = da_g;
     P.out1 = da_u;
+    P.out2 = dgate ? gate_parts : nullptr;
     ++launches;
     mark_before(MOE_KERNEL_BWD_DH_GEMM, stream);
     MOE_CUDA(launch_gemm_bwd_dh(P, shape_dh, stream));
     mark_after(MOE_KERNEL_BWD_DH_GEMM, stream);
+    if (dgate) {
+      MOE_CUDA(launch_dgate_finalize(gate_parts, dh_tiles, row_slot, topk_gate, offsets + E,
+                                     rows_max, dgate, stream));
+      ++launches;
+    }
   }
   // v'_g = s da_g B_g, v'_u = s da_u B_u
   if (use_lora) {

@@ -305,18 +305,37 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(
   float dot = 0.f;
   for (int v = lane; v < nvec; v += 32) {
     float fa[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float fb[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     add_bf16x8(fa, dyr[v], 1.f);
-    add_bf16x8(fb, y_perm[static_cast<size_t>(r) * nvec + v], 1.f);
+    if (y_perm) {
+      float fb[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      add_bf16x8(fb, y_perm[static_cast<size_t>(r) * nvec + v], 1.f);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      dot += fa[i] * fb[i];
-      fa[i] *= g;
+      for (int i = 0; i < 8; ++i) dot += fa[i] * fb[i];
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) fa[i] *= g;
     dz_perm[static_cast<size_t>(r) * nvec + v] = pack_bf16x8(fa);
   }
-  dot = warp_sum_f(dot);
-  if (lane == 0) dgate[slot] = g > 0.f ? dot / g : 0.f;
+  if (y_perm) dot = warp_sum_f(dot);
+  // without y_perm the kept slots' gate gradients come later (expert backward): zero here
+  if (lane == 0 && dgate) dgate[slot] = (y_perm && g > 0.f) ? dot / g : 0.f;
+}
+
+// dgate[row_slot[r]] = (sum over the dh GEMM's n-tiles of <dh, h> of row r) / gate, for the
+// kept rows r < offsets[E] (in a fixed order: deterministic).
+__global__ void dgate_finalize_kernel(const float* __restrict__ part, int n_tiles,
+                                      const int32_t* __restrict__ row_slot,
+                                      const float* __restrict__ gate,
+                                      const int32_t* __restrict__ n_rows, int rows_max,
+                                      float* __restrict__ dgate) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= rows_max || r >= __ldg(n_rows)) return;
+  const int slot = row_slot[r];
+  if (slot < 0) return;
+  float sum = 0.f;
+  for (int n = 0; n < n_tiles; ++n) sum += part[static_cast<size_t>(r) * n_tiles + n];
+  const float g = gate[slot];
+  dgate[slot] = g > 0.f ? sum / g : 0.f;
 }
 
 // dx[t] = sum over kept slots of dx_perm rows (fp32, overwritten).  One block per token.
@@ -783,6 +802,14 @@ int launch_combine_bwd(const __nv_bfloat16* dy, const __nv_bfloat16* y_perm,
   combine_bwd_kernel<<<grid_for_slots(static_cast<long long>(T) * k), 256, 0, s>>>(
       reinterpret_cast<const uint4*>(dy), reinterpret_cast<const uint4*>(y_perm), slot_row,
       gate, T, d, k, reinterpret_cast<uint4*>(dz_perm), dgate);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_dgate_finalize(const float* part, int n_tiles, const int32_t* row_slot,
+                          const float* gate, const int32_t* n_rows, int rows_max, float* dgate,
+                          cudaStream_t s) {
+  dgate_finalize_kernel<<<(rows_max + 255) / 256, 256, 0, s>>>(part, n_tiles, row_slot, gate,
+                                                                n_rows, rows_max, dgate);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -921,11 +921,14 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
           }
         }
       } else if constexpr (EPI == EPI_SWIGLU_BWD) {
-        // acc0 = dh; saved a_g (in0), a_u (in1) -> da_g (out0), da_u (out1)
+        // acc0 = dh; saved a_g (in0), a_u (in1) -> da_g (out0), da_u (out1); with out2, also
+        // this n-tile's part of <dh, h> (h = silu(a_g) a_u recomputed in fp32) per row: the
+        // gate gradient <dy, o> = <dh, h> / gate (dh = gate dy W_d (+ LoRA) is linear in dy)
         const __nv_bfloat16* ag = reinterpret_cast<const __nv_bfloat16*>(P.in0);
         const __nv_bfloat16* au = reinterpret_cast<const __nv_bfloat16*>(P.in1);
         __nv_bfloat16* dag = reinterpret_cast<__nv_bfloat16*>(P.out0);
         __nv_bfloat16* dau = reinterpret_cast<__nv_bfloat16*>(P.out1);
+        float hd = 0.f;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
           float dh[16];
@@ -942,11 +945,14 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
               const float sgm = 1.0f / (1.0f + __expf(-g[i]));
               o1[i] = dh[i] * u[i] * sgm * (1.0f + g[i] * (1.0f - sgm));
               o2[i] = dh[i] * g[i] * sgm;
+              hd += o2[i] * u[i];
             }
             store_bf16x16(dag + off, o1, P.N - col);
             store_bf16x16(dau + off, o2, P.N - col);
           }
         }
+        if (P.out2 && valid)
+          reinterpret_cast<float*>(P.out2)[row * P.n_tiles + tc.n] = hd;
       } else if constexpr (EPI == EPI_WGRAD) {
         // fp32 gradient of group g: [M, N] (ld N) or transposed [N, M] (ld M)
 #pragma unroll 1

@@ -66,6 +66,10 @@ int launch_combine(const __nv_bfloat16* y_perm, const int32_t* slot_row, int T, 
 int launch_combine_bwd(const __nv_bfloat16* dy, const __nv_bfloat16* y_perm,
                        const int32_t* slot_row, const float* gate, int T, int d, int k,
                        __nv_bfloat16* dz_perm, float* dgate, cudaStream_t s);
+// dgate[row_slot[r]] = sum_n part[r][n] / gate[slot] for rows r < *n_rows (device count)
+int launch_dgate_finalize(const float* part, int n_tiles, const int32_t* row_slot,
+                          const float* gate, const int32_t* n_rows, int rows_max, float* dgate,
+                          cudaStream_t s);
 int launch_dispatch_bwd(const __nv_bfloat16* dx_perm, const int32_t* slot_row, int T, int d,
                         int k, float* dx, cudaStream_t s);
 int launch_route_bwd(const int32_t* idx, const float* gate, const float* dgate,

@@ -96,6 +96,7 @@ _SIGS = {
     "moe_expert_ffn_bwd": (ctypes.c_int, [_P, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
                                           ctypes.POINTER(moe_lora), ctypes.POINTER(moe_ffn_saved),
                                           c_vp, c_vp, c_vp, ctypes.POINTER(moe_lora_grad),
+                                          c_vp, c_vp, c_vp,
                                           c_vp, c_sz, c_vp, c_vp]),
     "moe_dispatch_bwd": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp]),
     "moe_route_bwd": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
@@ -378,13 +379,15 @@ def moe_expert_ffn_bwd_workspace_size(p: Problem, rows_max: int) -> int:
 
 
 def moe_expert_ffn_bwd(p, rows_max, x_perm, offsets, w_gate, w_up, w_down, lora, saved, h,
-                       dz_perm, dx_perm, grads, workspace, dev_status=None, stream=None):
+                       dz_perm, dx_perm, grads, workspace, dev_status=None, stream=None,
+                       row_slot=None, topk_gate=None, dgate=None):
     wp, wn = _ws(workspace)
     _check("moe_expert_ffn_bwd",
            lib().moe_expert_ffn_bwd(p.c(), rows_max, _ptr(x_perm), _ptr(offsets), _ptr(w_gate),
                                     _ptr(w_up), _ptr(w_down), _lora(lora), _saved(saved), _ptr(h),
-                                    _ptr(dz_perm), _ptr(dx_perm), _grads(grads), wp, wn,
-                                    _ptr(dev_status), _stream(stream)))
+                                    _ptr(dz_perm), _ptr(dx_perm), _grads(grads), _ptr(row_slot),
+                                    _ptr(topk_gate), _ptr(dgate), wp, wn, _ptr(dev_status),
+                                    _stream(stream)))
 
 
 def moe_dispatch_bwd(p, dx_perm, slot_row, dx, stream=None):
@@ -575,15 +578,16 @@ def layer_forward(buf: LayerBuffers, x, w_router, bias, w_gate, w_up, w_down, lo
 def layer_backward(buf: LayerBuffers, dy, x, w_router, w_gate, w_up, w_down, lora=None,
                    stream=None):
     """Gradient of <dy, y> for the forward last run on ``buf`` (which must have been built
-    with train=True): combine backward -> expert backward (dx_perm, LoRA grads) -> dispatch
-    backward (expert path of dx) -> router backward (gate path of dx, accumulated)."""
+    with train=True): combine backward (dz_perm) -> expert backward (dx_perm, LoRA grads, and
+    the gate gradients from its dh product) -> dispatch backward (expert path of dx) -> router
+    backward (gate path of dx, accumulated)."""
     p = buf.p
     assert buf.train, "LayerBuffers(train=True) keeps what the backward needs"
-    moe_combine_bwd(p, dy, buf.y_perm, buf.slot_row, buf.topk_gate, buf.dz_perm, buf.dgate,
-                    stream)
+    moe_combine_bwd(p, dy, None, buf.slot_row, buf.topk_gate, buf.dz_perm, buf.dgate, stream)
     moe_expert_ffn_bwd(p, buf.rows_max, buf.x_perm, buf.offsets, w_gate, w_up, w_down, lora,
                        buf.saved, buf.h, buf.dz_perm, buf.dx_perm, buf.grads, buf.ws_bwd,
-                       buf.dev_status, stream)
+                       buf.dev_status, stream, row_slot=buf.row_slot, topk_gate=buf.topk_gate,
+                       dgate=buf.dgate)
     moe_dispatch_bwd(p, buf.dx_perm, buf.slot_row, buf.dx, stream)
     moe_route_bwd(p, buf.topk_idx, buf.topk_gate, buf.dgate, w_router, buf.dx, stream)
     return buf.dx
