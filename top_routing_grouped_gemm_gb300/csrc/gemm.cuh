@@ -14,6 +14,13 @@
 // except on 256-row tiles (two 128-row A subtiles per B stage), whose one accumulator fills
 // all 512 TMEM columns.
 //
+// CTA pairs (CG = 2, clusters of two CTAs on the two SMs of a TPC): one M = 256 tile per
+// pair, issued by the first CTA as tcgen05.mma.cta_group::2; each CTA stages its own 128 A
+// rows and half of every B tile, both CTAs' TMA copies complete on the first CTA's stage
+// barrier, and the first CTA's commits arrive on the stage-free and accumulator-full
+// barriers of both.  Each CTA keeps two accumulators of its 128 rows, so the epilogue still
+// overlaps the next tile, with half the weight bytes staged per SM.
+//
 // Operand tiles in shared memory use the 128-byte swizzle that TMA writes:
 //   K-major  (rows x 64 K): 128-byte rows, 8-row atoms of 1024 B -> SBO = 1024; the k-th
 //            16-wide MMA step starts 32 B further into the atom.
