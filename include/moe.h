@@ -380,6 +380,13 @@ int moe_dispatch_bwd(const moe_problem* p, const moe_bf16* dx_perm, const int32_
 int moe_route_bwd(const moe_problem* p, const int32_t* topk_idx, const float* topk_gate,
                   const float* dgate, const float* w_router, float* dx, moe_stream_t stream);
 
+/* moe_dispatch_bwd followed by moe_route_bwd in one pass over dx (each token's row read and
+ * written once; the same order of operations, so the same bits). */
+int moe_dispatch_route_bwd(const moe_problem* p, const moe_bf16* dx_perm,
+                           const int32_t* slot_row, const int32_t* topk_idx,
+                           const float* topk_gate, const float* dgate, const float* w_router,
+                           float* dx, moe_stream_t stream);
+
 /* ==================================================================== instrumentation
  * Profiling aids, not part of the layer.  moe_set_kernel_events() makes the library record
  * the caller's CUDA events (cudaEvent_t, passed as void*) on the launch stream immediately

@@ -94,6 +94,18 @@ def test_gate_gradient_from_dh_matches_combine_backward():
     assert bool((buf.dgate[dropped.view(buf.dgate.shape)] == 0).all())
 
 
+def test_fused_dispatch_route_backward_is_bit_exact():
+    cfg = small_cfg(T=257, cap_num=5, cap_den=4)
+    inp = synth.make_inputs(cfg, "cpu")
+    dev = to_dev(inp)
+    p, buf = run_fwd_bwd(cfg, dev)
+    dx2 = torch.empty_like(buf.dx)
+    moe.moe_dispatch_bwd(p, buf.dx_perm, buf.slot_row, dx2)
+    moe.moe_route_bwd(p, buf.topk_idx, buf.topk_gate, buf.dgate, dev["w_router"], dx2)
+    torch.cuda.synchronize()
+    assert torch.equal(buf.dx, dx2)
+
+
 def test_backward_gate_and_expert_paths_separately():
     cfg = small_cfg(T=200, cap_num=5, cap_den=4)
     inp = synth.make_inputs(cfg, "cpu")

@@ -927,6 +927,20 @@ int moe_route_bwd(const moe_problem* p, const int32_t* topk_idx, const float* to
                                       p->k, dx, stream));
 }
 
+int moe_dispatch_route_bwd(const moe_problem* p, const moe_bf16* dx_perm,
+                           const int32_t* slot_row, const int32_t* topk_idx,
+                           const float* topk_gate, const float* dgate, const float* w_router,
+                           float* dx, moe_stream_t stream) {
+  MOE_TRY(check_problem(p));
+  if (!dx_perm || !slot_row || !topk_idx || !topk_gate || !dgate || !w_router || !dx)
+    return MOE_ERR_INVALID_ARG;
+  if (!al16(dx_perm) || !al16(w_router) || !al16(dx)) return MOE_ERR_UNSUPPORTED;
+  count_launches(1);
+  return cuda_status(launch_dispatch_route_bwd(reinterpret_cast<const __nv_bfloat16*>(dx_perm),
+                                               slot_row, topk_idx, topk_gate, dgate, w_router,
+                                               p->T, p->d, p->E, p->k, dx, stream));
+}
+
 // ------------------------------------------------------------------------ instrumentation
 
 int moe_set_kernel_events(int kernel_id, void* event_before, void* event_after) {

@@ -360,6 +360,60 @@ __global__ void __launch_bounds__(kRowThreads) dispatch_bwd_kernel(
   }
 }
 
+// Both backward paths into dx in one pass, one block per token: dx[t] = sum_j dx_perm[row_j]
+// (the expert path, rank order) + sum_j c_j W_r[e_j] (the gate path, c_j as below), in the
+// same order of operations as dispatch_bwd_kernel followed by route_bwd_kernel.
+__global__ void __launch_bounds__(kRowThreads) dispatch_route_bwd_kernel(
+    const uint4* __restrict__ dx_perm, const int32_t* __restrict__ slot_row,
+    const int32_t* __restrict__ idx, const float* __restrict__ gate,
+    const float* __restrict__ dgate, const float4* __restrict__ w_router, int T, int d, int E,
+    int k, float4* __restrict__ dx) {
+  __shared__ int rows[32];
+  __shared__ float cs[32];
+  __shared__ int es[32];
+  const int t = blockIdx.x;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float g = 0.f, dg = 0.f;
+    int e = 0, r = -1;
+    if (lane < k) {
+      const size_t slot = static_cast<size_t>(t) * k + lane;
+      r = slot_row[slot];
+      g = gate[slot];
+      dg = dgate[slot];
+      e = idx[slot];
+      if (e < 0 || e >= E) { e = 0; g = 0.f; }
+    }
+    const float sgd = warp_sum_f(g * dg);
+    rows[lane] = r;
+    cs[lane] = g * (dg - sgd);
+    es[lane] = e;
+  }
+  __syncthreads();
+  const int nvec = d / 8;
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int j = 0; j < k; ++j) {
+      const int r = rows[j];
+      if (r >= 0) add_bf16x8(acc, dx_perm[static_cast<size_t>(r) * nvec + v], 1.f);
+    }
+    float4 a = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    float4 b = make_float4(acc[4], acc[5], acc[6], acc[7]);
+#pragma unroll 8
+    for (int j = 0; j < k; ++j) {
+      const float cj = cs[j];
+      const float4 w0 = __ldg(&w_router[static_cast<size_t>(es[j]) * (d / 4) + 2 * v]);
+      const float4 w1 = __ldg(&w_router[static_cast<size_t>(es[j]) * (d / 4) + 2 * v + 1]);
+      a.x += cj * w0.x; a.y += cj * w0.y; a.z += cj * w0.z; a.w += cj * w0.w;
+      b.x += cj * w1.x; b.y += cj * w1.y; b.z += cj * w1.z; b.w += cj * w1.w;
+    }
+    float4* o = dx + (static_cast<size_t>(t) * nvec + v) * 2;
+    o[0] = a;
+    o[1] = b;
+  }
+}
+
 // dx[t] += sum_j c_j W_r[e_j],  c_j = g_j (dg_j - sum_i g_i dg_i).  One block per token.
 __global__ void __launch_bounds__(kRowThreads) route_bwd_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ gate,
@@ -817,6 +871,16 @@ int launch_dispatch_bwd(const __nv_bfloat16* dx_perm, const int32_t* slot_row, i
                         int k, float* dx, cudaStream_t s) {
   dispatch_bwd_kernel<<<T, kRowThreads, 0, s>>>(
       reinterpret_cast<const uint4*>(dx_perm), slot_row, T, d, k, reinterpret_cast<float4*>(dx));
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_dispatch_route_bwd(const __nv_bfloat16* dx_perm, const int32_t* slot_row,
+                              const int32_t* idx, const float* gate, const float* dgate,
+                              const float* w_router, int T, int d, int E, int k, float* dx,
+                              cudaStream_t s) {
+  dispatch_route_bwd_kernel<<<T, kRowThreads, 0, s>>>(
+      reinterpret_cast<const uint4*>(dx_perm), slot_row, idx, gate, dgate,
+      reinterpret_cast<const float4*>(w_router), T, d, E, k, reinterpret_cast<float4*>(dx));
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -72,6 +72,11 @@ int launch_dgate_finalize(const float* part, int n_tiles, const int32_t* row_slo
                           cudaStream_t s);
 int launch_dispatch_bwd(const __nv_bfloat16* dx_perm, const int32_t* slot_row, int T, int d,
                         int k, float* dx, cudaStream_t s);
+// dispatch backward and router backward in one pass (dx overwritten)
+int launch_dispatch_route_bwd(const __nv_bfloat16* dx_perm, const int32_t* slot_row,
+                              const int32_t* idx, const float* gate, const float* dgate,
+                              const float* w_router, int T, int d, int E, int k, float* dx,
+                              cudaStream_t s);
 int launch_route_bwd(const int32_t* idx, const float* gate, const float* dgate,
                      const float* w_router, int T, int d, int E, int k, float* dx,
                      cudaStream_t s);

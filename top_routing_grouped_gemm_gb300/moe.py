@@ -92,6 +92,7 @@ _SIGS = {
     "moe_aux_loss_workspace_size": (c_sz, [_P]),
     "moe_aux_loss": (ctypes.c_int, [_P, c_vp, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp]),
     "moe_combine_bwd": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "moe_dispatch_route_bwd": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "moe_expert_ffn_bwd_workspace_size": (c_sz, [_P, c_i32]),
     "moe_expert_ffn_bwd": (ctypes.c_int, [_P, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
                                           ctypes.POINTER(moe_lora), ctypes.POINTER(moe_ffn_saved),
@@ -390,6 +391,14 @@ def moe_expert_ffn_bwd(p, rows_max, x_perm, offsets, w_gate, w_up, w_down, lora,
                                     _stream(stream)))
 
 
+def moe_dispatch_route_bwd(p, dx_perm, slot_row, topk_idx, topk_gate, dgate, w_router, dx,
+                           stream=None):
+    _check("moe_dispatch_route_bwd",
+           lib().moe_dispatch_route_bwd(p.c(), _ptr(dx_perm), _ptr(slot_row), _ptr(topk_idx),
+                                        _ptr(topk_gate), _ptr(dgate), _ptr(w_router), _ptr(dx),
+                                        _stream(stream)))
+
+
 def moe_dispatch_bwd(p, dx_perm, slot_row, dx, stream=None):
     _check("moe_dispatch_bwd", lib().moe_dispatch_bwd(p.c(), _ptr(dx_perm), _ptr(slot_row),
                                                       _ptr(dx), _stream(stream)))
@@ -579,8 +588,8 @@ def layer_backward(buf: LayerBuffers, dy, x, w_router, w_gate, w_up, w_down, lor
                    stream=None):
     """Gradient of <dy, y> for the forward last run on ``buf`` (which must have been built
     with train=True): combine backward (dz_perm) -> expert backward (dx_perm, LoRA grads, and
-    the gate gradients from its dh product) -> dispatch backward (expert path of dx) -> router
-    backward (gate path of dx, accumulated)."""
+    the gate gradients from its dh product) -> dispatch and router backward in one pass (the
+    expert path and the gate path of dx)."""
     p = buf.p
     assert buf.train, "LayerBuffers(train=True) keeps what the backward needs"
     moe_combine_bwd(p, dy, None, buf.slot_row, buf.topk_gate, buf.dz_perm, buf.dgate, stream)
@@ -588,6 +597,6 @@ def layer_backward(buf: LayerBuffers, dy, x, w_router, w_gate, w_up, w_down, lor
                        buf.saved, buf.h, buf.dz_perm, buf.dx_perm, buf.grads, buf.ws_bwd,
                        buf.dev_status, stream, row_slot=buf.row_slot, topk_gate=buf.topk_gate,
                        dgate=buf.dgate)
-    moe_dispatch_bwd(p, buf.dx_perm, buf.slot_row, buf.dx, stream)
-    moe_route_bwd(p, buf.topk_idx, buf.topk_gate, buf.dgate, w_router, buf.dx, stream)
+    moe_dispatch_route_bwd(p, buf.dx_perm, buf.slot_row, buf.topk_idx, buf.topk_gate,
+                           buf.dgate, w_router, buf.dx, stream)
     return buf.dx
