@@ -416,7 +416,8 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
     TileCoord tc;
     KRange kr;
     for (int tile = unit0; ok && next_tile<EPI, MSUB, CG>(P, tile, rank, tc, kr); tile += unit_step) {
-      for (int s = 0; ok && s < P.nseg; ++s) {
+      const int nseg = (EPI == EPI_WGRAD) ? 1 : P.nseg;
+      for (int s = 0; ok && s < nseg; ++s) {
         const GemmSeg& sg = P.seg[s];
         const int nkb = (EPI == EPI_WGRAD) ? kr.nkb : sg.nkb;
         for (int kb = 0; kb < nkb; ++kb) {
@@ -552,16 +553,11 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
       if (!w) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_base = tmem_base + acc * C::ACC_COLS;
-      // accumulators already written in this tile (bit b: B operand b's accumulator): a
-      // segment's first MMA into an accumulator that no earlier segment wrote overwrites it
-      uint32_t written = 0;
-      for (int s = 0; ok && s < P.nseg; ++s) {
+      // segment 0 writes every accumulator of the tile first (later segments add to them)
+      const int nseg = (EPI == EPI_WGRAD) ? 1 : P.nseg;
+      for (int s = 0; ok && s < nseg; ++s) {
         const GemmSeg& sg = P.seg[s];
         const int nkb = (EPI == EPI_WGRAD) ? kr.nkb : sg.nkb;
-        uint32_t seg_mask = 0;
-#pragma unroll
-        for (int b = 0; b < NB; ++b) seg_mask |= (sg.b_map[b] >= 0 && nkb > 0) ? (1u << b) : 0u;
-        if (C::SUMB) seg_mask &= 1u;
         for (int kb = 0; kb < nkb; ++kb) {
           if (lane == 0) {
             w = ((CG == 2) ? mbar_wait_cluster(&full[stage], phase, abort_flag)
@@ -598,12 +594,11 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
               const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
 #pragma unroll
               for (int k = 0; k < kBK / 16; ++k) {
-                const bool later = kb > 0 || k > 0;
+                const uint32_t accumulate = (s > 0 || kb > 0 || k > 0) ? 1u : 0u;
                 const uint64_t adesc = smem_desc_sw128(a_addr + k * 32, 16, 1024);
                 if constexpr (C::PAIR_JOIN) {
-                  // one MMA writes both accumulators (a missing operand's half is zeros)
                   const uint64_t bdesc = smem_desc_sw128(a_addr + C::A_BYTES + k * 32, 16, 1024);
-                  umma_bf16<2>(d_base, adesc, bdesc, idp, (later || written != 0u) ? 1u : 0u);
+                  umma_bf16<2>(d_base, adesc, bdesc, idp, accumulate);
                 } else {
 #pragma unroll
                   for (int b = 0; b < NB; ++b) {
@@ -611,13 +606,11 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
                     const uint32_t b_addr = a_addr + C::A_BYTES + b * C::B_BYTES;
                     const uint64_t bdesc = B_MN ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
                                                 : smem_desc_sw128(b_addr + k * 32, 16, 1024);
-                    const uint32_t acc_b =
-                        (later || ((written >> b) & 1u) || (C::SUMB && b > 0)) ? 1u : 0u;
                     if constexpr (C::SUMB) {
                       // the router's lo weight part adds to what the hi part wrote
-                      umma_bf16<2>(d_base, adesc, bdesc, idp, acc_b);
+                      umma_bf16<2>(d_base, adesc, bdesc, idp, (accumulate || b > 0) ? 1u : 0u);
                     } else {
-                      umma_bf16<2>(d_base + b * BN, adesc, bdesc, idp, acc_b);
+                      umma_bf16<2>(d_base + b * BN, adesc, bdesc, idp, accumulate);
                     }
                   }
                 }
@@ -630,7 +623,7 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
               if (k >= ksteps) break;
-              const bool later = kb > 0 || k > 0;
+              const uint32_t accumulate = (s > 0 || kb > 0 || k > 0) ? 1u : 0u;
 #pragma unroll
               for (int sub = 0; sub < MSUB; ++sub) {
                 if (sub >= nsub) break;
@@ -638,12 +631,11 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
                 const uint64_t adesc = A_MN ? smem_desc_sw128(as + k * 2048, 8192, 1024)
                                             : smem_desc_sw128(as + k * 32, 16, 1024);
                 const uint32_t d_sub = d_base + sub * C::ACC_NB * BN;
-                if (kJoinB && sg.b_map[0] >= 0 && sg.b_map[1] >= 0 &&
-                    (written == 0u || written == 3u)) {
+                if (kJoinB && sg.b_map[0] >= 0 && sg.b_map[1] >= 0) {
                   const uint32_t b_addr = a_addr + C::A_BYTES;
                   const uint64_t bdesc = B_MN ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
                                               : smem_desc_sw128(b_addr + k * 32, 16, 1024);
-                  umma_bf16(d_sub, adesc, bdesc, idesc2, (later || written != 0u) ? 1u : 0u);
+                  umma_bf16(d_sub, adesc, bdesc, idesc2, accumulate);
                   continue;
                 }
 #pragma unroll
@@ -652,13 +644,11 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
                   const uint32_t b_addr = a_addr + C::A_BYTES + b * C::B_BYTES;
                   const uint64_t bdesc = B_MN ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
                                               : smem_desc_sw128(b_addr + k * 32, 16, 1024);
-                  const uint32_t acc_b =
-                      (later || ((written >> b) & 1u) || (C::SUMB && b > 0)) ? 1u : 0u;
                   if constexpr (C::SUMB) {
                     // the second B adds to what the first wrote in this k step
-                    umma_bf16(d_sub, adesc, bdesc, idesc, acc_b);
+                    umma_bf16(d_sub, adesc, bdesc, idesc, (accumulate || b > 0) ? 1u : 0u);
                   } else {
-                    umma_bf16(d_sub + b * BN, adesc, bdesc, idesc, acc_b);
+                    umma_bf16(d_sub + b * BN, adesc, bdesc, idesc, accumulate);
                   }
                 }
               }
@@ -668,7 +658,6 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
           __syncwarp();
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
-        written |= seg_mask;
       }
       if (!ok) break;
       if (lane == 0) umma_commit<CG>(&acc_full[acc]);

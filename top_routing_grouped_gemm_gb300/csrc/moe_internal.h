@@ -74,7 +74,7 @@ struct GemmParams {
   CUtensorMap maps[kMaxMaps];
   int nmaps;
   GemmSeg seg[kMaxSegs];
-  int nseg;
+  int nseg;  // segment 0 must feed every accumulator: later segments add to what it wrote
   // M grouping.  Grouped: rows of group g are [group_off[g], group_off[g+1]) and its
   // m-tiles are numbered tile_off[g] .. tile_off[g+1]-1; B's third coordinate is g.
   // Dense (group_off == nullptr): one group of M rows, m_tiles tiles.
