@@ -759,8 +759,8 @@ int moe_expert_ffn_bwd(const moe_problem* p, int32_t rows_max, const moe_bf16* x
   float* gate_parts = cv.take<float>(static_cast<size_t>(rows_max) * dh_tiles);
   MOE_CUDA(launch_tile_schedule(offsets, E, rows_max, tile_off, pair_off, dev_status, stream));
   int launches = 1;
-  // 256-row tiles: dh only for big groups (its SwiGLU-backward epilogue is heavy and stays
-  // exposed with one accumulator); dx (plain store epilogue) also for two-tile groups
+  // dh and dx run on CTA pairs for big groups; for two-tile groups dx (plain store epilogue)
+  // takes 256-row tiles and dh (heavy SwiGLU-backward epilogue) stays on 128-row tiles
   const int shape_dh = expert_tile_shape(p, rows_max, false, kGemmDh);
   const int shape_dx = expert_tile_shape(p, rows_max, false, kGemmDx);
   auto grouped = [&](GemmParams& P) {
