@@ -533,6 +533,10 @@ def kernel_model(cfg, kept, nonempty, train, gather, fused_combine=False):
             m["wgrad"] = (kept * (2 * d + 3 * F) * 2 + kept * 5 * r * 2
                           + E * r * (3 * d + 3 * F) * 4,
                           kept * 2.0 * r * (3 * d + 3 * F))
+        # dz_perm = g dy (dy read, kept rows written; slot maps and gates read, dgate zeroed)
+        m["combine_bwd"] = (T * d * 2 + kept * d * 2 + T * k * 12, 0.0)
+        # dx = sum of the kept dx_perm rows + the router path (W_r read once, fp32 dx written)
+        m["dispatch_route_bwd"] = (kept * d * 2 + T * k * 16 + E * d * 4 + T * d * 4, 0.0)
     return m
 
 
@@ -727,7 +731,8 @@ def run_workload(name, ctx, with_cpu):
         kernels = ["router_gemm", "topk", "dispatch", "gateup_gemm", "down_gemm"] + \
             ([] if fuse_combine else ["combine"])
         if train:
-            kernels += ["bwd_dh_gemm", "bwd_dx_gemm"] + (["wgrad"] if cfg.r else [])
+            kernels += ["combine_bwd", "bwd_dh_gemm", "bwd_dx_gemm"] + \
+                (["wgrad"] if cfg.r else []) + ["dispatch_route_bwd"]
 
     for _ in range(max(args.warmup, 3)):
         step()

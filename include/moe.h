@@ -407,7 +407,9 @@ enum moe_kernel_id {
   MOE_KERNEL_GDR_CHUNK = 9,     /* linear attention: per-chunk factors           */
   MOE_KERNEL_GDR_SCAN = 10,     /* linear attention: state scan over chunks      */
   MOE_KERNEL_GDR_BWD = 11,      /* linear attention: per-chunk backward          */
-  MOE_KERNEL_COUNT = 12
+  MOE_KERNEL_COMBINE_BWD = 12,  /* combine backward (dz_perm, gate gradients)    */
+  MOE_KERNEL_DISPATCH_ROUTE_BWD = 13, /* dx from dx_perm and the router path      */
+  MOE_KERNEL_COUNT = 14
 };
 int moe_set_kernel_events(int kernel_id, void* event_before, void* event_after);
 long long moe_launch_count(void);

@@ -694,10 +694,13 @@ int moe_combine_bwd(const moe_problem* p, const moe_bf16* dy, const moe_bf16* y_
     return MOE_ERR_INVALID_ARG;
   if (!al16(dy) || (y_perm && !al16(y_perm)) || !al16(dz_perm)) return MOE_ERR_UNSUPPORTED;
   count_launches(1);
-  return cuda_status(launch_combine_bwd(
+  mark_before(MOE_KERNEL_COMBINE_BWD, stream);
+  const int st = cuda_status(launch_combine_bwd(
       reinterpret_cast<const __nv_bfloat16*>(dy), reinterpret_cast<const __nv_bfloat16*>(y_perm),
       slot_row, topk_gate, p->T, p->d, p->k, reinterpret_cast<__nv_bfloat16*>(dz_perm), dgate,
       stream));
+  mark_after(MOE_KERNEL_COMBINE_BWD, stream);
+  return st;
 }
 
 size_t moe_expert_ffn_bwd_workspace_size(const moe_problem* p, int32_t rows_max) {
@@ -936,9 +939,12 @@ int moe_dispatch_route_bwd(const moe_problem* p, const moe_bf16* dx_perm,
     return MOE_ERR_INVALID_ARG;
   if (!al16(dx_perm) || !al16(w_router) || !al16(dx)) return MOE_ERR_UNSUPPORTED;
   count_launches(1);
-  return cuda_status(launch_dispatch_route_bwd(reinterpret_cast<const __nv_bfloat16*>(dx_perm),
-                                               slot_row, topk_idx, topk_gate, dgate, w_router,
-                                               p->T, p->d, p->E, p->k, dx, stream));
+  mark_before(MOE_KERNEL_DISPATCH_ROUTE_BWD, stream);
+  const int st = cuda_status(launch_dispatch_route_bwd(
+      reinterpret_cast<const __nv_bfloat16*>(dx_perm), slot_row, topk_idx, topk_gate, dgate,
+      w_router, p->T, p->d, p->E, p->k, dx, stream));
+  mark_after(MOE_KERNEL_DISPATCH_ROUTE_BWD, stream);
+  return st;
 }
 
 // ------------------------------------------------------------------------ instrumentation
