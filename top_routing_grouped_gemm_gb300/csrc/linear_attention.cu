@@ -293,13 +293,16 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
 // S = gamma_C S + sum_j exp(G_C - G_j) w_j k^_j^T.  S_chunks (optional) receives the state
 // at every chunk start (the backward's checkpoints).
 //
-// Two phases per chunk: W, then the output and the state update together (the update
-// writes the other of two state buffers, so both read the chunk-start state without a
-// barrier between them).  The chunk tiles do not depend on the state, so they stream in with
-// cp.async while the other phase computes, one shared buffer per tile: Y, the U slice and
-// the log decays (phase 1) are reloaded for the next chunk right after phase 1, Q^, P and K^
-// (phase 2) right after phase 2; each phase waits only for the copies issued one phase
-// earlier (wait_group 1: the later group may still be in flight).
+// Two phases per chunk: W and Q^ S^T (both products with the chunk-start state), then the
+// output and the state update together (the update writes the other of two state buffers,
+// so both read the chunk-start state without a barrier between them).  The chunk tiles do
+// not depend on the state, so they stream in with cp.async while the other phase computes,
+// one shared buffer per tile: Y, Q^, the U slice and the log decays (phase 1) are reloaded
+// for the next chunk right after phase 1, P and K^ (phase 2) right after phase 2; each phase
+// waits only for the copies issued one phase earlier (wait_group 1: the later group may
+// still be in flight).  Each thread computes blocks of outputs from float4 shared reads that
+// a warp shares (a few distinct 16-byte pieces per read), so that shared-memory bandwidth
+// is not what the chain of chunks waits on.
 __device__ __forceinline__ void la_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void la_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
@@ -327,6 +330,7 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
     __nv_bfloat16* __restrict__ o, float* __restrict__ ST, float* __restrict__ Schk) {
   constexpr int LT = ScanLd<DK>::T, LP = ScanLd<DK>::P;
   constexpr int LS = ScanLd<DK>::T;  // state rows: 16-byte aligned (read as float4)
+  constexpr int LW = kC + 4;         // rows of W^T (one per value row, over the chunk's tokens)
   extern __shared__ float4 sm4[];
   float* sm = reinterpret_cast<float*>(sm4);
   float* sQ = sm;                   // [C][LT]
@@ -336,26 +340,25 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
   float* sU = sP + kC * LP;         // [C][RS] U slice
   float* sGr = sU + kC * kRS;       // [C] log decays
   float* sSb = sGr + kC;            // 2 x [RS][LS] state rows (ping-pong over chunks)
-  float* sW = sSb + 2 * kRS * LS;   // [C][4][4]: W[j][q + 4u] at j*16 + 4q + u
-  float* sWd = sW + kC * kRS;       // the same, decayed to the chunk end
-  static_assert(kC * kRS == 4 * 256, "W / O tiling: 4 outputs per thread");
-  static_assert(kRS == 16 && DK % 4 == 0, "thread tiling");
+  float* sWT = sSb + 2 * kRS * LS;  // [RS][LW]: W^T
+  float* sWd = sWT + kRS * LW;      // [C][RS]: W decayed to the chunk end
+  static_assert(kRS == 16 && kC == 64 && DK % 32 == 0, "thread tiling");
   const int r0 = blockIdx.x * kRS, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
   const size_t bh = static_cast<size_t>(b) * H + h;
-  auto issue_a = [&](int c) {  // Y, U slice, log decays (phase 1)
+  auto issue_a = [&](int c) {  // Y, Q^, U slice, log decays (phase 1)
     if (c < nch) {
       const size_t cid = bh * nch + c;
       tile_async<kC, DK, LT>(sY, Y + cid * kC * DK, DK, tid);
+      tile_async<kC, DK, LT>(sQ, Qh + cid * kC * DK, DK, tid);
       tile_async<kC, kRS, kRS>(sU, U + cid * kC * DV + r0, DV, tid);
       tile_async<1, kC, kC>(sGr, Gc + cid * kC, kC, tid);
     }
     la_commit();
   };
-  auto issue_b = [&](int c) {  // Q^, P, K^ (phase 2)
+  auto issue_b = [&](int c) {  // P, K^ (phase 2)
     if (c < nch) {
       const size_t cid = bh * nch + c;
-      tile_async<kC, DK, LT>(sQ, Qh + cid * kC * DK, DK, tid);
       tile_async<kC, kC, LP>(sP, Pm + cid * kC * kC, kC, tid);
       tile_async<kC, DK, LT>(sK, Kh + cid * kC * DK, DK, tid);
     }
@@ -367,114 +370,136 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
   }
   issue_a(0);
   issue_b(0);
-  // W / O tiling: token row i, value rows q, q + 4, q + 8, q + 12 (interleaved, so that the
-  // four 16-byte state reads of a quarter warp fall in different banks)
-  const int i = tid >> 2, q = tid & 3;
-  // state update tiling: columns 4 xg .. 4 xg + 3, value rows rp * RPG .. (rp: the warp's
-  // row group, so its row weights are broadcast reads)
-  constexpr int XG = DK / 4;                 // float4 column groups
-  constexpr int RP = 256 / XG;               // row groups (8 for DK 128, 16 for 64)
-  constexpr int RPG = kRS / RP;              // rows per group (2 for DK 128, 1 for 64)
-  static_assert(RPG >= 1 && RP * RPG == kRS, "state update tiling");
-  const int xg = tid % XG, rp = tid / XG;
+  // Phases 1 and 2a: this thread's token rows i0 = tid / 8 and i1 = i0 + 32 and value rows
+  // c0 = tid % 8 and c1 = c0 + 8 (a warp reads four token rows and eight state rows per step:
+  // one shared-memory wavefront each).
+  const int cq = tid & 7, i0 = tid >> 3, i1 = i0 + 32;
+  const int c0 = cq, c1 = cq + 8;
+  // Phase 2b: value rows rs * RPL .. + RPL - 1, float4 column group cg (a warp reads GW
+  // column groups of K^ and RSEL row pieces of the decayed W per token: one wavefront each).
+  constexpr int GW = DK / 32;          // column groups per warp
+  constexpr int RSEL = 32 / GW;        // row selectors per warp
+  constexpr int RPL = kRS / RSEL;      // rows per lane (2 for DK 128, 1 for 64)
+  static_assert(RPL * RSEL == kRS && (RPL == 1 || RPL == 2), "state update tiling");
+  const int lane = tid & 31, warp = tid >> 5;
+  const int cg = warp * GW + lane / RSEL, rs = lane % RSEL;
   for (int c = 0; c < nch; ++c) {
     const size_t cid = bh * nch + c;
     const float* sS = sSb + (c & 1) * kRS * LS;      // state at the chunk start
     float* sSn = sSb + ((c & 1) ^ 1) * kRS * LS;     // state at the chunk end
-    la_wait1();        // Y, U, decays of chunk c
+    la_wait1();        // Y, Q^, U, decays of chunk c
     __syncthreads();   // (everyone's copies; the previous chunk is done with every tile)
-    const float gi = sGr[i], gC = sGr[kC - 1];
-    const float gam_i = __expf(gi), dec_i = __expf(gC - gi), gam_C = __expf(gC);
+    const float gC = sGr[kC - 1];
+    const float gam_C = __expf(gC);
     if (Schk)
       for (int e = tid; e < kRS * DK; e += 256) {
         const int r = e / DK, x = e - r * DK;
         Schk[(cid * DV + r0 + r) * DK + x] = sS[r * LS + x];
       }
-    // phase 1: W = U - Y S^T ([C][RS])
+    // phase 1: Y S^T and Q^ S^T for rows i0, i1 and value rows c0, c1; W = U - Y S^T
+    float oq[2][2];
     {
-      float w[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) w[u] = sU[i * kRS + q + 4 * u];
-      const float4* yi = reinterpret_cast<const float4*>(sY + i * LT);
+      float gy[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, gq[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      const float4* y0 = reinterpret_cast<const float4*>(sY + i0 * LT);
+      const float4* y1 = reinterpret_cast<const float4*>(sY + i1 * LT);
+      const float4* q0 = reinterpret_cast<const float4*>(sQ + i0 * LT);
+      const float4* q1 = reinterpret_cast<const float4*>(sQ + i1 * LT);
+      const float4* s0 = reinterpret_cast<const float4*>(sS + c0 * LS);
+      const float4* s1 = reinterpret_cast<const float4*>(sS + c1 * LS);
 #pragma unroll 4
       for (int x4 = 0; x4 < DK / 4; ++x4) {
-        const float4 y = yi[x4];
+        const float4 a0 = y0[x4], a1 = y1[x4], b0 = q0[x4], b1 = q1[x4];
+        const float4 u0 = s0[x4], u1 = s1[x4];
+        gy[0][0] += a0.x * u0.x + a0.y * u0.y + a0.z * u0.z + a0.w * u0.w;
+        gy[0][1] += a0.x * u1.x + a0.y * u1.y + a0.z * u1.z + a0.w * u1.w;
+        gy[1][0] += a1.x * u0.x + a1.y * u0.y + a1.z * u0.z + a1.w * u0.w;
+        gy[1][1] += a1.x * u1.x + a1.y * u1.y + a1.z * u1.z + a1.w * u1.w;
+        gq[0][0] += b0.x * u0.x + b0.y * u0.y + b0.z * u0.z + b0.w * u0.w;
+        gq[0][1] += b0.x * u1.x + b0.y * u1.y + b0.z * u1.z + b0.w * u1.w;
+        gq[1][0] += b1.x * u0.x + b1.y * u0.y + b1.z * u0.z + b1.w * u0.w;
+        gq[1][1] += b1.x * u1.x + b1.y * u1.y + b1.z * u1.z + b1.w * u1.w;
+      }
+      const int ir[2] = {i0, i1}, cr[2] = {c0, c1};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float4 sv = reinterpret_cast<const float4*>(sS + (q + 4 * u) * LS)[x4];
-          w[u] -= y.x * sv.x + y.y * sv.y + y.z * sv.z + y.w * sv.w;
+      for (int a = 0; a < 2; ++a) {
+        const float gi = sGr[ir[a]];
+        const float gam_i = __expf(gi), dec_i = __expf(gC - gi);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float w = sU[ir[a] * kRS + cr[q]] - gy[a][q];
+          sWT[cr[q] * LW + ir[a]] = w;
+          sWd[ir[a] * kRS + cr[q]] = w * dec_i;
+          oq[a][q] = gam_i * gq[a][q];
         }
       }
-      *reinterpret_cast<float4*>(sW + i * kRS + 4 * q) = make_float4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<float4*>(sWd + i * kRS + 4 * q) =
-          make_float4(w[0] * dec_i, w[1] * dec_i, w[2] * dec_i, w[3] * dec_i);
     }
-    __syncthreads();   // W is complete; Y, U and the decays are free
+    __syncthreads();   // W is complete; Y, Q^, U and the decays are free
     issue_a(c + 1);
-    la_wait1();        // Q^, P, K^ of chunk c
+    la_wait1();        // P, K^ of chunk c
     __syncthreads();
     // phase 2a: O = scale (gamma_i Q^_i . S_r + sum_{j<=i} P_ij w_jr)  (P is zero above the
-    // diagonal)
+    // diagonal; i0 <= 4 * warp + 3 and i1 < 4 * warp + 36, so whole 4-token steps suffice)
     {
-      const int t = c * kC + i;
-      float a[4] = {0.f, 0.f, 0.f, 0.f};
-      const float4* qi = reinterpret_cast<const float4*>(sQ + i * LT);
-#pragma unroll 4
-      for (int x4 = 0; x4 < DK / 4; ++x4) {
-        const float4 qv = qi[x4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float4 sv = reinterpret_cast<const float4*>(sS + (q + 4 * u) * LS)[x4];
-          a[u] += qv.x * sv.x + qv.y * sv.y + qv.z * sv.z + qv.w * sv.w;
+      const float* p0 = sP + i0 * LP;
+      const float* p1 = sP + i1 * LP;
+      const float* w0 = sWT + c0 * LW;
+      const float* w1 = sWT + c1 * LW;
+      for (int j0 = 0; j0 <= i1; j0 += 4) {
+        const float4 wa = *reinterpret_cast<const float4*>(w0 + j0);
+        const float4 wb = *reinterpret_cast<const float4*>(w1 + j0);
+        const float4 pb = *reinterpret_cast<const float4*>(p1 + j0);
+        oq[1][0] += pb.x * wa.x + pb.y * wa.y + pb.z * wa.z + pb.w * wa.w;
+        oq[1][1] += pb.x * wb.x + pb.y * wb.y + pb.z * wb.z + pb.w * wb.w;
+        if (j0 <= i0) {
+          const float4 pa = *reinterpret_cast<const float4*>(p0 + j0);
+          oq[0][0] += pa.x * wa.x + pa.y * wa.y + pa.z * wa.z + pa.w * wa.w;
+          oq[0][1] += pa.x * wb.x + pa.y * wb.y + pa.z * wb.z + pa.w * wb.w;
         }
       }
+      const int ir[2] = {i0, i1}, cr[2] = {c0, c1};
 #pragma unroll
-      for (int u = 0; u < 4; ++u) a[u] *= gam_i;
-      const float* pi = sP + i * LP;
-      for (int j0 = 0; j0 <= i; j0 += 4) {
-        const float4 pv = *reinterpret_cast<const float4*>(pi + j0);
-        const float pj[4] = {pv.x, pv.y, pv.z, pv.w};
+      for (int a = 0; a < 2; ++a) {
+        const int t = c * kC + ir[a];
+        if (t < T) {
+          __nv_bfloat16* orow = o + ((static_cast<size_t>(b) * T + t) * H + h) * DV + r0;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const float4 wv = *reinterpret_cast<const float4*>(sW + (j0 + jj) * kRS + 4 * q);
-          a[0] += pj[jj] * wv.x;
-          a[1] += pj[jj] * wv.y;
-          a[2] += pj[jj] * wv.z;
-          a[3] += pj[jj] * wv.w;
+          for (int q = 0; q < 2; ++q) orow[cr[q]] = __float2bfloat16_rn(scale * oq[a][q]);
         }
-      }
-      if (t < T) {
-        __nv_bfloat16* orow = o + ((static_cast<size_t>(b) * T + t) * H + h) * DV + r0 + q;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) orow[4 * u] = __float2bfloat16_rn(scale * a[u]);
       }
     }
     // phase 2b (same phase: it writes the other state buffer):
     // S_r = gamma_C S_r + sum_j (gamma_C / gamma_j) w_jr k^_j
     {
-      float4 acc[RPG];
+      float4 acc[RPL];
 #pragma unroll
-      for (int v = 0; v < RPG; ++v) {
-        const float4 sv = reinterpret_cast<const float4*>(sS + (rp * RPG + v) * LS)[xg];
+      for (int v = 0; v < RPL; ++v) {
+        const float4 sv = reinterpret_cast<const float4*>(sS + (rs * RPL + v) * LS)[cg];
         acc[v] = make_float4(gam_C * sv.x, gam_C * sv.y, gam_C * sv.z, gam_C * sv.w);
       }
+#pragma unroll 8
       for (int j = 0; j < kC; ++j) {
-        const float4 kv = reinterpret_cast<const float4*>(sK + j * LT)[xg];
+        const float4 kv = reinterpret_cast<const float4*>(sK + j * LT)[cg];
+        float wd[RPL];
+        if constexpr (RPL == 2) {
+          const float2 w2 = *reinterpret_cast<const float2*>(sWd + j * kRS + 2 * rs);
+          wd[0] = w2.x;
+          wd[1] = w2.y;
+        } else {
+          wd[0] = sWd[j * kRS + rs];
+        }
 #pragma unroll
-        for (int v = 0; v < RPG; ++v) {
-          const int r = rp * RPG + v;
-          const float wd = sWd[j * kRS + 4 * (r & 3) + (r >> 2)];
-          acc[v].x += wd * kv.x;
-          acc[v].y += wd * kv.y;
-          acc[v].z += wd * kv.z;
-          acc[v].w += wd * kv.w;
+        for (int v = 0; v < RPL; ++v) {
+          acc[v].x += wd[v] * kv.x;
+          acc[v].y += wd[v] * kv.y;
+          acc[v].z += wd[v] * kv.z;
+          acc[v].w += wd[v] * kv.w;
         }
       }
 #pragma unroll
-      for (int v = 0; v < RPG; ++v)
-        reinterpret_cast<float4*>(sSn + (rp * RPG + v) * LS)[xg] = acc[v];
+      for (int v = 0; v < RPL; ++v)
+        reinterpret_cast<float4*>(sSn + (rs * RPL + v) * LS)[cg] = acc[v];
     }
-    __syncthreads();   // Q^, P and K^ are free (the next chunk's first barrier orders the state)
+    __syncthreads();   // P and K^ are free (the next chunk's first barrier orders the state)
     issue_b(c + 1);
   }
   __syncthreads();
@@ -490,7 +515,7 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
 template <int DK>
 constexpr size_t scan_smem_bytes() {
   return (3 * kC * ScanLd<DK>::T + kC * ScanLd<DK>::P + kC * kRS + kC +
-          2 * kRS * ScanLd<DK>::T + 2 * kC * kRS) * sizeof(float);
+          2 * kRS * ScanLd<DK>::T + kRS * (kC + 4) + kC * kRS) * sizeof(float);
 }
 
 // ---------------------------------------------------------------------------- backward
