@@ -562,9 +562,23 @@ def la_flops_per_chunk(dk, dv, C=64):
     return 2.0 * (chunk + scan)
 
 
+def la_bwd_flops_per_chunk(dk, dv, C=64):
+    """Multiply-adds of the backward of one 64-token chunk of one head, x 2: the chunk factors
+    rebuilt (as in the forward), the state-gradient scan (dW = s P^T dO + E dS1^T, and
+    dS0 = gamma_C dS1 + s dO^T diag(gamma) Q^ - dW^T Y), and the chunk-local backward
+    (W = U - Y S0^T, dP = s dO W^T, dQ^ and dK^ from Gam . dP and from S0 / dS1, dBv = A^-T dW,
+    dBk = -dBv S0, dM from dBv U^T + dBk Y^T, (Z + Z^T) K^)."""
+    tri = C * (C + 1) // 2
+    factors = 2 * tri * dk + C ** 3 // 6 + tri * dk + tri * dv
+    scan = tri * dv + 3 * C * dk * dv
+    local = 4 * C * dk * dv + 3 * tri * dv + 3 * tri * dk + C * C * dk
+    return 2.0 * (factors + scan + local)
+
+
 def run_linear_attention(name, ctx):
-    """The chunked gated delta-rule linear attention forward on its workload; K steps
-    replayed as one CUDA graph, per-kernel CUDA events from a host-launched pass."""
+    """The chunked gated delta-rule linear attention on its workload: the forward, and the
+    training step (the forward keeping every chunk-start state, then the backward); K steps
+    of each replayed as one CUDA graph, per-kernel CUDA events from a host-launched pass."""
     import torch
     from top_routing_grouped_gemm_gb300 import moe, synth
     args = ctx.args
@@ -618,6 +632,71 @@ def run_linear_attention(name, ctx):
     peak = fp32_alu_peak_tflops()
     tot_us = sum(us.values())
     achieved = flops / (tot_us * 1e-6) / 1e12
+    peak_src = "fp32 FMA pipes: 152 SMs x 128 lanes x 2 x 2.07 GHz"
+
+    # training step: the forward keeping every chunk-start state, then the backward
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1000 + ctx.rank)
+    d_o = torch.randn((B, T, H, dv), generator=gen, device="cuda").to(torch.bfloat16)
+    Schk = torch.empty((B, H, nch, dv, dk), dtype=torch.float32, device="cuda")
+    dq = torch.empty((B, T, H, dk), dtype=torch.float32, device="cuda")
+    dkk = torch.empty_like(dq)
+    dvv = torch.empty((B, T, H, dv), dtype=torch.float32, device="cuda")
+    dbeta = torch.empty((B, T, H), dtype=torch.float32, device="cuda")
+    dg = torch.empty_like(dbeta)
+    dS0 = torch.empty((B, H, dv, dk), dtype=torch.float32, device="cuda")
+    ws_b = torch.empty(moe.moe_gdr_backward_workspace_size(B, T, H, dk, dv), dtype=torch.uint8,
+                       device="cuda")
+
+    def train_step():
+        moe.moe_gdr_forward(B, T, H, dk, dv, inp["q"], inp["k"], inp["v"], inp["beta"],
+                            inp["g"], inp["S0"], dk ** -0.5, o, ST, Schk, ws)
+        moe.moe_gdr_backward(B, T, H, dk, dv, inp["q"], inp["k"], inp["v"], inp["beta"],
+                             inp["g"], dk ** -0.5, d_o, None, Schk, dq, dkk, dvv, dbeta, dg, dS0,
+                             ws_b)
+    for _ in range(max(args.warmup, 3)):
+        train_step()
+    torch.cuda.synchronize()
+    tk = kernels + ["gdr_bwd_factors", "gdr_bwd_scan", "gdr_bwd"]
+    tev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)] for n in tk}
+    for n in tk:
+        for a, b in tev[n]:
+            a.record()
+            b.record()
+    tgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(tgraph):
+        for _ in range(K):
+            train_step()
+    torch.cuda.synchronize()
+    tclocks = ClockSampler(ctx.local)
+    ctx.barrier()
+    s0.record()
+    tgraph.replay()
+    s1.record()
+    torch.cuda.synchronize()
+    ctx.barrier()
+    tclocks.stop()
+    for i in range(K):
+        for n in tk:
+            moe.moe_set_kernel_events(n, tev[n][i][0], tev[n][i][1])
+        train_step()
+    for n in tk:
+        moe.moe_set_kernel_events(n, None, None)
+    torch.cuda.synchronize()
+    t_ms = max_over_ranks(s0.elapsed_time(s1) / K, ctx.world, "cuda")
+    t_us = {n: 1000.0 * sum(a.elapsed_time(b) for a, b in tev[n]) / K for n in tk}
+    t_flops = flops + la_bwd_flops_per_chunk(dk, dv) * nch * B * H
+    t_ach = t_flops / (sum(t_us.values()) * 1e-6) / 1e12
+    train = {"value": job_throughput(ctx.world, B * T, t_ms), "unit": "tokens/s",
+             "ms_per_step": t_ms, "cuda_graph": True, "gpu_launches": 5 * K,
+             "what": "forward (chunk-start states kept) + backward to q, k, v, beta, g, S0",
+             "kernels": {n: {"us": t_us[n]} for n in tk},
+             "roofline": {"kernel": "all five", "bound": "alu", "achieved": t_ach,
+                          "peak": peak, "unit": "TFLOP/s", "frac": t_ach / peak,
+                          "traffic": None, "algorithmic_flops": t_flops,
+                          "peak_source": peak_src},
+             "clocks": tclocks.summary()}
     return {"value": job_throughput(ctx.world, B * T, ms), "unit": "tokens/s",
             "ms_per_step": ms, "cuda_graph": True, "gpu_launches": 2 * K,
             "config": {"workload": f"{cfg.name}: gated delta-rule linear attention, B={B} "
@@ -627,8 +706,8 @@ def run_linear_attention(name, ctx):
             "roofline": {"kernel": "gdr_chunk + gdr_scan", "bound": "alu",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": None,
-                         "algorithmic_flops": flops,
-                         "peak_source": "fp32 FMA pipes: 152 SMs x 128 lanes x 2 x 2.07 GHz"},
+                         "algorithmic_flops": flops, "peak_source": peak_src},
+            "train": train,
             "clocks": clocks.summary()}
 
 

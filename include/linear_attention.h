@@ -23,8 +23,8 @@
  *   64-token chunk (what a backward pass restarts from).
  * Supported: dk and dv in {64, 128}; any T >= 1 (the last chunk may be partial).  A zero
  * q or k row is treated as a zero vector (no division by zero).  q, k, v, the workspace (and
- * the backward's d_o) must be 16-byte aligned (the kernels read them in 16-byte pieces), else
- * MOE_ERR_UNSUPPORTED.
+ * the backward's d_o and S_chunks) must be 16-byte aligned (the kernels read them in 16-byte
+ * pieces), else MOE_ERR_UNSUPPORTED.
  */
 #ifndef MOE_LINEAR_ATTENTION_H
 #define MOE_LINEAR_ATTENTION_H

@@ -409,7 +409,9 @@ enum moe_kernel_id {
   MOE_KERNEL_GDR_BWD = 11,      /* linear attention: per-chunk backward          */
   MOE_KERNEL_COMBINE_BWD = 12,  /* combine backward (dz_perm, gate gradients)    */
   MOE_KERNEL_DISPATCH_ROUTE_BWD = 13, /* dx from dx_perm and the router path      */
-  MOE_KERNEL_COUNT = 14
+  MOE_KERNEL_GDR_BWD_FACTORS = 14, /* linear attention backward: chunk factors again */
+  MOE_KERNEL_GDR_BWD_SCAN = 15, /* linear attention backward: state-gradient scan  */
+  MOE_KERNEL_COUNT = 16
 };
 int moe_set_kernel_events(int kernel_id, void* event_before, void* event_after);
 long long moe_launch_count(void);

@@ -191,7 +191,9 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
   __syncthreads();
   // A^-1 (unit lower triangular), one row per step: X_i = e_i - sum_{j<i} A_ij X_j, the 64
   // columns in parallel with 4 threads per column (each a quarter of the j range, combined by
-  // shuffles within the 4 lanes)
+  // shuffles within the 4 lanes).  A column only reads its own earlier rows, written by its
+  // own four lanes, so the steps are ordered within the warp (the block barrier before Y
+  // publishes the whole inverse).
   {
     const int col = tid >> 2, part = tid & 3;
     for (int i = 0; i < kC; ++i) {
@@ -200,7 +202,7 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
       x += __shfl_xor_sync(0xffffffffu, x, 1);
       x += __shfl_xor_sync(0xffffffffu, x, 2);
       if (part == 0) sI[i * LC + col] = i < col ? 0.f : (i == col ? 1.f : x);
-      __syncthreads();
+      __syncwarp();
     }
   }
   // q^, k^ out for the scan; then K^ rows scaled by beta gamma in place
@@ -664,9 +666,115 @@ constexpr size_t bwd_scan_smem_bytes() {
           2 * kC * kRS) * sizeof(float);
 }
 
+// Register-tiled products of the per-chunk backward, for 256 threads: thread (ti, tj) =
+// (tid / 16, tid % 16) owns rows ti + 16 u (u < M / 16) and columns tj + 16 c (c < N / 16)
+// of an M x N result and adds its sums to acc[u][c] (k ascending, one fp32 chain per output).
+//   mm_nn:  A(m, k) and B(k, n) element callables (B's columns are consecutive across the
+//           16 lanes of a row group, A's rows are two per warp: broadcast reads)
+//   mm_nt4: A and B given by k-contiguous rows (shared or global, 16-byte aligned), read 16
+//           bytes at a time
+template <int M, int N, class FA, class FB>
+__device__ __forceinline__ void mm_nn(int K, FA A, FB B, float (&acc)[M / 16][N / 16]) {
+  const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
+#pragma unroll 2
+  for (int k = 0; k < K; ++k) {
+    float a[M / 16], bb[N / 16];
+#pragma unroll
+    for (int u = 0; u < M / 16; ++u) a[u] = A(ti + 16 * u, k);
+#pragma unroll
+    for (int c = 0; c < N / 16; ++c) bb[c] = B(k, tj + 16 * c);
+#pragma unroll
+    for (int u = 0; u < M / 16; ++u)
+#pragma unroll
+      for (int c = 0; c < N / 16; ++c) acc[u][c] += a[u] * bb[c];
+  }
+}
+
+template <int M, int N, class FA, class FB>
+__device__ __forceinline__ void mm_nt4(int K, FA Arow, FB Brow, float (&acc)[M / 16][N / 16]) {
+  const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
+  const float* ar[M / 16];
+  const float* br[N / 16];
+#pragma unroll
+  for (int u = 0; u < M / 16; ++u) ar[u] = Arow(ti + 16 * u);
+#pragma unroll
+  for (int c = 0; c < N / 16; ++c) br[c] = Brow(tj + 16 * c);
+#pragma unroll 2
+  for (int k = 0; k < K; k += 4) {
+    float4 a[M / 16], bb[N / 16];
+#pragma unroll
+    for (int u = 0; u < M / 16; ++u) a[u] = *reinterpret_cast<const float4*>(ar[u] + k);
+#pragma unroll
+    for (int c = 0; c < N / 16; ++c) bb[c] = *reinterpret_cast<const float4*>(br[c] + k);
+#pragma unroll
+    for (int u = 0; u < M / 16; ++u)
+#pragma unroll
+      for (int c = 0; c < N / 16; ++c)
+        acc[u][c] += a[u].x * bb[c].x + a[u].y * bb[c].y + a[u].z * bb[c].z + a[u].w * bb[c].w;
+  }
+}
+
+template <int M, int N>
+__device__ __forceinline__ void mm_zero(float (&acc)[M / 16][N / 16]) {
+#pragma unroll
+  for (int u = 0; u < M / 16; ++u)
+#pragma unroll
+    for (int c = 0; c < N / 16; ++c) acc[u][c] = 0.f;
+}
+
+// mm_nn with B in global memory, staged through shared memory 16 k rows at a time, so that
+// the CTA reads every element of B once (not once per row group): B(k, n) = Bg[k * ldb + n],
+// or Bg[n * ldb + k] with TRANS.  stage: 16 x (N + 4) floats.  Every thread of the block
+// must call it (it synchronises the block).
+template <int M, int N, bool TRANS, class FA>
+__device__ __forceinline__ void mm_nn_staged(int K, FA A, const float* __restrict__ Bg, int ldb,
+                                             float* stage, float (&acc)[M / 16][N / 16]) {
+  constexpr int LSG = N + 4;
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int e = threadIdx.x; e < 16 * N; e += 256) {
+      int kk, n;
+      if (TRANS) {
+        n = e >> 4;
+        kk = e & 15;
+      } else {
+        kk = e / N;
+        n = e - kk * N;
+      }
+      stage[kk * LSG + n] = TRANS ? __ldg(&Bg[static_cast<size_t>(n) * ldb + k0 + kk])
+                                  : __ldg(&Bg[static_cast<size_t>(k0 + kk) * ldb + n]);
+    }
+    __syncthreads();
+    mm_nn<M, N>(16, [&](int m, int k) { return A(m, k0 + k); },
+                [&](int k, int n) { return stage[k * LSG + n]; }, acc);
+    __syncthreads();
+  }
+}
+
+// sum over the 16 lanes of a row group (tj = lane % 16), every lane gets the total
+__device__ __forceinline__ float rowgroup_sum(float x) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+template <int DK, int DV>
+struct BwdLd {
+  static constexpr int K = DK + 4, V = DV + 4, X = (DK > DV ? DK : DV) + 4, C = kC + 4;
+};
+
+template <int DK, int DV>
+constexpr size_t bwd_chunk_smem_bytes() {
+  using L = BwdLd<DK, DV>;
+  return (2 * kC * L::K + 2 * kC * L::X + kC * L::V + 3 * kC * L::C + 5 * kC + 8 +
+          16 * L::X) * sizeof(float);
+}
+
 // Per-chunk backward (grid: chunks x H x B): everything local to the chunk once dW and the
-// state gradient at its end are known.  dq^, dk^ accumulate in the outputs dq, dk (fp32),
-// then the L2 normalisations are back-propagated in place.
+// state gradient at its end are known.  dq^ and dk^ stay in registers (rows ti + 16 u,
+// columns tj + 16 c of the thread) until the L2 normalisations are back-propagated and they
+// are written once; every other result goes through shared memory.  Row reductions (the
+// log-decay and beta gradients) are summed over the 16 lanes that own a row, in a fixed
+// order (deterministic).
 template <int DK, int DV>
 __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
@@ -678,25 +786,31 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
     const float* __restrict__ dWg, int T, int H, int nch, float scale,
     float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
     float* __restrict__ dbeta, float* __restrict__ dg) {
-  constexpr int LK = Ld<DK>::v, LV = Ld<DV>::v, LC = Ld<kC>::v;
-  constexpr int LX = LK > LV ? LK : LV;
-  extern __shared__ float sm[];
+  using L = BwdLd<DK, DV>;
+  constexpr int LK = L::K, LV = L::V, LX = L::X, LC = L::C;
+  constexpr int RU = kC / 16;            // rows per thread
+  constexpr int CK = DK / 16, CV = DV / 16, CC = kC / 16;  // columns per thread
+  extern __shared__ float4 smb4[];
+  float* sm = reinterpret_cast<float*>(smb4);
   float* sQ = sm;                   // [C][LK] q^
   float* sK = sQ + kC * LK;         // [C][LK] k^
   float* sW = sK + kC * LK;         // [C][LX] W, later dBk
-  float* sdW = sW + kC * LX;        // [C][LV] dW
-  float* sX = sdW + kC * LV;        // [C][LX] dO, later dY, later dBv
-  float* sC1 = sX + kC * LX;        // [C][LC] dP masked by Gam (G . dP), later Z
+  float* sX = sW + kC * LX;         // [C][LX] dO, later dY, later dBv
+  float* sdW = sX + kC * LX;        // [C][LV] dW
+  float* sC1 = sdW + kC * LV;       // [C][LC] Gam . dP, later Z
   float* sC2 = sC1 + kC * LC;       // [C][LC] R = dP . P + dM . M (log-decay gradient)
   float* sC3 = sC2 + kC * LC;       // [C][LC] dM . Gam . K^K^T (beta gradient)
   float* sG = sC3 + kC * LC;        // [C] cumulative log decay
   float* sB = sG + kC;              // [C] beta
   float* sdG = sB + kC;             // [C] log-decay gradient
   float* sdB = sdG + kC;            // [C] beta gradient
-  float* sPart = sdB + kC;          // [C][8] per-warp partial sums
-  float* sRed = sPart + kC * 8;     // [8] block reduction
+  float* sPart = sdB + kC;          // [C] per-row partial sums
+  float* sRed = sPart + kC;         // [8] block reduction
+  float* sStg = sRed + 8;           // [16][<= LX] staged rows of a global operand
+  static_assert(kC + 4 <= LX, "the staging buffer holds 16 rows of any operand");
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ti = tid >> 4, tj = tid & 15;
   const size_t bh = static_cast<size_t>(b) * H + h;
   const size_t cid = bh * nch + c;
   const int t0 = c * kC;
@@ -705,15 +819,8 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
   const float* cU = U + cid * kC * DV;
   const float* cY = Y + cid * kC * DK;
   const float* cP = Pm + cid * kC * kC;
-  const float* cA = Ai + cid * kC * kC;      // A^-1 (lower triangular)
+  const float* cA = Ai + cid * kC * kC;      // A^-1 (lower triangular, zeros above)
   auto row = [&](int i) { return ((static_cast<size_t>(b) * T + t0 + i) * H + h); };
-  // partial sums of 32 lanes, then the 8 warps in order (deterministic block reductions
-  // keyed by a row index i: one warp covers 32 consecutive columns of one row)
-  auto warp_sum = [](float x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-  };
 
   for (int e = tid; e < kC * DK; e += 256) {
     const int i = e / DK, x = e - i * DK;
@@ -731,164 +838,202 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
     sdG[tid] = 0.f;
     sdB[tid] = 0.f;
   }
-  __syncthreads();
-  const float gl = sG[kC - 1];
-  // W = U - Y S0^T  (lanes over i: Y staged rows; S0 row r broadcast)
-  for (int e = tid; e < kC * DV; e += 256) {
-    const int r = e / kC, i = e - r * kC;
-    float w = cU[i * DV + r];
-    const float* yi = cY + i * DK;
-    const float* s0 = S0 + r * DK;
-    for (int x = 0; x < DK; ++x) w -= __ldg(&yi[x]) * __ldg(&s0[x]);
-    sW[i * LX + r] = w;
-  }
-  __syncthreads();
-  // dP_ij = s dO_i . W_j (j <= i), kept as (Gam . dP); and R_ij = dP_ij P_ij
-  for (int e = tid; e < kC * kC; e += 256) {
-    const int i = e / kC, j = e - i * kC;
-    float gd = 0.f, rr = 0.f;
-    if (j <= i) {
-      float a = 0.f;
-      for (int r = 0; r < DV; ++r) a += sX[i * LX + r] * sW[j * LX + r];
-      const float dp = scale * a;
-      gd = __expf(sG[i] - sG[j]) * dp;
-      rr = dp * __ldg(&cP[i * kC + j]);
-    }
-    sC1[i * LC + j] = gd;
-    sC2[i * LC + j] = rr;
-  }
-  __syncthreads();
-  // dq^ = (Gam . dP) K^ + s gamma_i dO_i S0, and dG_i += s gamma_i (dO S0)_i . q^_i
-  for (int e = tid; e < kC * DK; e += 256) {
-    const int i = e / DK, x = e - i * DK;
-    float a = 0.f;
-    for (int j = 0; j <= i; ++j) a += sC1[i * LC + j] * sK[j * LK + x];
-    float os = 0.f;
-    for (int r = 0; r < DV; ++r) os += sX[i * LX + r] * __ldg(&S0[r * DK + x]);
-    const float gi = __expf(sG[i]);
-    a += scale * gi * os;
-    if (t0 + i < T) dq[row(i) * DK + x] = a;
-    const float part = warp_sum(scale * gi * os * sQ[i * LK + x]);
-    if (lane == 0) sPart[i * 8 + (x >> 5)] = part;
-  }
-  __syncthreads();
-  if (tid < kC) {
-    float a = 0.f;
-    for (int w = 0; w < DK / 32; ++w) a += sPart[tid * 8 + w];
-    sdG[tid] += a;
-  }
-  __syncthreads();
-  // dk^ = (Gam . dP)^T Q^ + diag(gamma_C / gamma) (W dS1); dG from E
-  for (int e = tid; e < kC * DK; e += 256) {
-    const int j = e / DK, x = e - j * DK;
-    float a = 0.f;
-    for (int i = j; i < kC; ++i) a += sC1[i * LC + j] * sQ[i * LK + x];
-    float de = 0.f;
-    for (int r = 0; r < DV; ++r) de += sW[j * LX + r] * __ldg(&dS1[r * DK + x]);
-    const float ej = __expf(gl - sG[j]);
-    a += ej * de;
-    if (t0 + j < T) dk[row(j) * DK + x] = a;
-    const float part = warp_sum(ej * de * sK[j * LK + x]);
-    if (lane == 0) sPart[j * 8 + (x >> 5)] = part;
-  }
   // gamma_C <dS1, S0> (block reduction in a fixed order)
   {
     float a = 0.f;
     for (int e = tid; e < DV * DK; e += 256) a += __ldg(&dS1[e]) * __ldg(&S0[e]);
-    a = warp_sum(a);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
     if (lane == 0) sRed[warp] = a;
   }
   __syncthreads();
-  if (tid < kC) {
-    float a = 0.f;
-    for (int w = 0; w < DK / 32; ++w) a += sPart[tid * 8 + w];
-    sdG[tid] -= a;                       // exp(G_C - G_j): d/dG_j = -(...)
-    float tot = 0.f;
-    if (tid == kC - 1) {
-      for (int j = 0; j < kC; ++j) {
-        float aj = 0.f;
-        for (int w = 0; w < DK / 32; ++w) aj += sPart[j * 8 + w];
-        tot += aj;                       // d/dG_C of every exp(G_C - G_j)
+  const float gl = sG[kC - 1];
+  // (1) W = U - Y S0^T  -> sW
+  {
+    float acc[RU][CV];
+    mm_zero<kC, DV>(acc);
+    mm_nn_staged<kC, DV, true>(DK, [&](int m, int x) { return __ldg(&cY[m * DK + x]); }, S0, DK,
+                               sStg, acc);
+#pragma unroll
+    for (int u = 0; u < RU; ++u)
+#pragma unroll
+      for (int cc = 0; cc < CV; ++cc) {
+        const int i = ti + 16 * u, r = tj + 16 * cc;
+        sW[i * LX + r] = __ldg(&cU[i * DV + r]) - acc[u][cc];
       }
-      float sr = 0.f;
-      for (int w = 0; w < 8; ++w) sr += sRed[w];
-      tot += __expf(gl) * sr;            // gamma_C S0
-      sdG[tid] += tot;
+  }
+  __syncthreads();
+  // (2) dP_ij = s dO_i . W_j (j <= i), kept as Gam . dP (sC1); R_ij = dP_ij P_ij (sC2)
+  {
+    float acc[RU][CC];
+    mm_zero<kC, kC>(acc);
+    mm_nt4<kC, kC>(DV, [&](int m) { return sX + m * LX; }, [&](int n) { return sW + n * LX; },
+                   acc);
+#pragma unroll
+    for (int u = 0; u < RU; ++u)
+#pragma unroll
+      for (int cc = 0; cc < CC; ++cc) {
+        const int i = ti + 16 * u, j = tj + 16 * cc;
+        float gd = 0.f, rr = 0.f;
+        if (j <= i) {
+          const float dp = scale * acc[u][cc];
+          gd = __expf(sG[i] - sG[j]) * dp;
+          rr = dp * __ldg(&cP[i * kC + j]);
+        }
+        sC1[i * LC + j] = gd;
+        sC2[i * LC + j] = rr;
+      }
+  }
+  __syncthreads();
+  // (3) dq^ = (Gam . dP) K^ + s gamma_i dO_i S0;  dG_i += s gamma_i (dO S0)_i . q^_i
+  float dqa[RU][CK];
+  mm_zero<kC, DK>(dqa);
+  mm_nn_staged<kC, DK, false>(DV, [&](int m, int r) { return sX[m * LX + r]; }, S0, DK, sStg,
+                              dqa);
+#pragma unroll
+  for (int u = 0; u < RU; ++u) {
+    const int i = ti + 16 * u;
+    const float sgi = scale * __expf(sG[i]);
+    float part = 0.f;
+#pragma unroll
+    for (int cc = 0; cc < CK; ++cc) {
+      dqa[u][cc] *= sgi;
+      part += dqa[u][cc] * sQ[i * LK + tj + 16 * cc];
+    }
+    part = rowgroup_sum(part);
+    if (tj == 0) sdG[i] += part;
+  }
+  mm_nn<kC, DK>(kC, [&](int m, int j) { return sC1[m * LC + j]; },
+                [&](int j, int n) { return sK[j * LK + n]; }, dqa);
+  // (4) dk^ = (Gam . dP)^T Q^ + diag(gamma_C / gamma) (W dS1); dG from E
+  float dka[RU][CK];
+  mm_zero<kC, DK>(dka);
+  mm_nn_staged<kC, DK, false>(DV, [&](int m, int r) { return sW[m * LX + r]; }, dS1, DK, sStg,
+                              dka);
+#pragma unroll
+  for (int u = 0; u < RU; ++u) {
+    const int j = ti + 16 * u;
+    const float ej = __expf(gl - sG[j]);
+    float part = 0.f;
+#pragma unroll
+    for (int cc = 0; cc < CK; ++cc) {
+      dka[u][cc] *= ej;
+      part += dka[u][cc] * sK[j * LK + tj + 16 * cc];
+    }
+    part = rowgroup_sum(part);
+    if (tj == 0) {
+      sdG[j] -= part;                    // exp(G_C - G_j): d/dG_j = -(...)
+      sPart[j] = part;                   // and d/dG_C = +(...)
+    }
+  }
+  mm_nn<kC, DK>(kC, [&](int m, int i) { return sC1[i * LC + m]; },
+                [&](int i, int n) { return sQ[i * LK + n]; }, dka);
+  __syncthreads();   // every row's part, the <dS1, S0> partials; dO and W are done with
+  if (tid == 0) {
+    float tot = 0.f;
+    for (int j = 0; j < kC; ++j) tot += sPart[j];
+    float sr = 0.f;
+    for (int w = 0; w < 8; ++w) sr += sRed[w];
+    sdG[kC - 1] += tot + __expf(gl) * sr;  // d/dG_C of every exp(G_C - G_j) and of gamma_C S0
+  }
+  // (5) dY = -dW S0 -> sX
+  {
+    float acc[RU][CK];
+    mm_zero<kC, DK>(acc);
+    mm_nn_staged<kC, DK, false>(DV, [&](int m, int r) { return sdW[m * LV + r]; }, S0, DK,
+                                sStg, acc);
+#pragma unroll
+    for (int u = 0; u < RU; ++u)
+#pragma unroll
+      for (int cc = 0; cc < CK; ++cc) sX[(ti + 16 * u) * LX + tj + 16 * cc] = -acc[u][cc];
+  }
+  __syncthreads();
+  // (6) dBk = A^-T dY -> sW; dk^ += beta gamma dBk; beta and G from Bk = beta gamma K^
+  {
+    float acc[RU][CK];
+    mm_zero<kC, DK>(acc);
+    mm_nn<kC, DK>(kC, [&](int m, int i) { return __ldg(&cA[i * kC + m]); },
+                  [&](int i, int n) { return sX[i * LX + n]; }, acc);
+#pragma unroll
+    for (int u = 0; u < RU; ++u) {
+      const int j = ti + 16 * u;
+      const float gj = __expf(sG[j]);
+      const float bg = sB[j] * gj;
+      float part = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < CK; ++cc) {
+        const int x = tj + 16 * cc;
+        sW[j * LX + x] = acc[u][cc];
+        dka[u][cc] += bg * acc[u][cc];
+        part += acc[u][cc] * sK[j * LK + x];
+      }
+      part = rowgroup_sum(part);
+      if (tj == 0) {
+        sdB[j] += gj * part;
+        sdG[j] += bg * part;
+      }
     }
   }
   __syncthreads();
-  // dY = -dW S0 -> sX (dO is no longer needed)
-  for (int e = tid; e < kC * DK; e += 256) {
-    const int i = e / DK, x = e - i * DK;
-    float a = 0.f;
-    for (int r = 0; r < DV; ++r) a -= sdW[i * LV + r] * __ldg(&S0[r * DK + x]);
-    sX[i * LX + x] = a;
-  }
-  __syncthreads();
-  // dBk = A^-T dY -> sW (W is no longer needed); dk^ += beta gamma dBk; beta, G from Bk
-  for (int e = tid; e < kC * DK; e += 256) {
-    const int j = e / DK, x = e - j * DK;
-    float a = 0.f;
-    for (int i = j; i < kC; ++i) a += __ldg(&cA[i * kC + j]) * sX[i * LX + x];
-    sW[j * LX + x] = a;
-    const float bg = sB[j] * __expf(sG[j]);
-    if (t0 + j < T) dk[row(j) * DK + x] += bg * a;
-    const float part = warp_sum(a * sK[j * LK + x]);
-    if (lane == 0) sPart[j * 8 + (x >> 5)] = part;
-  }
-  __syncthreads();
-  if (tid < kC) {
-    float a = 0.f;
-    for (int w = 0; w < DK / 32; ++w) a += sPart[tid * 8 + w];
-    const float gj = __expf(sG[tid]);
-    sdB[tid] += gj * a;
-    sdG[tid] += sB[tid] * gj * a;
-  }
-  __syncthreads();
-  // dBv = A^-T dW -> sX (dY is no longer needed); dV = beta dBv; beta from Bv
-  for (int e = tid; e < kC * DV; e += 256) {
-    const int j = e / DV, r = e - j * DV;
-    float a = 0.f;
-    for (int i = j; i < kC; ++i) a += __ldg(&cA[i * kC + j]) * sdW[i * LV + r];
-    sX[j * LX + r] = a;
-    float vj = 0.f;
-    if (t0 + j < T) {
-      dv[row(j) * DV + r] = sB[j] * a;
-      vj = bf(v[row(j) * DV + r]);
+  // (7) dBv = A^-T dW -> sX; dv = beta dBv; beta from Bv = beta V
+  {
+    float acc[RU][CV];
+    mm_zero<kC, DV>(acc);
+    mm_nn<kC, DV>(kC, [&](int m, int i) { return __ldg(&cA[i * kC + m]); },
+                  [&](int i, int n) { return sdW[i * LV + n]; }, acc);
+#pragma unroll
+    for (int u = 0; u < RU; ++u) {
+      const int j = ti + 16 * u;
+      float part = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < CV; ++cc) {
+        const int r = tj + 16 * cc;
+        const float a = acc[u][cc];
+        sX[j * LX + r] = a;
+        float vj = 0.f;
+        if (t0 + j < T) {
+          dv[row(j) * DV + r] = sB[j] * a;
+          vj = bf(v[row(j) * DV + r]);
+        }
+        part += a * vj;
+      }
+      part = rowgroup_sum(part);
+      if (tj == 0) sdB[j] += part;
     }
-    const float part = warp_sum(a * vj);
-    if (lane == 0) sPart[j * 8 + (r >> 5)] = part;
   }
   __syncthreads();
-  if (tid < kC) {
-    float a = 0.f;
-    for (int w = 0; w < DV / 32; ++w) a += sPart[tid * 8 + w];
-    sdB[tid] += a;
-  }
-  __syncthreads();
-  // dM_ij = -(dBv_i . U_j + dBk_i . Y_j) for j < i; with M_ij = beta_i Gam_ij k^_i.k^_j:
-  // Z_ij = dM_ij beta_i Gam_ij (-> sC1, for dk^), dM_ij M_ij (-> R in sC2, for dG) and
+  // (8) dM_ij = -(dBv_i . U_j + dBk_i . Y_j) for j < i; with M_ij = beta_i Gam_ij k^_i.k^_j:
+  // Z_ij = dM_ij beta_i Gam_ij (-> sC1, for dk^), dM_ij M_ij (added to R in sC2, for dG) and
   // dM_ij Gam_ij k^_i.k^_j (-> sC3, for dbeta)
-  for (int e = tid; e < kC * kC; e += 256) {
-    const int j = e / kC, i = e - j * kC;
-    float z = 0.f, bt = 0.f;
-    if (j < i) {
-      float a = 0.f;
-      const float* uj = cU + j * DV;
-      for (int r = 0; r < DV; ++r) a += sX[i * LX + r] * __ldg(&uj[r]);
-      const float* yj = cY + j * DK;
-      for (int x = 0; x < DK; ++x) a += sW[i * LX + x] * __ldg(&yj[x]);
-      float kk = 0.f;
-      for (int x = 0; x < DK; ++x) kk += sK[i * LK + x] * sK[j * LK + x];
-      const float gk = __expf(sG[i] - sG[j]) * kk;   // Gam_ij k^_i.k^_j
-      bt = -a * gk;
-      z = -a * sB[i] * __expf(sG[i] - sG[j]);
-      sC2[i * LC + j] += bt * sB[i];                   // dM_ij M_ij
-    }
-    sC1[i * LC + j] = z;
-    sC3[i * LC + j] = bt;
+  {
+    float acc[RU][CC], kk[RU][CC];
+    mm_zero<kC, kC>(acc);
+    mm_zero<kC, kC>(kk);
+    mm_nn_staged<kC, kC, true>(DV, [&](int m, int r) { return sX[m * LX + r]; }, cU, DV, sStg,
+                               acc);
+    mm_nn_staged<kC, kC, true>(DK, [&](int m, int x) { return sW[m * LX + x]; }, cY, DK, sStg,
+                               acc);
+    mm_nt4<kC, kC>(DK, [&](int m) { return sK + m * LK; }, [&](int n) { return sK + n * LK; },
+                   kk);
+#pragma unroll
+    for (int u = 0; u < RU; ++u)
+#pragma unroll
+      for (int cc = 0; cc < CC; ++cc) {
+        const int i = ti + 16 * u, j = tj + 16 * cc;
+        float z = 0.f, bt = 0.f;
+        if (j < i) {
+          const float a = acc[u][cc];
+          const float gam = __expf(sG[i] - sG[j]);
+          bt = -a * gam * kk[u][cc];
+          z = -a * sB[i] * gam;
+          sC2[i * LC + j] += bt * sB[i];
+        }
+        sC1[i * LC + j] = z;
+        sC3[i * LC + j] = bt;
+      }
   }
   __syncthreads();
+  // (9) row and column sums of R, row sums of the beta terms; dk^ += (Z + Z^T) K^
   if (tid < kC) {
     const int i = tid;
     float rs = 0.f, cs = 0.f, db = 0.f;
@@ -900,16 +1045,10 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
     sdB[i] += db;
     sdG[i] += rs - cs;
   }
+  mm_nn<kC, DK>(kC, [&](int i, int j) { return sC1[i * LC + j] + sC1[j * LC + i]; },
+                [&](int j, int n) { return sK[j * LK + n]; }, dka);
   __syncthreads();
-  // dk^ += Z K^ + Z^T K^
-  for (int e = tid; e < kC * DK; e += 256) {
-    const int i = e / DK, x = e - i * DK;
-    float a = 0.f;
-    for (int j = 0; j < kC; ++j) a += (sC1[i * LC + j] + sC1[j * LC + i]) * sK[j * LK + x];
-    if (t0 + i < T) dk[row(i) * DK + x] += a;
-  }
-  __syncthreads();
-  // dg = reverse cumulative sum of dG within the chunk; dbeta out
+  // (10) dg = reverse cumulative sum of dG within the chunk; dbeta out
   if (tid == 0) {
     float run = 0.f;
     for (int i = kC - 1; i >= 0; --i) {
@@ -920,26 +1059,35 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
       }
     }
   }
-  // L2 normalisations: dx = (dx^ - x^ (x^ . dx^)) / ||x||  (one warp per row)
-  for (int i = warp; i < kC; i += 8) {
-    if (t0 + i >= T) continue;
+  // L2 normalisations: dx = (dx^ - x^ (x^ . dx^)) / ||x||, over the 16 lanes owning a row
+#pragma unroll
+  for (int u = 0; u < RU; ++u) {
+    const int i = ti + 16 * u;
+    const bool in = t0 + i < T;
     float nq = 0.f, nk = 0.f, pq = 0.f, pk = 0.f;
-    for (int x = lane; x < DK; x += 32) {
-      const float qv = bf(q[row(i) * DK + x]), kv = bf(k[row(i) * DK + x]);
+#pragma unroll
+    for (int cc = 0; cc < CK; ++cc) {
+      const int x = tj + 16 * cc;
+      const float qv = in ? bf(q[row(i) * DK + x]) : 0.f;
+      const float kv = in ? bf(k[row(i) * DK + x]) : 0.f;
       nq += qv * qv;
       nk += kv * kv;
-      pq += dq[row(i) * DK + x] * sQ[i * LK + x];
-      pk += dk[row(i) * DK + x] * sK[i * LK + x];
+      pq += dqa[u][cc] * sQ[i * LK + x];
+      pk += dka[u][cc] * sK[i * LK + x];
     }
-    nq = warp_sum(nq);
-    nk = warp_sum(nk);
-    pq = warp_sum(pq);
-    pk = warp_sum(pk);
-    const float iq = nq > 0.f ? 1.0f / sqrtf(nq) : 0.f;
-    const float ik = nk > 0.f ? 1.0f / sqrtf(nk) : 0.f;
-    for (int x = lane; x < DK; x += 32) {
-      dq[row(i) * DK + x] = (dq[row(i) * DK + x] - sQ[i * LK + x] * pq) * iq;
-      dk[row(i) * DK + x] = (dk[row(i) * DK + x] - sK[i * LK + x] * pk) * ik;
+    nq = rowgroup_sum(nq);
+    nk = rowgroup_sum(nk);
+    pq = rowgroup_sum(pq);
+    pk = rowgroup_sum(pk);
+    if (in) {
+      const float iq = nq > 0.f ? 1.0f / sqrtf(nq) : 0.f;
+      const float ik = nk > 0.f ? 1.0f / sqrtf(nk) : 0.f;
+#pragma unroll
+      for (int cc = 0; cc < CK; ++cc) {
+        const int x = tj + 16 * cc;
+        dq[row(i) * DK + x] = (dqa[u][cc] - sQ[i * LK + x] * pq) * iq;
+        dk[row(i) * DK + x] = (dka[u][cc] - sK[i * LK + x] * pk) * ik;
+      }
     }
   }
 }
@@ -1015,16 +1163,18 @@ int gdr_bwd_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloa
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(sm1));
   if (e != cudaSuccess) return static_cast<int>(e);
+  mark_before(MOE_KERNEL_GDR_BWD_FACTORS, s);
   k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, Qh, Kh, Yw, Uw, Pw, Gw, Aw);
+  mark_after(MOE_KERNEL_GDR_BWD_FACTORS, s);
   const size_t sm2 = bwd_scan_smem_bytes<DK>();
   auto k2 = gdr_bwd_scan_kernel<DK, DV>;
   e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm2));
   if (e != cudaSuccess) return static_cast<int>(e);
+  mark_before(MOE_KERNEL_GDR_BWD_SCAN, s);
   k2<<<dim3(DV / kRS, H, B), 256, sm2, s>>>(Qh, Kh, Yw, Pw, Gw, dO, dST, T, H, nch, scale, dWw,
                                             dSw, dS0);
-  constexpr int LX = Ld<DK>::v > Ld<DV>::v ? Ld<DK>::v : Ld<DV>::v;
-  const size_t sm3 = (2 * kC * Ld<DK>::v + 2 * kC * LX + kC * Ld<DV>::v + 3 * kC * Ld<kC>::v +
-                      4 * kC + 8 * kC + 8) * sizeof(float);
+  mark_after(MOE_KERNEL_GDR_BWD_SCAN, s);
+  const size_t sm3 = bwd_chunk_smem_bytes<DK, DV>();
   auto k3 = gdr_bwd_chunk_kernel<DK, DV>;
   e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm3));
   if (e != cudaSuccess) return static_cast<int>(e);
@@ -1095,7 +1245,7 @@ int moe_gdr_backward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, co
   if (!workspace || workspace_bytes < gdr_bwd_ws(B, T, H, dk, dv)) return MOE_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(d_o) |
        reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-       reinterpret_cast<uintptr_t>(v)) & 15u)
+       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(S_chunks)) & 15u)
     return MOE_ERR_UNSUPPORTED;
   const auto* q_ = reinterpret_cast<const __nv_bfloat16*>(q);
   const auto* k_ = reinterpret_cast<const __nv_bfloat16*>(k);

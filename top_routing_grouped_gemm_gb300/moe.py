@@ -116,7 +116,8 @@ _SIGS = {
 
 KERNEL_IDS = {"router_gemm": 0, "topk": 1, "dispatch": 2, "gateup_gemm": 3, "down_gemm": 4,
               "combine": 5, "bwd_dh_gemm": 6, "bwd_dx_gemm": 7, "wgrad": 8, "gdr_chunk": 9,
-              "gdr_scan": 10, "gdr_bwd": 11, "combine_bwd": 12, "dispatch_route_bwd": 13}
+              "gdr_scan": 10, "gdr_bwd": 11, "combine_bwd": 12, "dispatch_route_bwd": 13,
+              "gdr_bwd_factors": 14, "gdr_bwd_scan": 15}
 
 _lib = None
 
