@@ -750,6 +750,75 @@ __device__ __forceinline__ void mm_nn_staged(int K, FA A, const float* __restric
   }
 }
 
+// Float4 form of the products: thread (ti, tj) owns rows ti + 16 u and the four consecutive
+// columns 64 g + 4 tj .. + 3 of every 64 (column c of the thread: bcol(tj, c)); A4(m, k)
+// returns A(m, k .. k+3) and B4(k, n) returns B(k, n .. n+3) (k, n multiples of 4), so a k
+// step costs one 16-byte read per row and per column group.
+__device__ __forceinline__ int bcol(int tj, int c) { return (c >> 2) * 64 + 4 * tj + (c & 3); }
+
+template <int M, int N, class FA4, class FB4>
+__device__ __forceinline__ void mm_nn4(int K, FA4 A4, FB4 B4, float (&acc)[M / 16][N / 16]) {
+  static_assert(N % 64 == 0, "four consecutive columns per lane, 64 per row group");
+  constexpr int RA = M / 16, NG = N / 64;
+  const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
+#pragma unroll 2
+  for (int k = 0; k < K; k += 4) {
+    float4 a[RA];
+#pragma unroll
+    for (int u = 0; u < RA; ++u) a[u] = A4(ti + 16 * u, k);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      float4 bq[NG];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) bq[g] = B4(k + kk, 64 * g + 4 * tj);
+#pragma unroll
+      for (int u = 0; u < RA; ++u) {
+        const float av = kk == 0 ? a[u].x : kk == 1 ? a[u].y : kk == 2 ? a[u].z : a[u].w;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          acc[u][4 * g] += av * bq[g].x;
+          acc[u][4 * g + 1] += av * bq[g].y;
+          acc[u][4 * g + 2] += av * bq[g].z;
+          acc[u][4 * g + 3] += av * bq[g].w;
+        }
+      }
+    }
+  }
+}
+
+// mm_nn4 with B in global memory staged through shared memory (as mm_nn_staged)
+template <int M, int N, bool TRANS, class FA4>
+__device__ __forceinline__ void mm_nn4_staged(int K, FA4 A4, const float* __restrict__ Bg,
+                                              int ldb, float* stage,
+                                              float (&acc)[M / 16][N / 16]) {
+  constexpr int LSG = N + 4;
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int e = threadIdx.x; e < 16 * N; e += 256) {
+      int kk, n;
+      if (TRANS) {
+        n = e >> 4;
+        kk = e & 15;
+      } else {
+        kk = e / N;
+        n = e - kk * N;
+      }
+      stage[kk * LSG + n] = TRANS ? __ldg(&Bg[static_cast<size_t>(n) * ldb + k0 + kk])
+                                  : __ldg(&Bg[static_cast<size_t>(k0 + kk) * ldb + n]);
+    }
+    __syncthreads();
+    mm_nn4<M, N>(16, [&](int m, int k) { return A4(m, k0 + k); },
+                 [&](int k, int n) { return *reinterpret_cast<const float4*>(stage + k * LSG + n); },
+                 acc);
+    __syncthreads();
+  }
+}
+
+// A4 / B4 readers: rows of a k-contiguous (A) or n-contiguous (B) matrix, 16-byte aligned
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ldg4(const float* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+
 // sum over the 16 lanes of a row group (tj = lane % 16), every lane gets the total
 __device__ __forceinline__ float rowgroup_sum(float x) {
 #pragma unroll
@@ -852,13 +921,13 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
   {
     float acc[RU][CV];
     mm_zero<kC, DV>(acc);
-    mm_nn_staged<kC, DV, true>(DK, [&](int m, int x) { return __ldg(&cY[m * DK + x]); }, S0, DK,
-                               sStg, acc);
+    mm_nn4_staged<kC, DV, true>(DK, [&](int m, int x) { return ldg4(cY + m * DK + x); }, S0, DK,
+                                sStg, acc);
 #pragma unroll
     for (int u = 0; u < RU; ++u)
 #pragma unroll
       for (int cc = 0; cc < CV; ++cc) {
-        const int i = ti + 16 * u, r = tj + 16 * cc;
+        const int i = ti + 16 * u, r = bcol(tj, cc);
         sW[i * LX + r] = __ldg(&cU[i * DV + r]) - acc[u][cc];
       }
   }
@@ -888,8 +957,8 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
   // (3) dq^ = (Gam . dP) K^ + s gamma_i dO_i S0;  dG_i += s gamma_i (dO S0)_i . q^_i
   float dqa[RU][CK];
   mm_zero<kC, DK>(dqa);
-  mm_nn_staged<kC, DK, false>(DV, [&](int m, int r) { return sX[m * LX + r]; }, S0, DK, sStg,
-                              dqa);
+  mm_nn4_staged<kC, DK, false>(DV, [&](int m, int r) { return ld4(sX + m * LX + r); }, S0, DK,
+                               sStg, dqa);
 #pragma unroll
   for (int u = 0; u < RU; ++u) {
     const int i = ti + 16 * u;
@@ -898,18 +967,18 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
 #pragma unroll
     for (int cc = 0; cc < CK; ++cc) {
       dqa[u][cc] *= sgi;
-      part += dqa[u][cc] * sQ[i * LK + tj + 16 * cc];
+      part += dqa[u][cc] * sQ[i * LK + bcol(tj, cc)];
     }
     part = rowgroup_sum(part);
     if (tj == 0) sdG[i] += part;
   }
-  mm_nn<kC, DK>(kC, [&](int m, int j) { return sC1[m * LC + j]; },
-                [&](int j, int n) { return sK[j * LK + n]; }, dqa);
+  mm_nn4<kC, DK>(kC, [&](int m, int j) { return ld4(sC1 + m * LC + j); },
+                 [&](int j, int n) { return ld4(sK + j * LK + n); }, dqa);
   // (4) dk^ = (Gam . dP)^T Q^ + diag(gamma_C / gamma) (W dS1); dG from E
   float dka[RU][CK];
   mm_zero<kC, DK>(dka);
-  mm_nn_staged<kC, DK, false>(DV, [&](int m, int r) { return sW[m * LX + r]; }, dS1, DK, sStg,
-                              dka);
+  mm_nn4_staged<kC, DK, false>(DV, [&](int m, int r) { return ld4(sW + m * LX + r); }, dS1, DK,
+                               sStg, dka);
 #pragma unroll
   for (int u = 0; u < RU; ++u) {
     const int j = ti + 16 * u;
@@ -918,7 +987,7 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
 #pragma unroll
     for (int cc = 0; cc < CK; ++cc) {
       dka[u][cc] *= ej;
-      part += dka[u][cc] * sK[j * LK + tj + 16 * cc];
+      part += dka[u][cc] * sK[j * LK + bcol(tj, cc)];
     }
     part = rowgroup_sum(part);
     if (tj == 0) {
@@ -926,8 +995,12 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
       sPart[j] = part;                   // and d/dG_C = +(...)
     }
   }
-  mm_nn<kC, DK>(kC, [&](int m, int i) { return sC1[i * LC + m]; },
-                [&](int i, int n) { return sQ[i * LK + n]; }, dka);
+  mm_nn4<kC, DK>(kC,
+                 [&](int m, int i) {
+                   return make_float4(sC1[i * LC + m], sC1[(i + 1) * LC + m],
+                                      sC1[(i + 2) * LC + m], sC1[(i + 3) * LC + m]);
+                 },
+                 [&](int i, int n) { return ld4(sQ + i * LK + n); }, dka);
   __syncthreads();   // every row's part, the <dS1, S0> partials; dO and W are done with
   if (tid == 0) {
     float tot = 0.f;
@@ -940,20 +1013,25 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
   {
     float acc[RU][CK];
     mm_zero<kC, DK>(acc);
-    mm_nn_staged<kC, DK, false>(DV, [&](int m, int r) { return sdW[m * LV + r]; }, S0, DK,
-                                sStg, acc);
+    mm_nn4_staged<kC, DK, false>(DV, [&](int m, int r) { return ld4(sdW + m * LV + r); }, S0,
+                                 DK, sStg, acc);
 #pragma unroll
     for (int u = 0; u < RU; ++u)
 #pragma unroll
-      for (int cc = 0; cc < CK; ++cc) sX[(ti + 16 * u) * LX + tj + 16 * cc] = -acc[u][cc];
+      for (int cc = 0; cc < CK; ++cc) sX[(ti + 16 * u) * LX + bcol(tj, cc)] = -acc[u][cc];
   }
   __syncthreads();
   // (6) dBk = A^-T dY -> sW; dk^ += beta gamma dBk; beta and G from Bk = beta gamma K^
   {
     float acc[RU][CK];
     mm_zero<kC, DK>(acc);
-    mm_nn<kC, DK>(kC, [&](int m, int i) { return __ldg(&cA[i * kC + m]); },
-                  [&](int i, int n) { return sX[i * LX + n]; }, acc);
+    mm_nn4<kC, DK>(kC,
+                   [&](int m, int i) {
+                     return make_float4(__ldg(&cA[i * kC + m]), __ldg(&cA[(i + 1) * kC + m]),
+                                        __ldg(&cA[(i + 2) * kC + m]),
+                                        __ldg(&cA[(i + 3) * kC + m]));
+                   },
+                   [&](int i, int n) { return ld4(sX + i * LX + n); }, acc);
 #pragma unroll
     for (int u = 0; u < RU; ++u) {
       const int j = ti + 16 * u;
@@ -962,7 +1040,7 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
       float part = 0.f;
 #pragma unroll
       for (int cc = 0; cc < CK; ++cc) {
-        const int x = tj + 16 * cc;
+        const int x = bcol(tj, cc);
         sW[j * LX + x] = acc[u][cc];
         dka[u][cc] += bg * acc[u][cc];
         part += acc[u][cc] * sK[j * LK + x];
@@ -979,15 +1057,20 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
   {
     float acc[RU][CV];
     mm_zero<kC, DV>(acc);
-    mm_nn<kC, DV>(kC, [&](int m, int i) { return __ldg(&cA[i * kC + m]); },
-                  [&](int i, int n) { return sdW[i * LV + n]; }, acc);
+    mm_nn4<kC, DV>(kC,
+                   [&](int m, int i) {
+                     return make_float4(__ldg(&cA[i * kC + m]), __ldg(&cA[(i + 1) * kC + m]),
+                                        __ldg(&cA[(i + 2) * kC + m]),
+                                        __ldg(&cA[(i + 3) * kC + m]));
+                   },
+                   [&](int i, int n) { return ld4(sdW + i * LV + n); }, acc);
 #pragma unroll
     for (int u = 0; u < RU; ++u) {
       const int j = ti + 16 * u;
       float part = 0.f;
 #pragma unroll
       for (int cc = 0; cc < CV; ++cc) {
-        const int r = tj + 16 * cc;
+        const int r = bcol(tj, cc);
         const float a = acc[u][cc];
         sX[j * LX + r] = a;
         float vj = 0.f;
@@ -1045,8 +1128,13 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
     sdB[i] += db;
     sdG[i] += rs - cs;
   }
-  mm_nn<kC, DK>(kC, [&](int i, int j) { return sC1[i * LC + j] + sC1[j * LC + i]; },
-                [&](int j, int n) { return sK[j * LK + n]; }, dka);
+  mm_nn4<kC, DK>(kC,
+                 [&](int i, int j) {
+                   const float4 r = ld4(sC1 + i * LC + j);
+                   return make_float4(r.x + sC1[j * LC + i], r.y + sC1[(j + 1) * LC + i],
+                                      r.z + sC1[(j + 2) * LC + i], r.w + sC1[(j + 3) * LC + i]);
+                 },
+                 [&](int j, int n) { return ld4(sK + j * LK + n); }, dka);
   __syncthreads();
   // (10) dg = reverse cumulative sum of dG within the chunk; dbeta out
   if (tid == 0) {
@@ -1067,7 +1155,7 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
     float nq = 0.f, nk = 0.f, pq = 0.f, pk = 0.f;
 #pragma unroll
     for (int cc = 0; cc < CK; ++cc) {
-      const int x = tj + 16 * cc;
+      const int x = bcol(tj, cc);
       const float qv = in ? bf(q[row(i) * DK + x]) : 0.f;
       const float kv = in ? bf(k[row(i) * DK + x]) : 0.f;
       nq += qv * qv;
@@ -1084,7 +1172,7 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
       const float ik = nk > 0.f ? 1.0f / sqrtf(nk) : 0.f;
 #pragma unroll
       for (int cc = 0; cc < CK; ++cc) {
-        const int x = tj + 16 * cc;
+        const int x = bcol(tj, cc);
         dq[row(i) * DK + x] = (dqa[u][cc] - sQ[i * LK + x] * pq) * iq;
         dk[row(i) * DK + x] = (dka[u][cc] - sK[i * LK + x] * pk) * ik;
       }
