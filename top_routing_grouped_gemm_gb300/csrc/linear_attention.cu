@@ -545,7 +545,8 @@ __global__ void __launch_bounds__(256) gdr_bwd_scan_kernel(
     const float* __restrict__ Pm, const float* __restrict__ Gc,
     const __nv_bfloat16* __restrict__ dO, const float* __restrict__ dST, int T, int H, int nch,
     float scale, float* __restrict__ dW, float* __restrict__ dSchk, float* __restrict__ dS0) {
-  constexpr int LS = Ld<DK>::v, LT = ScanLd<DK>::T, LP = ScanLd<DK>::P;
+  constexpr int LT = ScanLd<DK>::T, LP = ScanLd<DK>::P;
+  constexpr int LS = ScanLd<DK>::T;  // state-gradient rows: 16-byte aligned (read as float4)
   extern __shared__ float4 sm4[];
   float* sm = reinterpret_cast<float*>(sm4);
   float* sQ = sm;                   // [C][LT]
@@ -557,7 +558,7 @@ __global__ void __launch_bounds__(256) gdr_bwd_scan_kernel(
   float* sD = sGr + kC + kC * kRS / 2;  // [RS][LS] state gradient rows
   float* sW = sD + kRS * LS;        // [C][RS] dW slice
   float* sOg = sW + kC * kRS;       // [C][RS] s gamma_i dO
-  static_assert(kC * kRS == 4 * 256, "dW tiling: 4 outputs per thread");
+  static_assert(kRS == 16 && kC == 64 && DK % 32 == 0, "thread tiling");
   static_assert(kRS * 2 % 16 == 0, "dO slice rows are whole 16-byte pieces");
   const int r0 = blockIdx.x * kRS, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
@@ -593,61 +594,111 @@ __global__ void __launch_bounds__(256) gdr_bwd_scan_kernel(
   }
   issue_a(nch - 1);
   issue_b(nch - 1);
-  const int i = tid >> 2, rb = (tid & 3) * 4;  // dW tiling: row i, value rows rb .. rb+3
+  // dW phase: token rows i0 = tid / 8 and i1 = i0 + 32, value rows c0 = tid % 8, c1 = c0 + 8
+  const int cq = tid & 7, i0 = tid >> 3, i1 = i0 + 32;
+  const int c0 = cq, c1 = cq + 8;
+  // state-gradient phase: value rows rs * RPL .. + RPL - 1, float4 column group cg
+  constexpr int GW = DK / 32, RSEL = 32 / GW, RPL = kRS / RSEL;
+  static_assert(RPL * RSEL == kRS && (RPL == 1 || RPL == 2), "state-gradient tiling");
+  const int lane = tid & 31, warp = tid >> 5;
+  const int cg = warp * GW + lane / RSEL, rs = lane % RSEL;
   for (int c = nch - 1; c >= 0; --c) {
     const size_t cid = bh * nch + c;
     la_wait1();        // P, K^, dO, decays of chunk c
     __syncthreads();
-    const float gi = sGr[i], gC = sGr[kC - 1];
-    const float gam_i = __expf(gi), dec_i = __expf(gC - gi), gam_C = __expf(gC);
+    const float gC = sGr[kC - 1];
+    const float gam_C = __expf(gC);
     for (int e = tid; e < kRS * DK; e += 256) {
       const int r = e / DK, x = e - r * DK;
       dSchk[(cid * DV + r0 + r) * DK + x] = sD[r * LS + x];
     }
     // dW = s P^T dO + E dS1^T
     {
-      float a[4] = {0.f, 0.f, 0.f, 0.f}, bs[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int t = i; t < kC; ++t) {
-        const float pv = sP[t * LP + i];
-        const bool in = c * kC + t < T;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) a[u] += pv * (in ? bf(sOb[t * kRS + rb + u]) : 0.f);
-      }
-      const float* ki = sK + i * LT;
+      float kd[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, pd[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      const float4* ka = reinterpret_cast<const float4*>(sK + i0 * LT);
+      const float4* kb = reinterpret_cast<const float4*>(sK + i1 * LT);
+      const float4* da = reinterpret_cast<const float4*>(sD + c0 * LS);
+      const float4* db = reinterpret_cast<const float4*>(sD + c1 * LS);
 #pragma unroll 4
-      for (int x = 0; x < DK; ++x) {
-        const float kv = ki[x];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) bs[u] += kv * sD[(rb + u) * LS + x];
+      for (int x4 = 0; x4 < DK / 4; ++x4) {
+        const float4 a0 = ka[x4], a1 = kb[x4], u0 = da[x4], u1 = db[x4];
+        kd[0][0] += a0.x * u0.x + a0.y * u0.y + a0.z * u0.z + a0.w * u0.w;
+        kd[0][1] += a0.x * u1.x + a0.y * u1.y + a0.z * u1.z + a0.w * u1.w;
+        kd[1][0] += a1.x * u0.x + a1.y * u0.y + a1.z * u0.z + a1.w * u0.w;
+        kd[1][1] += a1.x * u1.x + a1.y * u1.y + a1.z * u1.z + a1.w * u1.w;
       }
-      const bool in_i = c * kC + i < T;
+      // P^T dO: P[t][i] is zero for t < i, so row i0 starts at the warp's first row 4 * warp
+      // and row i1 at 4 * warp + 32
+      const int tw = 4 * warp;
+      for (int t = tw; t < kC; ++t) {
+        const bool in = c * kC + t < T;
+        const float o0 = in ? bf(sOb[t * kRS + c0]) : 0.f;
+        const float o1 = in ? bf(sOb[t * kRS + c1]) : 0.f;
+        const float p0 = sP[t * LP + i0];
+        pd[0][0] += p0 * o0;
+        pd[0][1] += p0 * o1;
+        if (t >= tw + 32) {
+          const float p1 = sP[t * LP + i1];
+          pd[1][0] += p1 * o0;
+          pd[1][1] += p1 * o1;
+        }
+      }
+      const int ir[2] = {i0, i1}, cr[2] = {c0, c1};
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float w = scale * a[u] + dec_i * bs[u];
-        sW[i * kRS + rb + u] = w;
-        dW[cid * kC * DV + i * DV + r0 + rb + u] = w;
-        sOg[i * kRS + rb + u] = in_i ? scale * gam_i * bf(sOb[i * kRS + rb + u]) : 0.f;
+      for (int a = 0; a < 2; ++a) {
+        const int i = ir[a];
+        const float gi = sGr[i];
+        const float gam_i = __expf(gi), dec_i = __expf(gC - gi);
+        const bool in_i = c * kC + i < T;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float w = scale * pd[a][q] + dec_i * kd[a][q];
+          sW[i * kRS + cr[q]] = w;
+          dW[cid * kC * DV + i * DV + r0 + cr[q]] = w;
+          sOg[i * kRS + cr[q]] = in_i ? scale * gam_i * bf(sOb[i * kRS + cr[q]]) : 0.f;
+        }
       }
     }
     __syncthreads();   // dW is complete; P, K^, dO and the decays are free
     issue_a(c - 1);
     la_wait1();        // Q^, Y of chunk c
     __syncthreads();
-    // dS0 = gamma_C dS1 + sum_i (s gamma_i dO_ir) q^_i - sum_i dW_ir Y_i; thread: column x
+    // dS0 = gamma_C dS1 + sum_j (s gamma_j dO_jr) q^_j - sum_j dW_jr Y_j  (each thread reads
+    // and rewrites its own elements of the state gradient)
     {
-      constexpr int RPT = kRS * DK / 256;
-      const int x = tid % DK, rs = (tid / DK) * RPT;
-      float acc[RPT];
+      float4 acc[RPL];
 #pragma unroll
-      for (int u = 0; u < RPT; ++u) acc[u] = gam_C * sD[(rs + u) * LS + x];
+      for (int v = 0; v < RPL; ++v) {
+        const float4 sv = reinterpret_cast<const float4*>(sD + (rs * RPL + v) * LS)[cg];
+        acc[v] = make_float4(gam_C * sv.x, gam_C * sv.y, gam_C * sv.z, gam_C * sv.w);
+      }
+#pragma unroll 8
       for (int j = 0; j < kC; ++j) {
-        const float qv = sQ[j * LT + x], yv = sY[j * LT + x];
+        const float4 qv = reinterpret_cast<const float4*>(sQ + j * LT)[cg];
+        const float4 yv = reinterpret_cast<const float4*>(sY + j * LT)[cg];
+        float og[RPL], wv[RPL];
+        if constexpr (RPL == 2) {
+          const float2 o2 = *reinterpret_cast<const float2*>(sOg + j * kRS + 2 * rs);
+          const float2 w2 = *reinterpret_cast<const float2*>(sW + j * kRS + 2 * rs);
+          og[0] = o2.x;
+          og[1] = o2.y;
+          wv[0] = w2.x;
+          wv[1] = w2.y;
+        } else {
+          og[0] = sOg[j * kRS + rs];
+          wv[0] = sW[j * kRS + rs];
+        }
 #pragma unroll
-        for (int u = 0; u < RPT; ++u)
-          acc[u] += sOg[j * kRS + rs + u] * qv - sW[j * kRS + rs + u] * yv;
+        for (int v = 0; v < RPL; ++v) {
+          acc[v].x += og[v] * qv.x - wv[v] * yv.x;
+          acc[v].y += og[v] * qv.y - wv[v] * yv.y;
+          acc[v].z += og[v] * qv.z - wv[v] * yv.z;
+          acc[v].w += og[v] * qv.w - wv[v] * yv.w;
+        }
       }
 #pragma unroll
-      for (int u = 0; u < RPT; ++u) sD[(rs + u) * LS + x] = acc[u];
+      for (int v = 0; v < RPL; ++v)
+        reinterpret_cast<float4*>(sD + (rs * RPL + v) * LS)[cg] = acc[v];
     }
     __syncthreads();   // Q^ and Y are free
     issue_b(c - 1);
@@ -662,7 +713,7 @@ __global__ void __launch_bounds__(256) gdr_bwd_scan_kernel(
 
 template <int DK>
 constexpr size_t bwd_scan_smem_bytes() {
-  return (3 * kC * ScanLd<DK>::T + kC * ScanLd<DK>::P + kC + kC * kRS / 2 + kRS * Ld<DK>::v +
+  return (3 * kC * ScanLd<DK>::T + kC * ScanLd<DK>::P + kC + kC * kRS / 2 + kRS * ScanLd<DK>::T +
           2 * kC * kRS) * sizeof(float);
 }
 
