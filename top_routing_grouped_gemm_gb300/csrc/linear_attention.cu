@@ -773,33 +773,16 @@ __device__ __forceinline__ void mm_zero(float (&acc)[M / 16][N / 16]) {
     for (int c = 0; c < N / 16; ++c) acc[u][c] = 0.f;
 }
 
-// mm_nn with B in global memory, staged through shared memory 16 k rows at a time, so that
-// the CTA reads every element of B once (not once per row group): B(k, n) = Bg[k * ldb + n],
-// or Bg[n * ldb + k] with TRANS.  stage: 16 x (N + 4) floats.  Every thread of the block
-// must call it (it synchronises the block).
+// mm_nn with B in global memory, staged through shared memory 16 k rows at a time (see
+// Stager below: every element read once by the CTA, the next block loading while the
+// current one is used): B(k, n) = Bg[k * ldb + n], or Bg[n * ldb + k] with TRANS.  stage:
+// 16 x (N + 4) floats.  Every thread of the block must call it (it synchronises).
+template <int N, bool TRANS>
+struct Stager;
+
 template <int M, int N, bool TRANS, class FA>
 __device__ __forceinline__ void mm_nn_staged(int K, FA A, const float* __restrict__ Bg, int ldb,
-                                             float* stage, float (&acc)[M / 16][N / 16]) {
-  constexpr int LSG = N + 4;
-  for (int k0 = 0; k0 < K; k0 += 16) {
-    for (int e = threadIdx.x; e < 16 * N; e += 256) {
-      int kk, n;
-      if (TRANS) {
-        n = e >> 4;
-        kk = e & 15;
-      } else {
-        kk = e / N;
-        n = e - kk * N;
-      }
-      stage[kk * LSG + n] = TRANS ? __ldg(&Bg[static_cast<size_t>(n) * ldb + k0 + kk])
-                                  : __ldg(&Bg[static_cast<size_t>(k0 + kk) * ldb + n]);
-    }
-    __syncthreads();
-    mm_nn<M, N>(16, [&](int m, int k) { return A(m, k0 + k); },
-                [&](int k, int n) { return stage[k * LSG + n]; }, acc);
-    __syncthreads();
-  }
-}
+                                             float* stage, float (&acc)[M / 16][N / 16]);
 
 // Float4 form of the products: thread (ti, tj) owns rows ti + 16 u and the four consecutive
 // columns 64 g + 4 tj .. + 3 of every 64 (column c of the thread: bcol(tj, c)); A4(m, k)
@@ -837,29 +820,96 @@ __device__ __forceinline__ void mm_nn4(int K, FA4 A4, FB4 B4, float (&acc)[M / 1
   }
 }
 
-// mm_nn4 with B in global memory staged through shared memory (as mm_nn_staged)
+// 16 rows of a global matrix on their way to shared memory: each thread holds 16 N / 256
+// elements in registers, so that the next block's loads are in flight while the current
+// block is used.  Row kk, column n of the block is Bg[(k0 + kk) * ldb + n], or with TRANS
+// Bg[n * ldb + k0 + kk] (consecutive threads read consecutive addresses either way).
+template <int N, bool TRANS>
+struct Stager {
+  static constexpr int PER = 16 * N / 256;
+  static_assert(PER * 256 == 16 * N, "whole elements per thread");
+  float r[PER];
+  __device__ __forceinline__ static void where(int e, int& kk, int& n) {
+    if (TRANS) {
+      n = e >> 4;
+      kk = e & 15;
+    } else {
+      kk = e / N;
+      n = e - kk * N;
+    }
+  }
+  __device__ __forceinline__ void load(const float* __restrict__ Bg, int ldb, int k0) {
+#pragma unroll
+    for (int p = 0; p < PER; ++p) {
+      int kk, n;
+      where(threadIdx.x + 256 * p, kk, n);
+      r[p] = TRANS ? __ldg(&Bg[static_cast<size_t>(n) * ldb + k0 + kk])
+                   : __ldg(&Bg[static_cast<size_t>(k0 + kk) * ldb + n]);
+    }
+  }
+  __device__ __forceinline__ void store(float* stage) const {
+#pragma unroll
+    for (int p = 0; p < PER; ++p) {
+      int kk, n;
+      where(threadIdx.x + 256 * p, kk, n);
+      stage[kk * (N + 4) + n] = r[p];
+    }
+  }
+};
+
+template <int M, int N, bool TRANS, class FA>
+__device__ __forceinline__ void mm_nn_staged(int K, FA A, const float* __restrict__ Bg, int ldb,
+                                             float* stage, float (&acc)[M / 16][N / 16]) {
+  Stager<N, TRANS> st;
+  st.load(Bg, ldb, 0);
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    st.store(stage);
+    __syncthreads();
+    if (k0 + 16 < K) st.load(Bg, ldb, k0 + 16);
+    mm_nn<M, N>(16, [&](int m, int k) { return A(m, k0 + k); },
+                [&](int k, int n) { return stage[k * (N + 4) + n]; }, acc);
+    __syncthreads();
+  }
+}
+
+// mm_nn4 with B in global memory, staged through shared memory 16 k rows at a time (every
+// element read once by the CTA; the next block loads while the current one is used).
+// stage: 16 x (N + 4) floats.  Every thread of the block must call it (it synchronises).
 template <int M, int N, bool TRANS, class FA4>
 __device__ __forceinline__ void mm_nn4_staged(int K, FA4 A4, const float* __restrict__ Bg,
                                               int ldb, float* stage,
                                               float (&acc)[M / 16][N / 16]) {
-  constexpr int LSG = N + 4;
+  Stager<N, TRANS> st;
+  st.load(Bg, ldb, 0);
   for (int k0 = 0; k0 < K; k0 += 16) {
-    for (int e = threadIdx.x; e < 16 * N; e += 256) {
-      int kk, n;
-      if (TRANS) {
-        n = e >> 4;
-        kk = e & 15;
-      } else {
-        kk = e / N;
-        n = e - kk * N;
-      }
-      stage[kk * LSG + n] = TRANS ? __ldg(&Bg[static_cast<size_t>(n) * ldb + k0 + kk])
-                                  : __ldg(&Bg[static_cast<size_t>(k0 + kk) * ldb + n]);
-    }
+    st.store(stage);
     __syncthreads();
+    if (k0 + 16 < K) st.load(Bg, ldb, k0 + 16);
     mm_nn4<M, N>(16, [&](int m, int k) { return A4(m, k0 + k); },
-                 [&](int k, int n) { return *reinterpret_cast<const float4*>(stage + k * LSG + n); },
+                 [&](int k, int n) { return *reinterpret_cast<const float4*>(stage + k * (N + 4) + n); },
                  acc);
+    __syncthreads();
+  }
+}
+
+// mm_nn4 with A given transposed in global memory (A(m, k) = Ag[k * lda + m]), staged the
+// same way: stage holds 16 x (M + 4) floats.
+template <int M, int N, class FB4>
+__device__ __forceinline__ void mm_nn4_stagedA(int K, const float* __restrict__ Ag, int lda,
+                                               FB4 B4, float* stage,
+                                               float (&acc)[M / 16][N / 16]) {
+  Stager<M, false> st;
+  st.load(Ag, lda, 0);
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    st.store(stage);
+    __syncthreads();
+    if (k0 + 16 < K) st.load(Ag, lda, k0 + 16);
+    mm_nn4<M, N>(16,
+                 [&](int m, int k) {
+                   const float* col = stage + k * (M + 4) + m;
+                   return make_float4(col[0], col[M + 4], col[2 * (M + 4)], col[3 * (M + 4)]);
+                 },
+                 [&](int k, int n) { return B4(k0 + k, n); }, acc);
     __syncthreads();
   }
 }
@@ -1076,13 +1126,8 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
   {
     float acc[RU][CK];
     mm_zero<kC, DK>(acc);
-    mm_nn4<kC, DK>(kC,
-                   [&](int m, int i) {
-                     return make_float4(__ldg(&cA[i * kC + m]), __ldg(&cA[(i + 1) * kC + m]),
-                                        __ldg(&cA[(i + 2) * kC + m]),
-                                        __ldg(&cA[(i + 3) * kC + m]));
-                   },
-                   [&](int i, int n) { return ld4(sX + i * LX + n); }, acc);
+    mm_nn4_stagedA<kC, DK>(kC, cA, kC, [&](int i, int n) { return ld4(sX + i * LX + n); }, sStg,
+                           acc);
 #pragma unroll
     for (int u = 0; u < RU; ++u) {
       const int j = ti + 16 * u;
@@ -1108,13 +1153,8 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
   {
     float acc[RU][CV];
     mm_zero<kC, DV>(acc);
-    mm_nn4<kC, DV>(kC,
-                   [&](int m, int i) {
-                     return make_float4(__ldg(&cA[i * kC + m]), __ldg(&cA[(i + 1) * kC + m]),
-                                        __ldg(&cA[(i + 2) * kC + m]),
-                                        __ldg(&cA[(i + 3) * kC + m]));
-                   },
-                   [&](int i, int n) { return ld4(sdW + i * LV + n); }, acc);
+    mm_nn4_stagedA<kC, DV>(kC, cA, kC, [&](int i, int n) { return ld4(sdW + i * LV + n); },
+                           sStg, acc);
 #pragma unroll
     for (int u = 0; u < RU; ++u) {
       const int j = ti + 16 * u;
