@@ -81,6 +81,27 @@ struct GemmCfg {
                 "half B tiles stay whole boxes / swizzle atoms");
 };
 
+// 32 x 32 transpose across a warp: on entry lane l holds row l (v[j] = element (l, j)), on
+// exit column l (v[j] = element (j, l)).  Five butterfly stages: at stride s the lanes whose
+// bit s is set trade the s-wide off-diagonal blocks with their partner lane l ^ s.
+__device__ __forceinline__ void warp_transpose32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool up = (lane & s) != 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j & s) continue;
+      const float send = up ? v[j] : v[j | s];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, s);
+      if (up) {
+        v[j] = recv;
+      } else {
+        v[j | s] = recv;
+      }
+    }
+  }
+}
+
 struct TileCoord {
   int g, m, n, row0, rows_valid;
 };
@@ -963,40 +984,61 @@ __global__ void __launch_bounds__(256, CTAS) gemm_kernel(const __grid_constant__
           reinterpret_cast<float*>(P.out2)[row * P.n_tiles + tc.n] = hd;
       } else if constexpr (EPI == EPI_WGRAD) {
         // fp32 gradient of group g: [M, N] (ld N) or transposed [N, M] (ld M)
+        static_assert(BN % 32 == 0, "weight-gradient tiles are whole 32-column blocks");
 #pragma unroll 1
         for (int b = 0; b < NB; ++b) {
           float* o = reinterpret_cast<float*>(b == 0 ? P.out0 : P.out1);
           if (o == nullptr) continue;
           float* base = o + static_cast<size_t>(tc.g) * P.M * P.N;
-          const int m = tc.row0 + r_local;
+          if (P.out_transposed) {
+            // [N, M]: for each column the warp's 32 rows are 32 consecutive floats
+            const int m = tc.row0 + r_local;
 #pragma unroll 1
-          for (int c = 0; c < BN; c += 16) {
-            float v[16];
-            if (kr.nkb > 0) {
-              tmem_ld16(t_row + b * BN + c, v);
-              tmem_ld_wait();
-            } else {
+            for (int c = 0; c < BN; c += 16) {
+              float v[16];
+              if (kr.nkb > 0) {
+                tmem_ld16(t_row + b * BN + c, v);
+                tmem_ld_wait();
+              } else {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = 0.f;
-            }
-            const int col = col0 + c;
-            if (valid && col < P.N) {
-              if (P.out_transposed) {
+                for (int i = 0; i < 16; ++i) v[i] = 0.f;
+              }
+              const int col = col0 + c;
+              if (valid && col < P.N) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                   if (col + i < P.N) base[static_cast<size_t>(col + i) * P.M + m] = v[i];
-              } else {
-                float* dst = base + static_cast<size_t>(m) * P.N + col;
-                if (col + 16 <= P.N && (P.N & 3) == 0) {
-                  // the thread's row is contiguous: 16-byte stores
+              }
+            }
+          } else {
+            // [M, N]: each 32-column block of the warp's 32 rows is transposed across the warp
+            // (lane = column), so that every row leaves as one store of up to 128 contiguous
+            // bytes instead of 32 rows' pieces per store
+            const int m_w = tc.row0 + q * 32;
+#pragma unroll 1
+            for (int cb = 0; cb < BN; cb += 32) {
+              const int col = col0 + cb;
+              if (col >= P.N) break;  // warp-uniform
+              float v[32];
+              if (kr.nkb > 0) {
+                float v0[16], v1[16];
+                tmem_ld16(t_row + b * BN + cb, v0);
+                tmem_ld16(t_row + b * BN + cb + 16, v1);
+                tmem_ld_wait();
 #pragma unroll
-                  for (int i = 0; i < 16; i += 4)
-                    *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                } else {
-#pragma unroll
-                  for (int i = 0; i < 16; ++i)
-                    if (col + i < P.N) dst[i] = v[i];
+                for (int i = 0; i < 16; ++i) {
+                  v[i] = v0[i];
+                  v[16 + i] = v1[i];
                 }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+              }
+              warp_transpose32(v, lane);
+              if (col + lane < P.N) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (m_w + j < P.M) base[static_cast<size_t>(m_w + j) * P.N + col + lane] = v[j];
               }
             }
           }
