@@ -773,53 +773,6 @@ __device__ __forceinline__ void mm_zero(float (&acc)[M / 16][N / 16]) {
     for (int c = 0; c < N / 16; ++c) acc[u][c] = 0.f;
 }
 
-// mm_nn with B in global memory, staged through shared memory 16 k rows at a time (see
-// Stager below: every element read once by the CTA, the next block loading while the
-// current one is used): B(k, n) = Bg[k * ldb + n], or Bg[n * ldb + k] with TRANS.  stage:
-// 16 x (N + 4) floats.  Every thread of the block must call it (it synchronises).
-template <int N, bool TRANS>
-struct Stager;
-
-template <int M, int N, bool TRANS, class FA>
-__device__ __forceinline__ void mm_nn_staged(int K, FA A, const float* __restrict__ Bg, int ldb,
-                                             float* stage, float (&acc)[M / 16][N / 16]);
-
-// Float4 form of the products: thread (ti, tj) owns rows ti + 16 u and the four consecutive
-// columns 64 g + 4 tj .. + 3 of every 64 (column c of the thread: bcol(tj, c)); A4(m, k)
-// returns A(m, k .. k+3) and B4(k, n) returns B(k, n .. n+3) (k, n multiples of 4), so a k
-// step costs one 16-byte read per row and per column group.
-__device__ __forceinline__ int bcol(int tj, int c) { return (c >> 2) * 64 + 4 * tj + (c & 3); }
-
-template <int M, int N, class FA4, class FB4>
-__device__ __forceinline__ void mm_nn4(int K, FA4 A4, FB4 B4, float (&acc)[M / 16][N / 16]) {
-  static_assert(N % 64 == 0, "four consecutive columns per lane, 64 per row group");
-  constexpr int RA = M / 16, NG = N / 64;
-  const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
-#pragma unroll 2
-  for (int k = 0; k < K; k += 4) {
-    float4 a[RA];
-#pragma unroll
-    for (int u = 0; u < RA; ++u) a[u] = A4(ti + 16 * u, k);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      float4 bq[NG];
-#pragma unroll
-      for (int g = 0; g < NG; ++g) bq[g] = B4(k + kk, 64 * g + 4 * tj);
-#pragma unroll
-      for (int u = 0; u < RA; ++u) {
-        const float av = kk == 0 ? a[u].x : kk == 1 ? a[u].y : kk == 2 ? a[u].z : a[u].w;
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          acc[u][4 * g] += av * bq[g].x;
-          acc[u][4 * g + 1] += av * bq[g].y;
-          acc[u][4 * g + 2] += av * bq[g].z;
-          acc[u][4 * g + 3] += av * bq[g].w;
-        }
-      }
-    }
-  }
-}
-
 // 16 rows of a global matrix on their way to shared memory: each thread holds 16 N / 256
 // elements in registers, so that the next block's loads are in flight while the current
 // block is used.  Row kk, column n of the block is Bg[(k0 + kk) * ldb + n], or with TRANS
@@ -857,6 +810,10 @@ struct Stager {
   }
 };
 
+// mm_nn with B in global memory, staged through shared memory 16 k rows at a time (every
+// element read once by the CTA, the next block loading while the current one is used):
+// B(k, n) = Bg[k * ldb + n], or Bg[n * ldb + k] with TRANS.  stage: 16 x (N + 4) floats.
+// Every thread of the block must call it (it synchronises).
 template <int M, int N, bool TRANS, class FA>
 __device__ __forceinline__ void mm_nn_staged(int K, FA A, const float* __restrict__ Bg, int ldb,
                                              float* stage, float (&acc)[M / 16][N / 16]) {
@@ -869,6 +826,42 @@ __device__ __forceinline__ void mm_nn_staged(int K, FA A, const float* __restric
     mm_nn<M, N>(16, [&](int m, int k) { return A(m, k0 + k); },
                 [&](int k, int n) { return stage[k * (N + 4) + n]; }, acc);
     __syncthreads();
+  }
+}
+
+// Float4 form of the products: thread (ti, tj) owns rows ti + 16 u and the four consecutive
+// columns 64 g + 4 tj .. + 3 of every 64 (column c of the thread: bcol(tj, c)); A4(m, k)
+// returns A(m, k .. k+3) and B4(k, n) returns B(k, n .. n+3) (k, n multiples of 4), so a k
+// step costs one 16-byte read per row and per column group.
+__device__ __forceinline__ int bcol(int tj, int c) { return (c >> 2) * 64 + 4 * tj + (c & 3); }
+
+template <int M, int N, class FA4, class FB4>
+__device__ __forceinline__ void mm_nn4(int K, FA4 A4, FB4 B4, float (&acc)[M / 16][N / 16]) {
+  static_assert(N % 64 == 0, "four consecutive columns per lane, 64 per row group");
+  constexpr int RA = M / 16, NG = N / 64;
+  const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
+#pragma unroll 2
+  for (int k = 0; k < K; k += 4) {
+    float4 a[RA];
+#pragma unroll
+    for (int u = 0; u < RA; ++u) a[u] = A4(ti + 16 * u, k);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      float4 bq[NG];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) bq[g] = B4(k + kk, 64 * g + 4 * tj);
+#pragma unroll
+      for (int u = 0; u < RA; ++u) {
+        const float av = kk == 0 ? a[u].x : kk == 1 ? a[u].y : kk == 2 ? a[u].z : a[u].w;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          acc[u][4 * g] += av * bq[g].x;
+          acc[u][4 * g + 1] += av * bq[g].y;
+          acc[u][4 * g + 2] += av * bq[g].z;
+          acc[u][4 * g + 3] += av * bq[g].w;
+        }
+      }
+    }
   }
 }
 
