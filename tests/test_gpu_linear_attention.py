@@ -124,6 +124,8 @@ BWD_CASES = [
     synth.LAConfig("la_bwd_64x128", B=2, T=130, H=1, dk=64, dv=128),
     synth.LAConfig("la_bwd_128x64_one_chunk", B=1, T=64, H=3, dk=128, dv=64, with_state=True),
     synth.LAConfig("la_bwd_ragged", B=1, T=333, H=2, dk=64, dv=64),
+    # 16 chunks (the last of 40 tokens): the backward scan's chain over many steps
+    synth.LAConfig("la_bwd_long", B=1, T=1000, H=2, dk=128, dv=128, with_state=True),
 ]
 
 
