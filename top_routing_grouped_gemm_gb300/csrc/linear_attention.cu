@@ -985,15 +985,23 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
   const float* cA = Ai + cid * kC * kC;      // A^-1 (lower triangular, zeros above)
   auto row = [&](int i) { return ((static_cast<size_t>(b) * T + t0 + i) * H + h); };
 
-  for (int e = tid; e < kC * DK; e += 256) {
-    const int i = e / DK, x = e - i * DK;
-    sQ[i * LK + x] = Qh[cid * kC * DK + e];
-    sK[i * LK + x] = Kh[cid * kC * DK + e];
+  // the chunk's tiles, 16 bytes per load (rows of the shared tiles are 16-byte aligned)
+  for (int e = tid; e < kC * DK / 4; e += 256) {
+    const int i = e / (DK / 4), x = 4 * (e - i * (DK / 4));
+    *reinterpret_cast<float4*>(sQ + i * LK + x) = ldg4(Qh + cid * kC * DK + 4 * e);
+    *reinterpret_cast<float4*>(sK + i * LK + x) = ldg4(Kh + cid * kC * DK + 4 * e);
   }
-  for (int e = tid; e < kC * DV; e += 256) {
-    const int i = e / DV, r = e - i * DV;
-    sdW[i * LV + r] = dWg[cid * kC * DV + e];
-    sX[i * LX + r] = t0 + i < T ? bf(dO[row(i) * DV + r]) : 0.f;
+  for (int e = tid; e < kC * DV / 4; e += 256) {
+    const int i = e / (DV / 4), r = 4 * (e - i * (DV / 4));
+    *reinterpret_cast<float4*>(sdW + i * LV + r) = ldg4(dWg + cid * kC * DV + 4 * e);
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t0 + i < T) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(dO + row(i) * DV + r));
+      const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+      const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+      o = make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+    *reinterpret_cast<float4*>(sX + i * LX + r) = o;
   }
   if (tid < kC) {
     sG[tid] = Gc[cid * kC + tid];
@@ -1004,7 +1012,11 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
   // gamma_C <dS1, S0> (block reduction in a fixed order)
   {
     float a = 0.f;
-    for (int e = tid; e < DV * DK; e += 256) a += __ldg(&dS1[e]) * __ldg(&S0[e]);
+#pragma unroll 4
+    for (int e = tid; e < DV * DK / 4; e += 256) {
+      const float4 u = ldg4(dS1 + 4 * e), w = ldg4(S0 + 4 * e);
+      a += u.x * w.x + u.y * w.y + u.z * w.z + u.w * w.w;
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
     if (lane == 0) sRed[warp] = a;
