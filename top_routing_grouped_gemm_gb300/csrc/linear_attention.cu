@@ -300,13 +300,15 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
 // so both read the chunk-start state without a barrier between them).  The chunk tiles do
 // not depend on the state, so they stream in with cp.async while the other phase computes,
 // one shared buffer per tile: Y, Q^, the U slice and the log decays (phase 1) are reloaded
-// for the next chunk right after phase 1, P and K^ (phase 2) right after phase 2; each phase
-// waits only for the copies issued one phase earlier (wait_group 1: the later group may
-// still be in flight).  Each thread computes blocks of outputs from float4 shared reads that
+// for the next chunk right after phase 1, P and K^ (phase 2) right after phase 2; phase 1
+// waits only for its own group (wait_group 1: the later group may still be in flight), and
+// phase 2's group is waited for before the barrier that ends phase 1 (three barriers per
+// chunk).  Each thread computes blocks of outputs from float4 shared reads that
 // a warp shares (a few distinct 16-byte pieces per read), so that shared-memory bandwidth
 // is not what the chain of chunks waits on.
 __device__ __forceinline__ void la_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void la_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void la_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // rows x D fp32 tile (global row stride D) -> shared (row stride LDS, a multiple of 4)
 template <int ROWS, int D, int LDS>
@@ -435,10 +437,9 @@ __global__ void __launch_bounds__(256) gdr_scan_kernel(
         }
       }
     }
-    __syncthreads();   // W is complete; Y, Q^, U and the decays are free
+    la_wait0();        // this thread's copies of P, K^ of chunk c have landed
+    __syncthreads();   // W is complete; P, K^ are visible; Y, Q^, U and the decays are free
     issue_a(c + 1);
-    la_wait1();        // P, K^ of chunk c
-    __syncthreads();
     // phase 2a: O = scale (gamma_i Q^_i . S_r + sum_{j<=i} P_ij w_jr)  (P is zero above the
     // diagonal; i0 <= 4 * warp + 3 and i1 < 4 * warp + 36, so whole 4-token steps suffice)
     {
@@ -659,10 +660,9 @@ __global__ void __launch_bounds__(256) gdr_bwd_scan_kernel(
         }
       }
     }
-    __syncthreads();   // dW is complete; P, K^, dO and the decays are free
+    la_wait0();        // this thread's copies of Q^, Y of chunk c have landed
+    __syncthreads();   // dW is complete; Q^, Y are visible; P, K^, dO and the decays are free
     issue_a(c - 1);
-    la_wait1();        // Q^, Y of chunk c
-    __syncthreads();
     // dS0 = gamma_C dS1 + sum_j (s gamma_j dO_jr) q^_j - sum_j dW_jr Y_j  (each thread reads
     // and rewrites its own elements of the state gradient)
     {
