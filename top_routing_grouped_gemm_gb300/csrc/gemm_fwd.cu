@@ -25,7 +25,7 @@ int launch_gemm_router_topk(const GemmParams& P, int bn, cudaStream_t s) {
 // shape takes a gathered A operand.
 int launch_gemm_gateup(const GemmParams& P, int shape, cudaStream_t s) {
   if (shape != kTile128 && P.gather_slot != nullptr) return static_cast<int>(cudaErrorInvalidValue);
-  if (shape == kTilePair) return launch_gemm<128, 2, false, false, EPI_SWIGLU, 6, 1, 1, 2>(P, s);
+  if (shape == kTilePair) return launch_gemm<128, 2, false, false, EPI_SWIGLU, 7, 1, 1, 2>(P, s);
   if (shape == kTile256) return launch_gemm<128, 2, false, false, EPI_SWIGLU, 3, 1, 2>(P, s);
   return launch_gemm<128, 2, false, false, EPI_SWIGLU, 4>(P, s);
 }
