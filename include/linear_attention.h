@@ -22,9 +22,13 @@
  *   S_chunks [B, H, ceil(T/64), dv, dk] fp32 or NULL: the state at the start of every
  *   64-token chunk (what a backward pass restarts from).
  * Supported: dk and dv in {64, 128}; any T >= 1 (the last chunk may be partial).  A zero
- * q or k row is treated as a zero vector (no division by zero).  q, k, v, the workspace (and
- * the backward's d_o and S_chunks) must be 16-byte aligned (the kernels read them in 16-byte
- * pieces), else MOE_ERR_UNSUPPORTED.
+ * q or k row is treated as a zero vector (no division by zero).  q, k, v, the workspace, the
+ * forward's o (and the backward's d_o and S_chunks) must be 16-byte aligned (the kernels move
+ * them in 16-byte pieces), else MOE_ERR_UNSUPPORTED.
+ *
+ * Precision: the state and every accumulation are fp32.  The forward scan's products run on
+ * the tensor cores with each fp32 operand carried as two bf16 pieces (hi = bf16(x), mid =
+ * bf16(x - hi); three MMAs hi.hi + hi.mid + mid.hi): about 2^-16 relative per product.
  */
 #ifndef MOE_LINEAR_ATTENTION_H
 #define MOE_LINEAR_ATTENTION_H
@@ -44,11 +48,20 @@ size_t moe_gdr_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk, int32
 
 /* Forward of the gated delta rule over all B x H sequences (two launches: the per-chunk
  * factors of every chunk in parallel, then the scan over chunks in slices of 16 value rows
- * of the state). */
+ * of the state, on the tensor cores).  The scan's waits on its own tensor-core work are
+ * bounded; one that runs out ends the scan early and records MOE_ERR_TIMEOUT for
+ * moe_gdr_device_status. */
 int moe_gdr_forward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, const moe_bf16* q,
                     const moe_bf16* k, const moe_bf16* v, const float* beta, const float* g,
                     const float* S0, float scale, moe_bf16* o, float* S_T, float* S_chunks,
                     void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* Device-side status of the linear-attention kernels: waits for `stream`, writes the first
+ * error a kernel recorded since the previous call (MOE_OK if none; MOE_ERR_TIMEOUT when a
+ * bounded wait ran out, the outputs of that launch then being incomplete) to *status and
+ * clears it.  Returns MOE_ERR_INVALID_ARG for a NULL status, MOE_ERR_CUDA if the stream or
+ * the copy failed. */
+int moe_gdr_device_status(int32_t* status, moe_stream_t stream);
 
 /* Backward: gradients of <d_o, o> + <dS_T, S_T> with respect to q, k, v, beta, g and S0
  * (three launches: the per-chunk factors rebuilt, a backward scan over chunks for the state

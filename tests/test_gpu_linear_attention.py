@@ -13,8 +13,8 @@ from parity_util import f64, relerr
 
 pytestmark = pytest.mark.gpu
 
-RTOL_O = 5e-3      # o is rounded once to bf16 (fp32 arithmetic throughout)
-RTOL_S = 1e-4      # the fp32 state
+RTOL_O = 5e-3      # o is rounded once to bf16
+RTOL_S = 1e-4      # the fp32 state (the scan's products: two bf16 pieces per fp32 operand)
 
 
 def run_gdr(cfg, inp, checkpoints=False):
@@ -28,6 +28,7 @@ def run_gdr(cfg, inp, checkpoints=False):
     moe.moe_gdr_forward(B, T, H, dk, dv, dev["q"], dev["k"], dev["v"], dev["beta"], dev["g"],
                         dev["S0"], dk ** -0.5, o, ST, Sc, ws)
     torch.cuda.synchronize()
+    assert moe.moe_gdr_device_status() == moe.MOE_OK
     return o, ST, Sc
 
 

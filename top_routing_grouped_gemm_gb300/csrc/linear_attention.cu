@@ -18,8 +18,10 @@
 // U, Y and the masked Q^K^T depend only on the chunk, so they are computed for every chunk
 // at once (gdr_chunk_kernel); what needs the running state is a short scan over chunks, and
 // since each value row of the state evolves on its own (row r of S_t only involves v_t[r]),
-// the scan is split over slices of RS value rows (gdr_scan_kernel), so a few heads still
-// fill the GPU.  Everything after the bf16 inputs is fp32 (the state in particular).
+// the scan is split over slices of RS value rows (gdr_scan_tc_kernel), so a few heads still
+// fill the GPU.  Everything after the bf16 inputs is fp32 (the state in particular); the
+// forward scan's products run on the tensor cores with each fp32 operand carried as two bf16
+// pieces and fp32 accumulation.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -36,6 +38,124 @@ constexpr int kRS = 16;   // value rows of the state per scan CTA
 
 __device__ __forceinline__ float bf(const __nv_bfloat16 v) { return __bfloat162float(v); }
 
+// Byte offset of bf16 element (row, col) of a K-major [rows][64] block in the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw128_off(int row, int col) {
+  return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 +
+                               ((((col >> 3) ^ (row & 7)) << 4) | ((col & 7) << 1)));
+}
+
+__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& mid) {
+  hi = __float2bfloat16_rn(x);
+  mid = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
+
+__device__ int g_gdr_status;  // first error a linear-attention kernel reported (0: none)
+
+__device__ __forceinline__ void gdr_report(int code) { atomicCAS(&g_gdr_status, 0, code); }
+
+// Contiguous global -> shared bulk copy (the TMA unit, no tensor map), completing `bytes` of
+// transaction count on `bar`.  Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 32 lanes x 32 bits, 4 consecutive columns: thread i of the warp gets lane (base + i).
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Barrier `id` over the first `nthreads` threads of the block; true if `pred` held in any.
+__device__ __forceinline__ bool bar_sync_or(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbarrier.red.or.pred q, %2, %3, p;\n"
+      "selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// Sum of three accumulators 16 columns apart (columns taddr.., +16, +32), 4 columns each.
+__device__ __forceinline__ void tmem_ld_sum3(uint32_t taddr, float (&d)[4]) {
+  float a[4], b[4];
+  tmem_ld4(taddr, d);
+  tmem_ld4(taddr + 16, a);
+  tmem_ld4(taddr + 32, b);
+  tmem_ld_wait();
+#pragma unroll
+  for (int n = 0; n < 4; ++n) d[n] = (d[n] + a[n]) + b[n];
+}
+
+// Shared-memory image of one CTA of the tensor-core forward scan (gdr_scan_tc_kernel).  The
+// forward's gdr_chunk_kernel writes the scan's chunk tiles exactly as they sit here (the
+// 128-byte swizzle already applied: 16-byte piece p of a 128-byte row r at piece p ^ (r & 7),
+// 8-row atoms of 1024 B), so that each tile moves with one bulk copy.  Every fp32 value of
+// those tiles is carried as two bf16 pieces (hi, mid), each piece a tile of its own.
+// 16 consumer warps: warp w reads TMEM lanes 32 (w % 4) .. + 31 (its quadrant) and handles
+// value rows kTcCols (w / 4) .. + kTcCols - 1 of the slice, so each epilogue is spread over
+// four warps per scheduler; one more warp issues the bulk copies
+constexpr int kTcThreads = 512;
+constexpr int kTcCols = 4;
+constexpr int kTcBlock = kTcThreads + 32;
+
+template <int DK>
+struct TcScan {
+  static constexpr int NKB = DK / 64;                        // 64-wide blocks of a dk row
+  static constexpr uint32_t A1_SPLIT = NKB * 16384u;         // [Y; gamma Q^]: [128][64] per block
+  static constexpr uint32_t A1_BYTES = 2 * A1_SPLIT;
+  static constexpr uint32_t A3_SPLIT = NKB * 8192u;          // K^: [64 tokens][64 dk] per box
+  static constexpr uint32_t A3_BYTES = 2 * A3_SPLIT;
+  static constexpr uint32_t P_SPLIT = 8192u;                 // P: [64][64]
+  static constexpr uint32_t P_BYTES = 2 * P_SPLIT;
+  // B operands hold both pieces as one [32][64] K-major block (rows 0..15 hi, 16..31 mid):
+  // one N = 32 MMA takes hi.hi and hi.mid from a single read of the A tile
+  static constexpr uint32_t B1_KB = 4096u;                   // S slice: per 64-wide dk block
+  static constexpr uint32_t B1_BYTES = NKB * B1_KB;
+  static constexpr uint32_t BW_BYTES = 4096u;                // W, Wd: [32][64 tokens]
+  static constexpr uint32_t MID_ROWS = 2048u;                // offset of the mid rows
+  static constexpr uint32_t U_BYTES = kC * kRS * 4u;         // U slice [64][16] fp32
+  static constexpr uint32_t G_BYTES = kC * 4u;               // log decays [64] fp32
+  static constexpr uint32_t OFF_A1 = 0;                      // two buffers
+  static constexpr uint32_t OFF_A3 = 2 * A1_BYTES;
+  static constexpr uint32_t OFF_P = OFF_A3 + A3_BYTES;       // two buffers; 8 KB valid before
+  static constexpr uint32_t OFF_B1 = OFF_P + 2 * P_BYTES;
+  static constexpr uint32_t OFF_B2 = OFF_B1 + B1_BYTES;
+  static constexpr uint32_t OFF_B3 = OFF_B2 + BW_BYTES;
+  static constexpr uint32_t OFF_U = OFF_B3 + BW_BYTES;       // two buffers
+  static constexpr uint32_t OFF_G = OFF_U + 2 * U_BYTES;     // two buffers
+  static constexpr uint32_t OFF_BAR = OFF_G + 2 * G_BYTES;   // 12 mbarriers, TMEM slot, flag
+  static constexpr uint32_t BYTES = OFF_BAR + 128u;
+  static constexpr size_t SMEM = BYTES + 1024u;              // 1024-byte alignment slack
+  static_assert(OFF_A3 % 1024 == 0 && OFF_P % 1024 == 0 && OFF_B1 % 1024 == 0 &&
+                    OFF_B2 % 1024 == 0 && OFF_B3 % 1024 == 0 && OFF_U % 16 == 0,
+                "swizzled tiles start on 1024-byte atoms");
+  // the MN-major K^T operand reads a second 64-wide box 8 KB on even when dk = 64 (its rows
+  // feed D3 lanes 64..127, which are not read): that box must lie in the buffer
+  static_assert(OFF_A3 + A3_SPLIT + 16384u <= BYTES, "A3's second box stays in shared memory");
+  static_assert(SMEM <= 227u * 1024u, "fits one CTA per SM");
+  // bf16 element offsets within one chunk's image: piece s, row, column
+  __device__ static uint32_t a1(int s, int m, int x) {
+    return (s * A1_SPLIT + (x >> 6) * 16384u + sw128_off(m, x & 63)) >> 1;
+  }
+  __device__ static uint32_t a3(int s, int j, int x) {
+    return (s * A3_SPLIT + (x >> 6) * 8192u + sw128_off(j, x & 63)) >> 1;
+  }
+  __device__ static uint32_t p(int s, int i, int j) {
+    return (s * P_SPLIT + sw128_off(i, j)) >> 1;
+  }
+};
+
 // Rows of the fp32 tiles in shared memory are padded to an odd stride, so that a warp
 // reading one column of 32 rows touches 32 different banks.
 template <int D>
@@ -46,13 +166,19 @@ struct Ld {
 // Per chunk (grid: chunks x H x B, 256 threads): q^, k^, cumulative log decay, the WY
 // factors U, Y, the masked P = Gam . tril(Q^ K^T) (diagonal included), all fp32 to the
 // workspace.  Rows past the end of the sequence are zero (beta = g = 0: no effect).
-template <int DK, int DV>
+// SPLIT (the forward): Y, gamma Q^, K^ and P go out instead as the tensor-core scan's
+// shared-memory images (TcScan): each fp32 value as two bf16 pieces (hi, mid), per chunk
+// YQs (rows 0..63 Y, 64..127 diag(gamma) Q^), Ks and Ps; U as fp32 slices of 16 value rows,
+// [slice][64][16] per chunk; the log decays as fp32.
+template <int DK, int DV, bool SPLIT>
 __global__ void __launch_bounds__(256) gdr_chunk_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ beta,
     const float* __restrict__ g, int T, int H, int nch, float* __restrict__ Qh,
     float* __restrict__ Kh, float* __restrict__ Y, float* __restrict__ U,
-    float* __restrict__ Pm, float* __restrict__ Gc, float* __restrict__ Ai) {
+    float* __restrict__ Pm, float* __restrict__ Gc, float* __restrict__ Ai,
+    __nv_bfloat16* __restrict__ YQs, __nv_bfloat16* __restrict__ Ks,
+    __nv_bfloat16* __restrict__ Ps) {
   constexpr int LK = Ld<DK>::v, LC = Ld<kC>::v;
   extern __shared__ float sm[];
   float* sK = sm;                    // [C][LK]
@@ -185,7 +311,15 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
           pv = gam * aq[a][c2];
         }
         sA[i * LC + j] = av;
-        Pm[chunk_id * kC * kC + i * kC + j] = pv;
+        if constexpr (SPLIT) {
+          using L = TcScan<DK>;
+          __nv_bfloat16 hi, mid;
+          split_bf16(pv, hi, mid);
+          Ps[chunk_id * (L::P_BYTES / 2) + L::p(0, i, j)] = hi;
+          Ps[chunk_id * (L::P_BYTES / 2) + L::p(1, i, j)] = mid;
+        } else {
+          Pm[chunk_id * kC * kC + i * kC + j] = pv;
+        }
       }
   }
   __syncthreads();
@@ -205,11 +339,32 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
       __syncwarp();
     }
   }
-  // q^, k^ out for the scan; then K^ rows scaled by beta gamma in place
-  for (int e = tid; e < kC * DK; e += 256) {
-    const int i = e / DK, x = e - i * DK;
-    Qh[chunk_id * kC * DK + e] = sQ[i * LK + x];
-    Kh[chunk_id * kC * DK + e] = sK[i * LK + x];
+  // q^, k^ out for the scan (SPLIT: gamma q^ and k^ in two bf16 pieces); then K^ rows
+  // scaled by beta gamma in place
+  if constexpr (SPLIT) {
+    // (x, x + 1) share a 16-byte piece of the swizzled images: one 4-byte store per piece
+    using L = TcScan<DK>;
+    __nv_bfloat16* yq = YQs + chunk_id * (L::A1_BYTES / 2);
+    __nv_bfloat16* ko = Ks + chunk_id * (L::A3_BYTES / 2);
+    for (int e = tid; e < kC * DK / 2; e += 256) {
+      const int i = (2 * e) / DK, x = 2 * e - i * DK;
+      const float gam = __expf(sG[i]);
+      __nv_bfloat16 h0, m0, h1, m1;
+      split_bf16(gam * sQ[i * LK + x], h0, m0);
+      split_bf16(gam * sQ[i * LK + x + 1], h1, m1);
+      *reinterpret_cast<__nv_bfloat162*>(yq + L::a1(0, 64 + i, x)) = __halves2bfloat162(h0, h1);
+      *reinterpret_cast<__nv_bfloat162*>(yq + L::a1(1, 64 + i, x)) = __halves2bfloat162(m0, m1);
+      split_bf16(sK[i * LK + x], h0, m0);
+      split_bf16(sK[i * LK + x + 1], h1, m1);
+      *reinterpret_cast<__nv_bfloat162*>(ko + L::a3(0, i, x)) = __halves2bfloat162(h0, h1);
+      *reinterpret_cast<__nv_bfloat162*>(ko + L::a3(1, i, x)) = __halves2bfloat162(m0, m1);
+    }
+  } else {
+    for (int e = tid; e < kC * DK; e += 256) {
+      const int i = e / DK, x = e - i * DK;
+      Qh[chunk_id * kC * DK + e] = sQ[i * LK + x];
+      Kh[chunk_id * kC * DK + e] = sK[i * LK + x];
+    }
   }
   __syncthreads();
   for (int e = tid; e < kC * DK; e += 256) {
@@ -241,7 +396,18 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
-      for (int u = 0; u < TX; ++u) Y[chunk_id * kC * DK + (4 * ti + a) * DK + tx + 16 * u] = acc[a][u];
+      for (int u = 0; u < TX; ++u) {
+        const int row = 4 * ti + a, col = tx + 16 * u;
+        if constexpr (SPLIT) {
+          using L = TcScan<DK>;
+          __nv_bfloat16 hi, mid;
+          split_bf16(acc[a][u], hi, mid);
+          YQs[chunk_id * (L::A1_BYTES / 2) + L::a1(0, row, col)] = hi;
+          YQs[chunk_id * (L::A1_BYTES / 2) + L::a1(1, row, col)] = mid;
+        } else {
+          Y[chunk_id * kC * DK + row * DK + col] = acc[a][u];
+        }
+      }
   }
   __syncthreads();
   // V rows (beta-scaled) into the space of the K and Q tiles (no longer needed), then
@@ -283,29 +449,21 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
-      for (int u = 0; u < TX; ++u) U[chunk_id * kC * DV + (4 * ti + a) * DV + tx + 16 * u] = acc[a][u];
+      for (int u = 0; u < TX; ++u) {
+        const int row = 4 * ti + a, col = tx + 16 * u;
+        static_assert(kRS == 16, "U slices are this tiling's 16-column groups");
+        if constexpr (SPLIT)  // slice u of 16 value rows, column tx
+          U[((chunk_id * (DV / kRS) + u) * kC + row) * kRS + tx] = acc[a][u];
+        else
+          U[chunk_id * kC * DV + row * DV + col] = acc[a][u];
+      }
   }
   if (tid < kC) Gc[chunk_id * kC + tid] = sG[tid];
   if (Ai)
     for (int e = tid; e < kC * kC; e += 256) Ai[chunk_id * kC * kC + e] = sI[(e / kC) * LC + (e % kC)];
 }
 
-// Scan over the chunks of one (b, h) for RS value rows of the state (grid: DV/RS x H x B,
-// 256 threads).  Per chunk: W = U - Y S^T, O = scale (gamma Q^ S^T + P W), then
-// S = gamma_C S + sum_j exp(G_C - G_j) w_j k^_j^T.  S_chunks (optional) receives the state
-// at every chunk start (the backward's checkpoints).
-//
-// Two phases per chunk: W and Q^ S^T (both products with the chunk-start state), then the
-// output and the state update together (the update writes the other of two state buffers,
-// so both read the chunk-start state without a barrier between them).  The chunk tiles do
-// not depend on the state, so they stream in with cp.async while the other phase computes,
-// one shared buffer per tile: Y, Q^, the U slice and the log decays (phase 1) are reloaded
-// for the next chunk right after phase 1, P and K^ (phase 2) right after phase 2; phase 1
-// waits only for its own group (wait_group 1: the later group may still be in flight), and
-// phase 2's group is waited for before the barrier that ends phase 1 (three barriers per
-// chunk).  Each thread computes blocks of outputs from float4 shared reads that
-// a warp shares (a few distinct 16-byte pieces per read), so that shared-memory bandwidth
-// is not what the chain of chunks waits on.
+// cp.async groups of the scans' streamed chunk tiles.
 __device__ __forceinline__ void la_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void la_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void la_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
@@ -320,205 +478,304 @@ __device__ __forceinline__ void tile_async(float* dst, const float* src, int src
   }
 }
 
+// fp32 tile strides of the backward scan
 template <int DK>
 struct ScanLd {
   static constexpr int T = DK + 4;  // streamed tiles: 16-byte rows (bank offset 4 per row)
   static constexpr int P = kC + 4;
 };
 
+// Scan over the chunks of one (b, h) for RS = 16 value rows of the state (grid: DV/RS x H x B,
+// 16 consumer warps and a copy warp), on the tensor cores.  Per chunk, with S the slice of
+// the chunk-start state:
+//     D1 = [Y; diag(gamma) Q^] S^T                      (M = 128 token rows, N = 16, K = dk)
+//     W  = U - D1[0:64],  Wd = diag(gamma_C / gamma) W
+//     D3 = K^T Wd         ->  S^T = gamma_C S^T + D3     (M = dk, K = 64 tokens)
+//     D1[64:128] += P W   ->  O = scale D1[64:128]       (K = 64 tokens)
+// S_chunks (optional) receives the state at every chunk start (the backward's checkpoints).
+//
+// Each product is the three MMAs hi.hi + hi.mid + mid.hi of the operands' bf16 pieces,
+// accumulated in fp32 in TMEM (about 16 significant bits per operand where one bf16 MMA
+// keeps 8); the state and W are split by the threads that hold them.  TMEM lane x is row x
+// of D3 (the state's column x, kept in registers across chunks) and row x of D1 (W's token
+// row for x < 64, the output's row x - 64 above); the four warps reading a lane quadrant take
+// four value rows each.  One staged [64 tokens][dk] tile of K^ serves as the MN-major A
+// operand of K^T Wd (64-wide dk boxes 8 KB apart); a P tile is read as rows 64..127 of a
+// 128-row A operand whose first 64 rows (the 8 KB before it) only feed D1 rows that W has
+// already been read from.
+//
+// The chain from one chunk's state to the next is D1 -> W -> D3 -> S; P W and the output
+// are off it: their MMAs are issued after K^T Wd, and D1 is double-buffered in TMEM so
+// that the output rows of chunk c are read (by the warps of lane quadrants 2 and 3) while
+// the warps of quadrants 0 and 1 form W of chunk c + 1.  The copy warp streams the chunk
+// tiles through full / empty mbarrier pairs: [Y; gamma Q^] with the U slice and the log
+// decays, and P, two buffers each; K^ one buffer, refilled as soon as K^T Wd completes.
 template <int DK, int DV>
-__global__ void __launch_bounds__(256) gdr_scan_kernel(
-    const float* __restrict__ Qh, const float* __restrict__ Kh, const float* __restrict__ Y,
-    const float* __restrict__ U, const float* __restrict__ Pm, const float* __restrict__ Gc,
-    const float* __restrict__ S0, int T, int H, int nch, float scale,
-    __nv_bfloat16* __restrict__ o, float* __restrict__ ST, float* __restrict__ Schk) {
-  constexpr int LT = ScanLd<DK>::T, LP = ScanLd<DK>::P;
-  constexpr int LS = ScanLd<DK>::T;  // state rows: 16-byte aligned (read as float4)
-  constexpr int LW = kC + 4;         // rows of W^T (one per value row, over the chunk's tokens)
-  extern __shared__ float4 sm4[];
-  float* sm = reinterpret_cast<float*>(sm4);
-  float* sQ = sm;                   // [C][LT]
-  float* sK = sQ + kC * LT;         // [C][LT]
-  float* sY = sK + kC * LT;         // [C][LT]
-  float* sP = sY + kC * LT;         // [C][LP]
-  float* sU = sP + kC * LP;         // [C][RS] U slice
-  float* sGr = sU + kC * kRS;       // [C] log decays
-  float* sSb = sGr + kC;            // 2 x [RS][LS] state rows (ping-pong over chunks)
-  float* sWT = sSb + 2 * kRS * LS;  // [RS][LW]: W^T
-  float* sWd = sWT + kRS * LW;      // [C][RS]: W decayed to the chunk end
-  static_assert(kRS == 16 && kC == 64 && DK % 32 == 0, "thread tiling");
+__global__ void __launch_bounds__(kTcBlock, 1) gdr_scan_tc_kernel(
+    const __nv_bfloat16* __restrict__ YQs, const __nv_bfloat16* __restrict__ Ks,
+    const __nv_bfloat16* __restrict__ Ps, const float* __restrict__ Us,
+    const float* __restrict__ Gc, const float* __restrict__ S0, int T, int H, int nch,
+    float scale, __nv_bfloat16* __restrict__ o, float* __restrict__ ST,
+    float* __restrict__ Schk) {
+  using L = TcScan<DK>;
+  constexpr int NKB = L::NKB;
+  extern __shared__ uint8_t tc_smem_raw[];
+  const uint32_t raw = smem_u32(tc_smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = tc_smem_raw + (sbase - raw);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* d1_done = &bar[0];   // group 1 (and everything issued before it) complete
+  uint64_t* d3_done = &bar[1];   // K^T Wd complete
+  uint64_t* full_a = &bar[2];    // [2] [Y; gamma Q^], U slice, log decays landed
+  uint64_t* full_k = &bar[4];    // K^ landed
+  uint64_t* full_p = &bar[5];    // [2] P landed
+  uint64_t* empty_a = &bar[7];   // [2] buffer a free (its chunk's W formed)
+  uint64_t* empty_k = &bar[9];   // K^ free (K^T Wd complete)
+  uint64_t* empty_p = &bar[10];  // [2] P buffer free (P W complete)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_BAR + 96);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 100);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int x = 32 * (warp & 3) + (tid & 31);  // TMEM lane: token row of D1, dk column of D3
+  const int n0 = kTcCols * ((warp >> 2) & 3);  // this thread's first value row of the slice
   const int r0 = blockIdx.x * kRS, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x;
   const size_t bh = static_cast<size_t>(b) * H + h;
-  auto issue_a = [&](int c) {  // Y, Q^, U slice, log decays (phase 1)
-    if (c < nch) {
-      const size_t cid = bh * nch + c;
-      tile_async<kC, DK, LT>(sY, Y + cid * kC * DK, DK, tid);
-      tile_async<kC, DK, LT>(sQ, Qh + cid * kC * DK, DK, tid);
-      tile_async<kC, kRS, kRS>(sU, U + cid * kC * DV + r0, DV, tid);
-      tile_async<1, kC, kC>(sGr, Gc + cid * kC, kC, tid);
-    }
-    la_commit();
-  };
-  auto issue_b = [&](int c) {  // P, K^ (phase 2)
-    if (c < nch) {
-      const size_t cid = bh * nch + c;
-      tile_async<kC, kC, LP>(sP, Pm + cid * kC * kC, kC, tid);
-      tile_async<kC, DK, LT>(sK, Kh + cid * kC * DK, DK, tid);
-    }
-    la_commit();
-  };
-  for (int e = tid; e < kRS * DK; e += 256) {
-    const int r = e / DK, x = e - r * DK;
-    sSb[r * LS + x] = S0 ? S0[(bh * DV + r0 + r) * DK + x] : 0.f;
-  }
-  issue_a(0);
-  issue_b(0);
-  // Phases 1 and 2a: this thread's token rows i0 = tid / 8 and i1 = i0 + 32 and value rows
-  // c0 = tid % 8 and c1 = c0 + 8 (a warp reads four token rows and eight state rows per step:
-  // one shared-memory wavefront each).
-  const int cq = tid & 7, i0 = tid >> 3, i1 = i0 + 32;
-  const int c0 = cq, c1 = cq + 8;
-  // Phase 2b: value rows rs * RPL .. + RPL - 1, float4 column group cg (a warp reads GW
-  // column groups of K^ and RSEL row pieces of the decayed W per token: one wavefront each).
-  constexpr int GW = DK / 32;          // column groups per warp
-  constexpr int RSEL = 32 / GW;        // row selectors per warp
-  constexpr int RPL = kRS / RSEL;      // rows per lane (2 for DK 128, 1 for 64)
-  static_assert(RPL * RSEL == kRS && (RPL == 1 || RPL == 2), "state update tiling");
-  const int lane = tid & 31, warp = tid >> 5;
-  const int cg = warp * GW + lane / RSEL, rs = lane % RSEL;
-  for (int c = 0; c < nch; ++c) {
-    const size_t cid = bh * nch + c;
-    const float* sS = sSb + (c & 1) * kRS * LS;      // state at the chunk start
-    float* sSn = sSb + ((c & 1) ^ 1) * kRS * LS;     // state at the chunk end
-    la_wait1();        // Y, Q^, U, decays of chunk c
-    __syncthreads();   // (everyone's copies; the previous chunk is done with every tile)
-    const float gC = sGr[kC - 1];
-    const float gam_C = __expf(gC);
-    if (Schk)
-      for (int e = tid; e < kRS * DK; e += 256) {
-        const int r = e / DK, x = e - r * DK;
-        Schk[(cid * DV + r0 + r) * DK + x] = sS[r * LS + x];
-      }
-    // phase 1: Y S^T and Q^ S^T for rows i0, i1 and value rows c0, c1; W = U - Y S^T
-    float oq[2][2];
-    {
-      float gy[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, gq[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-      const float4* y0 = reinterpret_cast<const float4*>(sY + i0 * LT);
-      const float4* y1 = reinterpret_cast<const float4*>(sY + i1 * LT);
-      const float4* q0 = reinterpret_cast<const float4*>(sQ + i0 * LT);
-      const float4* q1 = reinterpret_cast<const float4*>(sQ + i1 * LT);
-      const float4* s0 = reinterpret_cast<const float4*>(sS + c0 * LS);
-      const float4* s1 = reinterpret_cast<const float4*>(sS + c1 * LS);
-#pragma unroll 4
-      for (int x4 = 0; x4 < DK / 4; ++x4) {
-        const float4 a0 = y0[x4], a1 = y1[x4], b0 = q0[x4], b1 = q1[x4];
-        const float4 u0 = s0[x4], u1 = s1[x4];
-        gy[0][0] += a0.x * u0.x + a0.y * u0.y + a0.z * u0.z + a0.w * u0.w;
-        gy[0][1] += a0.x * u1.x + a0.y * u1.y + a0.z * u1.z + a0.w * u1.w;
-        gy[1][0] += a1.x * u0.x + a1.y * u0.y + a1.z * u0.z + a1.w * u0.w;
-        gy[1][1] += a1.x * u1.x + a1.y * u1.y + a1.z * u1.z + a1.w * u1.w;
-        gq[0][0] += b0.x * u0.x + b0.y * u0.y + b0.z * u0.z + b0.w * u0.w;
-        gq[0][1] += b0.x * u1.x + b0.y * u1.y + b0.z * u1.z + b0.w * u1.w;
-        gq[1][0] += b1.x * u0.x + b1.y * u0.y + b1.z * u0.z + b1.w * u0.w;
-        gq[1][1] += b1.x * u1.x + b1.y * u1.y + b1.z * u1.z + b1.w * u1.w;
-      }
-      const int ir[2] = {i0, i1}, cr[2] = {c0, c1};
-#pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        const float gi = sGr[ir[a]];
-        const float gam_i = __expf(gi), dec_i = __expf(gC - gi);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const float w = sU[ir[a] * kRS + cr[q]] - gy[a][q];
-          sWT[cr[q] * LW + ir[a]] = w;
-          sWd[ir[a] * kRS + cr[q]] = w * dec_i;
-          oq[a][q] = gam_i * gq[a][q];
-        }
-      }
-    }
-    la_wait0();        // this thread's copies of P, K^ of chunk c have landed
-    __syncthreads();   // W is complete; P, K^ are visible; Y, Q^, U and the decays are free
-    issue_a(c + 1);
-    // phase 2a: O = scale (gamma_i Q^_i . S_r + sum_{j<=i} P_ij w_jr)  (P is zero above the
-    // diagonal; i0 <= 4 * warp + 3 and i1 < 4 * warp + 36, so whole 4-token steps suffice)
-    {
-      const float* p0 = sP + i0 * LP;
-      const float* p1 = sP + i1 * LP;
-      const float* w0 = sWT + c0 * LW;
-      const float* w1 = sWT + c1 * LW;
-      for (int j0 = 0; j0 <= i1; j0 += 4) {
-        const float4 wa = *reinterpret_cast<const float4*>(w0 + j0);
-        const float4 wb = *reinterpret_cast<const float4*>(w1 + j0);
-        const float4 pb = *reinterpret_cast<const float4*>(p1 + j0);
-        oq[1][0] += pb.x * wa.x + pb.y * wa.y + pb.z * wa.z + pb.w * wa.w;
-        oq[1][1] += pb.x * wb.x + pb.y * wb.y + pb.z * wb.z + pb.w * wb.w;
-        if (j0 <= i0) {
-          const float4 pa = *reinterpret_cast<const float4*>(p0 + j0);
-          oq[0][0] += pa.x * wa.x + pa.y * wa.y + pa.z * wa.z + pa.w * wa.w;
-          oq[0][1] += pa.x * wb.x + pa.y * wb.y + pa.z * wb.z + pa.w * wb.w;
-        }
-      }
-      const int ir[2] = {i0, i1}, cr[2] = {c0, c1};
-#pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        const int t = c * kC + ir[a];
-        if (t < T) {
-          __nv_bfloat16* orow = o + ((static_cast<size_t>(b) * T + t) * H + h) * DV + r0;
-#pragma unroll
-          for (int q = 0; q < 2; ++q) orow[cr[q]] = __float2bfloat16_rn(scale * oq[a][q]);
-        }
-      }
-    }
-    // phase 2b (same phase: it writes the other state buffer):
-    // S_r = gamma_C S_r + sum_j (gamma_C / gamma_j) w_jr k^_j
-    {
-      float4 acc[RPL];
-#pragma unroll
-      for (int v = 0; v < RPL; ++v) {
-        const float4 sv = reinterpret_cast<const float4*>(sS + (rs * RPL + v) * LS)[cg];
-        acc[v] = make_float4(gam_C * sv.x, gam_C * sv.y, gam_C * sv.z, gam_C * sv.w);
-      }
-#pragma unroll 8
-      for (int j = 0; j < kC; ++j) {
-        const float4 kv = reinterpret_cast<const float4*>(sK + j * LT)[cg];
-        float wd[RPL];
-        if constexpr (RPL == 2) {
-          const float2 w2 = *reinterpret_cast<const float2*>(sWd + j * kRS + 2 * rs);
-          wd[0] = w2.x;
-          wd[1] = w2.y;
-        } else {
-          wd[0] = sWd[j * kRS + rs];
-        }
-#pragma unroll
-        for (int v = 0; v < RPL; ++v) {
-          acc[v].x += wd[v] * kv.x;
-          acc[v].y += wd[v] * kv.y;
-          acc[v].z += wd[v] * kv.z;
-          acc[v].w += wd[v] * kv.w;
-        }
-      }
-#pragma unroll
-      for (int v = 0; v < RPL; ++v)
-        reinterpret_cast<float4*>(sSn + (rs * RPL + v) * LS)[cg] = acc[v];
-    }
-    __syncthreads();   // P and K^ are free (the next chunk's first barrier orders the state)
-    issue_b(c + 1);
-  }
-  __syncthreads();
-  if (ST) {
-    const float* sS = sSb + (nch & 1) * kRS * LS;
-    for (int e = tid; e < kRS * DK; e += 256) {
-      const int r = e / DK, x = e - r * DK;
-      ST[(bh * DV + r0 + r) * DK + x] = sS[r * LS + x];
-    }
-  }
-}
+  static_assert(kTcCols * (kTcThreads / 128) == kRS, "four warps per quadrant cover the slice");
 
-template <int DK>
-constexpr size_t scan_smem_bytes() {
-  return (3 * kC * ScanLd<DK>::T + kC * ScanLd<DK>::P + kC * kRS + kC +
-          2 * kRS * ScanLd<DK>::T + kRS * (kC + 4) + kC * kRS) * sizeof(float);
+  if (tid == 0) {
+#pragma unroll
+    for (int i = 0; i < 12; ++i) mbar_init(&bar[i], 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  // D1 buffers at columns 0 and 64 (each three accumulators of 16: hi.hi, hi.mid, mid.hi),
+  // D3 at 128; summed when read
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_d3 = tmem + 128;
+  bool failed = false;
+  // copy warp: the last copy issued on each full barrier and the phase it completes (bits 0,
+  // 1: full_a; 2: full_k; 3, 4: full_p), for the drain after an abort
+  uint32_t sent = 0, par = 0;
+
+  if (warp == kTcThreads / 32) {
+    // ------------------------------------------------------------ copy warp
+    if ((tid & 31) == 0) {
+      auto note = [&](int i, uint32_t phase) {
+        sent |= 1u << i;
+        par = (par & ~(1u << i)) | (phase << i);
+      };
+      for (int c = 0; c < nch && !failed; ++c) {
+        const int buf = c & 1;
+        const uint32_t use = static_cast<uint32_t>(c >> 1);
+        const size_t cid = bh * nch + c;
+        if (c >= 2 && !mbar_wait(&empty_a[buf], (use - 1) & 1, abort_flag)) { failed = true; break; }
+        mbar_arrive_expect_tx(&full_a[buf], L::A1_BYTES + L::U_BYTES + L::G_BYTES);
+        bulk_load(smem + L::OFF_A1 + buf * L::A1_BYTES, YQs + cid * (L::A1_BYTES / 2),
+                  L::A1_BYTES, &full_a[buf]);
+        bulk_load(smem + L::OFF_U + buf * L::U_BYTES,
+                  Us + (cid * (DV / kRS) + blockIdx.x) * (kC * kRS), L::U_BYTES, &full_a[buf]);
+        bulk_load(smem + L::OFF_G + buf * L::G_BYTES, Gc + cid * kC, L::G_BYTES, &full_a[buf]);
+        note(buf, use & 1);
+        if (c >= 1 && !mbar_wait(empty_k, (c - 1) & 1, abort_flag)) { failed = true; break; }
+        mbar_arrive_expect_tx(full_k, L::A3_BYTES);
+        bulk_load(smem + L::OFF_A3, Ks + cid * (L::A3_BYTES / 2), L::A3_BYTES, full_k);
+        note(2, c & 1);
+        if (c >= 2 && !mbar_wait(&empty_p[buf], (use - 1) & 1, abort_flag)) { failed = true; break; }
+        mbar_arrive_expect_tx(&full_p[buf], L::P_BYTES);
+        bulk_load(smem + L::OFF_P + buf * L::P_BYTES, Ps + cid * (L::P_BYTES / 2), L::P_BYTES,
+                  &full_p[buf]);
+        note(3 + buf, use & 1);
+      }
+      if (failed) *abort_flag = 1;
+    }
+  } else {
+    // ------------------------------------------------------------ consumer warps
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    // this thread's part of the state: column x for value rows n0 .. n0 + 3, in registers
+    // across chunks
+    const bool own_col = x < DK;
+    float S[kTcCols];
+#pragma unroll
+    for (int n = 0; n < kTcCols; ++n)
+      S[n] = (own_col && S0) ? S0[(bh * DV + r0 + n0 + n) * DK + x] : 0.f;
+    auto write_state_operand = [&]() {  // S^T -> B1 (K-major [16 rows][dk], both pieces)
+      if (own_col) {
+        const int kb = x >> 6, col = x & 63;
+#pragma unroll
+        for (int n = 0; n < kTcCols; ++n) {
+          __nv_bfloat16 hi, mid;
+          split_bf16(S[n], hi, mid);
+          const uint32_t off = L::OFF_B1 + kb * L::B1_KB + sw128_off(n0 + n, col);
+          *reinterpret_cast<__nv_bfloat16*>(smem + off) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(smem + off + L::MID_ROWS) = mid;
+        }
+      }
+    };
+    auto out_epilogue = [&](int cc, uint32_t t_out) {  // output row x - 64 of chunk cc
+      float d[kTcCols];
+      tmem_ld_sum3(t_out + lane_base + n0, d);
+      const int t = cc * kC + (x - 64);
+      if (t < T) {
+        uint2 pk;
+        pk.x = pack_bf16x2(scale * d[0], scale * d[1]);
+        pk.y = pack_bf16x2(scale * d[2], scale * d[3]);
+        *reinterpret_cast<uint2*>(o + ((static_cast<size_t>(b) * T + t) * H + h) * DV + r0 + n0) =
+            pk;
+      }
+    };
+    write_state_operand();
+    fence_proxy_async_smem();
+    constexpr uint32_t kIdK32 = idesc_bf16_f32(128, 32, false, false);
+    constexpr uint32_t kIdK16 = idesc_bf16_f32(128, 16, false, false);
+    constexpr uint32_t kIdMN32 = idesc_bf16_f32(128, 32, true, false);
+    constexpr uint32_t kIdMN16 = idesc_bf16_f32(128, 16, true, false);
+    // descriptors of the operand tiles' first atoms; an operand further on adds its byte
+    // offset / 16 (every address stays below 256 KB, so the 14-bit start field cannot carry)
+    const uint64_t dA1 = smem_desc_sw128(sbase + L::OFF_A1, 16, 1024);
+    const uint64_t dB1 = smem_desc_sw128(sbase + L::OFF_B1, 16, 1024);
+    const uint64_t dP = smem_desc_sw128(sbase + L::OFF_P - 8192, 16, 1024);
+    const uint64_t dB2 = smem_desc_sw128(sbase + L::OFF_B2, 16, 1024);
+    const uint64_t dA3 = smem_desc_sw128(sbase + L::OFF_A3, 8192, 1024);
+    const uint64_t dB3 = smem_desc_sw128(sbase + L::OFF_B3, 16, 1024);
+
+    for (int c = 0; c < nch; ++c) {
+      const int buf = c & 1;
+      const uint32_t use = static_cast<uint32_t>(c >> 1);
+      const size_t cid = bh * nch + c;
+      const uint32_t t_d1 = tmem + 64 * buf;
+      if (!mbar_wait(&full_a[buf], use & 1, abort_flag)) failed = true;
+      tc_fence_before();
+      // B1 holds this chunk's state; the previous chunk's TMEM reads are done
+      if (bar_sync_or(1, kTcThreads, failed)) { failed = true; break; }
+      if (tid == 0) {  // D1 = [Y; gamma Q^] S^T
+        tc_fence_after();
+        const uint64_t a0 = dA1 + ((buf * L::A1_BYTES) >> 4);
+#pragma unroll
+        for (int kb = 0; kb < NKB; ++kb)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t acc = (kb | k) ? 1u : 0u;
+            const uint64_t bd = dB1 + ((kb * L::B1_KB + k * 32) >> 4);
+            umma_bf16(t_d1, a0 + ((kb * 16384 + k * 32) >> 4), bd, kIdK32, acc);
+            umma_bf16(t_d1 + 32, a0 + ((L::A1_SPLIT + kb * 16384 + k * 32) >> 4), bd, kIdK16, acc);
+          }
+        umma_commit(d1_done);
+      }
+      // the state at the chunk start (overlaps the MMAs)
+      if (Schk && own_col) {
+#pragma unroll
+        for (int n = 0; n < kTcCols; ++n) Schk[(cid * DV + r0 + n0 + n) * DK + x] = S[n];
+      }
+      const float* sg = reinterpret_cast<const float*>(smem + L::OFF_G + buf * L::G_BYTES);
+      const float gC = sg[kC - 1];
+      const float gam_C = __expf(gC);
+      if (!mbar_wait(d1_done, c & 1, abort_flag)) failed = true;
+      failed = __any_sync(0xffffffffu, failed);  // the TMEM loads below are warp-collective
+      tc_fence_after();
+      if (!failed) {
+        if ((warp & 3) < 2) {  // W and Wd for token row j = x, value rows n0..
+          const int j = x;
+          float d[kTcCols];
+          tmem_ld_sum3(t_d1 + lane_base + n0, d);
+          const float4 u4 = *reinterpret_cast<const float4*>(
+              reinterpret_cast<const float*>(smem + L::OFF_U + buf * L::U_BYTES) + j * kRS + n0);
+          const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
+          const float dec = __expf(gC - sg[j]);
+#pragma unroll
+          for (int n = 0; n < kTcCols; ++n) {
+            const float w = uu[n] - d[n];
+            __nv_bfloat16 hi, mid;
+            const uint32_t off = sw128_off(n0 + n, j);
+            split_bf16(w, hi, mid);
+            *reinterpret_cast<__nv_bfloat16*>(smem + L::OFF_B2 + off) = hi;
+            *reinterpret_cast<__nv_bfloat16*>(smem + L::OFF_B2 + L::MID_ROWS + off) = mid;
+            split_bf16(w * dec, hi, mid);
+            *reinterpret_cast<__nv_bfloat16*>(smem + L::OFF_B3 + off) = hi;
+            *reinterpret_cast<__nv_bfloat16*>(smem + L::OFF_B3 + L::MID_ROWS + off) = mid;
+          }
+        } else if (c > 0) {  // the previous chunk's output (its P W completed before D1)
+          out_epilogue(c - 1, tmem + 64 * (buf ^ 1));
+        }
+      }
+      if (failed) *abort_flag = 1;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      if (bar_sync_or(1, kTcThreads, failed)) { failed = true; break; }  // W, Wd complete
+      if (tid == 0) {
+        mbar_arrive(&empty_a[buf]);  // [Y; gamma Q^], the U slice and the decays are read
+        if (!mbar_wait(full_k, c & 1, abort_flag) || !mbar_wait(&full_p[buf], use & 1, abort_flag)) {
+          failed = true;
+          *abort_flag = 1;
+        } else {
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // D3 = K^T Wd
+            const uint64_t bd3 = dB3 + ((k * 32) >> 4);
+            umma_bf16(t_d3, dA3 + ((k * 2048) >> 4), bd3, kIdMN32, k ? 1u : 0u);
+            umma_bf16(t_d3 + 32, dA3 + ((L::A3_SPLIT + k * 2048) >> 4), bd3, kIdMN16, k ? 1u : 0u);
+          }
+          umma_commit(d3_done);
+          umma_commit(empty_k);
+          const uint64_t p0 = dP + ((buf * L::P_BYTES) >> 4);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // D1[64:128] += P W
+            const uint64_t bd2 = dB2 + ((k * 32) >> 4);
+            umma_bf16(t_d1, p0 + ((k * 32) >> 4), bd2, kIdK32, 1u);
+            umma_bf16(t_d1 + 32, p0 + ((L::P_SPLIT + k * 32) >> 4), bd2, kIdK16, 1u);
+          }
+          umma_commit(&empty_p[buf]);
+        }
+      }
+      if (!mbar_wait(d3_done, c & 1, abort_flag)) failed = true;
+      failed = __any_sync(0xffffffffu, failed);
+      tc_fence_after();
+      if (!failed && (DK == 128 || (warp & 3) < 2)) {  // column x: S^T = gamma_C S^T + K^T Wd
+        float d[kTcCols];
+        tmem_ld_sum3(t_d3 + lane_base + n0, d);
+#pragma unroll
+        for (int n = 0; n < kTcCols; ++n) S[n] = gam_C * S[n] + d[n];
+        write_state_operand();
+      }
+      if (failed) *abort_flag = 1;
+      fence_proxy_async_smem();
+    }
+    if (!failed) {  // the last chunk's output, once its P W completed
+      if (tid == 0) umma_commit(d1_done);
+      if ((warp & 3) >= 2) {
+        if (!mbar_wait(d1_done, nch & 1, abort_flag)) failed = true;
+        failed = __any_sync(0xffffffffu, failed);
+        tc_fence_after();
+        if (!failed) out_epilogue(nch - 1, tmem + 64 * ((nch - 1) & 1));
+      }
+      if (failed) *abort_flag = 1;
+    }
+    if (failed) *abort_flag = 1;
+    if (!failed && !*abort_flag && ST && own_col) {
+#pragma unroll
+      for (int n = 0; n < kTcCols; ++n) ST[(bh * DV + r0 + n0 + n) * DK + x] = S[n];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    if (tid == 0) gdr_report(MOE_ERR_TIMEOUT);
+    if (tid == kTcThreads) {  // let the copies in flight land (bounded) before the CTA exits
+      volatile int no_abort = 0;
+      for (int i = 0; i < 5; ++i) {
+        uint64_t* f = i < 2 ? &full_a[i] : (i == 2 ? full_k : &full_p[i - 3]);
+        if (sent & (1u << i)) mbar_wait(f, (par >> i) & 1u, &no_abort);
+      }
+    }
+  }
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
 }
 
 // ---------------------------------------------------------------------------- backward
@@ -1290,29 +1547,34 @@ int gdr_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloat16*
                cudaStream_t s) {
   const int nch = (T + kC - 1) / kC;
   const size_t chunks = static_cast<size_t>(B) * H * nch;
+  // the workspace regions of gdr_ws, holding the tensor-core scan's operands: the split
+  // [Y; gamma Q^] tiles (twice the bytes of one fp32 [C][dk] tile set) over the first two
+  // regions, the split K^ over the third, U (fp32, slice-major), the split P over the fp32
+  // P's region
+  const size_t rk = up256(chunks * kC * DK * 4);
   uint8_t* w = static_cast<uint8_t*>(ws);
-  float* Qh = reinterpret_cast<float*>(w); w += up256(chunks * kC * DK * 4);
-  float* Kh = reinterpret_cast<float*>(w); w += up256(chunks * kC * DK * 4);
-  float* Yw = reinterpret_cast<float*>(w); w += up256(chunks * kC * DK * 4);
-  float* Uw = reinterpret_cast<float*>(w); w += up256(chunks * kC * DV * 4);
-  float* Pw = reinterpret_cast<float*>(w); w += up256(chunks * kC * kC * 4);
-  float* Gw = reinterpret_cast<float*>(w);
+  auto* YQs = reinterpret_cast<__nv_bfloat16*>(w);
+  auto* Ks = reinterpret_cast<__nv_bfloat16*>(w + 2 * rk);
+  float* Uw = reinterpret_cast<float*>(w + 3 * rk);
+  auto* Ps = reinterpret_cast<__nv_bfloat16*>(w + 3 * rk + up256(chunks * kC * DV * 4));
+  float* Gw = reinterpret_cast<float*>(w + 3 * rk + up256(chunks * kC * DV * 4) +
+                                       up256(chunks * kC * kC * 4));
   const size_t sm1 = (2 * kC * Ld<DK>::v + 2 * kC * Ld<kC>::v + 3 * kC) * sizeof(float);
-  auto k1 = gdr_chunk_kernel<DK, DV>;
+  auto k1 = gdr_chunk_kernel<DK, DV, true>;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(sm1));
   if (e != cudaSuccess) return static_cast<int>(e);
   mark_before(MOE_KERNEL_GDR_CHUNK, s);
-  k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, Qh, Kh, Yw, Uw, Pw, Gw,
-                                       nullptr);
+  k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, nullptr, nullptr, nullptr,
+                                       Uw, nullptr, Gw, nullptr, YQs, Ks, Ps);
   mark_after(MOE_KERNEL_GDR_CHUNK, s);
-  const size_t sm2 = scan_smem_bytes<DK>();
-  auto k2 = gdr_scan_kernel<DK, DV>;
+  constexpr size_t sm2 = TcScan<DK>::SMEM;
+  auto k2 = gdr_scan_tc_kernel<DK, DV>;
   e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm2));
   if (e != cudaSuccess) return static_cast<int>(e);
   mark_before(MOE_KERNEL_GDR_SCAN, s);
-  k2<<<dim3(DV / kRS, H, B), 256, sm2, s>>>(
-      Qh, Kh, Yw, Uw, Pw, Gw, S0, T, H, nch, scale, o, ST, Schk);
+  k2<<<dim3(DV / kRS, H, B), kTcBlock, sm2, s>>>(YQs, Ks, Ps, Uw, Gw, S0, T, H, nch, scale, o,
+                                                   ST, Schk);  // Uw: slice-major U
   mark_after(MOE_KERNEL_GDR_SCAN, s);
   return static_cast<int>(cudaGetLastError());
 }
@@ -1343,12 +1605,13 @@ int gdr_bwd_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloa
   float* dWw = reinterpret_cast<float*>(w); w += up256(chunks * kC * DV * 4);
   float* dSw = reinterpret_cast<float*>(w);
   const size_t sm1 = (2 * kC * Ld<DK>::v + 2 * kC * Ld<kC>::v + 3 * kC) * sizeof(float);
-  auto k1 = gdr_chunk_kernel<DK, DV>;
+  auto k1 = gdr_chunk_kernel<DK, DV, false>;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(sm1));
   if (e != cudaSuccess) return static_cast<int>(e);
   mark_before(MOE_KERNEL_GDR_BWD_FACTORS, s);
-  k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, Qh, Kh, Yw, Uw, Pw, Gw, Aw);
+  k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, Qh, Kh, Yw, Uw, Pw, Gw, Aw,
+                                       nullptr, nullptr, nullptr);
   mark_after(MOE_KERNEL_GDR_BWD_FACTORS, s);
   const size_t sm2 = bwd_scan_smem_bytes<DK>();
   auto k2 = gdr_bwd_scan_kernel<DK, DV>;
@@ -1392,7 +1655,8 @@ int moe_gdr_forward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, con
   if (static_cast<long long>(B) * H * ((T + kC - 1) / kC) > (1ll << 24)) return MOE_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < gdr_ws(B, T, H, dk, dv)) return MOE_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(q) |
-       reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u)
+       reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+       reinterpret_cast<uintptr_t>(o)) & 15u)
     return MOE_ERR_UNSUPPORTED;
   const auto* q_ = reinterpret_cast<const __nv_bfloat16*>(q);
   const auto* k_ = reinterpret_cast<const __nv_bfloat16*>(k);
@@ -1409,6 +1673,19 @@ int moe_gdr_forward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, con
     e = gdr_launch<64, 64>(B, T, H, q_, k_, v_, beta, g, S0, scale, o_, S_T, S_chunks, workspace, stream);
   count_launches(2);
   return e == 0 ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_gdr_device_status(int32_t* status, moe_stream_t stream) {
+  if (!status) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int v = 0;
+  const int zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_gdr_status, sizeof(int)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_gdr_status, &zero, sizeof(int)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  *status = v;
+  return MOE_OK;
 }
 
 size_t moe_gdr_backward_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv) {

@@ -105,6 +105,7 @@ _SIGS = {
     "moe_gdr_forward": (ctypes.c_int, [c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp,
                                        c_vp, c_vp, ctypes.c_float, c_vp, c_vp, c_vp, c_vp, c_sz,
                                        c_vp]),
+    "moe_gdr_device_status": (ctypes.c_int, [ctypes.POINTER(c_i32), c_vp]),
     "moe_gdr_backward_workspace_size": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
     "moe_gdr_backward": (ctypes.c_int, [c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp,
                                         c_vp, ctypes.c_float, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
@@ -424,6 +425,14 @@ def moe_gdr_forward(B, T, H, dk, dv, q, k, v, beta, g, S0, scale, o, S_T, S_chun
            lib().moe_gdr_forward(B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
                                  _ptr(S0), scale, _ptr(o), _ptr(S_T), _ptr(S_chunks), wp, wn,
                                  _stream(stream)))
+
+
+def moe_gdr_device_status(stream=None) -> int:
+    """Waits for ``stream``; the first status a linear-attention kernel recorded since the
+    previous call (0: none), cleared."""
+    st = c_i32(0)
+    _check("moe_gdr_device_status", lib().moe_gdr_device_status(ctypes.byref(st), _stream(stream)))
+    return int(st.value)
 
 
 def moe_gdr_backward_workspace_size(B, T, H, dk, dv) -> int:
