@@ -65,7 +65,9 @@ int moe_gdr_device_status(int32_t* status, moe_stream_t stream);
 
 /* Backward: gradients of <d_o, o> + <dS_T, S_T> with respect to q, k, v, beta, g and S0
  * (three launches: the per-chunk factors rebuilt, a backward scan over chunks for the state
- * gradient in slices of 16 value rows, then every chunk's local backward in parallel).
+ * gradient in slices of 16 value rows on the tensor cores (bounded waits as in the forward,
+ * reported through moe_gdr_device_status), then every chunk's local backward in
+ * parallel).
  * S_chunks: the forward's chunk-start states (required).  d_o [B, T, H, dv] bf16; dS_T
  * [B, H, dv, dk] fp32 or NULL (zero).  Outputs fp32, overwritten: dq, d_k [B, T, H, dk],
  * d_v [B, T, H, dv], dbeta, dg [B, T, H], dS0 [B, H, dv, dk] (may be NULL).  Deterministic:

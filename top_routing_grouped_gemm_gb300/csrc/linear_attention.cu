@@ -74,6 +74,56 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
   for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Shared-memory image of one CTA of the tensor-core backward scan (gdr_bwd_scan_tc_kernel);
+// the backward's gdr_chunk_kernel writes the tiles marked "image" exactly as they sit here.
+// Tiles of chunk c in the order the scan meets them (c descending):
+//   X (two buffers): sP (s P, both pieces; read as the MN-major A of P^T), sQ (s gamma Q^,
+//       both pieces, MN-major A of its transpose) and dO^T of the slice (bf16, K-major B);
+//   E (two buffers): E = diag(gamma_C / gamma) K^ (both pieces, K-major A) and the decays;
+//   Y (one buffer, both pieces, MN-major A of Y^T).
+template <int DK>
+struct TcBwd {
+  static constexpr int NKB = DK / 64;
+  static constexpr uint32_t SP_PIECE = 8192u;                // [64 t][64 i]
+  static constexpr uint32_t SQ_PIECE = NKB * 8192u;          // [64 j][64 dk] per box
+  static constexpr uint32_t OT_BYTES = 2048u;                // [16 n][64 t]
+  static constexpr uint32_t X_SP = 0, X_SQ = 2 * SP_PIECE, X_OT = X_SQ + 2 * SQ_PIECE;
+  static constexpr uint32_t X_BYTES = X_OT + 1024u * ((OT_BYTES + 1023u) / 1024u);
+  static constexpr uint32_t E_PIECE = NKB * 8192u;           // [64 i][64 dk] per block
+  static constexpr uint32_t E_BYTES = 2 * E_PIECE;
+  static constexpr uint32_t Y_PIECE = NKB * 8192u;
+  static constexpr uint32_t Y_BYTES = 2 * Y_PIECE;
+  static constexpr uint32_t B1_KB = 4096u;                   // dS pieces: [32][64] per block
+  static constexpr uint32_t B2_BYTES = 4096u;                // -dW pieces: [32][64 tokens]
+  static constexpr uint32_t MID_ROWS = 2048u;
+  static constexpr uint32_t G_BYTES = kC * 4u;
+  static constexpr uint32_t OFF_X = 0;                       // two buffers
+  static constexpr uint32_t OFF_E = 2 * X_BYTES;             // two buffers
+  static constexpr uint32_t OFF_Y = OFF_E + 2 * E_BYTES;
+  static constexpr uint32_t OFF_B1 = OFF_Y + Y_BYTES;
+  static constexpr uint32_t OFF_B2 = OFF_B1 + NKB * B1_KB;
+  static constexpr uint32_t OFF_G = OFF_B2 + B2_BYTES;       // two buffers
+  static constexpr uint32_t OFF_BAR = OFF_G + 2 * G_BYTES;   // 14 mbarriers, TMEM slot, flag
+  static constexpr uint32_t BYTES = OFF_BAR + 128u;
+  static constexpr size_t SMEM = BYTES + 1024u;
+  static_assert(X_BYTES % 1024 == 0 && OFF_E % 1024 == 0 && OFF_Y % 1024 == 0 &&
+                    OFF_B1 % 1024 == 0 && OFF_B2 % 1024 == 0,
+                "swizzled tiles start on 1024-byte atoms");
+  // M = 128 views read 8 KB past a 64-row tile (rows whose D lanes are not read): the last
+  // E block, the last sP / sQ / Y box must be followed by 8 KB of shared memory
+  static_assert(OFF_Y + Y_BYTES + 8192u <= BYTES, "views past Y stay in shared memory");
+  static_assert(SMEM <= 227u * 1024u, "fits one CTA per SM");
+  // bf16 element offsets within one chunk's images
+  __device__ static uint32_t e(int s, int i, int x) {  // K-major [64][64] blocks
+    return (s * E_PIECE + (x >> 6) * 8192u + sw128_off(i, x & 63)) >> 1;
+  }
+  __device__ static uint32_t mn(int s, int j, int x) {  // MN-major boxes (sQ, Y)
+    return (s * SQ_PIECE + (x >> 6) * 8192u + sw128_off(j, x & 63)) >> 1;
+  }
+  __device__ static uint32_t sp(int s, int t, int i) { return (s * SP_PIECE + sw128_off(t, i)) >> 1; }
+  __device__ static uint32_t ot(int n, int t) { return sw128_off(n, t) >> 1; }
+};
+
 // Barrier `id` over the first `nthreads` threads of the block; true if `pred` held in any.
 __device__ __forceinline__ bool bar_sync_or(uint32_t id, uint32_t nthreads, bool pred) {
   uint32_t r;
@@ -170,7 +220,17 @@ struct Ld {
 // shared-memory images (TcScan): each fp32 value as two bf16 pieces (hi, mid), per chunk
 // YQs (rows 0..63 Y, 64..127 diag(gamma) Q^), Ks and Ps; U as fp32 slices of 16 value rows,
 // [slice][64][16] per chunk; the log decays as fp32.
-template <int DK, int DV, bool SPLIT>
+// BIMG (the backward): the fp32 factors as above plus the tensor-core backward scan's
+// shared-memory images (TcBwd) of s P, s gamma Q^, E = diag(gamma_C / gamma) K^ and Y (two
+// bf16 pieces each) and, per slice of 16 value rows, dO^T of the chunk (zero past the
+// sequence).
+struct GdrBwdImages {
+  __nv_bfloat16 *sP, *sQ, *E, *Y, *OT;
+  const __nv_bfloat16* dO;
+  float scale;
+};
+
+template <int DK, int DV, bool SPLIT, bool BIMG>
 __global__ void __launch_bounds__(256) gdr_chunk_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ beta,
@@ -178,7 +238,8 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
     float* __restrict__ Kh, float* __restrict__ Y, float* __restrict__ U,
     float* __restrict__ Pm, float* __restrict__ Gc, float* __restrict__ Ai,
     __nv_bfloat16* __restrict__ YQs, __nv_bfloat16* __restrict__ Ks,
-    __nv_bfloat16* __restrict__ Ps) {
+    __nv_bfloat16* __restrict__ Ps, GdrBwdImages img) {
+  static_assert(!(SPLIT && BIMG), "one image set per launch");
   constexpr int LK = Ld<DK>::v, LC = Ld<kC>::v;
   extern __shared__ float sm[];
   float* sK = sm;                    // [C][LK]
@@ -319,6 +380,13 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
           Ps[chunk_id * (L::P_BYTES / 2) + L::p(1, i, j)] = mid;
         } else {
           Pm[chunk_id * kC * kC + i * kC + j] = pv;
+          if constexpr (BIMG) {
+            using LB = TcBwd<DK>;
+            __nv_bfloat16 hi, mid;
+            split_bf16(img.scale * pv, hi, mid);
+            img.sP[chunk_id * LB::SP_PIECE + LB::sp(0, i, j)] = hi;
+            img.sP[chunk_id * LB::SP_PIECE + LB::sp(1, i, j)] = mid;
+          }
         }
       }
   }
@@ -365,6 +433,41 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
       Qh[chunk_id * kC * DK + e] = sQ[i * LK + x];
       Kh[chunk_id * kC * DK + e] = sK[i * LK + x];
     }
+    if constexpr (BIMG) {  // s gamma q^ and E = (gamma_C / gamma) k^, pairs per 4-byte store
+      using LB = TcBwd<DK>;
+      __nv_bfloat16* sq = img.sQ + chunk_id * LB::SQ_PIECE;
+      __nv_bfloat16* eo = img.E + chunk_id * LB::E_PIECE;
+      const float gC = sG[kC - 1];
+      for (int e = tid; e < kC * DK / 2; e += 256) {
+        const int i = (2 * e) / DK, x = 2 * e - i * DK;
+        const float qs = img.scale * __expf(sG[i]), dec = __expf(gC - sG[i]);
+        __nv_bfloat16 h0, m0, h1, m1;
+        split_bf16(qs * sQ[i * LK + x], h0, m0);
+        split_bf16(qs * sQ[i * LK + x + 1], h1, m1);
+        *reinterpret_cast<__nv_bfloat162*>(sq + LB::mn(0, i, x)) = __halves2bfloat162(h0, h1);
+        *reinterpret_cast<__nv_bfloat162*>(sq + LB::mn(1, i, x)) = __halves2bfloat162(m0, m1);
+        split_bf16(dec * sK[i * LK + x], h0, m0);
+        split_bf16(dec * sK[i * LK + x + 1], h1, m1);
+        *reinterpret_cast<__nv_bfloat162*>(eo + LB::e(0, i, x)) = __halves2bfloat162(h0, h1);
+        *reinterpret_cast<__nv_bfloat162*>(eo + LB::e(1, i, x)) = __halves2bfloat162(m0, m1);
+      }
+      // dO^T of every 16-row value slice: 16-byte loads of dO rows, 2-byte image stores
+      constexpr int PPR = DV / 8;
+      for (int e = tid; e < kC * PPR; e += 256) {
+        const int t = e / PPR, pc = e - t * PPR;
+        const int tt = t0 + t;
+        const uint4 raw = tt < T ? *reinterpret_cast<const uint4*>(
+                                       img.dO + ((static_cast<size_t>(b) * T + tt) * H + h) * DV + pc * 8)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+        const __nv_bfloat16* vals = reinterpret_cast<const __nv_bfloat16*>(&raw);
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+          const int col = pc * 8 + q8;
+          img.OT[(chunk_id * (DV / kRS) + col / kRS) * (LB::OT_BYTES / 2) + LB::ot(col % kRS, t)] =
+              vals[q8];
+        }
+      }
+    }
   }
   __syncthreads();
   for (int e = tid; e < kC * DK; e += 256) {
@@ -406,6 +509,13 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
           YQs[chunk_id * (L::A1_BYTES / 2) + L::a1(1, row, col)] = mid;
         } else {
           Y[chunk_id * kC * DK + row * DK + col] = acc[a][u];
+          if constexpr (BIMG) {
+            using LB = TcBwd<DK>;
+            __nv_bfloat16 hi, mid;
+            split_bf16(acc[a][u], hi, mid);
+            img.Y[chunk_id * LB::Y_PIECE + LB::mn(0, row, col)] = hi;
+            img.Y[chunk_id * LB::Y_PIECE + LB::mn(1, row, col)] = mid;
+          }
         }
       }
   }
@@ -462,28 +572,6 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
   if (Ai)
     for (int e = tid; e < kC * kC; e += 256) Ai[chunk_id * kC * kC + e] = sI[(e / kC) * LC + (e % kC)];
 }
-
-// cp.async groups of the scans' streamed chunk tiles.
-__device__ __forceinline__ void la_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void la_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-__device__ __forceinline__ void la_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-// rows x D fp32 tile (global row stride D) -> shared (row stride LDS, a multiple of 4)
-template <int ROWS, int D, int LDS>
-__device__ __forceinline__ void tile_async(float* dst, const float* src, int src_ld, int tid) {
-  constexpr int CPR = D / 4;  // 16-byte pieces per row
-  for (int e = tid; e < ROWS * CPR; e += 256) {
-    const int i = e / CPR, x4 = e - i * CPR;
-    cp_async_16(dst + i * LDS + 4 * x4, src + static_cast<size_t>(i) * src_ld + 4 * x4, 16u);
-  }
-}
-
-// fp32 tile strides of the backward scan
-template <int DK>
-struct ScanLd {
-  static constexpr int T = DK + 4;  // streamed tiles: 16-byte rows (bank offset 4 per row)
-  static constexpr int P = kC + 4;
-};
 
 // Scan over the chunks of one (b, h) for RS = 16 value rows of the state (grid: DV/RS x H x B,
 // 16 consumer warps and a copy warp), on the tensor cores.  Per chunk, with S the slice of
@@ -792,187 +880,283 @@ __global__ void __launch_bounds__(kTcBlock, 1) gdr_scan_tc_kernel(
 //     dV = diag(beta) dBv,  Z = dM . beta Gam,  and the beta and log-decay gradients of every
 //     place they enter (A, U, Y, P, E, gamma); dg is the reverse cumulative sum of dG.
 
-// Backward scan over chunks for RS value rows of dS (grid: DV/RS x H x B).  Writes dW (the
-// slice's columns) and the state gradient at every chunk end; dS0 at the end.  The chunk
-// tiles stream in with cp.async as in the forward scan: P, K^, the dO slice and the log
-// decays (needed by dW) are reloaded for the next chunk right after dW, Q^ and Y (needed by
-// the state-gradient update) right after it (wait_group 1).
+// Backward scan over the chunks of one (b, h) for RS = 16 value rows of dS (grid: DV/RS x H x
+// B, 16 consumer warps and a copy warp), on the tensor cores.  Chunks are taken last to
+// first; with dS the slice of the state gradient at the chunk's end:
+//     dW = (s P)^T dO + E dS^T                        (M = 64 tokens, N = 16)
+//     dS = gamma_C dS + (s gamma Q^)^T dO - Y^T dW    (M = dk, K = 64 tokens)
+// dW (fp32, for the chunk-local backward) and the state gradient at every chunk end go to
+// global memory, dS0 at the end.  Operands and products as in the forward scan (two bf16
+// pieces per fp32 operand, three MMAs per product; dO is bf16 already, so its products take
+// two).  Only E dS^T and Y^T dW depend on the running state gradient: the two products with
+// dO of chunk c - 1 are issued right after Y^T dW of chunk c, into the other of two TMEM
+// buffers, and run while the state gradient of chunk c is formed.  TMEM: per buffer p, D_A
+// (dW's five accumulators: E.dS hi.hi, hi.mid, mid.hi, sP.dO hi, mid) at columns 128 p and
+// D_B (dS's: sQ.dO hi, mid, Y.dW hi.hi, hi.mid, mid.hi) at 256 + 128 p.
 template <int DK, int DV>
-__global__ void __launch_bounds__(256) gdr_bwd_scan_kernel(
-    const float* __restrict__ Qh, const float* __restrict__ Kh, const float* __restrict__ Y,
-    const float* __restrict__ Pm, const float* __restrict__ Gc,
-    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ dST, int T, int H, int nch,
-    float scale, float* __restrict__ dW, float* __restrict__ dSchk, float* __restrict__ dS0) {
-  constexpr int LT = ScanLd<DK>::T, LP = ScanLd<DK>::P;
-  constexpr int LS = ScanLd<DK>::T;  // state-gradient rows: 16-byte aligned (read as float4)
-  extern __shared__ float4 sm4[];
-  float* sm = reinterpret_cast<float*>(sm4);
-  float* sQ = sm;                   // [C][LT]
-  float* sK = sQ + kC * LT;         // [C][LT]
-  float* sY = sK + kC * LT;         // [C][LT]
-  float* sP = sY + kC * LT;         // [C][LP]
-  float* sGr = sP + kC * LP;        // [C] log decays
-  __nv_bfloat16* sOb = reinterpret_cast<__nv_bfloat16*>(sGr + kC);  // [C][RS] dO slice
-  float* sD = sGr + kC + kC * kRS / 2;  // [RS][LS] state gradient rows
-  float* sW = sD + kRS * LS;        // [C][RS] dW slice
-  float* sOg = sW + kC * kRS;       // [C][RS] s gamma_i dO
-  static_assert(kRS == 16 && kC == 64 && DK % 32 == 0, "thread tiling");
-  static_assert(kRS * 2 % 16 == 0, "dO slice rows are whole 16-byte pieces");
+__global__ void __launch_bounds__(kTcBlock, 1) gdr_bwd_scan_tc_kernel(
+    const __nv_bfloat16* __restrict__ sPs, const __nv_bfloat16* __restrict__ sQs,
+    const __nv_bfloat16* __restrict__ OTs, const __nv_bfloat16* __restrict__ Es,
+    const __nv_bfloat16* __restrict__ Ys, const float* __restrict__ Gc,
+    const float* __restrict__ dST, int H, int nch, float* __restrict__ dW,
+    float* __restrict__ dSchk, float* __restrict__ dS0) {
+  using L = TcBwd<DK>;
+  constexpr int NKB = L::NKB;
+  extern __shared__ uint8_t tc_smem_raw[];
+  const uint32_t raw = smem_u32(tc_smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = tc_smem_raw + (sbase - raw);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* a_done = &bar[0];    // E dS^T (and everything issued before it) complete
+  uint64_t* b_done = &bar[1];    // Y^T dW (and everything issued before it) complete
+  uint64_t* full_x = &bar[2];    // [2] sP, sQ, dO^T landed
+  uint64_t* full_e = &bar[4];    // [2] E, decays landed
+  uint64_t* full_y = &bar[6];    // Y landed
+  uint64_t* empty_x = &bar[7];   // [2] the products with dO complete
+  uint64_t* empty_e = &bar[9];   // [2] E dS^T complete and the decays read
+  uint64_t* empty_y = &bar[11];  // Y^T dW complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_BAR + 112);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 116);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int x = 32 * (warp & 3) + (tid & 31);  // TMEM lane: token row of D_A, dk column of D_B
+  const int n0 = kTcCols * ((warp >> 2) & 3);  // this thread's first value row of the slice
   const int r0 = blockIdx.x * kRS, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x;
   const size_t bh = static_cast<size_t>(b) * H + h;
-  auto issue_a = [&](int c) {  // P, K^, dO slice, log decays
-    if (c >= 0) {
-      const size_t cid = bh * nch + c;
-      tile_async<kC, kC, LP>(sP, Pm + cid * kC * kC, kC, tid);
-      tile_async<kC, DK, LT>(sK, Kh + cid * kC * DK, DK, tid);
-      tile_async<1, kC, kC>(sGr, Gc + cid * kC, kC, tid);
-      constexpr int PPR = kRS * 2 / 16;  // 16-byte pieces per dO row
-      for (int e = tid; e < kC * PPR; e += 256) {
-        const int i = e / PPR, pc = e - i * PPR;
-        const int t = c * kC + i;
-        // rows past the sequence read row 0 and are zeroed when used (t >= T below)
-        const size_t row = (static_cast<size_t>(b) * T + (t < T ? t : 0)) * H + h;
-        cp_async_16(sOb + i * kRS + pc * 8, dO + row * DV + r0 + pc * 8, 16u);
-      }
-    }
-    la_commit();
-  };
-  auto issue_b = [&](int c) {  // Q^, Y
-    if (c >= 0) {
-      const size_t cid = bh * nch + c;
-      tile_async<kC, DK, LT>(sQ, Qh + cid * kC * DK, DK, tid);
-      tile_async<kC, DK, LT>(sY, Y + cid * kC * DK, DK, tid);
-    }
-    la_commit();
-  };
-  for (int e = tid; e < kRS * DK; e += 256) {
-    const int r = e / DK, x = e - r * DK;
-    sD[r * LS + x] = dST ? dST[(bh * DV + r0 + r) * DK + x] : 0.f;
+
+  if (tid == 0) {
+#pragma unroll
+    for (int i = 0; i < 12; ++i) mbar_init(&bar[i], 1);
+    *abort_flag = 0;
+    fence_barrier_init();
   }
-  issue_a(nch - 1);
-  issue_b(nch - 1);
-  // dW phase: token rows i0 = tid / 8 and i1 = i0 + 32, value rows c0 = tid % 8, c1 = c0 + 8
-  const int cq = tid & 7, i0 = tid >> 3, i1 = i0 + 32;
-  const int c0 = cq, c1 = cq + 8;
-  // state-gradient phase: value rows rs * RPL .. + RPL - 1, float4 column group cg
-  constexpr int GW = DK / 32, RSEL = 32 / GW, RPL = kRS / RSEL;
-  static_assert(RPL * RSEL == kRS && (RPL == 1 || RPL == 2), "state-gradient tiling");
-  const int lane = tid & 31, warp = tid >> 5;
-  const int cg = warp * GW + lane / RSEL, rs = lane % RSEL;
-  for (int c = nch - 1; c >= 0; --c) {
-    const size_t cid = bh * nch + c;
-    la_wait1();        // P, K^, dO, decays of chunk c
-    __syncthreads();
-    const float gC = sGr[kC - 1];
-    const float gam_C = __expf(gC);
-    for (int e = tid; e < kRS * DK; e += 256) {
-      const int r = e / DK, x = e - r * DK;
-      dSchk[(cid * DV + r0 + r) * DK + x] = sD[r * LS + x];
-    }
-    // dW = s P^T dO + E dS1^T
-    {
-      float kd[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, pd[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-      const float4* ka = reinterpret_cast<const float4*>(sK + i0 * LT);
-      const float4* kb = reinterpret_cast<const float4*>(sK + i1 * LT);
-      const float4* da = reinterpret_cast<const float4*>(sD + c0 * LS);
-      const float4* db = reinterpret_cast<const float4*>(sD + c1 * LS);
-#pragma unroll 4
-      for (int x4 = 0; x4 < DK / 4; ++x4) {
-        const float4 a0 = ka[x4], a1 = kb[x4], u0 = da[x4], u1 = db[x4];
-        kd[0][0] += a0.x * u0.x + a0.y * u0.y + a0.z * u0.z + a0.w * u0.w;
-        kd[0][1] += a0.x * u1.x + a0.y * u1.y + a0.z * u1.z + a0.w * u1.w;
-        kd[1][0] += a1.x * u0.x + a1.y * u0.y + a1.z * u0.z + a1.w * u0.w;
-        kd[1][1] += a1.x * u1.x + a1.y * u1.y + a1.z * u1.z + a1.w * u1.w;
-      }
-      // P^T dO: P[t][i] is zero for t < i, so row i0 starts at the warp's first row 4 * warp
-      // and row i1 at 4 * warp + 32
-      const int tw = 4 * warp;
-      for (int t = tw; t < kC; ++t) {
-        const bool in = c * kC + t < T;
-        const float o0 = in ? bf(sOb[t * kRS + c0]) : 0.f;
-        const float o1 = in ? bf(sOb[t * kRS + c1]) : 0.f;
-        const float p0 = sP[t * LP + i0];
-        pd[0][0] += p0 * o0;
-        pd[0][1] += p0 * o1;
-        if (t >= tw + 32) {
-          const float p1 = sP[t * LP + i1];
-          pd[1][0] += p1 * o0;
-          pd[1][1] += p1 * o1;
-        }
-      }
-      const int ir[2] = {i0, i1}, cr[2] = {c0, c1};
-#pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        const int i = ir[a];
-        const float gi = sGr[i];
-        const float gam_i = __expf(gi), dec_i = __expf(gC - gi);
-        const bool in_i = c * kC + i < T;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const float w = scale * pd[a][q] + dec_i * kd[a][q];
-          sW[i * kRS + cr[q]] = w;
-          dW[cid * kC * DV + i * DV + r0 + cr[q]] = w;
-          sOg[i * kRS + cr[q]] = in_i ? scale * gam_i * bf(sOb[i * kRS + cr[q]]) : 0.f;
-        }
-      }
-    }
-    la_wait0();        // this thread's copies of Q^, Y of chunk c have landed
-    __syncthreads();   // dW is complete; Q^, Y are visible; P, K^, dO and the decays are free
-    issue_a(c - 1);
-    // dS0 = gamma_C dS1 + sum_j (s gamma_j dO_jr) q^_j - sum_j dW_jr Y_j  (each thread reads
-    // and rewrites its own elements of the state gradient)
-    {
-      float4 acc[RPL];
-#pragma unroll
-      for (int v = 0; v < RPL; ++v) {
-        const float4 sv = reinterpret_cast<const float4*>(sD + (rs * RPL + v) * LS)[cg];
-        acc[v] = make_float4(gam_C * sv.x, gam_C * sv.y, gam_C * sv.z, gam_C * sv.w);
-      }
-#pragma unroll 8
-      for (int j = 0; j < kC; ++j) {
-        const float4 qv = reinterpret_cast<const float4*>(sQ + j * LT)[cg];
-        const float4 yv = reinterpret_cast<const float4*>(sY + j * LT)[cg];
-        float og[RPL], wv[RPL];
-        if constexpr (RPL == 2) {
-          const float2 o2 = *reinterpret_cast<const float2*>(sOg + j * kRS + 2 * rs);
-          const float2 w2 = *reinterpret_cast<const float2*>(sW + j * kRS + 2 * rs);
-          og[0] = o2.x;
-          og[1] = o2.y;
-          wv[0] = w2.x;
-          wv[1] = w2.y;
-        } else {
-          og[0] = sOg[j * kRS + rs];
-          wv[0] = sW[j * kRS + rs];
-        }
-#pragma unroll
-        for (int v = 0; v < RPL; ++v) {
-          acc[v].x += og[v] * qv.x - wv[v] * yv.x;
-          acc[v].y += og[v] * qv.y - wv[v] * yv.y;
-          acc[v].z += og[v] * qv.z - wv[v] * yv.z;
-          acc[v].w += og[v] * qv.w - wv[v] * yv.w;
-        }
-      }
-#pragma unroll
-      for (int v = 0; v < RPL; ++v)
-        reinterpret_cast<float4*>(sD + (rs * RPL + v) * LS)[cg] = acc[v];
-    }
-    __syncthreads();   // Q^ and Y are free
-    issue_b(c - 1);
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
   }
   __syncthreads();
-  if (dS0)
-    for (int e = tid; e < kRS * DK; e += 256) {
-      const int r = e / DK, x = e - r * DK;
-      dS0[(bh * DV + r0 + r) * DK + x] = sD[r * LS + x];
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool failed = false;
+  // copy warp: the last copy issued on each full barrier and the phase it completes (bits 0,
+  // 1: full_x; 2, 3: full_e; 4: full_y), for the drain after an abort
+  uint32_t sent = 0, par = 0;
+
+  if (warp == kTcThreads / 32) {
+    // ------------------------------------------------------------ copy warp
+    if ((tid & 31) == 0) {
+      auto note = [&](int i, uint32_t phase) {
+        sent |= 1u << i;
+        par = (par & ~(1u << i)) | (phase << i);
+      };
+      for (int k = 0; k < nch && !failed; ++k) {  // k-th chunk met: c = nch - 1 - k
+        const int buf = k & 1;
+        const uint32_t use = static_cast<uint32_t>(k >> 1);
+        const size_t cid = bh * nch + (nch - 1 - k);
+        if (k >= 2 && !mbar_wait(&empty_x[buf], (use - 1) & 1, abort_flag)) { failed = true; break; }
+        uint8_t* xb = smem + L::OFF_X + buf * L::X_BYTES;
+        mbar_arrive_expect_tx(&full_x[buf], 2 * L::SP_PIECE + 2 * L::SQ_PIECE + L::OT_BYTES);
+        bulk_load(xb + L::X_SP, sPs + cid * L::SP_PIECE, 2 * L::SP_PIECE, &full_x[buf]);
+        bulk_load(xb + L::X_SQ, sQs + cid * L::SQ_PIECE, 2 * L::SQ_PIECE, &full_x[buf]);
+        bulk_load(xb + L::X_OT, OTs + (cid * (DV / kRS) + blockIdx.x) * (L::OT_BYTES / 2),
+                  L::OT_BYTES, &full_x[buf]);
+        note(buf, use & 1);
+        if (k >= 2 && !mbar_wait(&empty_e[buf], (use - 1) & 1, abort_flag)) { failed = true; break; }
+        mbar_arrive_expect_tx(&full_e[buf], L::E_BYTES + L::G_BYTES);
+        bulk_load(smem + L::OFF_E + buf * L::E_BYTES, Es + cid * L::E_PIECE, L::E_BYTES, &full_e[buf]);
+        bulk_load(smem + L::OFF_G + buf * L::G_BYTES, Gc + cid * kC, L::G_BYTES, &full_e[buf]);
+        note(2 + buf, use & 1);
+        if (k >= 1 && !mbar_wait(empty_y, (k - 1) & 1, abort_flag)) { failed = true; break; }
+        mbar_arrive_expect_tx(full_y, L::Y_BYTES);
+        bulk_load(smem + L::OFF_Y, Ys + cid * L::Y_PIECE, L::Y_BYTES, full_y);
+        note(4, k & 1);
+      }
+      if (failed) *abort_flag = 1;
     }
+  } else {
+    // ------------------------------------------------------------ consumer warps
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    // this thread's part of the state gradient: column x for value rows n0 .. n0 + 3
+    const bool own_col = x < DK;
+    float S[kTcCols];
+#pragma unroll
+    for (int n = 0; n < kTcCols; ++n)
+      S[n] = (own_col && dST) ? dST[(bh * DV + r0 + n0 + n) * DK + x] : 0.f;
+    auto write_state_operand = [&]() {  // dS -> B1 (K-major [16 rows][dk], both pieces)
+      if (own_col) {
+        const int kb = x >> 6, col = x & 63;
+#pragma unroll
+        for (int n = 0; n < kTcCols; ++n) {
+          __nv_bfloat16 hi, mid;
+          split_bf16(S[n], hi, mid);
+          const uint32_t off = L::OFF_B1 + kb * L::B1_KB + sw128_off(n0 + n, col);
+          *reinterpret_cast<__nv_bfloat16*>(smem + off) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(smem + off + L::MID_ROWS) = mid;
+        }
+      }
+    };
+    auto ld_sum5 = [&](uint32_t taddr, float (&d)[kTcCols]) {  // five accumulators, 16 apart
+      float a[kTcCols], c2[kTcCols];
+      tmem_ld4(taddr, d);
+      tmem_ld4(taddr + 16, a);
+      tmem_ld4(taddr + 32, c2);
+      tmem_ld_wait();
+#pragma unroll
+      for (int n = 0; n < kTcCols; ++n) d[n] = (d[n] + a[n]) + c2[n];
+      tmem_ld4(taddr + 48, a);
+      tmem_ld4(taddr + 64, c2);
+      tmem_ld_wait();
+#pragma unroll
+      for (int n = 0; n < kTcCols; ++n) d[n] += a[n] + c2[n];
+    };
+    write_state_operand();
+    fence_proxy_async_smem();
+    constexpr uint32_t kIdK32 = idesc_bf16_f32(128, 32, false, false);
+    constexpr uint32_t kIdK16 = idesc_bf16_f32(128, 16, false, false);
+    constexpr uint32_t kIdMN32 = idesc_bf16_f32(128, 32, true, false);
+    constexpr uint32_t kIdMN16 = idesc_bf16_f32(128, 16, true, false);
+    // descriptors of the tiles' first atoms; a tile further on adds its byte offset / 16
+    const uint64_t dE = smem_desc_sw128(sbase + L::OFF_E, 16, 1024);
+    const uint64_t dB1 = smem_desc_sw128(sbase + L::OFF_B1, 16, 1024);
+    const uint64_t dSP = smem_desc_sw128(sbase + L::OFF_X + L::X_SP, 8192, 1024);
+    const uint64_t dSQ = smem_desc_sw128(sbase + L::OFF_X + L::X_SQ, 8192, 1024);
+    const uint64_t dOT = smem_desc_sw128(sbase + L::OFF_X + L::X_OT, 16, 1024);
+    const uint64_t dY = smem_desc_sw128(sbase + L::OFF_Y, 8192, 1024);
+    const uint64_t dB2 = smem_desc_sw128(sbase + L::OFF_B2, 16, 1024);
+    // the products with dO of the k-th chunk met, into TMEM buffer k & 1 (thread 0)
+    auto issue_do_products = [&](int k) {
+      const int xb = k & 1;
+      if (!mbar_wait(&full_x[xb], (k >> 1) & 1, abort_flag)) return false;
+      tc_fence_after();
+      const uint32_t ta = tmem + 128 * xb, tb = tmem + 256 + 128 * xb;
+      const uint32_t o = (xb * L::X_BYTES) >> 4;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t bo = dOT + o + ((kk * 32) >> 4);
+        const uint32_t acc = kk ? 1u : 0u;
+        umma_bf16(ta + 48, dSP + o + ((kk * 2048) >> 4), bo, kIdMN16, acc);
+        umma_bf16(ta + 64, dSP + o + ((L::SP_PIECE + kk * 2048) >> 4), bo, kIdMN16, acc);
+        umma_bf16(tb, dSQ + o + ((kk * 2048) >> 4), bo, kIdMN16, acc);
+        umma_bf16(tb + 16, dSQ + o + ((L::SQ_PIECE + kk * 2048) >> 4), bo, kIdMN16, acc);
+      }
+      umma_commit(&empty_x[xb]);
+      return true;
+    };
+    if (tid == 0 && !issue_do_products(0)) {
+      failed = true;
+      *abort_flag = 1;
+    }
+
+    for (int k = 0; k < nch; ++k) {
+      const int c = nch - 1 - k, buf = k & 1;
+      const uint32_t use = static_cast<uint32_t>(k >> 1);
+      const size_t cid = bh * nch + c;
+      const uint32_t t_a = tmem + 128 * buf, t_b = tmem + 256 + 128 * buf;
+      if (!mbar_wait(&full_e[buf], use & 1, abort_flag)) failed = true;
+      const float gam_C = failed ? 0.f
+          : __expf(reinterpret_cast<const float*>(smem + L::OFF_G + buf * L::G_BYTES)[kC - 1]);
+      tc_fence_before();
+      // B1 holds this chunk's state gradient; the previous chunk's TMEM reads are done
+      if (bar_sync_or(1, kTcThreads, failed)) { failed = true; break; }
+      if (tid == 0) {  // D_A += E dS^T
+        tc_fence_after();
+        const uint64_t e0 = dE + ((buf * L::E_BYTES) >> 4);
+#pragma unroll
+        for (int kb = 0; kb < NKB; ++kb)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acc = (kb | kk) ? 1u : 0u;
+            const uint64_t bd = dB1 + ((kb * L::B1_KB + kk * 32) >> 4);
+            umma_bf16(t_a, e0 + ((kb * 8192 + kk * 32) >> 4), bd, kIdK32, acc);
+            umma_bf16(t_a + 32, e0 + ((L::E_PIECE + kb * 8192 + kk * 32) >> 4), bd, kIdK16, acc);
+          }
+        umma_commit(a_done);
+        umma_commit(&empty_e[buf]);  // the decays were read before the barrier above
+      }
+      // the state gradient at the chunk's end (overlaps the MMAs)
+      if (own_col) {
+#pragma unroll
+        for (int n = 0; n < kTcCols; ++n) dSchk[(cid * DV + r0 + n0 + n) * DK + x] = S[n];
+      }
+      if (!mbar_wait(a_done, k & 1, abort_flag)) failed = true;
+      failed = __any_sync(0xffffffffu, failed);  // the TMEM loads below are warp-collective
+      tc_fence_after();
+      if (!failed && (warp & 3) < 2) {  // dW row i = x, value rows n0..
+        const int i = x;
+        float d[kTcCols];
+        ld_sum5(t_a + lane_base + n0, d);
+        *reinterpret_cast<float4*>(dW + (cid * kC + i) * DV + r0 + n0) =
+            make_float4(d[0], d[1], d[2], d[3]);
+#pragma unroll
+        for (int n = 0; n < kTcCols; ++n) {
+          __nv_bfloat16 hi, mid;
+          const uint32_t off = L::OFF_B2 + sw128_off(n0 + n, i);
+          split_bf16(-d[n], hi, mid);
+          *reinterpret_cast<__nv_bfloat16*>(smem + off) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(smem + off + L::MID_ROWS) = mid;
+        }
+      }
+      if (failed) *abort_flag = 1;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      if (bar_sync_or(1, kTcThreads, failed)) { failed = true; break; }  // -dW complete
+      if (tid == 0) {
+        if (!mbar_wait(full_y, k & 1, abort_flag)) {
+          failed = true;
+          *abort_flag = 1;
+        } else {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {  // D_B += Y^T (-dW)
+            const uint64_t bd = dB2 + ((kk * 32) >> 4);
+            const uint32_t acc = kk ? 1u : 0u;
+            umma_bf16(t_b + 32, dY + ((kk * 2048) >> 4), bd, kIdMN32, acc);
+            umma_bf16(t_b + 64, dY + ((L::Y_PIECE + kk * 2048) >> 4), bd, kIdMN16, acc);
+          }
+          umma_commit(b_done);
+          umma_commit(empty_y);
+          if (k + 1 < nch && !issue_do_products(k + 1)) {
+            failed = true;
+            *abort_flag = 1;
+          }
+        }
+      }
+      if (!mbar_wait(b_done, k & 1, abort_flag)) failed = true;
+      failed = __any_sync(0xffffffffu, failed);
+      tc_fence_after();
+      if (!failed && (DK == 128 || (warp & 3) < 2)) {  // column x: dS = gamma_C dS + D_B
+        float d[kTcCols];
+        ld_sum5(t_b + lane_base + n0, d);
+#pragma unroll
+        for (int n = 0; n < kTcCols; ++n) S[n] = gam_C * S[n] + d[n];
+        write_state_operand();
+      }
+      if (failed) *abort_flag = 1;
+      fence_proxy_async_smem();
+    }
+    if (failed) *abort_flag = 1;
+    if (!failed && !*abort_flag && dS0 && own_col) {
+#pragma unroll
+      for (int n = 0; n < kTcCols; ++n) dS0[(bh * DV + r0 + n0 + n) * DK + x] = S[n];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    if (tid == 0) gdr_report(MOE_ERR_TIMEOUT);
+    if (tid == kTcThreads) {  // let the copies in flight land (bounded) before the CTA exits
+      volatile int no_abort = 0;
+      for (int i = 0; i < 5; ++i) {
+        uint64_t* f = i < 2 ? &full_x[i] : (i < 4 ? &full_e[i - 2] : full_y);
+        if (sent & (1u << i)) mbar_wait(f, (par >> i) & 1u, &no_abort);
+      }
+    }
+  }
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
 }
 
-template <int DK>
-constexpr size_t bwd_scan_smem_bytes() {
-  return (3 * kC * ScanLd<DK>::T + kC * ScanLd<DK>::P + kC + kC * kRS / 2 + kRS * ScanLd<DK>::T +
-          2 * kC * kRS) * sizeof(float);
-}
 
 // Register-tiled products of the per-chunk backward, for 256 threads: thread (ti, tj) =
 // (tid / 16, tid % 16) owns rows ti + 16 u (u < M / 16) and columns tj + 16 c (c < N / 16)
@@ -1560,13 +1744,13 @@ int gdr_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloat16*
   float* Gw = reinterpret_cast<float*>(w + 3 * rk + up256(chunks * kC * DV * 4) +
                                        up256(chunks * kC * kC * 4));
   const size_t sm1 = (2 * kC * Ld<DK>::v + 2 * kC * Ld<kC>::v + 3 * kC) * sizeof(float);
-  auto k1 = gdr_chunk_kernel<DK, DV, true>;
+  auto k1 = gdr_chunk_kernel<DK, DV, true, false>;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(sm1));
   if (e != cudaSuccess) return static_cast<int>(e);
   mark_before(MOE_KERNEL_GDR_CHUNK, s);
   k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, nullptr, nullptr, nullptr,
-                                       Uw, nullptr, Gw, nullptr, YQs, Ks, Ps);
+                                       Uw, nullptr, Gw, nullptr, YQs, Ks, Ps, GdrBwdImages{});
   mark_after(MOE_KERNEL_GDR_CHUNK, s);
   constexpr size_t sm2 = TcScan<DK>::SMEM;
   auto k2 = gdr_scan_tc_kernel<DK, DV>;
@@ -1579,11 +1763,17 @@ int gdr_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloat16*
   return static_cast<int>(cudaGetLastError());
 }
 
+// bytes per chunk of the backward scan's images: s P, s gamma Q^, E, Y (two bf16 pieces
+// each) and dO^T of every 16-row value slice
+size_t gdr_bwd_img_bytes(int dk, int dv) {
+  return 2 * 8192 + 3 * static_cast<size_t>(dk / 64) * 16384 + static_cast<size_t>(dv / kRS) * 2048;
+}
+
 size_t gdr_bwd_ws(int B, int T, int H, int dk, int dv) {
   const size_t nch = (T + kC - 1) / kC;
   const size_t chunks = static_cast<size_t>(B) * H * nch;
   return gdr_ws(B, T, H, dk, dv) + up256(chunks * kC * kC * 4) + up256(chunks * kC * dv * 4) +
-         up256(chunks * static_cast<size_t>(dv) * dk * 4);
+         up256(chunks * static_cast<size_t>(dv) * dk * 4) + up256(chunks * gdr_bwd_img_bytes(dk, dv));
 }
 
 template <int DK, int DV>
@@ -1603,23 +1793,32 @@ int gdr_bwd_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloa
   float* Gw = reinterpret_cast<float*>(w); w += up256(chunks * kC * 4);
   float* Aw = reinterpret_cast<float*>(w); w += up256(chunks * kC * kC * 4);
   float* dWw = reinterpret_cast<float*>(w); w += up256(chunks * kC * DV * 4);
-  float* dSw = reinterpret_cast<float*>(w);
+  float* dSw = reinterpret_cast<float*>(w); w += up256(chunks * static_cast<size_t>(DV) * DK * 4);
+  using LB = TcBwd<DK>;
+  GdrBwdImages img;
+  img.sP = reinterpret_cast<__nv_bfloat16*>(w); w += chunks * 2 * LB::SP_PIECE;
+  img.sQ = reinterpret_cast<__nv_bfloat16*>(w); w += chunks * 2 * LB::SQ_PIECE;
+  img.E = reinterpret_cast<__nv_bfloat16*>(w); w += chunks * 2 * LB::E_PIECE;
+  img.Y = reinterpret_cast<__nv_bfloat16*>(w); w += chunks * 2 * LB::Y_PIECE;
+  img.OT = reinterpret_cast<__nv_bfloat16*>(w);
+  img.dO = dO;
+  img.scale = scale;
   const size_t sm1 = (2 * kC * Ld<DK>::v + 2 * kC * Ld<kC>::v + 3 * kC) * sizeof(float);
-  auto k1 = gdr_chunk_kernel<DK, DV, false>;
+  auto k1 = gdr_chunk_kernel<DK, DV, false, true>;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(sm1));
   if (e != cudaSuccess) return static_cast<int>(e);
   mark_before(MOE_KERNEL_GDR_BWD_FACTORS, s);
   k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, Qh, Kh, Yw, Uw, Pw, Gw, Aw,
-                                       nullptr, nullptr, nullptr);
+                                       nullptr, nullptr, nullptr, img);
   mark_after(MOE_KERNEL_GDR_BWD_FACTORS, s);
-  const size_t sm2 = bwd_scan_smem_bytes<DK>();
-  auto k2 = gdr_bwd_scan_kernel<DK, DV>;
+  constexpr size_t sm2 = LB::SMEM;
+  auto k2 = gdr_bwd_scan_tc_kernel<DK, DV>;
   e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm2));
   if (e != cudaSuccess) return static_cast<int>(e);
   mark_before(MOE_KERNEL_GDR_BWD_SCAN, s);
-  k2<<<dim3(DV / kRS, H, B), 256, sm2, s>>>(Qh, Kh, Yw, Pw, Gw, dO, dST, T, H, nch, scale, dWw,
-                                            dSw, dS0);
+  k2<<<dim3(DV / kRS, H, B), kTcBlock, sm2, s>>>(img.sP, img.sQ, img.OT, img.E, img.Y, Gw, dST, H,
+                                                 nch, dWw, dSw, dS0);
   mark_after(MOE_KERNEL_GDR_BWD_SCAN, s);
   const size_t sm3 = bwd_chunk_smem_bytes<DK, DV>();
   auto k3 = gdr_bwd_chunk_kernel<DK, DV>;
