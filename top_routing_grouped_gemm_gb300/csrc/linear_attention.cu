@@ -49,6 +49,23 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bflo
   mid = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
 
+// Two bf16 pieces of 8 values scaled by `scale` (hi = bf16(scale x), mid = bf16(scale x - hi)),
+// packed in element order as 16-byte pieces.
+__device__ __forceinline__ void split8(const float (&f)[8], float scale, uint4& hi, uint4& mid) {
+  uint32_t hw[4], mw[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float a = scale * f[2 * u], b = scale * f[2 * u + 1];
+    const __nv_bfloat162 hb = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(hb);
+    const __nv_bfloat162 mb = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    hw[u] = *reinterpret_cast<const uint32_t*>(&hb);
+    mw[u] = *reinterpret_cast<const uint32_t*>(&mb);
+  }
+  hi = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  mid = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+}
+
 __device__ int g_gdr_status;  // first error a linear-attention kernel reported (0: none)
 
 __device__ __forceinline__ void gdr_report(int code) { atomicCAS(&g_gdr_status, 0, code); }
@@ -213,6 +230,33 @@ struct Ld {
   static constexpr int v = D + 1;
 };
 
+// Shared memory of gdr_chunk_kernel (one CTA per 64-token chunk and head, two CTAs per SM).
+// A1 holds, per bf16 piece and 64-wide dk block, a [128][64] K-major tile in the 128-byte
+// swizzle: rows 0..63 K^, rows 64..127 Q^.  Its K^ rows serve three times: as rows of the
+// A operand and as the K-major B operand of [K^; Q^] K^T, and (64-row boxes 16 KB apart) as
+// the MN-major B operand of Y.  After [K^; Q^] K^T the Q^ halves of the first block of each
+// piece hold the A operand of Y and then of U (A^-1 with its columns scaled, two pieces).
+// The fp32 A used by the inverse later becomes the V image (the MN-major B operand of U).
+template <int DK, int DV>
+struct TcChunk {
+  static constexpr int NKB = DK / 64;
+  static constexpr uint32_t BLK = 16384u;
+  static constexpr uint32_t OFF_A1 = 0;
+  static constexpr uint32_t A1_BYTES = 2 * NKB * BLK;
+  static constexpr uint32_t OFF_SA = A1_BYTES;               // fp32 A [64][65], then the V image
+  static constexpr uint32_t SA_BYTES = 17408u;
+  static constexpr uint32_t OFF_SI = OFF_SA + SA_BYTES;      // fp32 A^-1 [64][65]
+  static constexpr uint32_t OFF_MISC = OFF_SI + 16640u;      // beta, G, beta * gamma [64] each
+  static constexpr uint32_t OFF_BAR = OFF_MISC + 3 * kC * 4u;
+  static constexpr uint32_t BYTES = OFF_BAR + 32u;
+  static constexpr size_t SMEM = BYTES + 1024u;
+  static constexpr uint32_t SLOT0 = OFF_A1 + 8192u;          // A operands of Y and U: hi
+  static constexpr uint32_t SLOT1 = OFF_A1 + NKB * BLK + 8192u;  //                   mid
+  static_assert(kC * (kC + 1) * 4u <= SA_BYTES && (DV / 64) * 8192u <= SA_BYTES,
+                "A, then the V image, fit in their space");
+  static_assert(SMEM + 1024u <= 114u * 1024u, "two CTAs per SM");
+};
+
 // Per chunk (grid: chunks x H x B, 256 threads): q^, k^, cumulative log decay, the WY
 // factors U, Y, the masked P = Gam . tril(Q^ K^T) (diagonal included), all fp32 to the
 // workspace.  Rows past the end of the sequence are zero (beta = g = 0: no effect).
@@ -224,6 +268,13 @@ struct Ld {
 // shared-memory images (TcBwd) of s P, s gamma Q^, E = diag(gamma_C / gamma) K^ and Y (two
 // bf16 pieces each) and, per slice of 16 value rows, dO^T of the chunk (zero past the
 // sequence).
+//
+// The three dense products run on the tensor cores with the two-piece bf16 operands of the
+// scans (hi.hi + hi.mid + mid.hi, fp32 accumulation in TMEM): [K^; Q^] K^T (M = 128, N = 64,
+// K = dk), then, after the triangular inverse (fp32, four threads per column),
+// Y = (A^-1 diag(beta gamma)) K^ and U = (A^-1 diag(beta)) V (K = 64; V is bf16, so U takes
+// two products).  The masks, decays, the inverse and every output conversion run on the
+// fp32 pipes.
 struct GdrBwdImages {
   __nv_bfloat16 *sP, *sQ, *E, *Y, *OT;
   const __nv_bfloat16* dO;
@@ -231,7 +282,7 @@ struct GdrBwdImages {
 };
 
 template <int DK, int DV, bool SPLIT, bool BIMG>
-__global__ void __launch_bounds__(256) gdr_chunk_kernel(
+__global__ void __launch_bounds__(256, 2) gdr_chunk_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ beta,
     const float* __restrict__ g, int T, int H, int nch, float* __restrict__ Qh,
@@ -240,22 +291,36 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
     __nv_bfloat16* __restrict__ YQs, __nv_bfloat16* __restrict__ Ks,
     __nv_bfloat16* __restrict__ Ps, GdrBwdImages img) {
   static_assert(!(SPLIT && BIMG), "one image set per launch");
-  constexpr int LK = Ld<DK>::v, LC = Ld<kC>::v;
-  extern __shared__ float sm[];
-  float* sK = sm;                    // [C][LK]
-  float* sQ = sK + kC * LK;          // [C][LK]
-  float* sA = sQ + kC * LK;          // [C][LC]  A (unit lower)
-  float* sI = sA + kC * LC;          // [C][LC]  A^-1
-  float* sB = sI + kC * LC;          // [C] beta
-  float* sG = sB + kC;               // [C] cumulative log decay
-  float* sBG = sG + kC;              // [C] beta * gamma
+  using L = TcChunk<DK, DV>;
+  constexpr int NKB = L::NKB, LC = Ld<kC>::v;
+  extern __shared__ uint8_t tc_smem_raw[];
+  const uint32_t raw = smem_u32(tc_smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = tc_smem_raw + (sbase - raw);
+  float* sA = reinterpret_cast<float*>(smem + L::OFF_SA);   // [C][LC]  A (unit lower)
+  float* sI = reinterpret_cast<float*>(smem + L::OFF_SI);   // [C][LC]  A^-1
+  float* sB = reinterpret_cast<float*>(smem + L::OFF_MISC);  // [C] beta
+  float* sG = sB + kC;                                        // [C] cumulative log decay
+  float* sBG = sG + kC;                                       // [C] beta * gamma
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_BAR + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 12);
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t0 = c * kC;
   const size_t chunk_id = (static_cast<size_t>(b) * H + h) * nch + c;
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
 
-  // v rows: 16-byte loads issued first, held in registers until U needs them (rows past the
-  // sequence are zero)
+  // v rows: 16-byte loads issued first, held in registers until the V image is written (rows
+  // past the sequence are zero)
   constexpr int VPR = DV / 8, VPER = kC * VPR / 256;  // 16-byte pieces per row / per thread
   uint4 va[VPER];
 #pragma unroll
@@ -265,50 +330,6 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
     va[m] = t < T ? *reinterpret_cast<const uint4*>(
                         v + ((static_cast<size_t>(b) * T + t) * H + h) * DV + pc * 8)
                   : make_uint4(0u, 0u, 0u, 0u);
-  }
-  // q, k rows, L2 normalised: every 16-byte load of the two tiles in flight at once; a row's
-  // PPR pieces sit in PPR consecutive threads, which reduce its squared norm by shuffles
-  {
-    constexpr int PPR = DK / 8, PER = kC * PPR / 256;
-    static_assert(32 % PPR == 0 && PER * 256 == kC * PPR, "q/k tile loading");
-    uint4 qa[PER], ka[PER];
-#pragma unroll
-    for (int m = 0; m < PER; ++m) {
-      const int e = tid + 256 * m, i = e / PPR, pc = e - i * PPR;
-      const int t = t0 + i;
-      const size_t o = ((static_cast<size_t>(b) * T + t) * H + h) * DK + pc * 8;
-      qa[m] = t < T ? *reinterpret_cast<const uint4*>(q + o) : make_uint4(0u, 0u, 0u, 0u);
-      ka[m] = t < T ? *reinterpret_cast<const uint4*>(k + o) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int m = 0; m < PER; ++m) {
-      const int e = tid + 256 * m, i = e / PPR, pc = e - i * PPR;
-      float qf[8], kf[8];
-      const uint32_t qw[4] = {qa[m].x, qa[m].y, qa[m].z, qa[m].w};
-      const uint32_t kw[4] = {ka[m].x, ka[m].y, ka[m].z, ka[m].w};
-      float sq = 0.f, sk = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 a2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qw[j]));
-        const float2 b2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw[j]));
-        qf[2 * j] = a2.x; qf[2 * j + 1] = a2.y;
-        kf[2 * j] = b2.x; kf[2 * j + 1] = b2.y;
-        sq += a2.x * a2.x + a2.y * a2.y;
-        sk += b2.x * b2.x + b2.y * b2.y;
-      }
-#pragma unroll
-      for (int o = PPR / 2; o > 0; o >>= 1) {
-        sq += __shfl_xor_sync(0xffffffffu, sq, o);
-        sk += __shfl_xor_sync(0xffffffffu, sk, o);
-      }
-      const float iq = sq > 0.f ? 1.0f / sqrtf(sq) : 0.f;
-      const float ik = sk > 0.f ? 1.0f / sqrtf(sk) : 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        sQ[i * LK + pc * 8 + j] = qf[j] * iq;
-        sK[i * LK + pc * 8 + j] = kf[j] * ik;
-      }
-    }
   }
   // beta and the cumulative log decay (warp 0, in token order)
   if (warp == 0) {
@@ -331,72 +352,201 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
     }
   }
   __syncthreads();
-  // A (strictly lower part beta_i Gam_ij k^_i.k^_j, unit diagonal) and P (Gam_ij q^_i.k^_j,
-  // j <= i).  Thread (ti, tj) computes the 4 x 4 block of rows 4 ti .. and columns 4 tj ..
-  // (blocks above the diagonal are zero), 12 shared loads per 32 multiply-adds.
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // q, k rows, L2 normalised: a row's PPR 16-byte pieces sit in PPR consecutive threads, which
+  // reduce its squared norm by shuffles; each piece of 8 values goes out whole (16-byte
+  // stores) to the A1 operand and to every fp32 output and image this launch writes
   {
-    const int ti = tid >> 4, tj = tid & 15;
-    float ak[4][4], aq[4][4];
+    constexpr int PPR = DK / 8, PER = kC * PPR / 256;
+    static_assert(32 % PPR == 0 && PER * 256 == kC * PPR, "q/k tile loading");
+    uint4 qa[PER], ka[PER];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int m = 0; m < PER; ++m) {
+      const int e = tid + 256 * m, i = e / PPR, pc = e - i * PPR;
+      const int t = t0 + i;
+      const size_t o = ((static_cast<size_t>(b) * T + t) * H + h) * DK + pc * 8;
+      qa[m] = t < T ? *reinterpret_cast<const uint4*>(q + o) : make_uint4(0u, 0u, 0u, 0u);
+      ka[m] = t < T ? *reinterpret_cast<const uint4*>(k + o) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    const float gC = sG[kC - 1];
 #pragma unroll
-      for (int c2 = 0; c2 < 4; ++c2) ak[a][c2] = aq[a][c2] = 0.f;
-    if (tj <= ti) {
-#pragma unroll 4
-      for (int x = 0; x < DK; ++x) {
-        float ki[4], qi[4], kj[4];
+    for (int m = 0; m < PER; ++m) {
+      const int e = tid + 256 * m, i = e / PPR, pc = e - i * PPR;
+      const int x0 = pc * 8;
+      float qf[8], kf[8];
+      const uint32_t qw[4] = {qa[m].x, qa[m].y, qa[m].z, qa[m].w};
+      const uint32_t kw[4] = {ka[m].x, ka[m].y, ka[m].z, ka[m].w};
+      float sq = 0.f, sk = 0.f;
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-          ki[a] = sK[(4 * ti + a) * LK + x];
-          qi[a] = sQ[(4 * ti + a) * LK + x];
-          kj[a] = sK[(4 * tj + a) * LK + x];
+      for (int j = 0; j < 4; ++j) {
+        const float2 a2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qw[j]));
+        const float2 b2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw[j]));
+        qf[2 * j] = a2.x; qf[2 * j + 1] = a2.y;
+        kf[2 * j] = b2.x; kf[2 * j + 1] = b2.y;
+        sq += a2.x * a2.x + a2.y * a2.y;
+        sk += b2.x * b2.x + b2.y * b2.y;
+      }
+#pragma unroll
+      for (int o = PPR / 2; o > 0; o >>= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        sk += __shfl_xor_sync(0xffffffffu, sk, o);
+      }
+      const float iq = sq > 0.f ? 1.0f / sqrtf(sq) : 0.f;
+      const float ik = sk > 0.f ? 1.0f / sqrtf(sk) : 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        qf[j] *= iq;
+        kf[j] *= ik;
+      }
+      // the A1 operand: K^ row i, Q^ row 64 + i of block (piece, x0 / 64)
+      uint4 hi, mid;
+      split8(kf, 1.f, hi, mid);
+      const uint32_t kb_off = (x0 >> 6) * L::BLK;
+      *reinterpret_cast<uint4*>(smem + L::OFF_A1 + kb_off + sw128_off(i, x0 & 63)) = hi;
+      *reinterpret_cast<uint4*>(smem + L::OFF_A1 + NKB * L::BLK + kb_off + sw128_off(i, x0 & 63)) = mid;
+      split8(qf, 1.f, hi, mid);
+      *reinterpret_cast<uint4*>(smem + L::OFF_A1 + kb_off + sw128_off(64 + i, x0 & 63)) = hi;
+      *reinterpret_cast<uint4*>(smem + L::OFF_A1 + NKB * L::BLK + kb_off + sw128_off(64 + i, x0 & 63)) = mid;
+      if constexpr (SPLIT) {  // gamma q^ (rows 64.. of YQs) and k^ images for the scan
+        using LS = TcScan<DK>;
+        __nv_bfloat16* yq = YQs + chunk_id * (LS::A1_BYTES / 2);
+        __nv_bfloat16* ko = Ks + chunk_id * (LS::A3_BYTES / 2);
+        split8(qf, __expf(sG[i]), hi, mid);
+        *reinterpret_cast<uint4*>(yq + LS::a1(0, 64 + i, x0)) = hi;
+        *reinterpret_cast<uint4*>(yq + LS::a1(1, 64 + i, x0)) = mid;
+        split8(kf, 1.f, hi, mid);
+        *reinterpret_cast<uint4*>(ko + LS::a3(0, i, x0)) = hi;
+        *reinterpret_cast<uint4*>(ko + LS::a3(1, i, x0)) = mid;
+      } else {
+        float4* qo = reinterpret_cast<float4*>(Qh + chunk_id * kC * DK + i * DK + x0);
+        float4* ko = reinterpret_cast<float4*>(Kh + chunk_id * kC * DK + i * DK + x0);
+        qo[0] = make_float4(qf[0], qf[1], qf[2], qf[3]);
+        qo[1] = make_float4(qf[4], qf[5], qf[6], qf[7]);
+        ko[0] = make_float4(kf[0], kf[1], kf[2], kf[3]);
+        ko[1] = make_float4(kf[4], kf[5], kf[6], kf[7]);
+        if constexpr (BIMG) {  // s gamma q^ and E = (gamma_C / gamma) k^
+          using LB = TcBwd<DK>;
+          split8(qf, img.scale * __expf(sG[i]), hi, mid);
+          *reinterpret_cast<uint4*>(img.sQ + chunk_id * LB::SQ_PIECE + LB::mn(0, i, x0)) = hi;
+          *reinterpret_cast<uint4*>(img.sQ + chunk_id * LB::SQ_PIECE + LB::mn(1, i, x0)) = mid;
+          split8(kf, __expf(gC - sG[i]), hi, mid);
+          *reinterpret_cast<uint4*>(img.E + chunk_id * LB::E_PIECE + LB::e(0, i, x0)) = hi;
+          *reinterpret_cast<uint4*>(img.E + chunk_id * LB::E_PIECE + LB::e(1, i, x0)) = mid;
         }
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int c2 = 0; c2 < 4; ++c2) {
-            ak[a][c2] += ki[a] * kj[c2];
-            aq[a][c2] += qi[a] * kj[c2];
-          }
       }
     }
+  }
+  if constexpr (BIMG) {  // dO^T of every 16-row value slice (2-byte image stores)
+    using LB = TcBwd<DK>;
+    constexpr int PPR = DV / 8;
+    for (int e = tid; e < kC * PPR; e += 256) {
+      const int t = e / PPR, pc = e - t * PPR;
+      const int tt = t0 + t;
+      const uint4 raw = tt < T ? *reinterpret_cast<const uint4*>(
+                                     img.dO + ((static_cast<size_t>(b) * T + tt) * H + h) * DV + pc * 8)
+                               : make_uint4(0u, 0u, 0u, 0u);
+      const __nv_bfloat16* vals = reinterpret_cast<const __nv_bfloat16*>(&raw);
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+      for (int q8 = 0; q8 < 8; ++q8) {
+        const int col = pc * 8 + q8;
+        img.OT[(chunk_id * (DV / kRS) + col / kRS) * (LB::OT_BYTES / 2) + LB::ot(col % kRS, t)] =
+            vals[q8];
+      }
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  bool failed = false;
+  if (tid == 0) {  // D = [K^; Q^] K^T (columns 0..63)
+    tc_fence_after();
+    constexpr uint32_t kId = idesc_bf16_f32(128, 64, false, false);
+    const uint64_t d0 = smem_desc_sw128(sbase + L::OFF_A1, 16, 1024);
 #pragma unroll
-      for (int c2 = 0; c2 < 4; ++c2) {
-        const int i = 4 * ti + a, j = 4 * tj + c2;
-        float av = 0.f, pv = 0.f;
-        if (j <= i) {
-          const float gam = __expf(sG[i] - sG[j]);
-          av = j < i ? sB[i] * gam * ak[a][c2] : 1.f;
-          pv = gam * aq[a][c2];
+    for (int kb = 0; kb < NKB; ++kb)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int pr = 0; pr < 3; ++pr) {
+          const uint32_t sa = pr == 2, sb = pr == 1;
+          const uint64_t ad = d0 + (((sa * NKB + kb) * L::BLK + kk * 32) >> 4);
+          const uint64_t bd = d0 + (((sb * NKB + kb) * L::BLK + kk * 32) >> 4);
+          umma_bf16(tmem, ad, bd, kId, (kb | kk | pr) ? 1u : 0u);
         }
-        sA[i * LC + j] = av;
-        if constexpr (SPLIT) {
-          using L = TcScan<DK>;
-          __nv_bfloat16 hi, mid;
-          split_bf16(pv, hi, mid);
-          Ps[chunk_id * (L::P_BYTES / 2) + L::p(0, i, j)] = hi;
-          Ps[chunk_id * (L::P_BYTES / 2) + L::p(1, i, j)] = mid;
-        } else {
-          Pm[chunk_id * kC * kC + i * kC + j] = pv;
-          if constexpr (BIMG) {
-            using LB = TcBwd<DK>;
-            __nv_bfloat16 hi, mid;
-            split_bf16(img.scale * pv, hi, mid);
-            img.sP[chunk_id * LB::SP_PIECE + LB::sp(0, i, j)] = hi;
-            img.sP[chunk_id * LB::SP_PIECE + LB::sp(1, i, j)] = mid;
+    umma_commit(bar);
+  }
+  // A (strictly lower part beta_i Gam_ij k^_i.k^_j, unit diagonal) into shared memory and
+  // P (Gam_ij q^_i.k^_j, j <= i) out: warp w reads TMEM lanes 32 (w % 4).. (rows 0..63: A,
+  // 64..127: P) and columns 32 (w / 4) .. + 31
+  if (!mbar_wait(bar, 0, abort_flag)) failed = true;
+  failed = __any_sync(0xffffffffu, failed);
+  tc_fence_after();
+  const int row = 32 * (warp & 3) + lane, j0 = 32 * (warp >> 2);
+  if (!failed) {
+    float d[32];
+    {
+      float d1[16];
+      const uint32_t ta = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + j0;
+      tmem_ld16(ta, d1);
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) d[jj] = d1[jj];
+      tmem_ld16(ta + 16, d1);
+      tmem_ld_wait();
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) d[16 + jj] = d1[jj];
+    }
+    if (row < kC) {
+      const int i = row;
+      const float gi = sG[i], bi = sB[i];
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = j0 + jj;
+        sA[i * LC + j] = j < i ? bi * __expf(gi - sG[j]) * d[jj] : (j == i ? 1.f : 0.f);
+      }
+    } else {
+      const int i = row - kC;
+      const float gi = sG[i];
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = j0 + jj;
+        d[jj] = j <= i ? __expf(gi - sG[j]) * d[jj] : 0.f;
+      }
+      if constexpr (SPLIT) {
+        using LS = TcScan<DK>;
+        __nv_bfloat16* po = Ps + chunk_id * (LS::P_BYTES / 2);
+#pragma unroll
+        for (int p8 = 0; p8 < 4; ++p8) {
+          uint4 hi, mid;
+          split8(*reinterpret_cast<const float(*)[8]>(d + 8 * p8), 1.f, hi, mid);
+          *reinterpret_cast<uint4*>(po + LS::p(0, i, j0 + 8 * p8)) = hi;
+          *reinterpret_cast<uint4*>(po + LS::p(1, i, j0 + 8 * p8)) = mid;
+        }
+      } else {
+        float4* pm = reinterpret_cast<float4*>(Pm + chunk_id * kC * kC + i * kC + j0);
+#pragma unroll
+        for (int p4 = 0; p4 < 8; ++p4)
+          pm[p4] = make_float4(d[4 * p4], d[4 * p4 + 1], d[4 * p4 + 2], d[4 * p4 + 3]);
+        if constexpr (BIMG) {
+          using LB = TcBwd<DK>;
+#pragma unroll
+          for (int p8 = 0; p8 < 4; ++p8) {
+            uint4 hi, mid;
+            split8(*reinterpret_cast<const float(*)[8]>(d + 8 * p8), img.scale, hi, mid);
+            *reinterpret_cast<uint4*>(img.sP + chunk_id * LB::SP_PIECE + LB::sp(0, i, j0 + 8 * p8)) = hi;
+            *reinterpret_cast<uint4*>(img.sP + chunk_id * LB::SP_PIECE + LB::sp(1, i, j0 + 8 * p8)) = mid;
           }
         }
       }
+    }
   }
-  __syncthreads();
+  tc_fence_before();
+  if (__syncthreads_or(failed)) failed = true;
   // A^-1 (unit lower triangular), one row per step: X_i = e_i - sum_{j<i} A_ij X_j, the 64
   // columns in parallel with 4 threads per column (each a quarter of the j range, combined by
   // shuffles within the 4 lanes).  A column only reads its own earlier rows, written by its
-  // own four lanes, so the steps are ordered within the warp (the block barrier before Y
-  // publishes the whole inverse).
-  {
+  // own four lanes, so the steps are ordered within the warp.
+  if (!failed) {
     const int col = tid >> 2, part = tid & 3;
     for (int i = 0; i < kC; ++i) {
       float x = 0.f;
@@ -407,170 +557,138 @@ __global__ void __launch_bounds__(256) gdr_chunk_kernel(
       __syncwarp();
     }
   }
-  // q^, k^ out for the scan (SPLIT: gamma q^ and k^ in two bf16 pieces); then K^ rows
-  // scaled by beta gamma in place
-  if constexpr (SPLIT) {
-    // (x, x + 1) share a 16-byte piece of the swizzled images: one 4-byte store per piece
-    using L = TcScan<DK>;
-    __nv_bfloat16* yq = YQs + chunk_id * (L::A1_BYTES / 2);
-    __nv_bfloat16* ko = Ks + chunk_id * (L::A3_BYTES / 2);
-    for (int e = tid; e < kC * DK / 2; e += 256) {
-      const int i = (2 * e) / DK, x = 2 * e - i * DK;
-      const float gam = __expf(sG[i]);
-      __nv_bfloat16 h0, m0, h1, m1;
-      split_bf16(gam * sQ[i * LK + x], h0, m0);
-      split_bf16(gam * sQ[i * LK + x + 1], h1, m1);
-      *reinterpret_cast<__nv_bfloat162*>(yq + L::a1(0, 64 + i, x)) = __halves2bfloat162(h0, h1);
-      *reinterpret_cast<__nv_bfloat162*>(yq + L::a1(1, 64 + i, x)) = __halves2bfloat162(m0, m1);
-      split_bf16(sK[i * LK + x], h0, m0);
-      split_bf16(sK[i * LK + x + 1], h1, m1);
-      *reinterpret_cast<__nv_bfloat162*>(ko + L::a3(0, i, x)) = __halves2bfloat162(h0, h1);
-      *reinterpret_cast<__nv_bfloat162*>(ko + L::a3(1, i, x)) = __halves2bfloat162(m0, m1);
-    }
-  } else {
-    for (int e = tid; e < kC * DK; e += 256) {
-      const int i = e / DK, x = e - i * DK;
-      Qh[chunk_id * kC * DK + e] = sQ[i * LK + x];
-      Kh[chunk_id * kC * DK + e] = sK[i * LK + x];
-    }
-    if constexpr (BIMG) {  // s gamma q^ and E = (gamma_C / gamma) k^, pairs per 4-byte store
-      using LB = TcBwd<DK>;
-      __nv_bfloat16* sq = img.sQ + chunk_id * LB::SQ_PIECE;
-      __nv_bfloat16* eo = img.E + chunk_id * LB::E_PIECE;
-      const float gC = sG[kC - 1];
-      for (int e = tid; e < kC * DK / 2; e += 256) {
-        const int i = (2 * e) / DK, x = 2 * e - i * DK;
-        const float qs = img.scale * __expf(sG[i]), dec = __expf(gC - sG[i]);
-        __nv_bfloat16 h0, m0, h1, m1;
-        split_bf16(qs * sQ[i * LK + x], h0, m0);
-        split_bf16(qs * sQ[i * LK + x + 1], h1, m1);
-        *reinterpret_cast<__nv_bfloat162*>(sq + LB::mn(0, i, x)) = __halves2bfloat162(h0, h1);
-        *reinterpret_cast<__nv_bfloat162*>(sq + LB::mn(1, i, x)) = __halves2bfloat162(m0, m1);
-        split_bf16(dec * sK[i * LK + x], h0, m0);
-        split_bf16(dec * sK[i * LK + x + 1], h1, m1);
-        *reinterpret_cast<__nv_bfloat162*>(eo + LB::e(0, i, x)) = __halves2bfloat162(h0, h1);
-        *reinterpret_cast<__nv_bfloat162*>(eo + LB::e(1, i, x)) = __halves2bfloat162(m0, m1);
-      }
-      // dO^T of every 16-row value slice: 16-byte loads of dO rows, 2-byte image stores
-      constexpr int PPR = DV / 8;
-      for (int e = tid; e < kC * PPR; e += 256) {
-        const int t = e / PPR, pc = e - t * PPR;
-        const int tt = t0 + t;
-        const uint4 raw = tt < T ? *reinterpret_cast<const uint4*>(
-                                       img.dO + ((static_cast<size_t>(b) * T + tt) * H + h) * DV + pc * 8)
-                                 : make_uint4(0u, 0u, 0u, 0u);
-        const __nv_bfloat16* vals = reinterpret_cast<const __nv_bfloat16*>(&raw);
+  __syncthreads();
+  // the A operand of Y, A^-1 diag(beta gamma) (two pieces, K-major [64 i][64 j]), and the V
+  // image (MN-major [64 j][dv] in 64-wide boxes) over A's space
+  auto write_inverse_operand = [&](const float* colscale) {
+    const int i = tid >> 2, jq = 16 * (tid & 3);
 #pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {
-          const int col = pc * 8 + q8;
-          img.OT[(chunk_id * (DV / kRS) + col / kRS) * (LB::OT_BYTES / 2) + LB::ot(col % kRS, t)] =
-              vals[q8];
-        }
+    for (int p8 = 0; p8 < 2; ++p8) {
+      float f[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = jq + 8 * p8 + u;
+        f[u] = sI[i * LC + j] * colscale[j];
       }
+      uint4 hi, mid;
+      split8(f, 1.f, hi, mid);
+      *reinterpret_cast<uint4*>(smem + L::SLOT0 + sw128_off(i, jq + 8 * p8)) = hi;
+      *reinterpret_cast<uint4*>(smem + L::SLOT1 + sw128_off(i, jq + 8 * p8)) = mid;
+    }
+  };
+  if (!failed) {
+    write_inverse_operand(sBG);
+#pragma unroll
+    for (int m = 0; m < VPER; ++m) {
+      const int e = tid + 256 * m, j = e / VPR, pc = e - j * VPR;
+      const int n = pc * 8;
+      *reinterpret_cast<uint4*>(smem + L::OFF_SA + (n >> 6) * 8192 + sw128_off(j, n & 63)) = va[m];
     }
   }
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
-  for (int e = tid; e < kC * DK; e += 256) {
-    const int i = e / DK, x = e - i * DK;
-    sK[i * LK + x] *= sBG[i];
+  const uint64_t dS0 = smem_desc_sw128(sbase + L::SLOT0, 16, 1024);
+  const uint64_t dS1 = smem_desc_sw128(sbase + L::SLOT1, 16, 1024);
+  if (tid == 0 && !failed) {  // Y = (A^-1 diag(beta gamma)) K^ (columns 0 .. dk - 1)
+    tc_fence_after();
+    constexpr uint32_t kIdY = idesc_bf16_f32(128, DK, false, true);
+    const uint64_t dK = smem_desc_sw128(sbase + L::OFF_A1, L::BLK, 1024);  // MN-major boxes
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int pr = 0; pr < 3; ++pr) {
+        const uint64_t ad = (pr == 2 ? dS1 : dS0) + ((kk * 32) >> 4);
+        const uint64_t bd = dK + (((pr == 1 ? NKB * L::BLK : 0u) + kk * 2048) >> 4);
+        umma_bf16(tmem, ad, bd, kIdY, (kk | pr) ? 1u : 0u);
+      }
+    umma_commit(bar);
   }
-  __syncthreads();
-  // Y = A^-1 (diag(beta gamma) K^): thread (ti, tx) computes rows 4 ti .. 4 ti + 3 and
-  // columns tx, tx + 16, ... (A^-1 is zero above the diagonal)
-  {
-    constexpr int TX = DK / 16;
-    const int ti = tid >> 4, tx = tid & 15;
-    float acc[4][TX];
+  if (!failed && !mbar_wait(bar, 1, abort_flag)) failed = true;
+  // the A operand of U, A^-1 diag(beta), in the same places (Y's MMAs have read them)
+  if (!failed) write_inverse_operand(sB);
+  fence_proxy_async_smem();
+  tc_fence_before();
+  if (__syncthreads_or(failed)) failed = true;
+  if (tid == 0 && !failed) {  // U = (A^-1 diag(beta)) V (columns dk .. dk + dv - 1)
+    tc_fence_after();
+    constexpr uint32_t kIdU = idesc_bf16_f32(128, DV, false, true);
+    const uint64_t dV = smem_desc_sw128(sbase + L::OFF_SA, 8192, 1024);
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-      for (int u = 0; u < TX; ++u) acc[a][u] = 0.f;
-    for (int j = 0; j <= 4 * ti + 3; ++j) {
-      float ai[4], kv[TX];
+      for (int pr = 0; pr < 2; ++pr)
+        umma_bf16(tmem + DK, (pr ? dS1 : dS0) + ((kk * 32) >> 4), dV + ((kk * 2048) >> 4), kIdU,
+                  (kk | pr) ? 1u : 0u);
+    umma_commit(bar);
+  }
+  // Y out (while U's MMAs run): rows i = TMEM lanes 0..63, dk columns split over two warps
+  const bool yrows = (warp & 3) < 2;
+  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+  if (!failed && yrows) {
+    const int i = row;
+    constexpr int HX = DK / 2;
+#pragma unroll 1
+    for (int x0 = (warp >> 2) * HX; x0 < (warp >> 2) * HX + HX; x0 += 16) {
+      float y[16];
+      tmem_ld16(tl + x0, y);
+      tmem_ld_wait();
 #pragma unroll
-      for (int a = 0; a < 4; ++a) ai[a] = sI[(4 * ti + a) * LC + j];
-#pragma unroll
-      for (int u = 0; u < TX; ++u) kv[u] = sK[j * LK + tx + 16 * u];
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int u = 0; u < TX; ++u) acc[a][u] += ai[a] * kv[u];
-    }
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int u = 0; u < TX; ++u) {
-        const int row = 4 * ti + a, col = tx + 16 * u;
+      for (int p8 = 0; p8 < 2; ++p8) {
+        const float(&f)[8] = *reinterpret_cast<const float(*)[8]>(y + 8 * p8);
+        const int x = x0 + 8 * p8;
+        uint4 hi, mid;
         if constexpr (SPLIT) {
-          using L = TcScan<DK>;
-          __nv_bfloat16 hi, mid;
-          split_bf16(acc[a][u], hi, mid);
-          YQs[chunk_id * (L::A1_BYTES / 2) + L::a1(0, row, col)] = hi;
-          YQs[chunk_id * (L::A1_BYTES / 2) + L::a1(1, row, col)] = mid;
+          using LS = TcScan<DK>;
+          __nv_bfloat16* yq = YQs + chunk_id * (LS::A1_BYTES / 2);
+          split8(f, 1.f, hi, mid);
+          *reinterpret_cast<uint4*>(yq + LS::a1(0, i, x)) = hi;
+          *reinterpret_cast<uint4*>(yq + LS::a1(1, i, x)) = mid;
         } else {
-          Y[chunk_id * kC * DK + row * DK + col] = acc[a][u];
+          float4* yo = reinterpret_cast<float4*>(Y + chunk_id * kC * DK + i * DK + x);
+          yo[0] = make_float4(f[0], f[1], f[2], f[3]);
+          yo[1] = make_float4(f[4], f[5], f[6], f[7]);
           if constexpr (BIMG) {
             using LB = TcBwd<DK>;
-            __nv_bfloat16 hi, mid;
-            split_bf16(acc[a][u], hi, mid);
-            img.Y[chunk_id * LB::Y_PIECE + LB::mn(0, row, col)] = hi;
-            img.Y[chunk_id * LB::Y_PIECE + LB::mn(1, row, col)] = mid;
+            split8(f, 1.f, hi, mid);
+            *reinterpret_cast<uint4*>(img.Y + chunk_id * LB::Y_PIECE + LB::mn(0, i, x)) = hi;
+            *reinterpret_cast<uint4*>(img.Y + chunk_id * LB::Y_PIECE + LB::mn(1, i, x)) = mid;
           }
         }
       }
-  }
-  __syncthreads();
-  // V rows (beta-scaled) into the space of the K and Q tiles (no longer needed), then
-  // U = A^-1 (diag(beta) V) with the same tiling
-  constexpr int LV = Ld<DV>::v;
-  static_assert(kC * LV <= 2 * kC * LK, "the V tile fits where the K and Q tiles were");
-  float* sV = sK;  // [C][LV]
-#pragma unroll
-  for (int m = 0; m < VPER; ++m) {
-    const int e = tid + 256 * m, i = e / VPR, pc = e - i * VPR;
-    const uint32_t vw[4] = {va[m].x, va[m].y, va[m].z, va[m].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 a2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vw[j]));
-      sV[i * LV + pc * 8 + 2 * j] = sB[i] * a2.x;
-      sV[i * LV + pc * 8 + 2 * j + 1] = sB[i] * a2.y;
     }
   }
-  __syncthreads();
-  {
-    constexpr int TX = DV / 16;
-    const int ti = tid >> 4, tx = tid & 15;
-    float acc[4][TX];
+  if (!failed && !mbar_wait(bar, 0, abort_flag)) failed = true;  // U's MMAs (phase 2)
+  failed = __any_sync(0xffffffffu, failed);
+  tc_fence_after();
+  if (!failed && yrows) {  // U out: rows i, dv columns split over two warps
+    const int i = row;
+    constexpr int HN = DV / 2;
+#pragma unroll 1
+    for (int n0 = (warp >> 2) * HN; n0 < (warp >> 2) * HN + HN; n0 += 16) {
+      float u[16];
+      tmem_ld16(tl + DK + n0, u);
+      tmem_ld_wait();
+      float4* uo;
+      if constexpr (SPLIT)  // slice n0 / 16 of 16 value rows, row i
+        uo = reinterpret_cast<float4*>(U + ((chunk_id * (DV / kRS) + n0 / kRS) * kC + i) * kRS);
+      else
+        uo = reinterpret_cast<float4*>(U + chunk_id * kC * DV + i * DV + n0);
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int u = 0; u < TX; ++u) acc[a][u] = 0.f;
-    for (int j = 0; j <= 4 * ti + 3; ++j) {
-      float ai[4], vv[TX];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) ai[a] = sI[(4 * ti + a) * LC + j];
-#pragma unroll
-      for (int u = 0; u < TX; ++u) vv[u] = sV[j * LV + tx + 16 * u];
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int u = 0; u < TX; ++u) acc[a][u] += ai[a] * vv[u];
+      for (int p4 = 0; p4 < 4; ++p4)
+        uo[p4] = make_float4(u[4 * p4], u[4 * p4 + 1], u[4 * p4 + 2], u[4 * p4 + 3]);
     }
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int u = 0; u < TX; ++u) {
-        const int row = 4 * ti + a, col = tx + 16 * u;
-        static_assert(kRS == 16, "U slices are this tiling's 16-column groups");
-        if constexpr (SPLIT)  // slice u of 16 value rows, column tx
-          U[((chunk_id * (DV / kRS) + u) * kC + row) * kRS + tx] = acc[a][u];
-        else
-          U[chunk_id * kC * DV + row * DV + col] = acc[a][u];
-      }
   }
+  static_assert(kRS == 16, "U slices are 16-column groups");
   if (tid < kC) Gc[chunk_id * kC + tid] = sG[tid];
-  if (Ai)
+  if (Ai && !failed)
     for (int e = tid; e < kC * kC; e += 256) Ai[chunk_id * kC * kC + e] = sI[(e / kC) * LC + (e % kC)];
+  tc_fence_before();
+  if (__syncthreads_or(failed) && tid == 0) gdr_report(MOE_ERR_TIMEOUT);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
 }
 
 // Scan over the chunks of one (b, h) for RS = 16 value rows of the state (grid: DV/RS x H x B,
@@ -1743,7 +1861,7 @@ int gdr_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloat16*
   auto* Ps = reinterpret_cast<__nv_bfloat16*>(w + 3 * rk + up256(chunks * kC * DV * 4));
   float* Gw = reinterpret_cast<float*>(w + 3 * rk + up256(chunks * kC * DV * 4) +
                                        up256(chunks * kC * kC * 4));
-  const size_t sm1 = (2 * kC * Ld<DK>::v + 2 * kC * Ld<kC>::v + 3 * kC) * sizeof(float);
+  constexpr size_t sm1 = TcChunk<DK, DV>::SMEM;
   auto k1 = gdr_chunk_kernel<DK, DV, true, false>;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(sm1));
@@ -1803,7 +1921,7 @@ int gdr_bwd_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloa
   img.OT = reinterpret_cast<__nv_bfloat16*>(w);
   img.dO = dO;
   img.scale = scale;
-  const size_t sm1 = (2 * kC * Ld<DK>::v + 2 * kC * Ld<kC>::v + 3 * kC) * sizeof(float);
+  constexpr size_t sm1 = TcChunk<DK, DV>::SMEM;
   auto k1 = gdr_chunk_kernel<DK, DV, false, true>;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(sm1));
