@@ -542,19 +542,57 @@ __global__ void __launch_bounds__(256, 2) gdr_chunk_kernel(
   }
   tc_fence_before();
   if (__syncthreads_or(failed)) failed = true;
-  // A^-1 (unit lower triangular), one row per step: X_i = e_i - sum_{j<i} A_ij X_j, the 64
-  // columns in parallel with 4 threads per column (each a quarter of the j range, combined by
-  // shuffles within the 4 lanes).  A column only reads its own earlier rows, written by its
-  // own four lanes, so the steps are ordered within the warp.
+  // X = A^-1 (A unit lower triangular) by 16 x 16 blocks.  The four diagonal blocks by
+  // substitution, X_i = e_i - sum_{j<i} A_ij X_j within the block (16 steps; all blocks and
+  // their 16 columns at once, four threads per column combining by shuffles; a column only
+  // reads rows its own four lanes wrote, so the steps are ordered within the warp); the
+  // blocks above the diagonal are zero; then the blocks below it by distance d = 1, 2, 3
+  // from the diagonal (block indices, i - j = d):
+  //     X_ij = -X_ii (sum_{k=j}^{i-1} A_ik X_kj)
+  // each round fully parallel (the X_kj it reads are nearer the diagonal).
   if (!failed) {
-    const int col = tid >> 2, part = tid & 3;
-    for (int i = 0; i < kC; ++i) {
+    const int bb = tid >> 6, cc = (tid >> 2) & 15, part = tid & 3;
+    const int jg = 16 * bb + cc;
+    for (int r = 0; r < 16; ++r) {
+      const int i = 16 * bb + r;
       float x = 0.f;
-      for (int j = col + part; j < i; j += 4) x -= sA[i * LC + j] * sI[j * LC + col];
+      for (int j = jg + part; j < i; j += 4) x -= sA[i * LC + j] * sI[j * LC + jg];
       x += __shfl_xor_sync(0xffffffffu, x, 1);
       x += __shfl_xor_sync(0xffffffffu, x, 2);
-      if (part == 0) sI[i * LC + col] = i < col ? 0.f : (i == col ? 1.f : x);
+      if (part == 0) sI[i * LC + jg] = r < cc ? 0.f : (r == cc ? 1.f : x);
       __syncwarp();
+    }
+    for (int e = tid; e < 6 * 256; e += 256) {  // blocks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+      const int blk = e >> 8, w = e & 255;
+      const int ib = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+      const int jb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+      sI[(16 * ib + (w >> 4)) * LC + 16 * jb + (w & 15)] = 0.f;
+    }
+  }
+  __syncthreads();
+  if (!failed) {
+    // sums of the current round: [3][16][16] fp32 over the Q^ rows of A1 (read by the first
+    // MMAs only, which have completed)
+    float* sT = reinterpret_cast<float*>(smem + L::OFF_A1 + 8192);
+    for (int d = 1; d < 4; ++d) {
+      const int np = 4 - d;  // block pairs (jb + d, jb), jb = 0 .. np - 1
+      for (int e = tid; e < np * 256; e += 256) {
+        const int pj = e >> 8, w = e & 255;
+        const int i = 16 * (pj + d) + (w >> 4), jc = 16 * pj + (w & 15);
+        float t = 0.f;
+        for (int kk = 16 * pj; kk < 16 * (pj + d); ++kk) t += sA[i * LC + kk] * sI[kk * LC + jc];
+        sT[e] = t;
+      }
+      __syncthreads();
+      for (int e = tid; e < np * 256; e += 256) {
+        const int pj = e >> 8, w = e & 255, ib = pj + d;
+        const int i = 16 * ib + (w >> 4), cl = w & 15;
+        float x = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) x -= sI[i * LC + 16 * ib + m] * sT[pj * 256 + m * 16 + cl];
+        sI[i * LC + 16 * pj + cl] = x;
+      }
+      __syncthreads();
     }
   }
   __syncthreads();
