@@ -171,10 +171,12 @@ __device__ __forceinline__ void tmem_ld_sum3(uint32_t taddr, float (&d)[4]) {
 // those tiles is carried as two bf16 pieces (hi, mid), each piece a tile of its own.
 // 16 consumer warps: warp w reads TMEM lanes 32 (w % 4) .. + 31 (its quadrant) and handles
 // value rows kTcCols (w / 4) .. + kTcCols - 1 of the slice, so each epilogue is spread over
-// four warps per scheduler; one more warp issues the bulk copies
+// four warps per scheduler; warp 16 issues the bulk copies, warp 17 the MMAs (its lane 0),
+// so that neither waits on the other or on an epilogue
 constexpr int kTcThreads = 512;
 constexpr int kTcCols = 4;
-constexpr int kTcBlock = kTcThreads + 32;
+constexpr int kTcBlock = kTcThreads + 64;
+constexpr int kTcSync = kTcThreads + 32;  // the consumer warps and the MMA warp
 
 template <int DK>
 struct TcScan {
@@ -837,6 +839,72 @@ __global__ void __launch_bounds__(kTcBlock, 1) gdr_scan_tc_kernel(
       }
       if (failed) *abort_flag = 1;
     }
+  } else if (warp == kTcThreads / 32 + 1) {
+    // ------------------------------------------------------------ MMA warp (lane 0 issues)
+    const bool issuer = (tid & 31) == 0;
+    constexpr uint32_t kIdK32 = idesc_bf16_f32(128, 32, false, false);
+    constexpr uint32_t kIdK16 = idesc_bf16_f32(128, 16, false, false);
+    constexpr uint32_t kIdMN32 = idesc_bf16_f32(128, 32, true, false);
+    constexpr uint32_t kIdMN16 = idesc_bf16_f32(128, 16, true, false);
+    // descriptors of the operand tiles' first atoms; an operand further on adds its byte
+    // offset / 16 (every address stays below 256 KB, so the 14-bit start field cannot carry)
+    const uint64_t dA1 = smem_desc_sw128(sbase + L::OFF_A1, 16, 1024);
+    const uint64_t dB1 = smem_desc_sw128(sbase + L::OFF_B1, 16, 1024);
+    const uint64_t dP = smem_desc_sw128(sbase + L::OFF_P - 8192, 16, 1024);
+    const uint64_t dB2 = smem_desc_sw128(sbase + L::OFF_B2, 16, 1024);
+    const uint64_t dA3 = smem_desc_sw128(sbase + L::OFF_A3, 8192, 1024);
+    const uint64_t dB3 = smem_desc_sw128(sbase + L::OFF_B3, 16, 1024);
+    for (int c = 0; c < nch; ++c) {
+      const int buf = c & 1;
+      const uint32_t use = static_cast<uint32_t>(c >> 1);
+      const uint32_t t_d1 = tmem + 64 * buf;
+      if (issuer && !mbar_wait(&full_a[buf], use & 1, abort_flag)) failed = true;
+      tc_fence_before();
+      if (bar_sync_or(1, kTcSync, failed)) { failed = true; break; }  // B1 of this chunk
+      if (issuer) {  // D1 = [Y; gamma Q^] S^T
+        tc_fence_after();
+        const uint64_t a0 = dA1 + ((buf * L::A1_BYTES) >> 4);
+#pragma unroll
+        for (int kb = 0; kb < NKB; ++kb)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t acc = (kb | k) ? 1u : 0u;
+            const uint64_t bd = dB1 + ((kb * L::B1_KB + k * 32) >> 4);
+            umma_bf16(t_d1, a0 + ((kb * 16384 + k * 32) >> 4), bd, kIdK32, acc);
+            umma_bf16(t_d1 + 32, a0 + ((L::A1_SPLIT + kb * 16384 + k * 32) >> 4), bd, kIdK16, acc);
+          }
+        umma_commit(d1_done);
+      }
+      tc_fence_before();
+      if (bar_sync_or(1, kTcSync, failed)) { failed = true; break; }  // W, Wd formed
+      if (issuer) {
+        mbar_arrive(&empty_a[buf]);  // [Y; gamma Q^], the U slice and the decays are read
+        if (!mbar_wait(full_k, c & 1, abort_flag) || !mbar_wait(&full_p[buf], use & 1, abort_flag)) {
+          failed = true;
+          *abort_flag = 1;
+        } else {
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // D3 = K^T Wd
+            const uint64_t bd3 = dB3 + ((k * 32) >> 4);
+            umma_bf16(t_d3, dA3 + ((k * 2048) >> 4), bd3, kIdMN32, k ? 1u : 0u);
+            umma_bf16(t_d3 + 32, dA3 + ((L::A3_SPLIT + k * 2048) >> 4), bd3, kIdMN16, k ? 1u : 0u);
+          }
+          umma_commit(d3_done);
+          umma_commit(empty_k);
+          const uint64_t p0 = dP + ((buf * L::P_BYTES) >> 4);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // D1[64:128] += P W
+            const uint64_t bd2 = dB2 + ((k * 32) >> 4);
+            umma_bf16(t_d1, p0 + ((k * 32) >> 4), bd2, kIdK32, 1u);
+            umma_bf16(t_d1 + 32, p0 + ((L::P_SPLIT + k * 32) >> 4), bd2, kIdK16, 1u);
+          }
+          umma_commit(&empty_p[buf]);
+        }
+      }
+    }
+    if (failed) *abort_flag = 1;
+    if (issuer && !failed) umma_commit(d1_done);  // the last chunk's P W (its output rows)
   } else {
     // ------------------------------------------------------------ consumer warps
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
@@ -874,18 +942,6 @@ __global__ void __launch_bounds__(kTcBlock, 1) gdr_scan_tc_kernel(
     };
     write_state_operand();
     fence_proxy_async_smem();
-    constexpr uint32_t kIdK32 = idesc_bf16_f32(128, 32, false, false);
-    constexpr uint32_t kIdK16 = idesc_bf16_f32(128, 16, false, false);
-    constexpr uint32_t kIdMN32 = idesc_bf16_f32(128, 32, true, false);
-    constexpr uint32_t kIdMN16 = idesc_bf16_f32(128, 16, true, false);
-    // descriptors of the operand tiles' first atoms; an operand further on adds its byte
-    // offset / 16 (every address stays below 256 KB, so the 14-bit start field cannot carry)
-    const uint64_t dA1 = smem_desc_sw128(sbase + L::OFF_A1, 16, 1024);
-    const uint64_t dB1 = smem_desc_sw128(sbase + L::OFF_B1, 16, 1024);
-    const uint64_t dP = smem_desc_sw128(sbase + L::OFF_P - 8192, 16, 1024);
-    const uint64_t dB2 = smem_desc_sw128(sbase + L::OFF_B2, 16, 1024);
-    const uint64_t dA3 = smem_desc_sw128(sbase + L::OFF_A3, 8192, 1024);
-    const uint64_t dB3 = smem_desc_sw128(sbase + L::OFF_B3, 16, 1024);
 
     for (int c = 0; c < nch; ++c) {
       const int buf = c & 1;
@@ -895,21 +951,7 @@ __global__ void __launch_bounds__(kTcBlock, 1) gdr_scan_tc_kernel(
       if (!mbar_wait(&full_a[buf], use & 1, abort_flag)) failed = true;
       tc_fence_before();
       // B1 holds this chunk's state; the previous chunk's TMEM reads are done
-      if (bar_sync_or(1, kTcThreads, failed)) { failed = true; break; }
-      if (tid == 0) {  // D1 = [Y; gamma Q^] S^T
-        tc_fence_after();
-        const uint64_t a0 = dA1 + ((buf * L::A1_BYTES) >> 4);
-#pragma unroll
-        for (int kb = 0; kb < NKB; ++kb)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t acc = (kb | k) ? 1u : 0u;
-            const uint64_t bd = dB1 + ((kb * L::B1_KB + k * 32) >> 4);
-            umma_bf16(t_d1, a0 + ((kb * 16384 + k * 32) >> 4), bd, kIdK32, acc);
-            umma_bf16(t_d1 + 32, a0 + ((L::A1_SPLIT + kb * 16384 + k * 32) >> 4), bd, kIdK16, acc);
-          }
-        umma_commit(d1_done);
-      }
+      if (bar_sync_or(1, kTcSync, failed)) { failed = true; break; }
       // the state at the chunk start (overlaps the MMAs)
       if (Schk && own_col) {
 #pragma unroll
@@ -949,32 +991,7 @@ __global__ void __launch_bounds__(kTcBlock, 1) gdr_scan_tc_kernel(
       if (failed) *abort_flag = 1;
       fence_proxy_async_smem();
       tc_fence_before();
-      if (bar_sync_or(1, kTcThreads, failed)) { failed = true; break; }  // W, Wd complete
-      if (tid == 0) {
-        mbar_arrive(&empty_a[buf]);  // [Y; gamma Q^], the U slice and the decays are read
-        if (!mbar_wait(full_k, c & 1, abort_flag) || !mbar_wait(&full_p[buf], use & 1, abort_flag)) {
-          failed = true;
-          *abort_flag = 1;
-        } else {
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {  // D3 = K^T Wd
-            const uint64_t bd3 = dB3 + ((k * 32) >> 4);
-            umma_bf16(t_d3, dA3 + ((k * 2048) >> 4), bd3, kIdMN32, k ? 1u : 0u);
-            umma_bf16(t_d3 + 32, dA3 + ((L::A3_SPLIT + k * 2048) >> 4), bd3, kIdMN16, k ? 1u : 0u);
-          }
-          umma_commit(d3_done);
-          umma_commit(empty_k);
-          const uint64_t p0 = dP + ((buf * L::P_BYTES) >> 4);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {  // D1[64:128] += P W
-            const uint64_t bd2 = dB2 + ((k * 32) >> 4);
-            umma_bf16(t_d1, p0 + ((k * 32) >> 4), bd2, kIdK32, 1u);
-            umma_bf16(t_d1 + 32, p0 + ((L::P_SPLIT + k * 32) >> 4), bd2, kIdK16, 1u);
-          }
-          umma_commit(&empty_p[buf]);
-        }
-      }
+      if (bar_sync_or(1, kTcSync, failed)) { failed = true; break; }  // W, Wd complete
       if (!mbar_wait(d3_done, c & 1, abort_flag)) failed = true;
       failed = __any_sync(0xffffffffu, failed);
       tc_fence_after();
@@ -988,8 +1005,7 @@ __global__ void __launch_bounds__(kTcBlock, 1) gdr_scan_tc_kernel(
       if (failed) *abort_flag = 1;
       fence_proxy_async_smem();
     }
-    if (!failed) {  // the last chunk's output, once its P W completed
-      if (tid == 0) umma_commit(d1_done);
+    if (!failed) {  // the last chunk's output, once its P W completed (the MMA warp commits)
       if ((warp & 3) >= 2) {
         if (!mbar_wait(d1_done, nch & 1, abort_flag)) failed = true;
         failed = __any_sync(0xffffffffu, failed);
@@ -1128,6 +1144,91 @@ __global__ void __launch_bounds__(kTcBlock, 1) gdr_bwd_scan_tc_kernel(
       }
       if (failed) *abort_flag = 1;
     }
+  } else if (warp == kTcThreads / 32 + 1) {
+    // ------------------------------------------------------------ MMA warp (lane 0 issues)
+    const bool issuer = (tid & 31) == 0;
+    constexpr uint32_t kIdK32 = idesc_bf16_f32(128, 32, false, false);
+    constexpr uint32_t kIdK16 = idesc_bf16_f32(128, 16, false, false);
+    constexpr uint32_t kIdMN32 = idesc_bf16_f32(128, 32, true, false);
+    constexpr uint32_t kIdMN16 = idesc_bf16_f32(128, 16, true, false);
+    // descriptors of the tiles' first atoms; a tile further on adds its byte offset / 16
+    const uint64_t dE = smem_desc_sw128(sbase + L::OFF_E, 16, 1024);
+    const uint64_t dB1 = smem_desc_sw128(sbase + L::OFF_B1, 16, 1024);
+    const uint64_t dSP = smem_desc_sw128(sbase + L::OFF_X + L::X_SP, 8192, 1024);
+    const uint64_t dSQ = smem_desc_sw128(sbase + L::OFF_X + L::X_SQ, 8192, 1024);
+    const uint64_t dOT = smem_desc_sw128(sbase + L::OFF_X + L::X_OT, 16, 1024);
+    const uint64_t dY = smem_desc_sw128(sbase + L::OFF_Y, 8192, 1024);
+    const uint64_t dB2 = smem_desc_sw128(sbase + L::OFF_B2, 16, 1024);
+    // the products with dO of the k-th chunk met, into TMEM buffer k & 1
+    auto issue_do_products = [&](int k) {
+      const int xb = k & 1;
+      if (!mbar_wait(&full_x[xb], (k >> 1) & 1, abort_flag)) return false;
+      tc_fence_after();
+      const uint32_t ta = tmem + 128 * xb, tb = tmem + 256 + 128 * xb;
+      const uint32_t o = (xb * L::X_BYTES) >> 4;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t bo = dOT + o + ((kk * 32) >> 4);
+        const uint32_t acc = kk ? 1u : 0u;
+        umma_bf16(ta + 48, dSP + o + ((kk * 2048) >> 4), bo, kIdMN16, acc);
+        umma_bf16(ta + 64, dSP + o + ((L::SP_PIECE + kk * 2048) >> 4), bo, kIdMN16, acc);
+        umma_bf16(tb, dSQ + o + ((kk * 2048) >> 4), bo, kIdMN16, acc);
+        umma_bf16(tb + 16, dSQ + o + ((L::SQ_PIECE + kk * 2048) >> 4), bo, kIdMN16, acc);
+      }
+      umma_commit(&empty_x[xb]);
+      return true;
+    };
+    if (issuer && !issue_do_products(0)) {
+      failed = true;
+      *abort_flag = 1;
+    }
+    for (int k = 0; k < nch; ++k) {
+      const int buf = k & 1;
+      const uint32_t use = static_cast<uint32_t>(k >> 1);
+      const uint32_t t_a = tmem + 128 * buf, t_b = tmem + 256 + 128 * buf;
+      if (issuer && !mbar_wait(&full_e[buf], use & 1, abort_flag)) failed = true;
+      tc_fence_before();
+      if (bar_sync_or(1, kTcSync, failed)) { failed = true; break; }  // B1 of this chunk
+      if (issuer) {  // D_A += E dS^T
+        tc_fence_after();
+        const uint64_t e0 = dE + ((buf * L::E_BYTES) >> 4);
+#pragma unroll
+        for (int kb = 0; kb < NKB; ++kb)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acc = (kb | kk) ? 1u : 0u;
+            const uint64_t bd = dB1 + ((kb * L::B1_KB + kk * 32) >> 4);
+            umma_bf16(t_a, e0 + ((kb * 8192 + kk * 32) >> 4), bd, kIdK32, acc);
+            umma_bf16(t_a + 32, e0 + ((L::E_PIECE + kb * 8192 + kk * 32) >> 4), bd, kIdK16, acc);
+          }
+        umma_commit(a_done);
+        umma_commit(&empty_e[buf]);  // the consumers read the decays before the barrier above
+      }
+      tc_fence_before();
+      if (bar_sync_or(1, kTcSync, failed)) { failed = true; break; }  // -dW formed
+      if (issuer) {
+        if (!mbar_wait(full_y, k & 1, abort_flag)) {
+          failed = true;
+          *abort_flag = 1;
+        } else {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {  // D_B += Y^T (-dW)
+            const uint64_t bd = dB2 + ((kk * 32) >> 4);
+            const uint32_t acc = kk ? 1u : 0u;
+            umma_bf16(t_b + 32, dY + ((kk * 2048) >> 4), bd, kIdMN32, acc);
+            umma_bf16(t_b + 64, dY + ((L::Y_PIECE + kk * 2048) >> 4), bd, kIdMN16, acc);
+          }
+          umma_commit(b_done);
+          umma_commit(empty_y);
+          if (k + 1 < nch && !issue_do_products(k + 1)) {
+            failed = true;
+            *abort_flag = 1;
+          }
+        }
+      }
+    }
+    if (failed) *abort_flag = 1;
   } else {
     // ------------------------------------------------------------ consumer warps
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
@@ -1166,41 +1267,6 @@ __global__ void __launch_bounds__(kTcBlock, 1) gdr_bwd_scan_tc_kernel(
     };
     write_state_operand();
     fence_proxy_async_smem();
-    constexpr uint32_t kIdK32 = idesc_bf16_f32(128, 32, false, false);
-    constexpr uint32_t kIdK16 = idesc_bf16_f32(128, 16, false, false);
-    constexpr uint32_t kIdMN32 = idesc_bf16_f32(128, 32, true, false);
-    constexpr uint32_t kIdMN16 = idesc_bf16_f32(128, 16, true, false);
-    // descriptors of the tiles' first atoms; a tile further on adds its byte offset / 16
-    const uint64_t dE = smem_desc_sw128(sbase + L::OFF_E, 16, 1024);
-    const uint64_t dB1 = smem_desc_sw128(sbase + L::OFF_B1, 16, 1024);
-    const uint64_t dSP = smem_desc_sw128(sbase + L::OFF_X + L::X_SP, 8192, 1024);
-    const uint64_t dSQ = smem_desc_sw128(sbase + L::OFF_X + L::X_SQ, 8192, 1024);
-    const uint64_t dOT = smem_desc_sw128(sbase + L::OFF_X + L::X_OT, 16, 1024);
-    const uint64_t dY = smem_desc_sw128(sbase + L::OFF_Y, 8192, 1024);
-    const uint64_t dB2 = smem_desc_sw128(sbase + L::OFF_B2, 16, 1024);
-    // the products with dO of the k-th chunk met, into TMEM buffer k & 1 (thread 0)
-    auto issue_do_products = [&](int k) {
-      const int xb = k & 1;
-      if (!mbar_wait(&full_x[xb], (k >> 1) & 1, abort_flag)) return false;
-      tc_fence_after();
-      const uint32_t ta = tmem + 128 * xb, tb = tmem + 256 + 128 * xb;
-      const uint32_t o = (xb * L::X_BYTES) >> 4;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t bo = dOT + o + ((kk * 32) >> 4);
-        const uint32_t acc = kk ? 1u : 0u;
-        umma_bf16(ta + 48, dSP + o + ((kk * 2048) >> 4), bo, kIdMN16, acc);
-        umma_bf16(ta + 64, dSP + o + ((L::SP_PIECE + kk * 2048) >> 4), bo, kIdMN16, acc);
-        umma_bf16(tb, dSQ + o + ((kk * 2048) >> 4), bo, kIdMN16, acc);
-        umma_bf16(tb + 16, dSQ + o + ((L::SQ_PIECE + kk * 2048) >> 4), bo, kIdMN16, acc);
-      }
-      umma_commit(&empty_x[xb]);
-      return true;
-    };
-    if (tid == 0 && !issue_do_products(0)) {
-      failed = true;
-      *abort_flag = 1;
-    }
 
     for (int k = 0; k < nch; ++k) {
       const int c = nch - 1 - k, buf = k & 1;
@@ -1212,22 +1278,7 @@ __global__ void __launch_bounds__(kTcBlock, 1) gdr_bwd_scan_tc_kernel(
           : __expf(reinterpret_cast<const float*>(smem + L::OFF_G + buf * L::G_BYTES)[kC - 1]);
       tc_fence_before();
       // B1 holds this chunk's state gradient; the previous chunk's TMEM reads are done
-      if (bar_sync_or(1, kTcThreads, failed)) { failed = true; break; }
-      if (tid == 0) {  // D_A += E dS^T
-        tc_fence_after();
-        const uint64_t e0 = dE + ((buf * L::E_BYTES) >> 4);
-#pragma unroll
-        for (int kb = 0; kb < NKB; ++kb)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t acc = (kb | kk) ? 1u : 0u;
-            const uint64_t bd = dB1 + ((kb * L::B1_KB + kk * 32) >> 4);
-            umma_bf16(t_a, e0 + ((kb * 8192 + kk * 32) >> 4), bd, kIdK32, acc);
-            umma_bf16(t_a + 32, e0 + ((L::E_PIECE + kb * 8192 + kk * 32) >> 4), bd, kIdK16, acc);
-          }
-        umma_commit(a_done);
-        umma_commit(&empty_e[buf]);  // the decays were read before the barrier above
-      }
+      if (bar_sync_or(1, kTcSync, failed)) { failed = true; break; }
       // the state gradient at the chunk's end (overlaps the MMAs)
       if (own_col) {
 #pragma unroll
@@ -1254,28 +1305,7 @@ __global__ void __launch_bounds__(kTcBlock, 1) gdr_bwd_scan_tc_kernel(
       if (failed) *abort_flag = 1;
       fence_proxy_async_smem();
       tc_fence_before();
-      if (bar_sync_or(1, kTcThreads, failed)) { failed = true; break; }  // -dW complete
-      if (tid == 0) {
-        if (!mbar_wait(full_y, k & 1, abort_flag)) {
-          failed = true;
-          *abort_flag = 1;
-        } else {
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {  // D_B += Y^T (-dW)
-            const uint64_t bd = dB2 + ((kk * 32) >> 4);
-            const uint32_t acc = kk ? 1u : 0u;
-            umma_bf16(t_b + 32, dY + ((kk * 2048) >> 4), bd, kIdMN32, acc);
-            umma_bf16(t_b + 64, dY + ((L::Y_PIECE + kk * 2048) >> 4), bd, kIdMN16, acc);
-          }
-          umma_commit(b_done);
-          umma_commit(empty_y);
-          if (k + 1 < nch && !issue_do_products(k + 1)) {
-            failed = true;
-            *abort_flag = 1;
-          }
-        }
-      }
+      if (bar_sync_or(1, kTcSync, failed)) { failed = true; break; }  // -dW complete
       if (!mbar_wait(b_done, k & 1, abort_flag)) failed = true;
       failed = __any_sync(0xffffffffu, failed);
       tc_fence_after();
@@ -1829,15 +1859,29 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
                  },
                  [&](int j, int n) { return ld4(sK + j * LK + n); }, dka);
   __syncthreads();
-  // (10) dg = reverse cumulative sum of dG within the chunk; dbeta out
-  if (tid == 0) {
-    float run = 0.f;
-    for (int i = kC - 1; i >= 0; --i) {
-      run += sdG[i];
-      if (t0 + i < T) {
-        dg[row(i)] = run;
-        dbeta[row(i)] = sdB[i];
+  // (10) dg = reverse cumulative sum of dG within the chunk (warp 0: lane l holds rows l and
+  // 32 + l; suffix sums by shuffles in a fixed order, the upper half's total added to the
+  // lower half); dbeta out
+  if (tid < 32) {
+    const int l = tid;
+    float lo = sdG[l], hi = sdG[32 + l];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float a = __shfl_down_sync(0xffffffffu, lo, o);
+      const float c2 = __shfl_down_sync(0xffffffffu, hi, o);
+      if (l + o < 32) {
+        lo += a;
+        hi += c2;
       }
+    }
+    lo += __shfl_sync(0xffffffffu, hi, 0);
+    if (t0 + l < T) {
+      dg[row(l)] = lo;
+      dbeta[row(l)] = sdB[l];
+    }
+    if (t0 + 32 + l < T) {
+      dg[row(32 + l)] = hi;
+      dbeta[row(32 + l)] = sdB[32 + l];
     }
   }
   // L2 normalisations: dx = (dx^ - x^ (x^ . dx^)) / ||x||, over the 16 lanes owning a row
