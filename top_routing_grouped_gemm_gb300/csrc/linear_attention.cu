@@ -279,6 +279,7 @@ struct TcChunk {
 // fp32 pipes.
 struct GdrBwdImages {
   __nv_bfloat16 *sP, *sQ, *E, *Y, *OT;
+  float* KK;  // K^ K^T of the chunk, fp32 [64][64] (the tensor-core product, before masking)
   const __nv_bfloat16* dO;
   float scale;
 };
@@ -501,6 +502,12 @@ __global__ void __launch_bounds__(256, 2) gdr_chunk_kernel(
     if (row < kC) {
       const int i = row;
       const float gi = sG[i], bi = sB[i];
+      if constexpr (BIMG) {  // K^ K^T as it is, for the chunk-local backward
+        float4* kko = reinterpret_cast<float4*>(img.KK + chunk_id * kC * kC + i * kC + j0);
+#pragma unroll
+        for (int p4 = 0; p4 < 8; ++p4)
+          kko[p4] = make_float4(d[4 * p4], d[4 * p4 + 1], d[4 * p4 + 2], d[4 * p4 + 3]);
+      }
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = j0 + jj;
@@ -1573,7 +1580,7 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
     const float* __restrict__ Kh, const float* __restrict__ Y, const float* __restrict__ U,
     const float* __restrict__ Pm, const float* __restrict__ Gc, const float* __restrict__ Ai,
     const float* __restrict__ Schk, const float* __restrict__ dSchk,
-    const float* __restrict__ dWg, int T, int H, int nch, float scale,
+    const float* __restrict__ dWg, const float* __restrict__ KKg, int T, int H, int nch, float scale,
     float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
     float* __restrict__ dbeta, float* __restrict__ dg) {
   using L = BwdLd<DK, DV>;
@@ -1814,13 +1821,14 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
   {
     float acc[RU][CC], kk[RU][CC];
     mm_zero<kC, kC>(acc);
-    mm_zero<kC, kC>(kk);
     mm_nn_staged<kC, kC, true>(DV, [&](int m, int r) { return sX[m * LX + r]; }, cU, DV, sStg,
                                acc);
     mm_nn_staged<kC, kC, true>(DK, [&](int m, int x) { return sW[m * LX + x]; }, cY, DK, sStg,
                                acc);
-    mm_nt4<kC, kC>(DK, [&](int m) { return sK + m * LK; }, [&](int n) { return sK + n * LK; },
-                   kk);
+#pragma unroll
+    for (int u = 0; u < RU; ++u)  // K^ K^T from the factor kernel's tensor-core product
+#pragma unroll
+      for (int cc = 0; cc < CC; ++cc) kk[u][cc] = __ldg(&KKg[cid * kC * kC + (ti + 16 * u) * kC + tj + 16 * cc]);
 #pragma unroll
     for (int u = 0; u < RU; ++u)
 #pragma unroll
@@ -1973,7 +1981,8 @@ size_t gdr_bwd_ws(int B, int T, int H, int dk, int dv) {
   const size_t nch = (T + kC - 1) / kC;
   const size_t chunks = static_cast<size_t>(B) * H * nch;
   return gdr_ws(B, T, H, dk, dv) + up256(chunks * kC * kC * 4) + up256(chunks * kC * dv * 4) +
-         up256(chunks * static_cast<size_t>(dv) * dk * 4) + up256(chunks * gdr_bwd_img_bytes(dk, dv));
+         up256(chunks * static_cast<size_t>(dv) * dk * 4) + up256(chunks * gdr_bwd_img_bytes(dk, dv)) +
+         up256(chunks * kC * kC * 4);
 }
 
 template <int DK, int DV>
@@ -1996,11 +2005,14 @@ int gdr_bwd_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloa
   float* dSw = reinterpret_cast<float*>(w); w += up256(chunks * static_cast<size_t>(DV) * DK * 4);
   using LB = TcBwd<DK>;
   GdrBwdImages img;
+  uint8_t* const img_base = w;
   img.sP = reinterpret_cast<__nv_bfloat16*>(w); w += chunks * 2 * LB::SP_PIECE;
   img.sQ = reinterpret_cast<__nv_bfloat16*>(w); w += chunks * 2 * LB::SQ_PIECE;
   img.E = reinterpret_cast<__nv_bfloat16*>(w); w += chunks * 2 * LB::E_PIECE;
   img.Y = reinterpret_cast<__nv_bfloat16*>(w); w += chunks * 2 * LB::Y_PIECE;
   img.OT = reinterpret_cast<__nv_bfloat16*>(w);
+  w = img_base + up256(chunks * gdr_bwd_img_bytes(DK, DV));
+  img.KK = reinterpret_cast<float*>(w);
   img.dO = dO;
   img.scale = scale;
   constexpr size_t sm1 = TcChunk<DK, DV>::SMEM;
@@ -2026,7 +2038,7 @@ int gdr_bwd_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloa
   if (e != cudaSuccess) return static_cast<int>(e);
   mark_before(MOE_KERNEL_GDR_BWD, s);
   k3<<<dim3(nch, H, B), 256, sm3, s>>>(q, k, v, beta, dO, Qh, Kh, Yw, Uw, Pw, Gw, Aw, Schk, dSw,
-                                       dWw, T, H, nch, scale, dq, dk, dv, dbeta, dg);
+                                       dWw, img.KK, T, H, nch, scale, dq, dk, dv, dbeta, dg);
   mark_after(MOE_KERNEL_GDR_BWD, s);
   return static_cast<int>(cudaGetLastError());
 }
