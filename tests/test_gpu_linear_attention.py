@@ -117,6 +117,7 @@ def run_gdr_bwd(cfg, inp, d_o, dST):
                          dk ** -0.5, d_o.cuda(), None if dST is None else dST.cuda(), Sc,
                          out["dq"], out["dk"], out["dv"], out["dbeta"], out["dg"], out["dS0"], ws)
     torch.cuda.synchronize()
+    assert moe.moe_gdr_device_status() == moe.MOE_OK
     return out
 
 
