@@ -1,4 +1,5 @@
-// Chunked gated delta-rule linear attention, forward (declared in include/linear_attention.h).
+// Chunked gated delta-rule linear attention, forward and backward (declared in
+// include/linear_attention.h).
 //
 // "Fine-Tuning Trillion-Parameter Sparse MoE Models: Challenges and Engineering Practices",
 // section 5: normalization coefficients, gating and decay, intra-chunk query-state
@@ -20,8 +21,9 @@
 // since each value row of the state evolves on its own (row r of S_t only involves v_t[r]),
 // the scan is split over slices of RS value rows (gdr_scan_tc_kernel), so a few heads still
 // fill the GPU.  Everything after the bf16 inputs is fp32 (the state in particular); the
-// forward scan's products run on the tensor cores with each fp32 operand carried as two bf16
-// pieces and fp32 accumulation.
+// dense products of the chunk factors and of both scans run on the tensor cores with each
+// fp32 operand carried as two bf16 pieces and fp32 accumulation, the masks, decays, the
+// triangular inverse and the chunk-local backward on the fp32 pipes.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -1566,8 +1568,9 @@ constexpr size_t bwd_chunk_smem_bytes() {
           16 * L::X) * sizeof(float);
 }
 
-// Per-chunk backward (grid: chunks x H x B): everything local to the chunk once dW and the
-// state gradient at its end are known.  dq^ and dk^ stay in registers (rows ti + 16 u,
+// Per-chunk backward (grid: chunks x H x B, fp32 pipes): everything local to the chunk once
+// dW and the state gradient at its end are known (K^ K^T comes from the factor kernel's
+// tensor-core product).  dq^ and dk^ stay in registers (rows ti + 16 u,
 // columns tj + 16 c of the thread) until the L2 normalisations are back-propagated and they
 // are written once; every other result goes through shared memory.  Row reductions (the
 // log-decay and beta gradients) are summed over the 16 lanes that own a row, in a fixed
