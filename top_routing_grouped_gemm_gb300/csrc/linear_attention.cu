@@ -442,22 +442,26 @@ __global__ void __launch_bounds__(256, 2) gdr_chunk_kernel(
       }
     }
   }
-  if constexpr (BIMG) {  // dO^T of every 16-row value slice (2-byte image stores)
+  if constexpr (BIMG) {  // dO^T of every 16-row value slice: each thread gathers 8 tokens of
+    // one value column (2-byte loads, the tile's rows shared through L1) into one 16-byte piece
     using LB = TcBwd<DK>;
-    constexpr int PPR = DV / 8;
-    for (int e = tid; e < kC * PPR; e += 256) {
-      const int t = e / PPR, pc = e - t * PPR;
-      const int tt = t0 + t;
-      const uint4 raw = tt < T ? *reinterpret_cast<const uint4*>(
-                                     img.dO + ((static_cast<size_t>(b) * T + tt) * H + h) * DV + pc * 8)
-                               : make_uint4(0u, 0u, 0u, 0u);
-      const __nv_bfloat16* vals = reinterpret_cast<const __nv_bfloat16*>(&raw);
+    for (int e = tid; e < DV * (kC / 8); e += 256) {
+      const int col = e % DV, tb = 8 * (e / DV);  // consecutive threads: consecutive columns
+      uint32_t w[4];
 #pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
-        const int col = pc * 8 + q8;
-        img.OT[(chunk_id * (DV / kRS) + col / kRS) * (LB::OT_BYTES / 2) + LB::ot(col % kRS, t)] =
-            vals[q8];
+      for (int u = 0; u < 4; ++u) {
+        __nv_bfloat16 p2[2];
+#pragma unroll
+        for (int v2 = 0; v2 < 2; ++v2) {
+          const int tt = t0 + tb + 2 * u + v2;
+          p2[v2] = tt < T ? img.dO[((static_cast<size_t>(b) * T + tt) * H + h) * DV + col]
+                          : __float2bfloat16_rn(0.f);
+        }
+        w[u] = static_cast<uint32_t>(__bfloat16_as_ushort(p2[0])) |
+               (static_cast<uint32_t>(__bfloat16_as_ushort(p2[1])) << 16);
       }
+      *reinterpret_cast<uint4*>(img.OT + (chunk_id * (DV / kRS) + col / kRS) * (LB::OT_BYTES / 2) +
+                                LB::ot(col % kRS, tb)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
   fence_proxy_async_smem();
