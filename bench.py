@@ -639,6 +639,7 @@ def run_linear_attention(name, ctx):
     gen.manual_seed(1000 + ctx.rank)
     d_o = torch.randn((B, T, H, dv), generator=gen, device="cuda").to(torch.bfloat16)
     Schk = torch.empty((B, H, nch, dv, dk), dtype=torch.float32, device="cuda")
+    Wchk = torch.empty((B, H, nch, 64, dv), dtype=torch.float32, device="cuda")
     dq = torch.empty((B, T, H, dk), dtype=torch.float32, device="cuda")
     dkk = torch.empty_like(dq)
     dvv = torch.empty((B, T, H, dv), dtype=torch.float32, device="cuda")
@@ -650,10 +651,10 @@ def run_linear_attention(name, ctx):
 
     def train_step():
         moe.moe_gdr_forward(B, T, H, dk, dv, inp["q"], inp["k"], inp["v"], inp["beta"],
-                            inp["g"], inp["S0"], dk ** -0.5, o, ST, Schk, ws)
+                            inp["g"], inp["S0"], dk ** -0.5, o, ST, Schk, ws, W_chunks=Wchk)
         moe.moe_gdr_backward(B, T, H, dk, dv, inp["q"], inp["k"], inp["v"], inp["beta"],
                              inp["g"], dk ** -0.5, d_o, None, Schk, dq, dkk, dvv, dbeta, dg, dS0,
-                             ws_b)
+                             ws_b, W_chunks=Wchk)
     for _ in range(max(args.warmup, 3)):
         train_step()
     torch.cuda.synchronize()

@@ -20,10 +20,13 @@
  *   g <= 0 the log decay);  S0 [B, H, dv, dk] fp32 initial state or NULL (zero);
  *   o [B, T, H, dv] bf16;  S_T [B, H, dv, dk] fp32 final state or NULL;
  *   S_chunks [B, H, ceil(T/64), dv, dk] fp32 or NULL: the state at the start of every
- *   64-token chunk (what a backward pass restarts from).
+ *   64-token chunk (what a backward pass restarts from);  W_chunks [B, H, ceil(T/64), 64, dv]
+ *   fp32 or NULL: every chunk's W = U - Y S0^T (its tokens' values corrected by the state at
+ *   the chunk start; rows past the sequence zero), which the backward then reads instead of
+ *   forming it again.
  * Supported: dk and dv in {64, 128}; any T >= 1 (the last chunk may be partial).  A zero
  * q or k row is treated as a zero vector (no division by zero).  q, k, v, the workspace, the
- * forward's o (and the backward's d_o and S_chunks) must be 16-byte aligned (the kernels move
+ * forward's o, W_chunks (and the backward's d_o, S_chunks, W_chunks) must be 16-byte aligned (the kernels move
  * them in 16-byte pieces), else MOE_ERR_UNSUPPORTED.
  *
  * Precision: the state and every accumulation are fp32.  The forward scan's products run on
@@ -54,7 +57,8 @@ size_t moe_gdr_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk, int32
 int moe_gdr_forward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, const moe_bf16* q,
                     const moe_bf16* k, const moe_bf16* v, const float* beta, const float* g,
                     const float* S0, float scale, moe_bf16* o, float* S_T, float* S_chunks,
-                    void* workspace, size_t workspace_bytes, moe_stream_t stream);
+                    float* W_chunks, void* workspace, size_t workspace_bytes,
+                    moe_stream_t stream);
 
 /* Device-side status of the linear-attention kernels: waits for `stream`, writes the first
  * error a kernel recorded since the previous call (MOE_OK if none; MOE_ERR_TIMEOUT when a
@@ -68,7 +72,8 @@ int moe_gdr_device_status(int32_t* status, moe_stream_t stream);
  * gradient in slices of 16 value rows on the tensor cores (bounded waits as in the forward,
  * reported through moe_gdr_device_status), then every chunk's local backward in
  * parallel).
- * S_chunks: the forward's chunk-start states (required).  d_o [B, T, H, dv] bf16; dS_T
+ * S_chunks: the forward's chunk-start states (required); W_chunks: the forward's W_chunks, or
+ * NULL (then formed again from S_chunks).  d_o [B, T, H, dv] bf16; dS_T
  * [B, H, dv, dk] fp32 or NULL (zero).  Outputs fp32, overwritten: dq, d_k [B, T, H, dk],
  * d_v [B, T, H, dv], dbeta, dg [B, T, H], dS0 [B, H, dv, dk] (may be NULL).  Deterministic:
  * every reduction runs in a fixed order. */
@@ -77,6 +82,7 @@ size_t moe_gdr_backward_workspace_size(int32_t B, int32_t T, int32_t H, int32_t 
 int moe_gdr_backward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, const moe_bf16* q,
                      const moe_bf16* k, const moe_bf16* v, const float* beta, const float* g,
                      float scale, const moe_bf16* d_o, const float* dS_T, const float* S_chunks,
+                     const float* W_chunks,
                      float* dq, float* d_k, float* d_v, float* dbeta, float* dg, float* dS0,
                      void* workspace, size_t workspace_bytes, moe_stream_t stream);
 

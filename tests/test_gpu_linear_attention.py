@@ -17,18 +17,21 @@ RTOL_O = 5e-3      # o is rounded once to bf16
 RTOL_S = 1e-4      # the fp32 state (the scan's products: two bf16 pieces per fp32 operand)
 
 
-def run_gdr(cfg, inp, checkpoints=False):
+def run_gdr(cfg, inp, checkpoints=False, keep_w=False):
     B, T, H, dk, dv = cfg.B, cfg.T, cfg.H, cfg.dk, cfg.dv
     dev = {n: (None if t is None else t.cuda()) for n, t in inp.items()}
     o = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device="cuda")
     ST = torch.empty((B, H, dv, dk), dtype=torch.float32, device="cuda")
     nch = (T + 63) // 64
     Sc = torch.empty((B, H, nch, dv, dk), dtype=torch.float32, device="cuda") if checkpoints else None
+    Wc = torch.empty((B, H, nch, 64, dv), dtype=torch.float32, device="cuda") if keep_w else None
     ws = torch.empty(moe.moe_gdr_workspace_size(B, T, H, dk, dv), dtype=torch.uint8, device="cuda")
     moe.moe_gdr_forward(B, T, H, dk, dv, dev["q"], dev["k"], dev["v"], dev["beta"], dev["g"],
-                        dev["S0"], dk ** -0.5, o, ST, Sc, ws)
+                        dev["S0"], dk ** -0.5, o, ST, Sc, ws, W_chunks=Wc)
     torch.cuda.synchronize()
     assert moe.moe_gdr_device_status() == moe.MOE_OK
+    if keep_w:
+        return o, ST, Sc, Wc
     return o, ST, Sc
 
 
@@ -101,9 +104,13 @@ def test_gdr_long_sequence_sampled_heads():
 RTOL_G = 5e-3
 
 
-def run_gdr_bwd(cfg, inp, d_o, dST):
+def run_gdr_bwd(cfg, inp, d_o, dST, keep_w=False):
     B, T, H, dk, dv = cfg.B, cfg.T, cfg.H, cfg.dk, cfg.dv
-    _, _, Sc = run_gdr(cfg, inp, checkpoints=True)
+    Wc = None
+    if keep_w:
+        _, _, Sc, Wc = run_gdr(cfg, inp, checkpoints=True, keep_w=True)
+    else:
+        _, _, Sc = run_gdr(cfg, inp, checkpoints=True)
     dev = {n: (None if t is None else t.cuda()) for n, t in inp.items()}
     out = {"dq": torch.empty((B, T, H, dk), device="cuda"),
            "dk": torch.empty((B, T, H, dk), device="cuda"),
@@ -115,7 +122,8 @@ def run_gdr_bwd(cfg, inp, d_o, dST):
                      device="cuda")
     moe.moe_gdr_backward(B, T, H, dk, dv, dev["q"], dev["k"], dev["v"], dev["beta"], dev["g"],
                          dk ** -0.5, d_o.cuda(), None if dST is None else dST.cuda(), Sc,
-                         out["dq"], out["dk"], out["dv"], out["dbeta"], out["dg"], out["dS0"], ws)
+                         out["dq"], out["dk"], out["dv"], out["dbeta"], out["dg"], out["dS0"], ws,
+                         W_chunks=Wc)
     torch.cuda.synchronize()
     assert moe.moe_gdr_device_status() == moe.MOE_OK
     return out
@@ -144,6 +152,23 @@ def test_gdr_backward_whole(cfg, with_dST):
                                        dS_T=f64(dST), S0=f64(inp["S0"]))
     for name in ("dq", "dk", "dv", "dbeta", "dg", "dS0"):
         assert relerr(f64(got[name]), ref[name]) <= RTOL_G, name
+
+
+@pytest.mark.parametrize("cfg", [BWD_CASES[0], BWD_CASES[3]], ids=["dk128_dv128", "dk64_dv64"])
+def test_gdr_backward_with_forward_w(cfg):
+    """The backward reading the forward's W_chunks (formed by the tensor-core scan) matches the
+    oracle and the backward that forms W itself."""
+    inp = synth.make_la_inputs(cfg)
+    gen = torch.Generator().manual_seed(5)
+    d_o = torch.randn((cfg.B, cfg.T, cfg.H, cfg.dv), generator=gen).to(torch.bfloat16)
+    got = run_gdr_bwd(cfg, inp, d_o, None, keep_w=True)
+    own = run_gdr_bwd(cfg, inp, d_o, None)
+    ref = LA.gated_delta_rule_backward(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]),
+                                       f64(inp["beta"]), f64(inp["g"]), f64(d_o),
+                                       S0=f64(inp["S0"]))
+    for name in ("dq", "dk", "dv", "dbeta", "dg", "dS0"):
+        assert relerr(f64(got[name]), ref[name]) <= RTOL_G, name
+        assert relerr(f64(got[name]), f64(own[name])) <= 1e-3, name
 
 
 def test_gdr_backward_is_deterministic():

@@ -775,7 +775,7 @@ __global__ void __launch_bounds__(kTcBlock, 1) gdr_scan_tc_kernel(
     const __nv_bfloat16* __restrict__ Ps, const float* __restrict__ Us,
     const float* __restrict__ Gc, const float* __restrict__ S0, int T, int H, int nch,
     float scale, __nv_bfloat16* __restrict__ o, float* __restrict__ ST,
-    float* __restrict__ Schk) {
+    float* __restrict__ Schk, float* __restrict__ Wout) {
   using L = TcScan<DK>;
   constexpr int NKB = L::NKB;
   extern __shared__ uint8_t tc_smem_raw[];
@@ -985,6 +985,9 @@ __global__ void __launch_bounds__(kTcBlock, 1) gdr_scan_tc_kernel(
               reinterpret_cast<const float*>(smem + L::OFF_U + buf * L::U_BYTES) + j * kRS + n0);
           const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
           const float dec = __expf(gC - sg[j]);
+          if (Wout)  // W for the backward
+            *reinterpret_cast<float4*>(Wout + (cid * kC + j) * DV + r0 + n0) =
+                make_float4(uu[0] - d[0], uu[1] - d[1], uu[2] - d[2], uu[3] - d[3]);
 #pragma unroll
           for (int n = 0; n < kTcCols; ++n) {
             const float w = uu[n] - d[n];
@@ -1587,7 +1590,8 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
     const float* __restrict__ Kh, const float* __restrict__ Y, const float* __restrict__ U,
     const float* __restrict__ Pm, const float* __restrict__ Gc, const float* __restrict__ Ai,
     const float* __restrict__ Schk, const float* __restrict__ dSchk,
-    const float* __restrict__ dWg, const float* __restrict__ KKg, int T, int H, int nch, float scale,
+    const float* __restrict__ dWg, const float* __restrict__ KKg, const float* __restrict__ Wg,
+    int T, int H, int nch, float scale,
     float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
     float* __restrict__ dbeta, float* __restrict__ dg) {
   using L = BwdLd<DK, DV>;
@@ -1664,8 +1668,13 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
   }
   __syncthreads();
   const float gl = sG[kC - 1];
-  // (1) W = U - Y S0^T  -> sW
-  {
+  // (1) W = U - Y S0^T  -> sW (the forward's W when it kept it)
+  if (Wg) {
+    for (int e = tid; e < kC * DV / 4; e += 256) {
+      const int i = e / (DV / 4), r = 4 * (e - i * (DV / 4));
+      *reinterpret_cast<float4*>(sW + i * LX + r) = ldg4(Wg + cid * kC * DV + 4 * e);
+    }
+  } else {
     float acc[RU][CV];
     mm_zero<kC, DV>(acc);
     mm_nn4_staged<kC, DV, true>(DK, [&](int m, int x) { return ldg4(cY + m * DK + x); }, S0, DK,
@@ -1942,7 +1951,7 @@ size_t gdr_ws(int B, int T, int H, int dk, int dv) {
 template <int DK, int DV>
 int gdr_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloat16* k,
                const __nv_bfloat16* v, const float* beta, const float* g, const float* S0,
-               float scale, __nv_bfloat16* o, float* ST, float* Schk, void* ws,
+               float scale, __nv_bfloat16* o, float* ST, float* Schk, float* Wch, void* ws,
                cudaStream_t s) {
   const int nch = (T + kC - 1) / kC;
   const size_t chunks = static_cast<size_t>(B) * H * nch;
@@ -1973,7 +1982,7 @@ int gdr_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloat16*
   if (e != cudaSuccess) return static_cast<int>(e);
   mark_before(MOE_KERNEL_GDR_SCAN, s);
   k2<<<dim3(DV / kRS, H, B), kTcBlock, sm2, s>>>(YQs, Ks, Ps, Uw, Gw, S0, T, H, nch, scale, o,
-                                                   ST, Schk);  // Uw: slice-major U
+                                                   ST, Schk, Wch);  // Uw: slice-major U
   mark_after(MOE_KERNEL_GDR_SCAN, s);
   return static_cast<int>(cudaGetLastError());
 }
@@ -1995,7 +2004,8 @@ size_t gdr_bwd_ws(int B, int T, int H, int dk, int dv) {
 template <int DK, int DV>
 int gdr_bwd_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloat16* k,
                    const __nv_bfloat16* v, const float* beta, const float* g, float scale,
-                   const __nv_bfloat16* dO, const float* dST, const float* Schk, float* dq,
+                   const __nv_bfloat16* dO, const float* dST, const float* Schk, const float* Wch,
+                   float* dq,
                    float* dk, float* dv, float* dbeta, float* dg, float* dS0, void* ws,
                    cudaStream_t s) {
   const int nch = (T + kC - 1) / kC;
@@ -2045,7 +2055,7 @@ int gdr_bwd_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloa
   if (e != cudaSuccess) return static_cast<int>(e);
   mark_before(MOE_KERNEL_GDR_BWD, s);
   k3<<<dim3(nch, H, B), 256, sm3, s>>>(q, k, v, beta, dO, Qh, Kh, Yw, Uw, Pw, Gw, Aw, Schk, dSw,
-                                       dWw, img.KK, T, H, nch, scale, dq, dk, dv, dbeta, dg);
+                                       dWw, img.KK, Wch, T, H, nch, scale, dq, dk, dv, dbeta, dg);
   mark_after(MOE_KERNEL_GDR_BWD, s);
   return static_cast<int>(cudaGetLastError());
 }
@@ -2066,7 +2076,8 @@ size_t moe_gdr_workspace_size(int32_t B, int32_t T, int32_t H, int32_t dk, int32
 int moe_gdr_forward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, const moe_bf16* q,
                     const moe_bf16* k, const moe_bf16* v, const float* beta, const float* g,
                     const float* S0, float scale, moe_bf16* o, float* S_T, float* S_chunks,
-                    void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+                    float* W_chunks, void* workspace, size_t workspace_bytes,
+                    moe_stream_t stream) {
   if (B <= 0 || T <= 0 || H <= 0 || !q || !k || !v || !beta || !g || !o)
     return MOE_ERR_INVALID_ARG;
   if (!((dk == 64 || dk == 128) && (dv == 64 || dv == 128))) return MOE_ERR_UNSUPPORTED;
@@ -2074,7 +2085,7 @@ int moe_gdr_forward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, con
   if (!workspace || workspace_bytes < gdr_ws(B, T, H, dk, dv)) return MOE_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(q) |
        reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
-       reinterpret_cast<uintptr_t>(o)) & 15u)
+       reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(W_chunks)) & 15u)
     return MOE_ERR_UNSUPPORTED;
   const auto* q_ = reinterpret_cast<const __nv_bfloat16*>(q);
   const auto* k_ = reinterpret_cast<const __nv_bfloat16*>(k);
@@ -2082,13 +2093,13 @@ int moe_gdr_forward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, con
   auto* o_ = reinterpret_cast<__nv_bfloat16*>(o);
   int e;
   if (dk == 128 && dv == 128)
-    e = gdr_launch<128, 128>(B, T, H, q_, k_, v_, beta, g, S0, scale, o_, S_T, S_chunks, workspace, stream);
+    e = gdr_launch<128, 128>(B, T, H, q_, k_, v_, beta, g, S0, scale, o_, S_T, S_chunks, W_chunks, workspace, stream);
   else if (dk == 128)
-    e = gdr_launch<128, 64>(B, T, H, q_, k_, v_, beta, g, S0, scale, o_, S_T, S_chunks, workspace, stream);
+    e = gdr_launch<128, 64>(B, T, H, q_, k_, v_, beta, g, S0, scale, o_, S_T, S_chunks, W_chunks, workspace, stream);
   else if (dv == 128)
-    e = gdr_launch<64, 128>(B, T, H, q_, k_, v_, beta, g, S0, scale, o_, S_T, S_chunks, workspace, stream);
+    e = gdr_launch<64, 128>(B, T, H, q_, k_, v_, beta, g, S0, scale, o_, S_T, S_chunks, W_chunks, workspace, stream);
   else
-    e = gdr_launch<64, 64>(B, T, H, q_, k_, v_, beta, g, S0, scale, o_, S_T, S_chunks, workspace, stream);
+    e = gdr_launch<64, 64>(B, T, H, q_, k_, v_, beta, g, S0, scale, o_, S_T, S_chunks, W_chunks, workspace, stream);
   count_launches(2);
   return e == 0 ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -2114,7 +2125,8 @@ size_t moe_gdr_backward_workspace_size(int32_t B, int32_t T, int32_t H, int32_t 
 int moe_gdr_backward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, const moe_bf16* q,
                      const moe_bf16* k, const moe_bf16* v, const float* beta, const float* g,
                      float scale, const moe_bf16* d_o, const float* dS_T, const float* S_chunks,
-                     float* dq, float* dk_out, float* dv_out, float* dbeta, float* dg,
+                     const float* W_chunks, float* dq, float* dk_out, float* dv_out, float* dbeta,
+                     float* dg,
                      float* dS0, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
   if (B <= 0 || T <= 0 || H <= 0 || !q || !k || !v || !beta || !g || !d_o || !S_chunks || !dq ||
       !dk_out || !dv_out || !dbeta || !dg)
@@ -2124,7 +2136,8 @@ int moe_gdr_backward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, co
   if (!workspace || workspace_bytes < gdr_bwd_ws(B, T, H, dk, dv)) return MOE_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(d_o) |
        reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(S_chunks)) & 15u)
+       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(S_chunks) |
+       reinterpret_cast<uintptr_t>(W_chunks)) & 15u)
     return MOE_ERR_UNSUPPORTED;
   const auto* q_ = reinterpret_cast<const __nv_bfloat16*>(q);
   const auto* k_ = reinterpret_cast<const __nv_bfloat16*>(k);
@@ -2132,13 +2145,13 @@ int moe_gdr_backward(int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, co
   const auto* o_ = reinterpret_cast<const __nv_bfloat16*>(d_o);
   int e;
   if (dk == 128 && dv == 128)
-    e = gdr_bwd_launch<128, 128>(B, T, H, q_, k_, v_, beta, g, scale, o_, dS_T, S_chunks, dq, dk_out, dv_out, dbeta, dg, dS0, workspace, stream);
+    e = gdr_bwd_launch<128, 128>(B, T, H, q_, k_, v_, beta, g, scale, o_, dS_T, S_chunks, W_chunks, dq, dk_out, dv_out, dbeta, dg, dS0, workspace, stream);
   else if (dk == 128)
-    e = gdr_bwd_launch<128, 64>(B, T, H, q_, k_, v_, beta, g, scale, o_, dS_T, S_chunks, dq, dk_out, dv_out, dbeta, dg, dS0, workspace, stream);
+    e = gdr_bwd_launch<128, 64>(B, T, H, q_, k_, v_, beta, g, scale, o_, dS_T, S_chunks, W_chunks, dq, dk_out, dv_out, dbeta, dg, dS0, workspace, stream);
   else if (dv == 128)
-    e = gdr_bwd_launch<64, 128>(B, T, H, q_, k_, v_, beta, g, scale, o_, dS_T, S_chunks, dq, dk_out, dv_out, dbeta, dg, dS0, workspace, stream);
+    e = gdr_bwd_launch<64, 128>(B, T, H, q_, k_, v_, beta, g, scale, o_, dS_T, S_chunks, W_chunks, dq, dk_out, dv_out, dbeta, dg, dS0, workspace, stream);
   else
-    e = gdr_bwd_launch<64, 64>(B, T, H, q_, k_, v_, beta, g, scale, o_, dS_T, S_chunks, dq, dk_out, dv_out, dbeta, dg, dS0, workspace, stream);
+    e = gdr_bwd_launch<64, 64>(B, T, H, q_, k_, v_, beta, g, scale, o_, dS_T, S_chunks, W_chunks, dq, dk_out, dv_out, dbeta, dg, dS0, workspace, stream);
   count_launches(3);
   return e == 0 ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -103,13 +103,13 @@ _SIGS = {
     "moe_route_bwd": (ctypes.c_int, [_P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "moe_gdr_workspace_size": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
     "moe_gdr_forward": (ctypes.c_int, [c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp,
-                                       c_vp, c_vp, ctypes.c_float, c_vp, c_vp, c_vp, c_vp, c_sz,
-                                       c_vp]),
+                                       c_vp, c_vp, ctypes.c_float, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                       c_sz, c_vp]),
     "moe_gdr_device_status": (ctypes.c_int, [ctypes.POINTER(c_i32), c_vp]),
     "moe_gdr_backward_workspace_size": (c_sz, [c_i32, c_i32, c_i32, c_i32, c_i32]),
     "moe_gdr_backward": (ctypes.c_int, [c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp,
                                         c_vp, ctypes.c_float, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
-                                        c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
+                                        c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "moe_set_kernel_events": (ctypes.c_int, [ctypes.c_int, c_vp, c_vp]),
     "moe_launch_count": (ctypes.c_longlong, []),
     "moe_selftest_wait_timeout": (ctypes.c_int, [c_vp, c_i32, c_vp]),
@@ -419,12 +419,12 @@ def moe_gdr_workspace_size(B, T, H, dk, dv) -> int:
 
 
 def moe_gdr_forward(B, T, H, dk, dv, q, k, v, beta, g, S0, scale, o, S_T, S_chunks, workspace,
-                    stream=None):
+                    stream=None, W_chunks=None):
     wp, wn = _ws(workspace)
     _check("moe_gdr_forward",
            lib().moe_gdr_forward(B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
-                                 _ptr(S0), scale, _ptr(o), _ptr(S_T), _ptr(S_chunks), wp, wn,
-                                 _stream(stream)))
+                                 _ptr(S0), scale, _ptr(o), _ptr(S_T), _ptr(S_chunks),
+                                 _ptr(W_chunks), wp, wn, _stream(stream)))
 
 
 def moe_gdr_device_status(stream=None) -> int:
@@ -440,13 +440,13 @@ def moe_gdr_backward_workspace_size(B, T, H, dk, dv) -> int:
 
 
 def moe_gdr_backward(B, T, H, dk, dv, q, k, v, beta, g, scale, d_o, dS_T, S_chunks, dq, dk_,
-                     dv_, dbeta, dg, dS0, workspace, stream=None):
+                     dv_, dbeta, dg, dS0, workspace, stream=None, W_chunks=None):
     wp, wn = _ws(workspace)
     _check("moe_gdr_backward",
            lib().moe_gdr_backward(B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
-                                  scale, _ptr(d_o), _ptr(dS_T), _ptr(S_chunks), _ptr(dq), _ptr(dk_),
-                                  _ptr(dv_), _ptr(dbeta), _ptr(dg), _ptr(dS0), wp, wn,
-                                  _stream(stream)))
+                                  scale, _ptr(d_o), _ptr(dS_T), _ptr(S_chunks), _ptr(W_chunks),
+                                  _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dbeta), _ptr(dg), _ptr(dS0),
+                                  wp, wn, _stream(stream)))
 
 
 def moe_set_kernel_events(kernel, before, after):
