@@ -691,7 +691,7 @@ def run_linear_attention(name, ctx):
     t_ach = t_flops / (sum(t_us.values()) * 1e-6) / 1e12
     train = {"value": job_throughput(ctx.world, B * T, t_ms), "unit": "tokens/s",
              "ms_per_step": t_ms, "cuda_graph": True, "gpu_launches": 5 * K,
-             "what": "forward (chunk-start states kept) + backward to q, k, v, beta, g, S0",
+             "what": "forward (chunk-start states and W kept) + backward to q, k, v, beta, g, S0",
              "kernels": {n: {"us": t_us[n]} for n in tk},
              "roofline": {"kernel": "all five", "bound": "alu", "achieved": t_ach,
                           "peak": peak, "unit": "TFLOP/s", "frac": t_ach / peak,
