@@ -1363,27 +1363,8 @@ __global__ void __launch_bounds__(kTcBlock, 1) gdr_bwd_scan_tc_kernel(
 // Register-tiled products of the per-chunk backward, for 256 threads: thread (ti, tj) =
 // (tid / 16, tid % 16) owns rows ti + 16 u (u < M / 16) and columns tj + 16 c (c < N / 16)
 // of an M x N result and adds its sums to acc[u][c] (k ascending, one fp32 chain per output).
-//   mm_nn:  A(m, k) and B(k, n) element callables (B's columns are consecutive across the
-//           16 lanes of a row group, A's rows are two per warp: broadcast reads)
 //   mm_nt4: A and B given by k-contiguous rows (shared or global, 16-byte aligned), read 16
 //           bytes at a time
-template <int M, int N, class FA, class FB>
-__device__ __forceinline__ void mm_nn(int K, FA A, FB B, float (&acc)[M / 16][N / 16]) {
-  const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
-#pragma unroll 2
-  for (int k = 0; k < K; ++k) {
-    float a[M / 16], bb[N / 16];
-#pragma unroll
-    for (int u = 0; u < M / 16; ++u) a[u] = A(ti + 16 * u, k);
-#pragma unroll
-    for (int c = 0; c < N / 16; ++c) bb[c] = B(k, tj + 16 * c);
-#pragma unroll
-    for (int u = 0; u < M / 16; ++u)
-#pragma unroll
-      for (int c = 0; c < N / 16; ++c) acc[u][c] += a[u] * bb[c];
-  }
-}
-
 template <int M, int N, class FA, class FB>
 __device__ __forceinline__ void mm_nt4(int K, FA Arow, FB Brow, float (&acc)[M / 16][N / 16]) {
   const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
@@ -1452,25 +1433,6 @@ struct Stager {
     }
   }
 };
-
-// mm_nn with B in global memory, staged through shared memory 16 k rows at a time (every
-// element read once by the CTA, the next block loading while the current one is used):
-// B(k, n) = Bg[k * ldb + n], or Bg[n * ldb + k] with TRANS.  stage: 16 x (N + 4) floats.
-// Every thread of the block must call it (it synchronises).
-template <int M, int N, bool TRANS, class FA>
-__device__ __forceinline__ void mm_nn_staged(int K, FA A, const float* __restrict__ Bg, int ldb,
-                                             float* stage, float (&acc)[M / 16][N / 16]) {
-  Stager<N, TRANS> st;
-  st.load(Bg, ldb, 0);
-  for (int k0 = 0; k0 < K; k0 += 16) {
-    st.store(stage);
-    __syncthreads();
-    if (k0 + 16 < K) st.load(Bg, ldb, k0 + 16);
-    mm_nn<M, N>(16, [&](int m, int k) { return A(m, k0 + k); },
-                [&](int k, int n) { return stage[k * (N + 4) + n]; }, acc);
-    __syncthreads();
-  }
-}
 
 // Float4 form of the products: thread (ti, tj) owns rows ti + 16 u and the four consecutive
 // columns 64 g + 4 tj .. + 3 of every 64 (column c of the thread: bcol(tj, c)); A4(m, k)
@@ -1710,11 +1672,26 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
       }
   }
   __syncthreads();
-  // (3) dq^ = (Gam . dP) K^ + s gamma_i dO_i S0;  dG_i += s gamma_i (dO S0)_i . q^_i
+  // (3) dq^ = (Gam . dP) K^ + s gamma_i dO_i S0;  dG_i += s gamma_i (dO S0)_i . q^_i, and
+  // (5) dY = -dW S0 from the same pass over S0 ([dO; dW] S0 as one 128-row product) -> sX
   float dqa[RU][CK];
-  mm_zero<kC, DK>(dqa);
-  mm_nn4_staged<kC, DK, false>(DV, [&](int m, int r) { return ld4(sX + m * LX + r); }, S0, DK,
-                               sStg, dqa);
+  {
+    float acc[2 * RU][CK];
+    mm_zero<2 * kC, DK>(acc);
+    mm_nn4_staged<2 * kC, DK, false>(
+        DV,
+        [&](int m, int r) {
+          return ld4(m < kC ? sX + m * LX + r : sdW + (m - kC) * LV + r);
+        },
+        S0, DK, sStg, acc);
+#pragma unroll
+    for (int u = 0; u < RU; ++u)
+#pragma unroll
+      for (int cc = 0; cc < CK; ++cc) {
+        dqa[u][cc] = acc[u][cc];
+        sX[(ti + 16 * u) * LX + bcol(tj, cc)] = -acc[RU + u][cc];  // dO was read by all threads
+      }
+  }
 #pragma unroll
   for (int u = 0; u < RU; ++u) {
     const int i = ti + 16 * u;
@@ -1765,18 +1742,6 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
     for (int w = 0; w < 8; ++w) sr += sRed[w];
     sdG[kC - 1] += tot + __expf(gl) * sr;  // d/dG_C of every exp(G_C - G_j) and of gamma_C S0
   }
-  // (5) dY = -dW S0 -> sX
-  {
-    float acc[RU][CK];
-    mm_zero<kC, DK>(acc);
-    mm_nn4_staged<kC, DK, false>(DV, [&](int m, int r) { return ld4(sdW + m * LV + r); }, S0,
-                                 DK, sStg, acc);
-#pragma unroll
-    for (int u = 0; u < RU; ++u)
-#pragma unroll
-      for (int cc = 0; cc < CK; ++cc) sX[(ti + 16 * u) * LX + bcol(tj, cc)] = -acc[u][cc];
-  }
-  __syncthreads();
   // (6) dBk = A^-T dY -> sW; dk^ += beta gamma dBk; beta and G from Bk = beta gamma K^
   {
     float acc[RU][CK];
@@ -1837,19 +1802,20 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
   {
     float acc[RU][CC], kk[RU][CC];
     mm_zero<kC, kC>(acc);
-    mm_nn_staged<kC, kC, true>(DV, [&](int m, int r) { return sX[m * LX + r]; }, cU, DV, sStg,
-                               acc);
-    mm_nn_staged<kC, kC, true>(DK, [&](int m, int x) { return sW[m * LX + x]; }, cY, DK, sStg,
-                               acc);
+    mm_nn4_staged<kC, kC, true>(DV, [&](int m, int r) { return ld4(sX + m * LX + r); }, cU, DV,
+                                sStg, acc);
+    mm_nn4_staged<kC, kC, true>(DK, [&](int m, int x) { return ld4(sW + m * LX + x); }, cY, DK,
+                                sStg, acc);
 #pragma unroll
     for (int u = 0; u < RU; ++u)  // K^ K^T from the factor kernel's tensor-core product
 #pragma unroll
-      for (int cc = 0; cc < CC; ++cc) kk[u][cc] = __ldg(&KKg[cid * kC * kC + (ti + 16 * u) * kC + tj + 16 * cc]);
+      for (int cc = 0; cc < CC; ++cc)
+        kk[u][cc] = __ldg(&KKg[cid * kC * kC + (ti + 16 * u) * kC + bcol(tj, cc)]);
 #pragma unroll
     for (int u = 0; u < RU; ++u)
 #pragma unroll
       for (int cc = 0; cc < CC; ++cc) {
-        const int i = ti + 16 * u, j = tj + 16 * cc;
+        const int i = ti + 16 * u, j = bcol(tj, cc);
         float z = 0.f, bt = 0.f;
         if (j < i) {
           const float a = acc[u][cc];
