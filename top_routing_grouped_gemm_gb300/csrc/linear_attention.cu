@@ -1742,12 +1742,16 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
     for (int w = 0; w < 8; ++w) sr += sRed[w];
     sdG[kC - 1] += tot + __expf(gl) * sr;  // d/dG_C of every exp(G_C - G_j) and of gamma_C S0
   }
-  // (6) dBk = A^-T dY -> sW; dk^ += beta gamma dBk; beta and G from Bk = beta gamma K^
+  // (6) dBk = A^-T dY -> sW; dk^ += beta gamma dBk; beta and G from Bk = beta gamma K^, and
+  // (7) dBv = A^-T dW -> sX; dv = beta dBv; beta from Bv = beta V, from one pass over A^-1
+  // (result columns 0 .. dk - 1 from dY, dk .. dk + dv - 1 from dW)
   {
-    float acc[RU][CK];
-    mm_zero<kC, DK>(acc);
-    mm_nn4_stagedA<kC, DK>(kC, cA, kC, [&](int i, int n) { return ld4(sX + i * LX + n); }, sStg,
-                           acc);
+    float acc[RU][CK + CV];
+    mm_zero<kC, DK + DV>(acc);
+    mm_nn4_stagedA<kC, DK + DV>(
+        kC, cA, kC,
+        [&](int i, int n) { return ld4(n < DK ? sX + i * LX + n : sdW + i * LV + (n - DK)); },
+        sStg, acc);  // ends with a barrier: dY is no longer read when dBv replaces it
 #pragma unroll
     for (int u = 0; u < RU; ++u) {
       const int j = ti + 16 * u;
@@ -1767,14 +1771,6 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
         sdG[j] += bg * part;
       }
     }
-  }
-  __syncthreads();
-  // (7) dBv = A^-T dW -> sX; dv = beta dBv; beta from Bv = beta V
-  {
-    float acc[RU][CV];
-    mm_zero<kC, DV>(acc);
-    mm_nn4_stagedA<kC, DV>(kC, cA, kC, [&](int i, int n) { return ld4(sdW + i * LV + n); },
-                           sStg, acc);
 #pragma unroll
     for (int u = 0; u < RU; ++u) {
       const int j = ti + 16 * u;
@@ -1782,7 +1778,7 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
 #pragma unroll
       for (int cc = 0; cc < CV; ++cc) {
         const int r = bcol(tj, cc);
-        const float a = acc[u][cc];
+        const float a = acc[u][CK + cc];
         sX[j * LX + r] = a;
         float vj = 0.f;
         if (t0 + j < T) {
