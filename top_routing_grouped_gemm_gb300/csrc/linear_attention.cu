@@ -1650,7 +1650,8 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
       }
   }
   __syncthreads();
-  // (2) dP_ij = s dO_i . W_j (j <= i), kept as Gam . dP (sC1); R_ij = dP_ij P_ij (sC2)
+  // (2) dP_ij = s dO_i . W_j (j <= i), kept as Gam . dP (sC1, and transposed in sC3 for
+  // (4)); R_ij = dP_ij P_ij (sC2)
   {
     float acc[RU][CC];
     mm_zero<kC, kC>(acc);
@@ -1668,6 +1669,7 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
           rr = dp * __ldg(&cP[i * kC + j]);
         }
         sC1[i * LC + j] = gd;
+        sC3[j * LC + i] = gd;
         sC2[i * LC + j] = rr;
       }
   }
@@ -1729,10 +1731,7 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
     }
   }
   mm_nn4<kC, DK>(kC,
-                 [&](int m, int i) {
-                   return make_float4(sC1[i * LC + m], sC1[(i + 1) * LC + m],
-                                      sC1[(i + 2) * LC + m], sC1[(i + 3) * LC + m]);
-                 },
+                 [&](int m, int i) { return ld4(sC3 + m * LC + i); },
                  [&](int i, int n) { return ld4(sQ + i * LK + n); }, dka);
   __syncthreads();   // every row's part, the <dS1, S0> partials; dO and W are done with
   if (tid == 0) {
@@ -1793,8 +1792,8 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
   }
   __syncthreads();
   // (8) dM_ij = -(dBv_i . U_j + dBk_i . Y_j) for j < i; with M_ij = beta_i Gam_ij k^_i.k^_j:
-  // Z_ij = dM_ij beta_i Gam_ij (-> sC1, for dk^), dM_ij M_ij (added to R in sC2, for dG) and
-  // dM_ij Gam_ij k^_i.k^_j (-> sC3, for dbeta)
+  // Z_ij = dM_ij beta_i Gam_ij (-> sC1 as Z + Z^T, for dk^), dM_ij M_ij (added to R in sC2,
+  // for dG) and dM_ij Gam_ij k^_i.k^_j (-> sC3, for dbeta)
   {
     float acc[RU][CC], kk[RU][CC];
     mm_zero<kC, kC>(acc);
@@ -1820,7 +1819,10 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
           z = -a * sB[i] * gam;
           sC2[i * LC + j] += bt * sB[i];
         }
-        sC1[i * LC + j] = z;
+        if (j <= i) {  // Z + Z^T (Z strictly lower triangular): the owner of (i, j) writes both
+          sC1[i * LC + j] = z;
+          sC1[j * LC + i] = z;
+        }
         sC3[i * LC + j] = bt;
       }
   }
@@ -1838,11 +1840,7 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
     sdG[i] += rs - cs;
   }
   mm_nn4<kC, DK>(kC,
-                 [&](int i, int j) {
-                   const float4 r = ld4(sC1 + i * LC + j);
-                   return make_float4(r.x + sC1[j * LC + i], r.y + sC1[(j + 1) * LC + i],
-                                      r.z + sC1[(j + 2) * LC + i], r.w + sC1[(j + 3) * LC + i]);
-                 },
+                 [&](int i, int j) { return ld4(sC1 + i * LC + j); },
                  [&](int j, int n) { return ld4(sK + j * LK + n); }, dka);
   __syncthreads();
   // (10) dg = reverse cumulative sum of dG within the chunk (warp 0: lane l holds rows l and
