@@ -290,8 +290,8 @@ template <int DK, int DV, bool SPLIT, bool BIMG>
 __global__ void __launch_bounds__(256, 2) gdr_chunk_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ beta,
-    const float* __restrict__ g, int T, int H, int nch, float* __restrict__ Qh,
-    float* __restrict__ Kh, float* __restrict__ Y, float* __restrict__ U,
+    const float* __restrict__ g, int T, int H, int nch, float* __restrict__ Y,
+    float* __restrict__ U,
     float* __restrict__ Pm, float* __restrict__ Gc, float* __restrict__ Ai,
     __nv_bfloat16* __restrict__ YQs, __nv_bfloat16* __restrict__ Ks,
     __nv_bfloat16* __restrict__ Ps, GdrBwdImages img) {
@@ -424,12 +424,6 @@ __global__ void __launch_bounds__(256, 2) gdr_chunk_kernel(
         *reinterpret_cast<uint4*>(ko + LS::a3(0, i, x0)) = hi;
         *reinterpret_cast<uint4*>(ko + LS::a3(1, i, x0)) = mid;
       } else {
-        float4* qo = reinterpret_cast<float4*>(Qh + chunk_id * kC * DK + i * DK + x0);
-        float4* ko = reinterpret_cast<float4*>(Kh + chunk_id * kC * DK + i * DK + x0);
-        qo[0] = make_float4(qf[0], qf[1], qf[2], qf[3]);
-        qo[1] = make_float4(qf[4], qf[5], qf[6], qf[7]);
-        ko[0] = make_float4(kf[0], kf[1], kf[2], kf[3]);
-        ko[1] = make_float4(kf[4], kf[5], kf[6], kf[7]);
         if constexpr (BIMG) {  // s gamma q^ and E = (gamma_C / gamma) k^
           using LB = TcBwd<DK>;
           split8(qf, img.scale * __expf(sG[i]), hi, mid);
@@ -1548,8 +1542,7 @@ template <int DK, int DV>
 __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
     const __nv_bfloat16* __restrict__ v, const float* __restrict__ beta,
-    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ Qh,
-    const float* __restrict__ Kh, const float* __restrict__ Y, const float* __restrict__ U,
+    const __nv_bfloat16* __restrict__ dO, const float* __restrict__ Y, const float* __restrict__ U,
     const float* __restrict__ Pm, const float* __restrict__ Gc, const float* __restrict__ Ai,
     const float* __restrict__ Schk, const float* __restrict__ dSchk,
     const float* __restrict__ dWg, const float* __restrict__ KKg, const float* __restrict__ Wg,
@@ -1593,10 +1586,43 @@ __global__ void __launch_bounds__(256) gdr_bwd_chunk_kernel(
   auto row = [&](int i) { return ((static_cast<size_t>(b) * T + t0 + i) * H + h); };
 
   // the chunk's tiles, 16 bytes per load (rows of the shared tiles are 16-byte aligned)
-  for (int e = tid; e < kC * DK / 4; e += 256) {
-    const int i = e / (DK / 4), x = 4 * (e - i * (DK / 4));
-    *reinterpret_cast<float4*>(sQ + i * LK + x) = ldg4(Qh + cid * kC * DK + 4 * e);
-    *reinterpret_cast<float4*>(sK + i * LK + x) = ldg4(Kh + cid * kC * DK + 4 * e);
+  {  // q^ and k^: rows L2-normalised as the factor kernel does it (8 values per lane, the
+     // squares summed in order, then across the row's DK / 8 lanes by an xor tree)
+    constexpr int PPR = DK / 8;
+    static_assert(32 % PPR == 0 && (kC * PPR) % 256 == 0, "whole rows per warp, full warps");
+    for (int e = tid; e < kC * PPR; e += 256) {
+      const int i = e / PPR, x0 = 8 * (e - i * PPR);
+      uint4 qa = make_uint4(0u, 0u, 0u, 0u), ka = qa;
+      if (t0 + i < T) {
+        qa = __ldg(reinterpret_cast<const uint4*>(q + row(i) * DK + x0));
+        ka = __ldg(reinterpret_cast<const uint4*>(k + row(i) * DK + x0));
+      }
+      const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w};
+      const uint32_t kw[4] = {ka.x, ka.y, ka.z, ka.w};
+      float qf[8], kf[8], sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 a2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qw[j]));
+        const float2 b2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw[j]));
+        qf[2 * j] = a2.x; qf[2 * j + 1] = a2.y;
+        kf[2 * j] = b2.x; kf[2 * j + 1] = b2.y;
+        sq += a2.x * a2.x + a2.y * a2.y;
+        sk += b2.x * b2.x + b2.y * b2.y;
+      }
+#pragma unroll
+      for (int o = PPR / 2; o > 0; o >>= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        sk += __shfl_xor_sync(0xffffffffu, sk, o);
+      }
+      const float iq = sq > 0.f ? 1.0f / sqrtf(sq) : 0.f;
+      const float ik = sk > 0.f ? 1.0f / sqrtf(sk) : 0.f;
+      float4* qo = reinterpret_cast<float4*>(sQ + i * LK + x0);
+      float4* ko = reinterpret_cast<float4*>(sK + i * LK + x0);
+      qo[0] = make_float4(qf[0] * iq, qf[1] * iq, qf[2] * iq, qf[3] * iq);
+      qo[1] = make_float4(qf[4] * iq, qf[5] * iq, qf[6] * iq, qf[7] * iq);
+      ko[0] = make_float4(kf[0] * ik, kf[1] * ik, kf[2] * ik, kf[3] * ik);
+      ko[1] = make_float4(kf[4] * ik, kf[5] * ik, kf[6] * ik, kf[7] * ik);
+    }
   }
   for (int e = tid; e < kC * DV / 4; e += 256) {
     const int i = e / (DV / 4), r = 4 * (e - i * (DV / 4));
@@ -1933,7 +1959,7 @@ int gdr_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloat16*
                                        static_cast<int>(sm1));
   if (e != cudaSuccess) return static_cast<int>(e);
   mark_before(MOE_KERNEL_GDR_CHUNK, s);
-  k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, nullptr, nullptr, nullptr,
+  k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, nullptr,
                                        Uw, nullptr, Gw, nullptr, YQs, Ks, Ps, GdrBwdImages{});
   mark_after(MOE_KERNEL_GDR_CHUNK, s);
   constexpr size_t sm2 = TcScan<DK>::SMEM;
@@ -1971,8 +1997,7 @@ int gdr_bwd_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloa
   const int nch = (T + kC - 1) / kC;
   const size_t chunks = static_cast<size_t>(B) * H * nch;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  float* Qh = reinterpret_cast<float*>(w); w += up256(chunks * kC * DK * 4);
-  float* Kh = reinterpret_cast<float*>(w); w += up256(chunks * kC * DK * 4);
+  w += 2 * up256(chunks * kC * DK * 4);  // the forward's image regions, unused here
   float* Yw = reinterpret_cast<float*>(w); w += up256(chunks * kC * DK * 4);
   float* Uw = reinterpret_cast<float*>(w); w += up256(chunks * kC * DV * 4);
   float* Pw = reinterpret_cast<float*>(w); w += up256(chunks * kC * kC * 4);
@@ -1998,8 +2023,8 @@ int gdr_bwd_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloa
                                        static_cast<int>(sm1));
   if (e != cudaSuccess) return static_cast<int>(e);
   mark_before(MOE_KERNEL_GDR_BWD_FACTORS, s);
-  k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, Qh, Kh, Yw, Uw, Pw, Gw, Aw,
-                                       nullptr, nullptr, nullptr, img);
+  k1<<<dim3(nch, H, B), 256, sm1, s>>>(q, k, v, beta, g, T, H, nch, Yw, Uw, Pw, Gw, Aw, nullptr,
+                                       nullptr, nullptr, img);
   mark_after(MOE_KERNEL_GDR_BWD_FACTORS, s);
   constexpr size_t sm2 = LB::SMEM;
   auto k2 = gdr_bwd_scan_tc_kernel<DK, DV>;
@@ -2014,7 +2039,7 @@ int gdr_bwd_launch(int B, int T, int H, const __nv_bfloat16* q, const __nv_bfloa
   e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm3));
   if (e != cudaSuccess) return static_cast<int>(e);
   mark_before(MOE_KERNEL_GDR_BWD, s);
-  k3<<<dim3(nch, H, B), 256, sm3, s>>>(q, k, v, beta, dO, Qh, Kh, Yw, Uw, Pw, Gw, Aw, Schk, dSw,
+  k3<<<dim3(nch, H, B), 256, sm3, s>>>(q, k, v, beta, dO, Yw, Uw, Pw, Gw, Aw, Schk, dSw,
                                        dWw, img.KK, Wch, T, H, nch, scale, dq, dk, dv, dbeta, dg);
   mark_after(MOE_KERNEL_GDR_BWD, s);
   return static_cast<int>(cudaGetLastError());
